@@ -1,0 +1,591 @@
+/*
+ * gbdt_oracle.c -- CPU oracle for level-wise histogram GBDT with squared error.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is a plain, slow, FP64 restatement of
+ * what the training method computes.  Only the test suite, the smoke check
+ * and the benchmark's CPU-baseline leg may load it.  It shares no code, header,
+ * table or helper with the CUDA library, and it never reads anything the CUDA
+ * path produced except the optional lockstep guide of orc_train (see there),
+ * which can only choose between candidates this file itself rates as tied.
+ *
+ * Sources (page titles and sections):
+ *   [MPS-TC]  "Module Design: Training Core" (MPSBoost spec)
+ *             s.2 Single Mathematical Semantics  -- g, h, score, weight, gain
+ *             s.3 Tree Model                      -- flat BFS nodes, frozen
+ *                                                    tie-break, validity, routing,
+ *                                                    parameter rules
+ *             s.6 Tree Growth                     -- level-wise growth steps 1-7
+ *             s.7 CPU Oracle                      -- FP64 count/G/H per bin in
+ *                                                    row-index order
+ *   [LEAN]    "Gradient boosted trees (spec model)" (TorchLean)
+ *             Forward pass -- init + learning_rate * sum of tree outputs;
+ *             Tree representation -- goRight := x > threshold.
+ *
+ * Readings where the pages are silent (each also listed in the design notes):
+ *   - Quantile binning (the pages name a "Quantized" state only): exact order
+ *     statistics, see orc_quantize.
+ *   - The node total G_P is the row-order sum over the node's rows; G_R and
+ *     H_R are parent minus left; the gain is evaluated as
+ *     0.5*((s_L + s_R) - s_P) - gamma with s = G*G/(H+lambda), no fused
+ *     multiply-add (build with -ffp-contract=off).
+ *   - "meet minimum" reads as >=.
+ *   - Depth D: root at depth 0, nodes at depth D are leaves.
+ *   - Initial prediction: mean of the labels, FP64 sum in row order / N.
+ *   - Prediction update: pred + (lr * w), product rounded first.
+ *
+ * Parity pins: every function here is checked by tests that do not call it
+ * back (brute force, closed forms, the CART special case, invariants,
+ * hand-computed trees).  No function in this file is "parity unpinned".
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORC_OK 0
+#define ORC_EINVAL (-1)
+#define ORC_ENONFINITE (-2)
+#define ORC_ENOMEM (-3)
+
+#define ORC_NBINS 256      /* histogram width: every bin index a uint8 can hold */
+#define ORC_NEAR_MAX 8     /* near-tied candidates recorded per node */
+#define ORC_NEAR_REL 1e-12 /* relative gain gap that counts as a near-tie */
+
+typedef struct {
+  int32_t n_trees;
+  int32_t max_depth;
+  double learning_rate;
+  double reg_lambda;
+  double gamma;
+  int32_t min_samples_leaf;
+  double min_child_weight;
+  int32_t n_threads; /* OpenMP threads over features; results do not depend on it */
+} orc_params;
+
+typedef struct {
+  int32_t feature;       /* -1 for a leaf */
+  int32_t threshold_bin; /* -1 for a leaf; bin <= threshold_bin goes left */
+  int32_t left, right;   /* BFS child indices, -1 for a leaf */
+  double leaf_value;     /* weight(G,H) of the node (used for leaves) */
+  double gain;           /* gain of the chosen split, 0 for a leaf */
+  int32_t is_leaf;
+  int32_t depth;
+} orc_node;
+
+typedef struct {
+  int64_t n_rows;
+  double G, H, A; /* row-order sums of g, h and |g| over the node's rows */
+  double best_gain, second_gain; /* over distinct partitions; -INFINITY if none */
+  int32_t n_near;                /* candidates within ORC_NEAR_REL of the best */
+  int32_t near_feature[ORC_NEAR_MAX];
+  int32_t near_bin[ORC_NEAR_MAX];
+  int32_t adopted;        /* 1: the guide's near-tied choice replaced ours */
+  int32_t guide_mismatch; /* 1: the guide disagreed outside the near-tie set */
+} orc_node_info;
+
+typedef struct {
+  int32_t valid;   /* 1 if a valid candidate exists */
+  int32_t feature; /* best candidate (valid == 1) */
+  int32_t bin;
+  double gain;
+  int64_t cnt_left;
+  double G_left, H_left;
+  double second_gain; /* best gain over other distinct partitions */
+  int32_t n_near;
+  int32_t near_feature[ORC_NEAR_MAX];
+  int32_t near_bin[ORC_NEAR_MAX];
+} orc_split;
+
+/* ------------------------------------------------------------------------ */
+/* [MPS-TC] s.2: score, weight and gain, evaluated in the stated order.     */
+/* ------------------------------------------------------------------------ */
+static double orc_score(double G, double H, double lambda) { return (G * G) / (H + lambda); }
+
+double orc_weight(double G, double H, double lambda) { return -G / (H + lambda); }
+
+double orc_gain(double GL, double HL, double GR, double HR, double GP, double HP, double lambda,
+                double gamma) {
+  double sL = orc_score(GL, HL, lambda);
+  double sR = orc_score(GR, HR, lambda);
+  double sP = orc_score(GP, HP, lambda);
+  return 0.5 * ((sL + sR) - sP) - gamma;
+}
+
+/* [MPS-TC] s.3: parameter rules. */
+int orc_validate_params(const orc_params* p) {
+  if (!p) return ORC_EINVAL;
+  if (p->n_trees < 0 || p->max_depth < 0 || p->max_depth > 15) return ORC_EINVAL;
+  if (!isfinite(p->learning_rate) || !isfinite(p->reg_lambda) || !isfinite(p->gamma) ||
+      !isfinite(p->min_child_weight))
+    return ORC_EINVAL;
+  if (p->min_samples_leaf < 1 || p->min_child_weight < 0.0 || p->reg_lambda < 0.0 || p->gamma < 0.0)
+    return ORC_EINVAL;
+  return ORC_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Quantile binning (reading; the pages only name the "Quantized" state).   */
+/* ------------------------------------------------------------------------ */
+static int cmp_float(const void* a, const void* b) {
+  float x = *(const float*)a, y = *(const float*)b;
+  return (x < y) ? -1 : (x > y) ? 1 : 0;
+}
+
+/*
+ * For each feature j, with v the N values sorted ascending (-0.0 read as
+ * +0.0) and U the number of distinct values:
+ *   U <= B : edges are the U-1 smallest distinct values (one bin per value);
+ *   U >  B : for k = 1..B-1 take e_k = v[ceil(k*N/B) - 1]; keep the strictly
+ *            increasing subsequence; drop an edge equal to v[N-1].
+ * bin(x) = number of edges strictly below x, so x <= edges[b] means bin <= b,
+ * which matches routing "x > threshold goes right" ([LEAN] Tree representation)
+ * with threshold = edges[b].  Unused edge slots are +INFINITY.
+ * X is column-major [F][N]; bins is [F][N]; edges is [F][max_bins-1].
+ */
+int orc_quantize(const float* X, int64_t N, int32_t F, int32_t max_bins, int32_t n_threads,
+                 uint8_t* bins, float* edges, int32_t* n_bins) {
+  if (!X || !bins || !edges || !n_bins || N < 1 || F < 1 || max_bins < 2 || max_bins > 256)
+    return ORC_EINVAL;
+  for (int64_t i = 0; i < N * (int64_t)F; ++i)
+    if (!isfinite(X[i])) return ORC_ENONFINITE;
+  const int32_t B = max_bins;
+  int status = ORC_OK;
+#ifdef _OPENMP
+#pragma omp parallel for schedule(dynamic, 1) num_threads(n_threads > 0 ? n_threads : 1)
+#endif
+  for (int32_t j = 0; j < F; ++j) {
+    float* v = (float*)malloc((size_t)N * sizeof(float));
+    if (!v) {
+      status = ORC_ENOMEM;
+      continue;
+    }
+    const float* col = X + (int64_t)j * N;
+    for (int64_t i = 0; i < N; ++i) v[i] = (col[i] == 0.0f) ? 0.0f : col[i];
+    qsort(v, (size_t)N, sizeof(float), cmp_float);
+    int64_t U = 1;
+    for (int64_t i = 1; i < N; ++i)
+      if (v[i] != v[i - 1]) ++U;
+    float* e = edges + (int64_t)j * (B - 1);
+    int32_t ne = 0;
+    if (U <= B) {
+      for (int64_t i = 0; i < N && ne < U - 1; ++i)
+        if (i == 0 || v[i] != v[i - 1]) e[ne++] = v[i];
+    } else {
+      for (int32_t k = 1; k <= B - 1; ++k) {
+        /* ceil(k*N/B) - 1 in integer arithmetic */
+        int64_t pk = ((int64_t)k * N + B - 1) / B - 1;
+        float ek = v[pk];
+        if (ne > 0 && !(ek > e[ne - 1])) continue; /* keep strictly increasing */
+        if (ek == v[N - 1]) continue;              /* an edge at the maximum is empty above */
+        e[ne++] = ek;
+      }
+    }
+    for (int32_t k = ne; k < B - 1; ++k) e[k] = INFINITY;
+    n_bins[j] = ne + 1;
+    uint8_t* bj = bins + (int64_t)j * N;
+    for (int64_t i = 0; i < N; ++i) {
+      float x = col[i];
+      int32_t c = 0;
+      while (c < ne && e[c] < x) ++c; /* count of edges strictly below x */
+      bj[i] = (uint8_t)c;
+    }
+    free(v);
+  }
+  return status;
+}
+
+/* ------------------------------------------------------------------------ */
+/* [MPS-TC] s.2: gradients of squared error.                                */
+/* ------------------------------------------------------------------------ */
+int orc_gradients(const double* pred, const float* label, int64_t N, double* g, double* h) {
+  if (!pred || !label || !g || N < 0) return ORC_EINVAL;
+  for (int64_t i = 0; i < N; ++i) {
+    g[i] = pred[i] - (double)label[i];
+    if (h) h[i] = 1.0;
+  }
+  return ORC_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* [MPS-TC] s.7: per-bin count/G/H in supplied row-index order, FP64.       */
+/* ------------------------------------------------------------------------ */
+/*
+ * Histogram of one node: rows[0..n) in the order given.  cnt/G/H are
+ * [F][256]; A_out (optional) receives sum |g| over the node's rows.
+ */
+static void node_histogram(const uint8_t* bins, int64_t N, int32_t F, const double* g, const int64_t* rows,
+                           int64_t n, uint32_t* cnt, double* G, double* H, int32_t n_threads) {
+  memset(cnt, 0, sizeof(uint32_t) * (size_t)F * ORC_NBINS);
+  memset(G, 0, sizeof(double) * (size_t)F * ORC_NBINS);
+  memset(H, 0, sizeof(double) * (size_t)F * ORC_NBINS);
+  (void)n_threads;
+#ifdef _OPENMP
+#pragma omp parallel for schedule(static) num_threads(n_threads > 0 ? n_threads : 1)
+#endif
+  for (int32_t j = 0; j < F; ++j) {
+    const uint8_t* col = bins + (int64_t)j * N;
+    uint32_t* c = cnt + (int64_t)j * ORC_NBINS;
+    double* gg = G + (int64_t)j * ORC_NBINS;
+    double* hh = H + (int64_t)j * ORC_NBINS;
+    for (int64_t k = 0; k < n; ++k) {
+      int64_t r = rows[k];
+      int b = col[r];
+      c[b] += 1u;
+      gg[b] += g[r];
+      hh[b] += 1.0;
+    }
+  }
+}
+
+/*
+ * Histograms of every slot of a level in one call: slot_of_row[r] in
+ * [0, n_slots) selects the slot of row r (any other value: row inactive).
+ * Rows are visited in ascending index order, which is the supplied order.
+ * cnt/G/H are [n_slots][F][256]; n/Gt/Ht/At (optional) are per-slot row
+ * counts and row-order sums of g, h and |g|.
+ */
+int orc_histograms(const uint8_t* bins, int64_t N, int32_t F, const double* g, const int32_t* slot_of_row,
+                   int32_t n_slots, uint32_t* cnt, double* G, double* H, int64_t* n, double* Gt, double* Ht,
+                   double* At) {
+  if (!bins || !g || !slot_of_row || !cnt || !G || !H || N < 0 || F < 1 || n_slots < 0) return ORC_EINVAL;
+  const size_t per = (size_t)F * ORC_NBINS;
+  memset(cnt, 0, sizeof(uint32_t) * per * (size_t)n_slots);
+  memset(G, 0, sizeof(double) * per * (size_t)n_slots);
+  memset(H, 0, sizeof(double) * per * (size_t)n_slots);
+  if (n) memset(n, 0, sizeof(int64_t) * (size_t)n_slots);
+  if (Gt) memset(Gt, 0, sizeof(double) * (size_t)n_slots);
+  if (Ht) memset(Ht, 0, sizeof(double) * (size_t)n_slots);
+  if (At) memset(At, 0, sizeof(double) * (size_t)n_slots);
+  for (int64_t r = 0; r < N; ++r) {
+    int32_t s = slot_of_row[r];
+    if (s < 0 || s >= n_slots) continue;
+    if (n) n[s] += 1;
+    if (Gt) Gt[s] += g[r];
+    if (Ht) Ht[s] += 1.0;
+    if (At) At[s] += fabs(g[r]);
+    for (int32_t j = 0; j < F; ++j) {
+      size_t o = (size_t)s * per + (size_t)j * ORC_NBINS + bins[(int64_t)j * N + r];
+      cnt[o] += 1u;
+      G[o] += g[r];
+      H[o] += 1.0;
+    }
+  }
+  return ORC_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* [MPS-TC] s.3: split search under the frozen rule.                         */
+/* ------------------------------------------------------------------------ */
+/*
+ * One node, histograms cnt/G/H [F][256], node totals (n_P, G_P, H_P).
+ * For feature j and threshold b = 0..n_bins[j]-2: left = bins <= b, with
+ * G_L, H_L, cnt_L the running prefix sums in bin order; G_R = G_P - G_L,
+ * H_R = H_P - H_L, cnt_R = n_P - cnt_L.  A candidate is valid iff both sides
+ * have cnt >= min_samples_leaf, H >= min_child_weight and H > 0; invalid
+ * candidates never enter the comparison.  Best: strictly larger gain, then
+ * smaller feature, then smaller bin (scan order with replace-if-strictly-
+ * better gives exactly that).  The caller splits iff valid and gain > 0.
+ *
+ * Near-tie bookkeeping (for parity reports only): a threshold whose bin is
+ * empty gives the same partition as the threshold one below it, so it is not
+ * a distinct partition and is skipped for second_gain / the near list.
+ */
+int orc_best_split(const uint32_t* cnt, const double* G, const double* H, int32_t F, const int32_t* n_bins,
+                   int64_t n_P, double G_P, double H_P, const orc_params* p, orc_split* out) {
+  if (!cnt || !G || !H || !n_bins || !p || !out || F < 1) return ORC_EINVAL;
+  memset(out, 0, sizeof(*out));
+  out->feature = -1;
+  out->bin = -1;
+  out->gain = -INFINITY;
+  out->second_gain = -INFINITY;
+  const double lambda = p->reg_lambda, gamma = p->gamma, mcw = p->min_child_weight;
+  const int64_t msl = p->min_samples_leaf;
+  /* pass 1: the winner */
+  for (int32_t j = 0; j < F; ++j) {
+    const uint32_t* c = cnt + (int64_t)j * ORC_NBINS;
+    const double* gg = G + (int64_t)j * ORC_NBINS;
+    const double* hh = H + (int64_t)j * ORC_NBINS;
+    double GL = 0.0, HL = 0.0;
+    int64_t cL = 0;
+    int32_t nb = n_bins[j];
+    if (nb > ORC_NBINS) nb = ORC_NBINS;
+    for (int32_t b = 0; b <= nb - 2; ++b) {
+      GL += gg[b];
+      HL += hh[b];
+      cL += c[b];
+      int64_t cR = n_P - cL;
+      double GR = G_P - GL, HR = H_P - HL;
+      if (!(cL >= msl && cR >= msl && HL >= mcw && HR >= mcw && HL > 0.0 && HR > 0.0)) continue;
+      double gain = orc_gain(GL, HL, GR, HR, G_P, H_P, lambda, gamma);
+      if (!out->valid || gain > out->gain) {
+        out->valid = 1;
+        out->feature = j;
+        out->bin = b;
+        out->gain = gain;
+        out->cnt_left = cL;
+        out->G_left = GL;
+        out->H_left = HL;
+      }
+    }
+  }
+  if (!out->valid) return ORC_OK;
+  /* pass 2: runner-up over distinct partitions and the near-tie list */
+  const double g1 = out->gain;
+  for (int32_t j = 0; j < F; ++j) {
+    const uint32_t* c = cnt + (int64_t)j * ORC_NBINS;
+    const double* gg = G + (int64_t)j * ORC_NBINS;
+    const double* hh = H + (int64_t)j * ORC_NBINS;
+    double GL = 0.0, HL = 0.0;
+    int64_t cL = 0;
+    int32_t nb = n_bins[j];
+    if (nb > ORC_NBINS) nb = ORC_NBINS;
+    for (int32_t b = 0; b <= nb - 2; ++b) {
+      GL += gg[b];
+      HL += hh[b];
+      cL += c[b];
+      if (b > 0 && c[b] == 0) continue; /* same partition as threshold b-1 */
+      int64_t cR = n_P - cL;
+      double GR = G_P - GL, HR = H_P - HL;
+      if (!(cL >= msl && cR >= msl && HL >= mcw && HR >= mcw && HL > 0.0 && HR > 0.0)) continue;
+      double gain = orc_gain(GL, HL, GR, HR, G_P, H_P, lambda, gamma);
+      int is_best = (j == out->feature && b == out->bin);
+      if (!is_best && gain > out->second_gain) out->second_gain = gain;
+      if (fabs(g1 - gain) < ORC_NEAR_REL * fabs(g1) || is_best) {
+        if (out->n_near < ORC_NEAR_MAX) {
+          out->near_feature[out->n_near] = j;
+          out->near_bin[out->n_near] = b;
+        }
+        out->n_near++;
+      }
+    }
+  }
+  return ORC_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* [MPS-TC] s.6: level-wise depth-limited growth; [LEAN] forward pass.       */
+/* ------------------------------------------------------------------------ */
+/*
+ * Trains n_trees trees.  bins [F][N] column-major, n_bins [F], label [N].
+ * Outputs: pred [N] (after the last tree), *init_pred, nodes
+ * [n_trees][2^(max_depth+1)-1] in BFS order, nodes_per_tree [n_trees],
+ * optional info (same shape as nodes), optional leaf_of_row [N] (the BFS
+ * index of each row's leaf in the last tree).
+ *
+ * guide (optional, [n_trees][max_nodes][2] = feature, bin; feature -1 = leaf)
+ * is the lockstep rule of the parity harness: where this oracle's choice at
+ * a node differs from the guide's and the guide's (feature, bin) is among the
+ * candidates this oracle itself rates within ORC_NEAR_REL of its best gain,
+ * the guide's candidate is taken (info.adopted = 1).  Any other disagreement
+ * is recorded (info.guide_mismatch = 1) and this oracle keeps its own choice.
+ */
+int orc_train(const uint8_t* bins, const int32_t* n_bins, int64_t N, int32_t F, const float* label,
+              const orc_params* p, const int32_t* guide, double* pred, double* init_pred, orc_node* nodes,
+              int32_t* nodes_per_tree, orc_node_info* info, int32_t* leaf_of_row) {
+  if (!bins || !n_bins || !label || !pred || !init_pred || !nodes || !nodes_per_tree || N < 1 || F < 1)
+    return ORC_EINVAL;
+  int rc = orc_validate_params(p);
+  if (rc != ORC_OK) return rc;
+  for (int32_t j = 0; j < F; ++j)
+    if (n_bins[j] < 1 || n_bins[j] > ORC_NBINS) return ORC_EINVAL;
+  for (int64_t i = 0; i < N; ++i)
+    if (!isfinite(label[i])) return ORC_ENONFINITE;
+
+  const int32_t D = p->max_depth;
+  const int32_t max_nodes = (int32_t)((1u << (D + 1)) - 1u);
+  const double lambda = p->reg_lambda;
+
+  double* g = (double*)malloc(sizeof(double) * (size_t)N);
+  int64_t* order = (int64_t*)malloc(sizeof(int64_t) * (size_t)N); /* rows grouped by node */
+  int64_t* scratch = (int64_t*)malloc(sizeof(int64_t) * (size_t)N);
+  int64_t* seg_start = (int64_t*)malloc(sizeof(int64_t) * (size_t)max_nodes);
+  int64_t* seg_count = (int64_t*)malloc(sizeof(int64_t) * (size_t)max_nodes);
+  uint32_t* cnt = (uint32_t*)malloc(sizeof(uint32_t) * (size_t)F * ORC_NBINS);
+  double* G = (double*)malloc(sizeof(double) * (size_t)F * ORC_NBINS);
+  double* H = (double*)malloc(sizeof(double) * (size_t)F * ORC_NBINS);
+  if (!g || !order || !scratch || !seg_start || !seg_count || !cnt || !G || !H) {
+    free(g), free(order), free(scratch), free(seg_start), free(seg_count), free(cnt), free(G), free(H);
+    return ORC_ENOMEM;
+  }
+
+  /* initial prediction: mean label, FP64 sum in row order */
+  double sum = 0.0;
+  for (int64_t i = 0; i < N; ++i) sum += (double)label[i];
+  const double init = sum / (double)N;
+  *init_pred = init;
+  for (int64_t i = 0; i < N; ++i) pred[i] = init;
+
+  for (int32_t t = 0; t < p->n_trees; ++t) {
+    orc_node* tn = nodes + (int64_t)t * max_nodes;
+    orc_node_info* ti = info ? info + (int64_t)t * max_nodes : NULL;
+    const int32_t* tg = guide ? guide + (int64_t)t * max_nodes * 2 : NULL;
+    orc_gradients(pred, label, N, g, NULL);
+
+    for (int64_t i = 0; i < N; ++i) order[i] = i;
+    int32_t n_nodes = 1;
+    seg_start[0] = 0;
+    seg_count[0] = N;
+    int32_t level_begin = 0, level_end = 1;
+    for (int32_t d = 0; d <= D; ++d) {
+      for (int32_t v = level_begin; v < level_end; ++v) {
+        const int64_t* rows = order + seg_start[v];
+        const int64_t n = seg_count[v];
+        double GP = 0.0, HP = 0.0, A = 0.0;
+        for (int64_t k = 0; k < n; ++k) {
+          GP += g[rows[k]];
+          HP += 1.0;
+          A += fabs(g[rows[k]]);
+        }
+        orc_node* nd = &tn[v];
+        nd->feature = -1;
+        nd->threshold_bin = -1;
+        nd->left = -1;
+        nd->right = -1;
+        nd->leaf_value = orc_weight(GP, HP, lambda);
+        nd->gain = 0.0;
+        nd->is_leaf = 1;
+        nd->depth = d;
+        if (ti) {
+          memset(&ti[v], 0, sizeof(ti[v]));
+          ti[v].n_rows = n;
+          ti[v].G = GP;
+          ti[v].H = HP;
+          ti[v].A = A;
+          ti[v].best_gain = -INFINITY;
+          ti[v].second_gain = -INFINITY;
+        }
+        if (d == D) continue; /* depth limit: leaf without search */
+
+        node_histogram(bins, N, F, g, rows, n, cnt, G, H, p->n_threads);
+        orc_split sp;
+        orc_best_split(cnt, G, H, F, n_bins, n, GP, HP, p, &sp);
+        int do_split = sp.valid && sp.gain > 0.0;
+        int32_t f = sp.feature, b = sp.bin;
+        double gain = sp.gain;
+        if (ti) {
+          ti[v].best_gain = sp.valid ? sp.gain : -INFINITY;
+          ti[v].second_gain = sp.second_gain;
+          ti[v].n_near = sp.n_near;
+          for (int k = 0; k < ORC_NEAR_MAX; ++k) {
+            ti[v].near_feature[k] = sp.near_feature[k];
+            ti[v].near_bin[k] = sp.near_bin[k];
+          }
+        }
+        if (tg) {
+          int32_t gf = tg[2 * v], gb = tg[2 * v + 1];
+          int differs = do_split ? (gf != f || gb != b) : (gf != -1);
+          if (differs) {
+            int near = 0;
+            if (do_split && gf >= 0) {
+              int lim = sp.n_near < ORC_NEAR_MAX ? sp.n_near : ORC_NEAR_MAX;
+              for (int k = 0; k < lim; ++k)
+                if (sp.near_feature[k] == gf && sp.near_bin[k] == gb) near = 1;
+            }
+            if (near) {
+              /* recompute the adopted candidate's gain from its own prefix sums */
+              const double* gg = G + (int64_t)gf * ORC_NBINS;
+              const double* hh = H + (int64_t)gf * ORC_NBINS;
+              double GL = 0.0, HL = 0.0;
+              for (int32_t q = 0; q <= gb; ++q) {
+                GL += gg[q];
+                HL += hh[q];
+              }
+              f = gf;
+              b = gb;
+              gain = orc_gain(GL, HL, GP - GL, HP - HL, GP, HP, lambda, p->gamma);
+              if (ti) ti[v].adopted = 1;
+            } else if (ti) {
+              ti[v].guide_mismatch = 1;
+            }
+          }
+        }
+        if (!do_split) continue;
+
+        /* stable partition of the node's rows: bin <= b left, others right */
+        const uint8_t* col = bins + (int64_t)f * N;
+        int64_t* dst = scratch + seg_start[v];
+        int64_t w = 0;
+        for (int64_t k = 0; k < n; ++k)
+          if (col[rows[k]] <= b) dst[w++] = rows[k];
+        const int64_t nl = w;
+        for (int64_t k = 0; k < n; ++k)
+          if (!(col[rows[k]] <= b)) dst[w++] = rows[k];
+        memcpy(order + seg_start[v], dst, sizeof(int64_t) * (size_t)n);
+
+        int32_t L = n_nodes++, R = n_nodes++;
+        nd->feature = f;
+        nd->threshold_bin = b;
+        nd->left = L;
+        nd->right = R;
+        nd->gain = gain;
+        nd->is_leaf = 0;
+        seg_start[L] = seg_start[v];
+        seg_count[L] = nl;
+        seg_start[R] = seg_start[v] + nl;
+        seg_count[R] = n - nl;
+      }
+      level_begin = level_end;
+      level_end = n_nodes;
+      if (level_begin == level_end) break;
+    }
+    nodes_per_tree[t] = n_nodes;
+
+    /* [MPS-TC] s.6 step 7 / [LEAN] forward: pred += lr * w of the row's leaf */
+    for (int32_t v = 0; v < n_nodes; ++v) {
+      if (!tn[v].is_leaf) continue;
+      const double step = p->learning_rate * tn[v].leaf_value;
+      const int64_t* rows = order + seg_start[v];
+      for (int64_t k = 0; k < seg_count[v]; ++k) {
+        pred[rows[k]] = pred[rows[k]] + step;
+        if (leaf_of_row && t == p->n_trees - 1) leaf_of_row[rows[k]] = v;
+      }
+    }
+  }
+  free(g), free(order), free(scratch), free(seg_start), free(seg_count), free(cnt), free(G), free(H);
+  return ORC_OK;
+}
+
+/*
+ * Stable partition of one level's row-index segments (the oracle's own
+ * restatement of the partition step, [MPS-TC] s.6 step 5).  For slot s with
+ * split_feature[s] >= 0 the rows idx_in[seg_start[s] .. +seg_count[s]) are
+ * written to idx_out at the same offset, those with bin <= split_bin[s] first,
+ * both groups in their input order.  Slots without a split are copied.
+ */
+int orc_partition(const uint8_t* bins, int64_t N, int32_t n_slots, const int32_t* split_feature,
+                  const int32_t* split_bin, const int64_t* seg_start, const int64_t* seg_count,
+                  const int64_t* idx_in, int64_t* idx_out, int64_t* left_count) {
+  if (!bins || !split_feature || !split_bin || !seg_start || !seg_count || !idx_in || !idx_out) return ORC_EINVAL;
+  for (int32_t s = 0; s < n_slots; ++s) {
+    const int64_t* in = idx_in + seg_start[s];
+    int64_t* out = idx_out + seg_start[s];
+    const int64_t n = seg_count[s];
+    if (split_feature[s] < 0) {
+      memcpy(out, in, sizeof(int64_t) * (size_t)n);
+      if (left_count) left_count[s] = 0;
+      continue;
+    }
+    const uint8_t* col = bins + (int64_t)split_feature[s] * N;
+    int64_t w = 0;
+    for (int64_t k = 0; k < n; ++k)
+      if (col[in[k]] <= split_bin[s]) out[w++] = in[k];
+    if (left_count) left_count[s] = w;
+    for (int64_t k = 0; k < n; ++k)
+      if (!(col[in[k]] <= split_bin[s])) out[w++] = in[k];
+  }
+  return ORC_OK;
+}
+
+/* [MPS-TC] s.6 step 7: pred_i + (lr * leaf_value[node_of_row[i]]). */
+int orc_update_predictions(double* pred, const double* leaf_value, const int32_t* node_of_row, int64_t N,
+                           double lr) {
+  if (!pred || !leaf_value || !node_of_row) return ORC_EINVAL;
+  for (int64_t i = 0; i < N; ++i) {
+    const double step = lr * leaf_value[node_of_row[i]];
+    pred[i] = pred[i] + step;
+  }
+  return ORC_OK;
+}

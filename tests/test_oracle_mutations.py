@@ -1,0 +1,94 @@
+"""The oracle's pins must catch plausible mistakes.
+
+Each case plants one mistake (a dropped term, a wrong sign, a wrong index or
+comparison) in a temporary copy of the oracle's C source, builds it with gcc
+and runs a selection of the pins against it; at least one pin must fail.  The
+committed oracle source is never modified.
+"""
+import os
+import subprocess
+import sys
+
+import pytest
+
+import oracle
+from tests import test_oracle_hand_trees as hand
+from tests import test_oracle_pins as pins
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+MUTATIONS = {
+    "parent score sign": ("return 0.5 * ((sL + sR) - sP) - gamma;", "return 0.5 * ((sL + sR) + sP) - gamma;"),
+    "weight sign": ("return -G / (H + lambda);", "return G / (H + lambda);"),
+    "lambda dropped from score": ("return (G * G) / (H + lambda);", "return (G * G) / (H);"),
+    "gamma dropped": ("return 0.5 * ((sL + sR) - sP) - gamma;", "return 0.5 * ((sL + sR) - sP);"),
+    "routing < instead of <=": ("if (col[rows[k]] <= b) dst[w++] = rows[k];", "if (col[rows[k]] < b) dst[w++] = rows[k];"),
+    "tie-break keeps the later candidate": ("if (!out->valid || gain > out->gain) {", "if (!out->valid || gain >= out->gain) {"),
+    "min_samples_leaf strict": ("if (!(cL >= msl && cR >= msl && HL >= mcw && HR >= mcw && HL > 0.0 && HR > 0.0)) continue;\n      double gain = orc_gain(GL, HL, GR, HR, G_P, H_P, lambda, gamma);\n      if (!out->valid",
+                                "if (!(cL > msl && cR >= msl && HL >= mcw && HR >= mcw && HL > 0.0 && HR > 0.0)) continue;\n      double gain = orc_gain(GL, HL, GR, HR, G_P, H_P, lambda, gamma);\n      if (!out->valid"),
+    "right sum uses +": ("double GR = G_P - GL, HR = H_P - HL;\n      if (!(cL >= msl && cR >= msl && HL >= mcw && HR >= mcw && HL > 0.0 && HR > 0.0)) continue;\n      double gain = orc_gain(GL, HL, GR, HR, G_P, H_P, lambda, gamma);\n      if (!out->valid",
+                         "double GR = G_P + GL, HR = H_P - HL;\n      if (!(cL >= msl && cR >= msl && HL >= mcw && HR >= mcw && HL > 0.0 && HR > 0.0)) continue;\n      double gain = orc_gain(GL, HL, GR, HR, G_P, H_P, lambda, gamma);\n      if (!out->valid"),
+    "last threshold skipped": ("for (int32_t b = 0; b <= nb - 2; ++b) {\n      GL += gg[b];\n      HL += hh[b];\n      cL += c[b];\n      int64_t cR = n_P - cL;\n      double GR",
+                               "for (int32_t b = 0; b <= nb - 3; ++b) {\n      GL += gg[b];\n      HL += hh[b];\n      cL += c[b];\n      int64_t cR = n_P - cL;\n      double GR"),
+    "prediction update sign": ("pred[rows[k]] = pred[rows[k]] + step;", "pred[rows[k]] = pred[rows[k]] - step;"),
+    "quantile index off by one": ("int64_t pk = ((int64_t)k * N + B - 1) / B - 1;", "int64_t pk = ((int64_t)k * N + B - 1) / B;"),
+    "initial prediction": ("const double init = sum / (double)N;", "const double init = sum / (double)(N + 1);"),
+    "gradient sign": ("g[i] = pred[i] - (double)label[i];", "g[i] = (double)label[i] - pred[i];"),
+    "feature index transposed": ("const uint8_t* col = bins + (int64_t)j * N;\n    uint32_t* c", "const uint8_t* col = bins + (int64_t)(F - 1 - j) * N;\n    uint32_t* c"),
+}
+
+PINS = [
+    ("hand single split", lambda o: hand.test_hand_tree_single_split(o)),
+    ("hand two trees", lambda o: hand.test_hand_tree_two_trees_lambda_one(o)),
+    ("hand gamma 8", lambda o: hand.test_hand_tree_validity_rules(o, dict(gamma=8.0), None)),
+    ("hand msl 2", lambda o: hand.test_hand_tree_validity_rules(o, dict(min_samples_leaf=2), (0, 1))),
+    ("tie feature", lambda o: hand.test_tie_break_prefers_smaller_feature(o)),
+    ("cart", lambda o: [pins.test_depth1_tree_is_cart_stump(o, s) for s in range(3)]),
+    ("brute", lambda o: [pins.test_root_split_matches_brute_force(o, s) for s in range(12)]),
+    ("quantize balanced", lambda o: pins.test_quantize_all_distinct_balanced(o, 1000, 32)),
+    ("invariants", lambda o: pins.test_training_invariants(o, "tiny", None, 3)),
+]
+
+
+def _run_pins_against(src: str, so: str) -> list:
+    """Run the pins against a mutant build; returns the names of the pins that failed."""
+    oracle._SRC, oracle._LIB, oracle._lib = src, so, None
+    caught = []
+    for pin_name, pin in PINS:
+        try:
+            pin(oracle)
+        except (AssertionError, oracle.OracleError):
+            caught.append(pin_name)
+    return caught
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_pins_catch_planted_mistake(tmp_path, name):
+    old, new = MUTATIONS[name]
+    src = open(oracle._SRC).read()
+    assert src.count(old) == 1, f"mutation anchor not unique/missing: {name}"
+    mut_src = tmp_path / "gbdt_oracle_mut.c"
+    mut_src.write_text(src.replace(old, new))
+    so = tmp_path / "libmut.so"
+    subprocess.run(["gcc", "-O1", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off", "-o", str(so), str(mut_src),
+                    "-lm"], check=True, capture_output=True)
+    # a separate process, so that a mutant that reads out of bounds cannot take the suite down
+    r = subprocess.run([sys.executable, "-c",
+                        "import sys; from tests.test_oracle_mutations import _run_pins_against as r; "
+                        "c = r(sys.argv[1], sys.argv[2]); print(c); sys.exit(1 if c else 0)",
+                        str(mut_src), str(so)], cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert r.returncode != 0, f"no pin caught the planted mistake '{name}'"
+
+
+def test_control_unmutated_oracle_passes_runner(tmp_path):
+    # Guards the test above: the same runner on the unmodified source must report no failure.
+    mut_src = tmp_path / "gbdt_oracle_copy.c"
+    mut_src.write_text(open(oracle._SRC).read())
+    so = tmp_path / "libcopy.so"
+    subprocess.run(["gcc", "-O1", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off", "-o", str(so), str(mut_src),
+                    "-lm"], check=True, capture_output=True)
+    r = subprocess.run([sys.executable, "-c",
+                        "import sys; from tests.test_oracle_mutations import _run_pins_against as r; "
+                        "c = r(sys.argv[1], sys.argv[2]); print(c); sys.exit(1 if c else 0)",
+                        str(mut_src), str(so)], cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stdout + r.stderr
