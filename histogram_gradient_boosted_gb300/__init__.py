@@ -1,0 +1,292 @@
+"""Python binding of libgbdt.so, the GB300 (sm_103a) level-wise histogram GBDT library.
+
+Argument marshalling only: every step runs in the library's CUDA kernels; the
+functions here turn torch CUDA tensors into device pointers, allocate the
+caller-side workspace the C ABI asks for, pass the current CUDA stream, and
+raise ``GbdtError`` on a non-zero status.  There is no CPU path: without a
+CUDA device or without the built library every call raises.
+
+The C declarations, with their argument meaning, layout and error behaviour,
+are in ``include/gbdt.h``; names here match them without the ``gbdt_`` prefix
+(the raw symbols are reachable through ``lib()``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+from . import build as _build
+
+__all__ = ["lib", "GbdtError", "Params", "NODE_DTYPE", "SPLIT_DTYPE", "LEVEL_DTYPE", "SEGMENT_DTYPE",
+           "Diagnostics", "quantize", "train", "compute_gradients", "gradient_scale", "build_histograms",
+           "subtract_histograms", "find_splits", "partition", "update_predictions", "padded_ld",
+           "EXPORTED_SYMBOLS"]
+
+OK, ERR_INVALID_ARG, ERR_NONFINITE, ERR_WORKSPACE, ERR_CUDA, ERR_INTERNAL = 0, -1, -2, -3, -4, -5
+DTYPE_F32, DTYPE_F64 = 0, 1
+MAX_BINS, MAX_DEPTH = 256, 12
+
+EXPORTED_SYMBOLS = [
+    "gbdt_last_error", "gbdt_version", "gbdt_validate_params", "gbdt_quantize_workspace_size", "gbdt_quantize",
+    "gbdt_gradients_workspace_size", "gbdt_compute_gradients", "gbdt_gradient_scale",
+    "gbdt_histograms_workspace_size", "gbdt_build_histograms", "gbdt_subtract_histograms", "gbdt_find_splits",
+    "gbdt_partition_workspace_size", "gbdt_partition", "gbdt_update_predictions", "gbdt_train_workspace_size",
+    "gbdt_train", "gbdt_debug_inject_failure",
+]
+
+
+class GbdtError(RuntimeError):
+    def __init__(self, code: int, message: str):
+        super().__init__(f"[{code}] {message}")
+        self.code = code
+
+
+class Params(ctypes.Structure):
+    _fields_ = [("n_trees", ctypes.c_int32), ("max_depth", ctypes.c_int32), ("learning_rate", ctypes.c_double),
+                ("reg_lambda", ctypes.c_double), ("gamma", ctypes.c_double), ("min_samples_leaf", ctypes.c_int32),
+                ("min_child_weight", ctypes.c_double)]
+
+
+class Diagnostics(ctypes.Structure):
+    _fields_ = [("hist_launches", ctypes.c_int64), ("hist_ms", ctypes.c_double), ("hist_bytes", ctypes.c_double),
+                ("hist_rows", ctypes.c_int64), ("total_ms", ctypes.c_double), ("kernel_launches", ctypes.c_int64),
+                ("trees_at_full_size", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+    def as_dict(self):
+        return {k: getattr(self, k) for k, _ in self._fields_ if k != "reserved"}
+
+
+NODE_DTYPE = np.dtype([("feature", np.int32), ("threshold_bin", np.int32), ("left", np.int32), ("right", np.int32),
+                       ("leaf_value", np.float64), ("gain", np.float64), ("is_leaf", np.uint8),
+                       ("reserved", np.uint8, (7,))])
+SPLIT_DTYPE = np.dtype([("feature", np.int32), ("bin", np.int32), ("gain", np.float64), ("q_left", np.int64),
+                        ("q_total", np.int64), ("cnt_left", np.uint32), ("cnt_total", np.uint32)])
+LEVEL_DTYPE = np.dtype([("node_begin", np.int32), ("n_slots", np.int32)])
+SEGMENT_DTYPE = np.dtype([("start", np.int64), ("count", np.int64)])
+assert NODE_DTYPE.itemsize == 40 and SPLIT_DTYPE.itemsize == 40
+
+_lib = None
+
+
+def lib():
+    """Load (building first if needed) libgbdt.so and declare its signatures."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = _build.LIB if os.path.exists(_build.LIB) else _build.build()
+    L = ctypes.CDLL(path)
+    P, i32, i64, sz, dbl = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t, ctypes.c_double
+    sig = {
+        "gbdt_last_error": ([], ctypes.c_char_p),
+        "gbdt_version": ([], ctypes.c_char_p),
+        "gbdt_validate_params": ([P], i32),
+        "gbdt_quantize_workspace_size": ([i64, i32], sz),
+        "gbdt_quantize": ([P, i64, i64, i32, i32, P, i64, P, P, P, sz, P], i32),
+        "gbdt_gradients_workspace_size": ([i64], sz),
+        "gbdt_compute_gradients": ([P, P, i64, P, P, P, sz, P], i32),
+        "gbdt_gradient_scale": ([P, i32, i64, P, P, sz, P], i32),
+        "gbdt_histograms_workspace_size": ([i64, i32, i32], sz),
+        "gbdt_build_histograms": ([P, i64, i64, i32, P, i32, P, P, P, i32, P, i32, P, P, P, sz, P], i32),
+        "gbdt_subtract_histograms": ([P, P, P, P, P, i32, i32, P, P, P], i32),
+        "gbdt_find_splits": ([P, P, P, i32, P, P, i32, P, P, P], i32),
+        "gbdt_partition_workspace_size": ([i64, i32], sz),
+        "gbdt_partition": ([P, i64, i64, i32, P, P, i32, P, P, P, P, P, P, P, sz, P], i32),
+        "gbdt_update_predictions": ([P, P, P, i32, i64, dbl, P], i32),
+        "gbdt_train_workspace_size": ([i64, i32, P], sz),
+        "gbdt_train": ([P, i64, P, i64, i32, P, P, P, P, P, P, P, P, sz, P], i32),
+        "gbdt_debug_inject_failure": ([i32], None),
+    }
+    for name, (args, res) in sig.items():
+        fn = getattr(L, name)
+        fn.argtypes = args
+        fn.restype = res
+    _lib = L
+    return _lib
+
+
+# ---------------------------------------------------------------------------------------- helpers
+def _torch():
+    import torch
+
+    if not torch.cuda.is_available():
+        raise GbdtError(ERR_CUDA, "no CUDA device: this library has no CPU path")
+    return torch
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else None
+
+
+def _stream():
+    return ctypes.c_void_p(_torch().cuda.current_stream().cuda_stream)
+
+
+def _check(rc: int):
+    if rc != OK:
+        raise GbdtError(rc, lib().gbdt_last_error().decode())
+
+
+def _workspace(nbytes: int):
+    torch = _torch()
+    return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device="cuda")
+
+
+def _dev(arr, dtype):
+    """numpy structured array -> CUDA byte tensor with the same bytes."""
+    torch = _torch()
+    a = np.ascontiguousarray(arr, dtype=dtype)
+    return torch.from_numpy(a.view(np.uint8).reshape(-1).copy()).cuda()
+
+
+def _host(t, dtype, count):
+    return np.frombuffer(t.cpu().numpy().tobytes(), dtype=dtype, count=count)
+
+
+def padded_ld(n: int) -> int:
+    """Column stride for binned features: n rounded up to a multiple of 16."""
+    return (int(n) + 15) // 16 * 16
+
+
+def make_params(n_trees=1, max_depth=6, learning_rate=0.1, reg_lambda=1.0, gamma=0.0, min_samples_leaf=1,
+                min_child_weight=0.0, **_ignored) -> Params:
+    return Params(int(n_trees), int(max_depth), float(learning_rate), float(reg_lambda), float(gamma),
+                  int(min_samples_leaf), float(min_child_weight))
+
+
+def version() -> str:
+    return lib().gbdt_version().decode()
+
+
+def validate_params(**kw) -> int:
+    p = make_params(**kw)
+    return lib().gbdt_validate_params(ctypes.byref(p))
+
+
+# ---------------------------------------------------------------------------------------- entry points
+def quantize(X, max_bins: int, ldb: int | None = None):
+    """X: (F, N) float32 CUDA tensor -> bins (F, ldb) uint8, edges (F, max_bins-1) f32, n_bins (F,) i32."""
+    torch = _torch()
+    assert X.is_cuda and X.dtype == torch.float32 and X.dim() == 2 and X.stride(1) == 1
+    F, N = X.shape
+    ldb = padded_ld(N) if ldb is None else ldb
+    bins = torch.empty((F, ldb), dtype=torch.uint8, device="cuda")
+    edges = torch.empty((F, max_bins - 1), dtype=torch.float32, device="cuda")
+    n_bins = torch.empty(F, dtype=torch.int32, device="cuda")
+    ws = _workspace(lib().gbdt_quantize_workspace_size(N, F))
+    ldx = X.stride(0) if F > 1 else N  # a size-1 leading dim may carry any stride
+    _check(lib().gbdt_quantize(_ptr(X), ldx, N, F, max_bins, _ptr(bins), ldb, _ptr(edges), _ptr(n_bins),
+                               _ptr(ws), ws.numel(), _stream()))
+    return bins, edges, n_bins
+
+
+def compute_gradients(pred, label):
+    torch = _torch()
+    N = pred.shape[0]
+    g = torch.empty(N, dtype=torch.float64, device="cuda")
+    S = torch.empty(1, dtype=torch.int32, device="cuda")
+    ws = _workspace(lib().gbdt_gradients_workspace_size(N))
+    _check(lib().gbdt_compute_gradients(_ptr(pred), _ptr(label), N, _ptr(g), _ptr(S), _ptr(ws), ws.numel(),
+                                        _stream()))
+    return g, S
+
+
+def gradient_scale(g):
+    torch = _torch()
+    S = torch.empty(1, dtype=torch.int32, device="cuda")
+    ws = _workspace(lib().gbdt_gradients_workspace_size(g.shape[0]))
+    dt = DTYPE_F32 if g.dtype == torch.float32 else DTYPE_F64
+    _check(lib().gbdt_gradient_scale(_ptr(g), dt, g.shape[0], _ptr(S), _ptr(ws), ws.numel(), _stream()))
+    return S
+
+
+def build_histograms(bins, N, g, fixed_exp, node_of_row, level, max_slots, build_flag, max_build, hist_cnt=None,
+                     hist_q=None, ws=None):
+    """bins (F, ldb) uint8; g f32/f64 (N,); node_of_row uint16-valued int16 tensor or uint16 (N,);
+    level: CUDA tensor of LEVEL_DTYPE bytes; build_flag uint8 (max_slots,).  Returns (hist_cnt, hist_q)."""
+    torch = _torch()
+    F, ldb = bins.shape
+    if hist_cnt is None:
+        hist_cnt = torch.zeros((max_slots, F, 256), dtype=torch.int32, device="cuda")
+        hist_q = torch.zeros((max_slots, F, 256), dtype=torch.int64, device="cuda")
+    if ws is None:
+        ws = _workspace(lib().gbdt_histograms_workspace_size(N, F, max_slots))
+    dt = DTYPE_F32 if g.dtype == torch.float32 else DTYPE_F64
+    _check(lib().gbdt_build_histograms(_ptr(bins), ldb, N, F, _ptr(g), dt, _ptr(fixed_exp), _ptr(node_of_row),
+                                       _ptr(level), max_slots, _ptr(build_flag), max_build, _ptr(hist_cnt),
+                                       _ptr(hist_q), _ptr(ws), ws.numel(), _stream()))
+    return hist_cnt, hist_q
+
+
+def subtract_histograms(prev_cnt, prev_q, pair_parent, build_flag, level, max_slots, hist_cnt, hist_q):
+    F = hist_cnt.shape[1]
+    _check(lib().gbdt_subtract_histograms(_ptr(prev_cnt), _ptr(prev_q), _ptr(pair_parent), _ptr(build_flag),
+                                          _ptr(level), max_slots, F, _ptr(hist_cnt), _ptr(hist_q), _stream()))
+    return hist_cnt, hist_q
+
+
+def find_splits(hist_cnt, hist_q, fixed_exp, n_bins, level, max_slots, out=None, **params):
+    torch = _torch()
+    F = hist_cnt.shape[1]
+    p = make_params(**params)
+    if out is None:
+        out = torch.empty(max_slots * SPLIT_DTYPE.itemsize, dtype=torch.uint8, device="cuda")
+    _check(lib().gbdt_find_splits(_ptr(hist_cnt), _ptr(hist_q), _ptr(fixed_exp), F, _ptr(n_bins), _ptr(level),
+                                  max_slots, ctypes.byref(p), _ptr(out), _stream()))
+    return out
+
+
+def partition(bins, N, splits, level, max_slots, seg_in, idx_in, node_of_row, idx_out=None):
+    torch = _torch()
+    F, ldb = bins.shape
+    if idx_out is None:
+        idx_out = torch.zeros_like(idx_in)
+    seg_out = torch.zeros(2 * max_slots * SEGMENT_DTYPE.itemsize, dtype=torch.uint8, device="cuda")
+    next_level = torch.zeros(LEVEL_DTYPE.itemsize, dtype=torch.uint8, device="cuda")
+    ws = _workspace(lib().gbdt_partition_workspace_size(N, max_slots))
+    _check(lib().gbdt_partition(_ptr(bins), ldb, N, F, _ptr(splits), _ptr(level), max_slots, _ptr(seg_in),
+                                _ptr(idx_in), _ptr(node_of_row), _ptr(idx_out), _ptr(seg_out), _ptr(next_level),
+                                _ptr(ws), ws.numel(), _stream()))
+    return idx_out, seg_out, next_level
+
+
+def update_predictions(pred, leaf_of_row, leaf_value, lr):
+    _check(lib().gbdt_update_predictions(_ptr(pred), _ptr(leaf_of_row), _ptr(leaf_value), leaf_value.shape[0],
+                                         pred.shape[0], float(lr), _stream()))
+    return pred
+
+
+def train_workspace_size(N: int, F: int, **params) -> int:
+    p = make_params(**params)
+    return lib().gbdt_train_workspace_size(N, F, ctypes.byref(p))
+
+
+def train(bins, n_bins, label, N: int | None = None, diagnostics: bool = False, ws=None, pred=None, **params):
+    """Train on binned features.  bins (F, ldb) uint8 CUDA, n_bins (F,) int32 CUDA, label (N,) float32 CUDA.
+    Returns dict(nodes (T, M) NODE_DTYPE, nodes_per_tree, init_pred, pred (CUDA f64), diag)."""
+    torch = _torch()
+    F, ldb = bins.shape
+    N = label.shape[0] if N is None else N
+    p = make_params(**params)
+    T, M = p.n_trees, (1 << (p.max_depth + 1)) - 1
+    if pred is None:
+        pred = torch.empty(N, dtype=torch.float64, device="cuda")
+    if ws is None:
+        ws = _workspace(lib().gbdt_train_workspace_size(N, F, ctypes.byref(p)))
+    nodes = np.zeros((max(T, 1), M), NODE_DTYPE)
+    npt = np.zeros(max(T, 1), np.int32)
+    init = ctypes.c_double(0.0)
+    diag = Diagnostics() if diagnostics else None
+    rc = lib().gbdt_train(_ptr(bins), ldb, _ptr(n_bins), N, F, _ptr(label), ctypes.byref(p), _ptr(pred),
+                          ctypes.byref(init), nodes.ctypes.data_as(ctypes.c_void_p),
+                          npt.ctypes.data_as(ctypes.c_void_p), ctypes.byref(diag) if diag is not None else None,
+                          _ptr(ws), ws.numel(), _stream())
+    _check(rc)
+    return dict(nodes=nodes[:T], nodes_per_tree=npt[:T], init_pred=init.value, pred=pred,
+                diag=diag.as_dict() if diag is not None else None)
+
+
+def inject_failure(after_levels: int):
+    """Testing hook: make the next gbdt_train calls fail on the host after that many levels (-1 disables)."""
+    lib().gbdt_debug_inject_failure(int(after_levels))

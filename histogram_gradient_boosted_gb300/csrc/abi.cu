@@ -1,0 +1,65 @@
+// Error reporting, version, parameter rules and device queries of the C ABI.
+#include <cmath>
+#include <cstring>
+
+#include "common.cuh"
+
+namespace gbdt {
+
+namespace {
+thread_local char t_msg[512] = "";
+}
+
+void set_error(const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(t_msg, sizeof(t_msg), fmt, ap);
+  va_end(ap);
+}
+
+void clear_error() { t_msg[0] = '\0'; }
+
+int sm_count() {
+  static int n = [] {
+    int dev = 0, v = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 152;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) return 152;
+    return v;
+  }();
+  return n;
+}
+
+}  // namespace gbdt
+
+// "Module Design: Training Core" s.3: min_samples_leaf >= 1, min_child_weight >= 0,
+// reg_lambda >= 0, gamma >= 0, every floating parameter finite.
+int validate_params(const gbdt_params* p) {
+  using gbdt::set_error;
+  if (!p) {
+    set_error("parameters: null pointer");
+    return GBDT_ERR_INVALID_ARG;
+  }
+  if (!std::isfinite(p->learning_rate) || !std::isfinite(p->reg_lambda) || !std::isfinite(p->gamma) ||
+      !std::isfinite(p->min_child_weight)) {
+    set_error("parameters: every floating parameter must be finite");
+    return GBDT_ERR_INVALID_ARG;
+  }
+  if (p->min_samples_leaf < 1 || p->min_child_weight < 0.0 || p->reg_lambda < 0.0 || p->gamma < 0.0) {
+    set_error("parameters: need min_samples_leaf >= 1, min_child_weight >= 0, reg_lambda >= 0, gamma >= 0");
+    return GBDT_ERR_INVALID_ARG;
+  }
+  if (p->n_trees < 0 || p->max_depth < 0 || p->max_depth > GBDT_MAX_DEPTH) {
+    set_error("parameters: need n_trees >= 0 and 0 <= max_depth <= %d", GBDT_MAX_DEPTH);
+    return GBDT_ERR_INVALID_ARG;
+  }
+  return GBDT_OK;
+}
+
+extern "C" const char* gbdt_last_error(void) { return gbdt::t_msg; }
+
+extern "C" const char* gbdt_version(void) { return "gbdt-gb300 0.1 (sm_103a)"; }
+
+extern "C" int gbdt_validate_params(const gbdt_params* p) {
+  gbdt::clear_error();
+  return validate_params(p);
+}

@@ -1,0 +1,97 @@
+// Internal helpers shared by the library's translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <cstdarg>
+#include <cstdio>
+
+#include "gbdt.h"
+
+namespace gbdt {
+
+constexpr int kBins = 256;           // histogram width: every value of a uint8 bin
+constexpr int kMaxSlots = 4096;      // slots per level the kernels support
+constexpr size_t kWsAlign = 256;     // alignment of every workspace carve-out
+
+// Bits of the device error word (kernels OR them in; the host reports INTERNAL).
+enum : int32_t {
+  kErrHistTotals = 1,     // a feature's histogram does not add up to the node totals
+  kErrSlotRange = 2,      // a row's node id is outside the level it should be in
+  kErrPartitionCount = 4, // partition left count differs from the split record
+  kErrLevelSize = 8,      // a level has more slots than the launch bound
+};
+
+// ---- thread-local error message -------------------------------------------------
+void set_error(const char* fmt, ...);
+void clear_error();
+
+#define GBDT_CHECK_ARG(cond, ...)         \
+  do {                                    \
+    if (!(cond)) {                        \
+      ::gbdt::set_error(__VA_ARGS__);     \
+      return GBDT_ERR_INVALID_ARG;        \
+    }                                     \
+  } while (0)
+
+#define GBDT_CUDA(call)                                                                        \
+  do {                                                                                         \
+    cudaError_t e_ = (call);                                                                   \
+    if (e_ != cudaSuccess) {                                                                   \
+      ::gbdt::set_error("%s failed: %s (%s:%d)", #call, cudaGetErrorString(e_), __FILE__, __LINE__); \
+      return GBDT_ERR_CUDA;                                                                    \
+    }                                                                                          \
+  } while (0)
+
+// Error from the launches just queued (configuration errors surface here).
+#define GBDT_LAUNCH_CHECK() GBDT_CUDA(cudaGetLastError())
+
+inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Bump allocator over the caller's workspace.
+struct Carve {
+  char* base;
+  size_t cap;
+  size_t used = 0;
+  Carve(void* b, size_t c) : base(static_cast<char*>(b)), cap(c) {}
+  template <typename T>
+  T* take(size_t count) {
+    size_t off = (used + kWsAlign - 1) / kWsAlign * kWsAlign;
+    used = off + count * sizeof(T);
+    return (base && used <= cap) ? reinterpret_cast<T*>(base + off) : nullptr;
+  }
+  bool ok() const { return used <= cap; }
+};
+
+// Fixed-point exponent: S = 62 - ceil(log2 N) - E with maxabs < 2^E, so that
+// sum |round(g * 2^S)| < 2^62 for any row set; S = 0 when all g are zero.
+// Clamped to keep 2^S a normal double.
+__host__ __device__ inline int fixed_exponent(double maxabs, int64_t N) {
+  if (!(maxabs > 0.0)) return 0;
+  int E = 0;
+  frexp(maxabs, &E);  // maxabs = m * 2^E, 0.5 <= m < 1
+  int L = 0;
+  while ((int64_t(1) << L) < N) ++L;
+  int S = 62 - L - E;
+  if (S > 1000) S = 1000;
+  if (S < -1000) S = -1000;
+  return S;
+}
+
+// round-half-even(g * 2^S) for the scale 2^S (an exact power of two).
+__device__ __forceinline__ int64_t to_fixed(double g, double scale) { return __double2ll_rn(g * scale); }
+
+// Convert a fixed-point sum back to a double: q * 2^-S.
+__host__ __device__ inline double from_fixed(int64_t q, int S) { return ldexp(static_cast<double>(q), -S); }
+
+__device__ __forceinline__ void raise_error(int32_t* flag, int32_t bits) {
+  if (flag) atomicOr(flag, bits);
+}
+
+inline int ceil_div(int64_t a, int64_t b) { return static_cast<int>((a + b - 1) / b); }
+
+// Number of SMs of the current device (cached per process; one device per process).
+int sm_count();
+
+}  // namespace gbdt

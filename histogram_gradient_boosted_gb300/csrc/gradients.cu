@@ -1,0 +1,247 @@
+// Squared-error gradients, label mean, prediction update, fixed-point exponent.
+// "Module Design: Training Core" s.2 (g = pred - label, h = 1) and s.6 step 7
+// (update training predictions after the tree); "Gradient boosted trees
+// (spec model)", forward pass (init + learning_rate * tree output).
+#include "kernels.cuh"
+
+namespace gbdt {
+
+namespace {
+
+__device__ __forceinline__ unsigned long long abs_bits(double v) {
+  return static_cast<unsigned long long>(__double_as_longlong(fabs(v)));
+}
+
+// Block max of non-negative doubles held as their bit patterns, one atomic per block.
+__device__ __forceinline__ void block_max_to(unsigned long long v, unsigned long long* out) {
+  __shared__ unsigned long long red[32];
+  for (int o = 16; o > 0; o >>= 1) {
+    unsigned long long w = __shfl_xor_sync(0xffffffffu, v, o);
+    v = w > v ? w : v;
+  }
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  if (warp == 0) {
+    const int nw = (blockDim.x + 31) >> 5;
+    v = lane < nw ? red[lane] : 0ull;
+    for (int o = 16; o > 0; o >>= 1) {
+      unsigned long long w = __shfl_xor_sync(0xffffffffu, v, o);
+      v = w > v ? w : v;
+    }
+    if (lane == 0 && v) atomicMax(out, v);
+  }
+}
+
+// Fixed grid; each block sums a contiguous range in a fixed order, then a fixed tree.
+__global__ void label_sum_kernel(const float* __restrict__ label, int64_t N, double* __restrict__ partials,
+                                 int32_t* __restrict__ nonfinite) {
+  const int64_t per = (N + gridDim.x - 1) / gridDim.x;
+  const int64_t b0 = blockIdx.x * per;
+  const int64_t b1 = min(N, b0 + per);
+  double acc = 0.0;
+  bool bad = false;
+  for (int64_t i = b0 + threadIdx.x; i < b1; i += blockDim.x) {
+    float v = label[i];
+    bad |= !isfinite(v);
+    acc += static_cast<double>(v);
+  }
+  if (bad) atomicOr(nonfinite, 1);
+  __shared__ double red[kSumThreads];
+  red[threadIdx.x] = acc;
+  __syncthreads();
+  for (int w = blockDim.x / 2; w > 0; w >>= 1) {
+    if (threadIdx.x < w) red[threadIdx.x] += red[threadIdx.x + w];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) partials[blockIdx.x] = red[0];
+}
+
+__global__ void label_mean_kernel(const double* __restrict__ partials, int64_t N, double* __restrict__ init) {
+  __shared__ double red[kSumThreads];
+  double acc = 0.0;
+  for (int i = threadIdx.x; i < kSumBlocks; i += blockDim.x) acc += partials[i];
+  red[threadIdx.x] = acc;
+  __syncthreads();
+  for (int w = blockDim.x / 2; w > 0; w >>= 1) {
+    if (threadIdx.x < w) red[threadIdx.x] += red[threadIdx.x + w];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) *init = __ddiv_rn(red[0], static_cast<double>(N));
+}
+
+__global__ void start_tree0_kernel(const double* __restrict__ init, const float* __restrict__ label, int64_t N,
+                                   double* __restrict__ pred, double* __restrict__ g, uint16_t* __restrict__ node,
+                                   unsigned long long* maxabs) {
+  const double p0 = *init;
+  unsigned long long m = 0;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < N; i += (int64_t)gridDim.x * blockDim.x) {
+    pred[i] = p0;
+    const double gi = __dsub_rn(p0, static_cast<double>(label[i]));
+    g[i] = gi;
+    node[i] = 0;
+    const unsigned long long a = abs_bits(gi);
+    m = a > m ? a : m;
+  }
+  block_max_to(m, maxabs);
+}
+
+__global__ void finish_tree_kernel(const gbdt_node* __restrict__ tree, const int32_t* __restrict__ n_nodes,
+                                   int32_t max_nodes, double lr, const float* __restrict__ label, int64_t N,
+                                   double* __restrict__ pred, double* __restrict__ g, uint16_t* __restrict__ node,
+                                   unsigned long long* maxabs, int next) {
+  extern __shared__ double s_step[];  // lr * leaf_value per node of the tree
+  const int nn = min(*n_nodes, max_nodes);
+  for (int i = threadIdx.x; i < nn; i += blockDim.x) s_step[i] = __dmul_rn(lr, tree[i].leaf_value);
+  __syncthreads();
+  unsigned long long m = 0;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < N; i += (int64_t)gridDim.x * blockDim.x) {
+    const int v = node[i];
+    const double p = (v < nn) ? __dadd_rn(pred[i], s_step[v]) : pred[i];
+    pred[i] = p;
+    if (next) {
+      const double gi = __dsub_rn(p, static_cast<double>(label[i]));
+      g[i] = gi;
+      node[i] = 0;
+      const unsigned long long a = abs_bits(gi);
+      m = a > m ? a : m;
+    }
+  }
+  if (next) block_max_to(m, maxabs);
+}
+
+__global__ void gradients_kernel(const double* __restrict__ pred, const float* __restrict__ label, int64_t N,
+                                 double* __restrict__ g, unsigned long long* maxabs) {
+  unsigned long long m = 0;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < N; i += (int64_t)gridDim.x * blockDim.x) {
+    const double gi = __dsub_rn(pred[i], static_cast<double>(label[i]));
+    g[i] = gi;
+    const unsigned long long a = abs_bits(gi);
+    m = a > m ? a : m;
+  }
+  block_max_to(m, maxabs);
+}
+
+template <typename T>
+__global__ void maxabs_kernel(const T* __restrict__ g, int64_t N, unsigned long long* maxabs) {
+  unsigned long long m = 0;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < N; i += (int64_t)gridDim.x * blockDim.x) {
+    const unsigned long long a = abs_bits(static_cast<double>(g[i]));
+    m = a > m ? a : m;
+  }
+  block_max_to(m, maxabs);
+}
+
+__global__ void fixed_exp_kernel(const unsigned long long* maxabs, int64_t N, int32_t* fixed_exp) {
+  *fixed_exp = fixed_exponent(__longlong_as_double(static_cast<long long>(*maxabs)), N);
+}
+
+__global__ void update_predictions_kernel(double* __restrict__ pred, const uint16_t* __restrict__ leaf_of_row,
+                                          const double* __restrict__ leaf_value, int32_t n_values, int64_t N,
+                                          double lr) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < N; i += (int64_t)gridDim.x * blockDim.x) {
+    const int v = leaf_of_row[i];
+    if (v < n_values) pred[i] = __dadd_rn(pred[i], __dmul_rn(lr, leaf_value[v]));
+  }
+}
+
+int elementwise_grid(int64_t N) {
+  const int64_t want = (N + 255) / 256;
+  const int64_t cap = static_cast<int64_t>(sm_count()) * 8;
+  return static_cast<int>(want < 1 ? 1 : (want < cap ? want : cap));
+}
+
+}  // namespace
+
+void launch_label_sum(const float* label, int64_t N, double* partials, int32_t* nonfinite, cudaStream_t s) {
+  label_sum_kernel<<<kSumBlocks, kSumThreads, 0, s>>>(label, N, partials, nonfinite);
+}
+void launch_label_mean(const double* partials, int64_t N, double* init, cudaStream_t s) {
+  label_mean_kernel<<<1, kSumThreads, 0, s>>>(partials, N, init);
+}
+void launch_start_tree0(const double* init, const float* label, int64_t N, double* pred, double* g, uint16_t* node,
+                        unsigned long long* maxabs, cudaStream_t s) {
+  start_tree0_kernel<<<elementwise_grid(N), 256, 0, s>>>(init, label, N, pred, g, node, maxabs);
+}
+void launch_finish_tree(const gbdt_node* tree_nodes, const int32_t* n_nodes, int32_t max_nodes, double lr,
+                        const float* label, int64_t N, double* pred, double* g, uint16_t* node,
+                        unsigned long long* maxabs, bool next, cudaStream_t s) {
+  static bool once = (cudaFuncSetAttribute(finish_tree_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(sizeof(double) * ((1 << (GBDT_MAX_DEPTH + 1)) - 1))),
+                      true);
+  (void)once;
+  finish_tree_kernel<<<elementwise_grid(N), 256, sizeof(double) * max_nodes, s>>>(
+      tree_nodes, n_nodes, max_nodes, lr, label, N, pred, g, node, maxabs, next ? 1 : 0);
+}
+void launch_gradients(const double* pred, const float* label, int64_t N, double* g, unsigned long long* maxabs,
+                      cudaStream_t s) {
+  gradients_kernel<<<elementwise_grid(N), 256, 0, s>>>(pred, label, N, g, maxabs);
+}
+void launch_maxabs(const void* g, int32_t dtype, int64_t N, unsigned long long* maxabs, cudaStream_t s) {
+  if (dtype == GBDT_DTYPE_F32)
+    maxabs_kernel<float><<<elementwise_grid(N), 256, 0, s>>>(static_cast<const float*>(g), N, maxabs);
+  else
+    maxabs_kernel<double><<<elementwise_grid(N), 256, 0, s>>>(static_cast<const double*>(g), N, maxabs);
+}
+void launch_fixed_exp(const unsigned long long* maxabs, int64_t N, int32_t* fixed_exp, cudaStream_t s) {
+  fixed_exp_kernel<<<1, 1, 0, s>>>(maxabs, N, fixed_exp);
+}
+
+}  // namespace gbdt
+
+using namespace gbdt;
+
+extern "C" size_t gbdt_gradients_workspace_size(int64_t N) {
+  (void)N;
+  return kWsAlign;  // one 8-byte max accumulator
+}
+
+extern "C" int gbdt_compute_gradients(const double* pred, const float* label, int64_t N, double* g,
+                                      int32_t* fixed_exp, void* ws, size_t ws_bytes, void* stream) {
+  clear_error();
+  GBDT_CHECK_ARG(pred && label && g && fixed_exp, "gbdt_compute_gradients: null pointer");
+  GBDT_CHECK_ARG(N >= 1, "gbdt_compute_gradients: N must be >= 1 (got %lld)", (long long)N);
+  if (!ws || ws_bytes < gbdt_gradients_workspace_size(N) || !aligned(ws, kWsAlign)) {
+    set_error("gbdt_compute_gradients: workspace too small or misaligned");
+    return ws ? GBDT_ERR_WORKSPACE : GBDT_ERR_INVALID_ARG;
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  auto* maxabs = static_cast<unsigned long long*>(ws);
+  GBDT_CUDA(cudaMemsetAsync(maxabs, 0, sizeof(*maxabs), s));
+  launch_gradients(pred, label, N, g, maxabs, s);
+  launch_fixed_exp(maxabs, N, fixed_exp, s);
+  GBDT_LAUNCH_CHECK();
+  return GBDT_OK;
+}
+
+extern "C" int gbdt_gradient_scale(const void* g, int32_t g_dtype, int64_t N, int32_t* fixed_exp, void* ws,
+                                   size_t ws_bytes, void* stream) {
+  clear_error();
+  GBDT_CHECK_ARG(g && fixed_exp, "gbdt_gradient_scale: null pointer");
+  GBDT_CHECK_ARG(N >= 1, "gbdt_gradient_scale: N must be >= 1");
+  GBDT_CHECK_ARG(g_dtype == GBDT_DTYPE_F32 || g_dtype == GBDT_DTYPE_F64, "gbdt_gradient_scale: bad dtype %d",
+                 g_dtype);
+  if (!ws || ws_bytes < gbdt_gradients_workspace_size(N) || !aligned(ws, kWsAlign)) {
+    set_error("gbdt_gradient_scale: workspace too small or misaligned");
+    return ws ? GBDT_ERR_WORKSPACE : GBDT_ERR_INVALID_ARG;
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  auto* maxabs = static_cast<unsigned long long*>(ws);
+  GBDT_CUDA(cudaMemsetAsync(maxabs, 0, sizeof(*maxabs), s));
+  launch_maxabs(g, g_dtype, N, maxabs, s);
+  launch_fixed_exp(maxabs, N, fixed_exp, s);
+  GBDT_LAUNCH_CHECK();
+  return GBDT_OK;
+}
+
+extern "C" int gbdt_update_predictions(double* pred, const uint16_t* leaf_of_row, const double* leaf_value,
+                                       int32_t n_leaf_values, int64_t N, double lr, void* stream) {
+  clear_error();
+  GBDT_CHECK_ARG(pred && leaf_of_row && leaf_value, "gbdt_update_predictions: null pointer");
+  GBDT_CHECK_ARG(N >= 1 && n_leaf_values >= 1, "gbdt_update_predictions: bad sizes");
+  GBDT_CHECK_ARG(isfinite(lr), "gbdt_update_predictions: learning rate must be finite");
+  update_predictions_kernel<<<elementwise_grid(N), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      pred, leaf_of_row, leaf_value, n_leaf_values, N, lr);
+  GBDT_LAUNCH_CHECK();
+  return GBDT_OK;
+}

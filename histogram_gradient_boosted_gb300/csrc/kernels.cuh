@@ -1,0 +1,65 @@
+// Internal launchers shared between the entry points and the training driver.
+#pragma once
+
+#include "common.cuh"
+
+namespace gbdt {
+
+// ---- gradients.cu -------------------------------------------------------------------
+// Deterministic mean of labels: fixed grid, fixed reduction order.
+constexpr int kSumBlocks = 512;
+constexpr int kSumThreads = 256;
+void launch_label_sum(const float* label, int64_t N, double* partials /*[kSumBlocks]*/, int32_t* nonfinite,
+                      cudaStream_t s);
+void launch_label_mean(const double* partials, int64_t N, double* init /*device*/, cudaStream_t s);
+// pred = *init; g = pred - label; node = 0; maxabs = max |g| (maxabs must be reset to 0 first).
+void launch_start_tree0(const double* init, const float* label, int64_t N, double* pred, double* g, uint16_t* node,
+                        unsigned long long* maxabs, cudaStream_t s);
+// pred += lr * leaf_value(node); if next: g = pred - label, node = 0, maxabs = max|g|.
+void launch_finish_tree(const gbdt_node* tree_nodes, const int32_t* n_nodes, int32_t max_nodes, double lr,
+                        const float* label, int64_t N, double* pred, double* g, uint16_t* node,
+                        unsigned long long* maxabs, bool next, cudaStream_t s);
+void launch_gradients(const double* pred, const float* label, int64_t N, double* g, unsigned long long* maxabs,
+                      cudaStream_t s);
+void launch_maxabs(const void* g, int32_t dtype, int64_t N, unsigned long long* maxabs, cudaStream_t s);
+void launch_fixed_exp(const unsigned long long* maxabs, int64_t N, int32_t* fixed_exp, cudaStream_t s);
+
+// ---- histogram.cu ---------------------------------------------------------------------
+struct HistPlan {
+  int group_slots;  // built slots per CTA
+  int group_feats;  // features per CTA
+  int n_sgroups, n_fgroups, n_chunks;
+  int64_t rows_per_chunk;
+  size_t smem;
+  int blocks() const { return n_sgroups * n_fgroups * n_chunks; }
+};
+HistPlan plan_histograms(int64_t N, int32_t F, int32_t max_slots, int32_t max_build);
+// Zeroes the flagged slots of hist_cnt/hist_q.
+void launch_hist_zero(const gbdt_level* level, int32_t max_slots, const uint8_t* build_flag, int32_t F,
+                      uint32_t* hist_cnt, int64_t* hist_q, cudaStream_t s);
+int launch_hist_build(const HistPlan& plan, const uint8_t* bins, int64_t ldb, int64_t N, int32_t F, const void* g,
+                      int32_t g_dtype, const int32_t* fixed_exp, const uint16_t* node_of_row,
+                      const gbdt_level* level, int32_t max_slots, const uint8_t* build_flag, uint32_t* hist_cnt,
+                      int64_t* hist_q, int32_t* err, cudaStream_t s);
+void launch_hist_subtract(const uint32_t* prev_cnt, const int64_t* prev_q, const int32_t* pair_parent,
+                          const uint8_t* build_flag, const gbdt_level* level, int32_t max_slots, int32_t F,
+                          uint32_t* hist_cnt, int64_t* hist_q, int32_t* err, cudaStream_t s);
+
+// ---- split.cu -------------------------------------------------------------------------
+void launch_find_splits(const uint32_t* hist_cnt, const int64_t* hist_q, const int32_t* fixed_exp, int32_t F,
+                        const int32_t* n_bins, const gbdt_level* level, int32_t max_slots, const gbdt_params& p,
+                        gbdt_split* out, int32_t* err, cudaStream_t s);
+
+// ---- partition.cu ---------------------------------------------------------------------
+// Routing entry of a slot: split feature (-1: none), threshold bin, left child node id.
+struct Route {
+  int32_t feature;
+  int32_t bin;
+  int32_t left_node;
+  int32_t pad;
+};
+// node_of_row[r] = left_node + (bins[feature][r] > bin) for rows of slots with a split.
+void launch_route_rows(const uint8_t* bins, int64_t ldb, int64_t N, const Route* route, const gbdt_level* level,
+                       int32_t max_slots, uint16_t* node_of_row, int32_t* err, cudaStream_t s);
+
+}  // namespace gbdt

@@ -1,0 +1,437 @@
+// Training driver: level-wise growth of each tree ("Module Design: Training
+// Core" s.6): for every level, build the histograms of the active nodes (the
+// smaller child of each sibling pair directly, the larger by subtraction),
+// select splits by the frozen rule, route rows to the children, then freeze
+// the last level as leaves and update the training predictions.
+//
+// The host only queues work: every grid is sized from host-known bounds
+// (at most 2^d slots at level d), kernels read the actual level sizes from
+// device memory and idle blocks exit, so no level needs a device-to-host
+// round trip.  The only synchronisations are the input checks at the start
+// and the single copy of the finished model at the end ("Module Design:
+// Training Core" s.5: no partial model leaves a failed run).
+#include <atomic>
+#include <vector>
+
+#include "kernels.cuh"
+
+namespace gbdt {
+
+namespace {
+
+struct SlotTotals {
+  int64_t q;
+  uint32_t cnt;
+  uint32_t pad;
+};
+
+struct LevelStats {
+  int64_t n_act;  // rows in the level's nodes
+  int32_t n_slots;
+  int32_t n_built;
+};
+
+std::atomic<int32_t> g_fail_after_levels{-1};
+
+__global__ void reset_root_kernel(gbdt_level* level, uint8_t* build_flag) {
+  level->node_begin = 0;
+  level->n_slots = 1;
+  build_flag[0] = 1;
+}
+
+// Root totals when the root is also the last level (max_depth 0): count and
+// fixed-point sum of g over all rows; integer adds, so the order is irrelevant.
+__global__ void root_totals_kernel(const double* __restrict__ g, int64_t N, const int32_t* __restrict__ fixed_exp,
+                                   SlotTotals* __restrict__ tot) {
+  const double scale = ldexp(1.0, *fixed_exp);
+  long long acc = 0;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < N; i += (int64_t)gridDim.x * blockDim.x)
+    acc += to_fixed(g[i], scale);
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  if ((threadIdx.x & 31) == 0 && acc != 0)
+    atomicAdd(reinterpret_cast<unsigned long long*>(&tot->q), static_cast<unsigned long long>(acc));
+  if (blockIdx.x == 0 && threadIdx.x == 0) tot->cnt = static_cast<uint32_t>(N);
+}
+
+// One CTA of 1024 threads: child numbering by an in-order scan of the split
+// flags, node records of this level, and the next level's bookkeeping.
+__global__ void __launch_bounds__(1024)
+    apply_level_kernel(int d, int D, const gbdt_level* __restrict__ level, int32_t max_slots,
+                       const gbdt_split* __restrict__ splits, const SlotTotals* __restrict__ totals,
+                       const uint8_t* __restrict__ build_flag, const int32_t* __restrict__ fixed_exp, double lambda,
+                       gbdt_node* __restrict__ tree, int32_t* __restrict__ n_nodes_out,
+                       gbdt_level* __restrict__ next_level, SlotTotals* __restrict__ next_totals,
+                       int32_t* __restrict__ pair_parent, uint8_t* __restrict__ next_build, Route* __restrict__ route,
+                       LevelStats* __restrict__ stats, int32_t* __restrict__ err) {
+  __shared__ int s_a[1024];
+  __shared__ int s_pre;
+  __shared__ unsigned long long s_act;
+  __shared__ int s_built;
+  if (threadIdx.x == 0) {
+    s_pre = 0;
+    s_act = 0;
+    s_built = 0;
+  }
+  __syncthreads();
+  const int node_begin = level->node_begin;
+  int n_slots = level->n_slots;
+  if (n_slots > max_slots) {
+    if (threadIdx.x == 0) raise_error(err, kErrLevelSize);
+    n_slots = max_slots;
+  }
+  const int next_begin = node_begin + n_slots;
+  const int S = *fixed_exp;
+  for (int c0 = 0; c0 < n_slots; c0 += blockDim.x) {
+    const int s = c0 + threadIdx.x;
+    const bool in = s < n_slots;
+    int is_split = 0;
+    gbdt_split sp{};
+    SlotTotals tot{};
+    if (in) {
+      if (d < D) {
+        sp = splits[s];
+        is_split = sp.feature >= 0;
+        if (d > 0 && (sp.q_total != totals[s].q || sp.cnt_total != totals[s].cnt)) raise_error(err, kErrHistTotals);
+        tot.q = sp.q_total;
+        tot.cnt = sp.cnt_total;
+      } else {
+        tot = totals[s];
+      }
+      atomicAdd(&s_act, static_cast<unsigned long long>(tot.cnt));
+      if (d < D && build_flag[s]) atomicAdd(&s_built, 1);
+    }
+    s_a[threadIdx.x] = is_split;
+    __syncthreads();
+    for (int o = 1; o < blockDim.x; o <<= 1) {
+      const int v = threadIdx.x >= o ? s_a[threadIdx.x - o] : 0;
+      __syncthreads();
+      s_a[threadIdx.x] += v;
+      __syncthreads();
+    }
+    if (in) {
+      const int k = s_pre + s_a[threadIdx.x] - is_split;
+      const double G = from_fixed(tot.q, S);
+      const double H = static_cast<double>(tot.cnt);
+      gbdt_node nd;
+      nd.leaf_value = __ddiv_rn(-G, __dadd_rn(H, lambda));
+      nd.reserved[0] = nd.reserved[1] = nd.reserved[2] = nd.reserved[3] = 0;
+      nd.reserved[4] = nd.reserved[5] = nd.reserved[6] = 0;
+      Route rt{-1, -1, -1, k};
+      if (is_split) {
+        nd.feature = sp.feature;
+        nd.threshold_bin = sp.bin;
+        nd.left = next_begin + 2 * k;
+        nd.right = next_begin + 2 * k + 1;
+        nd.gain = sp.gain;
+        nd.is_leaf = 0;
+        const uint32_t cl = sp.cnt_left, cr = sp.cnt_total - sp.cnt_left;
+        next_totals[2 * k] = SlotTotals{sp.q_left, cl, 0};
+        next_totals[2 * k + 1] = SlotTotals{
+            static_cast<int64_t>(static_cast<uint64_t>(sp.q_total) - static_cast<uint64_t>(sp.q_left)), cr, 0};
+        pair_parent[k] = s;
+        const uint8_t left_small = cl <= cr ? 1 : 0;  // build the smaller child; ties build the left one
+        next_build[2 * k] = left_small;
+        next_build[2 * k + 1] = 1 - left_small;
+        rt = Route{sp.feature, sp.bin, next_begin + 2 * k, k};
+      } else {
+        nd.feature = nd.threshold_bin = nd.left = nd.right = -1;
+        nd.gain = 0.0;
+        nd.is_leaf = 1;
+      }
+      tree[node_begin + s] = nd;
+      route[s] = rt;
+    }
+    __syncthreads();
+    if (threadIdx.x == blockDim.x - 1) s_pre += s_a[threadIdx.x];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    next_level->node_begin = next_begin;
+    next_level->n_slots = 2 * s_pre;
+    *n_nodes_out = next_begin + 2 * s_pre;
+    stats->n_act = static_cast<int64_t>(s_act);
+    stats->n_slots = n_slots;
+    stats->n_built = s_built;
+  }
+}
+
+struct TrainWs {
+  double* g;
+  uint16_t* node;
+  uint32_t* hist_cnt[2];
+  int64_t* hist_q[2];
+  gbdt_split* splits;
+  SlotTotals* totals[2];
+  gbdt_level* level[2];
+  uint8_t* build[2];
+  int32_t* pair_parent;
+  Route* route;
+  gbdt_node* trees;
+  int32_t* n_nodes;
+  LevelStats* stats;
+  unsigned long long* maxabs;
+  int32_t* fixed_exp;
+  double* init;
+  double* label_partials;
+  int32_t* err;
+  int32_t* nonfinite;
+};
+
+int32_t max_nodes_of(int D) { return (1 << (D + 1)) - 1; }
+
+TrainWs carve_train(void* ws, size_t bytes, int64_t N, int32_t F, const gbdt_params& p, size_t* need) {
+  Carve c(ws, bytes);
+  TrainWs w{};
+  const int D = p.max_depth;
+  const int64_t hist_slots = D >= 1 ? (int64_t(1) << (D - 1)) : 1;
+  const int level_slots = 1 << D;
+  const int64_t hist_entries = hist_slots * F * kBins;
+  const int T = p.n_trees > 0 ? p.n_trees : 1;
+  w.g = c.take<double>(N);
+  w.node = c.take<uint16_t>((N + 15) / 16 * 16);
+  for (int i = 0; i < 2; ++i) {
+    w.hist_cnt[i] = c.take<uint32_t>(hist_entries);
+    w.hist_q[i] = c.take<int64_t>(hist_entries);
+  }
+  w.splits = c.take<gbdt_split>(level_slots);
+  for (int i = 0; i < 2; ++i) {
+    w.totals[i] = c.take<SlotTotals>(level_slots);
+    w.level[i] = c.take<gbdt_level>(1);
+    w.build[i] = c.take<uint8_t>(level_slots);
+  }
+  w.pair_parent = c.take<int32_t>(level_slots / 2 + 1);
+  w.route = c.take<Route>(level_slots);
+  w.trees = c.take<gbdt_node>(static_cast<size_t>(T) * max_nodes_of(D));
+  w.n_nodes = c.take<int32_t>(T);
+  w.stats = c.take<LevelStats>(static_cast<size_t>(T) * (D + 1));
+  w.maxabs = c.take<unsigned long long>(1);
+  w.fixed_exp = c.take<int32_t>(1);
+  w.init = c.take<double>(1);
+  w.label_partials = c.take<double>(kSumBlocks);
+  w.err = c.take<int32_t>(1);
+  w.nonfinite = c.take<int32_t>(1);
+  *need = c.used;
+  return w;
+}
+
+// Timing events of the histogram launches, reused across calls.
+struct EventPool {
+  std::vector<cudaEvent_t> ev;
+  cudaError_t ensure(size_t n) {
+    while (ev.size() < n) {
+      cudaEvent_t e;
+      cudaError_t r = cudaEventCreate(&e);
+      if (r != cudaSuccess) return r;
+      ev.push_back(e);
+    }
+    return cudaSuccess;
+  }
+};
+EventPool& event_pool() {
+  static EventPool pool;
+  return pool;
+}
+
+}  // namespace
+
+}  // namespace gbdt
+
+using namespace gbdt;
+
+int validate_params(const gbdt_params* p);
+
+extern "C" size_t gbdt_train_workspace_size(int64_t N, int32_t F, const gbdt_params* p) {
+  if (!p || N < 1 || F < 1 || p->max_depth < 0 || p->max_depth > GBDT_MAX_DEPTH) return 0;
+  size_t need = 0;
+  carve_train(nullptr, 0, N, F, *p, &need);
+  return need;
+}
+
+extern "C" void gbdt_debug_inject_failure(int32_t after_levels) { g_fail_after_levels.store(after_levels); }
+
+extern "C" int gbdt_train(const uint8_t* bins, int64_t ldb, const int32_t* n_bins, int64_t N, int32_t F,
+                          const float* label, const gbdt_params* p, double* pred_out, double* init_pred_out,
+                          gbdt_node* nodes_out, int32_t* nodes_per_tree, gbdt_diagnostics* diag, void* ws,
+                          size_t ws_bytes, void* stream) {
+  clear_error();
+  GBDT_CHECK_ARG(bins && n_bins && label && p && pred_out && init_pred_out && nodes_out && nodes_per_tree,
+                 "gbdt_train: null pointer");
+  int rc = validate_params(p);
+  if (rc != GBDT_OK) return rc;
+  for (int t = 0; t < p->n_trees; ++t) nodes_per_tree[t] = 0;
+  GBDT_CHECK_ARG(N >= 1 && N < (int64_t(1) << 31), "gbdt_train: N out of range");
+  GBDT_CHECK_ARG(F >= 1 && F <= 4096, "gbdt_train: F out of range");
+  GBDT_CHECK_ARG(ldb >= N && ldb % 16 == 0 && aligned(bins, 16), "gbdt_train: bins need ldb >= N, ldb %% 16 == 0 "
+                 "and a 16-byte aligned base");
+  size_t need = 0;
+  TrainWs w = carve_train(ws, ws_bytes, N, F, *p, &need);
+  if (!ws || ws_bytes < need || !aligned(ws, kWsAlign)) {
+    set_error("gbdt_train: workspace needs %zu bytes (got %zu)", need, ws_bytes);
+    return ws ? GBDT_ERR_WORKSPACE : GBDT_ERR_INVALID_ARG;
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int D = p->max_depth, T = p->n_trees, M = max_nodes_of(D);
+
+  // ---- input checks (one synchronisation) ----
+  std::vector<int32_t> hb(F);
+  GBDT_CUDA(cudaMemcpyAsync(hb.data(), n_bins, sizeof(int32_t) * F, cudaMemcpyDeviceToHost, s));
+  GBDT_CUDA(cudaMemsetAsync(w.err, 0, sizeof(int32_t), s));
+  GBDT_CUDA(cudaMemsetAsync(w.nonfinite, 0, sizeof(int32_t), s));
+  launch_label_sum(label, N, w.label_partials, w.nonfinite, s);
+  int32_t nonfinite = 0;
+  GBDT_CUDA(cudaMemcpyAsync(&nonfinite, w.nonfinite, sizeof(int32_t), cudaMemcpyDeviceToHost, s));
+  GBDT_CUDA(cudaStreamSynchronize(s));
+  for (int j = 0; j < F; ++j)
+    GBDT_CHECK_ARG(hb[j] >= 1 && hb[j] <= GBDT_MAX_BINS, "gbdt_train: n_bins[%d] = %d outside 1..256", j, hb[j]);
+  if (nonfinite) {
+    set_error("gbdt_train: labels contain NaN or Inf");
+    return GBDT_ERR_NONFINITE;
+  }
+
+  EventPool& pool = event_pool();
+  const bool timing = diag != nullptr;
+  if (timing) GBDT_CUDA(pool.ensure(2 + 2 * static_cast<size_t>(T) * (D > 0 ? D : 1)));
+  int64_t launches = 0;
+  size_t ev_i = 2;
+  if (timing) GBDT_CUDA(cudaEventRecord(pool.ev[0], s));
+
+  launch_label_mean(w.label_partials, N, w.init, s);
+  ++launches;
+  const int fail_after = g_fail_after_levels.load();
+  int levels_done = 0;
+  for (int t = 0; t < T; ++t) {
+    gbdt_node* tree = w.trees + static_cast<size_t>(t) * M;
+    if (t == 0) {
+      GBDT_CUDA(cudaMemsetAsync(w.maxabs, 0, sizeof(unsigned long long), s));
+      launch_start_tree0(w.init, label, N, pred_out, w.g, w.node, w.maxabs, s);
+      ++launches;
+    }
+    launch_fixed_exp(w.maxabs, N, w.fixed_exp, s);
+    reset_root_kernel<<<1, 1, 0, s>>>(w.level[0], w.build[0]);
+    launches += 2;
+    if (D == 0) {
+      GBDT_CUDA(cudaMemsetAsync(w.totals[0], 0, sizeof(SlotTotals), s));
+      root_totals_kernel<<<sm_count() * 4, 256, 0, s>>>(w.g, N, w.fixed_exp, w.totals[0]);
+      ++launches;
+    }
+    for (int d = 0; d <= D; ++d) {
+      const int cur = d & 1, nxt = cur ^ 1;
+      const int max_slots = 1 << d;
+      LevelStats* st = w.stats + static_cast<size_t>(t) * (D + 1) + d;
+      if (d < D) {
+        const int max_build = d == 0 ? 1 : max_slots / 2;
+        const HistPlan plan = plan_histograms(N, F, max_slots, max_build);
+        launch_hist_zero(w.level[cur], max_slots, w.build[cur], F, w.hist_cnt[cur], w.hist_q[cur], s);
+        if (timing) GBDT_CUDA(cudaEventRecord(pool.ev[ev_i++], s));
+        rc = launch_hist_build(plan, bins, ldb, N, F, w.g, GBDT_DTYPE_F64, w.fixed_exp, w.node, w.level[cur],
+                               max_slots, w.build[cur], w.hist_cnt[cur], w.hist_q[cur], w.err, s);
+        if (rc != GBDT_OK) return rc;
+        if (timing) GBDT_CUDA(cudaEventRecord(pool.ev[ev_i++], s));
+        launches += 2;
+        if (d > 0) {
+          launch_hist_subtract(w.hist_cnt[nxt], w.hist_q[nxt], w.pair_parent, w.build[cur], w.level[cur], max_slots,
+                               F, w.hist_cnt[cur], w.hist_q[cur], w.err, s);
+          ++launches;
+        }
+        launch_find_splits(w.hist_cnt[cur], w.hist_q[cur], w.fixed_exp, F, n_bins, w.level[cur], max_slots, *p,
+                           w.splits, w.err, s);
+        ++launches;
+      }
+      apply_level_kernel<<<1, 1024, 0, s>>>(d, D, w.level[cur], max_slots, d < D ? w.splits : nullptr, w.totals[cur],
+                                            w.build[cur], w.fixed_exp, p->reg_lambda, tree, w.n_nodes + t,
+                                            w.level[nxt], w.totals[nxt], w.pair_parent, w.build[nxt], w.route, st,
+                                            w.err);
+      ++launches;
+      if (d < D) {
+        launch_route_rows(bins, ldb, N, w.route, w.level[cur], max_slots, w.node, w.err, s);
+        ++launches;
+      }
+      GBDT_LAUNCH_CHECK();
+      ++levels_done;
+      if (fail_after >= 0 && levels_done >= fail_after) {
+        cudaStreamSynchronize(s);
+        set_error("gbdt_train: failure injected after %d levels", levels_done);
+        return GBDT_ERR_INTERNAL;
+      }
+    }
+    const bool next = t + 1 < T;
+    if (next) GBDT_CUDA(cudaMemsetAsync(w.maxabs, 0, sizeof(unsigned long long), s));
+    launch_finish_tree(tree, w.n_nodes + t, M, p->learning_rate, label, N, pred_out, w.g, w.node, w.maxabs, next,
+                       s);
+    ++launches;
+    GBDT_LAUNCH_CHECK();
+  }
+  if (T == 0) {
+    // no tree: predictions are the initial value
+    GBDT_CUDA(cudaMemsetAsync(w.maxabs, 0, sizeof(unsigned long long), s));
+    launch_start_tree0(w.init, label, N, pred_out, w.g, w.node, w.maxabs, s);
+    ++launches;
+  }
+  if (timing) GBDT_CUDA(cudaEventRecord(pool.ev[1], s));
+
+  // ---- one copy of the finished model ----
+  std::vector<gbdt_node> h_nodes(static_cast<size_t>(T) * M);
+  std::vector<int32_t> h_n(T > 0 ? T : 1);
+  std::vector<LevelStats> h_stats(static_cast<size_t>(T) * (D + 1) + 1);
+  int32_t h_err = 0;
+  double h_init = 0.0;
+  if (T > 0) {
+    GBDT_CUDA(cudaMemcpyAsync(h_nodes.data(), w.trees, sizeof(gbdt_node) * h_nodes.size(), cudaMemcpyDeviceToHost, s));
+    GBDT_CUDA(cudaMemcpyAsync(h_n.data(), w.n_nodes, sizeof(int32_t) * T, cudaMemcpyDeviceToHost, s));
+    GBDT_CUDA(cudaMemcpyAsync(h_stats.data(), w.stats, sizeof(LevelStats) * T * (D + 1), cudaMemcpyDeviceToHost, s));
+  }
+  GBDT_CUDA(cudaMemcpyAsync(&h_err, w.err, sizeof(int32_t), cudaMemcpyDeviceToHost, s));
+  GBDT_CUDA(cudaMemcpyAsync(&h_init, w.init, sizeof(double), cudaMemcpyDeviceToHost, s));
+  GBDT_CUDA(cudaStreamSynchronize(s));
+  if (h_err != 0) {
+    set_error("gbdt_train: device consistency check failed (error bits 0x%x)", h_err);
+    return GBDT_ERR_INTERNAL;
+  }
+  for (int t = 0; t < T; ++t) {
+    if (h_n[t] < 1 || h_n[t] > M) {
+      set_error("gbdt_train: tree %d has an invalid node count %d", t, h_n[t]);
+      return GBDT_ERR_INTERNAL;
+    }
+    const gbdt_node* tn = h_nodes.data() + static_cast<size_t>(t) * M;
+    for (int i = 0; i < h_n[t]; ++i) {  // "Validate all indices on creation" (s.3)
+      const gbdt_node& nd = tn[i];
+      const bool ok = nd.is_leaf ? (nd.left == -1 && nd.right == -1 && nd.feature == -1)
+                                 : (nd.left > i && nd.right == nd.left + 1 && nd.right < h_n[t] && nd.feature >= 0 &&
+                                    nd.feature < F && nd.threshold_bin >= 0 && nd.threshold_bin < GBDT_MAX_BINS);
+      if (!ok) {
+        set_error("gbdt_train: tree %d node %d failed index validation", t, i);
+        return GBDT_ERR_INTERNAL;
+      }
+    }
+  }
+  // success: publish the model
+  for (int t = 0; t < T; ++t) {
+    std::copy(h_nodes.begin() + static_cast<size_t>(t) * M, h_nodes.begin() + static_cast<size_t>(t) * M + h_n[t],
+              nodes_out + static_cast<size_t>(t) * M);
+    nodes_per_tree[t] = h_n[t];
+  }
+  *init_pred_out = h_init;
+  if (timing) {
+    gbdt_diagnostics dg{};
+    float ms = 0.f;
+    GBDT_CUDA(cudaEventElapsedTime(&ms, pool.ev[0], pool.ev[1]));
+    dg.total_ms = ms;
+    size_t e = 2;
+    const double row_bytes = static_cast<double>(F) + 8.0 + 2.0;  // bins + fp64 g + uint16 node id
+    for (int t = 0; t < T; ++t) {
+      for (int d = 0; d < D; ++d) {
+        GBDT_CUDA(cudaEventElapsedTime(&ms, pool.ev[e], pool.ev[e + 1]));
+        e += 2;
+        const LevelStats& ls = h_stats[static_cast<size_t>(t) * (D + 1) + d];
+        dg.hist_ms += ms;
+        dg.hist_launches += 1;
+        dg.hist_rows += ls.n_act;
+        dg.hist_bytes += static_cast<double>(ls.n_act) * row_bytes + static_cast<double>(ls.n_built) * F * kBins * 12.0;
+      }
+      if (h_n[t] == M) dg.trees_at_full_size += 1;
+    }
+    dg.kernel_launches = launches;
+    *diag = dg;
+  }
+  return GBDT_OK;
+}

@@ -1,0 +1,284 @@
+/*
+ * gbdt.h -- C ABI of the GB300 (sm_103a) level-wise histogram GBDT library.
+ *
+ * The library trains gradient-boosted decision trees with the squared-error
+ * objective, growing each tree level by level over uint8-binned features.
+ * Its entry points follow the ComputeBackend contract of "Module Design:
+ * Training Core" (MPSBoost spec), s.4 Backend Interface: the caller passes
+ * plain views and preallocated outputs, the core decides when to call, the
+ * backend decides how to compute; split search and partition are exposed as
+ * the "fine-grained capability interfaces" that section anticipates.
+ *
+ * Conventions for every entry point
+ *   - Return value: GBDT_OK (0) or a negative GBDT_ERR_* code; on error
+ *     gbdt_last_error() returns a message for the calling thread.
+ *   - Array arguments are DEVICE pointers owned by the caller unless the
+ *     comment says "host".  The library allocates no memory: scratch space is
+ *     the caller's workspace `ws` of `ws_bytes` bytes, sized by the matching
+ *     *_workspace_size function; too small a workspace gives
+ *     GBDT_ERR_WORKSPACE.  Workspace pointers must be 256-byte aligned.
+ *   - Work is queued asynchronously on `stream` (a cudaStream_t passed as
+ *     void*; NULL is the legacy default stream), except where a function says
+ *     it synchronises.
+ *   - Arguments are validated before any launch; an invalid argument returns
+ *     GBDT_ERR_INVALID_ARG and queues nothing.
+ *   - Binned features are column-major uint8: feature j occupies
+ *     bins[j*ldb .. j*ldb + N); ldb >= N, ldb % 16 == 0 and the base pointer
+ *     16-byte aligned, so every column is read with 16-byte vector loads.
+ *     Bytes N..ldb-1 of a column are never interpreted.
+ *   - Gradients are accumulated in histograms as exact 64-bit fixed point:
+ *     q = round-half-even(g * 2^S) with one exponent S per call sequence
+ *     (gbdt_gradient_scale), so histogram sums are independent of thread
+ *     order and sibling subtraction is exact.  H is the row count (h = 1 for
+ *     squared error), so no H array is stored.
+ *
+ * Histogram layout: hist_cnt[slot][feature][256] (uint32) and
+ * hist_q[slot][feature][256] (int64, fixed point with exponent S); G of an
+ * entry is hist_q * 2^-S.
+ */
+#ifndef GBDT_H_
+#define GBDT_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define GBDT_OK 0
+#define GBDT_ERR_INVALID_ARG (-1) /* bad pointer, size, alignment or parameter */
+#define GBDT_ERR_NONFINITE (-2)   /* NaN or Inf in features or labels */
+#define GBDT_ERR_WORKSPACE (-3)   /* workspace smaller than *_workspace_size */
+#define GBDT_ERR_CUDA (-4)        /* a CUDA runtime call failed */
+#define GBDT_ERR_INTERNAL (-5)    /* a kernel detected an inconsistency */
+
+#define GBDT_MAX_BINS 256
+#define GBDT_MAX_DEPTH 12
+
+#define GBDT_DTYPE_F32 0
+#define GBDT_DTYPE_F64 1
+
+/* Training parameters; rules of "Module Design: Training Core" s.3:
+ * min_samples_leaf >= 1, min_child_weight >= 0, reg_lambda >= 0, gamma >= 0,
+ * every floating parameter finite; here also 0 <= max_depth <= GBDT_MAX_DEPTH
+ * and n_trees >= 0. */
+typedef struct gbdt_params {
+  int32_t n_trees;
+  int32_t max_depth;        /* root at depth 0; nodes at depth max_depth are leaves */
+  double learning_rate;     /* shrinkage applied to each tree's output */
+  double reg_lambda;        /* lambda in score G^2/(H+lambda) and weight -G/(H+lambda) */
+  double gamma;             /* subtracted from every split gain */
+  int32_t min_samples_leaf; /* rows each child must hold */
+  double min_child_weight;  /* H each child must hold */
+} gbdt_params;
+
+/* One tree node, "Module Design: Training Core" s.3 Tree Model: feature,
+ * threshold bin, child indices, leaf value, gain and a leaf flag.  Trees are
+ * breadth-first: the root is node 0 and the children of a split are appended
+ * left then right in the order of their parent's index.  Rows with
+ * bin <= threshold_bin go left. */
+typedef struct gbdt_node {
+  int32_t feature;       /* -1 for a leaf */
+  int32_t threshold_bin; /* -1 for a leaf */
+  int32_t left;          /* -1 for a leaf */
+  int32_t right;         /* -1 for a leaf */
+  double leaf_value;     /* weight(G,H) = -G/(H+lambda) of the node's rows */
+  double gain;           /* gain of the split; 0 for a leaf */
+  uint8_t is_leaf;       /* 1 for a leaf */
+  uint8_t reserved[7];
+} gbdt_node; /* 40 bytes */
+
+/* Per-level descriptor (device memory).  A level's nodes are the BFS indices
+ * [node_begin, node_begin + n_slots); slot s is node node_begin + s.  A row is
+ * active at the level iff its node id lies in that range. */
+typedef struct gbdt_level {
+  int32_t node_begin;
+  int32_t n_slots;
+} gbdt_level;
+
+/* Result of the split search for one slot (device memory). */
+typedef struct gbdt_split {
+  int32_t feature;    /* -1: no valid candidate with gain > 0 (the node stays a leaf) */
+  int32_t bin;        /* threshold bin: bin <= this goes left */
+  double gain;        /* gain of the chosen candidate */
+  int64_t q_left;     /* fixed-point G of the left child */
+  int64_t q_total;    /* fixed-point G of the node */
+  uint32_t cnt_left;  /* rows (= H) of the left child */
+  uint32_t cnt_total; /* rows (= H) of the node */
+} gbdt_split; /* 40 bytes */
+
+/* A contiguous run of the row-index array that holds one node's rows. */
+typedef struct gbdt_segment {
+  int64_t start;
+  int64_t count;
+} gbdt_segment;
+
+/* Library diagnostics ("Module Design: Training Core" s.4, diagnostics()).
+ * Filled by gbdt_train when a non-NULL pointer is passed; device times are
+ * CUDA-event times on the training stream, summed over all launches of each
+ * kernel family; bytes are algorithmic bytes (what the launch must move). */
+typedef struct gbdt_diagnostics {
+  int64_t hist_launches;     /* histogram-construction launches */
+  double hist_ms;            /* their total device time */
+  double hist_bytes;         /* their algorithmic bytes */
+  int64_t hist_rows;         /* active rows scanned, summed over launches */
+  double total_ms;           /* device time of the whole training call */
+  int64_t kernel_launches;   /* kernels launched by the call */
+  int32_t trees_at_full_size; /* trees that reached 2^max_depth leaves */
+  int32_t reserved;
+} gbdt_diagnostics;
+
+/* Message of the last error on the calling thread ("" if none). */
+const char* gbdt_last_error(void);
+
+/* Library version string. */
+const char* gbdt_version(void);
+
+/* Parameter rules of "Module Design: Training Core" s.3 (see gbdt_params);
+ * GBDT_OK or GBDT_ERR_INVALID_ARG.  Host only, queues nothing. */
+int gbdt_validate_params(const gbdt_params* p);
+
+/* ---------------------------------------------------------------------------
+ * gbdt_quantize: exact quantile binning of fp32 features to uint8 bins.
+ * The pages name the "Quantized" state ("Module Design: Training Core" s.5)
+ * but not the rule; this library's rule, for feature j with v its N values
+ * sorted ascending (-0.0 read as +0.0) and U distinct values:
+ *   U <= max_bins: edges are the U-1 smallest distinct values;
+ *   U >  max_bins: e_k = v[ceil(k*N/max_bins) - 1], k = 1..max_bins-1, keeping
+ *                  the strictly increasing ones and dropping one equal to v[N-1].
+ * bin(x) = number of edges strictly below x, so x <= edges[b] means bin <= b,
+ * which is routing "x > threshold goes right" of "Gradient boosted trees (spec
+ * model)", Tree representation, with threshold edges[b].
+ *   X      [F][ldx] fp32 column-major, ldx >= N (feature j at X + j*ldx)
+ *   bins   [F][ldb] uint8 output
+ *   edges  [F][max_bins-1] fp32 output; unused entries are +INFINITY
+ *   n_bins [F] int32 output, |edges|+1 per feature
+ * 2 <= max_bins <= 256, 1 <= N < 2^31.  NaN/Inf in X: GBDT_ERR_NONFINITE and
+ * no output written.  Synchronises the stream once (the finiteness check).
+ * ------------------------------------------------------------------------- */
+size_t gbdt_quantize_workspace_size(int64_t N, int32_t F);
+int gbdt_quantize(const float* X, int64_t ldx, int64_t N, int32_t F, int32_t max_bins, uint8_t* bins,
+                  int64_t ldb, float* edges, int32_t* n_bins, void* ws, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * gbdt_compute_gradients: squared error, "Module Design: Training Core" s.2:
+ * g_i = pred_i - label_i (FP64), h_i = 1 (implicit).  Also computes the
+ * fixed-point exponent S of these g into *fixed_exp (device int32), as
+ * gbdt_gradient_scale does.
+ *   pred [N] fp64, label [N] fp32, g [N] fp64 output.
+ * ------------------------------------------------------------------------- */
+size_t gbdt_gradients_workspace_size(int64_t N);
+int gbdt_compute_gradients(const double* pred, const float* label, int64_t N, double* g, int32_t* fixed_exp,
+                           void* ws, size_t ws_bytes, void* stream);
+
+/* gbdt_gradient_scale: exponent S for gradients g [N] (g_dtype F32 or F64):
+ * S = 62 - ceil(log2 N) - E where max|g| < 2^E (S = 0 if all g are 0), so the
+ * sum of |round(g*2^S)| over any set of rows is below 2^62. */
+int gbdt_gradient_scale(const void* g, int32_t g_dtype, int64_t N, int32_t* fixed_exp, void* ws, size_t ws_bytes,
+                        void* stream);
+
+/* ---------------------------------------------------------------------------
+ * gbdt_build_histograms: per-bin count and fixed-point G of every slot of a
+ * level that has build_flag[slot] = 1, over all features, in one call
+ * ("Module Design: Training Core" s.6 step 2 and s.7: count/G/H per bin).
+ *   bins [F][ldb] uint8; g [N] of g_dtype; fixed_exp: device int32 S
+ *   node_of_row [N] uint16: BFS node id of each row
+ *   level: device gbdt_level; max_slots: host bound on level->n_slots
+ *   build_flag [max_slots] uint8 (device); max_build: host bound on the number
+ *     of flagged slots
+ *   hist_cnt/hist_q [max_slots][F][256]: the flagged slots are overwritten;
+ *     other slots are not touched.
+ * 1 <= max_slots <= 4096.
+ * ------------------------------------------------------------------------- */
+size_t gbdt_histograms_workspace_size(int64_t N, int32_t F, int32_t max_slots);
+int gbdt_build_histograms(const uint8_t* bins, int64_t ldb, int64_t N, int32_t F, const void* g, int32_t g_dtype,
+                          const int32_t* fixed_exp, const uint16_t* node_of_row, const gbdt_level* level,
+                          int32_t max_slots, const uint8_t* build_flag, int32_t max_build, uint32_t* hist_cnt,
+                          int64_t* hist_q, void* ws, size_t ws_bytes, void* stream);
+
+/* gbdt_subtract_histograms: sibling subtraction.  Slots come in sibling pairs
+ * (2p, 2p+1); for p < level->n_slots/2 the slot of the pair with
+ * build_flag = 0 receives parent - built, where the parent is slot
+ * pair_parent[p] of prev_cnt/prev_q (the previous level's histograms).  Exact
+ * (integer).  pair_parent [max_slots/2] int32 (device). */
+int gbdt_subtract_histograms(const uint32_t* prev_cnt, const int64_t* prev_q, const int32_t* pair_parent,
+                             const uint8_t* build_flag, const gbdt_level* level, int32_t max_slots, int32_t F,
+                             uint32_t* hist_cnt, int64_t* hist_q, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * gbdt_find_splits: best split of every slot of a level, "Module Design:
+ * Training Core" s.2-s.3.  For feature j and threshold b = 0..n_bins[j]-2 the
+ * left side is bins <= b (prefix over bins), the right side is node minus
+ * left.  Valid iff both sides have cnt >= min_samples_leaf,
+ * H >= min_child_weight and H > 0.  gain = 0.5*((s_L + s_R) - s_P) - gamma
+ * with s = G*G/(H+lambda), FP64, no contraction.  Best = strictly larger
+ * gain, then smaller feature, then smaller bin; a slot splits iff its best
+ * valid gain is > 0 (else out[slot].feature = -1).  Node totals are the sums
+ * over the bins of feature 0 (the same for every feature).
+ *   out [max_slots] gbdt_split (device); p: host pointer.
+ * ------------------------------------------------------------------------- */
+int gbdt_find_splits(const uint32_t* hist_cnt, const int64_t* hist_q, const int32_t* fixed_exp, int32_t F,
+                     const int32_t* n_bins, const gbdt_level* level, int32_t max_slots, const gbdt_params* p,
+                     gbdt_split* out, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * gbdt_partition: "Module Design: Training Core" s.6 step 5.  The k-th slot
+ * (in slot order) whose split has feature >= 0 gets the child slots 2k (left)
+ * and 2k+1 (right) of the next level, whose node_begin is
+ * level->node_begin + level->n_slots.  For such a slot s:
+ *   - rows r of s get node_of_row[r] = child node (left iff
+ *     bins[feature][r] <= bin);
+ *   - its segment seg_in[s] of idx_in is written to idx_out at the same
+ *     positions, left rows first, each side in input order (stable);
+ *   - seg_out[2k], seg_out[2k+1] are the children's segments.
+ * Segments of slots without a split are copied unchanged to idx_out.
+ * next_level (device) receives {node_begin + n_slots, 2*splits}.  Positions
+ * outside the level's segments are not written.
+ * ------------------------------------------------------------------------- */
+size_t gbdt_partition_workspace_size(int64_t N, int32_t max_slots);
+int gbdt_partition(const uint8_t* bins, int64_t ldb, int64_t N, int32_t F, const gbdt_split* splits,
+                   const gbdt_level* level, int32_t max_slots, const gbdt_segment* seg_in, const uint32_t* idx_in,
+                   uint16_t* node_of_row, uint32_t* idx_out, gbdt_segment* seg_out, gbdt_level* next_level,
+                   void* ws, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * gbdt_update_predictions: "Module Design: Training Core" s.6 step 7 and
+ * "Gradient boosted trees (spec model)", forward pass:
+ * pred[i] = pred[i] + (lr * leaf_value[leaf_of_row[i]]) (product rounded
+ * first).  leaf_value [n_leaf_values] fp64, leaf_of_row [N] uint16.
+ * ------------------------------------------------------------------------- */
+int gbdt_update_predictions(double* pred, const uint16_t* leaf_of_row, const double* leaf_value,
+                            int32_t n_leaf_values, int64_t N, double lr, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * gbdt_train: whole training run ("Module Design: Training Core" s.6).
+ *   bins [F][ldb] uint8, n_bins [F] int32 (1..256), label [N] fp32 (device)
+ *   p: host pointer
+ *   pred_out [N] fp64 (device): predictions after the last tree
+ *   init_pred_out: host double, the initial prediction mean(label)
+ *   nodes_out: HOST array [n_trees][2^(max_depth+1)-1] gbdt_node; tree t's
+ *     nodes are nodes_out[t*(2^(max_depth+1)-1) + i], i < nodes_per_tree[t]
+ *   nodes_per_tree: HOST [n_trees] int32
+ *   diag: optional HOST diagnostics (NULL to skip the timing events)
+ * Synchronises the stream twice: after the input checks (n_bins range, finite
+ * labels) and at the end.  On any error after parameter validation nodes_out
+ * is left untouched and nodes_per_tree[*] = 0 (no partial model, s.5 State
+ * Machine).
+ * NaN/Inf labels: GBDT_ERR_NONFINITE.  1 <= N < 2^31, 1 <= F <= 4096.
+ * ------------------------------------------------------------------------- */
+size_t gbdt_train_workspace_size(int64_t N, int32_t F, const gbdt_params* p);
+int gbdt_train(const uint8_t* bins, int64_t ldb, const int32_t* n_bins, int64_t N, int32_t F, const float* label,
+               const gbdt_params* p, double* pred_out, double* init_pred_out, gbdt_node* nodes_out,
+               int32_t* nodes_per_tree, gbdt_diagnostics* diag, void* ws, size_t ws_bytes, void* stream);
+
+/* Testing hook for "Module Design: Training Core" s.5 ("Failed must not
+ * export a model"): while after_levels >= 0, gbdt_train fails with
+ * GBDT_ERR_INTERNAL on the host after that many levels, leaving nodes_out
+ * untouched; -1 (the initial state) disables it.  Process-wide. */
+void gbdt_debug_inject_failure(int32_t after_levels);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* GBDT_H_ */

@@ -1,0 +1,86 @@
+"""The C-ABI library builds, loads and exports every entry point include/gbdt.h declares
+(no compute calls: these run without a GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "gbdt.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(gbdt_[a-z_0-9]+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import histogram_gradient_boosted_gb300 as g
+    from histogram_gradient_boosted_gb300 import build
+
+    build.build()
+    return g.lib()
+
+
+def test_header_declares_the_entry_points():
+    names = _declared()
+    for required in ("gbdt_quantize", "gbdt_compute_gradients", "gbdt_build_histograms", "gbdt_find_splits",
+                     "gbdt_partition", "gbdt_update_predictions", "gbdt_train"):
+        assert required in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in _declared():
+        assert hasattr(lib, name), f"{name} declared in gbdt.h but not exported"
+
+
+def test_binding_covers_every_declared_symbol():
+    import histogram_gradient_boosted_gb300 as g
+
+    assert sorted(g.EXPORTED_SYMBOLS) == _declared()
+
+
+def test_version_and_workspace_queries_without_gpu(lib):
+    import histogram_gradient_boosted_gb300 as g
+
+    assert b"sm_103a" in lib.gbdt_version()
+    p = g.make_params(n_trees=10, max_depth=8)
+    n = lib.gbdt_train_workspace_size(10_000_000, 100, ctypes.byref(p))
+    # g (8 B/row) + node ids (2 B/row) + two histogram buffers of 128 slots x 100 x 256 x 12 B
+    assert n >= 10_000_000 * 10 + 2 * 128 * 100 * 256 * 12
+    assert lib.gbdt_quantize_workspace_size(1000, 4) >= 2 * 4 * 1000 * 4
+    assert lib.gbdt_partition_workspace_size(1000, 8) > 0
+    bad = g.make_params(max_depth=13)
+    assert lib.gbdt_train_workspace_size(100, 1, ctypes.byref(bad)) == 0
+
+
+def test_parameter_rules_on_host(lib):
+    import histogram_gradient_boosted_gb300 as g
+
+    assert g.validate_params(n_trees=1, max_depth=3) == g.OK
+    for bad in (dict(min_samples_leaf=0), dict(min_child_weight=-1.0), dict(reg_lambda=-0.1), dict(gamma=-1.0),
+                dict(learning_rate=float("nan")), dict(reg_lambda=float("inf")), dict(max_depth=13),
+                dict(n_trees=-1)):
+        assert g.validate_params(**bad) == g.ERR_INVALID_ARG, bad
+    assert b"min_samples_leaf" in lib.gbdt_last_error() or b"finite" in lib.gbdt_last_error() or \
+        b"max_depth" in lib.gbdt_last_error()
+
+
+def test_struct_layouts_match_header():
+    import histogram_gradient_boosted_gb300 as g
+
+    assert ctypes.sizeof(g.Params) == 48
+    assert g.NODE_DTYPE.itemsize == 40 and g.SPLIT_DTYPE.itemsize == 40
+    assert g.LEVEL_DTYPE.itemsize == 8 and g.SEGMENT_DTYPE.itemsize == 16
+    assert ctypes.sizeof(g.Diagnostics) == 56
+
+
+def test_entry_points_reject_bad_arguments_before_any_launch(lib):
+    # null pointers are caught on the host, so no GPU is touched
+    assert lib.gbdt_quantize(None, 0, 0, 0, 0, None, 0, None, None, None, 0, None) == -1
+    assert lib.gbdt_train(None, 0, None, 0, 0, None, None, None, None, None, None, None, None, 0, None) == -1
+    assert lib.gbdt_build_histograms(None, 0, 0, 0, None, 0, None, None, None, 0, None, 0, None, None, None, 0,
+                                     None) == -1
+    assert b"null pointer" in lib.gbdt_last_error()

@@ -1,0 +1,127 @@
+"""End-to-end training parity (gbdt_train through the C ABI) against the oracle,
+plus determinism and the failure contract ("Module Design: Training Core"
+s.5: Failed must not export a model; s.8: repeated training is deterministic)."""
+import ctypes
+
+import numpy as np
+import pytest
+
+from tests.gpu_util import compare_training, g, needs_gpu, oracle, torch
+import synth
+
+pytestmark = [pytest.mark.gpu, needs_gpu]
+
+
+def _prepare(name, n):
+    X, y = synth.make(name, n=n)
+    B = synth.CONFIGS[name]["max_bins"]
+    bins, _, n_bins = g.quantize(torch.from_numpy(X).cuda(), B)
+    ob, _, on = oracle.quantize(X, B, n_threads=8)
+    assert np.array_equal(bins[:, : X.shape[1]].cpu().numpy(), ob)
+    return bins, n_bins, torch.from_numpy(y).cuda(), ob, on, y
+
+
+@pytest.mark.parametrize("name,n,trees", [("tiny", None, 5), ("mid", 20_011, 8), ("covtype", 30_007, 4),
+                                          ("large", 40_009, 4)])
+def test_training_matches_oracle(name, n, trees):
+    bins, n_bins, yd, ob, on, y = _prepare(name, n)
+    params = dict(synth.CONFIGS[name])
+    params["n_trees"] = trees
+    out = g.train(bins, n_bins, yd, **params)
+    rep = {}
+    compare_training(out, ob, on, y, params, rep)
+    print(name, rep)
+
+
+@pytest.mark.parametrize("extra", [dict(max_depth=0), dict(max_depth=1, reg_lambda=0.0),
+                                   dict(min_child_weight=50.0, gamma=0.2), dict(min_samples_leaf=400),
+                                   dict(max_depth=12, min_samples_leaf=1), dict(n_trees=0)])
+def test_training_parameter_corners(extra):
+    bins, n_bins, yd, ob, on, y = _prepare("tiny", 3_001)
+    params = dict(synth.CONFIGS["tiny"], n_trees=3)
+    params.update(extra)
+    out = g.train(bins, n_bins, yd, **params)
+    if params["n_trees"] == 0:
+        assert np.allclose(out["pred"].cpu().numpy(), np.float64(y).mean(), rtol=1e-12)
+        return
+    compare_training(out, ob, on, y, params)
+
+
+def test_constant_labels_give_single_leaf_trees():
+    bins, n_bins, _, ob, on, _ = _prepare("tiny", 1000)
+    y = np.full(1000, 2.5, np.float32)
+    out = g.train(bins, n_bins, torch.from_numpy(y).cuda(), **dict(synth.CONFIGS["tiny"], n_trees=2))
+    assert list(out["nodes_per_tree"]) == [1, 1]
+    assert np.all(out["nodes"][:, 0]["is_leaf"] == 1) and np.all(out["nodes"][:, 0]["leaf_value"] == 0.0)
+    assert np.all(out["pred"].cpu().numpy() == 2.5)
+
+
+def test_repeated_training_is_bit_identical():
+    bins, n_bins, yd, *_ = _prepare("covtype", 20_000)
+    params = dict(synth.CONFIGS["covtype"], n_trees=3)
+    a = g.train(bins, n_bins, yd, **params)
+    b = g.train(bins, n_bins, yd, **params)
+    assert a["nodes"].tobytes() == b["nodes"].tobytes()
+    assert torch.equal(a["pred"], b["pred"])
+
+
+def _raw_train(bins, n_bins, label, params, nodes, npt):
+    L = g.lib()
+    p = g.make_params(**params)
+    N = label.shape[0]
+    ws = torch.empty(L.gbdt_train_workspace_size(N, bins.shape[0], ctypes.byref(p)), dtype=torch.uint8,
+                     device="cuda")
+    pred = torch.empty(N, dtype=torch.float64, device="cuda")
+    init = ctypes.c_double(0)
+    return L.gbdt_train(ctypes.c_void_p(bins.data_ptr()), bins.shape[1], ctypes.c_void_p(n_bins.data_ptr()), N,
+                        bins.shape[0], ctypes.c_void_p(label.data_ptr()), ctypes.byref(p),
+                        ctypes.c_void_p(pred.data_ptr()), ctypes.byref(init), nodes.ctypes.data_as(ctypes.c_void_p),
+                        npt.ctypes.data_as(ctypes.c_void_p), None, ctypes.c_void_p(ws.data_ptr()), ws.numel(),
+                        ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+
+
+def test_failures_leave_no_partial_model():
+    bins, n_bins, yd, *_ = _prepare("tiny", 2000)
+    params = dict(synth.CONFIGS["tiny"])
+    M = (1 << (params["max_depth"] + 1)) - 1
+    sentinel = np.full((params["n_trees"], M), 0, g.NODE_DTYPE)
+    sentinel["feature"] = 777
+    # non-finite label
+    bad = yd.clone()
+    bad[1234] = float("nan")
+    nodes, npt = sentinel.copy(), np.full(params["n_trees"], 9, np.int32)
+    assert _raw_train(bins, n_bins, bad, params, nodes, npt) == g.ERR_NONFINITE
+    assert np.all(nodes["feature"] == 777) and np.all(npt == 0)
+    # failure injected on the host after 7 levels (inside tree 2)
+    g.inject_failure(7)
+    try:
+        nodes, npt = sentinel.copy(), np.full(params["n_trees"], 9, np.int32)
+        assert _raw_train(bins, n_bins, yd, params, nodes, npt) == g.ERR_INTERNAL
+        assert np.all(nodes["feature"] == 777) and np.all(npt == 0)
+        assert b"injected" in g.lib().gbdt_last_error()
+    finally:
+        g.inject_failure(-1)
+    # the library still trains normally afterwards
+    nodes, npt = sentinel.copy(), np.zeros(params["n_trees"], np.int32)
+    assert _raw_train(bins, n_bins, yd, params, nodes, npt) == g.OK and np.all(npt >= 1)
+    # n_bins out of range and invalid parameters are rejected
+    with pytest.raises(g.GbdtError) as e:
+        g.train(bins, torch.full_like(n_bins, 300), yd, **params)
+    assert e.value.code == g.ERR_INVALID_ARG
+    with pytest.raises(g.GbdtError) as e:
+        g.train(bins, n_bins, yd, **dict(params, min_samples_leaf=0))
+    assert e.value.code == g.ERR_INVALID_ARG
+    with pytest.raises(g.GbdtError) as e:
+        g.train(bins, n_bins, yd, ws=torch.empty(1024, dtype=torch.uint8, device="cuda"), **params)
+    assert e.value.code == g.ERR_WORKSPACE
+
+
+def test_diagnostics_report_histogram_work():
+    bins, n_bins, yd, *_ = _prepare("mid", 50_000)
+    params = dict(synth.CONFIGS["mid"], n_trees=3)
+    out = g.train(bins, n_bins, yd, diagnostics=True, **params)
+    d = out["diag"]
+    assert d["hist_launches"] == 3 * params["max_depth"]
+    assert d["hist_ms"] > 0 and d["total_ms"] >= d["hist_ms"]
+    assert d["hist_rows"] <= 3 * params["max_depth"] * 50_000 and d["hist_rows"] >= 3 * 50_000
+    assert d["hist_bytes"] >= d["hist_rows"] * (28 + 10)
