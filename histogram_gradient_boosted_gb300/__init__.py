@@ -33,7 +33,7 @@ EXPORTED_SYMBOLS = [
     "gbdt_gradients_workspace_size", "gbdt_compute_gradients", "gbdt_gradient_scale",
     "gbdt_histograms_workspace_size", "gbdt_build_histograms", "gbdt_subtract_histograms", "gbdt_find_splits",
     "gbdt_partition_workspace_size", "gbdt_partition", "gbdt_update_predictions", "gbdt_train_workspace_size",
-    "gbdt_train", "gbdt_debug_inject_failure",
+    "gbdt_train", "gbdt_debug_inject_failure", "gbdt_kernel_launch_count",
 ]
 
 
@@ -97,6 +97,7 @@ def lib():
         "gbdt_train_workspace_size": ([i64, i32, P], sz),
         "gbdt_train": ([P, i64, P, i64, i32, P, P, P, P, P, P, P, P, sz, P], i32),
         "gbdt_debug_inject_failure": ([i32], None),
+        "gbdt_kernel_launch_count": ([], i64),
     }
     for name, (args, res) in sig.items():
         fn = getattr(L, name)
@@ -285,6 +286,11 @@ def train(bins, n_bins, label, N: int | None = None, diagnostics: bool = False, 
     _check(rc)
     return dict(nodes=nodes[:T], nodes_per_tree=npt[:T], init_pred=init.value, pred=pred,
                 diag=diag.as_dict() if diag is not None else None)
+
+
+def kernel_launch_count() -> int:
+    """Kernels the library has launched in this process so far."""
+    return int(lib().gbdt_kernel_launch_count())
 
 
 def inject_failure(after_levels: int):

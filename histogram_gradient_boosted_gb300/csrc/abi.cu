@@ -1,4 +1,5 @@
 // Error reporting, version, parameter rules and device queries of the C ABI.
+#include <atomic>
 #include <cmath>
 #include <cstring>
 
@@ -18,6 +19,13 @@ void set_error(const char* fmt, ...) {
 }
 
 void clear_error() { t_msg[0] = '\0'; }
+
+namespace {
+std::atomic<int64_t> g_launches{0};
+}
+
+void count_launches(int n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+int64_t launch_count() { return g_launches.load(std::memory_order_relaxed); }
 
 int sm_count() {
   static int n = [] {
@@ -63,3 +71,5 @@ extern "C" int gbdt_validate_params(const gbdt_params* p) {
   gbdt::clear_error();
   return validate_params(p);
 }
+
+extern "C" int64_t gbdt_kernel_launch_count(void) { return gbdt::launch_count(); }

@@ -94,4 +94,9 @@ inline int ceil_div(int64_t a, int64_t b) { return static_cast<int>((a + b - 1) 
 // Number of SMs of the current device (cached per process; one device per process).
 int sm_count();
 
+// Process-wide count of kernels this library has launched (reported through
+// gbdt_kernel_launch_count so a caller can count launches in a timed region).
+void count_launches(int n = 1);
+int64_t launch_count();
+
 }  // namespace gbdt

@@ -155,13 +155,16 @@ int elementwise_grid(int64_t N) {
 
 void launch_label_sum(const float* label, int64_t N, double* partials, int32_t* nonfinite, cudaStream_t s) {
   label_sum_kernel<<<kSumBlocks, kSumThreads, 0, s>>>(label, N, partials, nonfinite);
+  count_launches();
 }
 void launch_label_mean(const double* partials, int64_t N, double* init, cudaStream_t s) {
   label_mean_kernel<<<1, kSumThreads, 0, s>>>(partials, N, init);
+  count_launches();
 }
 void launch_start_tree0(const double* init, const float* label, int64_t N, double* pred, double* g, uint16_t* node,
                         unsigned long long* maxabs, cudaStream_t s) {
   start_tree0_kernel<<<elementwise_grid(N), 256, 0, s>>>(init, label, N, pred, g, node, maxabs);
+  count_launches();
 }
 void launch_finish_tree(const gbdt_node* tree_nodes, const int32_t* n_nodes, int32_t max_nodes, double lr,
                         const float* label, int64_t N, double* pred, double* g, uint16_t* node,
@@ -172,19 +175,23 @@ void launch_finish_tree(const gbdt_node* tree_nodes, const int32_t* n_nodes, int
   (void)once;
   finish_tree_kernel<<<elementwise_grid(N), 256, sizeof(double) * max_nodes, s>>>(
       tree_nodes, n_nodes, max_nodes, lr, label, N, pred, g, node, maxabs, next ? 1 : 0);
+  count_launches();
 }
 void launch_gradients(const double* pred, const float* label, int64_t N, double* g, unsigned long long* maxabs,
                       cudaStream_t s) {
   gradients_kernel<<<elementwise_grid(N), 256, 0, s>>>(pred, label, N, g, maxabs);
+  count_launches();
 }
 void launch_maxabs(const void* g, int32_t dtype, int64_t N, unsigned long long* maxabs, cudaStream_t s) {
   if (dtype == GBDT_DTYPE_F32)
     maxabs_kernel<float><<<elementwise_grid(N), 256, 0, s>>>(static_cast<const float*>(g), N, maxabs);
   else
     maxabs_kernel<double><<<elementwise_grid(N), 256, 0, s>>>(static_cast<const double*>(g), N, maxabs);
+    count_launches();
 }
 void launch_fixed_exp(const unsigned long long* maxabs, int64_t N, int32_t* fixed_exp, cudaStream_t s) {
   fixed_exp_kernel<<<1, 1, 0, s>>>(maxabs, N, fixed_exp);
+  count_launches();
 }
 
 }  // namespace gbdt
@@ -242,6 +249,7 @@ extern "C" int gbdt_update_predictions(double* pred, const uint16_t* leaf_of_row
   GBDT_CHECK_ARG(isfinite(lr), "gbdt_update_predictions: learning rate must be finite");
   update_predictions_kernel<<<elementwise_grid(N), 256, 0, static_cast<cudaStream_t>(stream)>>>(
       pred, leaf_of_row, leaf_value, n_leaf_values, N, lr);
+  count_launches();
   GBDT_LAUNCH_CHECK();
   return GBDT_OK;
 }

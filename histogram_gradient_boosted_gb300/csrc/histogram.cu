@@ -310,6 +310,7 @@ void launch_hist_zero(const gbdt_level* level, int32_t max_slots, const uint8_t*
   const int64_t per_slot = static_cast<int64_t>(F) * kBins;
   dim3 grid(static_cast<unsigned>((per_slot + 1023) / 1024), static_cast<unsigned>(max_slots));
   hist_zero_kernel<<<grid, 256, 0, s>>>(level, max_slots, build_flag, F, hist_cnt, hist_q);
+  count_launches();
 }
 
 int launch_hist_build(const HistPlan& plan, const uint8_t* bins, int64_t ldb, int64_t N, int32_t F, const void* g,
@@ -326,12 +327,14 @@ int launch_hist_build(const HistPlan& plan, const uint8_t* bins, int64_t ldb, in
         bins, ldb, N, F, static_cast<const float*>(g), fixed_exp, node_of_row, level, max_slots, build_flag,
         plan.group_slots, plan.group_feats, plan.n_fgroups, plan.n_chunks, plan.rows_per_chunk, hist_cnt, hist_q,
         err);
+    count_launches();
   } else {
     GBDT_CUDA(set_smem_attr(hist_build_kernel<double>, plan.smem));
     hist_build_kernel<double><<<plan.blocks(), kHistThreads, plan.smem, s>>>(
         bins, ldb, N, F, static_cast<const double*>(g), fixed_exp, node_of_row, level, max_slots, build_flag,
         plan.group_slots, plan.group_feats, plan.n_fgroups, plan.n_chunks, plan.rows_per_chunk, hist_cnt, hist_q,
         err);
+    count_launches();
   }
   return GBDT_OK;
 }
@@ -345,6 +348,7 @@ void launch_hist_subtract(const uint32_t* prev_cnt, const int64_t* prev_q, const
   dim3 grid(static_cast<unsigned>(pairs), static_cast<unsigned>((per_slot + 1023) / 1024));
   hist_subtract_kernel<<<grid, 256, 0, s>>>(prev_cnt, prev_q, pair_parent, build_flag, level, max_slots, F, hist_cnt,
                                              hist_q, err);
+  count_launches();
 }
 
 }  // namespace gbdt

@@ -308,6 +308,7 @@ void launch_route_rows(const uint8_t* bins, int64_t ldb, int64_t N, const Route*
                       true);
   (void)once;
   route_rows_kernel<<<grid, kRouteThreads, smem, s>>>(bins, ldb, N, route, level, max_slots, node_of_row, err);
+  count_launches();
 }
 
 }  // namespace gbdt
@@ -365,14 +366,18 @@ extern "C" int gbdt_partition(const uint8_t* bins, int64_t ldb, int64_t N, int32
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   GBDT_CUDA(cudaMemsetAsync(w.err, 0, sizeof(int32_t), s));
   part_setup_kernel<<<1, 1024, 0, s>>>(splits, level, max_slots, seg_in, w.route, w.tile_start, w.st, next_level);
+  count_launches();
   const int max_tiles = ceil_div(N, kTile) + max_slots;
   part_count_kernel<<<max_tiles, kPartThreads, 0, s>>>(bins, ldb, level, max_slots, seg_in, idx_in, w.route,
                                                        w.tile_start, w.st, w.tile_left);
+  count_launches();
   part_scan_kernel<<<1, 1024, 0, s>>>(splits, level, max_slots, seg_in, w.route, w.tile_start, w.st, w.tile_left,
                                       w.tile_excl, w.seg_left, seg_out, w.err);
+  count_launches();
   part_scatter_kernel<<<max_tiles, kPartThreads, 0, s>>>(bins, ldb, level, max_slots, seg_in, idx_in, w.route,
                                                          w.tile_start, w.st, w.tile_excl, w.seg_left, node_of_row,
                                                          idx_out);
+  count_launches();
   GBDT_LAUNCH_CHECK();
   return GBDT_OK;
 }

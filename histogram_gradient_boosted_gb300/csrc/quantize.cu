@@ -288,6 +288,7 @@ extern "C" int gbdt_quantize(const float* X, int64_t ldx, int64_t N, int32_t F, 
   GBDT_CUDA(cudaMemsetAsync(w.flag, 0, sizeof(int32_t), s));
   const int gx = std::min<int64_t>(ceil_div(N, 256), sm_count() * 4);
   finite_kernel<<<dim3(gx, std::min(F, 64)), 256, 0, s>>>(X, ldx, N, F, w.flag);
+  count_launches();
   int32_t bad = 0;
   GBDT_CUDA(cudaMemcpyAsync(&bad, w.flag, sizeof(int32_t), cudaMemcpyDeviceToHost, s));
   GBDT_CUDA(cudaStreamSynchronize(s));
@@ -300,16 +301,22 @@ extern "C" int gbdt_quantize(const float* X, int64_t ldx, int64_t N, int32_t F, 
   for (int j0 = 0; j0 < F; j0 += fb) {
     const int nb = std::min(fb, F - j0);
     keys_kernel<<<dim3(gx, nb), 256, 0, s>>>(X, ldx, N, j0, w.a);
+    count_launches();
     uint32_t* src = w.a;
     uint32_t* dst = w.b;
     for (int pass = 0; pass < 4; ++pass) {
       radix_count_kernel<<<dim3(tiles, nb), kQThreads, 0, s>>>(src, N, tiles, 8 * pass, w.counts);
+      count_launches();
       radix_scan_kernel<<<nb, 1024, 0, s>>>(w.counts, tiles);
+      count_launches();
       radix_scatter_kernel<<<dim3(tiles, nb), kQThreads, 0, s>>>(src, dst, N, tiles, 8 * pass, w.counts);
+      count_launches();
       std::swap(src, dst);
     }
     edges_kernel<<<nb, 1024, 0, s>>>(src, N, j0, max_bins, edges, n_bins);
+    count_launches();
     bin_kernel<<<dim3(gx, nb), 256, 0, s>>>(X, ldx, N, j0, max_bins, edges, n_bins, bins, ldb);
+    count_launches();
     GBDT_LAUNCH_CHECK();
   }
   return GBDT_OK;

@@ -190,6 +190,7 @@ void launch_find_splits(const uint32_t* hist_cnt, const int64_t* hist_q, const i
   find_splits_kernel<<<max_slots, kSplitThreads, 0, s>>>(hist_cnt, hist_q, fixed_exp, F, n_bins, level, max_slots,
                                                           p.reg_lambda, p.gamma, p.min_samples_leaf,
                                                           p.min_child_weight, out, err);
+  count_launches();
 }
 
 }  // namespace gbdt

@@ -291,12 +291,11 @@ extern "C" int gbdt_train(const uint8_t* bins, int64_t ldb, const int32_t* n_bin
   EventPool& pool = event_pool();
   const bool timing = diag != nullptr;
   if (timing) GBDT_CUDA(pool.ensure(2 + 2 * static_cast<size_t>(T) * (D > 0 ? D : 1)));
-  int64_t launches = 0;
+  const int64_t launches0 = launch_count();
   size_t ev_i = 2;
   if (timing) GBDT_CUDA(cudaEventRecord(pool.ev[0], s));
 
   launch_label_mean(w.label_partials, N, w.init, s);
-  ++launches;
   const int fail_after = g_fail_after_levels.load();
   int levels_done = 0;
   for (int t = 0; t < T; ++t) {
@@ -304,15 +303,14 @@ extern "C" int gbdt_train(const uint8_t* bins, int64_t ldb, const int32_t* n_bin
     if (t == 0) {
       GBDT_CUDA(cudaMemsetAsync(w.maxabs, 0, sizeof(unsigned long long), s));
       launch_start_tree0(w.init, label, N, pred_out, w.g, w.node, w.maxabs, s);
-      ++launches;
     }
     launch_fixed_exp(w.maxabs, N, w.fixed_exp, s);
     reset_root_kernel<<<1, 1, 0, s>>>(w.level[0], w.build[0]);
-    launches += 2;
+    count_launches();
     if (D == 0) {
       GBDT_CUDA(cudaMemsetAsync(w.totals[0], 0, sizeof(SlotTotals), s));
       root_totals_kernel<<<sm_count() * 4, 256, 0, s>>>(w.g, N, w.fixed_exp, w.totals[0]);
-      ++launches;
+      count_launches();
     }
     for (int d = 0; d <= D; ++d) {
       const int cur = d & 1, nxt = cur ^ 1;
@@ -327,24 +325,20 @@ extern "C" int gbdt_train(const uint8_t* bins, int64_t ldb, const int32_t* n_bin
                                max_slots, w.build[cur], w.hist_cnt[cur], w.hist_q[cur], w.err, s);
         if (rc != GBDT_OK) return rc;
         if (timing) GBDT_CUDA(cudaEventRecord(pool.ev[ev_i++], s));
-        launches += 2;
         if (d > 0) {
           launch_hist_subtract(w.hist_cnt[nxt], w.hist_q[nxt], w.pair_parent, w.build[cur], w.level[cur], max_slots,
                                F, w.hist_cnt[cur], w.hist_q[cur], w.err, s);
-          ++launches;
         }
         launch_find_splits(w.hist_cnt[cur], w.hist_q[cur], w.fixed_exp, F, n_bins, w.level[cur], max_slots, *p,
                            w.splits, w.err, s);
-        ++launches;
       }
       apply_level_kernel<<<1, 1024, 0, s>>>(d, D, w.level[cur], max_slots, d < D ? w.splits : nullptr, w.totals[cur],
                                             w.build[cur], w.fixed_exp, p->reg_lambda, tree, w.n_nodes + t,
                                             w.level[nxt], w.totals[nxt], w.pair_parent, w.build[nxt], w.route, st,
                                             w.err);
-      ++launches;
+      count_launches();
       if (d < D) {
         launch_route_rows(bins, ldb, N, w.route, w.level[cur], max_slots, w.node, w.err, s);
-        ++launches;
       }
       GBDT_LAUNCH_CHECK();
       ++levels_done;
@@ -358,14 +352,12 @@ extern "C" int gbdt_train(const uint8_t* bins, int64_t ldb, const int32_t* n_bin
     if (next) GBDT_CUDA(cudaMemsetAsync(w.maxabs, 0, sizeof(unsigned long long), s));
     launch_finish_tree(tree, w.n_nodes + t, M, p->learning_rate, label, N, pred_out, w.g, w.node, w.maxabs, next,
                        s);
-    ++launches;
     GBDT_LAUNCH_CHECK();
   }
   if (T == 0) {
     // no tree: predictions are the initial value
     GBDT_CUDA(cudaMemsetAsync(w.maxabs, 0, sizeof(unsigned long long), s));
     launch_start_tree0(w.init, label, N, pred_out, w.g, w.node, w.maxabs, s);
-    ++launches;
   }
   if (timing) GBDT_CUDA(cudaEventRecord(pool.ev[1], s));
 
@@ -430,7 +422,7 @@ extern "C" int gbdt_train(const uint8_t* bins, int64_t ldb, const int32_t* n_bin
       }
       if (h_n[t] == M) dg.trees_at_full_size += 1;
     }
-    dg.kernel_launches = launches;
+    dg.kernel_launches = launch_count() - launches0;
     *diag = dg;
   }
   return GBDT_OK;

@@ -135,6 +135,10 @@ const char* gbdt_last_error(void);
 /* Library version string. */
 const char* gbdt_version(void);
 
+/* Number of kernels this library has launched in the process so far
+ * (monotonic; a caller takes differences around a region of interest). */
+int64_t gbdt_kernel_launch_count(void);
+
 /* Parameter rules of "Module Design: Training Core" s.3 (see gbdt_params);
  * GBDT_OK or GBDT_ERR_INVALID_ARG.  Host only, queues nothing. */
 int gbdt_validate_params(const gbdt_params* p);
