@@ -1,0 +1,400 @@
+#!/usr/bin/env python3
+"""Benchmark: GBDT training throughput (rows*features*trees/s) on one GB300,
+with the level-histogram kernel's HBM roofline.
+
+Default workload: the large heavy-tailed configuration (10,000,000 rows x 100
+fp32 features, 255 bins, depth 8, 200 trees, lr 0.05, lambda 1, gamma 0.1,
+min_samples_leaf 20), seeded synthetic data.  One step is one pass of the whole
+hot path over that matrix: quantile binning (gbdt_quantize) followed by a full
+training run (gbdt_train: gradients, level histograms, subtraction, split
+search, partition, leaves, prediction updates) -- features already resident
+in HBM.  Inputs (4 GB fp32 features, 1 GB bins) are larger than L2.
+
+Also reported on the same line:
+  e2e                  the same metric through the public API with host inputs:
+                       pinned host -> device copy of X and labels, quantize,
+                       train, device -> host read of the model and predictions;
+  roofline             algorithmic bytes / CUDA-event time of the histogram
+                       launches inside the timed steps, against measured HBM;
+  histogram_microbench one tree level at 50,000,000 rows x 64 pre-binned
+                       features, 256 nodes: build (smaller siblings),
+                       subtraction and split search, each timed with events;
+  cpu_baseline         the CPU oracle (test infrastructure) on a bounded sample.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+For N > 1 (torchrun), each rank trains an independent replica; value is the
+sum of the ranks' units over the slowest rank's time ("replicas only").
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "GBDT train rows·features·trees/sec on 1 GB300; histogram HBM GB/s vs peak"
+UNIT = "rows*features*trees/s"
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ------------------------------------------------------------------------------------ helpers
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    if ws <= 1:
+        return 0, 0, 1, None
+    import torch.distributed as dist
+
+    dist.init_process_group("gloo")  # host-side barrier and timing exchange only
+    return dist.get_rank(), int(os.environ.get("LOCAL_RANK", "0")), ws, dist
+
+
+def _max_over_ranks(x: float, dist):
+    if dist is None:
+        return x
+    import torch
+
+    t = torch.tensor([x], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def _barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi sampled every 200 ms while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(prefix="clocks", suffix=".csv")
+        os.close(fd)
+        try:
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.out,
+                                         stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.out.close()
+
+    def summary(self):
+        rows = []
+        if self.path and os.path.exists(self.path):
+            for line in open(self.path):
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 8:
+                    rows.append(parts)
+            os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(r[0]) for r in rows if num(r[0]) is not None]
+        mx = [num(r[1]) for r in rows if num(r[1]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[4 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows),
+                "power_w_max": max((num(r[2]) for r in rows if num(r[2]) is not None), default=None)}
+
+
+def _traffic_record(hist_src: str):
+    """ncu DRAM bytes per histogram launch, if recorded for the current kernel source."""
+    p = os.path.join(ROOT, "profiles", "histogram_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        rec = json.load(f)
+    sha = hashlib.sha256(open(hist_src, "rb").read()).hexdigest()
+    return rec if rec.get("kernel_source_sha256") == sha else None
+
+
+# ------------------------------------------------------------------------------------ reference arm
+def cpu_baseline_sample(X, y, cfg, n_rows, n_trees, threads, repeats=1):
+    """The oracle as it stands on the first n_rows rows: quantize (untimed), train (timed)."""
+    import oracle
+
+    oracle.build()
+    Xs = np.ascontiguousarray(X[:, :n_rows])
+    ys = np.ascontiguousarray(y[:n_rows])
+    bins, _, n_bins = oracle.quantize(Xs, cfg["max_bins"], n_threads=threads)
+    params = dict(cfg, n_trees=n_trees, n_threads=threads)
+    times = []
+    for _ in range(repeats):
+        t0 = time.perf_counter()
+        oracle.train(bins, n_bins, ys, want_info=False, **params)
+        times.append(time.perf_counter() - t0)
+    units = n_rows * X.shape[0] * n_trees
+    return units, times
+
+
+def run_reference(args, rank, ws, dist):
+    if rank != 0:
+        return 0
+    name = args.config
+    cfg = dict(synth.CONFIGS[name])
+    n_rows = min(cfg["n"], args.cpu_rows)
+    X, y = synth.make(name, n=n_rows)
+    threads = os.cpu_count() or 1
+    units, times = cpu_baseline_sample(X, y, cfg, n_rows, args.cpu_trees, threads, repeats=args.warmup + args.steps)
+    timed = times[args.warmup:]
+    t = sum(timed)
+    value = units * len(timed) / t
+    sample = f"{n_rows:,} rows x {X.shape[0]} features x {args.cpu_trees} trees of the '{name}' workload per step"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1e3 * t / len(timed), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": name, "rows": n_rows, "features": int(X.shape[0]), "trees": args.cpu_trees,
+                       "max_depth": cfg["max_depth"], "what": "CPU oracle (plain C, FP64, row-order)"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------------------------ our arm
+def microbench(g, torch, args, peak):
+    """One level at 50M x 64 pre-binned features, 256 nodes (128 sibling pairs)."""
+    cfg = synth.CONFIGS["micro"]
+    N, F, n_nodes = args.micro_rows, cfg["f"], cfg["n_nodes"]
+    bins_h, node_h, g_h = synth.make_micro(n=N, f=F, n_nodes=n_nodes, grouped=False)
+    bins = torch.zeros((F, g.padded_ld(N)), dtype=torch.uint8, device="cuda")
+    bins[:, :N] = torch.from_numpy(bins_h).cuda()
+    del bins_h
+    node = torch.from_numpy(node_h.view(np.int16)).cuda()
+    parent = torch.from_numpy((node_h >> 1).astype(np.uint16).view(np.int16)).cuda()
+    gd = torch.from_numpy(g_h).cuda()
+    counts = np.bincount(node_h, minlength=n_nodes)
+    left_small = counts[0::2] <= counts[1::2]
+    flags = np.empty(n_nodes, np.uint8)
+    flags[0::2], flags[1::2] = left_small, ~left_small
+    fd = torch.from_numpy(flags).cuda()
+    lvl = g._dev(np.array([(0, n_nodes)], g.LEVEL_DTYPE), g.LEVEL_DTYPE)
+    plvl = g._dev(np.array([(0, n_nodes // 2)], g.LEVEL_DTYPE), g.LEVEL_DTYPE)
+    S = g.gradient_scale(gd)
+    n_bins = torch.full((F,), 256, dtype=torch.int32, device="cuda")
+    pc, pq = g.build_histograms(bins, N, gd, S, parent, plvl, n_nodes // 2,
+                                torch.ones(n_nodes // 2, dtype=torch.uint8, device="cuda"), n_nodes // 2)
+    hc = torch.zeros((n_nodes, F, 256), dtype=torch.int32, device="cuda")
+    hq = torch.zeros((n_nodes, F, 256), dtype=torch.int64, device="cuda")
+    ws = g._workspace(g.lib().gbdt_histograms_workspace_size(N, F, n_nodes))
+    pair_parent = torch.arange(n_nodes // 2, dtype=torch.int32, device="cuda")
+    split_out = torch.empty(n_nodes * g.SPLIT_DTYPE.itemsize, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    times = {"build": [], "subtract": [], "find": []}
+    for it in range(args.warmup + args.steps):
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        ev[0].record(stream)
+        g.build_histograms(bins, N, gd, S, node, lvl, n_nodes, fd, n_nodes // 2, hc, hq, ws=ws)
+        ev[1].record(stream)
+        g.subtract_histograms(pc, pq, pair_parent, fd, lvl, n_nodes, hc, hq)
+        ev[2].record(stream)
+        g.find_splits(hc, hq, S, n_bins, lvl, n_nodes, out=split_out, reg_lambda=1.0, gamma=0.0,
+                      min_samples_leaf=1, min_child_weight=0.0)
+        ev[3].record(stream)
+        torch.cuda.synchronize()
+        if it >= args.warmup:
+            times["build"].append(ev[0].elapsed_time(ev[1]))
+            times["subtract"].append(ev[1].elapsed_time(ev[2]))
+            times["find"].append(ev[2].elapsed_time(ev[3]))
+    ms = {k: statistics.mean(v) for k, v in times.items()}
+    n_built = int(flags.sum())
+    node_bytes = 2  # uint16 node ids
+    alg = N * (F * 1 + 4 + node_bytes) + n_built * F * 256 * 12
+    gbs = alg / (ms["build"] * 1e-3) / 1e9
+    return {"workload": f"one level: {N:,} rows x {F} pre-binned uint8 features (Zipf 1.1), {n_nodes} nodes, "
+                        f"{n_built} built directly, fp32 g, uint16 node ids, rows in random node order",
+            "build_ms": ms["build"], "subtract_ms": ms["subtract"], "find_splits_ms": ms["find"],
+            "total_ms": sum(ms.values()), "build_algorithmic_bytes": alg, "build_gbs": gbs, "peak_gbs": peak,
+            "build_frac": gbs / peak, "target_frac": 0.5}
+
+
+def run_ours(args, rank, local_rank, ws, dist):
+    import torch
+
+    import histogram_gradient_boosted_gb300 as g
+    from histogram_gradient_boosted_gb300 import build as gb
+
+    torch.cuda.set_device(local_rank)
+    gb.build()
+    g.lib()
+    name = args.config
+    cfg = dict(synth.CONFIGS[name])
+    if args.trees is not None:
+        cfg["n_trees"] = args.trees
+    X, y = synth.make(name, n=args.rows)
+    F, N = X.shape
+    T = cfg["n_trees"]
+    Xd = torch.from_numpy(X).cuda()
+    yd = torch.from_numpy(y).cuda()
+    peak, peak_kind = _peaks()
+    stream = torch.cuda.current_stream()
+    train_ws = g._workspace(g.train_workspace_size(N, F, **cfg))
+    pred = torch.empty(N, dtype=torch.float64, device="cuda")
+
+    def step(diag=False):
+        bins, _, n_bins = g.quantize(Xd, cfg["max_bins"])
+        return g.train(bins, n_bins, yd, diagnostics=diag, ws=train_ws, pred=pred, **cfg)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    # ---- timed region: K steps, device time by CUDA events ----
+    diags = []
+    _barrier(dist)
+    torch.cuda.synchronize()
+    l0 = g.kernel_launch_count()
+    with ClockSampler(local_rank) as clk:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            out = step(diag=True)
+            diags.append(out["diag"])
+        e1.record(stream)
+        torch.cuda.synchronize()
+    launches = g.kernel_launch_count() - l0
+    _barrier(dist)
+    ms_total = _max_over_ranks(e0.elapsed_time(e1), dist)
+    units = N * F * T * args.steps * ws
+    value = units / (ms_total * 1e-3)
+    clocks = clk.summary()
+
+    # train-only (bins already binned), from the library's own device time of the call
+    train_ms = statistics.mean(d["total_ms"] for d in diags)
+    hist_ms = sum(d["hist_ms"] for d in diags)
+    hist_bytes = sum(d["hist_bytes"] for d in diags)
+    hist_launches = sum(d["hist_launches"] for d in diags)
+    achieved = hist_bytes / (hist_ms * 1e-3) / 1e9
+    trec = _traffic_record(os.path.join(ROOT, "histogram_gradient_boosted_gb300", "csrc", "histogram.cu"))
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                "traffic": (trec["dram_bytes_per_launch"] if trec else None),
+                "kernel": "hist_build_kernel (level histograms inside gbdt_train)",
+                "launches": hist_launches, "avg_launch_ms": hist_ms / hist_launches,
+                "algorithmic_bytes_per_launch": hist_bytes / hist_launches, "peak_kind": peak_kind,
+                "share_of_step": hist_ms / (ms_total / 1.0) if ms_total else None}
+
+    # ---- e2e: public API with host inputs ----
+    Xp = torch.empty((F, N), dtype=torch.float32, pin_memory=True)
+    Xp.copy_(torch.from_numpy(X))
+    yp = torch.empty(N, dtype=torch.float32, pin_memory=True)
+    yp.copy_(torch.from_numpy(y))
+    pred_h = torch.empty(N, dtype=torch.float64, pin_memory=True)
+    e2e_steps = max(1, min(args.steps, 2))
+    _barrier(dist)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        Xd.copy_(Xp, non_blocking=True)
+        yd.copy_(yp, non_blocking=True)
+        out = step()
+        pred_h.copy_(out["pred"], non_blocking=True)
+        torch.cuda.synchronize()
+    e2e_s = _max_over_ranks(time.perf_counter() - t0, dist)
+    M = (1 << (cfg["max_depth"] + 1)) - 1
+    h2d = Xp.numel() * 4 + yp.numel() * 4
+    d2h = T * M * 40 + T * 4 + N * 8
+    e2e = {"value": N * F * T * e2e_steps * ws / e2e_s, "unit": UNIT, "h2d_bytes_per_step": h2d,
+           "d2h_bytes_per_step": d2h, "ms_per_step": 1e3 * e2e_s / e2e_steps}
+
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms_total / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "int64 fixed-point histograms, f64 gradients/gains", "data": "synthetic (seeded numpy)",
+            "config": {"workload": f"{name}: {N:,} rows x {F} features, {cfg['max_bins']} bins, depth "
+                                   f"{cfg['max_depth']}, {T} trees", "rows": N, "features": F, "trees": T,
+                       "max_depth": cfg["max_depth"], "step": "gbdt_quantize + gbdt_train (all hot-path steps)",
+                       "l2": "inputs larger than L2 (4 GB fp32 features, 1 GB bins)",
+                       "parallelism": "replicas" if ws > 1 else "single GPU"},
+            "e2e": e2e, "gpu_launches": launches, "gpu_launches_per_step": launches / args.steps,
+            "roofline": roofline, "clocks": clocks,
+            "train_only": {"ms_per_run": train_ms, "value": N * F * T / (train_ms * 1e-3)},
+            "trees_at_full_size": diags[-1]["trees_at_full_size"]}
+    if rank == 0 and not args.no_micro:
+        line["histogram_microbench"] = microbench(g, torch, args, peak)
+    if rank == 0 and not args.no_cpu:
+        threads = os.cpu_count() or 1
+        n_rows = min(N, args.cpu_rows)
+        units_c, times_c = cpu_baseline_sample(X, y, cfg, n_rows, args.cpu_trees, threads)
+        line["cpu_baseline"] = {"value": units_c / times_c[0], "unit": UNIT, "cores": threads, "kind": "oracle",
+                                "sample": f"first {n_rows:,} rows x {F} features x {args.cpu_trees} trees of the "
+                                          f"same matrix (oracle quantize untimed)", "seconds": times_c[0]}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default="large", choices=["tiny", "mid", "covtype", "large"])
+    ap.add_argument("--rows", type=int, default=None, help="override the workload's row count")
+    ap.add_argument("--trees", type=int, default=None, help="override the workload's tree count (profiling runs)")
+    ap.add_argument("--micro-rows", type=int, default=synth.CONFIGS["micro"]["n"])
+    ap.add_argument("--cpu-rows", type=int, default=1_000_000)
+    ap.add_argument("--cpu-trees", type=int, default=2)
+    ap.add_argument("--no-micro", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        print("note: fewer than 3 warm-up steps", file=sys.stderr)
+    rank, local_rank, ws, dist = _dist()
+    try:
+        if args.impl == "reference":
+            return run_reference(args, rank, ws, dist)
+        return run_ours(args, rank, local_rank, ws, dist)
+    finally:
+        if dist is not None:
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    sys.exit(main())
