@@ -33,7 +33,7 @@ EXPORTED_SYMBOLS = [
     "gbdt_gradients_workspace_size", "gbdt_compute_gradients", "gbdt_gradient_scale",
     "gbdt_histograms_workspace_size", "gbdt_build_histograms", "gbdt_subtract_histograms", "gbdt_find_splits",
     "gbdt_partition_workspace_size", "gbdt_partition", "gbdt_update_predictions", "gbdt_train_workspace_size",
-    "gbdt_train", "gbdt_debug_inject_failure", "gbdt_kernel_launch_count",
+    "gbdt_train", "gbdt_debug_inject_failure", "gbdt_kernel_launch_count", "gbdt_partition_noalloc",
 ]
 
 
@@ -98,6 +98,7 @@ def lib():
         "gbdt_train": ([P, i64, P, i64, i32, P, P, P, P, P, P, P, P, sz, P], i32),
         "gbdt_debug_inject_failure": ([i32], None),
         "gbdt_kernel_launch_count": ([], i64),
+        "gbdt_partition_noalloc": ([P, i64, i64, i32, P, P, i32, P, P, P, P, P, P, P], i32),
     }
     for name, (args, res) in sig.items():
         fn = getattr(L, name)
@@ -249,6 +250,20 @@ def partition(bins, N, splits, level, max_slots, seg_in, idx_in, node_of_row, id
     _check(lib().gbdt_partition(_ptr(bins), ldb, N, F, _ptr(splits), _ptr(level), max_slots, _ptr(seg_in),
                                 _ptr(idx_in), _ptr(node_of_row), _ptr(idx_out), _ptr(seg_out), _ptr(next_level),
                                 _ptr(ws), ws.numel(), _stream()))
+    return idx_out, seg_out, next_level
+
+
+def partition_noalloc(bins, N, splits, level, max_slots, seg_in, idx_in, node_of_row, idx_out=None):
+    """gbdt_partition with the library's built-in scratch instead of a workspace."""
+    torch = _torch()
+    F, ldb = bins.shape
+    if idx_out is None:
+        idx_out = torch.zeros_like(idx_in)
+    seg_out = torch.zeros(2 * max_slots * SEGMENT_DTYPE.itemsize, dtype=torch.uint8, device="cuda")
+    next_level = torch.zeros(LEVEL_DTYPE.itemsize, dtype=torch.uint8, device="cuda")
+    _check(lib().gbdt_partition_noalloc(_ptr(bins), ldb, N, F, _ptr(splits), _ptr(level), max_slots, _ptr(seg_in),
+                                        _ptr(idx_in), _ptr(node_of_row), _ptr(idx_out), _ptr(seg_out),
+                                        _ptr(next_level), _stream()))
     return idx_out, seg_out, next_level
 
 

@@ -8,6 +8,8 @@
 //  * gbdt_partition: additionally the stable partition of each node's segment
 //    of a row-index array (left rows first, input order kept on both sides),
 //    built as a tile count, a per-segment scan and a block-scan scatter.
+#include <mutex>
+
 #include "kernels.cuh"
 
 namespace gbdt {
@@ -364,6 +366,86 @@ extern "C" int gbdt_partition(const uint8_t* bins, int64_t ldb, int64_t N, int32
     return ws ? GBDT_ERR_WORKSPACE : GBDT_ERR_INVALID_ARG;
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  GBDT_CUDA(cudaMemsetAsync(w.err, 0, sizeof(int32_t), s));
+  part_setup_kernel<<<1, 1024, 0, s>>>(splits, level, max_slots, seg_in, w.route, w.tile_start, w.st, next_level);
+  count_launches();
+  const int max_tiles = ceil_div(N, kTile) + max_slots;
+  part_count_kernel<<<max_tiles, kPartThreads, 0, s>>>(bins, ldb, level, max_slots, seg_in, idx_in, w.route,
+                                                       w.tile_start, w.st, w.tile_left);
+  count_launches();
+  part_scan_kernel<<<1, 1024, 0, s>>>(splits, level, max_slots, seg_in, w.route, w.tile_start, w.st, w.tile_left,
+                                      w.tile_excl, w.seg_left, seg_out, w.err);
+  count_launches();
+  part_scatter_kernel<<<max_tiles, kPartThreads, 0, s>>>(bins, ldb, level, max_slots, seg_in, idx_in, w.route,
+                                                         w.tile_start, w.st, w.tile_excl, w.seg_left, node_of_row,
+                                                         idx_out);
+  count_launches();
+  GBDT_LAUNCH_CHECK();
+  return GBDT_OK;
+}
+
+// ---- gbdt_partition_noalloc: the same partition with library-owned scratch -------------------
+// For callers that cannot allocate device memory: the scratch lives in one
+// file-scope device array, sized for at most kNoAllocMaxRows rows and
+// kNoAllocMaxSlots slots.  Every call on a device shares that array.
+namespace {
+
+constexpr int64_t kNoAllocMaxRows = int64_t(1) << 24;  // 16,777,216 rows
+constexpr int32_t kNoAllocMaxSlots = 1024;
+constexpr size_t kNoAllocScratchBytes = 128 * 1024;  // >= the carve for the limits above (about 90 KB)
+constexpr int kNoAllocMaxDevices = 64;
+
+static __device__ __align__(256) unsigned char g_partition_scratch[kNoAllocScratchBytes];
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[kNoAllocMaxDevices] = {};
+
+// Device address of the scratch array on the current device, looked up once per device.
+int noalloc_scratch(void** out) {
+  int dev = -1;
+  GBDT_CUDA(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= kNoAllocMaxDevices) {
+    set_error("gbdt_partition_noalloc: device %d outside the supported range", dev);
+    return GBDT_ERR_INVALID_ARG;
+  }
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    GBDT_CUDA(cudaGetSymbolAddress(&p, g_partition_scratch));
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return GBDT_OK;
+}
+
+}  // namespace
+
+extern "C" int gbdt_partition_noalloc(const uint8_t* bins, int64_t ldb, int64_t N, int32_t F,
+                                      const gbdt_split* splits, const gbdt_level* level, int32_t max_slots,
+                                      const gbdt_segment* seg_in, const uint32_t* idx_in, uint16_t* node_of_row,
+                                      uint32_t* idx_out, gbdt_segment* seg_out, gbdt_level* next_level,
+                                      void* stream) {
+  clear_error();
+  GBDT_CHECK_ARG(bins && splits && level && seg_in && idx_in && node_of_row && idx_out && seg_out && next_level,
+                 "gbdt_partition_noalloc: null pointer");
+  GBDT_CHECK_ARG(N >= 1 && F >= 1 && ldb >= N, "gbdt_partition_noalloc: sizes out of range");
+  GBDT_CHECK_ARG(N <= kNoAllocMaxRows, "gbdt_partition_noalloc: N = %lld exceeds the limit of %lld rows of its "
+                 "built-in scratch; use gbdt_partition with a workspace", (long long)N, (long long)kNoAllocMaxRows);
+  GBDT_CHECK_ARG(max_slots >= 1 && max_slots <= kNoAllocMaxSlots, "gbdt_partition_noalloc: max_slots = %d outside "
+                 "1..%d supported by its built-in scratch", max_slots, kNoAllocMaxSlots);
+  GBDT_CHECK_ARG(idx_in != idx_out, "gbdt_partition_noalloc: idx_in and idx_out must differ");
+  size_t need = 0;
+  carve_partition(nullptr, 0, N, max_slots, &need);
+  if (need > kNoAllocScratchBytes) {
+    set_error("gbdt_partition_noalloc: needs %zu bytes of scratch, has %zu", need, kNoAllocScratchBytes);
+    return GBDT_ERR_INVALID_ARG;
+  }
+  void* scratch = nullptr;
+  int rc = noalloc_scratch(&scratch);
+  if (rc != GBDT_OK) return rc;
+  PartWs w = carve_partition(scratch, kNoAllocScratchBytes, N, max_slots, &need);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // the error word is the only scratch that must start at zero; the rest is rewritten by each call
   GBDT_CUDA(cudaMemsetAsync(w.err, 0, sizeof(int32_t), s));
   part_setup_kernel<<<1, 1024, 0, s>>>(splits, level, max_slots, seg_in, w.route, w.tile_start, w.st, next_level);
   count_launches();

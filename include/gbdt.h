@@ -246,6 +246,27 @@ int gbdt_partition(const uint8_t* bins, int64_t ldb, int64_t N, int32_t F, const
                    uint16_t* node_of_row, uint32_t* idx_out, gbdt_segment* seg_out, gbdt_level* next_level,
                    void* ws, size_t ws_bytes, void* stream);
 
+/* gbdt_partition_noalloc: gbdt_partition without a workspace argument.  The
+ * pages have no counterpart; this entry point exists for callers that cannot
+ * allocate device memory at the point where they partition -- code that runs
+ * inside another framework's fixed memory pool, a plugin that has no access
+ * to the host application's allocator, or a latency-critical loop where a
+ * cudaMalloc (which can synchronise the device) is not allowed.  It calls no
+ * allocator: its scratch is a 128 KiB array in the library's device memory,
+ * which every GPU that loads the library holds until the process exits.
+ * Limits of that scratch: N <= 16,777,216 rows and max_slots <= 1024; larger
+ * sizes return GBDT_ERR_INVALID_ARG with a message naming the limit.
+ * The first call on each device looks the array's device address up (with
+ * that device current); make that first call before any stream capture.
+ * All calls on a device share the one array, and it keeps the previous
+ * call's contents: each call clears what must start at zero, but calls that
+ * overlap on the GPU (different streams, or host threads) race on it and must
+ * be serialised by the caller.  Arguments and results are as gbdt_partition. */
+int gbdt_partition_noalloc(const uint8_t* bins, int64_t ldb, int64_t N, int32_t F, const gbdt_split* splits,
+                           const gbdt_level* level, int32_t max_slots, const gbdt_segment* seg_in,
+                           const uint32_t* idx_in, uint16_t* node_of_row, uint32_t* idx_out,
+                           gbdt_segment* seg_out, gbdt_level* next_level, void* stream);
+
 /* ---------------------------------------------------------------------------
  * gbdt_update_predictions: "Module Design: Training Core" s.6 step 7 and
  * "Gradient boosted trees (spec model)", forward pass:
