@@ -32,8 +32,11 @@ EXPORTED_SYMBOLS = [
     "gbdt_last_error", "gbdt_version", "gbdt_validate_params", "gbdt_quantize_workspace_size", "gbdt_quantize",
     "gbdt_gradients_workspace_size", "gbdt_compute_gradients", "gbdt_gradient_scale",
     "gbdt_histograms_workspace_size", "gbdt_build_histograms", "gbdt_subtract_histograms", "gbdt_find_splits",
+    "gbdt_find_splits_workspace_size",
     "gbdt_partition_workspace_size", "gbdt_partition", "gbdt_update_predictions", "gbdt_train_workspace_size",
     "gbdt_train", "gbdt_debug_inject_failure", "gbdt_kernel_launch_count", "gbdt_partition_noalloc",
+    "gbdt_histograms_segmented_workspace_size", "gbdt_build_histograms_segmented", "gbdt_partition_rows_workspace_size",
+    "gbdt_partition_rows",
 ]
 
 
@@ -51,7 +54,8 @@ class Params(ctypes.Structure):
 
 class Diagnostics(ctypes.Structure):
     _fields_ = [("hist_launches", ctypes.c_int64), ("hist_ms", ctypes.c_double), ("hist_bytes", ctypes.c_double),
-                ("hist_rows", ctypes.c_int64), ("total_ms", ctypes.c_double), ("kernel_launches", ctypes.c_int64),
+                ("hist_rows", ctypes.c_int64), ("part_ms", ctypes.c_double), ("part_bytes", ctypes.c_double),
+                ("total_ms", ctypes.c_double), ("kernel_launches", ctypes.c_int64),
                 ("trees_at_full_size", ctypes.c_int32), ("reserved", ctypes.c_int32)]
 
     def as_dict(self):
@@ -90,7 +94,8 @@ def lib():
         "gbdt_histograms_workspace_size": ([i64, i32, i32], sz),
         "gbdt_build_histograms": ([P, i64, i64, i32, P, i32, P, P, P, i32, P, i32, P, P, P, sz, P], i32),
         "gbdt_subtract_histograms": ([P, P, P, P, P, i32, i32, P, P, P], i32),
-        "gbdt_find_splits": ([P, P, P, i32, P, P, i32, P, P, P], i32),
+        "gbdt_find_splits_workspace_size": ([i32, i32], sz),
+        "gbdt_find_splits": ([P, P, P, i32, P, P, i32, P, P, P, sz, P], i32),
         "gbdt_partition_workspace_size": ([i64, i32], sz),
         "gbdt_partition": ([P, i64, i64, i32, P, P, i32, P, P, P, P, P, P, P, sz, P], i32),
         "gbdt_update_predictions": ([P, P, P, i32, i64, dbl, P], i32),
@@ -99,6 +104,10 @@ def lib():
         "gbdt_debug_inject_failure": ([i32], None),
         "gbdt_kernel_launch_count": ([], i64),
         "gbdt_partition_noalloc": ([P, i64, i64, i32, P, P, i32, P, P, P, P, P, P, P], i32),
+        "gbdt_histograms_segmented_workspace_size": ([i32], sz),
+        "gbdt_build_histograms_segmented": ([P, i64, i64, i32, P, i32, P, P, i32, P, i32, P, P, P, P, sz, P], i32),
+        "gbdt_partition_rows_workspace_size": ([i64, i32], sz),
+        "gbdt_partition_rows": ([P, P, i64, i64, i32, P, P, i32, P, P, P, P, P, i32, P, P, P, P, P, sz, P], i32),
     }
     for name, (args, res) in sig.items():
         fn = getattr(L, name)
@@ -221,6 +230,43 @@ def build_histograms(bins, N, g, fixed_exp, node_of_row, level, max_slots, build
     return hist_cnt, hist_q
 
 
+def build_histograms_segmented(bins, N, g, fixed_exp, level, max_slots, build_flag, max_build, segments,
+                               hist_cnt=None, hist_q=None, ws=None):
+    """Histograms of flagged slots whose rows are contiguous segments (SEGMENT_DTYPE bytes, device)."""
+    torch = _torch()
+    F, ldb = bins.shape
+    if hist_cnt is None:
+        hist_cnt = torch.zeros((max_slots, F, 256), dtype=torch.int32, device="cuda")
+        hist_q = torch.zeros((max_slots, F, 256), dtype=torch.int64, device="cuda")
+    if ws is None:
+        ws = _workspace(lib().gbdt_histograms_segmented_workspace_size(max_slots))
+    dt = DTYPE_F32 if g.dtype == torch.float32 else DTYPE_F64
+    _check(lib().gbdt_build_histograms_segmented(_ptr(bins), ldb, N, F, _ptr(g), dt, _ptr(fixed_exp), _ptr(level),
+                                                 max_slots, _ptr(build_flag), max_build, _ptr(segments),
+                                                 _ptr(hist_cnt), _ptr(hist_q), _ptr(ws), ws.numel(), _stream()))
+    return hist_cnt, hist_q
+
+
+def partition_rows(bins_in, N, g_in, orig_in, splits, level, max_slots, seg_in, go_right=None, leaf_of_row=None,
+                   out=None, ws=None):
+    """Stable partition of the per-position data.  Returns (bins_out, g_out, orig_out, seg_out, next_level)."""
+    torch = _torch()
+    F, ldb = bins_in.shape
+    if out is None:
+        out = (torch.empty_like(bins_in), torch.empty_like(g_in), torch.empty_like(orig_in))
+    bins_out, g_out, orig_out = out
+    seg_out = torch.zeros(2 * max_slots * SEGMENT_DTYPE.itemsize, dtype=torch.uint8, device="cuda")
+    next_level = torch.zeros(LEVEL_DTYPE.itemsize, dtype=torch.uint8, device="cuda")
+    if ws is None:
+        ws = _workspace(lib().gbdt_partition_rows_workspace_size(N, max_slots))
+    dt = DTYPE_F32 if g_in.dtype == torch.float32 else DTYPE_F64
+    _check(lib().gbdt_partition_rows(_ptr(bins_in), _ptr(bins_out), ldb, N, F, _ptr(g_in), _ptr(g_out), dt,
+                                     _ptr(orig_in), _ptr(orig_out), _ptr(go_right), _ptr(splits), _ptr(level),
+                                     max_slots, _ptr(seg_in), _ptr(seg_out), _ptr(next_level), _ptr(leaf_of_row),
+                                     _ptr(ws), ws.numel(), _stream()))
+    return bins_out, g_out, orig_out, seg_out, next_level
+
+
 def subtract_histograms(prev_cnt, prev_q, pair_parent, build_flag, level, max_slots, hist_cnt, hist_q):
     F = hist_cnt.shape[1]
     _check(lib().gbdt_subtract_histograms(_ptr(prev_cnt), _ptr(prev_q), _ptr(pair_parent), _ptr(build_flag),
@@ -234,8 +280,9 @@ def find_splits(hist_cnt, hist_q, fixed_exp, n_bins, level, max_slots, out=None,
     p = make_params(**params)
     if out is None:
         out = torch.empty(max_slots * SPLIT_DTYPE.itemsize, dtype=torch.uint8, device="cuda")
+    ws = _workspace(lib().gbdt_find_splits_workspace_size(F, max_slots))
     _check(lib().gbdt_find_splits(_ptr(hist_cnt), _ptr(hist_q), _ptr(fixed_exp), F, _ptr(n_bins), _ptr(level),
-                                  max_slots, ctypes.byref(p), _ptr(out), _stream()))
+                                  max_slots, ctypes.byref(p), _ptr(out), _ptr(ws), ws.numel(), _stream()))
     return out
 
 

@@ -46,9 +46,10 @@ void launch_hist_subtract(const uint32_t* prev_cnt, const int64_t* prev_q, const
                           uint32_t* hist_cnt, int64_t* hist_q, int32_t* err, cudaStream_t s);
 
 // ---- split.cu -------------------------------------------------------------------------
+size_t find_splits_scratch_bytes(int32_t F, int32_t max_slots);
 void launch_find_splits(const uint32_t* hist_cnt, const int64_t* hist_q, const int32_t* fixed_exp, int32_t F,
                         const int32_t* n_bins, const gbdt_level* level, int32_t max_slots, const gbdt_params& p,
-                        gbdt_split* out, int32_t* err, cudaStream_t s);
+                        gbdt_split* out, void* scratch, int32_t* err, cudaStream_t s);
 
 // ---- partition.cu ---------------------------------------------------------------------
 // Routing entry of a slot: split feature (-1: none), threshold bin, left child node id.
@@ -58,6 +59,29 @@ struct Route {
   int32_t left_node;
   int32_t pad;
 };
+// ---- segments.cu ----------------------------------------------------------------------
+// Histograms of the flagged slots of a level whose rows are contiguous segments.
+struct SegHistPlan {
+  int n_fgroups, group_feats;
+  int64_t chunk_rows;  // positions per CTA
+  int max_chunks;      // host bound on chunks over all flagged slots
+  size_t smem;
+};
+SegHistPlan plan_seg_histograms(int64_t N, int32_t F, int32_t max_slots, int32_t max_build);
+size_t seg_hist_scratch_bytes(int32_t max_slots);
+int launch_seg_histograms(const SegHistPlan& plan, const uint8_t* bins, int64_t ldb, int64_t N, int32_t F,
+                          const void* g, int32_t g_dtype, const int32_t* fixed_exp, const gbdt_level* level,
+                          int32_t max_slots, const uint8_t* build_flag, const gbdt_segment* seg, void* scratch,
+                          uint32_t* hist_cnt, int64_t* hist_q, cudaStream_t s);
+// Stable partition of the per-position data of every split slot (bins columns, g, original row
+// id) from *_in to *_out; slots without a split record leaf_of_row[orig] = their node id.
+size_t move_scratch_bytes(int64_t N, int32_t max_slots);
+void launch_move_rows(const uint8_t* bins_in, uint8_t* bins_out, int64_t ldb, int64_t N, int32_t F,
+                      const void* g_in, void* g_out, int g_size, const uint32_t* orig_in, uint32_t* orig_out,
+                      const uint8_t* go_right, const gbdt_level* level, int32_t max_slots, const gbdt_segment* seg,
+                      const Route* route, const gbdt_split* splits, gbdt_segment* seg_out,
+                      uint16_t* leaf_of_row, void* scratch, int32_t* err, cudaStream_t s);
+
 // node_of_row[r] = left_node + (bins[feature][r] > bin) for rows of slots with a split.
 void launch_route_rows(const uint8_t* bins, int64_t ldb, int64_t N, const Route* route, const gbdt_level* level,
                        int32_t max_slots, uint16_t* node_of_row, int32_t* err, cudaStream_t s);

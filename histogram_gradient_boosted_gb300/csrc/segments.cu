@@ -1,0 +1,662 @@
+// Level pass over node-contiguous rows.
+//
+// "Module Design: Training Core" s.6 steps 2 and 5: build the histograms of a
+// level's nodes, and partition the samples into the children.  Here the
+// partition moves the per-position data itself (every bin column, the
+// gradient and the original row id), stably, so that each node's rows are one
+// contiguous range of positions in every column.  Then:
+//  * the histogram of a node reads only that node's range: one node per CTA,
+//    up to 64 features per CTA in shared memory, no per-row node lookups, the
+//    gradient of a row read once per CTA and reused for all its features;
+//  * only the smaller child of each sibling pair is read (the larger comes by
+//    subtraction), so a level reads at most half of the rows.
+// The shared-memory accumulation is the exact fixed-point scheme of
+// histogram.cu: 32-bit atomics only (count, low word with carry from the
+// returned value, high word when needed), merged into global memory once.
+//
+// The partition is a tile count, a scan over tiles, and a move in which each
+// CTA ranks its tile once and then streams several columns through shared
+// memory, writing the left and right runs with aligned 16-byte stores.
+#include "kernels.cuh"
+
+namespace gbdt {
+
+namespace {
+
+// ---------------------------------------------------------------------------------------- histograms
+constexpr int kSegThreads = 1024;
+constexpr int kSegMaxFeats = 64;  // features per CTA (64 x 256 x 12 B = 192 KB of shared memory)
+
+struct SegChunks {
+  int32_t total;    // chunks over all built slots
+  int32_t n_built;  // built slots
+};
+
+// One CTA: compact list of built slots and the prefix of their chunk counts.
+__global__ void seg_chunk_setup_kernel(const gbdt_level* __restrict__ level, int32_t max_slots,
+                                       const uint8_t* __restrict__ build_flag, const gbdt_segment* __restrict__ seg,
+                                       int64_t chunk_rows, int32_t* __restrict__ build_slot,
+                                       int32_t* __restrict__ chunk_start /*[max_slots+1]*/, SegChunks* __restrict__ st) {
+  __shared__ int s_a[1024], s_b[1024];
+  __shared__ int s_pre_slots, s_pre_chunks;
+  if (threadIdx.x == 0) s_pre_slots = s_pre_chunks = 0;
+  __syncthreads();
+  const int n_slots = min(level->n_slots, max_slots);
+  for (int c0 = 0; c0 < n_slots; c0 += blockDim.x) {
+    const int s = c0 + threadIdx.x;
+    const bool in = s < n_slots && build_flag[s];
+    const int chunks = in ? static_cast<int>((seg[s].count + chunk_rows - 1) / chunk_rows) : 0;
+    s_a[threadIdx.x] = in ? 1 : 0;
+    s_b[threadIdx.x] = chunks;
+    __syncthreads();
+    for (int o = 1; o < blockDim.x; o <<= 1) {
+      const int a = threadIdx.x >= o ? s_a[threadIdx.x - o] : 0;
+      const int b = threadIdx.x >= o ? s_b[threadIdx.x - o] : 0;
+      __syncthreads();
+      s_a[threadIdx.x] += a;
+      s_b[threadIdx.x] += b;
+      __syncthreads();
+    }
+    if (in) {
+      const int k = s_pre_slots + s_a[threadIdx.x] - 1;
+      build_slot[k] = s;
+      chunk_start[k] = s_pre_chunks + s_b[threadIdx.x] - chunks;
+    }
+    __syncthreads();
+    if (threadIdx.x == blockDim.x - 1) {
+      s_pre_slots += s_a[threadIdx.x];
+      s_pre_chunks += s_b[threadIdx.x];
+    }
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    chunk_start[s_pre_slots] = s_pre_chunks;
+    st->total = s_pre_chunks;
+    st->n_built = s_pre_slots;
+  }
+}
+
+__device__ __forceinline__ void add_entry(uint32_t* s_cnt, uint32_t* s_lo, int32_t* s_hi, int e, int64_t q) {
+  atomicAdd(s_cnt + e, 1u);
+  const uint32_t ql = static_cast<uint32_t>(static_cast<uint64_t>(q));
+  int32_t qh = static_cast<int32_t>(q >> 32);
+  const uint32_t old = atomicAdd(s_lo + e, ql);
+  qh += (old + ql < old) ? 1 : 0;  // carry out of the low word
+  if (qh != 0) atomicAdd(s_hi + e, qh);
+}
+
+template <typename GT>
+__global__ void __launch_bounds__(kSegThreads, 1)
+    seg_hist_kernel(const uint8_t* __restrict__ bins, int64_t ldb, int64_t N, int32_t F, const GT* __restrict__ g,
+                    const int32_t* __restrict__ fixed_exp, const gbdt_segment* __restrict__ seg,
+                    const int32_t* __restrict__ build_slot, const int32_t* __restrict__ chunk_start,
+                    const SegChunks* __restrict__ st, int64_t chunk_rows, int32_t group_feats,
+                    uint32_t* __restrict__ hist_cnt, int64_t* __restrict__ hist_q) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  const int c = blockIdx.x;
+  if (c >= st->total) return;
+  const int n_built = st->n_built;
+  int lo = 0, hi = n_built - 1;  // last built slot whose first chunk <= c
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (chunk_start[mid] <= c) lo = mid;
+    else hi = mid - 1;
+  }
+  const int slot = build_slot[lo];
+  const int f_lo = blockIdx.y * group_feats;
+  const int nf = min(group_feats, F - f_lo);
+  if (nf <= 0) return;
+  const int entries = group_feats * kBins;
+  uint32_t* s_cnt = reinterpret_cast<uint32_t*>(smem);
+  uint32_t* s_lo = s_cnt + entries;
+  int32_t* s_hi = reinterpret_cast<int32_t*>(s_lo + entries);
+  for (int e = threadIdx.x; e < entries; e += blockDim.x) {
+    s_cnt[e] = 0;
+    s_lo[e] = 0;
+    s_hi[e] = 0;
+  }
+  __syncthreads();
+  const gbdt_segment sg = seg[slot];
+  const int64_t p0 = sg.start + static_cast<int64_t>(c - chunk_start[lo]) * chunk_rows;
+  const int64_t p1 = min(sg.start + sg.count, p0 + chunk_rows);
+  const double scale = ldexp(1.0, *fixed_exp);
+
+  // aligned 16-position blocks covering [p0, p1); positions outside are masked
+  for (int64_t b = (p0 >> 4) + threadIdx.x; (b << 4) < p1; b += blockDim.x) {
+    const int64_t r0 = b << 4;
+    uint32_t valid = 0;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) valid |= (r0 + i >= p0 && r0 + i < p1) ? (1u << i) : 0u;
+    int64_t q[16];
+    if (r0 + 16 <= N) {
+      if (sizeof(GT) == 8) {
+        const double2* gp = reinterpret_cast<const double2*>(g + r0);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const double2 v = __ldg(gp + i);
+          q[2 * i] = to_fixed(v.x, scale);
+          q[2 * i + 1] = to_fixed(v.y, scale);
+        }
+      } else {
+        const float4* gp = reinterpret_cast<const float4*>(g + r0);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float4 v = __ldg(gp + i);
+          q[4 * i] = to_fixed(v.x, scale);
+          q[4 * i + 1] = to_fixed(v.y, scale);
+          q[4 * i + 2] = to_fixed(v.z, scale);
+          q[4 * i + 3] = to_fixed(v.w, scale);
+        }
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) q[i] = (valid >> i & 1u) ? to_fixed(static_cast<double>(g[r0 + i]), scale) : 0;
+    }
+    for (int fl = 0; fl < nf; ++fl) {
+      const uint4 bv = __ldg(reinterpret_cast<const uint4*>(bins + static_cast<int64_t>(f_lo + fl) * ldb + r0));
+      const uint32_t words[4] = {bv.x, bv.y, bv.z, bv.w};
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        if (valid >> i & 1u) {
+          const int bin = (words[i >> 2] >> (8 * (i & 3))) & 0xff;
+          add_entry(s_cnt, s_lo, s_hi, (fl << 8) | bin, q[i]);
+        }
+      }
+    }
+  }
+  __syncthreads();
+  const int used = nf * kBins;
+  for (int e = threadIdx.x; e < used; e += blockDim.x) {
+    const uint32_t cn = s_cnt[e];
+    if (cn == 0) continue;
+    const int64_t v = static_cast<int64_t>(s_hi[e]) * 4294967296ll + static_cast<int64_t>(s_lo[e]);
+    const int64_t o = (static_cast<int64_t>(slot) * F + f_lo + (e >> 8)) * kBins + (e & 0xff);
+    atomicAdd(hist_cnt + o, cn);
+    atomicAdd(reinterpret_cast<unsigned long long*>(hist_q + o), static_cast<unsigned long long>(v));
+  }
+}
+
+// ---------------------------------------------------------------------------------------- partition
+constexpr int kMvThreads = 256;
+constexpr int kMvTile = 4096;  // positions per tile
+constexpr int kMvCols = 16;    // columns streamed per CTA
+
+struct MvState {
+  int32_t total_tiles;
+  int32_t pad;
+};
+
+// One CTA: tiles per slot (every slot of the level: split slots are moved,
+// the others have their rows recorded as leaves).
+__global__ void mv_setup_kernel(const gbdt_level* __restrict__ level, int32_t max_slots,
+                                const gbdt_segment* __restrict__ seg, int32_t* __restrict__ tile_start,
+                                MvState* __restrict__ st) {
+  __shared__ int s_b[1024];
+  __shared__ int s_pre;
+  if (threadIdx.x == 0) s_pre = 0;
+  __syncthreads();
+  const int n_slots = min(level->n_slots, max_slots);
+  for (int c0 = 0; c0 < n_slots; c0 += blockDim.x) {
+    const int s = c0 + threadIdx.x;
+    const int tiles = s < n_slots ? static_cast<int>((seg[s].count + kMvTile - 1) / kMvTile) : 0;
+    s_b[threadIdx.x] = tiles;
+    __syncthreads();
+    for (int o = 1; o < blockDim.x; o <<= 1) {
+      const int b = threadIdx.x >= o ? s_b[threadIdx.x - o] : 0;
+      __syncthreads();
+      s_b[threadIdx.x] += b;
+      __syncthreads();
+    }
+    if (s < n_slots) tile_start[s] = s_pre + s_b[threadIdx.x] - tiles;
+    __syncthreads();
+    if (threadIdx.x == blockDim.x - 1) s_pre += s_b[threadIdx.x];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    tile_start[n_slots] = s_pre;
+    st->total_tiles = s_pre;
+  }
+}
+
+__device__ __forceinline__ int slot_of_tile(const int32_t* __restrict__ tile_start, int n_slots, int t) {
+  int lo = 0, hi = n_slots - 1;  // last slot whose first tile <= t (skips empty slots)
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (tile_start[mid] <= t) lo = mid;
+    else hi = mid - 1;
+  }
+  return lo;
+}
+
+__device__ __forceinline__ int block_scan_excl(int v, int* s_warp, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = v;
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += t;
+  }
+  if (lane == 31) s_warp[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const int nw = blockDim.x >> 5;
+    const int w = lane < nw ? s_warp[lane] : 0;
+    int wi = w;
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, wi, o);
+      if (lane >= o) wi += t;
+    }
+    if (lane < nw) s_warp[lane] = wi - w;
+    if (lane == 31) s_warp[32] = wi;
+  }
+  __syncthreads();
+  const int r = s_warp[warp] + incl - v;
+  *total = s_warp[32];
+  __syncthreads();
+  return r;
+}
+
+// Decision of position p of a split slot: 1 = goes right.
+__device__ __forceinline__ int goes_right(const uint8_t* __restrict__ col, int bin, const uint8_t* __restrict__ go_right,
+                                          int64_t p) {
+  return go_right ? (go_right[p] != 0) : (col[p] > bin);
+}
+
+__global__ void __launch_bounds__(kMvThreads)
+    mv_count_kernel(const uint8_t* __restrict__ bins, int64_t ldb, const uint8_t* __restrict__ go_right,
+                    const gbdt_level* __restrict__ level, int32_t max_slots, const gbdt_segment* __restrict__ seg,
+                    const Route* __restrict__ route, const int32_t* __restrict__ tile_start,
+                    const MvState* __restrict__ st, int32_t* __restrict__ tile_left) {
+  const int t = blockIdx.x;
+  if (t >= st->total_tiles) return;
+  __shared__ int s_warp[33];
+  const int n_slots = min(level->n_slots, max_slots);
+  const int s = slot_of_tile(tile_start, n_slots, t);
+  const Route rt = route[s];
+  if (rt.feature < 0) {
+    if (threadIdx.x == 0) tile_left[t] = 0;
+    return;
+  }
+  const int64_t p0 = seg[s].start + static_cast<int64_t>(t - tile_start[s]) * kMvTile;
+  const int64_t p1 = min(seg[s].start + seg[s].count, p0 + kMvTile);
+  const uint8_t* col = bins + static_cast<int64_t>(rt.feature) * ldb;
+  int c = 0;
+  for (int64_t p = p0 + threadIdx.x; p < p1; p += blockDim.x) c += 1 - goes_right(col, rt.bin, go_right, p);
+  int total;
+  block_scan_excl(c, s_warp, &total);
+  if (threadIdx.x == 0) tile_left[t] = total;
+}
+
+// One CTA: exclusive scan of tile left counts over all tiles; left totals per slot.
+__global__ void __launch_bounds__(1024)
+    mv_scan_kernel(const gbdt_level* __restrict__ level, int32_t max_slots, const Route* __restrict__ route,
+                   const int32_t* __restrict__ tile_start, const MvState* __restrict__ st,
+                   const int32_t* __restrict__ tile_left, int64_t* __restrict__ tile_excl,
+                   int64_t* __restrict__ seg_left, const gbdt_segment* __restrict__ seg, gbdt_segment* __restrict__ seg_out,
+                   const gbdt_split* __restrict__ splits, int32_t* __restrict__ err) {
+  __shared__ int s_warp[33];
+  __shared__ long long s_carry;
+  const int total = st->total_tiles;
+  if (threadIdx.x == 0) s_carry = 0;
+  __syncthreads();
+  for (int c0 = 0; c0 < total; c0 += blockDim.x) {
+    const int t = c0 + threadIdx.x;
+    const int v = t < total ? tile_left[t] : 0;
+    int chunk_total;
+    const int e = block_scan_excl(v, s_warp, &chunk_total);
+    if (t < total) tile_excl[t] = s_carry + e;
+    __syncthreads();
+    if (threadIdx.x == 0) s_carry += chunk_total;
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) tile_excl[total] = s_carry;
+  __syncthreads();
+  const int n_slots = min(level->n_slots, max_slots);
+  for (int s = threadIdx.x; s < n_slots; s += blockDim.x) {
+    const Route rt = route[s];
+    if (rt.feature < 0) continue;
+    const int64_t left = tile_excl[tile_start[s + 1]] - tile_excl[tile_start[s]];
+    seg_left[s] = left;
+    if (splits && left != static_cast<int64_t>(splits[s].cnt_left)) raise_error(err, kErrPartitionCount);
+    if (seg_out) {
+      const int k = rt.pad;
+      seg_out[2 * k] = gbdt_segment{seg[s].start, left};
+      seg_out[2 * k + 1] = gbdt_segment{seg[s].start + left, seg[s].count - left};
+    }
+  }
+}
+
+// Column c < F: bins column c; c == F: gradient (8 B); c == F + 1: original row id (4 B).
+__global__ void __launch_bounds__(kMvThreads)
+    mv_move_kernel(const uint8_t* __restrict__ bins_in, uint8_t* __restrict__ bins_out, int64_t ldb, int32_t F,
+                   const void* __restrict__ g_in, void* __restrict__ g_out, int g_size, const uint32_t* __restrict__ orig_in,
+                   uint32_t* __restrict__ orig_out, const uint8_t* __restrict__ go_right,
+                   const gbdt_level* __restrict__ level, int32_t max_slots, const gbdt_segment* __restrict__ seg,
+                   const Route* __restrict__ route, const int32_t* __restrict__ tile_start,
+                   const MvState* __restrict__ st, const int64_t* __restrict__ tile_excl,
+                   const int64_t* __restrict__ seg_left, uint16_t* __restrict__ leaf_of_row) {
+  __shared__ uint16_t s_dst[kMvTile];              // tile position -> position in partitioned tile order
+  __shared__ __align__(16) uint32_t s_stage[kMvTile / 4 + 8];  // one byte column in partitioned order
+  __shared__ int s_warp[33];
+  const int t = blockIdx.x;
+  if (t >= st->total_tiles) return;
+  const int n_slots = min(level->n_slots, max_slots);
+  const int s = slot_of_tile(tile_start, n_slots, t);
+  const Route rt = route[s];
+  const int64_t tile_off = static_cast<int64_t>(t - tile_start[s]) * kMvTile;
+  const int64_t p0 = seg[s].start + tile_off;
+  const int64_t p1 = min(seg[s].start + seg[s].count, p0 + kMvTile);
+  const int n = static_cast<int>(p1 - p0);
+  if (rt.feature < 0) {  // a leaf: remember each row's leaf, nothing moves
+    if (blockIdx.y == 0 && leaf_of_row) {
+      const uint16_t node = static_cast<uint16_t>(level->node_begin + s);
+      for (int i = threadIdx.x; i < n; i += blockDim.x) leaf_of_row[orig_in[p0 + i]] = node;
+    }
+    return;
+  }
+  // rank the tile: thread t owns positions [16t, 16t+16) of the tile
+  const uint8_t* col = bins_in + static_cast<int64_t>(rt.feature) * ldb;
+  uint32_t rmask = 0;
+  int nl = 0;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const int j = threadIdx.x * 16 + i;
+    if (j < n) {
+      const int r = goes_right(col, rt.bin, go_right, p0 + j);
+      rmask |= static_cast<uint32_t>(r) << i;
+      nl += 1 - r;
+    }
+  }
+  int tile_nl;
+  const int lrank = block_scan_excl(nl, s_warp, &tile_nl);
+  {
+    int li = lrank, ri = threadIdx.x * 16 - lrank;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int j = threadIdx.x * 16 + i;
+      if (j < n) s_dst[j] = static_cast<uint16_t>((rmask >> i & 1u) ? tile_nl + ri++ : li++);
+    }
+  }
+  __syncthreads();
+  const int64_t left_before = tile_excl[t] - tile_excl[tile_start[s]];
+  const int64_t dst_l = seg[s].start + left_before;                                 // left run of this tile
+  const int64_t dst_r = seg[s].start + seg_left[s] + (tile_off - left_before);      // right run of this tile
+  const int tile_nr = n - tile_nl;
+
+  const int c_lo = blockIdx.y * kMvCols;
+  const int c_hi = min(F + 2, c_lo + kMvCols);
+  for (int c = c_lo; c < c_hi; ++c) {
+    if (c == F) {  // gradients: direct writes, lanes of a warp land in at most two runs
+      for (int j = threadIdx.x; j < n; j += blockDim.x) {
+        const int d = s_dst[j];
+        const int64_t o = d < tile_nl ? dst_l + d : dst_r + (d - tile_nl);
+        if (g_size == 8)
+          static_cast<uint64_t*>(g_out)[o] = static_cast<const uint64_t*>(g_in)[p0 + j];
+        else
+          static_cast<uint32_t*>(g_out)[o] = static_cast<const uint32_t*>(g_in)[p0 + j];
+      }
+      continue;
+    }
+    if (c == F + 1) {
+      for (int j = threadIdx.x; j < n; j += blockDim.x) {
+        const int d = s_dst[j];
+        orig_out[d < tile_nl ? dst_l + d : dst_r + (d - tile_nl)] = orig_in[p0 + j];
+      }
+      continue;
+    }
+    const uint8_t* in = bins_in + static_cast<int64_t>(c) * ldb;
+    uint8_t* out = bins_out + static_cast<int64_t>(c) * ldb;
+    uint8_t* stage = reinterpret_cast<uint8_t*>(s_stage);
+    // gather the tile into partitioned order (aligned 16-byte loads)
+    const int64_t a0 = p0 & ~int64_t(15);
+    for (int64_t b = a0 + 16 * threadIdx.x; b < p1; b += 16 * blockDim.x) {
+      const uint4 v = __ldg(reinterpret_cast<const uint4*>(in + b));
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const int64_t p = b + i;
+        if (p >= p0 && p < p1) stage[s_dst[p - p0]] = static_cast<uint8_t>(w[i >> 2] >> (8 * (i & 3)));
+      }
+    }
+    __syncthreads();
+    // write the two runs: byte stores for unaligned ends, 16-byte stores inside
+    for (int run = 0; run < 2; ++run) {
+      const int64_t dst = run == 0 ? dst_l : dst_r;
+      const int len = run == 0 ? tile_nl : tile_nr;
+      const int src0 = run == 0 ? 0 : tile_nl;
+      if (len <= 0) continue;
+      const int64_t a = (dst + 15) & ~int64_t(15);  // first aligned address
+      const int head = static_cast<int>(a - dst < len ? a - dst : static_cast<int64_t>(len));
+      const int body16 = (len - head) / 16;
+      const int tail0 = head + body16 * 16;
+      for (int i = threadIdx.x; i < head; i += blockDim.x) out[dst + i] = stage[src0 + i];
+      for (int i = tail0 + threadIdx.x; i < len; i += blockDim.x) out[dst + i] = stage[src0 + i];
+      for (int k = threadIdx.x; k < body16; k += blockDim.x) {
+        const int o = src0 + head + 16 * k;  // byte offset in the stage
+        const int wa = o >> 2, sh = 8 * (o & 3);
+        const uint32_t x0 = s_stage[wa], x1 = s_stage[wa + 1], x2 = s_stage[wa + 2], x3 = s_stage[wa + 3],
+                       x4 = s_stage[wa + 4];
+        uint4 v;
+        v.x = __funnelshift_r(x0, x1, sh);
+        v.y = __funnelshift_r(x1, x2, sh);
+        v.z = __funnelshift_r(x2, x3, sh);
+        v.w = __funnelshift_r(x3, x4, sh);
+        *reinterpret_cast<uint4*>(out + a + 16 * k) = v;
+      }
+    }
+    __syncthreads();
+  }
+}
+
+// One CTA: routing of every slot from its split record; the k-th splitting slot
+// (in slot order) gets child slots 2k, 2k+1 of the next level.
+__global__ void routes_from_splits_kernel(const gbdt_split* __restrict__ splits, const gbdt_level* __restrict__ level,
+                                          int32_t max_slots, Route* __restrict__ route,
+                                          gbdt_level* __restrict__ next_level) {
+  __shared__ int s_a[1024];
+  __shared__ int s_pre;
+  if (threadIdx.x == 0) s_pre = 0;
+  __syncthreads();
+  const int n_slots = min(level->n_slots, max_slots);
+  const int next_begin = level->node_begin + level->n_slots;
+  for (int c0 = 0; c0 < n_slots; c0 += blockDim.x) {
+    const int s = c0 + threadIdx.x;
+    const int sp = (s < n_slots && splits[s].feature >= 0) ? 1 : 0;
+    s_a[threadIdx.x] = sp;
+    __syncthreads();
+    for (int o = 1; o < blockDim.x; o <<= 1) {
+      const int a = threadIdx.x >= o ? s_a[threadIdx.x - o] : 0;
+      __syncthreads();
+      s_a[threadIdx.x] += a;
+      __syncthreads();
+    }
+    if (s < n_slots) {
+      const int k = s_pre + s_a[threadIdx.x] - sp;
+      route[s] = sp ? Route{splits[s].feature, splits[s].bin, next_begin + 2 * k, k} : Route{-1, -1, -1, k};
+    }
+    __syncthreads();
+    if (threadIdx.x == blockDim.x - 1) s_pre += s_a[threadIdx.x];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0 && next_level) {
+    next_level->node_begin = next_begin;
+    next_level->n_slots = 2 * s_pre;
+  }
+}
+
+template <typename K>
+cudaError_t smem_attr(K kernel, size_t bytes) {
+  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+}
+
+}  // namespace
+
+// ---- plans and launchers ------------------------------------------------------------------------
+SegHistPlan plan_seg_histograms(int64_t N, int32_t F, int32_t max_slots, int32_t max_build) {
+  SegHistPlan p{};
+  p.n_fgroups = ceil_div(F, kSegMaxFeats);
+  p.group_feats = ceil_div(F, p.n_fgroups);
+  const int64_t target = static_cast<int64_t>(sm_count()) * 3;
+  int64_t cr = (N * p.n_fgroups + target - 1) / target;
+  if (cr < 32768) cr = 32768;
+  p.chunk_rows = (cr + 15) / 16 * 16;
+  p.max_chunks = ceil_div(N, p.chunk_rows) + (max_build < max_slots ? max_build : max_slots);
+  p.smem = static_cast<size_t>(p.group_feats) * kBins * 12;
+  return p;
+}
+
+size_t seg_hist_scratch_bytes(int32_t max_slots) {
+  return sizeof(SegChunks) + sizeof(int32_t) * (2 * static_cast<size_t>(max_slots) + 2) + 3 * kWsAlign;
+}
+
+int launch_seg_histograms(const SegHistPlan& plan, const uint8_t* bins, int64_t ldb, int64_t N, int32_t F,
+                          const void* g, int32_t g_dtype, const int32_t* fixed_exp, const gbdt_level* level,
+                          int32_t max_slots, const uint8_t* build_flag, const gbdt_segment* seg, void* scratch,
+                          uint32_t* hist_cnt, int64_t* hist_q, cudaStream_t s) {
+  Carve c(scratch, seg_hist_scratch_bytes(max_slots));
+  SegChunks* st = c.take<SegChunks>(1);
+  int32_t* build_slot = c.take<int32_t>(max_slots + 1);
+  int32_t* chunk_start = c.take<int32_t>(max_slots + 1);
+  launch_hist_zero(level, max_slots, build_flag, F, hist_cnt, hist_q, s);
+  seg_chunk_setup_kernel<<<1, 1024, 0, s>>>(level, max_slots, build_flag, seg, plan.chunk_rows, build_slot,
+                                            chunk_start, st);
+  count_launches();
+  dim3 grid(static_cast<unsigned>(plan.max_chunks), static_cast<unsigned>(plan.n_fgroups));
+  if (g_dtype == GBDT_DTYPE_F32) {
+    GBDT_CUDA(smem_attr(seg_hist_kernel<float>, plan.smem));
+    seg_hist_kernel<float><<<grid, kSegThreads, plan.smem, s>>>(bins, ldb, N, F, static_cast<const float*>(g),
+                                                                fixed_exp, seg, build_slot, chunk_start, st,
+                                                                plan.chunk_rows, plan.group_feats, hist_cnt, hist_q);
+  } else {
+    GBDT_CUDA(smem_attr(seg_hist_kernel<double>, plan.smem));
+    seg_hist_kernel<double><<<grid, kSegThreads, plan.smem, s>>>(bins, ldb, N, F, static_cast<const double*>(g),
+                                                                 fixed_exp, seg, build_slot, chunk_start, st,
+                                                                 plan.chunk_rows, plan.group_feats, hist_cnt, hist_q);
+  }
+  count_launches();
+  return GBDT_OK;
+}
+
+size_t move_scratch_bytes(int64_t N, int32_t max_slots) {
+  const size_t tiles = static_cast<size_t>(ceil_div(N, kMvTile)) + max_slots;
+  return sizeof(MvState) + sizeof(int32_t) * (max_slots + 1) + sizeof(int32_t) * tiles +
+         sizeof(int64_t) * (tiles + 1) + sizeof(int64_t) * max_slots + 6 * kWsAlign;
+}
+
+void launch_move_rows(const uint8_t* bins_in, uint8_t* bins_out, int64_t ldb, int64_t N, int32_t F,
+                      const void* g_in, void* g_out, int g_size, const uint32_t* orig_in, uint32_t* orig_out,
+                      const uint8_t* go_right, const gbdt_level* level, int32_t max_slots, const gbdt_segment* seg,
+                      const Route* route, const gbdt_split* splits, gbdt_segment* seg_out,
+                      uint16_t* leaf_of_row, void* scratch, int32_t* err, cudaStream_t s) {
+  Carve c(scratch, move_scratch_bytes(N, max_slots));
+  MvState* st = c.take<MvState>(1);
+  int32_t* tile_start = c.take<int32_t>(max_slots + 1);
+  const int max_tiles = ceil_div(N, kMvTile) + max_slots;
+  int32_t* tile_left = c.take<int32_t>(max_tiles);
+  int64_t* tile_excl = c.take<int64_t>(max_tiles + 1);
+  int64_t* seg_left = c.take<int64_t>(max_slots);
+  mv_setup_kernel<<<1, 1024, 0, s>>>(level, max_slots, seg, tile_start, st);
+  count_launches();
+  mv_count_kernel<<<max_tiles, kMvThreads, 0, s>>>(bins_in, ldb, go_right, level, max_slots, seg, route, tile_start,
+                                                   st, tile_left);
+  count_launches();
+  mv_scan_kernel<<<1, 1024, 0, s>>>(level, max_slots, route, tile_start, st, tile_left, tile_excl, seg_left, seg,
+                                    seg_out, splits, err);
+  count_launches();
+  dim3 grid(static_cast<unsigned>(max_tiles), static_cast<unsigned>(ceil_div(F + 2, kMvCols)));
+  mv_move_kernel<<<grid, kMvThreads, 0, s>>>(bins_in, bins_out, ldb, F, g_in, g_out, g_size, orig_in, orig_out,
+                                             go_right,
+                                             level, max_slots, seg, route, tile_start, st, tile_excl, seg_left,
+                                             leaf_of_row);
+  count_launches();
+}
+
+}  // namespace gbdt
+
+using namespace gbdt;
+
+extern "C" size_t gbdt_histograms_segmented_workspace_size(int32_t max_slots) {
+  return seg_hist_scratch_bytes(max_slots);
+}
+
+extern "C" int gbdt_build_histograms_segmented(const uint8_t* bins, int64_t ldb, int64_t N, int32_t F, const void* g,
+                                               int32_t g_dtype, const int32_t* fixed_exp, const gbdt_level* level,
+                                               int32_t max_slots, const uint8_t* build_flag, int32_t max_build,
+                                               const gbdt_segment* segments, uint32_t* hist_cnt, int64_t* hist_q,
+                                               void* ws, size_t ws_bytes, void* stream) {
+  clear_error();
+  GBDT_CHECK_ARG(bins && g && fixed_exp && level && build_flag && segments && hist_cnt && hist_q,
+                 "gbdt_build_histograms_segmented: null pointer");
+  GBDT_CHECK_ARG(N >= 1 && N < (int64_t(1) << 31) && F >= 1 && F <= 4096,
+                 "gbdt_build_histograms_segmented: sizes out of range");
+  GBDT_CHECK_ARG(ldb >= N && ldb % 16 == 0 && aligned(bins, 16) && aligned(g, 16),
+                 "gbdt_build_histograms_segmented: need ldb >= N, ldb %% 16 == 0, 16-byte aligned bins and g");
+  GBDT_CHECK_ARG(g_dtype == GBDT_DTYPE_F32 || g_dtype == GBDT_DTYPE_F64, "gbdt_build_histograms_segmented: bad dtype");
+  GBDT_CHECK_ARG(max_slots >= 1 && max_slots <= kMaxSlots && max_build >= 1 && max_build <= max_slots,
+                 "gbdt_build_histograms_segmented: slot bounds out of range");
+  if (!ws || ws_bytes < seg_hist_scratch_bytes(max_slots) || !aligned(ws, kWsAlign)) {
+    set_error("gbdt_build_histograms_segmented: workspace needs %zu bytes", seg_hist_scratch_bytes(max_slots));
+    return ws ? GBDT_ERR_WORKSPACE : GBDT_ERR_INVALID_ARG;
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const SegHistPlan plan = plan_seg_histograms(N, F, max_slots, max_build);
+  int rc = launch_seg_histograms(plan, bins, ldb, N, F, g, g_dtype, fixed_exp, level, max_slots, build_flag, segments,
+                                 ws, hist_cnt, hist_q, s);
+  if (rc != GBDT_OK) return rc;
+  GBDT_LAUNCH_CHECK();
+  return GBDT_OK;
+}
+
+namespace {
+struct RowsWs {
+  int32_t* err;
+  Route* route;
+  void* move;
+};
+RowsWs carve_rows(void* ws, size_t bytes, int64_t N, int32_t max_slots, size_t* need) {
+  Carve c(ws, bytes);
+  RowsWs w{};
+  w.err = c.take<int32_t>(1);
+  w.route = c.take<Route>(max_slots);
+  w.move = c.take<unsigned char>(move_scratch_bytes(N, max_slots));
+  *need = c.used;
+  return w;
+}
+}  // namespace
+
+extern "C" size_t gbdt_partition_rows_workspace_size(int64_t N, int32_t max_slots) {
+  size_t need = 0;
+  carve_rows(nullptr, 0, N, max_slots, &need);
+  return need;
+}
+
+extern "C" int gbdt_partition_rows(const uint8_t* bins_in, uint8_t* bins_out, int64_t ldb, int64_t N, int32_t F,
+                                   const void* g_in, void* g_out, int32_t g_dtype, const uint32_t* orig_in,
+                                   uint32_t* orig_out, const uint8_t* go_right, const gbdt_split* splits,
+                                   const gbdt_level* level, int32_t max_slots, const gbdt_segment* seg_in,
+                                   gbdt_segment* seg_out, gbdt_level* next_level, uint16_t* leaf_of_row, void* ws,
+                                   size_t ws_bytes, void* stream) {
+  clear_error();
+  GBDT_CHECK_ARG(bins_in && bins_out && g_in && g_out && orig_in && orig_out && splits && level && seg_in && seg_out,
+                 "gbdt_partition_rows: null pointer");
+  GBDT_CHECK_ARG(bins_in != bins_out && g_in != g_out && orig_in != orig_out,
+                 "gbdt_partition_rows: inputs and outputs must not alias");
+  GBDT_CHECK_ARG(N >= 1 && N < (int64_t(1) << 31) && F >= 1 && F <= 4096, "gbdt_partition_rows: sizes out of range");
+  GBDT_CHECK_ARG(ldb >= N && ldb % 16 == 0 && aligned(bins_in, 16) && aligned(bins_out, 16),
+                 "gbdt_partition_rows: need ldb >= N, ldb %% 16 == 0 and 16-byte aligned bins");
+  GBDT_CHECK_ARG(g_dtype == GBDT_DTYPE_F32 || g_dtype == GBDT_DTYPE_F64, "gbdt_partition_rows: bad g dtype");
+  GBDT_CHECK_ARG(max_slots >= 1 && max_slots <= kMaxSlots, "gbdt_partition_rows: max_slots out of range");
+  size_t need = 0;
+  RowsWs w = carve_rows(ws, ws_bytes, N, max_slots, &need);
+  if (!ws || ws_bytes < need || !aligned(ws, kWsAlign)) {
+    set_error("gbdt_partition_rows: workspace needs %zu bytes", need);
+    return ws ? GBDT_ERR_WORKSPACE : GBDT_ERR_INVALID_ARG;
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  GBDT_CUDA(cudaMemsetAsync(w.err, 0, sizeof(int32_t), s));
+  routes_from_splits_kernel<<<1, 1024, 0, s>>>(splits, level, max_slots, w.route, next_level);
+  count_launches();
+  launch_move_rows(bins_in, bins_out, ldb, N, F, g_in, g_out, g_dtype == GBDT_DTYPE_F64 ? 8 : 4, orig_in, orig_out,
+                   go_right, level, max_slots, seg_in, w.route, splits, seg_out, leaf_of_row, w.move, w.err, s);
+  GBDT_LAUNCH_CHECK();
+  return GBDT_OK;
+}

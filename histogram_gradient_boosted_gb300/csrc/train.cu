@@ -26,17 +26,25 @@ struct SlotTotals {
 };
 
 struct LevelStats {
-  int64_t n_act;  // rows in the level's nodes
+  int64_t n_act;         // rows in the level's nodes
+  int64_t n_built_rows;  // rows of the nodes whose histograms are built directly
+  int64_t n_split_rows;  // rows of the nodes that split (moved by the partition)
   int32_t n_slots;
   int32_t n_built;
 };
 
 std::atomic<int32_t> g_fail_after_levels{-1};
 
-__global__ void reset_root_kernel(gbdt_level* level, uint8_t* build_flag) {
+__global__ void reset_root_kernel(gbdt_level* level, uint8_t* build_flag, gbdt_segment* seg, int64_t N) {
   level->node_begin = 0;
   level->n_slots = 1;
   build_flag[0] = 1;
+  seg[0] = gbdt_segment{0, N};
+}
+
+__global__ void iota_kernel(uint32_t* __restrict__ v, int64_t N) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < N; i += (int64_t)gridDim.x * blockDim.x)
+    v[i] = static_cast<uint32_t>(i);
 }
 
 // Root totals when the root is also the last level (max_depth 0): count and
@@ -59,17 +67,18 @@ __global__ void __launch_bounds__(1024)
     apply_level_kernel(int d, int D, const gbdt_level* __restrict__ level, int32_t max_slots,
                        const gbdt_split* __restrict__ splits, const SlotTotals* __restrict__ totals,
                        const uint8_t* __restrict__ build_flag, const int32_t* __restrict__ fixed_exp, double lambda,
-                       gbdt_node* __restrict__ tree, int32_t* __restrict__ n_nodes_out,
-                       gbdt_level* __restrict__ next_level, SlotTotals* __restrict__ next_totals,
+                       const gbdt_segment* __restrict__ seg, gbdt_node* __restrict__ tree,
+                       int32_t* __restrict__ n_nodes_out, gbdt_level* __restrict__ next_level,
+                       SlotTotals* __restrict__ next_totals, gbdt_segment* __restrict__ next_seg,
                        int32_t* __restrict__ pair_parent, uint8_t* __restrict__ next_build, Route* __restrict__ route,
                        LevelStats* __restrict__ stats, int32_t* __restrict__ err) {
   __shared__ int s_a[1024];
   __shared__ int s_pre;
-  __shared__ unsigned long long s_act;
+  __shared__ unsigned long long s_act, s_built_rows, s_split_rows;
   __shared__ int s_built;
   if (threadIdx.x == 0) {
     s_pre = 0;
-    s_act = 0;
+    s_act = s_built_rows = s_split_rows = 0;
     s_built = 0;
   }
   __syncthreads();
@@ -98,7 +107,12 @@ __global__ void __launch_bounds__(1024)
         tot = totals[s];
       }
       atomicAdd(&s_act, static_cast<unsigned long long>(tot.cnt));
-      if (d < D && build_flag[s]) atomicAdd(&s_built, 1);
+      if (d < D && build_flag[s]) {
+        atomicAdd(&s_built, 1);
+        atomicAdd(&s_built_rows, static_cast<unsigned long long>(tot.cnt));
+      }
+      if (is_split) atomicAdd(&s_split_rows, static_cast<unsigned long long>(tot.cnt));
+      if (seg[s].count != static_cast<int64_t>(tot.cnt)) raise_error(err, kErrHistTotals);
     }
     s_a[threadIdx.x] = is_split;
     __syncthreads();
@@ -128,6 +142,8 @@ __global__ void __launch_bounds__(1024)
         next_totals[2 * k] = SlotTotals{sp.q_left, cl, 0};
         next_totals[2 * k + 1] = SlotTotals{
             static_cast<int64_t>(static_cast<uint64_t>(sp.q_total) - static_cast<uint64_t>(sp.q_left)), cr, 0};
+        next_seg[2 * k] = gbdt_segment{seg[s].start, static_cast<int64_t>(cl)};
+        next_seg[2 * k + 1] = gbdt_segment{seg[s].start + cl, static_cast<int64_t>(cr)};
         pair_parent[k] = s;
         const uint8_t left_small = cl <= cr ? 1 : 0;  // build the smaller child; ties build the left one
         next_build[2 * k] = left_small;
@@ -150,17 +166,27 @@ __global__ void __launch_bounds__(1024)
     next_level->n_slots = 2 * s_pre;
     *n_nodes_out = next_begin + 2 * s_pre;
     stats->n_act = static_cast<int64_t>(s_act);
+    stats->n_built_rows = static_cast<int64_t>(s_built_rows);
+    stats->n_split_rows = static_cast<int64_t>(s_split_rows);
     stats->n_slots = n_slots;
     stats->n_built = s_built;
   }
 }
 
 struct TrainWs {
-  double* g;
-  uint16_t* node;
+  double* g0;         // gradients in original row order (level 0 positions)
+  uint32_t* orig0;    // identity: original row id of level-0 positions
+  uint16_t* leaf;     // leaf of each original row in the current tree
+  uint8_t* bins_xy[2];  // per-position copies for levels >= 1 (alternating)
+  double* g_xy[2];
+  uint32_t* orig_xy[2];
+  gbdt_segment* seg[2];
+  void* seg_scratch;
+  void* move_scratch;
   uint32_t* hist_cnt[2];
   int64_t* hist_q[2];
   gbdt_split* splits;
+  void* split_scratch;
   SlotTotals* totals[2];
   gbdt_level* level[2];
   uint8_t* build[2];
@@ -179,7 +205,8 @@ struct TrainWs {
 
 int32_t max_nodes_of(int D) { return (1 << (D + 1)) - 1; }
 
-TrainWs carve_train(void* ws, size_t bytes, int64_t N, int32_t F, const gbdt_params& p, size_t* need) {
+TrainWs carve_train(void* ws, size_t bytes, int64_t N, int32_t F, int64_t ldb, const gbdt_params& p,
+                    size_t* need) {
   Carve c(ws, bytes);
   TrainWs w{};
   const int D = p.max_depth;
@@ -187,13 +214,26 @@ TrainWs carve_train(void* ws, size_t bytes, int64_t N, int32_t F, const gbdt_par
   const int level_slots = 1 << D;
   const int64_t hist_entries = hist_slots * F * kBins;
   const int T = p.n_trees > 0 ? p.n_trees : 1;
-  w.g = c.take<double>(N);
-  w.node = c.take<uint16_t>((N + 15) / 16 * 16);
+  const int64_t n16 = (N + 15) / 16 * 16;
+  w.g0 = c.take<double>(n16);
+  w.orig0 = c.take<uint32_t>(n16);
+  w.leaf = c.take<uint16_t>(n16);
+  if (D >= 1) {
+    for (int i = 0; i < 2; ++i) {
+      w.bins_xy[i] = c.take<uint8_t>(static_cast<size_t>(F) * ldb);
+      w.g_xy[i] = c.take<double>(n16);
+      w.orig_xy[i] = c.take<uint32_t>(n16);
+    }
+  }
+  for (int i = 0; i < 2; ++i) w.seg[i] = c.take<gbdt_segment>(level_slots);
+  w.seg_scratch = c.take<unsigned char>(seg_hist_scratch_bytes(static_cast<int32_t>(hist_slots)));
+  w.move_scratch = c.take<unsigned char>(move_scratch_bytes(N, level_slots));
   for (int i = 0; i < 2; ++i) {
     w.hist_cnt[i] = c.take<uint32_t>(hist_entries);
     w.hist_q[i] = c.take<int64_t>(hist_entries);
   }
   w.splits = c.take<gbdt_split>(level_slots);
+  w.split_scratch = c.take<unsigned char>(find_splits_scratch_bytes(F, static_cast<int32_t>(hist_slots)));
   for (int i = 0; i < 2; ++i) {
     w.totals[i] = c.take<SlotTotals>(level_slots);
     w.level[i] = c.take<gbdt_level>(1);
@@ -243,7 +283,7 @@ int validate_params(const gbdt_params* p);
 extern "C" size_t gbdt_train_workspace_size(int64_t N, int32_t F, const gbdt_params* p) {
   if (!p || N < 1 || F < 1 || p->max_depth < 0 || p->max_depth > GBDT_MAX_DEPTH) return 0;
   size_t need = 0;
-  carve_train(nullptr, 0, N, F, *p, &need);
+  carve_train(nullptr, 0, N, F, (N + 15) / 16 * 16, *p, &need);
   return need;
 }
 
@@ -264,7 +304,7 @@ extern "C" int gbdt_train(const uint8_t* bins, int64_t ldb, const int32_t* n_bin
   GBDT_CHECK_ARG(ldb >= N && ldb % 16 == 0 && aligned(bins, 16), "gbdt_train: bins need ldb >= N, ldb %% 16 == 0 "
                  "and a 16-byte aligned base");
   size_t need = 0;
-  TrainWs w = carve_train(ws, ws_bytes, N, F, *p, &need);
+  TrainWs w = carve_train(ws, ws_bytes, N, F, ldb, *p, &need);
   if (!ws || ws_bytes < need || !aligned(ws, kWsAlign)) {
     set_error("gbdt_train: workspace needs %zu bytes (got %zu)", need, ws_bytes);
     return ws ? GBDT_ERR_WORKSPACE : GBDT_ERR_INVALID_ARG;
@@ -290,56 +330,65 @@ extern "C" int gbdt_train(const uint8_t* bins, int64_t ldb, const int32_t* n_bin
 
   EventPool& pool = event_pool();
   const bool timing = diag != nullptr;
-  if (timing) GBDT_CUDA(pool.ensure(2 + 2 * static_cast<size_t>(T) * (D > 0 ? D : 1)));
+  // per tree and level: histogram start/end, partition start/end
+  if (timing) GBDT_CUDA(pool.ensure(2 + 4 * static_cast<size_t>(T) * (D + 1)));
+  auto ev_hist = [&](int t, int d, int k) { return pool.ev[2 + 4 * (static_cast<size_t>(t) * (D + 1) + d) + k]; };
   const int64_t launches0 = launch_count();
-  size_t ev_i = 2;
   if (timing) GBDT_CUDA(cudaEventRecord(pool.ev[0], s));
 
   launch_label_mean(w.label_partials, N, w.init, s);
+  iota_kernel<<<sm_count() * 4, 256, 0, s>>>(w.orig0, N);
+  count_launches();
   const int fail_after = g_fail_after_levels.load();
   int levels_done = 0;
   for (int t = 0; t < T; ++t) {
     gbdt_node* tree = w.trees + static_cast<size_t>(t) * M;
     if (t == 0) {
       GBDT_CUDA(cudaMemsetAsync(w.maxabs, 0, sizeof(unsigned long long), s));
-      launch_start_tree0(w.init, label, N, pred_out, w.g, w.node, w.maxabs, s);
+      launch_start_tree0(w.init, label, N, pred_out, w.g0, w.leaf, w.maxabs, s);
     }
     launch_fixed_exp(w.maxabs, N, w.fixed_exp, s);
-    reset_root_kernel<<<1, 1, 0, s>>>(w.level[0], w.build[0]);
+    reset_root_kernel<<<1, 1, 0, s>>>(w.level[0], w.build[0], w.seg[0], N);
     count_launches();
     if (D == 0) {
       GBDT_CUDA(cudaMemsetAsync(w.totals[0], 0, sizeof(SlotTotals), s));
-      root_totals_kernel<<<sm_count() * 4, 256, 0, s>>>(w.g, N, w.fixed_exp, w.totals[0]);
+      root_totals_kernel<<<sm_count() * 4, 256, 0, s>>>(w.g0, N, w.fixed_exp, w.totals[0]);
       count_launches();
     }
     for (int d = 0; d <= D; ++d) {
       const int cur = d & 1, nxt = cur ^ 1;
       const int max_slots = 1 << d;
       LevelStats* st = w.stats + static_cast<size_t>(t) * (D + 1) + d;
+      // per-position data of level d: the caller's bins and g0 at level 0, then alternating copies
+      const uint8_t* lb = d == 0 ? bins : w.bins_xy[(d - 1) & 1];
+      const double* lg = d == 0 ? w.g0 : w.g_xy[(d - 1) & 1];
+      const uint32_t* lo = d == 0 ? w.orig0 : w.orig_xy[(d - 1) & 1];
       if (d < D) {
         const int max_build = d == 0 ? 1 : max_slots / 2;
-        const HistPlan plan = plan_histograms(N, F, max_slots, max_build);
-        launch_hist_zero(w.level[cur], max_slots, w.build[cur], F, w.hist_cnt[cur], w.hist_q[cur], s);
-        if (timing) GBDT_CUDA(cudaEventRecord(pool.ev[ev_i++], s));
-        rc = launch_hist_build(plan, bins, ldb, N, F, w.g, GBDT_DTYPE_F64, w.fixed_exp, w.node, w.level[cur],
-                               max_slots, w.build[cur], w.hist_cnt[cur], w.hist_q[cur], w.err, s);
+        const SegHistPlan plan = plan_seg_histograms(N, F, max_slots, max_build);
+        if (timing) GBDT_CUDA(cudaEventRecord(ev_hist(t, d, 0), s));
+        rc = launch_seg_histograms(plan, lb, ldb, N, F, lg, GBDT_DTYPE_F64, w.fixed_exp, w.level[cur], max_slots,
+                                   w.build[cur], w.seg[cur], w.seg_scratch, w.hist_cnt[cur], w.hist_q[cur], s);
         if (rc != GBDT_OK) return rc;
-        if (timing) GBDT_CUDA(cudaEventRecord(pool.ev[ev_i++], s));
+        if (timing) GBDT_CUDA(cudaEventRecord(ev_hist(t, d, 1), s));
         if (d > 0) {
           launch_hist_subtract(w.hist_cnt[nxt], w.hist_q[nxt], w.pair_parent, w.build[cur], w.level[cur], max_slots,
                                F, w.hist_cnt[cur], w.hist_q[cur], w.err, s);
         }
         launch_find_splits(w.hist_cnt[cur], w.hist_q[cur], w.fixed_exp, F, n_bins, w.level[cur], max_slots, *p,
-                           w.splits, w.err, s);
+                           w.splits, w.split_scratch, w.err, s);
       }
       apply_level_kernel<<<1, 1024, 0, s>>>(d, D, w.level[cur], max_slots, d < D ? w.splits : nullptr, w.totals[cur],
-                                            w.build[cur], w.fixed_exp, p->reg_lambda, tree, w.n_nodes + t,
-                                            w.level[nxt], w.totals[nxt], w.pair_parent, w.build[nxt], w.route, st,
-                                            w.err);
+                                            w.build[cur], w.fixed_exp, p->reg_lambda, w.seg[cur], tree,
+                                            w.n_nodes + t, w.level[nxt], w.totals[nxt], w.seg[nxt], w.pair_parent,
+                                            w.build[nxt], w.route, st, w.err);
       count_launches();
-      if (d < D) {
-        launch_route_rows(bins, ldb, N, w.route, w.level[cur], max_slots, w.node, w.err, s);
-      }
+      // move the rows of split nodes into child order; frozen nodes record their rows' leaf
+      if (timing) GBDT_CUDA(cudaEventRecord(ev_hist(t, d, 2), s));
+      launch_move_rows(lb, d < D ? w.bins_xy[d & 1] : nullptr, ldb, N, F, lg, d < D ? w.g_xy[d & 1] : nullptr, 8, lo,
+                       d < D ? w.orig_xy[d & 1] : nullptr, nullptr, w.level[cur], max_slots, w.seg[cur], w.route,
+                       d < D ? w.splits : nullptr, nullptr, w.leaf, w.move_scratch, w.err, s);
+      if (timing) GBDT_CUDA(cudaEventRecord(ev_hist(t, d, 3), s));
       GBDT_LAUNCH_CHECK();
       ++levels_done;
       if (fail_after >= 0 && levels_done >= fail_after) {
@@ -350,14 +399,14 @@ extern "C" int gbdt_train(const uint8_t* bins, int64_t ldb, const int32_t* n_bin
     }
     const bool next = t + 1 < T;
     if (next) GBDT_CUDA(cudaMemsetAsync(w.maxabs, 0, sizeof(unsigned long long), s));
-    launch_finish_tree(tree, w.n_nodes + t, M, p->learning_rate, label, N, pred_out, w.g, w.node, w.maxabs, next,
+    launch_finish_tree(tree, w.n_nodes + t, M, p->learning_rate, label, N, pred_out, w.g0, w.leaf, w.maxabs, next,
                        s);
     GBDT_LAUNCH_CHECK();
   }
   if (T == 0) {
     // no tree: predictions are the initial value
     GBDT_CUDA(cudaMemsetAsync(w.maxabs, 0, sizeof(unsigned long long), s));
-    launch_start_tree0(w.init, label, N, pred_out, w.g, w.node, w.maxabs, s);
+    launch_start_tree0(w.init, label, N, pred_out, w.g0, w.leaf, w.maxabs, s);
   }
   if (timing) GBDT_CUDA(cudaEventRecord(pool.ev[1], s));
 
@@ -408,17 +457,23 @@ extern "C" int gbdt_train(const uint8_t* bins, int64_t ldb, const int32_t* n_bin
     float ms = 0.f;
     GBDT_CUDA(cudaEventElapsedTime(&ms, pool.ev[0], pool.ev[1]));
     dg.total_ms = ms;
-    size_t e = 2;
-    const double row_bytes = static_cast<double>(F) + 8.0 + 2.0;  // bins + fp64 g + uint16 node id
+    const double row_bytes = static_cast<double>(F) + 8.0;       // a built row: bins + fp64 g
+    const double move_bytes = 2.0 * (F + 8.0 + 4.0) + 1.0;       // a moved row: read + write, + split column
     for (int t = 0; t < T; ++t) {
-      for (int d = 0; d < D; ++d) {
-        GBDT_CUDA(cudaEventElapsedTime(&ms, pool.ev[e], pool.ev[e + 1]));
-        e += 2;
+      for (int d = 0; d <= D; ++d) {
         const LevelStats& ls = h_stats[static_cast<size_t>(t) * (D + 1) + d];
-        dg.hist_ms += ms;
-        dg.hist_launches += 1;
-        dg.hist_rows += ls.n_act;
-        dg.hist_bytes += static_cast<double>(ls.n_act) * row_bytes + static_cast<double>(ls.n_built) * F * kBins * 12.0;
+        if (d < D) {
+          GBDT_CUDA(cudaEventElapsedTime(&ms, ev_hist(t, d, 0), ev_hist(t, d, 1)));
+          dg.hist_ms += ms;
+          dg.hist_launches += 1;
+          dg.hist_rows += ls.n_built_rows;
+          dg.hist_bytes += static_cast<double>(ls.n_built_rows) * row_bytes +
+                           static_cast<double>(ls.n_built) * F * kBins * 12.0;
+        }
+        GBDT_CUDA(cudaEventElapsedTime(&ms, ev_hist(t, d, 2), ev_hist(t, d, 3)));
+        dg.part_ms += ms;
+        dg.part_bytes += static_cast<double>(ls.n_split_rows) * move_bytes +
+                         static_cast<double>(ls.n_act - ls.n_split_rows) * 6.0;
       }
       if (h_n[t] == M) dg.trees_at_full_size += 1;
     }

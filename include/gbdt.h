@@ -122,7 +122,9 @@ typedef struct gbdt_diagnostics {
   int64_t hist_launches;     /* histogram-construction launches */
   double hist_ms;            /* their total device time */
   double hist_bytes;         /* their algorithmic bytes */
-  int64_t hist_rows;         /* active rows scanned, summed over launches */
+  int64_t hist_rows;         /* rows read for directly built histograms, summed */
+  double part_ms;            /* device time of the row partitions (data moves) */
+  double part_bytes;         /* their algorithmic bytes */
   double total_ms;           /* device time of the whole training call */
   int64_t kernel_launches;   /* kernels launched by the call */
   int32_t trees_at_full_size; /* trees that reached 2^max_depth leaves */
@@ -210,6 +212,22 @@ int gbdt_subtract_histograms(const uint32_t* prev_cnt, const int64_t* prev_q, co
                              const uint8_t* build_flag, const gbdt_level* level, int32_t max_slots, int32_t F,
                              uint32_t* hist_cnt, int64_t* hist_q, void* stream);
 
+/* gbdt_build_histograms_segmented: the same per-bin count and fixed-point G
+ * of every flagged slot of a level ("Module Design: Training Core" s.6 step 2,
+ * s.7), for rows already grouped by node: the rows of slot s are exactly the
+ * positions segments[s].start .. + segments[s].count of every column of
+ * bins [F][ldb] and of g (as gbdt_partition_rows leaves them).  Only the
+ * flagged segments are read (with sibling subtraction, the smaller child of
+ * each pair), one node per CTA with up to 64 features of shared-memory
+ * histograms.  segments [max_slots] (device); other arguments and outputs as
+ * gbdt_build_histograms.  Workspace: gbdt_histograms_segmented_workspace_size. */
+size_t gbdt_histograms_segmented_workspace_size(int32_t max_slots);
+int gbdt_build_histograms_segmented(const uint8_t* bins, int64_t ldb, int64_t N, int32_t F, const void* g,
+                                    int32_t g_dtype, const int32_t* fixed_exp, const gbdt_level* level,
+                                    int32_t max_slots, const uint8_t* build_flag, int32_t max_build,
+                                    const gbdt_segment* segments, uint32_t* hist_cnt, int64_t* hist_q, void* ws,
+                                    size_t ws_bytes, void* stream);
+
 /* ---------------------------------------------------------------------------
  * gbdt_find_splits: best split of every slot of a level, "Module Design:
  * Training Core" s.2-s.3.  For feature j and threshold b = 0..n_bins[j]-2 the
@@ -221,10 +239,13 @@ int gbdt_subtract_histograms(const uint32_t* prev_cnt, const int64_t* prev_q, co
  * valid gain is > 0 (else out[slot].feature = -1).  Node totals are the sums
  * over the bins of feature 0 (the same for every feature).
  *   out [max_slots] gbdt_split (device); p: host pointer.
+ * Work is spread over (slot, feature) pairs, then reduced per slot; since the
+ * comparison is a total order the result does not depend on that split.
  * ------------------------------------------------------------------------- */
+size_t gbdt_find_splits_workspace_size(int32_t F, int32_t max_slots);
 int gbdt_find_splits(const uint32_t* hist_cnt, const int64_t* hist_q, const int32_t* fixed_exp, int32_t F,
                      const int32_t* n_bins, const gbdt_level* level, int32_t max_slots, const gbdt_params* p,
-                     gbdt_split* out, void* stream);
+                     gbdt_split* out, void* ws, size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------
  * gbdt_partition: "Module Design: Training Core" s.6 step 5.  The k-th slot
@@ -245,6 +266,25 @@ int gbdt_partition(const uint8_t* bins, int64_t ldb, int64_t N, int32_t F, const
                    const gbdt_level* level, int32_t max_slots, const gbdt_segment* seg_in, const uint32_t* idx_in,
                    uint16_t* node_of_row, uint32_t* idx_out, gbdt_segment* seg_out, gbdt_level* next_level,
                    void* ws, size_t ws_bytes, void* stream);
+
+/* gbdt_partition_rows: "Module Design: Training Core" s.6 step 5 carried out
+ * on the data itself.  For every slot whose split has feature >= 0, the
+ * positions seg_in[s] of every per-position array -- bins [F][ldb] (uint8),
+ * g [N] (g_dtype), orig [N] (uint32, the original row id) -- are copied to the
+ * same positions of the *_out arrays, rows going left first, each side in
+ * input order (stable).  A row goes right iff bins[feature][p] > bin, or, when
+ * go_right [N] (uint8, device) is given, iff go_right[p] != 0.  The k-th
+ * splitting slot (slot order) gets seg_out[2k] (left), seg_out[2k+1] (right);
+ * next_level (optional) receives {node_begin + n_slots, 2*splits}.  Slots
+ * without a split are not copied; if leaf_of_row [original rows] (uint16) is
+ * given, leaf_of_row[orig_in[p]] = node_begin + s for their positions.
+ * Inputs and outputs must not alias. */
+size_t gbdt_partition_rows_workspace_size(int64_t N, int32_t max_slots);
+int gbdt_partition_rows(const uint8_t* bins_in, uint8_t* bins_out, int64_t ldb, int64_t N, int32_t F,
+                        const void* g_in, void* g_out, int32_t g_dtype, const uint32_t* orig_in, uint32_t* orig_out,
+                        const uint8_t* go_right, const gbdt_split* splits, const gbdt_level* level,
+                        int32_t max_slots, const gbdt_segment* seg_in, gbdt_segment* seg_out,
+                        gbdt_level* next_level, uint16_t* leaf_of_row, void* ws, size_t ws_bytes, void* stream);
 
 /* gbdt_partition_noalloc: gbdt_partition without a workspace argument.  The
  * pages have no counterpart; this entry point exists for callers that cannot

@@ -74,7 +74,7 @@ def test_struct_layouts_match_header():
     assert ctypes.sizeof(g.Params) == 48
     assert g.NODE_DTYPE.itemsize == 40 and g.SPLIT_DTYPE.itemsize == 40
     assert g.LEVEL_DTYPE.itemsize == 8 and g.SEGMENT_DTYPE.itemsize == 16
-    assert ctypes.sizeof(g.Diagnostics) == 56
+    assert ctypes.sizeof(g.Diagnostics) == 72
 
 
 def test_entry_points_reject_bad_arguments_before_any_launch(lib):
