@@ -200,59 +200,109 @@ def run_reference(args, rank, ws, dist):
 
 # ------------------------------------------------------------------------------------ our arm
 def microbench(g, torch, args, peak):
-    """One level at 50M x 64 pre-binned features, 256 nodes (128 sibling pairs)."""
+    """One tree level at 50M rows x 64 pre-binned features, 256 nodes (128 sibling pairs).
+
+    Rows are stored grouped by parent (the order the trainer holds them in after the previous
+    level's partition); each row's child is uniform.  Timed, each with CUDA events: the partition
+    of every parent's rows into its two children (all columns move), the segmented histograms of
+    the smaller children, sibling subtraction, and split search.  The node-id scan over rows in
+    random node order (the first design) is timed too, for comparison.
+    """
     cfg = synth.CONFIGS["micro"]
     N, F, n_nodes = args.micro_rows, cfg["f"], cfg["n_nodes"]
-    bins_h, node_h, g_h = synth.make_micro(n=N, f=F, n_nodes=n_nodes, grouped=False)
-    bins = torch.zeros((F, g.padded_ld(N)), dtype=torch.uint8, device="cuda")
+    P = n_nodes // 2
+    bins_h, node_h, g_h = synth.make_micro(n=N, f=F, n_nodes=n_nodes, grouped=True)
+    ld = g.padded_ld(N)
+    bins = torch.zeros((F, ld), dtype=torch.uint8, device="cuda")
     bins[:, :N] = torch.from_numpy(bins_h).cuda()
     del bins_h
-    node = torch.from_numpy(node_h.view(np.int16)).cuda()
-    parent = torch.from_numpy((node_h >> 1).astype(np.uint16).view(np.int16)).cuda()
     gd = torch.from_numpy(g_h).cuda()
-    counts = np.bincount(node_h, minlength=n_nodes)
+    orig = torch.arange(N, dtype=torch.int32, device="cuda")
+    go_right = torch.from_numpy((node_h & 1).astype(np.uint8)).cuda()
+    counts = np.bincount(node_h, minlength=n_nodes).astype(np.int64)
+    pc = counts[0::2] + counts[1::2]
+    pstart = np.concatenate([[0], np.cumsum(pc)[:-1]])
+    pseg = np.zeros(P, g.SEGMENT_DTYPE)
+    pseg["start"], pseg["count"] = pstart, pc
+    sp = np.zeros(P, g.SPLIT_DTYPE)
+    sp["feature"], sp["bin"], sp["cnt_left"], sp["cnt_total"] = 0, 0, counts[0::2], pc
     left_small = counts[0::2] <= counts[1::2]
     flags = np.empty(n_nodes, np.uint8)
     flags[0::2], flags[1::2] = left_small, ~left_small
     fd = torch.from_numpy(flags).cuda()
-    lvl = g._dev(np.array([(0, n_nodes)], g.LEVEL_DTYPE), g.LEVEL_DTYPE)
-    plvl = g._dev(np.array([(0, n_nodes // 2)], g.LEVEL_DTYPE), g.LEVEL_DTYPE)
+    dev = g._dev
+    plvl, lvl = dev(np.array([(0, P)], g.LEVEL_DTYPE), g.LEVEL_DTYPE), dev(np.array([(P, n_nodes)], g.LEVEL_DTYPE),
+                                                                           g.LEVEL_DTYPE)
+    pseg_d, sp_d = dev(pseg, g.SEGMENT_DTYPE), dev(sp, g.SPLIT_DTYPE)
     S = g.gradient_scale(gd)
     n_bins = torch.full((F,), 256, dtype=torch.int32, device="cuda")
-    pc, pq = g.build_histograms(bins, N, gd, S, parent, plvl, n_nodes // 2,
-                                torch.ones(n_nodes // 2, dtype=torch.uint8, device="cuda"), n_nodes // 2)
+    # parents' histograms, untimed, from the parent-grouped rows
+    ph_c, ph_q = g.build_histograms_segmented(bins, N, gd, S, plvl, P, torch.ones(P, dtype=torch.uint8,
+                                              device="cuda"), P, pseg_d)
+    out = (torch.empty_like(bins), torch.empty_like(gd), torch.empty_like(orig))
+    pws = g._workspace(g.lib().gbdt_partition_rows_workspace_size(N, P))
+    hws = g._workspace(g.lib().gbdt_histograms_segmented_workspace_size(n_nodes))
     hc = torch.zeros((n_nodes, F, 256), dtype=torch.int32, device="cuda")
     hq = torch.zeros((n_nodes, F, 256), dtype=torch.int64, device="cuda")
-    ws = g._workspace(g.lib().gbdt_histograms_workspace_size(N, F, n_nodes))
-    pair_parent = torch.arange(n_nodes // 2, dtype=torch.int32, device="cuda")
+    pair_parent = torch.arange(P, dtype=torch.int32, device="cuda")
     split_out = torch.empty(n_nodes * g.SPLIT_DTYPE.itemsize, dtype=torch.uint8, device="cuda")
     stream = torch.cuda.current_stream()
-    times = {"build": [], "subtract": [], "find": []}
+    times = {"partition": [], "build": [], "subtract": [], "find": []}
     for it in range(args.warmup + args.steps):
-        ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
         ev[0].record(stream)
-        g.build_histograms(bins, N, gd, S, node, lvl, n_nodes, fd, n_nodes // 2, hc, hq, ws=ws)
+        cb, cg, co, cseg, _ = g.partition_rows(bins, N, gd, orig, sp_d, plvl, P, pseg_d, go_right=go_right, out=out,
+                                               ws=pws)
         ev[1].record(stream)
-        g.subtract_histograms(pc, pq, pair_parent, fd, lvl, n_nodes, hc, hq)
+        g.build_histograms_segmented(cb, N, cg, S, lvl, n_nodes, fd, P, cseg, hc, hq, ws=hws)
         ev[2].record(stream)
+        g.subtract_histograms(ph_c, ph_q, pair_parent, fd, lvl, n_nodes, hc, hq)
+        ev[3].record(stream)
         g.find_splits(hc, hq, S, n_bins, lvl, n_nodes, out=split_out, reg_lambda=1.0, gamma=0.0,
                       min_samples_leaf=1, min_child_weight=0.0)
-        ev[3].record(stream)
+        ev[4].record(stream)
         torch.cuda.synchronize()
         if it >= args.warmup:
-            times["build"].append(ev[0].elapsed_time(ev[1]))
-            times["subtract"].append(ev[1].elapsed_time(ev[2]))
-            times["find"].append(ev[2].elapsed_time(ev[3]))
+            for k, name in enumerate(times):
+                times[name].append(ev[k].elapsed_time(ev[k + 1]))
     ms = {k: statistics.mean(v) for k, v in times.items()}
-    n_built = int(flags.sum())
-    node_bytes = 2  # uint16 node ids
-    alg = N * (F * 1 + 4 + node_bytes) + n_built * F * 256 * 12
-    gbs = alg / (ms["build"] * 1e-3) / 1e9
-    return {"workload": f"one level: {N:,} rows x {F} pre-binned uint8 features (Zipf 1.1), {n_nodes} nodes, "
-                        f"{n_built} built directly, fp32 g, uint16 node ids, rows in random node order",
-            "build_ms": ms["build"], "subtract_ms": ms["subtract"], "find_splits_ms": ms["find"],
-            "total_ms": sum(ms.values()), "build_algorithmic_bytes": alg, "build_gbs": gbs, "peak_gbs": peak,
-            "build_frac": gbs / peak, "target_frac": 0.5}
+    n_small = int(np.minimum(counts[0::2], counts[1::2]).sum())
+    build_bytes = n_small * (F + 4) + P * F * 256 * 12
+    part_bytes = N * (2 * (F + 4 + 4) + 1)
+    formula_bytes = N * (F + 4 + 1) + P * F * 256 * 12  # full-scan accounting: every active row read once
+    level_ms = sum(ms.values())
+    res = {"workload": f"one level: {N:,} rows x {F} pre-binned uint8 features (Zipf 1.1), {n_nodes} nodes "
+                       f"(uniform), rows grouped by parent, fp32 g",
+           "partition_ms": ms["partition"], "build_ms": ms["build"], "subtract_ms": ms["subtract"],
+           "find_splits_ms": ms["find"], "level_ms": level_ms,
+           "build_algorithmic_bytes": build_bytes, "build_gbs": build_bytes / (ms["build"] * 1e-3) / 1e9,
+           "build_frac": build_bytes / (ms["build"] * 1e-3) / 1e9 / peak,
+           "partition_gbs": part_bytes / (ms["partition"] * 1e-3) / 1e9,
+           "partition_frac": part_bytes / (ms["partition"] * 1e-3) / 1e9 / peak,
+           "level_effective_gbs": formula_bytes / (level_ms * 1e-3) / 1e9,
+           "level_effective_frac": formula_bytes / (level_ms * 1e-3) / 1e9 / peak,
+           "peak_gbs": peak, "target_frac": 0.5,
+           "note": "build_* = the histogram kernel on its own bytes (smaller children only); level_effective_* = "
+                   "N x (F + 4 + 1) + output bytes over partition + build + subtract + find"}
+    # the first design: node-id scan over rows in random node order
+    perm = torch.randperm(N, device="cuda", generator=torch.Generator(device="cuda").manual_seed(0))
+    rb = bins[:, :N][:, perm].contiguous()
+    rbins = torch.zeros_like(bins)
+    rbins[:, :N] = rb
+    del rb
+    rnode = torch.from_numpy(node_h.view(np.int16)).cuda()[perm].contiguous()
+    rg = gd[perm].contiguous()
+    rt = []
+    for it in range(2):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        g.build_histograms(rbins, N, rg, S, rnode, dev(np.array([(0, n_nodes)], g.LEVEL_DTYPE), g.LEVEL_DTYPE),
+                           n_nodes, fd, P, hc, hq)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        rt.append(e0.elapsed_time(e1))
+    res["node_id_scan_random_order_build_ms"] = rt[-1]
+    return res
 
 
 def run_ours(args, rank, local_rank, ws, dist):
@@ -264,6 +314,9 @@ def run_ours(args, rank, local_rank, ws, dist):
     torch.cuda.set_device(local_rank)
     gb.build()
     g.lib()
+    if args.only_micro:
+        print(json.dumps({"histogram_microbench": microbench(g, torch, args, _peaks()[0])}), flush=True)
+        return 0
     name = args.config
     cfg = dict(synth.CONFIGS[name])
     if args.trees is not None:
@@ -313,12 +366,14 @@ def run_ours(args, rank, local_rank, ws, dist):
     hist_launches = sum(d["hist_launches"] for d in diags)
     achieved = hist_bytes / (hist_ms * 1e-3) / 1e9
     trec = _traffic_record(os.path.join(ROOT, "histogram_gradient_boosted_gb300", "csrc", "histogram.cu"))
+    part_ms = sum(d["part_ms"] for d in diags)
+    part_bytes = sum(d["part_bytes"] for d in diags)
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                 "traffic": (trec["dram_bytes_per_launch"] if trec else None),
-                "kernel": "hist_build_kernel (level histograms inside gbdt_train)",
+                "kernel": "seg_hist_kernel (level histograms inside gbdt_train; smaller children, node-contiguous)",
                 "launches": hist_launches, "avg_launch_ms": hist_ms / hist_launches,
                 "algorithmic_bytes_per_launch": hist_bytes / hist_launches, "peak_kind": peak_kind,
-                "share_of_step": hist_ms / (ms_total / 1.0) if ms_total else None}
+                "share_of_step": hist_ms / ms_total if ms_total else None}
 
     # ---- e2e: public API with host inputs ----
     Xp = torch.empty((F, N), dtype=torch.float32, pin_memory=True)
@@ -353,6 +408,9 @@ def run_ours(args, rank, local_rank, ws, dist):
                        "parallelism": "replicas" if ws > 1 else "single GPU"},
             "e2e": e2e, "gpu_launches": launches, "gpu_launches_per_step": launches / args.steps,
             "roofline": roofline, "clocks": clocks,
+            "partition": {"ms_per_step": part_ms / args.steps, "achieved_gbs": part_bytes / (part_ms * 1e-3) / 1e9,
+                          "frac": part_bytes / (part_ms * 1e-3) / 1e9 / peak,
+                          "share_of_step": part_ms / ms_total if ms_total else None},
             "train_only": {"ms_per_run": train_ms, "value": N * F * T / (train_ms * 1e-3)},
             "trees_at_full_size": diags[-1]["trees_at_full_size"]}
     if rank == 0 and not args.no_micro:
@@ -383,6 +441,7 @@ def main():
     ap.add_argument("--cpu-trees", type=int, default=2)
     ap.add_argument("--no-micro", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--only-micro", action="store_true", help="run only the level microbench (profiling)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         print("note: fewer than 3 warm-up steps", file=sys.stderr)

@@ -179,7 +179,6 @@ __global__ void __launch_bounds__(kSegThreads, 1)
 // ---------------------------------------------------------------------------------------- partition
 constexpr int kMvThreads = 256;
 constexpr int kMvTile = 4096;  // positions per tile
-constexpr int kMvCols = 16;    // columns streamed per CTA
 
 struct MvState {
   int32_t total_tiles;
@@ -277,10 +276,10 @@ __global__ void __launch_bounds__(kMvThreads)
     return;
   }
   const int64_t p0 = seg[s].start + static_cast<int64_t>(t - tile_start[s]) * kMvTile;
-  const int64_t p1 = min(seg[s].start + seg[s].count, p0 + kMvTile);
+  const int n = static_cast<int>(min(seg[s].start + seg[s].count - p0, static_cast<int64_t>(kMvTile)));
   const uint8_t* col = bins + static_cast<int64_t>(rt.feature) * ldb;
   int c = 0;
-  for (int64_t p = p0 + threadIdx.x; p < p1; p += blockDim.x) c += 1 - goes_right(col, rt.bin, go_right, p);
+  for (int j = threadIdx.x; j < n; j += blockDim.x) c += 1 - goes_right(col, rt.bin, go_right, p0 + j);
   int total;
   block_scan_excl(c, s_warp, &total);
   if (threadIdx.x == 0) tile_left[t] = total;
@@ -325,17 +324,34 @@ __global__ void __launch_bounds__(1024)
   }
 }
 
-// Column c < F: bins column c; c == F: gradient (8 B); c == F + 1: original row id (4 B).
-__global__ void __launch_bounds__(kMvThreads)
+// Column c < F: bins column c; c == F: gradient (4 or 8 B); c == F + 1: original row id (4 B).
+// Output-centric move.  Once per tile: the rows' decisions (lane = row,
+// ballots), their ranks, and the inverse permutation inv[o] = tile position of
+// the o-th output row (left rows first, then right rows) in shared memory.
+// Each thread then owns up to kMvWordsPerThread aligned 4-byte words of the
+// tile's two output runs and keeps, in registers, the source positions of
+// their bytes.  Per column the tile is staged in shared memory with 16-byte
+// loads, and every output word is gathered from the stage and written with one
+// aligned 4-byte store (byte stores only where a run starts or ends inside a
+// word), so stores fill whole sectors.
+constexpr int kMvChunks = kMvTile / 32;
+constexpr int kMvChunksPerWarp = kMvChunks / (kMvThreads / 32);
+constexpr int kMvWordsPerThread = (kMvTile / 4 + 4 + kMvThreads - 1) / kMvThreads;  // 5: both runs, edges included
+
+__global__ void __launch_bounds__(kMvThreads, 4)
     mv_move_kernel(const uint8_t* __restrict__ bins_in, uint8_t* __restrict__ bins_out, int64_t ldb, int32_t F,
-                   const void* __restrict__ g_in, void* __restrict__ g_out, int g_size, const uint32_t* __restrict__ orig_in,
-                   uint32_t* __restrict__ orig_out, const uint8_t* __restrict__ go_right,
-                   const gbdt_level* __restrict__ level, int32_t max_slots, const gbdt_segment* __restrict__ seg,
-                   const Route* __restrict__ route, const int32_t* __restrict__ tile_start,
-                   const MvState* __restrict__ st, const int64_t* __restrict__ tile_excl,
-                   const int64_t* __restrict__ seg_left, uint16_t* __restrict__ leaf_of_row) {
-  __shared__ uint16_t s_dst[kMvTile];              // tile position -> position in partitioned tile order
-  __shared__ __align__(16) uint32_t s_stage[kMvTile / 4 + 8];  // one byte column in partitioned order
+                   const void* __restrict__ g_in, void* __restrict__ g_out, int g_size,
+                   const uint32_t* __restrict__ orig_in, uint32_t* __restrict__ orig_out,
+                   const uint8_t* __restrict__ go_right, const gbdt_level* __restrict__ level, int32_t max_slots,
+                   const gbdt_segment* __restrict__ seg, const Route* __restrict__ route,
+                   const int32_t* __restrict__ tile_start, const MvState* __restrict__ st,
+                   const int64_t* __restrict__ tile_excl, const int64_t* __restrict__ seg_left,
+                   uint16_t* __restrict__ leaf_of_row) {
+  __shared__ uint32_t s_right[kMvChunks];
+  __shared__ uint32_t s_valid[kMvChunks];
+  __shared__ int s_lbase[kMvChunks];
+  __shared__ uint16_t s_inv[kMvTile];
+  __shared__ __align__(16) uint8_t s_stage[kMvTile + 32];
   __shared__ int s_warp[33];
   const int t = blockIdx.x;
   if (t >= st->total_tiles) return;
@@ -344,106 +360,129 @@ __global__ void __launch_bounds__(kMvThreads)
   const Route rt = route[s];
   const int64_t tile_off = static_cast<int64_t>(t - tile_start[s]) * kMvTile;
   const int64_t p0 = seg[s].start + tile_off;
-  const int64_t p1 = min(seg[s].start + seg[s].count, p0 + kMvTile);
-  const int n = static_cast<int>(p1 - p0);
+  const int n = static_cast<int>(min(seg[s].start + seg[s].count - p0, static_cast<int64_t>(kMvTile)));
   if (rt.feature < 0) {  // a leaf: remember each row's leaf, nothing moves
-    if (blockIdx.y == 0 && leaf_of_row) {
+    if (leaf_of_row) {
       const uint16_t node = static_cast<uint16_t>(level->node_begin + s);
       for (int i = threadIdx.x; i < n; i += blockDim.x) leaf_of_row[orig_in[p0 + i]] = node;
     }
     return;
   }
-  // rank the tile: thread t owns positions [16t, 16t+16) of the tile
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const uint8_t* col = bins_in + static_cast<int64_t>(rt.feature) * ldb;
-  uint32_t rmask = 0;
-  int nl = 0;
-#pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    const int j = threadIdx.x * 16 + i;
-    if (j < n) {
-      const int r = goes_right(col, rt.bin, go_right, p0 + j);
-      rmask |= static_cast<uint32_t>(r) << i;
-      nl += 1 - r;
-    }
-  }
-  int tile_nl;
-  const int lrank = block_scan_excl(nl, s_warp, &tile_nl);
-  {
-    int li = lrank, ri = threadIdx.x * 16 - lrank;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const int j = threadIdx.x * 16 + i;
-      if (j < n) s_dst[j] = static_cast<uint16_t>((rmask >> i & 1u) ? tile_nl + ri++ : li++);
+  // ---- rank the tile (lane = row) and build the inverse permutation
+#pragma unroll 1
+  for (int k = 0; k < kMvChunksPerWarp; ++k) {
+    const int ch = warp * kMvChunksPerWarp + k;
+    const int j = ch * 32 + lane;
+    const bool v = j < n;
+    const int r = v ? goes_right(col, rt.bin, go_right, p0 + j) : 0;
+    const uint32_t rm = __ballot_sync(0xffffffffu, r);
+    const uint32_t vm = __ballot_sync(0xffffffffu, v);
+    if (lane == 0) {
+      s_right[ch] = rm;
+      s_valid[ch] = vm;
     }
   }
   __syncthreads();
+  const int lc = threadIdx.x < kMvChunks ? __popc(s_valid[threadIdx.x] & ~s_right[threadIdx.x]) : 0;
+  int nl;
+  const int lex = block_scan_excl(lc, s_warp, &nl);
+  if (threadIdx.x < kMvChunks) s_lbase[threadIdx.x] = lex;
+  __syncthreads();
+  const uint32_t lt = (1u << lane) - 1u;
+#pragma unroll 1
+  for (int k = 0; k < kMvChunksPerWarp; ++k) {
+    const int ch = warp * kMvChunksPerWarp + k;
+    const uint32_t vm = s_valid[ch], rm = s_right[ch];
+    if (vm >> lane & 1u) {
+      const int lb = s_lbase[ch];
+      const int o = (rm >> lane & 1u) ? nl + (ch * 32 - lb) + __popc(rm & lt) : lb + __popc(vm & ~rm & lt);
+      s_inv[o] = static_cast<uint16_t>(ch * 32 + lane);
+    }
+  }
+  __syncthreads();
+  const int nr = n - nl;
   const int64_t left_before = tile_excl[t] - tile_excl[tile_start[s]];
-  const int64_t dst_l = seg[s].start + left_before;                                 // left run of this tile
-  const int64_t dst_r = seg[s].start + seg_left[s] + (tile_off - left_before);      // right run of this tile
-  const int tile_nr = n - tile_nl;
-
-  const int c_lo = blockIdx.y * kMvCols;
-  const int c_hi = min(F + 2, c_lo + kMvCols);
-  for (int c = c_lo; c < c_hi; ++c) {
-    if (c == F) {  // gradients: direct writes, lanes of a warp land in at most two runs
-      for (int j = threadIdx.x; j < n; j += blockDim.x) {
-        const int d = s_dst[j];
-        const int64_t o = d < tile_nl ? dst_l + d : dst_r + (d - tile_nl);
-        if (g_size == 8)
-          static_cast<uint64_t*>(g_out)[o] = static_cast<const uint64_t*>(g_in)[p0 + j];
-        else
-          static_cast<uint32_t*>(g_out)[o] = static_cast<const uint32_t*>(g_in)[p0 + j];
-      }
-      continue;
-    }
-    if (c == F + 1) {
-      for (int j = threadIdx.x; j < n; j += blockDim.x) {
-        const int d = s_dst[j];
-        orig_out[d < tile_nl ? dst_l + d : dst_r + (d - tile_nl)] = orig_in[p0 + j];
-      }
-      continue;
-    }
-    const uint8_t* in = bins_in + static_cast<int64_t>(c) * ldb;
-    uint8_t* out = bins_out + static_cast<int64_t>(c) * ldb;
-    uint8_t* stage = reinterpret_cast<uint8_t*>(s_stage);
-    // gather the tile into partitioned order (aligned 16-byte loads)
-    const int64_t a0 = p0 & ~int64_t(15);
-    for (int64_t b = a0 + 16 * threadIdx.x; b < p1; b += 16 * blockDim.x) {
-      const uint4 v = __ldg(reinterpret_cast<const uint4*>(in + b));
-      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  const int64_t dst_l = seg[s].start + left_before;                             // this tile's left run
+  const int64_t dst_r = seg[s].start + seg_left[s] + (tile_off - left_before);  // this tile's right run
+  // ---- the output words this thread owns: left run words, then right run words
+  const int64_t wl0 = dst_l >> 2, wr0 = dst_r >> 2;
+  const int nwl = nl > 0 ? static_cast<int>(((dst_l + nl + 3) >> 2) - wl0) : 0;
+  const int nwr = nr > 0 ? static_cast<int>(((dst_r + nr + 3) >> 2) - wr0) : 0;
+  const int ol = static_cast<int>(dst_l & 3), orr = static_cast<int>(dst_r & 3);  // run start inside its first word
+  int wrel[kMvWordsPerThread];       // word offset within its run's words; bit 30: right run; -1: none
+  uint32_t srcl[kMvWordsPerThread];  // tile positions of bytes 0,1 (16 bits each; 0xffff: not written)
+  uint32_t srch[kMvWordsPerThread];  // tile positions of bytes 2,3
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const int64_t p = b + i;
-        if (p >= p0 && p < p1) stage[s_dst[p - p0]] = static_cast<uint8_t>(w[i >> 2] >> (8 * (i & 3)));
+  for (int m = 0; m < kMvWordsPerThread; ++m) {
+    const int vw = threadIdx.x + m * kMvThreads;
+    uint32_t sp[4] = {0xffffu, 0xffffu, 0xffffu, 0xffffu};
+    int wr = -1;
+    if (vw < nwl + nwr) {
+      const bool left = vw < nwl;
+      const int rel = left ? vw : vw - nwl;
+      const int len = left ? nl : nr, base = left ? 0 : nl, first = left ? ol : orr;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int o = 4 * rel + i - first;  // offset in the run
+        if (o >= 0 && o < len) sp[i] = s_inv[base + o];
+      }
+      wr = left ? rel : (rel | 0x40000000);
+    }
+    wrel[m] = wr;
+    srcl[m] = sp[0] | (sp[1] << 16);
+    srch[m] = sp[2] | (sp[3] << 16);
+  }
+  const int a_off = static_cast<int>(p0 & 15);  // stage index of tile position 0
+  // ---- move every column
+#pragma unroll 1
+  for (int c = 0; c < F + 2; ++c) {
+    if (c < F) {
+      const uint8_t* in = bins_in + static_cast<int64_t>(c) * ldb;
+      uint32_t* out = reinterpret_cast<uint32_t*>(bins_out + static_cast<int64_t>(c) * ldb);
+      const int64_t a0 = p0 & ~int64_t(15);
+      const int nvec = static_cast<int>((p0 + n + 15 - a0) >> 4);
+      for (int v = threadIdx.x; v < nvec; v += blockDim.x)
+        reinterpret_cast<uint4*>(s_stage)[v] = __ldg(reinterpret_cast<const uint4*>(in + a0) + v);
+      __syncthreads();
+#pragma unroll
+      for (int m = 0; m < kMvWordsPerThread; ++m) {
+        const int wr = wrel[m];
+        if (wr < 0) continue;
+        const int64_t wa = (wr & 0x40000000) ? wr0 + (wr & 0x3fffffff) : wl0 + wr;
+        const uint32_t s0 = srcl[m] & 0xffffu, s1 = srcl[m] >> 16, s2 = srch[m] & 0xffffu, s3 = srch[m] >> 16;
+        if (s0 != 0xffffu && s1 != 0xffffu && s2 != 0xffffu && s3 != 0xffffu) {
+          out[wa] = static_cast<uint32_t>(s_stage[a_off + s0]) | (static_cast<uint32_t>(s_stage[a_off + s1]) << 8) |
+                    (static_cast<uint32_t>(s_stage[a_off + s2]) << 16) |
+                    (static_cast<uint32_t>(s_stage[a_off + s3]) << 24);
+        } else {  // a run starts or ends inside this word: write only its own bytes
+          uint8_t* ob = reinterpret_cast<uint8_t*>(out + wa);
+          if (s0 != 0xffffu) ob[0] = s_stage[a_off + s0];
+          if (s1 != 0xffffu) ob[1] = s_stage[a_off + s1];
+          if (s2 != 0xffffu) ob[2] = s_stage[a_off + s2];
+          if (s3 != 0xffffu) ob[3] = s_stage[a_off + s3];
+        }
+      }
+      __syncthreads();
+    } else {
+#pragma unroll
+      for (int m = 0; m < kMvWordsPerThread; ++m) {
+        const int wr = wrel[m];
+        if (wr < 0) continue;
+        const int64_t wa = (wr & 0x40000000) ? wr0 + (wr & 0x3fffffff) : wl0 + wr;
+#pragma unroll 1
+        for (int i = 0; i < 4; ++i) {
+          const uint32_t sv = i < 2 ? (srcl[m] >> (16 * i)) & 0xffffu : (srch[m] >> (16 * (i - 2))) & 0xffffu;
+          if (sv == 0xffffu) continue;
+          const int64_t d = (wa << 2) + i;
+          const int64_t src = p0 + sv;
+          if (c == F + 1) orig_out[d] = orig_in[src];
+          else if (g_size == 8) static_cast<uint64_t*>(g_out)[d] = static_cast<const uint64_t*>(g_in)[src];
+          else static_cast<uint32_t*>(g_out)[d] = static_cast<const uint32_t*>(g_in)[src];
+        }
       }
     }
-    __syncthreads();
-    // write the two runs: byte stores for unaligned ends, 16-byte stores inside
-    for (int run = 0; run < 2; ++run) {
-      const int64_t dst = run == 0 ? dst_l : dst_r;
-      const int len = run == 0 ? tile_nl : tile_nr;
-      const int src0 = run == 0 ? 0 : tile_nl;
-      if (len <= 0) continue;
-      const int64_t a = (dst + 15) & ~int64_t(15);  // first aligned address
-      const int head = static_cast<int>(a - dst < len ? a - dst : static_cast<int64_t>(len));
-      const int body16 = (len - head) / 16;
-      const int tail0 = head + body16 * 16;
-      for (int i = threadIdx.x; i < head; i += blockDim.x) out[dst + i] = stage[src0 + i];
-      for (int i = tail0 + threadIdx.x; i < len; i += blockDim.x) out[dst + i] = stage[src0 + i];
-      for (int k = threadIdx.x; k < body16; k += blockDim.x) {
-        const int o = src0 + head + 16 * k;  // byte offset in the stage
-        const int wa = o >> 2, sh = 8 * (o & 3);
-        const uint32_t x0 = s_stage[wa], x1 = s_stage[wa + 1], x2 = s_stage[wa + 2], x3 = s_stage[wa + 3],
-                       x4 = s_stage[wa + 4];
-        uint4 v;
-        v.x = __funnelshift_r(x0, x1, sh);
-        v.y = __funnelshift_r(x1, x2, sh);
-        v.z = __funnelshift_r(x2, x3, sh);
-        v.w = __funnelshift_r(x3, x4, sh);
-        *reinterpret_cast<uint4*>(out + a + 16 * k) = v;
-      }
-    }
-    __syncthreads();
   }
 }
 
@@ -562,8 +601,7 @@ void launch_move_rows(const uint8_t* bins_in, uint8_t* bins_out, int64_t ldb, in
   mv_scan_kernel<<<1, 1024, 0, s>>>(level, max_slots, route, tile_start, st, tile_left, tile_excl, seg_left, seg,
                                     seg_out, splits, err);
   count_launches();
-  dim3 grid(static_cast<unsigned>(max_tiles), static_cast<unsigned>(ceil_div(F + 2, kMvCols)));
-  mv_move_kernel<<<grid, kMvThreads, 0, s>>>(bins_in, bins_out, ldb, F, g_in, g_out, g_size, orig_in, orig_out,
+  mv_move_kernel<<<max_tiles, kMvThreads, 0, s>>>(bins_in, bins_out, ldb, F, g_in, g_out, g_size, orig_in, orig_out,
                                              go_right,
                                              level, max_slots, seg, route, tile_start, st, tile_excl, seg_left,
                                              leaf_of_row);
