@@ -76,13 +76,39 @@ __global__ void seg_chunk_setup_kernel(const gbdt_level* __restrict__ level, int
   }
 }
 
-__device__ __forceinline__ void add_entry(uint32_t* s_cnt, uint32_t* s_lo, int32_t* s_hi, int e, int64_t q) {
+// One exact fixed-point update of the entry at word e (count, low word with
+// the carry taken from the returned old value, high word when it changes).
+__device__ __forceinline__ void add_entry(uint32_t* s_cnt, uint32_t* s_lo, int32_t* s_hi, int e, uint32_t ql,
+                                          int32_t qh) {
   atomicAdd(s_cnt + e, 1u);
-  const uint32_t ql = static_cast<uint32_t>(static_cast<uint64_t>(q));
-  int32_t qh = static_cast<int32_t>(q >> 32);
   const uint32_t old = atomicAdd(s_lo + e, ql);
   qh += (old + ql < old) ? 1 : 0;  // carry out of the low word
   if (qh != 0) atomicAdd(s_hi + e, qh);
+}
+
+// Lane = feature: a warp takes 32 consecutive rows at a time and each lane adds
+// those rows of one feature (two features when the group has more than 32),
+// so the 32 lanes of one atomic instruction update 32 different features'
+// histograms.  The shared histograms are stored bin-major with the lane
+// innermost (word (half * 256 + bin) * 32 + lane for feature half * 32 + lane),
+// so every word a lane touches lies in the lane's own bank: an atomic
+// instruction is one shared-memory wavefront whatever the bins are, with no
+// bank conflicts and no same-address serialisation.  Gradients are loaded
+// once per warp (lane = row) and broadcast with shuffles.
+constexpr int kHalfWords = kBins * 32;
+
+template <bool kFull>
+__device__ __forceinline__ void seg_rows32(uint32_t* s_cnt, uint32_t* s_lo, int32_t* s_hi, int e0, int e1, bool has0,
+                                           bool has1, const uint32_t (&wa)[8], const uint32_t (&wc)[8], uint32_t qlo,
+                                           int32_t qhi, uint32_t valid) {
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    if (!kFull && !(valid >> i & 1u)) continue;  // warp-uniform
+    const uint32_t l = __shfl_sync(0xffffffffu, qlo, i);
+    const int32_t h = __shfl_sync(0xffffffffu, qhi, i);
+    if (has0) add_entry(s_cnt, s_lo, s_hi, e0 + (((wa[i >> 2] >> (8 * (i & 3))) & 0xffu) << 5), l, h);
+    if (has1) add_entry(s_cnt, s_lo, s_hi, e1 + (((wc[i >> 2] >> (8 * (i & 3))) & 0xffu) << 5), l, h);
+  }
 }
 
 template <typename GT>
@@ -106,71 +132,59 @@ __global__ void __launch_bounds__(kSegThreads, 1)
   const int f_lo = blockIdx.y * group_feats;
   const int nf = min(group_feats, F - f_lo);
   if (nf <= 0) return;
-  const int entries = group_feats * kBins;
+  const int entries = ((group_feats + 31) >> 5) * kHalfWords;
   uint32_t* s_cnt = reinterpret_cast<uint32_t*>(smem);
   uint32_t* s_lo = s_cnt + entries;
   int32_t* s_hi = reinterpret_cast<int32_t*>(s_lo + entries);
-  for (int e = threadIdx.x; e < entries; e += blockDim.x) {
-    s_cnt[e] = 0;
-    s_lo[e] = 0;
-    s_hi[e] = 0;
+  for (int e = threadIdx.x * 4; e < entries; e += blockDim.x * 4) {
+    *reinterpret_cast<uint4*>(s_cnt + e) = make_uint4(0, 0, 0, 0);
+    *reinterpret_cast<uint4*>(s_lo + e) = make_uint4(0, 0, 0, 0);
+    *reinterpret_cast<uint4*>(s_hi + e) = make_uint4(0, 0, 0, 0);
   }
   __syncthreads();
   const gbdt_segment sg = seg[slot];
   const int64_t p0 = sg.start + static_cast<int64_t>(c - chunk_start[lo]) * chunk_rows;
   const int64_t p1 = min(sg.start + sg.count, p0 + chunk_rows);
   const double scale = ldexp(1.0, *fixed_exp);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, n_warps = blockDim.x >> 5;
+  const bool has0 = lane < nf, has1 = lane + 32 < nf;
+  const uint8_t* col0 = bins + static_cast<int64_t>(f_lo + (has0 ? lane : 0)) * ldb;
+  const uint8_t* col1 = bins + static_cast<int64_t>(f_lo + (has1 ? lane + 32 : 0)) * ldb;
+  const int e0 = lane, e1 = kHalfWords + lane;
 
-  // aligned 16-position blocks covering [p0, p1); positions outside are masked
-  for (int64_t b = (p0 >> 4) + threadIdx.x; (b << 4) < p1; b += blockDim.x) {
-    const int64_t r0 = b << 4;
-    uint32_t valid = 0;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) valid |= (r0 + i >= p0 && r0 + i < p1) ? (1u << i) : 0u;
-    int64_t q[16];
-    if (r0 + 16 <= N) {
-      if (sizeof(GT) == 8) {
-        const double2* gp = reinterpret_cast<const double2*>(g + r0);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const double2 v = __ldg(gp + i);
-          q[2 * i] = to_fixed(v.x, scale);
-          q[2 * i + 1] = to_fixed(v.y, scale);
-        }
-      } else {
-        const float4* gp = reinterpret_cast<const float4*>(g + r0);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float4 v = __ldg(gp + i);
-          q[4 * i] = to_fixed(v.x, scale);
-          q[4 * i + 1] = to_fixed(v.y, scale);
-          q[4 * i + 2] = to_fixed(v.z, scale);
-          q[4 * i + 3] = to_fixed(v.w, scale);
-        }
-      }
-    } else {
-#pragma unroll
-      for (int i = 0; i < 16; ++i) q[i] = (valid >> i & 1u) ? to_fixed(static_cast<double>(g[r0 + i]), scale) : 0;
+  // aligned 32-position blocks covering [p0, p1); positions outside are masked
+  for (int64_t b = (p0 >> 5) + warp; (b << 5) < p1; b += n_warps) {
+    const int64_t r0 = b << 5;
+    const int64_t pr = r0 + lane;
+    const bool v = pr >= p0 && pr < p1;
+    const uint32_t valid = __ballot_sync(0xffffffffu, v);
+    const int64_t q = v ? to_fixed(static_cast<double>(g[pr]), scale) : 0;
+    const uint32_t qlo = static_cast<uint32_t>(static_cast<uint64_t>(q));
+    const int32_t qhi = static_cast<int32_t>(q >> 32);
+    const bool second = r0 + 16 < p1;  // any row of the block's upper half is in range
+    uint4 a0 = make_uint4(0, 0, 0, 0), a1 = a0, c0 = a0, c1 = a0;
+    if (has0) {
+      a0 = __ldg(reinterpret_cast<const uint4*>(col0 + r0));
+      if (second) a1 = __ldg(reinterpret_cast<const uint4*>(col0 + r0 + 16));
     }
-    for (int fl = 0; fl < nf; ++fl) {
-      const uint4 bv = __ldg(reinterpret_cast<const uint4*>(bins + static_cast<int64_t>(f_lo + fl) * ldb + r0));
-      const uint32_t words[4] = {bv.x, bv.y, bv.z, bv.w};
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        if (valid >> i & 1u) {
-          const int bin = (words[i >> 2] >> (8 * (i & 3))) & 0xff;
-          add_entry(s_cnt, s_lo, s_hi, (fl << 8) | bin, q[i]);
-        }
-      }
+    if (has1) {
+      c0 = __ldg(reinterpret_cast<const uint4*>(col1 + r0));
+      if (second) c1 = __ldg(reinterpret_cast<const uint4*>(col1 + r0 + 16));
     }
+    const uint32_t wa[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+    const uint32_t wc[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+    if (valid == 0xffffffffu) seg_rows32<true>(s_cnt, s_lo, s_hi, e0, e1, has0, has1, wa, wc, qlo, qhi, valid);
+    else seg_rows32<false>(s_cnt, s_lo, s_hi, e0, e1, has0, has1, wa, wc, qlo, qhi, valid);
   }
   __syncthreads();
-  const int used = nf * kBins;
-  for (int e = threadIdx.x; e < used; e += blockDim.x) {
+  for (int e = threadIdx.x; e < entries; e += blockDim.x) {
+    const int j = ((e / kHalfWords) << 5) + (e & 31);  // feature within the group
+    if (j >= nf) continue;
     const uint32_t cn = s_cnt[e];
     if (cn == 0) continue;
+    const int bin = (e >> 5) & (kBins - 1);
     const int64_t v = static_cast<int64_t>(s_hi[e]) * 4294967296ll + static_cast<int64_t>(s_lo[e]);
-    const int64_t o = (static_cast<int64_t>(slot) * F + f_lo + (e >> 8)) * kBins + (e & 0xff);
+    const int64_t o = (static_cast<int64_t>(slot) * F + f_lo + j) * kBins + bin;
     atomicAdd(hist_cnt + o, cn);
     atomicAdd(reinterpret_cast<unsigned long long*>(hist_q + o), static_cast<unsigned long long>(v));
   }
@@ -539,7 +553,7 @@ SegHistPlan plan_seg_histograms(int64_t N, int32_t F, int32_t max_slots, int32_t
   if (cr < 32768) cr = 32768;
   p.chunk_rows = (cr + 15) / 16 * 16;
   p.max_chunks = ceil_div(N, p.chunk_rows) + (max_build < max_slots ? max_build : max_slots);
-  p.smem = static_cast<size_t>(p.group_feats) * kBins * 12;
+  p.smem = static_cast<size_t>(ceil_div(p.group_feats, 32)) * kHalfWords * 12;
   return p;
 }
 
