@@ -76,38 +76,139 @@ __global__ void seg_chunk_setup_kernel(const gbdt_level* __restrict__ level, int
   }
 }
 
-// One exact fixed-point update of the entry at word e (count, low word with
-// the carry taken from the returned old value, high word when it changes).
-__device__ __forceinline__ void add_entry(uint32_t* s_cnt, uint32_t* s_lo, int32_t* s_hi, int e, uint32_t ql,
-                                          int32_t qh) {
-  atomicAdd(s_cnt + e, 1u);
-  const uint32_t old = atomicAdd(s_lo + e, ql);
-  qh += (old + ql < old) ? 1 : 0;  // carry out of the low word
-  if (qh != 0) atomicAdd(s_hi + e, qh);
+// Lane = feature: a warp takes 32 consecutive rows at a time and each lane adds
+// those rows of one feature per group half (features j and j + 32), so the 32
+// lanes of one atomic instruction update 32 different features' histograms.
+// The shared histograms are stored bin-major with the lane innermost (word
+// (half * 256 + bin) * 32 + lane for feature half * 32 + lane): every word a
+// lane touches lies in the lane's own bank, so an atomic instruction is one
+// shared-memory wavefront whatever the bins are.  Lanes with no feature in a
+// half add to that half's unused entries (bin 0 of a feature past the group),
+// which are never flushed: this keeps the update branch-free and costs no
+// extra wavefront.  The fixed-point gradients of a 32-row block are staged
+// per warp in shared memory and read back two rows per broadcast load.
+constexpr int kHalfWords = kBins * 32;
+constexpr uint32_t kHalfBytes = kHalfWords * 4;
+
+// One exact fixed-point update: count, low word (the returned old value gives
+// the carry), high word when high part + carry is non-zero.  addr is the
+// shared-memory byte address of the entry's count word; the low and high
+// words sit kLo and kHi bytes above it.
+template <uint32_t kLo, uint32_t kHi>
+__device__ __forceinline__ void add_entry(uint32_t addr, uint32_t ql, int32_t qh) {
+  asm volatile(
+      "{\n\t"
+      ".reg .u32 o, t;\n\t"
+      ".reg .pred p;\n\t"
+      "red.shared.add.u32 [%0], 1;\n\t"
+      "atom.shared.add.u32 o, [%0+%3], %1;\n\t"
+      "add.cc.u32 t, o, %1;\n\t"
+      "addc.s32 t, %2, 0;\n\t"
+      "setp.ne.s32 p, t, 0;\n\t"
+      "@p red.shared.add.s32 [%0+%4], t;\n\t"
+      "}" ::"r"(addr),
+      "r"(ql), "r"(qh), "n"(kLo), "n"(kHi)
+      : "memory");
 }
 
-// Lane = feature: a warp takes 32 consecutive rows at a time and each lane adds
-// those rows of one feature (two features when the group has more than 32),
-// so the 32 lanes of one atomic instruction update 32 different features'
-// histograms.  The shared histograms are stored bin-major with the lane
-// innermost (word (half * 256 + bin) * 32 + lane for feature half * 32 + lane),
-// so every word a lane touches lies in the lane's own bank: an atomic
-// instruction is one shared-memory wavefront whatever the bins are, with no
-// bank conflicts and no same-address serialisation.  Gradients are loaded
-// once per warp (lane = row) and broadcast with shuffles.
-constexpr int kHalfWords = kBins * 32;
+// Byte k of w times 128 (the byte stride between bins) plus base.
+template <int k>
+__device__ __forceinline__ uint32_t bin_addr(uint32_t w, uint32_t base) {
+  return base + (__byte_perm(w, 0u, 0x4440u | k) << 7);
+}
 
-template <bool kFull>
-__device__ __forceinline__ void seg_rows32(uint32_t* s_cnt, uint32_t* s_lo, int32_t* s_hi, int e0, int e1, bool has0,
-                                           bool has1, const uint32_t (&wa)[8], const uint32_t (&wc)[8], uint32_t qlo,
-                                           int32_t qhi, uint32_t valid) {
+template <int NH, bool kFull>
+__device__ __forceinline__ void seg_rows32(uint32_t base, const uint32_t (&w)[NH][8], const uint4* s_q,
+                                           uint32_t valid) {
+  constexpr uint32_t kLo = NH * kHalfBytes, kHi = 2 * NH * kHalfBytes;
 #pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    if (!kFull && !(valid >> i & 1u)) continue;  // warp-uniform
-    const uint32_t l = __shfl_sync(0xffffffffu, qlo, i);
-    const int32_t h = __shfl_sync(0xffffffffu, qhi, i);
-    if (has0) add_entry(s_cnt, s_lo, s_hi, e0 + (((wa[i >> 2] >> (8 * (i & 3))) & 0xffu) << 5), l, h);
-    if (has1) add_entry(s_cnt, s_lo, s_hi, e1 + (((wc[i >> 2] >> (8 * (i & 3))) & 0xffu) << 5), l, h);
+  for (int i = 0; i < 32; i += 2) {
+    if (!kFull && !(valid >> i & 3u)) continue;  // warp-uniform
+    const uint4 qq = s_q[i >> 1];  // rows i and i + 1: (low, high, low, high)
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      if (!kFull && !(valid >> (i + r) & 1u)) continue;
+      const uint32_t ql = r ? qq.z : qq.x;
+      const int32_t qh = static_cast<int32_t>(r ? qq.w : qq.y);
+#pragma unroll
+      for (int h = 0; h < NH; ++h) {
+        const uint32_t wd = w[h][(i + r) >> 2];
+        const uint32_t hb = base + h * kHalfBytes;
+        uint32_t a;
+        switch ((i + r) & 3) {
+          case 0: a = bin_addr<0>(wd, hb); break;
+          case 1: a = bin_addr<1>(wd, hb); break;
+          case 2: a = bin_addr<2>(wd, hb); break;
+          default: a = bin_addr<3>(wd, hb); break;
+        }
+        add_entry<kLo, kHi>(a, ql, qh);
+      }
+    }
+  }
+}
+
+template <typename GT, int NH>
+__device__ __forceinline__ void seg_hist_body(unsigned char* smem, const uint8_t* __restrict__ bins, int64_t ldb,
+                                              int32_t F, const GT* __restrict__ g, double scale, int64_t p0,
+                                              int64_t p1, int slot, int f_lo, int nf, uint32_t* __restrict__ hist_cnt,
+                                              int64_t* __restrict__ hist_q) {
+  constexpr int entries = NH * kHalfWords;
+  uint32_t* s_cnt = reinterpret_cast<uint32_t*>(smem);
+  uint32_t* s_lo = s_cnt + entries;
+  int32_t* s_hi = reinterpret_cast<int32_t*>(s_lo + entries);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, n_warps = blockDim.x >> 5;
+  uint4* s_q = reinterpret_cast<uint4*>(s_hi + entries) + warp * 16;  // 32 rows x (low, high)
+  for (int e = threadIdx.x * 4; e < entries; e += blockDim.x * 4) {
+    *reinterpret_cast<uint4*>(s_cnt + e) = make_uint4(0, 0, 0, 0);
+    *reinterpret_cast<uint4*>(s_lo + e) = make_uint4(0, 0, 0, 0);
+    *reinterpret_cast<uint4*>(s_hi + e) = make_uint4(0, 0, 0, 0);
+  }
+  __syncthreads();
+  const uint32_t base = static_cast<uint32_t>(__cvta_generic_to_shared(s_cnt)) + lane * 4;
+  bool has[NH];
+  const uint8_t* col[NH];
+#pragma unroll
+  for (int h = 0; h < NH; ++h) {
+    has[h] = h * 32 + lane < nf;
+    col[h] = bins + static_cast<int64_t>(f_lo + (has[h] ? h * 32 + lane : 0)) * ldb;
+  }
+  // aligned 32-position blocks covering [p0, p1); positions outside are masked
+  for (int64_t b = (p0 >> 5) + warp; (b << 5) < p1; b += n_warps) {
+    const int64_t r0 = b << 5;
+    const int64_t pr = r0 + lane;
+    const bool v = pr >= p0 && pr < p1;
+    const uint32_t valid = __ballot_sync(0xffffffffu, v);
+    const int64_t q = v ? to_fixed(static_cast<double>(g[pr]), scale) : 0;
+    const bool second = r0 + 16 < p1;  // any row of the block's upper half is in range
+    uint32_t w[NH][8];
+#pragma unroll
+    for (int h = 0; h < NH; ++h) {
+      uint4 x0 = make_uint4(0, 0, 0, 0), x1 = x0;
+      if (has[h]) {
+        x0 = __ldg(reinterpret_cast<const uint4*>(col[h] + r0));
+        if (second) x1 = __ldg(reinterpret_cast<const uint4*>(col[h] + r0 + 16));
+      }
+      w[h][0] = x0.x, w[h][1] = x0.y, w[h][2] = x0.z, w[h][3] = x0.w;
+      w[h][4] = x1.x, w[h][5] = x1.y, w[h][6] = x1.z, w[h][7] = x1.w;
+    }
+    __syncwarp();
+    reinterpret_cast<uint2*>(s_q)[lane] =
+        make_uint2(static_cast<uint32_t>(static_cast<uint64_t>(q)), static_cast<uint32_t>(q >> 32));
+    __syncwarp();
+    if (valid == 0xffffffffu) seg_rows32<NH, true>(base, w, s_q, valid);
+    else seg_rows32<NH, false>(base, w, s_q, valid);
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < entries; e += blockDim.x) {
+    const int j = ((e / kHalfWords) << 5) + (e & 31);  // feature within the group
+    if (j >= nf) continue;
+    const uint32_t cn = s_cnt[e];
+    if (cn == 0) continue;
+    const int bin = (e >> 5) & (kBins - 1);
+    const int64_t v = static_cast<int64_t>(s_hi[e]) * 4294967296ll + static_cast<int64_t>(s_lo[e]);
+    const int64_t o = (static_cast<int64_t>(slot) * F + f_lo + j) * kBins + bin;
+    atomicAdd(hist_cnt + o, cn);
+    atomicAdd(reinterpret_cast<unsigned long long*>(hist_q + o), static_cast<unsigned long long>(v));
   }
 }
 
@@ -132,62 +233,14 @@ __global__ void __launch_bounds__(kSegThreads, 1)
   const int f_lo = blockIdx.y * group_feats;
   const int nf = min(group_feats, F - f_lo);
   if (nf <= 0) return;
-  const int entries = ((group_feats + 31) >> 5) * kHalfWords;
-  uint32_t* s_cnt = reinterpret_cast<uint32_t*>(smem);
-  uint32_t* s_lo = s_cnt + entries;
-  int32_t* s_hi = reinterpret_cast<int32_t*>(s_lo + entries);
-  for (int e = threadIdx.x * 4; e < entries; e += blockDim.x * 4) {
-    *reinterpret_cast<uint4*>(s_cnt + e) = make_uint4(0, 0, 0, 0);
-    *reinterpret_cast<uint4*>(s_lo + e) = make_uint4(0, 0, 0, 0);
-    *reinterpret_cast<uint4*>(s_hi + e) = make_uint4(0, 0, 0, 0);
-  }
-  __syncthreads();
   const gbdt_segment sg = seg[slot];
   const int64_t p0 = sg.start + static_cast<int64_t>(c - chunk_start[lo]) * chunk_rows;
   const int64_t p1 = min(sg.start + sg.count, p0 + chunk_rows);
   const double scale = ldexp(1.0, *fixed_exp);
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, n_warps = blockDim.x >> 5;
-  const bool has0 = lane < nf, has1 = lane + 32 < nf;
-  const uint8_t* col0 = bins + static_cast<int64_t>(f_lo + (has0 ? lane : 0)) * ldb;
-  const uint8_t* col1 = bins + static_cast<int64_t>(f_lo + (has1 ? lane + 32 : 0)) * ldb;
-  const int e0 = lane, e1 = kHalfWords + lane;
-
-  // aligned 32-position blocks covering [p0, p1); positions outside are masked
-  for (int64_t b = (p0 >> 5) + warp; (b << 5) < p1; b += n_warps) {
-    const int64_t r0 = b << 5;
-    const int64_t pr = r0 + lane;
-    const bool v = pr >= p0 && pr < p1;
-    const uint32_t valid = __ballot_sync(0xffffffffu, v);
-    const int64_t q = v ? to_fixed(static_cast<double>(g[pr]), scale) : 0;
-    const uint32_t qlo = static_cast<uint32_t>(static_cast<uint64_t>(q));
-    const int32_t qhi = static_cast<int32_t>(q >> 32);
-    const bool second = r0 + 16 < p1;  // any row of the block's upper half is in range
-    uint4 a0 = make_uint4(0, 0, 0, 0), a1 = a0, c0 = a0, c1 = a0;
-    if (has0) {
-      a0 = __ldg(reinterpret_cast<const uint4*>(col0 + r0));
-      if (second) a1 = __ldg(reinterpret_cast<const uint4*>(col0 + r0 + 16));
-    }
-    if (has1) {
-      c0 = __ldg(reinterpret_cast<const uint4*>(col1 + r0));
-      if (second) c1 = __ldg(reinterpret_cast<const uint4*>(col1 + r0 + 16));
-    }
-    const uint32_t wa[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-    const uint32_t wc[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-    if (valid == 0xffffffffu) seg_rows32<true>(s_cnt, s_lo, s_hi, e0, e1, has0, has1, wa, wc, qlo, qhi, valid);
-    else seg_rows32<false>(s_cnt, s_lo, s_hi, e0, e1, has0, has1, wa, wc, qlo, qhi, valid);
-  }
-  __syncthreads();
-  for (int e = threadIdx.x; e < entries; e += blockDim.x) {
-    const int j = ((e / kHalfWords) << 5) + (e & 31);  // feature within the group
-    if (j >= nf) continue;
-    const uint32_t cn = s_cnt[e];
-    if (cn == 0) continue;
-    const int bin = (e >> 5) & (kBins - 1);
-    const int64_t v = static_cast<int64_t>(s_hi[e]) * 4294967296ll + static_cast<int64_t>(s_lo[e]);
-    const int64_t o = (static_cast<int64_t>(slot) * F + f_lo + j) * kBins + bin;
-    atomicAdd(hist_cnt + o, cn);
-    atomicAdd(reinterpret_cast<unsigned long long*>(hist_q + o), static_cast<unsigned long long>(v));
-  }
+  if (group_feats > 32)
+    seg_hist_body<GT, 2>(smem, bins, ldb, F, g, scale, p0, p1, slot, f_lo, nf, hist_cnt, hist_q);
+  else
+    seg_hist_body<GT, 1>(smem, bins, ldb, F, g, scale, p0, p1, slot, f_lo, nf, hist_cnt, hist_q);
 }
 
 // ---------------------------------------------------------------------------------------- partition
@@ -553,7 +606,7 @@ SegHistPlan plan_seg_histograms(int64_t N, int32_t F, int32_t max_slots, int32_t
   if (cr < 32768) cr = 32768;
   p.chunk_rows = (cr + 15) / 16 * 16;
   p.max_chunks = ceil_div(N, p.chunk_rows) + (max_build < max_slots ? max_build : max_slots);
-  p.smem = static_cast<size_t>(ceil_div(p.group_feats, 32)) * kHalfWords * 12;
+  p.smem = static_cast<size_t>(ceil_div(p.group_feats, 32)) * kHalfWords * 12 + (kSegThreads / 32) * 256;
   return p;
 }
 
