@@ -81,6 +81,12 @@ void launch_move_rows(const uint8_t* bins_in, uint8_t* bins_out, int64_t ldb, in
                       const uint8_t* go_right, const gbdt_level* level, int32_t max_slots, const gbdt_segment* seg,
                       const Route* route, const gbdt_split* splits, gbdt_segment* seg_out,
                       uint16_t* leaf_of_row, void* scratch, int32_t* err, cudaStream_t s);
+// Last split level: record every row's leaf (its child, or its own node when
+// its slot did not split) without moving any data.  Needs route from the
+// level's splits; scratch is move_scratch_bytes(N, max_slots).
+void launch_leaf_rows(const uint8_t* bins_in, int64_t ldb, int64_t N, const uint32_t* orig_in,
+                      const uint8_t* go_right, const gbdt_level* level, int32_t max_slots, const gbdt_segment* seg,
+                      const Route* route, uint16_t* leaf_of_row, void* scratch, cudaStream_t s);
 
 // node_of_row[r] = left_node + (bins[feature][r] > bin) for rows of slots with a split.
 void launch_route_rows(const uint8_t* bins, int64_t ldb, int64_t N, const Route* route, const gbdt_level* level,

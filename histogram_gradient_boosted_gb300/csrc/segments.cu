@@ -91,21 +91,21 @@ constexpr int kHalfWords = kBins * 32;
 constexpr uint32_t kHalfBytes = kHalfWords * 4;
 
 // One exact fixed-point update: count, low word (the returned old value gives
-// the carry), high word when high part + carry is non-zero.  addr is the
-// shared-memory byte address of the entry's count word; the low and high
-// words sit kLo and kHi bytes above it.
+// the carry), high word += high part + carry.  The high-word add is
+// unconditional: with the fixed-point scale the high part is non-zero for
+// almost every row, and a skipped add would cost a branch, not a wavefront.
+// addr is the shared-memory byte address of the entry's count word; the low
+// and high words sit kLo and kHi bytes above it.
 template <uint32_t kLo, uint32_t kHi>
 __device__ __forceinline__ void add_entry(uint32_t addr, uint32_t ql, int32_t qh) {
   asm volatile(
       "{\n\t"
       ".reg .u32 o, t;\n\t"
-      ".reg .pred p;\n\t"
       "red.shared.add.u32 [%0], 1;\n\t"
       "atom.shared.add.u32 o, [%0+%3], %1;\n\t"
       "add.cc.u32 t, o, %1;\n\t"
       "addc.s32 t, %2, 0;\n\t"
-      "setp.ne.s32 p, t, 0;\n\t"
-      "@p red.shared.add.s32 [%0+%4], t;\n\t"
+      "red.shared.add.s32 [%0+%4], t;\n\t"
       "}" ::"r"(addr),
       "r"(ql), "r"(qh), "n"(kLo), "n"(kHi)
       : "memory");
@@ -553,6 +553,32 @@ __global__ void __launch_bounds__(kMvThreads, 4)
   }
 }
 
+// Last split level: the children are leaves, so nothing moves.  Every row
+// records its leaf: the child its split sends it to, or the slot's own node
+// when the slot did not split.
+__global__ void __launch_bounds__(kMvThreads)
+    mv_leaves_kernel(const uint8_t* __restrict__ bins_in, int64_t ldb, const uint32_t* __restrict__ orig_in,
+                     const uint8_t* __restrict__ go_right, const gbdt_level* __restrict__ level, int32_t max_slots,
+                     const gbdt_segment* __restrict__ seg, const Route* __restrict__ route,
+                     const int32_t* __restrict__ tile_start, const MvState* __restrict__ st,
+                     uint16_t* __restrict__ leaf_of_row) {
+  const int t = blockIdx.x;
+  if (t >= st->total_tiles) return;
+  const int n_slots = min(level->n_slots, max_slots);
+  const int s = slot_of_tile(tile_start, n_slots, t);
+  const Route rt = route[s];
+  const int64_t p0 = seg[s].start + static_cast<int64_t>(t - tile_start[s]) * kMvTile;
+  const int n = static_cast<int>(min(seg[s].start + seg[s].count - p0, static_cast<int64_t>(kMvTile)));
+  if (rt.feature < 0) {
+    const uint16_t node = static_cast<uint16_t>(level->node_begin + s);
+    for (int i = threadIdx.x; i < n; i += blockDim.x) leaf_of_row[orig_in[p0 + i]] = node;
+    return;
+  }
+  const uint8_t* col = bins_in + static_cast<int64_t>(rt.feature) * ldb;
+  for (int i = threadIdx.x; i < n; i += blockDim.x)
+    leaf_of_row[orig_in[p0 + i]] = static_cast<uint16_t>(rt.left_node + goes_right(col, rt.bin, go_right, p0 + i));
+}
+
 // One CTA: routing of every slot from its split record; the k-th splitting slot
 // (in slot order) gets child slots 2k, 2k+1 of the next level.
 __global__ void routes_from_splits_kernel(const gbdt_split* __restrict__ splits, const gbdt_level* __restrict__ level,
@@ -672,6 +698,20 @@ void launch_move_rows(const uint8_t* bins_in, uint8_t* bins_out, int64_t ldb, in
                                              go_right,
                                              level, max_slots, seg, route, tile_start, st, tile_excl, seg_left,
                                              leaf_of_row);
+  count_launches();
+}
+
+void launch_leaf_rows(const uint8_t* bins_in, int64_t ldb, int64_t N, const uint32_t* orig_in,
+                      const uint8_t* go_right, const gbdt_level* level, int32_t max_slots, const gbdt_segment* seg,
+                      const Route* route, uint16_t* leaf_of_row, void* scratch, cudaStream_t s) {
+  Carve c(scratch, move_scratch_bytes(N, max_slots));
+  MvState* st = c.take<MvState>(1);
+  int32_t* tile_start = c.take<int32_t>(max_slots + 1);
+  const int max_tiles = ceil_div(N, kMvTile) + max_slots;
+  mv_setup_kernel<<<1, 1024, 0, s>>>(level, max_slots, seg, tile_start, st);
+  count_launches();
+  mv_leaves_kernel<<<max_tiles, kMvThreads, 0, s>>>(bins_in, ldb, orig_in, go_right, level, max_slots, seg, route,
+                                                    tile_start, st, leaf_of_row);
   count_launches();
 }
 

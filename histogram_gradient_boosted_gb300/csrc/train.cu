@@ -383,11 +383,18 @@ extern "C" int gbdt_train(const uint8_t* bins, int64_t ldb, const int32_t* n_bin
                                             w.n_nodes + t, w.level[nxt], w.totals[nxt], w.seg[nxt], w.pair_parent,
                                             w.build[nxt], w.route, st, w.err);
       count_launches();
-      // move the rows of split nodes into child order; frozen nodes record their rows' leaf
+      // move the rows of split nodes into child order; frozen nodes record their rows' leaf.  At the last
+      // split level the children are leaves: rows only record them, nothing moves (and at the leaf level
+      // itself there is then nothing left to do, except for a tree that is a single leaf).
       if (timing) GBDT_CUDA(cudaEventRecord(ev_hist(t, d, 2), s));
-      launch_move_rows(lb, d < D ? w.bins_xy[d & 1] : nullptr, ldb, N, F, lg, d < D ? w.g_xy[d & 1] : nullptr, 8, lo,
-                       d < D ? w.orig_xy[d & 1] : nullptr, nullptr, w.level[cur], max_slots, w.seg[cur], w.route,
-                       d < D ? w.splits : nullptr, nullptr, w.leaf, w.move_scratch, w.err, s);
+      if (d + 1 < D) {
+        launch_move_rows(lb, w.bins_xy[d & 1], ldb, N, F, lg, w.g_xy[d & 1], 8, lo, w.orig_xy[d & 1], nullptr,
+                         w.level[cur], max_slots, w.seg[cur], w.route, w.splits, nullptr, w.leaf, w.move_scratch,
+                         w.err, s);
+      } else if (d + 1 == D || D == 0) {
+        launch_leaf_rows(lb, ldb, N, lo, nullptr, w.level[cur], max_slots, w.seg[cur], w.route, w.leaf,
+                         w.move_scratch, s);
+      }
       if (timing) GBDT_CUDA(cudaEventRecord(ev_hist(t, d, 3), s));
       GBDT_LAUNCH_CHECK();
       ++levels_done;
@@ -472,7 +479,10 @@ extern "C" int gbdt_train(const uint8_t* bins, int64_t ldb, const int32_t* n_bin
         }
         GBDT_CUDA(cudaEventElapsedTime(&ms, ev_hist(t, d, 2), ev_hist(t, d, 3)));
         dg.part_ms += ms;
-        dg.part_bytes += static_cast<double>(ls.n_split_rows) * move_bytes +
+        // moved rows read and write every column; a row that only records its leaf reads its row id (and
+        // the split column, when its slot split) and writes a 2-byte leaf id
+        const bool moves = d + 1 < D;
+        dg.part_bytes += static_cast<double>(ls.n_split_rows) * (moves ? move_bytes : 7.0) +
                          static_cast<double>(ls.n_act - ls.n_split_rows) * 6.0;
       }
       if (h_n[t] == M) dg.trees_at_full_size += 1;
