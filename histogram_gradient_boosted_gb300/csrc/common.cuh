@@ -21,6 +21,7 @@ enum : int32_t {
   kErrSlotRange = 2,      // a row's node id is outside the level it should be in
   kErrPartitionCount = 4, // partition left count differs from the split record
   kErrLevelSize = 8,      // a level has more slots than the launch bound
+  kErrWaitTimeout = 16,   // an asynchronous copy did not complete within its wait limit
 };
 
 // ---- thread-local error message -------------------------------------------------
@@ -87,6 +88,51 @@ __host__ __device__ inline double from_fixed(int64_t q, int S) { return ldexp(st
 
 __device__ __forceinline__ void raise_error(int32_t* flag, int32_t bits) {
   if (flag) atomicOr(flag, bits);
+}
+
+// ---- bulk asynchronous copies (global -> shared memory) completed on an mbarrier
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t arrivals) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(arrivals) : "memory");
+}
+
+// Make initialised mbarriers visible to the asynchronous (copy) proxy.
+__device__ __forceinline__ void mbar_init_fence() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
+
+// Copy `bytes` (a multiple of 16; both addresses 16-byte aligned) from global
+// to shared memory; the copy's completion is one phase of `bar`, which this
+// call arms with the expected byte count.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "{\n\t.reg .b64 st;\n\t"
+      "mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(smem_u32(bar)),
+      "r"(bytes)
+      : "memory");
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_u32(dst)),
+               "l"(src), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
+
+// Wait until the phase with parity `parity` of bar has completed.  Gives up
+// after `limit` polls and returns false, so that no wait can hang.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t limit) {
+  const uint32_t a = smem_u32(bar);
+  for (uint32_t i = 0; i < limit; ++i) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(a), "r"(parity)
+        : "memory");
+    if (done) return true;
+  }
+  return false;
 }
 
 inline int ceil_div(int64_t a, int64_t b) { return static_cast<int>((a + b - 1) / b); }

@@ -395,15 +395,40 @@ __global__ void __launch_bounds__(1024)
 // Output-centric move.  Once per tile: the rows' decisions (lane = row,
 // ballots), their ranks, and the inverse permutation inv[o] = tile position of
 // the o-th output row (left rows first, then right rows) in shared memory.
-// Each thread then owns up to kMvWordsPerThread aligned 4-byte words of the
-// tile's two output runs and keeps, in registers, the source positions of
-// their bytes.  Per column the tile is staged in shared memory with 16-byte
-// loads, and every output word is gathered from the stage and written with one
+// The gradient and the row id move one output position per thread, in
+// batches of independent loads.  For the bin columns each thread owns up to
+// kMvWordsPerThread aligned 4-byte words of the tile's two output runs and
+// keeps, in registers, the source positions of their bytes; every output word
+// is gathered from the column's tile in shared memory and written with one
 // aligned 4-byte store (byte stores only where a run starts or ends inside a
-// word), so stores fill whole sectors.
+// word), so stores fill whole sectors.  The column tiles arrive by bulk
+// asynchronous copies, kMvStages columns ahead of the one being gathered, so
+// the loads of later columns overlap the gathers and stores of earlier ones.
 constexpr int kMvChunks = kMvTile / 32;
 constexpr int kMvChunksPerWarp = kMvChunks / (kMvThreads / 32);
 constexpr int kMvWordsPerThread = (kMvTile / 4 + 4 + kMvThreads - 1) / kMvThreads;  // 5: both runs, edges included
+constexpr int kMvStages = 4;
+constexpr int kMvStageBytes = kMvTile + 16;  // a tile plus its 16-byte alignment slack
+constexpr uint32_t kMvWaitPolls = 1u << 20;
+
+template <typename T>
+__device__ __forceinline__ void move_positions(const T* __restrict__ in, T* __restrict__ out, int64_t p0, int n,
+                                               int nl, int64_t dst_l, int64_t dst_r, const uint16_t* s_inv) {
+  constexpr int U = 8;
+  for (int o0 = threadIdx.x; o0 < n; o0 += U * kMvThreads) {
+    T v[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int o = o0 + u * kMvThreads;
+      if (o < n) v[u] = in[p0 + s_inv[o]];
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int o = o0 + u * kMvThreads;
+      if (o < n) out[o < nl ? dst_l + o : dst_r + (o - nl)] = v[u];
+    }
+  }
+}
 
 __global__ void __launch_bounds__(kMvThreads, 4)
     mv_move_kernel(const uint8_t* __restrict__ bins_in, uint8_t* __restrict__ bins_out, int64_t ldb, int32_t F,
@@ -413,12 +438,13 @@ __global__ void __launch_bounds__(kMvThreads, 4)
                    const gbdt_segment* __restrict__ seg, const Route* __restrict__ route,
                    const int32_t* __restrict__ tile_start, const MvState* __restrict__ st,
                    const int64_t* __restrict__ tile_excl, const int64_t* __restrict__ seg_left,
-                   uint16_t* __restrict__ leaf_of_row) {
+                   uint16_t* __restrict__ leaf_of_row, int32_t* __restrict__ err) {
   __shared__ uint32_t s_right[kMvChunks];
   __shared__ uint32_t s_valid[kMvChunks];
   __shared__ int s_lbase[kMvChunks];
   __shared__ uint16_t s_inv[kMvTile];
-  __shared__ __align__(16) uint8_t s_stage[kMvTile + 32];
+  __shared__ __align__(128) uint8_t s_stage[kMvStages][kMvStageBytes];
+  __shared__ __align__(8) uint64_t s_full[kMvStages];
   __shared__ int s_warp[33];
   const int t = blockIdx.x;
   if (t >= st->total_tiles) return;
@@ -434,6 +460,15 @@ __global__ void __launch_bounds__(kMvThreads, 4)
       for (int i = threadIdx.x; i < n; i += blockDim.x) leaf_of_row[orig_in[p0 + i]] = node;
     }
     return;
+  }
+  // ---- start the first column copies: the tile's 16-byte-aligned span of each column
+  const int64_t a0 = p0 & ~int64_t(15);
+  const uint32_t span = static_cast<uint32_t>(((p0 + n + 15) & ~int64_t(15)) - a0);
+  const int a_off = static_cast<int>(p0 & 15);  // stage index of tile position 0
+  if (threadIdx.x == 0) {
+    for (int k = 0; k < kMvStages; ++k) mbar_init(&s_full[k], 1);
+    mbar_init_fence();
+    for (int c = 0; c < F && c < kMvStages; ++c) bulk_load(s_stage[c], bins_in + c * ldb + a0, span, &s_full[c]);
   }
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const uint8_t* col = bins_in + static_cast<int64_t>(rt.feature) * ldb;
@@ -473,14 +508,20 @@ __global__ void __launch_bounds__(kMvThreads, 4)
   const int64_t left_before = tile_excl[t] - tile_excl[tile_start[s]];
   const int64_t dst_l = seg[s].start + left_before;                             // this tile's left run
   const int64_t dst_r = seg[s].start + seg_left[s] + (tile_off - left_before);  // this tile's right run
+  // ---- gradient and row id, while the first column copies are in flight
+  if (g_size == 8)
+    move_positions(static_cast<const uint64_t*>(g_in), static_cast<uint64_t*>(g_out), p0, n, nl, dst_l, dst_r, s_inv);
+  else
+    move_positions(static_cast<const uint32_t*>(g_in), static_cast<uint32_t*>(g_out), p0, n, nl, dst_l, dst_r, s_inv);
+  move_positions(orig_in, orig_out, p0, n, nl, dst_l, dst_r, s_inv);
   // ---- the output words this thread owns: left run words, then right run words
   const int64_t wl0 = dst_l >> 2, wr0 = dst_r >> 2;
   const int nwl = nl > 0 ? static_cast<int>(((dst_l + nl + 3) >> 2) - wl0) : 0;
   const int nwr = nr > 0 ? static_cast<int>(((dst_r + nr + 3) >> 2) - wr0) : 0;
   const int ol = static_cast<int>(dst_l & 3), orr = static_cast<int>(dst_r & 3);  // run start inside its first word
   int wrel[kMvWordsPerThread];       // word offset within its run's words; bit 30: right run; -1: none
-  uint32_t srcl[kMvWordsPerThread];  // tile positions of bytes 0,1 (16 bits each; 0xffff: not written)
-  uint32_t srch[kMvWordsPerThread];  // tile positions of bytes 2,3
+  uint32_t srcl[kMvWordsPerThread];  // stage positions of bytes 0,1 (16 bits each; 0xffff: not written)
+  uint32_t srch[kMvWordsPerThread];  // stage positions of bytes 2,3
 #pragma unroll
   for (int m = 0; m < kMvWordsPerThread; ++m) {
     const int vw = threadIdx.x + m * kMvThreads;
@@ -493,7 +534,7 @@ __global__ void __launch_bounds__(kMvThreads, 4)
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int o = 4 * rel + i - first;  // offset in the run
-        if (o >= 0 && o < len) sp[i] = s_inv[base + o];
+        if (o >= 0 && o < len) sp[i] = s_inv[base + o] + a_off;
       }
       wr = left ? rel : (rel | 0x40000000);
     }
@@ -501,18 +542,15 @@ __global__ void __launch_bounds__(kMvThreads, 4)
     srcl[m] = sp[0] | (sp[1] << 16);
     srch[m] = sp[2] | (sp[3] << 16);
   }
-  const int a_off = static_cast<int>(p0 & 15);  // stage index of tile position 0
-  // ---- move every column
+  // ---- bin columns, each from its stage
+  int c_fail = -1;
 #pragma unroll 1
-  for (int c = 0; c < F + 2; ++c) {
-    if (c < F) {
-      const uint8_t* in = bins_in + static_cast<int64_t>(c) * ldb;
+  for (int c = 0; c < F; ++c) {
+    const int k = c % kMvStages;
+    const uint8_t* stage = s_stage[k];
+    const bool ok = mbar_wait(&s_full[k], static_cast<uint32_t>((c / kMvStages) & 1), kMvWaitPolls);
+    if (ok) {
       uint32_t* out = reinterpret_cast<uint32_t*>(bins_out + static_cast<int64_t>(c) * ldb);
-      const int64_t a0 = p0 & ~int64_t(15);
-      const int nvec = static_cast<int>((p0 + n + 15 - a0) >> 4);
-      for (int v = threadIdx.x; v < nvec; v += blockDim.x)
-        reinterpret_cast<uint4*>(s_stage)[v] = __ldg(reinterpret_cast<const uint4*>(in + a0) + v);
-      __syncthreads();
 #pragma unroll
       for (int m = 0; m < kMvWordsPerThread; ++m) {
         const int wr = wrel[m];
@@ -520,35 +558,32 @@ __global__ void __launch_bounds__(kMvThreads, 4)
         const int64_t wa = (wr & 0x40000000) ? wr0 + (wr & 0x3fffffff) : wl0 + wr;
         const uint32_t s0 = srcl[m] & 0xffffu, s1 = srcl[m] >> 16, s2 = srch[m] & 0xffffu, s3 = srch[m] >> 16;
         if (s0 != 0xffffu && s1 != 0xffffu && s2 != 0xffffu && s3 != 0xffffu) {
-          out[wa] = static_cast<uint32_t>(s_stage[a_off + s0]) | (static_cast<uint32_t>(s_stage[a_off + s1]) << 8) |
-                    (static_cast<uint32_t>(s_stage[a_off + s2]) << 16) |
-                    (static_cast<uint32_t>(s_stage[a_off + s3]) << 24);
+          out[wa] = static_cast<uint32_t>(stage[s0]) | (static_cast<uint32_t>(stage[s1]) << 8) |
+                    (static_cast<uint32_t>(stage[s2]) << 16) | (static_cast<uint32_t>(stage[s3]) << 24);
         } else {  // a run starts or ends inside this word: write only its own bytes
           uint8_t* ob = reinterpret_cast<uint8_t*>(out + wa);
-          if (s0 != 0xffffu) ob[0] = s_stage[a_off + s0];
-          if (s1 != 0xffffu) ob[1] = s_stage[a_off + s1];
-          if (s2 != 0xffffu) ob[2] = s_stage[a_off + s2];
-          if (s3 != 0xffffu) ob[3] = s_stage[a_off + s3];
+          if (s0 != 0xffffu) ob[0] = stage[s0];
+          if (s1 != 0xffffu) ob[1] = stage[s1];
+          if (s2 != 0xffffu) ob[2] = stage[s2];
+          if (s3 != 0xffffu) ob[3] = stage[s3];
         }
       }
-      __syncthreads();
-    } else {
-#pragma unroll
-      for (int m = 0; m < kMvWordsPerThread; ++m) {
-        const int wr = wrel[m];
-        if (wr < 0) continue;
-        const int64_t wa = (wr & 0x40000000) ? wr0 + (wr & 0x3fffffff) : wl0 + wr;
-#pragma unroll 1
-        for (int i = 0; i < 4; ++i) {
-          const uint32_t sv = i < 2 ? (srcl[m] >> (16 * i)) & 0xffffu : (srch[m] >> (16 * (i - 2))) & 0xffffu;
-          if (sv == 0xffffu) continue;
-          const int64_t d = (wa << 2) + i;
-          const int64_t src = p0 + sv;
-          if (c == F + 1) orig_out[d] = orig_in[src];
-          else if (g_size == 8) static_cast<uint64_t*>(g_out)[d] = static_cast<const uint64_t*>(g_in)[src];
-          else static_cast<uint32_t*>(g_out)[d] = static_cast<const uint32_t*>(g_in)[src];
-        }
-      }
+    }
+    if (__syncthreads_or(!ok)) {  // every thread is done with this stage (or a copy timed out)
+      c_fail = c;
+      break;
+    }
+    if (threadIdx.x == 0 && c + kMvStages < F)
+      bulk_load(s_stage[k], bins_in + static_cast<int64_t>(c + kMvStages) * ldb + a0, span, &s_full[k]);
+  }
+  if (c_fail >= 0 && threadIdx.x == 0) {
+    raise_error(err, kErrWaitTimeout);
+    // let the copies still in flight (columns c_fail .. issued - 1) land before the CTA's shared memory is
+    // released; each stage completes in order, so waiting for its last issued column suffices
+    const int issued = min(F, c_fail + kMvStages);
+    for (int c = c_fail; c < issued; ++c) {
+      if (c + kMvStages < issued) continue;  // a later column of the same stage is waited for instead
+      mbar_wait(&s_full[c % kMvStages], static_cast<uint32_t>((c / kMvStages) & 1), kMvWaitPolls);
     }
   }
 }
@@ -697,7 +732,7 @@ void launch_move_rows(const uint8_t* bins_in, uint8_t* bins_out, int64_t ldb, in
   mv_move_kernel<<<max_tiles, kMvThreads, 0, s>>>(bins_in, bins_out, ldb, F, g_in, g_out, g_size, orig_in, orig_out,
                                              go_right,
                                              level, max_slots, seg, route, tile_start, st, tile_excl, seg_left,
-                                             leaf_of_row);
+                                             leaf_of_row, err);
   count_launches();
 }
 
