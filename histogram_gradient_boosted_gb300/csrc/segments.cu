@@ -90,33 +90,44 @@ __global__ void seg_chunk_setup_kernel(const gbdt_level* __restrict__ level, int
 constexpr int kHalfWords = kBins * 32;
 constexpr uint32_t kHalfBytes = kHalfWords * 4;
 
-// One exact fixed-point update: count, low word (the returned old value gives
-// the carry), high word += high part + carry.  The high-word add is
-// unconditional: with the fixed-point scale the high part is non-zero for
-// almost every row, and a skipped add would cost a branch, not a wavefront.
-// addr is the shared-memory byte address of the entry's count word; the low
-// and high words sit kLo and kHi bytes above it.
-template <uint32_t kLo, uint32_t kHi>
-__device__ __forceinline__ void add_entry(uint32_t addr, uint32_t ql, int32_t qh) {
+// One exact fixed-point update, in two halves so that a warp can have several
+// updates' atomics in flight: entry_lo adds the count and the low word and
+// returns the low word's old value; entry_hi adds high part + carry (the carry
+// out of old + low) to the high word.  The high-word add is unconditional:
+// with the fixed-point scale the high part is non-zero for almost every row,
+// and a skipped add would cost a branch, not a wavefront.  addr is the
+// shared-memory byte address of the entry's count word; the low and high
+// words sit kLo and kHi bytes above it.
+template <uint32_t kLo>
+__device__ __forceinline__ uint32_t entry_lo(uint32_t addr, uint32_t ql) {
+  uint32_t old;
   asm volatile(
-      "{\n\t"
-      ".reg .u32 o, t;\n\t"
-      "red.shared.add.u32 [%0], 1;\n\t"
-      "atom.shared.add.u32 o, [%0+%3], %1;\n\t"
-      "add.cc.u32 t, o, %1;\n\t"
-      "addc.s32 t, %2, 0;\n\t"
-      "red.shared.add.s32 [%0+%4], t;\n\t"
-      "}" ::"r"(addr),
-      "r"(ql), "r"(qh), "n"(kLo), "n"(kHi)
+      "red.shared.add.u32 [%1], 1;\n\t"
+      "atom.shared.add.u32 %0, [%1+%3], %2;"
+      : "=r"(old)
+      : "r"(addr), "r"(ql), "n"(kLo)
+      : "memory");
+  return old;
+}
+
+template <uint32_t kHi>
+__device__ __forceinline__ void entry_hi(uint32_t addr, uint32_t ql, int32_t qh, uint32_t old) {
+  asm volatile(
+      "{\n\t.reg .u32 t;\n\t"
+      "add.cc.u32 t, %2, %1;\n\t"
+      "addc.s32 t, %3, 0;\n\t"
+      "red.shared.add.s32 [%0+%4], t;\n\t}" ::"r"(addr),
+      "r"(ql), "r"(old), "r"(qh), "n"(kHi)
       : "memory");
 }
 
 // Byte k of w times 128 (the byte stride between bins) plus base.
-template <int k>
-__device__ __forceinline__ uint32_t bin_addr(uint32_t w, uint32_t base) {
-  return base + (__byte_perm(w, 0u, 0x4440u | k) << 7);
+__device__ __forceinline__ uint32_t bin_addr(uint32_t w, int k, uint32_t base) {
+  return base + (__byte_perm(w, 0u, 0x4440u | static_cast<uint32_t>(k)) << 7);
 }
 
+// Rows i and i + 1 of the block, every half: the low-word atomics of all of
+// them are issued before the first carry is needed.
 template <int NH, bool kFull>
 __device__ __forceinline__ void seg_rows32(uint32_t base, const uint32_t (&w)[NH][8], const uint4* s_q,
                                            uint32_t valid) {
@@ -125,29 +136,43 @@ __device__ __forceinline__ void seg_rows32(uint32_t base, const uint32_t (&w)[NH
   for (int i = 0; i < 32; i += 2) {
     if (!kFull && !(valid >> i & 3u)) continue;  // warp-uniform
     const uint4 qq = s_q[i >> 1];  // rows i and i + 1: (low, high, low, high)
+    const bool use1 = kFull || (valid >> (i + 1) & 1u);
+    const bool use0 = kFull || (valid >> i & 1u);
+    uint32_t a[2][NH], old[2][NH];
 #pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      if (!kFull && !(valid >> (i + r) & 1u)) continue;
-      const uint32_t ql = r ? qq.z : qq.x;
-      const int32_t qh = static_cast<int32_t>(r ? qq.w : qq.y);
+    for (int r = 0; r < 2; ++r)
 #pragma unroll
-      for (int h = 0; h < NH; ++h) {
-        const uint32_t wd = w[h][(i + r) >> 2];
-        const uint32_t hb = base + h * kHalfBytes;
-        uint32_t a;
-        switch ((i + r) & 3) {
-          case 0: a = bin_addr<0>(wd, hb); break;
-          case 1: a = bin_addr<1>(wd, hb); break;
-          case 2: a = bin_addr<2>(wd, hb); break;
-          default: a = bin_addr<3>(wd, hb); break;
-        }
-        add_entry<kLo, kHi>(a, ql, qh);
-      }
+      for (int h = 0; h < NH; ++h) a[r][h] = bin_addr(w[h][(i + r) >> 2], (i + r) & 3, base + h * kHalfBytes);
+#pragma unroll
+    for (int h = 0; h < NH; ++h) {
+      if (use0) old[0][h] = entry_lo<kLo>(a[0][h], qq.x);
+      if (use1) old[1][h] = entry_lo<kLo>(a[1][h], qq.z);
+    }
+#pragma unroll
+    for (int h = 0; h < NH; ++h) {
+      if (use0) entry_hi<kHi>(a[0][h], qq.x, static_cast<int32_t>(qq.y), old[0][h]);
+      if (use1) entry_hi<kHi>(a[1][h], qq.z, static_cast<int32_t>(qq.w), old[1][h]);
     }
   }
 }
 
-template <typename GT, int NH>
+// 32 bytes of a column (rows r0 .. r0 + 31 of one feature).  With kV8 the
+// column starts are 32-byte aligned and one 256-bit load reads them all.
+template <bool kV8>
+__device__ __forceinline__ void load_rows32(const uint8_t* p, bool second, uint32_t (&w)[8]) {
+  if (kV8 && second) {
+    asm volatile("ld.global.nc.L1::no_allocate.v8.u32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]), "=r"(w[6]), "=r"(w[7])
+                 : "l"(p));
+    return;
+  }
+  const uint4 x0 = __ldg(reinterpret_cast<const uint4*>(p));
+  const uint4 x1 = second ? __ldg(reinterpret_cast<const uint4*>(p + 16)) : make_uint4(0, 0, 0, 0);
+  w[0] = x0.x, w[1] = x0.y, w[2] = x0.z, w[3] = x0.w;
+  w[4] = x1.x, w[5] = x1.y, w[6] = x1.z, w[7] = x1.w;
+}
+
+template <typename GT, int NH, bool kV8>
 __device__ __forceinline__ void seg_hist_body(unsigned char* smem, const uint8_t* __restrict__ bins, int64_t ldb,
                                               int32_t F, const GT* __restrict__ g, double scale, int64_t p0,
                                               int64_t p1, int slot, int f_lo, int nf, uint32_t* __restrict__ hist_cnt,
@@ -164,7 +189,7 @@ __device__ __forceinline__ void seg_hist_body(unsigned char* smem, const uint8_t
     *reinterpret_cast<uint4*>(s_hi + e) = make_uint4(0, 0, 0, 0);
   }
   __syncthreads();
-  const uint32_t base = static_cast<uint32_t>(__cvta_generic_to_shared(s_cnt)) + lane * 4;
+  const uint32_t base = smem_u32(s_cnt) + lane * 4;
   bool has[NH];
   const uint8_t* col[NH];
 #pragma unroll
@@ -183,13 +208,12 @@ __device__ __forceinline__ void seg_hist_body(unsigned char* smem, const uint8_t
     uint32_t w[NH][8];
 #pragma unroll
     for (int h = 0; h < NH; ++h) {
-      uint4 x0 = make_uint4(0, 0, 0, 0), x1 = x0;
       if (has[h]) {
-        x0 = __ldg(reinterpret_cast<const uint4*>(col[h] + r0));
-        if (second) x1 = __ldg(reinterpret_cast<const uint4*>(col[h] + r0 + 16));
+        load_rows32<kV8>(col[h] + r0, second, w[h]);
+      } else {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) w[h][k] = 0;
       }
-      w[h][0] = x0.x, w[h][1] = x0.y, w[h][2] = x0.z, w[h][3] = x0.w;
-      w[h][4] = x1.x, w[h][5] = x1.y, w[h][6] = x1.z, w[h][7] = x1.w;
     }
     __syncwarp();
     reinterpret_cast<uint2*>(s_q)[lane] =
@@ -212,7 +236,7 @@ __device__ __forceinline__ void seg_hist_body(unsigned char* smem, const uint8_t
   }
 }
 
-template <typename GT>
+template <typename GT, bool kV8>
 __global__ void __launch_bounds__(kSegThreads, 1)
     seg_hist_kernel(const uint8_t* __restrict__ bins, int64_t ldb, int64_t N, int32_t F, const GT* __restrict__ g,
                     const int32_t* __restrict__ fixed_exp, const gbdt_segment* __restrict__ seg,
@@ -238,9 +262,9 @@ __global__ void __launch_bounds__(kSegThreads, 1)
   const int64_t p1 = min(sg.start + sg.count, p0 + chunk_rows);
   const double scale = ldexp(1.0, *fixed_exp);
   if (group_feats > 32)
-    seg_hist_body<GT, 2>(smem, bins, ldb, F, g, scale, p0, p1, slot, f_lo, nf, hist_cnt, hist_q);
+    seg_hist_body<GT, 2, kV8>(smem, bins, ldb, F, g, scale, p0, p1, slot, f_lo, nf, hist_cnt, hist_q);
   else
-    seg_hist_body<GT, 1>(smem, bins, ldb, F, g, scale, p0, p1, slot, f_lo, nf, hist_cnt, hist_q);
+    seg_hist_body<GT, 1, kV8>(smem, bins, ldb, F, g, scale, p0, p1, slot, f_lo, nf, hist_cnt, hist_q);
 }
 
 // ---------------------------------------------------------------------------------------- partition
@@ -688,17 +712,23 @@ int launch_seg_histograms(const SegHistPlan& plan, const uint8_t* bins, int64_t 
                                             chunk_start, st);
   count_launches();
   dim3 grid(static_cast<unsigned>(plan.max_chunks), static_cast<unsigned>(plan.n_fgroups));
+  // 256-bit column loads need every column start 32-byte aligned
+  const bool v8 = aligned(bins, 32) && ldb % 32 == 0;
+  auto launch = [&](auto kernel, const auto* gp) -> int {
+    GBDT_CUDA(smem_attr(kernel, plan.smem));
+    kernel<<<grid, kSegThreads, plan.smem, s>>>(bins, ldb, N, F, gp, fixed_exp, seg, build_slot, chunk_start, st,
+                                                plan.chunk_rows, plan.group_feats, hist_cnt, hist_q);
+    return GBDT_OK;
+  };
+  int rc;
   if (g_dtype == GBDT_DTYPE_F32) {
-    GBDT_CUDA(smem_attr(seg_hist_kernel<float>, plan.smem));
-    seg_hist_kernel<float><<<grid, kSegThreads, plan.smem, s>>>(bins, ldb, N, F, static_cast<const float*>(g),
-                                                                fixed_exp, seg, build_slot, chunk_start, st,
-                                                                plan.chunk_rows, plan.group_feats, hist_cnt, hist_q);
+    const float* gp = static_cast<const float*>(g);
+    rc = v8 ? launch(seg_hist_kernel<float, true>, gp) : launch(seg_hist_kernel<float, false>, gp);
   } else {
-    GBDT_CUDA(smem_attr(seg_hist_kernel<double>, plan.smem));
-    seg_hist_kernel<double><<<grid, kSegThreads, plan.smem, s>>>(bins, ldb, N, F, static_cast<const double*>(g),
-                                                                 fixed_exp, seg, build_slot, chunk_start, st,
-                                                                 plan.chunk_rows, plan.group_feats, hist_cnt, hist_q);
+    const double* gp = static_cast<const double*>(g);
+    rc = v8 ? launch(seg_hist_kernel<double, true>, gp) : launch(seg_hist_kernel<double, false>, gp);
   }
+  if (rc != GBDT_OK) return rc;
   count_launches();
   return GBDT_OK;
 }
