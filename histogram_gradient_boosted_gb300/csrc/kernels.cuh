@@ -63,8 +63,8 @@ struct Route {
 // Histograms of the flagged slots of a level whose rows are contiguous segments.
 struct SegHistPlan {
   int n_fgroups, group_feats;
-  int64_t chunk_rows;  // positions per CTA
-  int max_chunks;      // host bound on chunks over all flagged slots
+  int max_ctas;      // CTAs per feature group (one wave over the SMs)
+  int64_t min_rows;  // fewest rows a CTA takes when the level is small
   size_t smem;
 };
 SegHistPlan plan_seg_histograms(int64_t N, int32_t F, int32_t max_slots, int32_t max_build);

@@ -17,6 +17,8 @@
 // The partition is a tile count, a scan over tiles, and a move in which each
 // CTA ranks its tile once and then streams several columns through shared
 // memory, writing the left and right runs with aligned 16-byte stores.
+#include <type_traits>
+
 #include "kernels.cuh"
 
 namespace gbdt {
@@ -27,31 +29,36 @@ namespace {
 constexpr int kSegThreads = 1024;
 constexpr int kSegMaxFeats = 64;  // features per CTA (64 x 256 x 12 B = 192 KB of shared memory)
 
-struct SegChunks {
-  int32_t total;    // chunks over all built slots
-  int32_t n_built;  // built slots
+struct SegWork {
+  int64_t total_rows;  // rows over all built slots
+  int32_t n_built;     // built slots
+  int32_t ctas;        // CTAs per feature group that have rows
 };
 
-// One CTA: compact list of built slots and the prefix of their chunk counts.
-__global__ void seg_chunk_setup_kernel(const gbdt_level* __restrict__ level, int32_t max_slots,
-                                       const uint8_t* __restrict__ build_flag, const gbdt_segment* __restrict__ seg,
-                                       int64_t chunk_rows, int32_t* __restrict__ build_slot,
-                                       int32_t* __restrict__ chunk_start /*[max_slots+1]*/, SegChunks* __restrict__ st) {
-  __shared__ int s_a[1024], s_b[1024];
-  __shared__ int s_pre_slots, s_pre_chunks;
-  if (threadIdx.x == 0) s_pre_slots = s_pre_chunks = 0;
+// One CTA: compact list of built slots, the prefix of their row counts, and
+// how many CTAs per feature group share the rows (at most max_ctas, and no
+// fewer than min_rows rows each).
+__global__ void seg_work_setup_kernel(const gbdt_level* __restrict__ level, int32_t max_slots,
+                                      const uint8_t* __restrict__ build_flag, const gbdt_segment* __restrict__ seg,
+                                      int32_t max_ctas, int64_t min_rows, int32_t* __restrict__ build_slot,
+                                      int64_t* __restrict__ row_start /*[max_slots+1]*/, SegWork* __restrict__ st) {
+  __shared__ int s_a[1024];
+  __shared__ long long s_b[1024];
+  __shared__ int s_pre_slots;
+  __shared__ long long s_pre_rows;
+  if (threadIdx.x == 0) s_pre_slots = 0, s_pre_rows = 0;
   __syncthreads();
   const int n_slots = min(level->n_slots, max_slots);
   for (int c0 = 0; c0 < n_slots; c0 += blockDim.x) {
     const int s = c0 + threadIdx.x;
-    const bool in = s < n_slots && build_flag[s];
-    const int chunks = in ? static_cast<int>((seg[s].count + chunk_rows - 1) / chunk_rows) : 0;
+    const bool in = s < n_slots && build_flag[s] && seg[s].count > 0;
+    const long long rows = in ? seg[s].count : 0;
     s_a[threadIdx.x] = in ? 1 : 0;
-    s_b[threadIdx.x] = chunks;
+    s_b[threadIdx.x] = rows;
     __syncthreads();
     for (int o = 1; o < blockDim.x; o <<= 1) {
       const int a = threadIdx.x >= o ? s_a[threadIdx.x - o] : 0;
-      const int b = threadIdx.x >= o ? s_b[threadIdx.x - o] : 0;
+      const long long b = threadIdx.x >= o ? s_b[threadIdx.x - o] : 0;
       __syncthreads();
       s_a[threadIdx.x] += a;
       s_b[threadIdx.x] += b;
@@ -60,19 +67,21 @@ __global__ void seg_chunk_setup_kernel(const gbdt_level* __restrict__ level, int
     if (in) {
       const int k = s_pre_slots + s_a[threadIdx.x] - 1;
       build_slot[k] = s;
-      chunk_start[k] = s_pre_chunks + s_b[threadIdx.x] - chunks;
+      row_start[k] = s_pre_rows + s_b[threadIdx.x] - rows;
     }
     __syncthreads();
     if (threadIdx.x == blockDim.x - 1) {
       s_pre_slots += s_a[threadIdx.x];
-      s_pre_chunks += s_b[threadIdx.x];
+      s_pre_rows += s_b[threadIdx.x];
     }
     __syncthreads();
   }
   if (threadIdx.x == 0) {
-    chunk_start[s_pre_slots] = s_pre_chunks;
-    st->total = s_pre_chunks;
+    row_start[s_pre_slots] = s_pre_rows;
+    st->total_rows = s_pre_rows;
     st->n_built = s_pre_slots;
+    const long long by_size = (s_pre_rows + min_rows - 1) / min_rows;
+    st->ctas = static_cast<int32_t>(by_size < max_ctas ? by_size : max_ctas);
   }
 }
 
@@ -172,31 +181,12 @@ __device__ __forceinline__ void load_rows32(const uint8_t* p, bool second, uint3
   w[4] = x1.x, w[5] = x1.y, w[6] = x1.z, w[7] = x1.w;
 }
 
+// Add the rows at positions [p0, p1) of one slot to the CTA's shared histograms.
 template <typename GT, int NH, bool kV8>
-__device__ __forceinline__ void seg_hist_body(unsigned char* smem, const uint8_t* __restrict__ bins, int64_t ldb,
-                                              int32_t F, const GT* __restrict__ g, double scale, int64_t p0,
-                                              int64_t p1, int slot, int f_lo, int nf, uint32_t* __restrict__ hist_cnt,
-                                              int64_t* __restrict__ hist_q) {
-  constexpr int entries = NH * kHalfWords;
-  uint32_t* s_cnt = reinterpret_cast<uint32_t*>(smem);
-  uint32_t* s_lo = s_cnt + entries;
-  int32_t* s_hi = reinterpret_cast<int32_t*>(s_lo + entries);
+__device__ __forceinline__ void seg_hist_rows(uint32_t base, const uint8_t* const (&col)[NH], const bool (&has)[NH],
+                                              const GT* __restrict__ g, double scale, int64_t p0, int64_t p1,
+                                              uint4* s_q) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, n_warps = blockDim.x >> 5;
-  uint4* s_q = reinterpret_cast<uint4*>(s_hi + entries) + warp * 16;  // 32 rows x (low, high)
-  for (int e = threadIdx.x * 4; e < entries; e += blockDim.x * 4) {
-    *reinterpret_cast<uint4*>(s_cnt + e) = make_uint4(0, 0, 0, 0);
-    *reinterpret_cast<uint4*>(s_lo + e) = make_uint4(0, 0, 0, 0);
-    *reinterpret_cast<uint4*>(s_hi + e) = make_uint4(0, 0, 0, 0);
-  }
-  __syncthreads();
-  const uint32_t base = smem_u32(s_cnt) + lane * 4;
-  bool has[NH];
-  const uint8_t* col[NH];
-#pragma unroll
-  for (int h = 0; h < NH; ++h) {
-    has[h] = h * 32 + lane < nf;
-    col[h] = bins + static_cast<int64_t>(f_lo + (has[h] ? h * 32 + lane : 0)) * ldb;
-  }
   // aligned 32-position blocks covering [p0, p1); positions outside are masked
   for (int64_t b = (p0 >> 5) + warp; (b << 5) < p1; b += n_warps) {
     const int64_t r0 = b << 5;
@@ -222,49 +212,94 @@ __device__ __forceinline__ void seg_hist_body(unsigned char* smem, const uint8_t
     if (valid == 0xffffffffu) seg_rows32<NH, true>(base, w, s_q, valid);
     else seg_rows32<NH, false>(base, w, s_q, valid);
   }
-  __syncthreads();
+}
+
+// Merge the CTA's shared histograms into slot's global histograms and leave
+// the shared ones zeroed for the next slot.
+template <int NH>
+__device__ __forceinline__ void seg_hist_flush(uint32_t* s_cnt, uint32_t* s_lo, int32_t* s_hi, int slot, int32_t F,
+                                               int f_lo, int nf, uint32_t* __restrict__ hist_cnt,
+                                               int64_t* __restrict__ hist_q) {
+  constexpr int entries = NH * kHalfWords;
   for (int e = threadIdx.x; e < entries; e += blockDim.x) {
-    const int j = ((e / kHalfWords) << 5) + (e & 31);  // feature within the group
-    if (j >= nf) continue;
     const uint32_t cn = s_cnt[e];
     if (cn == 0) continue;
-    const int bin = (e >> 5) & (kBins - 1);
+    const int j = ((e / kHalfWords) << 5) + (e & 31);  // feature within the group
     const int64_t v = static_cast<int64_t>(s_hi[e]) * 4294967296ll + static_cast<int64_t>(s_lo[e]);
+    s_cnt[e] = 0;
+    s_lo[e] = 0;
+    s_hi[e] = 0;
+    if (j >= nf) continue;  // unused entries of lanes without a feature
+    const int bin = (e >> 5) & (kBins - 1);
     const int64_t o = (static_cast<int64_t>(slot) * F + f_lo + j) * kBins + bin;
     atomicAdd(hist_cnt + o, cn);
     atomicAdd(reinterpret_cast<unsigned long long*>(hist_q + o), static_cast<unsigned long long>(v));
   }
 }
 
+// One CTA per (share of the level's built rows, feature group): the built
+// slots' rows are concatenated in slot order and cut into equal shares, one
+// per CTA, so the level runs as one balanced wave.  A share that crosses
+// slot boundaries flushes its histograms at each crossing.
 template <typename GT, bool kV8>
 __global__ void __launch_bounds__(kSegThreads, 1)
-    seg_hist_kernel(const uint8_t* __restrict__ bins, int64_t ldb, int64_t N, int32_t F, const GT* __restrict__ g,
+    seg_hist_kernel(const uint8_t* __restrict__ bins, int64_t ldb, int32_t F, const GT* __restrict__ g,
                     const int32_t* __restrict__ fixed_exp, const gbdt_segment* __restrict__ seg,
-                    const int32_t* __restrict__ build_slot, const int32_t* __restrict__ chunk_start,
-                    const SegChunks* __restrict__ st, int64_t chunk_rows, int32_t group_feats,
-                    uint32_t* __restrict__ hist_cnt, int64_t* __restrict__ hist_q) {
+                    const int32_t* __restrict__ build_slot, const int64_t* __restrict__ row_start,
+                    const SegWork* __restrict__ st, int32_t group_feats, uint32_t* __restrict__ hist_cnt,
+                    int64_t* __restrict__ hist_q) {
   extern __shared__ __align__(16) unsigned char smem[];
-  const int c = blockIdx.x;
-  if (c >= st->total) return;
-  const int n_built = st->n_built;
-  int lo = 0, hi = n_built - 1;  // last built slot whose first chunk <= c
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (chunk_start[mid] <= c) lo = mid;
-    else hi = mid - 1;
-  }
-  const int slot = build_slot[lo];
+  const int ctas = st->ctas;
+  if (static_cast<int>(blockIdx.x) >= ctas) return;
   const int f_lo = blockIdx.y * group_feats;
   const int nf = min(group_feats, F - f_lo);
   if (nf <= 0) return;
-  const gbdt_segment sg = seg[slot];
-  const int64_t p0 = sg.start + static_cast<int64_t>(c - chunk_start[lo]) * chunk_rows;
-  const int64_t p1 = min(sg.start + sg.count, p0 + chunk_rows);
+  const int64_t total = st->total_rows;
+  const int64_t lo = total * blockIdx.x / ctas, hi = total * (blockIdx.x + 1) / ctas;
+  if (lo >= hi) return;
+  const int n_built = st->n_built;
+  int k = 0, kh = n_built - 1;  // last built slot whose first row <= lo
+  while (k < kh) {
+    const int mid = (k + kh + 1) >> 1;
+    if (row_start[mid] <= lo) k = mid;
+    else kh = mid - 1;
+  }
   const double scale = ldexp(1.0, *fixed_exp);
-  if (group_feats > 32)
-    seg_hist_body<GT, 2, kV8>(smem, bins, ldb, F, g, scale, p0, p1, slot, f_lo, nf, hist_cnt, hist_q);
-  else
-    seg_hist_body<GT, 1, kV8>(smem, bins, ldb, F, g, scale, p0, p1, slot, f_lo, nf, hist_cnt, hist_q);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  auto run = [&](auto nh_tag) {
+    constexpr int NH = decltype(nh_tag)::value;
+    constexpr int entries = NH * kHalfWords;
+    uint32_t* s_cnt = reinterpret_cast<uint32_t*>(smem);
+    uint32_t* s_lo = s_cnt + entries;
+    int32_t* s_hi = reinterpret_cast<int32_t*>(s_lo + entries);
+    uint4* s_q = reinterpret_cast<uint4*>(s_hi + entries) + warp * 16;  // 32 rows x (low, high)
+    for (int e = threadIdx.x * 4; e < entries; e += blockDim.x * 4) {
+      *reinterpret_cast<uint4*>(s_cnt + e) = make_uint4(0, 0, 0, 0);
+      *reinterpret_cast<uint4*>(s_lo + e) = make_uint4(0, 0, 0, 0);
+      *reinterpret_cast<uint4*>(s_hi + e) = make_uint4(0, 0, 0, 0);
+    }
+    __syncthreads();
+    const uint32_t base = smem_u32(s_cnt) + lane * 4;
+    bool has[NH];
+    const uint8_t* col[NH];
+#pragma unroll
+    for (int h = 0; h < NH; ++h) {
+      has[h] = h * 32 + lane < nf;
+      col[h] = bins + static_cast<int64_t>(f_lo + (has[h] ? h * 32 + lane : 0)) * ldb;
+    }
+    for (int64_t r = lo; r < hi; ++k) {
+      const int64_t r_end = min(hi, row_start[k + 1]);
+      const int slot = build_slot[k];
+      const int64_t p0 = seg[slot].start + (r - row_start[k]);
+      seg_hist_rows<GT, NH, kV8>(base, col, has, g, scale, p0, p0 + (r_end - r), s_q);
+      __syncthreads();
+      seg_hist_flush<NH>(s_cnt, s_lo, s_hi, slot, F, f_lo, nf, hist_cnt, hist_q);
+      __syncthreads();
+      r = r_end;
+    }
+  };
+  if (group_feats > 32) run(std::integral_constant<int, 2>{});
+  else run(std::integral_constant<int, 1>{});
 }
 
 // ---------------------------------------------------------------------------------------- partition
@@ -683,41 +718,42 @@ cudaError_t smem_attr(K kernel, size_t bytes) {
 
 // ---- plans and launchers ------------------------------------------------------------------------
 SegHistPlan plan_seg_histograms(int64_t N, int32_t F, int32_t max_slots, int32_t max_build) {
+  (void)N, (void)max_slots, (void)max_build;
   SegHistPlan p{};
   p.n_fgroups = ceil_div(F, kSegMaxFeats);
   p.group_feats = ceil_div(F, p.n_fgroups);
-  const int64_t target = static_cast<int64_t>(sm_count()) * 3;
-  int64_t cr = (N * p.n_fgroups + target - 1) / target;
-  if (cr < 32768) cr = 32768;
-  p.chunk_rows = (cr + 15) / 16 * 16;
-  p.max_chunks = ceil_div(N, p.chunk_rows) + (max_build < max_slots ? max_build : max_slots);
+  p.max_ctas = sm_count() / p.n_fgroups;  // one wave: a CTA per SM
+  if (p.max_ctas < 1) p.max_ctas = 1;
+  p.min_rows = 4096;
   p.smem = static_cast<size_t>(ceil_div(p.group_feats, 32)) * kHalfWords * 12 + (kSegThreads / 32) * 256;
   return p;
 }
 
 size_t seg_hist_scratch_bytes(int32_t max_slots) {
-  return sizeof(SegChunks) + sizeof(int32_t) * (2 * static_cast<size_t>(max_slots) + 2) + 3 * kWsAlign;
+  return sizeof(SegWork) + sizeof(int32_t) * (static_cast<size_t>(max_slots) + 1) +
+         sizeof(int64_t) * (static_cast<size_t>(max_slots) + 1) + 3 * kWsAlign;
 }
 
 int launch_seg_histograms(const SegHistPlan& plan, const uint8_t* bins, int64_t ldb, int64_t N, int32_t F,
                           const void* g, int32_t g_dtype, const int32_t* fixed_exp, const gbdt_level* level,
                           int32_t max_slots, const uint8_t* build_flag, const gbdt_segment* seg, void* scratch,
                           uint32_t* hist_cnt, int64_t* hist_q, cudaStream_t s) {
+  (void)N;
   Carve c(scratch, seg_hist_scratch_bytes(max_slots));
-  SegChunks* st = c.take<SegChunks>(1);
+  SegWork* st = c.take<SegWork>(1);
   int32_t* build_slot = c.take<int32_t>(max_slots + 1);
-  int32_t* chunk_start = c.take<int32_t>(max_slots + 1);
+  int64_t* row_start = c.take<int64_t>(max_slots + 1);
   launch_hist_zero(level, max_slots, build_flag, F, hist_cnt, hist_q, s);
-  seg_chunk_setup_kernel<<<1, 1024, 0, s>>>(level, max_slots, build_flag, seg, plan.chunk_rows, build_slot,
-                                            chunk_start, st);
+  seg_work_setup_kernel<<<1, 1024, 0, s>>>(level, max_slots, build_flag, seg, plan.max_ctas, plan.min_rows,
+                                           build_slot, row_start, st);
   count_launches();
-  dim3 grid(static_cast<unsigned>(plan.max_chunks), static_cast<unsigned>(plan.n_fgroups));
+  dim3 grid(static_cast<unsigned>(plan.max_ctas), static_cast<unsigned>(plan.n_fgroups));
   // 256-bit column loads need every column start 32-byte aligned
   const bool v8 = aligned(bins, 32) && ldb % 32 == 0;
   auto launch = [&](auto kernel, const auto* gp) -> int {
     GBDT_CUDA(smem_attr(kernel, plan.smem));
-    kernel<<<grid, kSegThreads, plan.smem, s>>>(bins, ldb, N, F, gp, fixed_exp, seg, build_slot, chunk_start, st,
-                                                plan.chunk_rows, plan.group_feats, hist_cnt, hist_q);
+    kernel<<<grid, kSegThreads, plan.smem, s>>>(bins, ldb, F, gp, fixed_exp, seg, build_slot, row_start, st,
+                                                plan.group_feats, hist_cnt, hist_q);
     return GBDT_OK;
   };
   int rc;
