@@ -69,6 +69,7 @@ SPLIT_DTYPE = np.dtype([("feature", np.int32), ("bin", np.int32), ("gain", np.fl
                         ("q_total", np.int64), ("cnt_left", np.uint32), ("cnt_total", np.uint32)])
 LEVEL_DTYPE = np.dtype([("node_begin", np.int32), ("n_slots", np.int32)])
 SEGMENT_DTYPE = np.dtype([("start", np.int64), ("count", np.int64)])
+FILTER_DTYPE = np.dtype([("feature", np.int32), ("bin", np.int32), ("side", np.int32), ("reserved", np.int32)])
 assert NODE_DTYPE.itemsize == 40 and SPLIT_DTYPE.itemsize == 40
 
 _lib = None
@@ -105,7 +106,7 @@ def lib():
         "gbdt_kernel_launch_count": ([], i64),
         "gbdt_partition_noalloc": ([P, i64, i64, i32, P, P, i32, P, P, P, P, P, P, P], i32),
         "gbdt_histograms_segmented_workspace_size": ([i32], sz),
-        "gbdt_build_histograms_segmented": ([P, i64, i64, i32, P, i32, P, P, i32, P, i32, P, P, P, P, sz, P], i32),
+        "gbdt_build_histograms_segmented": ([P, i64, i64, i32, P, i32, P, P, i32, P, i32, P, P, P, P, P, sz, P], i32),
         "gbdt_partition_rows_workspace_size": ([i64, i32], sz),
         "gbdt_partition_rows": ([P, P, i64, i64, i32, P, P, i32, P, P, P, P, P, i32, P, P, P, P, P, sz, P], i32),
     }
@@ -231,8 +232,9 @@ def build_histograms(bins, N, g, fixed_exp, node_of_row, level, max_slots, build
 
 
 def build_histograms_segmented(bins, N, g, fixed_exp, level, max_slots, build_flag, max_build, segments,
-                               hist_cnt=None, hist_q=None, ws=None):
-    """Histograms of flagged slots whose rows are contiguous segments (SEGMENT_DTYPE bytes, device)."""
+                               hist_cnt=None, hist_q=None, ws=None, filters=None):
+    """Histograms of flagged slots whose rows are contiguous segments (SEGMENT_DTYPE bytes, device),
+    optionally narrowed per slot by FILTER_DTYPE records (device bytes)."""
     torch = _torch()
     F, ldb = bins.shape
     if hist_cnt is None:
@@ -243,7 +245,8 @@ def build_histograms_segmented(bins, N, g, fixed_exp, level, max_slots, build_fl
     dt = DTYPE_F32 if g.dtype == torch.float32 else DTYPE_F64
     _check(lib().gbdt_build_histograms_segmented(_ptr(bins), ldb, N, F, _ptr(g), dt, _ptr(fixed_exp), _ptr(level),
                                                  max_slots, _ptr(build_flag), max_build, _ptr(segments),
-                                                 _ptr(hist_cnt), _ptr(hist_q), _ptr(ws), ws.numel(), _stream()))
+                                                 _ptr(filters) if filters is not None else None, _ptr(hist_cnt),
+                                                 _ptr(hist_q), _ptr(ws), ws.numel(), _stream()))
     return hist_cnt, hist_q
 
 

@@ -1,6 +1,7 @@
 // Internal helpers shared by the library's translation units.
 #pragma once
 
+#include <cuda.h>  // CUtensorMap (the tensor-map type only; encoding goes through the runtime entry point)
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -134,6 +135,33 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32
   }
   return false;
 }
+
+// Load one box of a 3-D tensor map (coordinates innermost first) into shared
+// memory; completion is one phase of `bar`, armed here with the box's bytes.
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int x, int y, int z, uint32_t bytes,
+                                            uint64_t* bar) {
+  asm volatile(
+      "{\n\t.reg .b64 st;\n\t"
+      "mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(smem_u32(bar)),
+      "r"(bytes)
+      : "memory");
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+      "[%5];" ::"r"(smem_u32(dst)),
+      "l"(map), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// ---- row-block layout of binned features (training-internal) ---------------------------------
+// Position p of feature f sits at byte (p / 32) * pitch + 32 * f + p % 32, pitch = 32 * F: the 32
+// rows of a row block are contiguous per feature and the features of a row block contiguous, so a
+// warp reading 32 rows of 32 consecutive features reads one contiguous kilobyte.
+constexpr int kRowBlock = 32;
+__host__ __device__ __forceinline__ int64_t rb_offset(int f, int64_t p, int64_t pitch) {
+  return (p >> 5) * pitch + static_cast<int64_t>(f) * kRowBlock + (p & 31);
+}
+inline int64_t rb_pitch(int32_t F) { return static_cast<int64_t>(F) * kRowBlock; }
+inline int64_t rb_blocks(int64_t N) { return (N + kRowBlock - 1) / kRowBlock; }
 
 inline int ceil_div(int64_t a, int64_t b) { return static_cast<int>((a + b - 1) / b); }
 

@@ -17,6 +17,8 @@
 // The partition is a tile count, a scan over tiles, and a move in which each
 // CTA ranks its tile once and then streams several columns through shared
 // memory, writing the left and right runs with aligned 16-byte stores.
+#include <algorithm>
+#include <mutex>
 #include <type_traits>
 
 #include "kernels.cuh"
@@ -42,6 +44,7 @@ __global__ void seg_work_setup_kernel(const gbdt_level* __restrict__ level, int3
                                       const uint8_t* __restrict__ build_flag, const gbdt_segment* __restrict__ seg,
                                       int32_t max_ctas, int64_t min_rows, int32_t* __restrict__ build_slot,
                                       int64_t* __restrict__ row_start /*[max_slots+1]*/, SegWork* __restrict__ st) {
+  // (a slot's rows are its segment's positions, narrowed by its filter inside the histogram kernel)
   __shared__ int s_a[1024];
   __shared__ long long s_b[1024];
   __shared__ int s_pre_slots;
@@ -165,6 +168,33 @@ __device__ __forceinline__ void seg_rows32(uint32_t base, const uint32_t (&w)[NH
   }
 }
 
+// Partial block (some rows outside the slot or filtered out): only the valid
+// rows are visited, word by word of the loaded bytes, so a row that does not
+// belong to the slot costs nothing.  The byte of row 4 * wi + k is selected
+// with a register selector.
+template <int NH>
+__device__ __forceinline__ void seg_rows_sparse(uint32_t base, const uint32_t (&w)[NH][8], const uint4* s_q,
+                                                uint32_t valid) {
+  constexpr uint32_t kLo = NH * kHalfBytes, kHi = 2 * NH * kHalfBytes;
+  const uint2* s_q2 = reinterpret_cast<const uint2*>(s_q);
+#pragma unroll
+  for (int wi = 0; wi < 8; ++wi) {
+    uint32_t m = (valid >> (4 * wi)) & 0xfu;  // warp-uniform
+    while (m != 0) {
+      const uint32_t k = __ffs(m) - 1;
+      m &= m - 1;
+      const uint2 q = s_q2[4 * wi + k];
+      uint32_t a[NH], old[NH];
+#pragma unroll
+      for (int h = 0; h < NH; ++h) a[h] = base + h * kHalfBytes + (__byte_perm(w[h][wi], 0u, 0x4440u | k) << 7);
+#pragma unroll
+      for (int h = 0; h < NH; ++h) old[h] = entry_lo<kLo>(a[h], q.x);
+#pragma unroll
+      for (int h = 0; h < NH; ++h) entry_hi<kHi>(a[h], q.x, static_cast<int32_t>(q.y), old[h]);
+    }
+  }
+}
+
 // 32 bytes of a column (rows r0 .. r0 + 31 of one feature).  With kV8 the
 // column starts are 32-byte aligned and one 256-bit load reads them all.
 template <bool kV8>
@@ -182,35 +212,47 @@ __device__ __forceinline__ void load_rows32(const uint8_t* p, bool second, uint3
 }
 
 // Add the rows at positions [p0, p1) of one slot to the CTA's shared histograms.
-template <typename GT, int NH, bool kV8>
+// With a filter (fcol != nullptr) only the rows whose decision fcol[p] > fbin
+// equals fside are added.
+// kRB: bins in the row-block layout (ldb is then the row-block pitch and col[h]
+// points at the feature's 32 bytes of row block 0).
+template <typename GT, int NH, bool kV8, bool kRB>
 __device__ __forceinline__ void seg_hist_rows(uint32_t base, const uint8_t* const (&col)[NH], const bool (&has)[NH],
-                                              const GT* __restrict__ g, double scale, int64_t p0, int64_t p1,
+                                              int64_t ldb, const GT* __restrict__ g, double scale, int64_t p0,
+                                              int64_t p1, const uint8_t* __restrict__ fcol, int fbin, int fside,
                                               uint4* s_q) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, n_warps = blockDim.x >> 5;
   // aligned 32-position blocks covering [p0, p1); positions outside are masked
   for (int64_t b = (p0 >> 5) + warp; (b << 5) < p1; b += n_warps) {
     const int64_t r0 = b << 5;
     const int64_t pr = r0 + lane;
-    const bool v = pr >= p0 && pr < p1;
-    const uint32_t valid = __ballot_sync(0xffffffffu, v);
-    const int64_t q = v ? to_fixed(static_cast<double>(g[pr]), scale) : 0;
+    const bool in = pr >= p0 && pr < p1;
     const bool second = r0 + 16 < p1;  // any row of the block's upper half is in range
+    // all of the block's loads are issued before any of them is used: the filter byte, the gradient
+    // and the bins (the bins of a block whose rows are all filtered out are loaded for nothing)
+    const int64_t boff = kRB ? (r0 >> 5) * ldb : r0;  // the block's bytes of a feature, from col[h]
+    const int fb = (fcol && in) ? static_cast<int>(fcol[boff + lane]) : 0;
+    const double gv = in ? static_cast<double>(g[pr]) : 0.0;
     uint32_t w[NH][8];
 #pragma unroll
     for (int h = 0; h < NH; ++h) {
       if (has[h]) {
-        load_rows32<kV8>(col[h] + r0, second, w[h]);
+        load_rows32<kV8>(col[h] + boff, second, w[h]);
       } else {
 #pragma unroll
         for (int k = 0; k < 8; ++k) w[h][k] = 0;
       }
     }
+    const bool v = in && (!fcol || (fb > fbin) == (fside != 0));
+    const uint32_t valid = __ballot_sync(0xffffffffu, v);
+    if (valid == 0) continue;  // warp-uniform: no row of this block belongs to the slot
+    const int64_t q = v ? to_fixed(gv, scale) : 0;
     __syncwarp();
     reinterpret_cast<uint2*>(s_q)[lane] =
         make_uint2(static_cast<uint32_t>(static_cast<uint64_t>(q)), static_cast<uint32_t>(q >> 32));
     __syncwarp();
     if (valid == 0xffffffffu) seg_rows32<NH, true>(base, w, s_q, valid);
-    else seg_rows32<NH, false>(base, w, s_q, valid);
+    else seg_rows_sparse<NH>(base, w, s_q, valid);
   }
 }
 
@@ -241,13 +283,13 @@ __device__ __forceinline__ void seg_hist_flush(uint32_t* s_cnt, uint32_t* s_lo, 
 // slots' rows are concatenated in slot order and cut into equal shares, one
 // per CTA, so the level runs as one balanced wave.  A share that crosses
 // slot boundaries flushes its histograms at each crossing.
-template <typename GT, bool kV8>
+template <typename GT, bool kV8, bool kRB>
 __global__ void __launch_bounds__(kSegThreads, 1)
     seg_hist_kernel(const uint8_t* __restrict__ bins, int64_t ldb, int32_t F, const GT* __restrict__ g,
                     const int32_t* __restrict__ fixed_exp, const gbdt_segment* __restrict__ seg,
-                    const int32_t* __restrict__ build_slot, const int64_t* __restrict__ row_start,
-                    const SegWork* __restrict__ st, int32_t group_feats, uint32_t* __restrict__ hist_cnt,
-                    int64_t* __restrict__ hist_q) {
+                    const gbdt_filter* __restrict__ filters, const int32_t* __restrict__ build_slot,
+                    const int64_t* __restrict__ row_start, const SegWork* __restrict__ st, int32_t group_feats,
+                    uint32_t* __restrict__ hist_cnt, int64_t* __restrict__ hist_q) {
   extern __shared__ __align__(16) unsigned char smem[];
   const int ctas = st->ctas;
   if (static_cast<int>(blockIdx.x) >= ctas) return;
@@ -285,13 +327,17 @@ __global__ void __launch_bounds__(kSegThreads, 1)
 #pragma unroll
     for (int h = 0; h < NH; ++h) {
       has[h] = h * 32 + lane < nf;
-      col[h] = bins + static_cast<int64_t>(f_lo + (has[h] ? h * 32 + lane : 0)) * ldb;
+      col[h] = bins + static_cast<int64_t>(f_lo + (has[h] ? h * 32 + lane : 0)) * (kRB ? kRowBlock : ldb);
     }
     for (int64_t r = lo; r < hi; ++k) {
       const int64_t r_end = min(hi, row_start[k + 1]);
       const int slot = build_slot[k];
       const int64_t p0 = seg[slot].start + (r - row_start[k]);
-      seg_hist_rows<GT, NH, kV8>(base, col, has, g, scale, p0, p0 + (r_end - r), s_q);
+      const gbdt_filter fl = filters ? filters[slot] : gbdt_filter{-1, 0, 0, 0};
+      const uint8_t* fcol =
+          fl.feature >= 0 ? bins + static_cast<int64_t>(fl.feature) * (kRB ? kRowBlock : ldb) : nullptr;
+      seg_hist_rows<GT, NH, kV8, kRB>(base, col, has, ldb, g, scale, p0, p0 + (r_end - r), fcol, fl.bin, fl.side,
+                                      s_q);
       __syncthreads();
       seg_hist_flush<NH>(s_cnt, s_lo, s_hi, slot, F, f_lo, nf, hist_cnt, hist_q);
       __syncthreads();
@@ -450,30 +496,45 @@ __global__ void __launch_bounds__(1024)
   }
 }
 
-// Column c < F: bins column c; c == F: gradient (4 or 8 B); c == F + 1: original row id (4 B).
 // Output-centric move.  Once per tile: the rows' decisions (lane = row,
 // ballots), their ranks, and the inverse permutation inv[o] = tile position of
-// the o-th output row (left rows first, then right rows) in shared memory.
-// The gradient and the row id move one output position per thread, in
-// batches of independent loads.  For the bin columns each thread owns up to
-// kMvWordsPerThread aligned 4-byte words of the tile's two output runs and
-// keeps, in registers, the source positions of their bytes; every output word
-// is gathered from the column's tile in shared memory and written with one
-// aligned 4-byte store (byte stores only where a run starts or ends inside a
-// word), so stores fill whole sectors.  The column tiles arrive by bulk
-// asynchronous copies, kMvStages columns ahead of the one being gathered, so
-// the loads of later columns overlap the gathers and stores of earlier ones.
+// the o-th output row (the rows of each output run in order, the runs one
+// after another) in shared memory.  The gradient and the row id move one
+// output position per thread, in batches of independent loads.  For the bin
+// columns each thread owns up to kMvWordsPerThread aligned 4-byte words of the
+// tile's output runs and keeps, in registers, the source positions of their
+// bytes; every output word is gathered from the column's tile in shared
+// memory and written with one aligned 4-byte store (byte stores only where a
+// run starts or ends inside a word), so stores fill whole sectors.  The column
+// tiles arrive by bulk asynchronous copies, kMvStages columns ahead of the one
+// being gathered, so the loads of later columns overlap the gathers and stores
+// of earlier ones.
 constexpr int kMvChunks = kMvTile / 32;
 constexpr int kMvChunksPerWarp = kMvChunks / (kMvThreads / 32);
-constexpr int kMvWordsPerThread = (kMvTile / 4 + 4 + kMvThreads - 1) / kMvThreads;  // 5: both runs, edges included
+constexpr int kMvWordsPerThread = (kMvTile / 4 + 8 + kMvThreads - 1) / kMvThreads;  // 5: up to 4 runs, edges included
 constexpr int kMvStages = 4;
-constexpr int kMvStageBytes = kMvTile + 16;  // a tile plus its 16-byte alignment slack
+// A stage holds a tile's span of one column: in the column layout up to kMvTile + 15 bytes from a
+// 16-byte boundary; in the row-block layout kMvBoxBlocks row blocks of 32 bytes (a tile plus its
+// offset inside its first row block), the box of one tensor copy.  128-byte aligned stages.
+constexpr int kMvBoxBlocks = kMvTile / kRowBlock + 1;
+constexpr uint32_t kMvBoxBytes = kMvBoxBlocks * kRowBlock;
+constexpr int kMvStageBytes = (kMvBoxBytes + 127) / 128 * 128;
 constexpr uint32_t kMvWaitPolls = 1u << 20;
 
-template <typename T>
-__device__ __forceinline__ void move_positions(const T* __restrict__ in, T* __restrict__ out, int64_t p0, int n,
-                                               int nl, int64_t dst_l, int64_t dst_r, const uint16_t* s_inv) {
+// The output runs of one tile: run r's rows are inv[base[r] .. base[r] + len[r])
+// and go to positions dst[r] ...
+template <int R>
+struct MvRuns {
+  int64_t dst[R];
+  int len[R];
+  int base[R];
+};
+
+template <typename T, int R>
+__device__ __forceinline__ void move_positions(const T* __restrict__ in, T* __restrict__ out, int64_t p0,
+                                               const MvRuns<R>& ru, const uint16_t* s_inv) {
   constexpr int U = 8;
+  const int n = ru.base[R - 1] + ru.len[R - 1];
   for (int o0 = threadIdx.x; o0 < n; o0 += U * kMvThreads) {
     T v[U];
 #pragma unroll
@@ -484,11 +545,127 @@ __device__ __forceinline__ void move_positions(const T* __restrict__ in, T* __re
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int o = o0 + u * kMvThreads;
-      if (o < n) out[o < nl ? dst_l + o : dst_r + (o - nl)] = v[u];
+      if (o < n) {
+        int r = 0;
+#pragma unroll
+        for (int k = 1; k < R; ++k) r = o >= ru.base[k] ? k : r;
+        out[ru.dst[r] + (o - ru.base[r])] = v[u];
+      }
     }
   }
 }
 
+// Thread 0: arm the stage barriers and start the first column copies: in the
+// column layout the tile's 16-byte-aligned span [a0, a0 + span) of each
+// column, in the row-block layout the box of row blocks z0 .. of each feature.
+template <bool kRB>
+__device__ __forceinline__ void mv_start_copies(uint8_t (*s_stage)[kMvStageBytes], uint64_t* s_full,
+                                                const uint8_t* __restrict__ bins_in, int64_t ldb, int F, int64_t a0,
+                                                uint32_t span, const CUtensorMap* map, int z0) {
+  if (threadIdx.x != 0) return;
+  for (int k = 0; k < kMvStages; ++k) mbar_init(&s_full[k], 1);
+  mbar_init_fence();
+  for (int c = 0; c < F && c < kMvStages; ++c) {
+    if (kRB) tma_load_3d(s_stage[c], map, 0, c, z0, kMvBoxBytes, &s_full[c]);
+    else bulk_load(s_stage[c], bins_in + c * ldb + a0, span, &s_full[c]);
+  }
+}
+
+// The output words this thread owns: the runs' words listed one run after
+// another; off = the word's byte offset from the column's (or in the
+// row-block layout the feature's) first byte, -1: none; src = stage positions
+// of its four bytes (16 bits each, 0xffff: byte not written).
+template <int R, bool kRB>
+__device__ __forceinline__ void mv_own_words(const MvRuns<R>& ru, const uint16_t* s_inv, int a_off, int64_t pitch,
+                                             int64_t (&off)[kMvWordsPerThread], uint32_t (&srcl)[kMvWordsPerThread],
+                                             uint32_t (&srch)[kMvWordsPerThread]) {
+  int nw[R];
+#pragma unroll
+  for (int r = 0; r < R; ++r)
+    nw[r] = ru.len[r] > 0 ? static_cast<int>(((ru.dst[r] + ru.len[r] + 3) >> 2) - (ru.dst[r] >> 2)) : 0;
+#pragma unroll
+  for (int m = 0; m < kMvWordsPerThread; ++m) {
+    int vw = threadIdx.x + m * kMvThreads;
+    uint32_t sp[4] = {0xffffu, 0xffffu, 0xffffu, 0xffffu};
+    int64_t w = -1;
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      if (w < 0 && vw >= 0 && vw < nw[r]) {
+        const int first = static_cast<int>(ru.dst[r] & 3);  // run start inside its first word
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int o = 4 * vw + i - first;  // offset in the run
+          if (o >= 0 && o < ru.len[r]) sp[i] = s_inv[ru.base[r] + o] + a_off;
+        }
+        w = (ru.dst[r] >> 2) + vw;  // word index
+      }
+      vw -= nw[r];
+    }
+    off[m] = w < 0 ? -1 : (kRB ? (w >> 3) * pitch + ((w & 7) << 2) : w << 2);
+    srcl[m] = sp[0] | (sp[1] << 16);
+    srch[m] = sp[2] | (sp[3] << 16);
+  }
+}
+
+// Move every bin column of the tile through the stages.  Returns false when
+// a copy did not complete within its wait limit (the error bit is raised and
+// the copies still in flight have landed).
+template <bool kRB>
+__device__ __forceinline__ bool mv_columns(const uint8_t* __restrict__ bins_in, uint8_t* __restrict__ bins_out,
+                                           int64_t ldb, int F, int64_t a0, uint32_t span, const CUtensorMap* map,
+                                           int z0, uint8_t (*s_stage)[kMvStageBytes], uint64_t* s_full,
+                                           const int64_t (&off)[kMvWordsPerThread],
+                                           const uint32_t (&srcl)[kMvWordsPerThread],
+                                           const uint32_t (&srch)[kMvWordsPerThread], int32_t* err) {
+  int c_fail = -1;
+#pragma unroll 1
+  for (int c = 0; c < F; ++c) {
+    const int k = c % kMvStages;
+    const uint8_t* stage = s_stage[k];
+    const bool ok = mbar_wait(&s_full[k], static_cast<uint32_t>((c / kMvStages) & 1), kMvWaitPolls);
+    if (ok) {
+      uint8_t* out = bins_out + static_cast<int64_t>(c) * (kRB ? kRowBlock : ldb);
+#pragma unroll
+      for (int m = 0; m < kMvWordsPerThread; ++m) {
+        if (off[m] < 0) continue;
+        const uint32_t s0 = srcl[m] & 0xffffu, s1 = srcl[m] >> 16, s2 = srch[m] & 0xffffu, s3 = srch[m] >> 16;
+        if (s0 != 0xffffu && s1 != 0xffffu && s2 != 0xffffu && s3 != 0xffffu) {
+          *reinterpret_cast<uint32_t*>(out + off[m]) =
+              static_cast<uint32_t>(stage[s0]) | (static_cast<uint32_t>(stage[s1]) << 8) |
+              (static_cast<uint32_t>(stage[s2]) << 16) | (static_cast<uint32_t>(stage[s3]) << 24);
+        } else {  // a run starts or ends inside this word: write only its own bytes
+          uint8_t* ob = out + off[m];
+          if (s0 != 0xffffu) ob[0] = stage[s0];
+          if (s1 != 0xffffu) ob[1] = stage[s1];
+          if (s2 != 0xffffu) ob[2] = stage[s2];
+          if (s3 != 0xffffu) ob[3] = stage[s3];
+        }
+      }
+    }
+    if (__syncthreads_or(!ok)) {  // every thread is done with this stage (or a copy timed out)
+      c_fail = c;
+      break;
+    }
+    if (threadIdx.x == 0 && c + kMvStages < F) {
+      if (kRB) tma_load_3d(s_stage[k], map, 0, c + kMvStages, z0, kMvBoxBytes, &s_full[k]);
+      else bulk_load(s_stage[k], bins_in + static_cast<int64_t>(c + kMvStages) * ldb + a0, span, &s_full[k]);
+    }
+  }
+  if (c_fail < 0) return true;
+  if (threadIdx.x == 0) {
+    raise_error(err, kErrWaitTimeout);
+    // let the copies still in flight (columns c_fail .. issued - 1) land before the CTA's shared memory is
+    // released; each stage completes in order, so waiting for its last issued column suffices
+    const int issued = min(F, c_fail + kMvStages);
+    for (int c = c_fail; c < issued; ++c) {
+      if (c + kMvStages < issued) continue;  // a later column of the same stage is waited for instead
+      mbar_wait(&s_full[c % kMvStages], static_cast<uint32_t>((c / kMvStages) & 1), kMvWaitPolls);
+    }
+  }
+  return false;
+}
+
+// Move of one level: two runs (left, right) per split slot.
 __global__ void __launch_bounds__(kMvThreads, 4)
     mv_move_kernel(const uint8_t* __restrict__ bins_in, uint8_t* __restrict__ bins_out, int64_t ldb, int32_t F,
                    const void* __restrict__ g_in, void* __restrict__ g_out, int g_size,
@@ -520,15 +697,10 @@ __global__ void __launch_bounds__(kMvThreads, 4)
     }
     return;
   }
-  // ---- start the first column copies: the tile's 16-byte-aligned span of each column
   const int64_t a0 = p0 & ~int64_t(15);
   const uint32_t span = static_cast<uint32_t>(((p0 + n + 15) & ~int64_t(15)) - a0);
   const int a_off = static_cast<int>(p0 & 15);  // stage index of tile position 0
-  if (threadIdx.x == 0) {
-    for (int k = 0; k < kMvStages; ++k) mbar_init(&s_full[k], 1);
-    mbar_init_fence();
-    for (int c = 0; c < F && c < kMvStages; ++c) bulk_load(s_stage[c], bins_in + c * ldb + a0, span, &s_full[c]);
-  }
+  mv_start_copies<false>(s_stage, s_full, bins_in, ldb, F, a0, span, nullptr, 0);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const uint8_t* col = bins_in + static_cast<int64_t>(rt.feature) * ldb;
   // ---- rank the tile (lane = row) and build the inverse permutation
@@ -563,104 +735,40 @@ __global__ void __launch_bounds__(kMvThreads, 4)
     }
   }
   __syncthreads();
-  const int nr = n - nl;
   const int64_t left_before = tile_excl[t] - tile_excl[tile_start[s]];
-  const int64_t dst_l = seg[s].start + left_before;                             // this tile's left run
-  const int64_t dst_r = seg[s].start + seg_left[s] + (tile_off - left_before);  // this tile's right run
+  MvRuns<2> ru;
+  ru.dst[0] = seg[s].start + left_before;                             // this tile's left run
+  ru.dst[1] = seg[s].start + seg_left[s] + (tile_off - left_before);  // this tile's right run
+  ru.len[0] = nl, ru.len[1] = n - nl;
+  ru.base[0] = 0, ru.base[1] = nl;
   // ---- gradient and row id, while the first column copies are in flight
   if (g_size == 8)
-    move_positions(static_cast<const uint64_t*>(g_in), static_cast<uint64_t*>(g_out), p0, n, nl, dst_l, dst_r, s_inv);
+    move_positions(static_cast<const uint64_t*>(g_in), static_cast<uint64_t*>(g_out), p0, ru, s_inv);
   else
-    move_positions(static_cast<const uint32_t*>(g_in), static_cast<uint32_t*>(g_out), p0, n, nl, dst_l, dst_r, s_inv);
-  move_positions(orig_in, orig_out, p0, n, nl, dst_l, dst_r, s_inv);
-  // ---- the output words this thread owns: left run words, then right run words
-  const int64_t wl0 = dst_l >> 2, wr0 = dst_r >> 2;
-  const int nwl = nl > 0 ? static_cast<int>(((dst_l + nl + 3) >> 2) - wl0) : 0;
-  const int nwr = nr > 0 ? static_cast<int>(((dst_r + nr + 3) >> 2) - wr0) : 0;
-  const int ol = static_cast<int>(dst_l & 3), orr = static_cast<int>(dst_r & 3);  // run start inside its first word
-  int wrel[kMvWordsPerThread];       // word offset within its run's words; bit 30: right run; -1: none
-  uint32_t srcl[kMvWordsPerThread];  // stage positions of bytes 0,1 (16 bits each; 0xffff: not written)
-  uint32_t srch[kMvWordsPerThread];  // stage positions of bytes 2,3
-#pragma unroll
-  for (int m = 0; m < kMvWordsPerThread; ++m) {
-    const int vw = threadIdx.x + m * kMvThreads;
-    uint32_t sp[4] = {0xffffu, 0xffffu, 0xffffu, 0xffffu};
-    int wr = -1;
-    if (vw < nwl + nwr) {
-      const bool left = vw < nwl;
-      const int rel = left ? vw : vw - nwl;
-      const int len = left ? nl : nr, base = left ? 0 : nl, first = left ? ol : orr;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int o = 4 * rel + i - first;  // offset in the run
-        if (o >= 0 && o < len) sp[i] = s_inv[base + o] + a_off;
-      }
-      wr = left ? rel : (rel | 0x40000000);
-    }
-    wrel[m] = wr;
-    srcl[m] = sp[0] | (sp[1] << 16);
-    srch[m] = sp[2] | (sp[3] << 16);
-  }
-  // ---- bin columns, each from its stage
-  int c_fail = -1;
-#pragma unroll 1
-  for (int c = 0; c < F; ++c) {
-    const int k = c % kMvStages;
-    const uint8_t* stage = s_stage[k];
-    const bool ok = mbar_wait(&s_full[k], static_cast<uint32_t>((c / kMvStages) & 1), kMvWaitPolls);
-    if (ok) {
-      uint32_t* out = reinterpret_cast<uint32_t*>(bins_out + static_cast<int64_t>(c) * ldb);
-#pragma unroll
-      for (int m = 0; m < kMvWordsPerThread; ++m) {
-        const int wr = wrel[m];
-        if (wr < 0) continue;
-        const int64_t wa = (wr & 0x40000000) ? wr0 + (wr & 0x3fffffff) : wl0 + wr;
-        const uint32_t s0 = srcl[m] & 0xffffu, s1 = srcl[m] >> 16, s2 = srch[m] & 0xffffu, s3 = srch[m] >> 16;
-        if (s0 != 0xffffu && s1 != 0xffffu && s2 != 0xffffu && s3 != 0xffffu) {
-          out[wa] = static_cast<uint32_t>(stage[s0]) | (static_cast<uint32_t>(stage[s1]) << 8) |
-                    (static_cast<uint32_t>(stage[s2]) << 16) | (static_cast<uint32_t>(stage[s3]) << 24);
-        } else {  // a run starts or ends inside this word: write only its own bytes
-          uint8_t* ob = reinterpret_cast<uint8_t*>(out + wa);
-          if (s0 != 0xffffu) ob[0] = stage[s0];
-          if (s1 != 0xffffu) ob[1] = stage[s1];
-          if (s2 != 0xffffu) ob[2] = stage[s2];
-          if (s3 != 0xffffu) ob[3] = stage[s3];
-        }
-      }
-    }
-    if (__syncthreads_or(!ok)) {  // every thread is done with this stage (or a copy timed out)
-      c_fail = c;
-      break;
-    }
-    if (threadIdx.x == 0 && c + kMvStages < F)
-      bulk_load(s_stage[k], bins_in + static_cast<int64_t>(c + kMvStages) * ldb + a0, span, &s_full[k]);
-  }
-  if (c_fail >= 0 && threadIdx.x == 0) {
-    raise_error(err, kErrWaitTimeout);
-    // let the copies still in flight (columns c_fail .. issued - 1) land before the CTA's shared memory is
-    // released; each stage completes in order, so waiting for its last issued column suffices
-    const int issued = min(F, c_fail + kMvStages);
-    for (int c = c_fail; c < issued; ++c) {
-      if (c + kMvStages < issued) continue;  // a later column of the same stage is waited for instead
-      mbar_wait(&s_full[c % kMvStages], static_cast<uint32_t>((c / kMvStages) & 1), kMvWaitPolls);
-    }
-  }
+    move_positions(static_cast<const uint32_t*>(g_in), static_cast<uint32_t*>(g_out), p0, ru, s_inv);
+  move_positions(orig_in, orig_out, p0, ru, s_inv);
+  int64_t wa[kMvWordsPerThread];
+  uint32_t srcl[kMvWordsPerThread], srch[kMvWordsPerThread];
+  mv_own_words<2, false>(ru, s_inv, a_off, ldb, wa, srcl, srch);
+  mv_columns<false>(bins_in, bins_out, ldb, F, a0, span, nullptr, 0, s_stage, s_full, wa, srcl, srch, err);
 }
 
 // Last split level: the children are leaves, so nothing moves.  Every row
 // records its leaf: the child its split sends it to, or the slot's own node
-// when the slot did not split.
+// when the slot did not split.  With frozen_only, only the slots that did not
+// split record their rows (the others are handled at a later level).  Bins in
+// the row-block layout (pitch).
 __global__ void __launch_bounds__(kMvThreads)
-    mv_leaves_kernel(const uint8_t* __restrict__ bins_in, int64_t ldb, const uint32_t* __restrict__ orig_in,
-                     const uint8_t* __restrict__ go_right, const gbdt_level* __restrict__ level, int32_t max_slots,
-                     const gbdt_segment* __restrict__ seg, const Route* __restrict__ route,
-                     const int32_t* __restrict__ tile_start, const MvState* __restrict__ st,
-                     uint16_t* __restrict__ leaf_of_row) {
+    mv_leaves_kernel(const uint8_t* __restrict__ bins_in, int64_t pitch, const uint32_t* __restrict__ orig_in,
+                     const gbdt_level* __restrict__ level, int32_t max_slots, const gbdt_segment* __restrict__ seg,
+                     const Route* __restrict__ route, const int32_t* __restrict__ tile_start,
+                     const MvState* __restrict__ st, bool frozen_only, uint16_t* __restrict__ leaf_of_row) {
   const int t = blockIdx.x;
   if (t >= st->total_tiles) return;
   const int n_slots = min(level->n_slots, max_slots);
   const int s = slot_of_tile(tile_start, n_slots, t);
   const Route rt = route[s];
+  if (frozen_only && rt.feature >= 0) return;
   const int64_t p0 = seg[s].start + static_cast<int64_t>(t - tile_start[s]) * kMvTile;
   const int n = static_cast<int>(min(seg[s].start + seg[s].count - p0, static_cast<int64_t>(kMvTile)));
   if (rt.feature < 0) {
@@ -668,9 +776,306 @@ __global__ void __launch_bounds__(kMvThreads)
     for (int i = threadIdx.x; i < n; i += blockDim.x) leaf_of_row[orig_in[p0 + i]] = node;
     return;
   }
-  const uint8_t* col = bins_in + static_cast<int64_t>(rt.feature) * ldb;
-  for (int i = threadIdx.x; i < n; i += blockDim.x)
-    leaf_of_row[orig_in[p0 + i]] = static_cast<uint16_t>(rt.left_node + goes_right(col, rt.bin, go_right, p0 + i));
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    const int right = bins_in[rb_offset(rt.feature, p0 + i, pitch)] > rt.bin ? 1 : 0;
+    leaf_of_row[orig_in[p0 + i]] = static_cast<uint16_t>(rt.left_node + right);
+  }
+}
+
+// Column layout [F][ldb] -> row-block layout: one thread per (feature, row block) piece of 32 bytes;
+// consecutive threads take consecutive row blocks of one feature, so the reads are coalesced and
+// every write is one whole 32-byte sector.  Bytes of the last block past N are copied as they are.
+__global__ void cols_to_row_blocks_kernel(const uint8_t* __restrict__ cols, int64_t ldb, int64_t n_blocks,
+                                          int32_t F, uint8_t* __restrict__ rb, int64_t pitch) {
+  const int64_t pieces = n_blocks * F;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < pieces;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int f = static_cast<int>(i / n_blocks);
+    const int64_t blk = i - static_cast<int64_t>(f) * n_blocks;
+    const uint8_t* src = cols + static_cast<int64_t>(f) * ldb + blk * kRowBlock;
+    const uint4 a = *reinterpret_cast<const uint4*>(src);  // blk * 32 < N <= ldb, ldb % 16 == 0
+    const uint4 b = blk * kRowBlock + 32 <= ldb ? *reinterpret_cast<const uint4*>(src + 16) : make_uint4(0, 0, 0, 0);
+    uint4* dst = reinterpret_cast<uint4*>(rb + blk * pitch + static_cast<int64_t>(f) * kRowBlock);
+    dst[0] = a;
+    dst[1] = b;
+  }
+}
+
+// ------------------------------------------------------------------------- two levels at once
+// At an odd level the rows of each sibling pair still sit, unpartitioned, in
+// their parent's segment.  After the level's splits are known they move once,
+// straight into the four grandchildren's runs (child 0 left, child 0 right,
+// child 1 left, child 1 right); rows of a child that does not split record
+// that child as their leaf instead.  The grandchildren's segments are the
+// next level's (virtual) segments computed from the split records.
+struct PairRoute {
+  int64_t start, count;  // the pair's rows (both children) in the current order
+  int64_t dst[4];        // first position of each grandchild in the next order
+  int64_t want[4];       // its row count from the split records; -1: its child does not split
+  int32_t f1, b1;        // the parent's split: which child a row belongs to
+  int32_t f2[2], b2[2];  // the children's splits; f2 < 0: the child is a leaf
+  int32_t node[2];       // the children's node ids
+  int32_t left[2];       // node id of each child's left child
+};
+
+struct PairState {
+  int32_t n_pairs;
+  int32_t total_tiles;
+};
+
+struct RunPrefix {  // rows of each of the four runs before a tile
+  long long r[4];
+};
+
+// One CTA: the pair records of a level and the tiles per pair.  level, seg and
+// route_cur describe the level (slots in sibling pairs); route_prev and
+// pair_parent the level above; seg_next the next level.
+__global__ void pair_routes_kernel(const gbdt_level* __restrict__ level, int32_t max_slots,
+                                   const gbdt_segment* __restrict__ seg, const Route* __restrict__ route_cur,
+                                   const Route* __restrict__ route_prev, const int32_t* __restrict__ pair_parent,
+                                   const gbdt_segment* __restrict__ seg_next, PairRoute* __restrict__ pairs,
+                                   int32_t* __restrict__ tile_start, PairState* __restrict__ st) {
+  __shared__ int s_b[1024];
+  __shared__ int s_pre;
+  if (threadIdx.x == 0) s_pre = 0;
+  __syncthreads();
+  const int n_pairs = min(level->n_slots, max_slots) / 2;
+  for (int c0 = 0; c0 < n_pairs; c0 += blockDim.x) {
+    const int k = c0 + threadIdx.x;
+    int tiles = 0;
+    if (k < n_pairs) {
+      PairRoute pr;
+      const Route up = route_prev[pair_parent[k]];
+      pr.f1 = up.feature, pr.b1 = up.bin;
+      pr.start = seg[2 * k].start;
+      pr.count = seg[2 * k].count + seg[2 * k + 1].count;
+      for (int c = 0; c < 2; ++c) {
+        const Route rt = route_cur[2 * k + c];
+        pr.node[c] = level->node_begin + 2 * k + c;
+        pr.f2[c] = rt.feature, pr.b2[c] = rt.bin, pr.left[c] = rt.left_node;
+        for (int j = 0; j < 2; ++j) {
+          if (rt.feature >= 0) {
+            const gbdt_segment g2 = seg_next[2 * rt.pad + j];
+            pr.dst[2 * c + j] = g2.start, pr.want[2 * c + j] = g2.count;
+          } else {
+            pr.dst[2 * c + j] = 0, pr.want[2 * c + j] = -1;
+          }
+        }
+      }
+      pairs[k] = pr;
+      tiles = static_cast<int>((pr.count + kMvTile - 1) / kMvTile);
+    }
+    s_b[threadIdx.x] = tiles;
+    __syncthreads();
+    for (int o = 1; o < blockDim.x; o <<= 1) {
+      const int b = threadIdx.x >= o ? s_b[threadIdx.x - o] : 0;
+      __syncthreads();
+      s_b[threadIdx.x] += b;
+      __syncthreads();
+    }
+    if (k < n_pairs) tile_start[k] = s_pre + s_b[threadIdx.x] - tiles;
+    __syncthreads();
+    if (threadIdx.x == blockDim.x - 1) s_pre += s_b[threadIdx.x];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    tile_start[n_pairs] = s_pre;
+    st->n_pairs = n_pairs;
+    st->total_tiles = s_pre;
+  }
+}
+
+// Run of position p of pair pr: 0..3, or -1 when its child is a leaf (*child is set either way).
+// (bins in the row-block layout)
+__device__ __forceinline__ int pair_run(const PairRoute& pr, const uint8_t* __restrict__ bins, int64_t pitch,
+                                        int64_t p, int* child) {
+  const int c = bins[rb_offset(pr.f1, p, pitch)] > pr.b1 ? 1 : 0;
+  *child = c;
+  const int f2 = c ? pr.f2[1] : pr.f2[0];
+  if (f2 < 0) return -1;
+  const int b2 = c ? pr.b2[1] : pr.b2[0];
+  return 2 * c + (bins[rb_offset(f2, p, pitch)] > b2 ? 1 : 0);
+}
+
+__global__ void __launch_bounds__(kMvThreads)
+    pair_count_kernel(const uint8_t* __restrict__ bins, int64_t pitch, const PairRoute* __restrict__ pairs,
+                      const int32_t* __restrict__ tile_start, const PairState* __restrict__ st,
+                      int4* __restrict__ tile_cnt) {
+  const int t = blockIdx.x;
+  if (t >= st->total_tiles) return;
+  __shared__ int s_warp[33];
+  const int k = slot_of_tile(tile_start, st->n_pairs, t);
+  const PairRoute& pr = pairs[k];
+  const int64_t p0 = pr.start + static_cast<int64_t>(t - tile_start[k]) * kMvTile;
+  const int n = static_cast<int>(min(pr.start + pr.count - p0, static_cast<int64_t>(kMvTile)));
+  int c[4] = {0, 0, 0, 0};
+  for (int j = threadIdx.x; j < n; j += blockDim.x) {
+    int child;
+    const int r = pair_run(pr, bins, pitch, p0 + j, &child);
+    if (r >= 0) ++c[r];
+  }
+  int tot[4];
+  for (int r = 0; r < 4; ++r) block_scan_excl(c[r], s_warp, &tot[r]);
+  if (threadIdx.x == 0) tile_cnt[t] = make_int4(tot[0], tot[1], tot[2], tot[3]);
+}
+
+// One CTA: exclusive scan of each run's tile counts over all tiles; checks each
+// grandchild's total against its split record.
+__global__ void __launch_bounds__(1024)
+    pair_scan_kernel(const PairRoute* __restrict__ pairs, const int32_t* __restrict__ tile_start,
+                     const PairState* __restrict__ st, const int4* __restrict__ tile_cnt,
+                     RunPrefix* __restrict__ tile_excl, int32_t* __restrict__ err) {
+  __shared__ int s_warp[33];
+  __shared__ long long s_carry[4];
+  const int total = st->total_tiles;
+  if (threadIdx.x < 4) s_carry[threadIdx.x] = 0;
+  __syncthreads();
+  for (int c0 = 0; c0 < total; c0 += blockDim.x) {
+    const int t = c0 + threadIdx.x;
+    const int4 v = t < total ? tile_cnt[t] : make_int4(0, 0, 0, 0);
+    const int vv[4] = {v.x, v.y, v.z, v.w};
+    int ct[4], e[4];
+    for (int r = 0; r < 4; ++r) e[r] = block_scan_excl(vv[r], s_warp, &ct[r]);
+    if (t < total) {
+      RunPrefix x;
+      for (int r = 0; r < 4; ++r) x.r[r] = s_carry[r] + e[r];
+      tile_excl[t] = x;
+    }
+    __syncthreads();
+    if (threadIdx.x < 4) s_carry[threadIdx.x] += ct[threadIdx.x];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    RunPrefix x;
+    for (int r = 0; r < 4; ++r) x.r[r] = s_carry[r];
+    tile_excl[total] = x;
+  }
+  __syncthreads();
+  for (int k = threadIdx.x; k < st->n_pairs; k += blockDim.x) {
+    const RunPrefix a = tile_excl[tile_start[k]], b = tile_excl[tile_start[k + 1]];
+    for (int r = 0; r < 4; ++r)
+      if (pairs[k].want[r] >= 0 && b.r[r] - a.r[r] != pairs[k].want[r]) raise_error(err, kErrPartitionCount);
+  }
+}
+
+__global__ void __launch_bounds__(kMvThreads, 4)
+    pair_move_kernel(const __grid_constant__ CUtensorMap map_in, uint8_t* __restrict__ bins_out, int64_t pitch,
+                     const uint8_t* __restrict__ bins_in, int32_t F,
+                     const uint64_t* __restrict__ g_in, uint64_t* __restrict__ g_out,
+                     const uint32_t* __restrict__ orig_in, uint32_t* __restrict__ orig_out,
+                     const PairRoute* __restrict__ pairs, const int32_t* __restrict__ tile_start,
+                     const PairState* __restrict__ st, const RunPrefix* __restrict__ tile_excl,
+                     uint16_t* __restrict__ leaf_of_row, int32_t* __restrict__ err) {
+  __shared__ uint32_t s_mask[4][kMvChunks];  // per run, per 32-row chunk: rows of the run
+  __shared__ int s_cbase[4][kMvChunks];      // per run, per chunk: the run's rows before the chunk
+  __shared__ uint16_t s_inv[kMvTile];
+  __shared__ __align__(128) uint8_t s_stage[kMvStages][kMvStageBytes];
+  __shared__ __align__(8) uint64_t s_full[kMvStages];
+  __shared__ int s_warp[33];
+  const int t = blockIdx.x;
+  if (t >= st->total_tiles) return;
+  // the destinations come from the split records: if any run disagreed with its record (raised by
+  // the scan before this launch), nothing moves and the caller sees the error
+  if (*reinterpret_cast<volatile int32_t*>(err) & kErrPartitionCount) return;
+  const int k = slot_of_tile(tile_start, st->n_pairs, t);
+  const PairRoute pr = pairs[k];
+  const int64_t tile_off = static_cast<int64_t>(t - tile_start[k]) * kMvTile;
+  const int64_t p0 = pr.start + tile_off;
+  const int n = static_cast<int>(min(pr.start + pr.count - p0, static_cast<int64_t>(kMvTile)));
+  const int z0 = static_cast<int>(p0 >> 5);     // first row block of the tile
+  const int a_off = static_cast<int>(p0 & 31);  // stage index of tile position 0
+  mv_start_copies<true>(s_stage, s_full, bins_in, 0, F, 0, 0, &map_in, z0);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  // ---- rank the tile (lane = row) into four runs; rows of a leaf child record their leaf
+#pragma unroll 1
+  for (int kk = 0; kk < kMvChunksPerWarp; ++kk) {
+    const int ch = warp * kMvChunksPerWarp + kk;
+    const int j = ch * 32 + lane;
+    int r = -1;
+    if (j < n) {
+      int child;
+      r = pair_run(pr, bins_in, pitch, p0 + j, &child);
+      if (r < 0 && leaf_of_row)
+        leaf_of_row[orig_in[p0 + j]] = static_cast<uint16_t>(child ? pr.node[1] : pr.node[0]);
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint32_t m = __ballot_sync(0xffffffffu, r == q);
+      if (lane == 0) s_mask[q][ch] = m;
+    }
+  }
+  __syncthreads();
+  int len[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int c = threadIdx.x < kMvChunks ? __popc(s_mask[q][threadIdx.x]) : 0;
+    const int e = block_scan_excl(c, s_warp, &len[q]);
+    if (threadIdx.x < kMvChunks) s_cbase[q][threadIdx.x] = e;
+  }
+  __syncthreads();
+  MvRuns<4> ru;
+  const RunPrefix ex = tile_excl[t], ex0 = tile_excl[tile_start[k]];
+  int acc = 0;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    ru.dst[q] = pr.dst[q] + (ex.r[q] - ex0.r[q]);
+    ru.len[q] = len[q];
+    ru.base[q] = acc;
+    acc += len[q];
+  }
+  const uint32_t lt = (1u << lane) - 1u;
+#pragma unroll 1
+  for (int kk = 0; kk < kMvChunksPerWarp; ++kk) {
+    const int ch = warp * kMvChunksPerWarp + kk;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint32_t m = s_mask[q][ch];
+      if (m >> lane & 1u) s_inv[ru.base[q] + s_cbase[q][ch] + __popc(m & lt)] = static_cast<uint16_t>(ch * 32 + lane);
+    }
+  }
+  __syncthreads();
+  // ---- gradient and row id, while the first column copies are in flight
+  move_positions(g_in, g_out, p0, ru, s_inv);
+  move_positions(orig_in, orig_out, p0, ru, s_inv);
+  int64_t wa[kMvWordsPerThread];
+  uint32_t srcl[kMvWordsPerThread], srch[kMvWordsPerThread];
+  mv_own_words<4, true>(ru, s_inv, a_off, pitch, wa, srcl, srch);
+  mv_columns<true>(bins_in, bins_out, pitch, F, 0, 0, &map_in, z0, s_stage, s_full, wa, srcl, srch, err);
+}
+
+// Last split level when it is an odd level: every row of a pair records its
+// leaf (a grandchild when its child splits, else the child), nothing moves.
+__global__ void __launch_bounds__(kMvThreads)
+    pair_leaves_kernel(const uint8_t* __restrict__ bins_in, int64_t pitch, const uint32_t* __restrict__ orig_in,
+                       const PairRoute* __restrict__ pairs, const int32_t* __restrict__ tile_start,
+                       const PairState* __restrict__ st, uint16_t* __restrict__ leaf_of_row) {
+  const int t = blockIdx.x;
+  if (t >= st->total_tiles) return;
+  const int k = slot_of_tile(tile_start, st->n_pairs, t);
+  const PairRoute pr = pairs[k];
+  const int64_t p0 = pr.start + static_cast<int64_t>(t - tile_start[k]) * kMvTile;
+  const int n = static_cast<int>(min(pr.start + pr.count - p0, static_cast<int64_t>(kMvTile)));
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    int child;
+    const int r = pair_run(pr, bins_in, pitch, p0 + i, &child);
+    const int node = child ? pr.node[1] : pr.node[0], left = child ? pr.left[1] : pr.left[0];
+    leaf_of_row[orig_in[p0 + i]] = static_cast<uint16_t>(r < 0 ? node : left + (r & 1));
+  }
+}
+
+// Odd level: each slot's histogram scans its pair's rows (its parent's
+// segment) with the parent's split as the filter.
+__global__ void pair_scan_ranges_kernel(const gbdt_level* __restrict__ level, int32_t max_slots,
+                                        const gbdt_segment* __restrict__ seg, const Route* __restrict__ route_prev,
+                                        const int32_t* __restrict__ pair_parent, gbdt_segment* __restrict__ scan,
+                                        gbdt_filter* __restrict__ filters) {
+  const int n_slots = min(level->n_slots, max_slots);
+  for (int s = blockIdx.x * blockDim.x + threadIdx.x; s < n_slots; s += gridDim.x * blockDim.x) {
+    const int k = s >> 1;
+    const Route up = route_prev[pair_parent[k]];
+    scan[s] = gbdt_segment{seg[2 * k].start, seg[2 * k].count + seg[2 * k + 1].count};
+    filters[s] = gbdt_filter{up.feature, up.bin, s & 1, 0};
+  }
 }
 
 // One CTA: routing of every slot from its split record; the k-th splitting slot
@@ -736,8 +1141,9 @@ size_t seg_hist_scratch_bytes(int32_t max_slots) {
 
 int launch_seg_histograms(const SegHistPlan& plan, const uint8_t* bins, int64_t ldb, int64_t N, int32_t F,
                           const void* g, int32_t g_dtype, const int32_t* fixed_exp, const gbdt_level* level,
-                          int32_t max_slots, const uint8_t* build_flag, const gbdt_segment* seg, void* scratch,
-                          uint32_t* hist_cnt, int64_t* hist_q, cudaStream_t s) {
+                          int32_t max_slots, const uint8_t* build_flag, const gbdt_segment* seg,
+                          const gbdt_filter* filters, void* scratch, uint32_t* hist_cnt, int64_t* hist_q,
+                          cudaStream_t s, bool row_blocks) {
   (void)N;
   Carve c(scratch, seg_hist_scratch_bytes(max_slots));
   SegWork* st = c.take<SegWork>(1);
@@ -752,27 +1158,67 @@ int launch_seg_histograms(const SegHistPlan& plan, const uint8_t* bins, int64_t 
   const bool v8 = aligned(bins, 32) && ldb % 32 == 0;
   auto launch = [&](auto kernel, const auto* gp) -> int {
     GBDT_CUDA(smem_attr(kernel, plan.smem));
-    kernel<<<grid, kSegThreads, plan.smem, s>>>(bins, ldb, F, gp, fixed_exp, seg, build_slot, row_start, st,
-                                                plan.group_feats, hist_cnt, hist_q);
+    kernel<<<grid, kSegThreads, plan.smem, s>>>(bins, ldb, F, gp, fixed_exp, seg, filters, build_slot, row_start,
+                                                st, plan.group_feats, hist_cnt, hist_q);
     return GBDT_OK;
   };
   int rc;
   if (g_dtype == GBDT_DTYPE_F32) {
     const float* gp = static_cast<const float*>(g);
-    rc = v8 ? launch(seg_hist_kernel<float, true>, gp) : launch(seg_hist_kernel<float, false>, gp);
+    rc = row_blocks ? launch(seg_hist_kernel<float, true, true>, gp)
+         : v8       ? launch(seg_hist_kernel<float, true, false>, gp)
+                    : launch(seg_hist_kernel<float, false, false>, gp);
   } else {
     const double* gp = static_cast<const double*>(g);
-    rc = v8 ? launch(seg_hist_kernel<double, true>, gp) : launch(seg_hist_kernel<double, false>, gp);
+    rc = row_blocks ? launch(seg_hist_kernel<double, true, true>, gp)
+         : v8       ? launch(seg_hist_kernel<double, true, false>, gp)
+                    : launch(seg_hist_kernel<double, false, false>, gp);
   }
   if (rc != GBDT_OK) return rc;
   count_launches();
   return GBDT_OK;
 }
 
-size_t move_scratch_bytes(int64_t N, int32_t max_slots) {
+namespace {
+size_t two_way_scratch_bytes(int64_t N, int32_t max_slots) {
   const size_t tiles = static_cast<size_t>(ceil_div(N, kMvTile)) + max_slots;
   return sizeof(MvState) + sizeof(int32_t) * (max_slots + 1) + sizeof(int32_t) * tiles +
          sizeof(int64_t) * (tiles + 1) + sizeof(int64_t) * max_slots + 6 * kWsAlign;
+}
+
+size_t pair_scratch_bytes(int64_t N, int32_t max_slots) {
+  const size_t pairs = static_cast<size_t>(max_slots) / 2 + 1;
+  const size_t tiles = static_cast<size_t>(ceil_div(N, kMvTile)) + pairs;
+  return sizeof(PairState) + sizeof(PairRoute) * pairs + sizeof(int32_t) * (pairs + 1) + sizeof(int4) * tiles +
+         sizeof(RunPrefix) * (tiles + 1) + 6 * kWsAlign;
+}
+
+struct PairScratch {
+  PairState* st;
+  PairRoute* pairs;
+  int32_t* tile_start;
+  int4* tile_cnt;
+  RunPrefix* tile_excl;
+  int max_tiles;
+};
+
+PairScratch carve_pairs(void* scratch, int64_t N, int32_t max_slots) {
+  Carve c(scratch, pair_scratch_bytes(N, max_slots));
+  PairScratch p;
+  const int pairs = max_slots / 2 + 1;
+  p.max_tiles = ceil_div(N, kMvTile) + pairs;
+  p.st = c.take<PairState>(1);
+  p.pairs = c.take<PairRoute>(pairs);
+  p.tile_start = c.take<int32_t>(pairs + 1);
+  p.tile_cnt = c.take<int4>(p.max_tiles);
+  p.tile_excl = c.take<RunPrefix>(p.max_tiles + 1);
+  return p;
+}
+}  // namespace
+
+size_t move_scratch_bytes(int64_t N, int32_t max_slots) {
+  const size_t a = two_way_scratch_bytes(N, max_slots), b = pair_scratch_bytes(N, max_slots);
+  return a > b ? a : b;
 }
 
 void launch_move_rows(const uint8_t* bins_in, uint8_t* bins_out, int64_t ldb, int64_t N, int32_t F,
@@ -780,7 +1226,7 @@ void launch_move_rows(const uint8_t* bins_in, uint8_t* bins_out, int64_t ldb, in
                       const uint8_t* go_right, const gbdt_level* level, int32_t max_slots, const gbdt_segment* seg,
                       const Route* route, const gbdt_split* splits, gbdt_segment* seg_out,
                       uint16_t* leaf_of_row, void* scratch, int32_t* err, cudaStream_t s) {
-  Carve c(scratch, move_scratch_bytes(N, max_slots));
+  Carve c(scratch, two_way_scratch_bytes(N, max_slots));
   MvState* st = c.take<MvState>(1);
   int32_t* tile_start = c.take<int32_t>(max_slots + 1);
   const int max_tiles = ceil_div(N, kMvTile) + max_slots;
@@ -796,24 +1242,109 @@ void launch_move_rows(const uint8_t* bins_in, uint8_t* bins_out, int64_t ldb, in
                                     seg_out, splits, err);
   count_launches();
   mv_move_kernel<<<max_tiles, kMvThreads, 0, s>>>(bins_in, bins_out, ldb, F, g_in, g_out, g_size, orig_in, orig_out,
-                                             go_right,
-                                             level, max_slots, seg, route, tile_start, st, tile_excl, seg_left,
-                                             leaf_of_row, err);
+                                                  go_right, level, max_slots, seg, route, tile_start, st, tile_excl,
+                                                  seg_left, leaf_of_row, err);
   count_launches();
 }
 
-void launch_leaf_rows(const uint8_t* bins_in, int64_t ldb, int64_t N, const uint32_t* orig_in,
-                      const uint8_t* go_right, const gbdt_level* level, int32_t max_slots, const gbdt_segment* seg,
-                      const Route* route, uint16_t* leaf_of_row, void* scratch, cudaStream_t s) {
-  Carve c(scratch, move_scratch_bytes(N, max_slots));
+void launch_leaf_rows(const uint8_t* bins_rb, int64_t pitch, int64_t N, const uint32_t* orig_in,
+                      const gbdt_level* level, int32_t max_slots, const gbdt_segment* seg, const Route* route,
+                      bool frozen_only, uint16_t* leaf_of_row, void* scratch, cudaStream_t s) {
+  Carve c(scratch, two_way_scratch_bytes(N, max_slots));
   MvState* st = c.take<MvState>(1);
   int32_t* tile_start = c.take<int32_t>(max_slots + 1);
   const int max_tiles = ceil_div(N, kMvTile) + max_slots;
   mv_setup_kernel<<<1, 1024, 0, s>>>(level, max_slots, seg, tile_start, st);
   count_launches();
-  mv_leaves_kernel<<<max_tiles, kMvThreads, 0, s>>>(bins_in, ldb, orig_in, go_right, level, max_slots, seg, route,
-                                                    tile_start, st, leaf_of_row);
+  mv_leaves_kernel<<<max_tiles, kMvThreads, 0, s>>>(bins_rb, pitch, orig_in, level, max_slots, seg, route, tile_start,
+                                                    st, frozen_only, leaf_of_row);
   count_launches();
+}
+
+void launch_pair_scan_ranges(const gbdt_level* level, int32_t max_slots, const gbdt_segment* seg,
+                             const Route* route_prev, const int32_t* pair_parent, gbdt_segment* scan,
+                             gbdt_filter* filters, cudaStream_t s) {
+  pair_scan_ranges_kernel<<<ceil_div(max_slots, 256), 256, 0, s>>>(level, max_slots, seg, route_prev, pair_parent,
+                                                                    scan, filters);
+  count_launches();
+}
+
+void launch_move_pairs(const CUtensorMap& map_in, const uint8_t* bins_rb_in, uint8_t* bins_rb_out, int64_t pitch,
+                       int64_t N, int32_t F, const double* g_in, double* g_out, const uint32_t* orig_in,
+                       uint32_t* orig_out, const gbdt_level* level, int32_t max_slots, const gbdt_segment* seg,
+                       const Route* route_cur, const Route* route_prev, const int32_t* pair_parent,
+                       const gbdt_segment* seg_next, uint16_t* leaf_of_row, void* scratch, int32_t* err,
+                       cudaStream_t s) {
+  const PairScratch p = carve_pairs(scratch, N, max_slots);
+  pair_routes_kernel<<<1, 1024, 0, s>>>(level, max_slots, seg, route_cur, route_prev, pair_parent, seg_next, p.pairs,
+                                        p.tile_start, p.st);
+  count_launches();
+  pair_count_kernel<<<p.max_tiles, kMvThreads, 0, s>>>(bins_rb_in, pitch, p.pairs, p.tile_start, p.st, p.tile_cnt);
+  count_launches();
+  pair_scan_kernel<<<1, 1024, 0, s>>>(p.pairs, p.tile_start, p.st, p.tile_cnt, p.tile_excl, err);
+  count_launches();
+  pair_move_kernel<<<p.max_tiles, kMvThreads, 0, s>>>(
+      map_in, bins_rb_out, pitch, bins_rb_in, F, reinterpret_cast<const uint64_t*>(g_in),
+      reinterpret_cast<uint64_t*>(g_out), orig_in, orig_out, p.pairs, p.tile_start, p.st, p.tile_excl, leaf_of_row,
+      err);
+  count_launches();
+}
+
+void launch_leaf_pairs(const uint8_t* bins_rb, int64_t pitch, int64_t N, const uint32_t* orig_in,
+                       const gbdt_level* level, int32_t max_slots, const gbdt_segment* seg, const Route* route_cur,
+                       const Route* route_prev, const int32_t* pair_parent, const gbdt_segment* seg_next,
+                       uint16_t* leaf_of_row, void* scratch, cudaStream_t s) {
+  const PairScratch p = carve_pairs(scratch, N, max_slots);
+  pair_routes_kernel<<<1, 1024, 0, s>>>(level, max_slots, seg, route_cur, route_prev, pair_parent, seg_next, p.pairs,
+                                        p.tile_start, p.st);
+  count_launches();
+  pair_leaves_kernel<<<p.max_tiles, kMvThreads, 0, s>>>(bins_rb, pitch, orig_in, p.pairs, p.tile_start, p.st,
+                                                        leaf_of_row);
+  count_launches();
+}
+
+size_t row_block_bytes(int64_t N, int32_t F) { return static_cast<size_t>(rb_blocks(N)) * rb_pitch(F); }
+
+void launch_cols_to_row_blocks(const uint8_t* cols, int64_t ldb, int64_t N, int32_t F, uint8_t* rb, cudaStream_t s) {
+  const int64_t pieces = rb_blocks(N) * F;
+  const int grid = static_cast<int>(std::min<int64_t>((pieces + 255) / 256, static_cast<int64_t>(sm_count()) * 16));
+  cols_to_row_blocks_kernel<<<grid, 256, 0, s>>>(cols, ldb, rb_blocks(N), F, rb, rb_pitch(F));
+  count_launches();
+}
+
+// The tensor map the pair move reads a row-block buffer through: a 3-D byte tensor (32 bytes of a
+// row block, F features, the row blocks) and a box of one feature over kMvBoxBlocks row blocks.
+int make_row_block_map(CUtensorMap* map, const uint8_t* rb, int64_t N, int32_t F) {
+  using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+  static EncodeTiled encode = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      encode = reinterpret_cast<EncodeTiled>(fn);
+  });
+  if (!encode) {
+    set_error("tensor-map encoding is not available from the CUDA driver");
+    return GBDT_ERR_CUDA;
+  }
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kRowBlock), static_cast<cuuint64_t>(F),
+                              static_cast<cuuint64_t>(rb_blocks(N))};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kRowBlock), static_cast<cuuint64_t>(rb_pitch(F))};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(kRowBlock), 1u, static_cast<cuuint32_t>(kMvBoxBlocks)};
+  const cuuint32_t elem[3] = {1u, 1u, 1u};
+  const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t*>(rb), dims, strides, box, elem,
+                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    set_error("cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
+    return GBDT_ERR_CUDA;
+  }
+  return GBDT_OK;
 }
 
 }  // namespace gbdt
@@ -827,8 +1358,9 @@ extern "C" size_t gbdt_histograms_segmented_workspace_size(int32_t max_slots) {
 extern "C" int gbdt_build_histograms_segmented(const uint8_t* bins, int64_t ldb, int64_t N, int32_t F, const void* g,
                                                int32_t g_dtype, const int32_t* fixed_exp, const gbdt_level* level,
                                                int32_t max_slots, const uint8_t* build_flag, int32_t max_build,
-                                               const gbdt_segment* segments, uint32_t* hist_cnt, int64_t* hist_q,
-                                               void* ws, size_t ws_bytes, void* stream) {
+                                               const gbdt_segment* segments, const gbdt_filter* filters,
+                                               uint32_t* hist_cnt, int64_t* hist_q, void* ws, size_t ws_bytes,
+                                               void* stream) {
   clear_error();
   GBDT_CHECK_ARG(bins && g && fixed_exp && level && build_flag && segments && hist_cnt && hist_q,
                  "gbdt_build_histograms_segmented: null pointer");
@@ -846,7 +1378,7 @@ extern "C" int gbdt_build_histograms_segmented(const uint8_t* bins, int64_t ldb,
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const SegHistPlan plan = plan_seg_histograms(N, F, max_slots, max_build);
   int rc = launch_seg_histograms(plan, bins, ldb, N, F, g, g_dtype, fixed_exp, level, max_slots, build_flag, segments,
-                                 ws, hist_cnt, hist_q, s);
+                                 filters, ws, hist_cnt, hist_q, s);
   if (rc != GBDT_OK) return rc;
   GBDT_LAUNCH_CHECK();
   return GBDT_OK;

@@ -28,7 +28,8 @@ struct SlotTotals {
 struct LevelStats {
   int64_t n_act;         // rows in the level's nodes
   int64_t n_built_rows;  // rows of the nodes whose histograms are built directly
-  int64_t n_split_rows;  // rows of the nodes that split (moved by the partition)
+  int64_t n_split_rows;  // rows of the nodes that split
+  int64_t n_scan_rows;   // rows the histogram pass reads (at odd levels a built node's whole pair)
   int32_t n_slots;
   int32_t n_built;
 };
@@ -74,11 +75,11 @@ __global__ void __launch_bounds__(1024)
                        LevelStats* __restrict__ stats, int32_t* __restrict__ err) {
   __shared__ int s_a[1024];
   __shared__ int s_pre;
-  __shared__ unsigned long long s_act, s_built_rows, s_split_rows;
+  __shared__ unsigned long long s_act, s_built_rows, s_split_rows, s_scan_rows;
   __shared__ int s_built;
   if (threadIdx.x == 0) {
     s_pre = 0;
-    s_act = s_built_rows = s_split_rows = 0;
+    s_act = s_built_rows = s_split_rows = s_scan_rows = 0;
     s_built = 0;
   }
   __syncthreads();
@@ -110,6 +111,9 @@ __global__ void __launch_bounds__(1024)
       if (d < D && build_flag[s]) {
         atomicAdd(&s_built, 1);
         atomicAdd(&s_built_rows, static_cast<unsigned long long>(tot.cnt));
+        // at odd levels a node's rows still sit in its pair's (its parent's) segment
+        const int64_t scan = (d & 1) ? seg[s & ~1].count + seg[s | 1].count : seg[s].count;
+        atomicAdd(&s_scan_rows, static_cast<unsigned long long>(scan));
       }
       if (is_split) atomicAdd(&s_split_rows, static_cast<unsigned long long>(tot.cnt));
       if (seg[s].count != static_cast<int64_t>(tot.cnt)) raise_error(err, kErrHistTotals);
@@ -168,6 +172,7 @@ __global__ void __launch_bounds__(1024)
     stats->n_act = static_cast<int64_t>(s_act);
     stats->n_built_rows = static_cast<int64_t>(s_built_rows);
     stats->n_split_rows = static_cast<int64_t>(s_split_rows);
+    stats->n_scan_rows = static_cast<int64_t>(s_scan_rows);
     stats->n_slots = n_slots;
     stats->n_built = s_built;
   }
@@ -177,10 +182,13 @@ struct TrainWs {
   double* g0;         // gradients in original row order (level 0 positions)
   uint32_t* orig0;    // identity: original row id of level-0 positions
   uint16_t* leaf;     // leaf of each original row in the current tree
-  uint8_t* bins_xy[2];  // per-position copies for levels >= 1 (alternating)
+  uint8_t* bins_rb0;    // the caller's bins in the row-block layout (levels 0 and 1)
+  uint8_t* bins_xy[2];  // row-block copies in later orders (alternating)
   double* g_xy[2];
   uint32_t* orig_xy[2];
   gbdt_segment* seg[2];
+  gbdt_segment* scan;    // odd levels: each slot's scan range (its pair's rows)
+  gbdt_filter* filters;  // odd levels: each slot's side of its parent's split
   void* seg_scratch;
   void* move_scratch;
   uint32_t* hist_cnt[2];
@@ -190,8 +198,8 @@ struct TrainWs {
   SlotTotals* totals[2];
   gbdt_level* level[2];
   uint8_t* build[2];
-  int32_t* pair_parent;
-  Route* route;
+  int32_t* pair_parent[2];  // by level parity: sibling pair -> parent slot
+  Route* route[2];          // by level parity: each slot's split routing
   gbdt_node* trees;
   int32_t* n_nodes;
   LevelStats* stats;
@@ -219,13 +227,16 @@ TrainWs carve_train(void* ws, size_t bytes, int64_t N, int32_t F, int64_t ldb, c
   w.orig0 = c.take<uint32_t>(n16);
   w.leaf = c.take<uint16_t>(n16);
   if (D >= 1) {
+    w.bins_rb0 = c.take<uint8_t>(row_block_bytes(N, F));
     for (int i = 0; i < 2; ++i) {
-      w.bins_xy[i] = c.take<uint8_t>(static_cast<size_t>(F) * ldb);
+      w.bins_xy[i] = c.take<uint8_t>(row_block_bytes(N, F));
       w.g_xy[i] = c.take<double>(n16);
       w.orig_xy[i] = c.take<uint32_t>(n16);
     }
   }
   for (int i = 0; i < 2; ++i) w.seg[i] = c.take<gbdt_segment>(level_slots);
+  w.scan = c.take<gbdt_segment>(level_slots);
+  w.filters = c.take<gbdt_filter>(level_slots);
   w.seg_scratch = c.take<unsigned char>(seg_hist_scratch_bytes(static_cast<int32_t>(hist_slots)));
   w.move_scratch = c.take<unsigned char>(move_scratch_bytes(N, level_slots));
   for (int i = 0; i < 2; ++i) {
@@ -239,8 +250,10 @@ TrainWs carve_train(void* ws, size_t bytes, int64_t N, int32_t F, int64_t ldb, c
     w.level[i] = c.take<gbdt_level>(1);
     w.build[i] = c.take<uint8_t>(level_slots);
   }
-  w.pair_parent = c.take<int32_t>(level_slots / 2 + 1);
-  w.route = c.take<Route>(level_slots);
+  for (int i = 0; i < 2; ++i) {
+    w.pair_parent[i] = c.take<int32_t>(level_slots / 2 + 1);
+    w.route[i] = c.take<Route>(level_slots);
+  }
   w.trees = c.take<gbdt_node>(static_cast<size_t>(T) * max_nodes_of(D));
   w.n_nodes = c.take<int32_t>(T);
   w.stats = c.take<LevelStats>(static_cast<size_t>(T) * (D + 1));
@@ -339,6 +352,18 @@ extern "C" int gbdt_train(const uint8_t* bins, int64_t ldb, const int32_t* n_bin
   launch_label_mean(w.label_partials, N, w.init, s);
   iota_kernel<<<sm_count() * 4, 256, 0, s>>>(w.orig0, N);
   count_launches();
+  // the training levels read the bins in the row-block layout; the pair moves read them through
+  // tensor maps (one per buffer: the converted input and the two alternating orders)
+  const int64_t pitch = rb_pitch(F);
+  CUtensorMap maps[3];
+  if (D >= 1) {
+    launch_cols_to_row_blocks(bins, ldb, N, F, w.bins_rb0, s);
+    const uint8_t* bufs[3] = {w.bins_rb0, w.bins_xy[0], w.bins_xy[1]};
+    for (int i = 0; i < 3; ++i) {
+      rc = make_row_block_map(&maps[i], bufs[i], N, F);
+      if (rc != GBDT_OK) return rc;
+    }
+  }
   const int fail_after = g_fail_after_levels.load();
   int levels_done = 0;
   for (int t = 0; t < T; ++t) {
@@ -357,42 +382,65 @@ extern "C" int gbdt_train(const uint8_t* bins, int64_t ldb, const int32_t* n_bin
     }
     for (int d = 0; d <= D; ++d) {
       const int cur = d & 1, nxt = cur ^ 1;
+      const bool odd = (d & 1) != 0;
       const int max_slots = 1 << d;
       LevelStats* st = w.stats + static_cast<size_t>(t) * (D + 1) + d;
-      // per-position data of level d: the caller's bins and g0 at level 0, then alternating copies
-      const uint8_t* lb = d == 0 ? bins : w.bins_xy[(d - 1) & 1];
-      const double* lg = d == 0 ? w.g0 : w.g_xy[(d - 1) & 1];
-      const uint32_t* lo = d == 0 ? w.orig0 : w.orig_xy[(d - 1) & 1];
+      // Rows are partitioned every second level: levels 0 and 1 read the caller's order; after each
+      // odd level the rows move straight into the order of the level below it.  At an odd level a
+      // node's rows still sit in its pair's segment, and its histogram filters them by the parent's
+      // split; its segment is where its rows will be once they move (a virtual segment).
+      const int ph = d < 2 ? -1 : ((d >> 1) - 1) & 1;
+      const uint8_t* lb = D == 0 ? bins : ph < 0 ? w.bins_rb0 : w.bins_xy[ph];
+      const double* lg = ph < 0 ? w.g0 : w.g_xy[ph];
+      const uint32_t* lo = ph < 0 ? w.orig0 : w.orig_xy[ph];
       if (d < D) {
         const int max_build = d == 0 ? 1 : max_slots / 2;
         const SegHistPlan plan = plan_seg_histograms(N, F, max_slots, max_build);
         if (timing) GBDT_CUDA(cudaEventRecord(ev_hist(t, d, 0), s));
-        rc = launch_seg_histograms(plan, lb, ldb, N, F, lg, GBDT_DTYPE_F64, w.fixed_exp, w.level[cur], max_slots,
-                                   w.build[cur], w.seg[cur], w.seg_scratch, w.hist_cnt[cur], w.hist_q[cur], s);
+        const gbdt_segment* hseg = w.seg[cur];
+        const gbdt_filter* hfil = nullptr;
+        if (odd) {
+          launch_pair_scan_ranges(w.level[cur], max_slots, w.seg[cur], w.route[nxt], w.pair_parent[cur], w.scan,
+                                  w.filters, s);
+          hseg = w.scan;
+          hfil = w.filters;
+        }
+        rc = launch_seg_histograms(plan, lb, pitch, N, F, lg, GBDT_DTYPE_F64, w.fixed_exp, w.level[cur], max_slots,
+                                   w.build[cur], hseg, hfil, w.seg_scratch, w.hist_cnt[cur], w.hist_q[cur], s,
+                                   true);
         if (rc != GBDT_OK) return rc;
         if (timing) GBDT_CUDA(cudaEventRecord(ev_hist(t, d, 1), s));
         if (d > 0) {
-          launch_hist_subtract(w.hist_cnt[nxt], w.hist_q[nxt], w.pair_parent, w.build[cur], w.level[cur], max_slots,
-                               F, w.hist_cnt[cur], w.hist_q[cur], w.err, s);
+          launch_hist_subtract(w.hist_cnt[nxt], w.hist_q[nxt], w.pair_parent[cur], w.build[cur], w.level[cur],
+                               max_slots, F, w.hist_cnt[cur], w.hist_q[cur], w.err, s);
         }
         launch_find_splits(w.hist_cnt[cur], w.hist_q[cur], w.fixed_exp, F, n_bins, w.level[cur], max_slots, *p,
                            w.splits, w.split_scratch, w.err, s);
       }
       apply_level_kernel<<<1, 1024, 0, s>>>(d, D, w.level[cur], max_slots, d < D ? w.splits : nullptr, w.totals[cur],
                                             w.build[cur], w.fixed_exp, p->reg_lambda, w.seg[cur], tree,
-                                            w.n_nodes + t, w.level[nxt], w.totals[nxt], w.seg[nxt], w.pair_parent,
-                                            w.build[nxt], w.route, st, w.err);
+                                            w.n_nodes + t, w.level[nxt], w.totals[nxt], w.seg[nxt],
+                                            w.pair_parent[nxt], w.build[nxt], w.route[cur], st, w.err);
       count_launches();
-      // move the rows of split nodes into child order; frozen nodes record their rows' leaf.  At the last
-      // split level the children are leaves: rows only record them, nothing moves (and at the leaf level
-      // itself there is then nothing left to do, except for a tree that is a single leaf).
+      // rows: after an odd level they move into the next order (four grandchild runs per pair); at
+      // even levels nothing moves and the rows of nodes that do not split record their leaf; at the
+      // last split level every row records its leaf.
       if (timing) GBDT_CUDA(cudaEventRecord(ev_hist(t, d, 2), s));
-      if (d + 1 < D) {
-        launch_move_rows(lb, w.bins_xy[d & 1], ldb, N, F, lg, w.g_xy[d & 1], 8, lo, w.orig_xy[d & 1], nullptr,
-                         w.level[cur], max_slots, w.seg[cur], w.route, w.splits, nullptr, w.leaf, w.move_scratch,
-                         w.err, s);
+      if (d < D && d + 1 < D) {
+        if (odd) {
+          const int out = ((d + 1) >> 1) - 1 & 1;
+          launch_move_pairs(maps[ph + 1], lb, w.bins_xy[out], pitch, N, F, lg, w.g_xy[out], lo, w.orig_xy[out],
+                            w.level[cur], max_slots, w.seg[cur], w.route[cur], w.route[nxt], w.pair_parent[cur],
+                            w.seg[nxt], w.leaf, w.move_scratch, w.err, s);
+        } else {
+          launch_leaf_rows(lb, pitch, N, lo, w.level[cur], max_slots, w.seg[cur], w.route[cur], true, w.leaf,
+                           w.move_scratch, s);
+        }
+      } else if (d + 1 == D && odd) {
+        launch_leaf_pairs(lb, pitch, N, lo, w.level[cur], max_slots, w.seg[cur], w.route[cur], w.route[nxt],
+                          w.pair_parent[cur], w.seg[nxt], w.leaf, w.move_scratch, s);
       } else if (d + 1 == D || D == 0) {
-        launch_leaf_rows(lb, ldb, N, lo, nullptr, w.level[cur], max_slots, w.seg[cur], w.route, w.leaf,
+        launch_leaf_rows(lb, pitch, N, lo, w.level[cur], max_slots, w.seg[cur], w.route[cur], false, w.leaf,
                          w.move_scratch, s);
       }
       if (timing) GBDT_CUDA(cudaEventRecord(ev_hist(t, d, 3), s));
@@ -464,26 +512,32 @@ extern "C" int gbdt_train(const uint8_t* bins, int64_t ldb, const int32_t* n_bin
     float ms = 0.f;
     GBDT_CUDA(cudaEventElapsedTime(&ms, pool.ev[0], pool.ev[1]));
     dg.total_ms = ms;
-    const double row_bytes = static_cast<double>(F) + 8.0;       // a built row: bins + fp64 g
-    const double move_bytes = 2.0 * (F + 8.0 + 4.0) + 1.0;       // a moved row: read + write, + split column
+    const double row_bytes = static_cast<double>(F) + 8.0;       // a scanned row: bins + fp64 g
+    const double move_bytes = 2.0 * (F + 8.0 + 4.0);             // a moved row: read + write every column
     for (int t = 0; t < T; ++t) {
       for (int d = 0; d <= D; ++d) {
         const LevelStats& ls = h_stats[static_cast<size_t>(t) * (D + 1) + d];
+        const bool odd = (d & 1) != 0;
         if (d < D) {
           GBDT_CUDA(cudaEventElapsedTime(&ms, ev_hist(t, d, 0), ev_hist(t, d, 1)));
           dg.hist_ms += ms;
           dg.hist_launches += 1;
           dg.hist_rows += ls.n_built_rows;
-          dg.hist_bytes += static_cast<double>(ls.n_built_rows) * row_bytes +
+          dg.hist_bytes += static_cast<double>(ls.n_scan_rows) * (row_bytes + (odd ? 1.0 : 0.0)) +
                            static_cast<double>(ls.n_built) * F * kBins * 12.0;
         }
         GBDT_CUDA(cudaEventElapsedTime(&ms, ev_hist(t, d, 2), ev_hist(t, d, 3)));
         dg.part_ms += ms;
-        // moved rows read and write every column; a row that only records its leaf reads its row id (and
-        // the split column, when its slot split) and writes a 2-byte leaf id
-        const bool moves = d + 1 < D;
-        dg.part_bytes += static_cast<double>(ls.n_split_rows) * (moves ? move_bytes : 7.0) +
-                         static_cast<double>(ls.n_act - ls.n_split_rows) * 6.0;
+        // a moved row reads and writes every column and its two decision bytes are read; a row that
+        // records its leaf reads its row id (and its decision bytes) and writes a 2-byte leaf id
+        const double split = static_cast<double>(ls.n_split_rows), frozen = static_cast<double>(ls.n_act) - split;
+        if (d + 1 < D) {
+          dg.part_bytes += odd ? split * (move_bytes + 2.0) + frozen * 7.0 : frozen * 6.0;
+        } else if (d + 1 == D) {
+          dg.part_bytes += odd ? static_cast<double>(ls.n_act) * 8.0 : split * 7.0 + frozen * 6.0;
+        } else if (D == 0) {
+          dg.part_bytes += static_cast<double>(ls.n_act) * 6.0;
+        }
       }
       if (h_n[t] == M) dg.trees_at_full_size += 1;
     }

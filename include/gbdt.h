@@ -114,6 +114,17 @@ typedef struct gbdt_segment {
   int64_t count;
 } gbdt_segment;
 
+/* A row filter for one slot: the slot's rows are those of its segment whose
+ * decision (bins[feature][p] > bin) equals side (0: left, 1: right), i.e. one
+ * child of a split whose rows have not been partitioned yet.  feature < 0: no
+ * filter (every row of the segment). */
+typedef struct gbdt_filter {
+  int32_t feature;
+  int32_t bin;
+  int32_t side;
+  int32_t reserved;
+} gbdt_filter;
+
 /* Library diagnostics ("Module Design: Training Core" s.4, diagnostics()).
  * Filled by gbdt_train when a non-NULL pointer is passed; device times are
  * CUDA-event times on the training stream, summed over all launches of each
@@ -214,19 +225,22 @@ int gbdt_subtract_histograms(const uint32_t* prev_cnt, const int64_t* prev_q, co
 
 /* gbdt_build_histograms_segmented: the same per-bin count and fixed-point G
  * of every flagged slot of a level ("Module Design: Training Core" s.6 step 2,
- * s.7), for rows already grouped by node: the rows of slot s are exactly the
+ * s.7), for rows already grouped by node: the rows of slot s are the
  * positions segments[s].start .. + segments[s].count of every column of
- * bins [F][ldb] and of g (as gbdt_partition_rows leaves them).  Only the
- * flagged segments are read (with sibling subtraction, the smaller child of
- * each pair), one node per CTA with up to 64 features of shared-memory
- * histograms.  segments [max_slots] (device); other arguments and outputs as
+ * bins [F][ldb] and of g (as gbdt_partition_rows leaves them), restricted by
+ * filters[s] when filters is not NULL (a child whose rows still sit inside
+ * its parent's segment: the segment is then the parent's).  Only the flagged
+ * segments are read (with sibling subtraction, the smaller child of each
+ * pair); the flagged rows are cut into equal shares, one per CTA and up to
+ * 64 features of shared-memory histograms per CTA.  segments, filters
+ * [max_slots] (device; filters may be NULL); other arguments and outputs as
  * gbdt_build_histograms.  Workspace: gbdt_histograms_segmented_workspace_size. */
 size_t gbdt_histograms_segmented_workspace_size(int32_t max_slots);
 int gbdt_build_histograms_segmented(const uint8_t* bins, int64_t ldb, int64_t N, int32_t F, const void* g,
                                     int32_t g_dtype, const int32_t* fixed_exp, const gbdt_level* level,
                                     int32_t max_slots, const uint8_t* build_flag, int32_t max_build,
-                                    const gbdt_segment* segments, uint32_t* hist_cnt, int64_t* hist_q, void* ws,
-                                    size_t ws_bytes, void* stream);
+                                    const gbdt_segment* segments, const gbdt_filter* filters, uint32_t* hist_cnt,
+                                    int64_t* hist_q, void* ws, size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------
  * gbdt_find_splits: best split of every slot of a level, "Module Design:

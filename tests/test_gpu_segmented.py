@@ -66,6 +66,55 @@ def test_segmented_histograms_match_oracle(N, F, n_slots, gdtype):
         assert torch.equal(hc[s], dc[s]) and torch.equal(hq[s], dq[s])
 
 
+@pytest.mark.parametrize("N,F,n_slots,gdtype", [(180_001, 9, 6, np.float64), (120_003, 70, 4, np.float32),
+                                                 (33, 3, 2, np.float64)])
+def test_filtered_histograms_match_oracle(N, F, n_slots, gdtype):
+    """A slot whose rows still sit inside its parent's segment: the segment is the parent's and
+    the filter keeps the rows on the slot's side of the parent's split."""
+    rng = np.random.default_rng(3 * N + F)
+    par, par_slot = _segments(rng, N, n_slots // 2)
+    bins = rng.integers(0, 256, (F, N)).astype(np.uint8)
+    bins[1] = rng.integers(0, 4, N).astype(np.uint8)  # coarse column: sides of very different sizes
+    gv = rng.normal(0, 2, N).astype(gdtype)
+    seg = np.zeros(n_slots, g.SEGMENT_DTYPE)
+    filt = np.zeros(n_slots, g.FILTER_DTYPE)
+    feats = rng.integers(0, F, n_slots // 2)
+    thr = rng.integers(0, 255, n_slots // 2)
+    feats[0], thr[0] = 1, 1
+    slot = np.full(N, -1)
+    for s in range(n_slots):
+        k = s // 2
+        seg[s] = par[k]
+        filt[s] = (feats[k], thr[k], s & 1, 0)
+        if s == n_slots - 1 and n_slots > 2:
+            filt[s]["feature"] = -1  # no filter: every row of the segment
+    flags = np.zeros(n_slots, np.uint8)
+    flags[0::2] = 1
+    flags[n_slots - 1] = 1
+    S = g.gradient_scale(torch.from_numpy(gv).cuda())
+    s_exp = int(S.item())
+    hc, hq = g.build_histograms_segmented(dev_bins(bins), N, torch.from_numpy(gv).cuda(), S, level(0, n_slots),
+                                          n_slots, torch.from_numpy(flags).cuda(), int(flags.sum()),
+                                          dev_struct(seg, g.SEGMENT_DTYPE), filters=dev_struct(filt, g.FILTER_DTYPE))
+    hc_h, hq_h = hc.cpu().numpy().view(np.uint32), hq.cpu().numpy()
+    for s in range(n_slots):
+        if not flags[s]:
+            continue
+        a, c = seg["start"][s], seg["count"][s]
+        rows = np.arange(a, a + c)
+        if filt["feature"][s] >= 0:
+            right = bins[filt["feature"][s], rows] > filt["bin"][s]
+            rows = rows[right == bool(filt["side"][s])]
+        m = np.zeros(N, np.int32) - 1
+        m[rows] = 0
+        ref = oracle.histograms(bins, gv.astype(np.float64), m, 1)
+        assert np.array_equal(hc_h[s], ref["cnt"][0]), f"slot {s}"
+        A = np.stack([np.bincount(bins[f][rows], weights=np.abs(gv[rows].astype(np.float64)), minlength=256)
+                      for f in range(F)])
+        G = np.ldexp(hq_h[s].astype(np.float64), -s_exp)
+        assert np.all(np.abs(G - ref["G"][0]) <= g_tolerance(A, ref["cnt"][0], s_exp)), f"slot {s}"
+
+
 @pytest.mark.parametrize("N,F,n_slots,gdtype,explicit", [(300_007, 9, 6, np.float64, False),
                                                           (100_003, 35, 11, np.float32, False),
                                                           (65_536, 3, 2, np.float64, True),
