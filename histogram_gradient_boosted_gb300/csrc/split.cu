@@ -7,8 +7,9 @@
 //
 // One CTA per slot, one warp per feature at a time.  A lane holds 8
 // consecutive bins; the warp forms prefix sums of (count, fixed-point G) with
-// shuffles, evaluates every threshold in FP64 with explicitly rounded
-// operations (no contraction), and reduces to the best candidate.  The
+// shuffles, screens every threshold in FP32 with a proven error margin, and
+// evaluates the survivors in FP64 with explicitly rounded operations (no
+// contraction), reducing to the best candidate.  The
 // comparison (gain desc, feature asc, bin asc) is a total order on distinct
 // candidates, so the result does not depend on the reduction order.
 #include "kernels.cuh"
@@ -135,19 +136,49 @@ __global__ void __launch_bounds__(kSplitThreads)
 
   int nb = n_bins[f];
   nb = nb < 1 ? 1 : (nb > kBins ? kBins : nb);
-  Cand lb{-INFINITY, -1, -1, 0, 0};
+  // Screening in FP32.  Within a node the gain is a non-decreasing function of
+  // x = qL^2/(HL+lambda) + qR^2/(HR+lambda) (fixed-point units; score_P,
+  // gamma and the scale are the node's constants).  x is a sum of two
+  // non-negative terms, so its FP32 value is within 8 * 2^-24 relative of the
+  // exact one; every candidate that could reach the FP64 maximum (ties
+  // included) has x32 >= max x32 * (1 - 2^-16), and only those are evaluated
+  // in FP64.  The chosen candidate is the one a full FP64 scan would choose.
+  const float lam = static_cast<float>(lambda);
+  float x32[8];
+  uint32_t ok = 0;
+  float xmax = -1.0f;
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const int b = lane * 8 + i;
-    if (b > nb - 2) break;
     const uint32_t cL = ce + c[i];
     const int64_t qL = qe + q[i];
     const uint32_t cR = tot_cnt - cL;
     const int64_t qR = static_cast<int64_t>(static_cast<uint64_t>(tot_q) - static_cast<uint64_t>(qL));
     const double HL = static_cast<double>(cL), HR = static_cast<double>(cR);
+    x32[i] = 0.0f;
+    if (b > nb - 2) continue;
     if (!(static_cast<int64_t>(cL) >= msl && static_cast<int64_t>(cR) >= msl && HL >= mcw && HR >= mcw &&
           HL > 0.0 && HR > 0.0))
       continue;
+    const float gl = __ll2float_rn(qL), gr = __ll2float_rn(qR);
+    const float x = __fadd_rn(__fdiv_rn(__fmul_rn(gl, gl), __fadd_rn(static_cast<float>(cL), lam)),
+                              __fdiv_rn(__fmul_rn(gr, gr), __fadd_rn(static_cast<float>(cR), lam)));
+    x32[i] = x;
+    ok |= 1u << i;
+    xmax = fmaxf(xmax, x);
+  }
+  for (int o = 16; o > 0; o >>= 1) xmax = fmaxf(xmax, __shfl_xor_sync(0xffffffffu, xmax, o));
+  const float keep = xmax - xmax * 1.52587890625e-05f;  // xmax * (1 - 2^-16)
+  Cand lb{-INFINITY, -1, -1, 0, 0};
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    if (!(ok >> i & 1u) || x32[i] < keep) continue;
+    const int b = lane * 8 + i;
+    const uint32_t cL = ce + c[i];
+    const int64_t qL = qe + q[i];
+    const uint32_t cR = tot_cnt - cL;
+    const int64_t qR = static_cast<int64_t>(static_cast<uint64_t>(tot_q) - static_cast<uint64_t>(qL));
+    const double HL = static_cast<double>(cL), HR = static_cast<double>(cR);
     const double GL = static_cast<double>(qL) * inv;
     const double GR = static_cast<double>(qR) * inv;
     const double sL = score(GL, HL, lambda), sR = score(GR, HR, lambda);
