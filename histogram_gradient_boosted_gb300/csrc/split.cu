@@ -49,6 +49,14 @@ __device__ __forceinline__ Cand shfl_cand(const Cand& c, int src) {
   return o;
 }
 
+// |q| as a float within 3 ulps: the two 32-bit halves of |q|, both
+// non-negative (no cancellation), converted and combined with one FMA.
+__device__ __forceinline__ float abs_to_float(int64_t q) {
+  const uint64_t a = q < 0 ? static_cast<uint64_t>(0) - static_cast<uint64_t>(q) : static_cast<uint64_t>(q);
+  return __fmaf_rn(__uint2float_rn(static_cast<uint32_t>(a >> 32)), 4294967296.0f,
+                   __uint2float_rn(static_cast<uint32_t>(a)));
+}
+
 __device__ __forceinline__ double score(double G, double H, double lambda) {
   return __ddiv_rn(__dmul_rn(G, G), __dadd_rn(H, lambda));
 }
@@ -139,10 +147,12 @@ __global__ void __launch_bounds__(kSplitThreads)
   // Screening in FP32.  Within a node the gain is a non-decreasing function of
   // x = qL^2/(HL+lambda) + qR^2/(HR+lambda) (fixed-point units; score_P,
   // gamma and the scale are the node's constants).  x is a sum of two
-  // non-negative terms, so its FP32 value is within 8 * 2^-24 relative of the
-  // exact one; every candidate that could reach the FP64 maximum (ties
-  // included) has x32 >= max x32 * (1 - 2^-16), and only those are evaluated
-  // in FP64.  The chosen candidate is the one a full FP64 scan would choose.
+  // non-negative terms, so its FP32 value (|q| converted within 3 ulps, the
+  // division within 2 ulps, H + lambda, the square and the sum rounded once
+  // each) is within 12 * 2^-24 relative of the exact one; every candidate
+  // that could reach the FP64 maximum (ties included) has
+  // x32 >= max x32 * (1 - 2^-16), and only those are evaluated in FP64.  The
+  // chosen candidate is the one a full FP64 scan would choose.
   const float lam = static_cast<float>(lambda);
   float x32[8];
   uint32_t ok = 0;
@@ -160,9 +170,9 @@ __global__ void __launch_bounds__(kSplitThreads)
     if (!(static_cast<int64_t>(cL) >= msl && static_cast<int64_t>(cR) >= msl && HL >= mcw && HR >= mcw &&
           HL > 0.0 && HR > 0.0))
       continue;
-    const float gl = __ll2float_rn(qL), gr = __ll2float_rn(qR);
-    const float x = __fadd_rn(__fdiv_rn(__fmul_rn(gl, gl), __fadd_rn(static_cast<float>(cL), lam)),
-                              __fdiv_rn(__fmul_rn(gr, gr), __fadd_rn(static_cast<float>(cR), lam)));
+    const float gl = abs_to_float(qL), gr = abs_to_float(qR);
+    const float x = __fadd_rn(__fdividef(__fmul_rn(gl, gl), __fadd_rn(static_cast<float>(cL), lam)),
+                              __fdividef(__fmul_rn(gr, gr), __fadd_rn(static_cast<float>(cR), lam)));
     x32[i] = x;
     ok |= 1u << i;
     xmax = fmaxf(xmax, x);
