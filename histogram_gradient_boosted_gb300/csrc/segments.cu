@@ -776,9 +776,18 @@ __global__ void __launch_bounds__(kMvThreads)
     for (int i = threadIdx.x; i < n; i += blockDim.x) leaf_of_row[orig_in[p0 + i]] = node;
     return;
   }
-  for (int i = threadIdx.x; i < n; i += blockDim.x) {
-    const int right = bins_in[rb_offset(rt.feature, p0 + i, pitch)] > rt.bin ? 1 : 0;
-    leaf_of_row[orig_in[p0 + i]] = static_cast<uint16_t>(rt.left_node + right);
+  for (int i0 = threadIdx.x; i0 < n; i0 += 4 * blockDim.x) {  // four rows in flight per thread
+    int d[4];
+    uint32_t o[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = i0 + u * blockDim.x;
+      d[u] = i < n ? bins_in[rb_offset(rt.feature, p0 + i, pitch)] : -1;
+      o[u] = i < n ? orig_in[p0 + i] : 0u;
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      if (d[u] >= 0) leaf_of_row[o[u]] = static_cast<uint16_t>(rt.left_node + (d[u] > rt.bin ? 1 : 0));
   }
 }
 
@@ -886,15 +895,18 @@ __global__ void pair_routes_kernel(const gbdt_level* __restrict__ level, int32_t
 }
 
 // Run of position p of pair pr: 0..3, or -1 when its child is a leaf (*child is set either way).
-// (bins in the row-block layout)
+// (bins in the row-block layout).  The parent's decision and both children's
+// are loaded together (independent loads), then the child's is selected.
 __device__ __forceinline__ int pair_run(const PairRoute& pr, const uint8_t* __restrict__ bins, int64_t pitch,
                                         int64_t p, int* child) {
-  const int c = bins[rb_offset(pr.f1, p, pitch)] > pr.b1 ? 1 : 0;
+  const int d1 = bins[rb_offset(pr.f1, p, pitch)];
+  const int d20 = pr.f2[0] >= 0 ? bins[rb_offset(pr.f2[0], p, pitch)] : 0;
+  const int d21 = pr.f2[1] >= 0 ? bins[rb_offset(pr.f2[1], p, pitch)] : 0;
+  const int c = d1 > pr.b1 ? 1 : 0;
   *child = c;
   const int f2 = c ? pr.f2[1] : pr.f2[0];
   if (f2 < 0) return -1;
-  const int b2 = c ? pr.b2[1] : pr.b2[0];
-  return 2 * c + (bins[rb_offset(f2, p, pitch)] > b2 ? 1 : 0);
+  return 2 * c + ((c ? d21 > pr.b2[1] : d20 > pr.b2[0]) ? 1 : 0);
 }
 
 __global__ void __launch_bounds__(kMvThreads)
@@ -909,10 +921,21 @@ __global__ void __launch_bounds__(kMvThreads)
   const int64_t p0 = pr.start + static_cast<int64_t>(t - tile_start[k]) * kMvTile;
   const int n = static_cast<int>(min(pr.start + pr.count - p0, static_cast<int64_t>(kMvTile)));
   int c[4] = {0, 0, 0, 0};
-  for (int j = threadIdx.x; j < n; j += blockDim.x) {
-    int child;
-    const int r = pair_run(pr, bins, pitch, p0 + j, &child);
-    if (r >= 0) ++c[r];
+  for (int j0 = threadIdx.x; j0 < n; j0 += 4 * blockDim.x) {  // four rows in flight per thread
+    int r[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int j = j0 + u * blockDim.x;
+      int child;
+      r[u] = j < n ? pair_run(pr, bins, pitch, p0 + j, &child) : -1;
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      c[0] += r[u] == 0;
+      c[1] += r[u] == 1;
+      c[2] += r[u] == 2;
+      c[3] += r[u] == 3;
+    }
   }
   int tot[4];
   for (int r = 0; r < 4; ++r) block_scan_excl(c[r], s_warp, &tot[r]);
@@ -987,21 +1010,26 @@ __global__ void __launch_bounds__(kMvThreads, 4)
   mv_start_copies<true>(s_stage, s_full, bins_in, 0, F, 0, 0, &map_in, z0);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   // ---- rank the tile (lane = row) into four runs; rows of a leaf child record their leaf
+  static_assert(kMvChunksPerWarp % 4 == 0, "chunks are ranked four at a time");
 #pragma unroll 1
-  for (int kk = 0; kk < kMvChunksPerWarp; ++kk) {
-    const int ch = warp * kMvChunksPerWarp + kk;
-    const int j = ch * 32 + lane;
-    int r = -1;
-    if (j < n) {
-      int child;
-      r = pair_run(pr, bins_in, pitch, p0 + j, &child);
-      if (r < 0 && leaf_of_row)
-        leaf_of_row[orig_in[p0 + j]] = static_cast<uint16_t>(child ? pr.node[1] : pr.node[0]);
+  for (int k0 = 0; k0 < kMvChunksPerWarp; k0 += 4) {
+    int r[4], child[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {  // four chunks' decisions in flight
+      const int j = (warp * kMvChunksPerWarp + k0 + u) * 32 + lane;
+      r[u] = j < n ? pair_run(pr, bins_in, pitch, p0 + j, &child[u]) : -2;
     }
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const uint32_t m = __ballot_sync(0xffffffffu, r == q);
-      if (lane == 0) s_mask[q][ch] = m;
+    for (int u = 0; u < 4; ++u) {
+      const int ch = warp * kMvChunksPerWarp + k0 + u;
+      const int j = ch * 32 + lane;
+      if (r[u] == -1 && leaf_of_row)
+        leaf_of_row[orig_in[p0 + j]] = static_cast<uint16_t>(child[u] ? pr.node[1] : pr.node[0]);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint32_t m = __ballot_sync(0xffffffffu, r[u] == q);
+        if (lane == 0) s_mask[q][ch] = m;
+      }
     }
   }
   __syncthreads();
@@ -1055,11 +1083,21 @@ __global__ void __launch_bounds__(kMvThreads)
   const PairRoute pr = pairs[k];
   const int64_t p0 = pr.start + static_cast<int64_t>(t - tile_start[k]) * kMvTile;
   const int n = static_cast<int>(min(pr.start + pr.count - p0, static_cast<int64_t>(kMvTile)));
-  for (int i = threadIdx.x; i < n; i += blockDim.x) {
-    int child;
-    const int r = pair_run(pr, bins_in, pitch, p0 + i, &child);
-    const int node = child ? pr.node[1] : pr.node[0], left = child ? pr.left[1] : pr.left[0];
-    leaf_of_row[orig_in[p0 + i]] = static_cast<uint16_t>(r < 0 ? node : left + (r & 1));
+  for (int i0 = threadIdx.x; i0 < n; i0 += 4 * blockDim.x) {  // four rows in flight per thread
+    int r[4], ch[4];
+    uint32_t o[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = i0 + u * blockDim.x;
+      r[u] = i < n ? pair_run(pr, bins_in, pitch, p0 + i, &ch[u]) : -2;
+      o[u] = i < n ? orig_in[p0 + i] : 0u;
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      if (r[u] == -2) continue;
+      const int node = ch[u] ? pr.node[1] : pr.node[0], left = ch[u] ? pr.left[1] : pr.left[0];
+      leaf_of_row[o[u]] = static_cast<uint16_t>(r[u] < 0 ? node : left + (r[u] & 1));
+    }
   }
 }
 
