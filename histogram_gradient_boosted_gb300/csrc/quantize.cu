@@ -6,9 +6,10 @@
 //
 // Per batch of columns: map each value to an order-preserving uint32 key
 // (-0.0 read as +0.0), sort every column with a stable 4-pass LSD radix sort
-// (8-bit digits; tile counts, a per-column scan, and a stable scatter that
-// ranks equal digits inside a warp with 8 ballots), read the edges off the
-// sorted keys, then bin every value by binary search over its column's edges.
+// (8-bit digits; tile counts, a scan over tiles per (column, digit) and over
+// digits per column, and a stable scatter that ranks equal digits inside a warp
+// with 8 ballots), read the edges off the sorted keys (run starts counted in
+// chunks), then bin every value by binary search over its column's edges.
 #include <algorithm>
 
 #include "kernels.cuh"
@@ -62,53 +63,75 @@ __global__ void __launch_bounds__(kQThreads)
   counts[(static_cast<int64_t>(j) * 256 + threadIdx.x) * tiles + t] = h[threadIdx.x];
 }
 
-// In-place exclusive scan of one column's counts in (digit, tile) order.
-__global__ void __launch_bounds__(1024) radix_scan_kernel(uint32_t* __restrict__ counts, int tiles) {
+// In-place exclusive scan over the tiles of one (column, digit) row of the
+// counts; the row's total goes to dtot[j][digit].
+__global__ void __launch_bounds__(256)
+    radix_tile_scan_kernel(uint32_t* __restrict__ counts, int tiles, uint32_t* __restrict__ dtot) {
   __shared__ uint32_t s_warp[33];
   __shared__ uint32_t s_carry;
-  const int64_t total = static_cast<int64_t>(256) * tiles;
-  uint32_t* c = counts + blockIdx.x * total;
+  const int d = blockIdx.x, j = blockIdx.y;
+  uint32_t* c = counts + (static_cast<int64_t>(j) * 256 + d) * tiles;
   if (threadIdx.x == 0) s_carry = 0;
   __syncthreads();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  for (int64_t c0 = 0; c0 < total; c0 += blockDim.x) {
-    const int64_t i = c0 + threadIdx.x;
-    const uint32_t v = i < total ? c[i] : 0u;
+  for (int c0 = 0; c0 < tiles; c0 += blockDim.x) {
+    const int i = c0 + threadIdx.x;
+    const uint32_t v = i < tiles ? c[i] : 0u;
     uint32_t incl = v;
     for (int o = 1; o < 32; o <<= 1) {
-      uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
+      const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
       if (lane >= o) incl += t;
     }
     if (lane == 31) s_warp[warp] = incl;
     __syncthreads();
     if (warp == 0) {
-      uint32_t w = s_warp[lane], wi = w;
+      const int nw = blockDim.x >> 5;
+      const uint32_t w = lane < nw ? s_warp[lane] : 0u;
+      uint32_t wi = w;
       for (int o = 1; o < 32; o <<= 1) {
-        uint32_t t = __shfl_up_sync(0xffffffffu, wi, o);
+        const uint32_t t = __shfl_up_sync(0xffffffffu, wi, o);
         if (lane >= o) wi += t;
       }
-      s_warp[lane] = wi - w;
+      if (lane < nw) s_warp[lane] = wi - w;
       if (lane == 31) s_warp[32] = wi;
     }
     __syncthreads();
-    if (i < total) c[i] = s_carry + s_warp[warp] + incl - v;
+    if (i < tiles) c[i] = s_carry + s_warp[warp] + incl - v;
     __syncthreads();
     if (threadIdx.x == 0) s_carry += s_warp[32];
     __syncthreads();
   }
+  if (threadIdx.x == 0) dtot[j * 256 + d] = s_carry;
+}
+
+// Exclusive scan of one column's 256 digit totals (in place): the digit's first position.
+__global__ void __launch_bounds__(256) radix_digit_scan_kernel(uint32_t* __restrict__ dtot) {
+  __shared__ uint32_t s[256];
+  uint32_t* t = dtot + blockIdx.x * 256;
+  const uint32_t v = t[threadIdx.x];
+  s[threadIdx.x] = v;
+  __syncthreads();
+  for (int o = 1; o < 256; o <<= 1) {
+    const uint32_t a = threadIdx.x >= o ? s[threadIdx.x - o] : 0u;
+    __syncthreads();
+    s[threadIdx.x] += a;
+    __syncthreads();
+  }
+  t[threadIdx.x] = s[threadIdx.x] - v;
 }
 
 // Stable scatter: keys of a tile, taken in order 256 at a time; equal digits
 // inside a warp are ranked with ballots, across warps and rounds with counters.
 __global__ void __launch_bounds__(kQThreads)
     radix_scatter_kernel(const uint32_t* __restrict__ in, uint32_t* __restrict__ out, int64_t N, int tiles, int shift,
-                         const uint32_t* __restrict__ offsets) {
+                         const uint32_t* __restrict__ offsets, const uint32_t* __restrict__ dbase) {
   constexpr int kWarps = kQThreads / 32;
   __shared__ uint32_t s_base[256];       // running position of each digit in this tile
   __shared__ uint32_t s_wc[kWarps][256];  // per-warp count, then per-warp start, of each digit
   const int j = blockIdx.y, t = blockIdx.x;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  s_base[threadIdx.x] = offsets[(static_cast<int64_t>(j) * 256 + threadIdx.x) * tiles + t];
+  s_base[threadIdx.x] =
+      dbase[j * 256 + threadIdx.x] + offsets[(static_cast<int64_t>(j) * 256 + threadIdx.x) * tiles + t];
   const uint32_t* k = in + j * N;
   uint32_t* o = out + j * N;
   const int64_t b0 = static_cast<int64_t>(t) * kQTile;
@@ -145,47 +168,70 @@ __global__ void __launch_bounds__(kQThreads)
   }
 }
 
-// One CTA per column: distinct count, edges, n_bins.
-__global__ void __launch_bounds__(1024)
-    edges_kernel(const uint32_t* __restrict__ sorted, int64_t N, int j0, int B, float* __restrict__ edges,
-                 int32_t* __restrict__ n_bins) {
+// Distinct values of a sorted column, in chunks: each CTA counts the run
+// starts of its chunk (position i starts a run if i == 0 or v[i] != v[i-1])
+// with coalesced reads, and keeps up to kRunKeep of their values (unordered).
+constexpr int kEdgeChunks = 64;
+constexpr int kRunKeep = 257;
+
+__global__ void __launch_bounds__(256)
+    run_starts_kernel(const uint32_t* __restrict__ sorted, int64_t N, uint32_t* __restrict__ chunk_cnt,
+                      uint32_t* __restrict__ chunk_vals /*[col][chunk][kRunKeep]*/) {
+  const int j = blockIdx.y, c = blockIdx.x;
+  const uint32_t* v = sorted + j * N;
+  const int64_t per = (N + kEdgeChunks - 1) / kEdgeChunks;
+  const int64_t a = c * per, bnd = min(N, a + per);
+  __shared__ uint32_t s_cnt;
+  if (threadIdx.x == 0) s_cnt = 0;
+  __syncthreads();
+  uint32_t* keep = chunk_vals + (static_cast<int64_t>(j) * kEdgeChunks + c) * kRunKeep;
+  for (int64_t i = a + threadIdx.x; i < bnd; i += blockDim.x) {
+    const uint32_t x = v[i];
+    if (i == 0 || x != v[i - 1]) {
+      const uint32_t slot = atomicAdd(&s_cnt, 1u);
+      if (slot < kRunKeep) keep[slot] = x;
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) chunk_cnt[j * kEdgeChunks + c] = s_cnt;
+}
+
+// One CTA per column: U = number of distinct values; U <= B: the U-1 smallest
+// distinct values (all of them were kept: every chunk has at most U run
+// starts); otherwise the order statistics v[ceil(kN/B) - 1], strictly
+// increasing, without one equal to the largest value.
+__global__ void __launch_bounds__(256)
+    edges_kernel(const uint32_t* __restrict__ sorted, int64_t N, int j0, int B, const uint32_t* __restrict__ chunk_cnt,
+                 const uint32_t* __restrict__ chunk_vals, float* __restrict__ edges, int32_t* __restrict__ n_bins) {
   const int j = blockIdx.x;
   const uint32_t* v = sorted + j * N;
-  __shared__ uint32_t s_warp[33];
+  __shared__ uint32_t s_cnt[kEdgeChunks + 1];
+  __shared__ uint32_t s_vals[256];
   __shared__ float s_e[256];
   __shared__ int s_ne;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  // run starts per contiguous thread chunk
-  const int64_t per = (N + blockDim.x - 1) / blockDim.x;
-  const int64_t a = threadIdx.x * per, bnd = min(N, a + per);
-  uint32_t c = 0;
-  for (int64_t i = a; i < bnd; ++i) c += (i == 0 || v[i] != v[i - 1]) ? 1u : 0u;
-  uint32_t incl = c;
-  for (int o = 1; o < 32; o <<= 1) {
-    uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += t;
-  }
-  if (lane == 31) s_warp[warp] = incl;
-  __syncthreads();
-  if (warp == 0) {
-    uint32_t w = s_warp[lane], wi = w;
-    for (int o = 1; o < 32; o <<= 1) {
-      uint32_t t = __shfl_up_sync(0xffffffffu, wi, o);
-      if (lane >= o) wi += t;
+  if (threadIdx.x == 0) {
+    uint32_t acc = 0;
+    for (int c = 0; c < kEdgeChunks; ++c) {
+      s_cnt[c] = acc;
+      acc += chunk_cnt[j * kEdgeChunks + c];
     }
-    s_warp[lane] = wi - w;
-    if (lane == 31) s_warp[32] = wi;
+    s_cnt[kEdgeChunks] = acc;
   }
   __syncthreads();
-  const uint32_t U = s_warp[32];
+  const uint32_t U = s_cnt[kEdgeChunks];
   float* e = edges + static_cast<int64_t>(j0 + j) * (B - 1);
   if (U <= static_cast<uint32_t>(B)) {
-    uint32_t r = s_warp[warp] + incl - c;  // rank of this thread's first run start
-    for (int64_t i = a; i < bnd; ++i) {
-      if (i == 0 || v[i] != v[i - 1]) {
-        if (r + 1 < U) e[r] = key2f(v[i]);
-        ++r;
-      }
+    for (int c = 0; c < kEdgeChunks; ++c) {  // gather the distinct values (at most B <= 256)
+      const uint32_t n = s_cnt[c + 1] - s_cnt[c];
+      for (uint32_t i = threadIdx.x; i < n; i += blockDim.x)
+        s_vals[s_cnt[c] + i] = chunk_vals[(static_cast<int64_t>(j) * kEdgeChunks + c) * kRunKeep + i];
+    }
+    __syncthreads();
+    for (uint32_t i = threadIdx.x; i < U; i += blockDim.x) {  // rank among distinct values
+      const uint32_t x = s_vals[i];
+      uint32_t r = 0;
+      for (uint32_t m = 0; m < U; ++m) r += s_vals[m] < x ? 1u : 0u;
+      if (r + 1 < U) e[r] = key2f(x);
     }
     for (int k = static_cast<int>(U) - 1 + threadIdx.x; k < B - 1; k += blockDim.x) e[k] = INFINITY;
     if (threadIdx.x == 0) n_bins[j0 + j] = static_cast<int32_t>(U);
@@ -243,6 +289,9 @@ struct QuantWs {
   uint32_t* a;
   uint32_t* b;
   uint32_t* counts;
+  uint32_t* dtot;
+  uint32_t* chunk_cnt;
+  uint32_t* chunk_vals;
   int32_t* flag;
 };
 QuantWs carve_quant(void* ws, size_t bytes, int64_t N, int32_t F, size_t* need) {
@@ -252,6 +301,9 @@ QuantWs carve_quant(void* ws, size_t bytes, int64_t N, int32_t F, size_t* need) 
   w.a = c.take<uint32_t>(static_cast<size_t>(fb) * N);
   w.b = c.take<uint32_t>(static_cast<size_t>(fb) * N);
   w.counts = c.take<uint32_t>(static_cast<size_t>(fb) * 256 * ceil_div(N, kQTile));
+  w.dtot = c.take<uint32_t>(static_cast<size_t>(fb) * 256);
+  w.chunk_cnt = c.take<uint32_t>(static_cast<size_t>(fb) * kEdgeChunks);
+  w.chunk_vals = c.take<uint32_t>(static_cast<size_t>(fb) * kEdgeChunks * kRunKeep);
   w.flag = c.take<int32_t>(1);
   *need = c.used;
   return w;
@@ -307,13 +359,17 @@ extern "C" int gbdt_quantize(const float* X, int64_t ldx, int64_t N, int32_t F, 
     for (int pass = 0; pass < 4; ++pass) {
       radix_count_kernel<<<dim3(tiles, nb), kQThreads, 0, s>>>(src, N, tiles, 8 * pass, w.counts);
       count_launches();
-      radix_scan_kernel<<<nb, 1024, 0, s>>>(w.counts, tiles);
+      radix_tile_scan_kernel<<<dim3(256, nb), 256, 0, s>>>(w.counts, tiles, w.dtot);
       count_launches();
-      radix_scatter_kernel<<<dim3(tiles, nb), kQThreads, 0, s>>>(src, dst, N, tiles, 8 * pass, w.counts);
+      radix_digit_scan_kernel<<<nb, 256, 0, s>>>(w.dtot);
+      count_launches();
+      radix_scatter_kernel<<<dim3(tiles, nb), kQThreads, 0, s>>>(src, dst, N, tiles, 8 * pass, w.counts, w.dtot);
       count_launches();
       std::swap(src, dst);
     }
-    edges_kernel<<<nb, 1024, 0, s>>>(src, N, j0, max_bins, edges, n_bins);
+    run_starts_kernel<<<dim3(kEdgeChunks, nb), 256, 0, s>>>(src, N, w.chunk_cnt, w.chunk_vals);
+    count_launches();
+    edges_kernel<<<nb, 256, 0, s>>>(src, N, j0, max_bins, w.chunk_cnt, w.chunk_vals, edges, n_bins);
     count_launches();
     bin_kernel<<<dim3(gx, nb), 256, 0, s>>>(X, ldx, N, j0, max_bins, edges, n_bins, bins, ldb);
     count_launches();
