@@ -84,6 +84,7 @@ def lib():
         L.orc_train.argtypes = [P, P, i64, i32, P, ctypes.POINTER(Params), P, P, P, P, P, P, P]
         L.orc_partition.argtypes = [P, i64, i32, P, P, P, P, P, P, P]
         L.orc_update_predictions.argtypes = [P, P, P, i64, dbl]
+        L.orc_predict.argtypes = [P, i64, i32, P, i32, P, i32, i32, dbl, dbl, P]
         L.orc_weight.argtypes = [dbl, dbl, dbl]
         L.orc_weight.restype = dbl
         L.orc_gain.argtypes = [dbl] * 8
@@ -224,3 +225,16 @@ def update_predictions(pred, leaf_value, node_of_row, lr):
     nr = np.ascontiguousarray(node_of_row, np.int32)
     _check(lib().orc_update_predictions(_p(pred), _p(lv), _p(nr), pred.shape[0], float(lr)), "update")
     return pred
+
+
+def predict(X, edges, nodes, init_pred, learning_rate):
+    """Predictions on raw fp32 features [F][N] of trees nodes (T, M) NODE_DTYPE with quantize edges."""
+    X = np.ascontiguousarray(X, dtype=np.float32)
+    F, N = X.shape
+    edges = np.ascontiguousarray(edges, dtype=np.float32)
+    nodes = np.ascontiguousarray(nodes, dtype=NODE_DTYPE)
+    T, M = (nodes.shape if nodes.ndim == 2 else (0, 1))
+    out = np.empty(N, np.float64)
+    _check(lib().orc_predict(_p(X), N, F, _p(edges), edges.shape[1] + 1, _p(nodes) if T else None, T, M,
+                             float(init_pred), float(learning_rate), _p(out)), "predict")
+    return out

@@ -589,3 +589,37 @@ int orc_update_predictions(double* pred, const double* leaf_value, const int32_t
   }
   return ORC_OK;
 }
+
+/* ------------------------------------------------------------------------ */
+/* [LEAN] "Gradient boosted trees (spec model)", Forward pass and Tree        */
+/* representation: the prediction of a row is init + learning_rate * (sum of */
+/* its tree outputs), a tree sending x right when x > threshold.  On raw      */
+/* features the threshold of split (feature j, bin b) is the edge             */
+/* edges[j][b]: by the quantize rule bin(x) = #{edges < x}, so x > edges[b]   */
+/* exactly when bin(x) > b, the training routing.  The sum is taken tree by   */
+/* tree as in training ([MPS-TC] s.6 step 7): pred + (lr * leaf value).  A    */
+/* NaN compares false and goes left.                                          */
+int orc_predict(const float* X, int64_t N, int32_t F, const float* edges, int32_t max_bins, const orc_node* nodes,
+                int32_t n_trees, int32_t max_nodes, double init, double lr, double* out) {
+  if (!X || !edges || !out || N < 0 || F < 1 || max_bins < 2 || n_trees < 0 || (n_trees > 0 && !nodes) ||
+      max_nodes < 1)
+    return ORC_EINVAL;
+  for (int64_t i = 0; i < N; ++i) {
+    double pred = init;
+    for (int32_t t = 0; t < n_trees; ++t) {
+      const orc_node* tn = nodes + (int64_t)t * max_nodes;
+      int32_t v = 0;
+      for (int32_t steps = 0; !tn[v].is_leaf; ++steps) {
+        if (steps > 64 || tn[v].feature < 0 || tn[v].feature >= F || tn[v].left < 0 || tn[v].right >= max_nodes)
+          return ORC_EINVAL;
+        const float x = X[(int64_t)tn[v].feature * N + i];
+        const float thr = edges[(int64_t)tn[v].feature * (max_bins - 1) + tn[v].threshold_bin];
+        v = x > thr ? tn[v].right : tn[v].left;
+      }
+      const double step = lr * tn[v].leaf_value;
+      pred = pred + step;
+    }
+    out[i] = pred;
+  }
+  return ORC_OK;
+}

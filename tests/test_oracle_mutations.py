@@ -14,6 +14,7 @@ import pytest
 import oracle
 from tests import test_oracle_hand_trees as hand
 from tests import test_oracle_pins as pins
+from tests import test_oracle_predict as tp
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
@@ -34,6 +35,10 @@ MUTATIONS = {
     "quantile index off by one": ("int64_t pk = ((int64_t)k * N + B - 1) / B - 1;", "int64_t pk = ((int64_t)k * N + B - 1) / B;"),
     "initial prediction": ("const double init = sum / (double)N;", "const double init = sum / (double)(N + 1);"),
     "gradient sign": ("g[i] = pred[i] - (double)label[i];", "g[i] = (double)label[i] - pred[i];"),
+    "raw routing >= instead of >": ("v = x > thr ? tn[v].right : tn[v].left;", "v = x >= thr ? tn[v].right : tn[v].left;"),
+    "raw routing children swapped": ("v = x > thr ? tn[v].right : tn[v].left;", "v = x > thr ? tn[v].left : tn[v].right;"),
+    "raw prediction without learning rate": ("const double step = lr * tn[v].leaf_value;\n      pred = pred + step;",
+                                             "const double step = tn[v].leaf_value;\n      pred = pred + step;"),
     "feature index transposed": ("const uint8_t* col = bins + (int64_t)j * N;\n    uint32_t* c", "const uint8_t* col = bins + (int64_t)(F - 1 - j) * N;\n    uint32_t* c"),
 }
 
@@ -47,6 +52,9 @@ PINS = [
     ("brute", lambda o: [pins.test_root_split_matches_brute_force(o, s) for s in range(12)]),
     ("quantize balanced", lambda o: pins.test_quantize_all_distinct_balanced(o, 1000, 32)),
     ("invariants", lambda o: pins.test_training_invariants(o, "tiny", None, 3)),
+    ("predict hand", lambda o: tp.test_hand_model(o)),
+    ("predict = training",
+     lambda o: tp.test_prediction_of_training_rows_equals_training_predictions("tiny", 3, 2, o=o)),
 ]
 
 
