@@ -36,7 +36,7 @@ EXPORTED_SYMBOLS = [
     "gbdt_partition_workspace_size", "gbdt_partition", "gbdt_update_predictions", "gbdt_train_workspace_size",
     "gbdt_train", "gbdt_debug_inject_failure", "gbdt_kernel_launch_count", "gbdt_partition_noalloc",
     "gbdt_histograms_segmented_workspace_size", "gbdt_build_histograms_segmented", "gbdt_partition_rows_workspace_size",
-    "gbdt_partition_rows",
+    "gbdt_partition_rows", "gbdt_predict_workspace_size", "gbdt_predict",
 ]
 
 
@@ -109,6 +109,8 @@ def lib():
         "gbdt_build_histograms_segmented": ([P, i64, i64, i32, P, i32, P, P, i32, P, i32, P, P, P, P, P, sz, P], i32),
         "gbdt_partition_rows_workspace_size": ([i64, i32], sz),
         "gbdt_partition_rows": ([P, P, i64, i64, i32, P, P, i32, P, P, P, P, P, i32, P, P, P, P, P, sz, P], i32),
+        "gbdt_predict_workspace_size": ([i32, i32], sz),
+        "gbdt_predict": ([P, i64, i64, i32, P, i32, P, P, i32, i32, dbl, dbl, P, P, sz, P], i32),
     }
     for name, (args, res) in sig.items():
         fn = getattr(L, name)
@@ -361,3 +363,25 @@ def kernel_launch_count() -> int:
 def inject_failure(after_levels: int):
     """Testing hook: make the next gbdt_train calls fail on the host after that many levels (-1 disables)."""
     lib().gbdt_debug_inject_failure(int(after_levels))
+
+
+def predict(X, edges, nodes, init_pred, learning_rate, nodes_per_tree=None, out=None, ws=None):
+    """Predictions on raw fp32 features X (F, ldx) CUDA of a model: nodes (T, M) NODE_DTYPE (host numpy, as
+    train returns them) with nodes_per_tree (T,) (None: every slot is a node), edges (F, max_bins - 1) CUDA."""
+    torch = _torch()
+    F, ldx = X.shape
+    N = ldx if out is None else out.shape[0]
+    max_bins = edges.shape[1] + 1
+    if not isinstance(nodes, np.ndarray):
+        raise TypeError("nodes: a (T, M) NODE_DTYPE numpy array")
+    T, M = (nodes.shape[0], nodes.shape[1]) if nodes.ndim == 2 else (0, 1)
+    nodes_d = torch.from_numpy(np.ascontiguousarray(nodes).view(np.uint8).reshape(-1).copy()).cuda() if T else None
+    npt_d = (torch.from_numpy(np.ascontiguousarray(nodes_per_tree, np.int32)).cuda()
+             if nodes_per_tree is not None and T else None)
+    if out is None:
+        out = torch.empty(N, dtype=torch.float64, device="cuda")
+    if ws is None:
+        ws = _workspace(lib().gbdt_predict_workspace_size(T, max(M, 1)))
+    _check(lib().gbdt_predict(_ptr(X), ldx, N, F, _ptr(edges), max_bins, _ptr(nodes_d), _ptr(npt_d), T, max(M, 1),
+                              float(init_pred), float(learning_rate), _ptr(out), _ptr(ws), ws.numel(), _stream()))
+    return out

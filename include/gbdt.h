@@ -331,6 +331,31 @@ int gbdt_update_predictions(double* pred, const uint16_t* leaf_of_row, const dou
                             int32_t n_leaf_values, int64_t N, double lr, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * gbdt_predict: batched prediction on raw fp32 features ("Gradient boosted
+ * trees (spec model)", Forward pass: init + learning_rate * sum of tree
+ * outputs; Tree representation: x > threshold goes right).  The threshold of a
+ * split (feature j, bin b) is edges[j][b] from gbdt_quantize, so routing raw
+ * values is exactly the training's routing on bins; the sum is taken tree by
+ * tree, pred + (learning_rate * leaf_value) with the product rounded first, so
+ * the predictions of the training rows equal gbdt_train's pred_out bit for
+ * bit.  A NaN compares false and goes left.
+ *   X [F][ldx] fp32 column-major (device); edges [F][max_bins-1] (device) as
+ *   gbdt_quantize wrote them; nodes [n_trees][max_nodes] gbdt_node (device,
+ *   the layout gbdt_train returns: BFS, right = left + 1); nodes_per_tree
+ *   [n_trees] int32 (device; NULL: every slot is a node): the nodes a tree
+ *   uses are its first nodes_per_tree[t] slots; out [N] fp64.
+ * Every used internal node is checked (feature < F, bin < max_bins - 1,
+ * children a pair after the node among the used nodes); a bad node or count
+ * makes the call return GBDT_ERR_INVALID_ARG (out is then unspecified).  Workspace:
+ * gbdt_predict_workspace_size(n_trees, max_nodes).  Synchronises the stream
+ * once at the end (to report model errors).
+ * ------------------------------------------------------------------------- */
+size_t gbdt_predict_workspace_size(int32_t n_trees, int32_t max_nodes);
+int gbdt_predict(const float* X, int64_t ldx, int64_t N, int32_t F, const float* edges, int32_t max_bins,
+                 const gbdt_node* nodes, const int32_t* nodes_per_tree, int32_t n_trees, int32_t max_nodes,
+                 double init_pred, double learning_rate, double* out, void* ws, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
  * gbdt_train: whole training run ("Module Design: Training Core" s.6).
  *   bins [F][ldb] uint8, n_bins [F] int32 (1..256), label [N] fp32 (device)
  *   p: host pointer
