@@ -144,15 +144,26 @@ class ClockSampler:
                 "power_w_max": max((num(r[2]) for r in rows if num(r[2]) is not None), default=None)}
 
 
-def _traffic_record(hist_src: str):
-    """ncu DRAM bytes per histogram launch, if recorded for the current kernel source."""
+HIST_SOURCES = [os.path.join("histogram_gradient_boosted_gb300", "csrc", f) for f in ("segments.cu", "train.cu")]
+
+
+def hist_source_sha256() -> str:
+    """Hash of the sources that define the level-histogram launches (the kernel and the level loop)."""
+    h = hashlib.sha256()
+    for rel in HIST_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def _traffic_record():
+    """ncu DRAM bytes per histogram launch, if recorded for the current sources (else None)."""
     p = os.path.join(ROOT, "profiles", "histogram_traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
         rec = json.load(f)
-    sha = hashlib.sha256(open(hist_src, "rb").read()).hexdigest()
-    return rec if rec.get("kernel_source_sha256") == sha else None
+    return rec if rec.get("kernel_source_sha256") == hist_source_sha256() else None
 
 
 # ------------------------------------------------------------------------------------ reference arm
@@ -365,7 +376,7 @@ def run_ours(args, rank, local_rank, ws, dist):
     hist_bytes = sum(d["hist_bytes"] for d in diags)
     hist_launches = sum(d["hist_launches"] for d in diags)
     achieved = hist_bytes / (hist_ms * 1e-3) / 1e9
-    trec = _traffic_record(os.path.join(ROOT, "histogram_gradient_boosted_gb300", "csrc", "histogram.cu"))
+    trec = _traffic_record()
     part_ms = sum(d["part_ms"] for d in diags)
     part_bytes = sum(d["part_bytes"] for d in diags)
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
@@ -413,6 +424,29 @@ def run_ours(args, rank, local_rank, ws, dist):
                           "share_of_step": part_ms / ms_total if ms_total else None},
             "train_only": {"ms_per_run": train_ms, "value": N * F * T / (train_ms * 1e-3)},
             "trees_at_full_size": diags[-1]["trees_at_full_size"]}
+    # ---- batched prediction of the training rows with the trained model (raw fp32 features) ----
+    bins_i, edges_i, n_bins_i = g.quantize(Xd, cfg["max_bins"])
+    model = g.train(bins_i, n_bins_i, yd, ws=train_ws, pred=pred, **cfg)
+    del bins_i
+    pout = torch.empty(N, dtype=torch.float64, device="cuda")
+    pws = g._workspace(g.lib().gbdt_predict_workspace_size(T, M))
+    for _ in range(2):
+        g.predict(Xd, edges_i, model["nodes"], model["init_pred"], cfg["learning_rate"], model["nodes_per_tree"],
+                  out=pout, ws=pws)
+    torch.cuda.synchronize()
+    p_steps = 3
+    e0.record(stream)
+    for _ in range(p_steps):
+        g.predict(Xd, edges_i, model["nodes"], model["init_pred"], cfg["learning_rate"], model["nodes_per_tree"],
+                  out=pout, ws=pws)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    p_ms = e0.elapsed_time(e1) / p_steps
+    line["inference"] = {"metric": "rows x trees predicted per second (raw fp32 features)",
+                         "value": N * T / (p_ms * 1e-3), "ms": p_ms, "rows": N, "trees": T,
+                         "equals_training_predictions": bool(torch.equal(pout, model["pred"])),
+                         "note": "gbdt_predict on the training rows, inputs resident; the call includes its node "
+                                 "preparation pass and one stream synchronisation"}
     if rank == 0 and not args.no_micro:
         line["histogram_microbench"] = microbench(g, torch, args, peak)
     if rank == 0 and not args.no_cpu:
