@@ -62,7 +62,8 @@ typedef struct {
   double gamma;
   int32_t min_samples_leaf;
   double min_child_weight;
-  int32_t n_threads; /* OpenMP threads over features; results do not depend on it */
+  int32_t num_leaves; /* leaf budget per tree; 0: none (NEXT-2, see orc_train) */
+  int32_t n_threads;  /* OpenMP threads over features; results do not depend on it */
 } orc_params;
 
 typedef struct {
@@ -123,6 +124,7 @@ int orc_validate_params(const orc_params* p) {
     return ORC_EINVAL;
   if (p->min_samples_leaf < 1 || p->min_child_weight < 0.0 || p->reg_lambda < 0.0 || p->gamma < 0.0)
     return ORC_EINVAL;
+  if (p->num_leaves < 0 || p->num_leaves == 1) return ORC_EINVAL;
   return ORC_OK;
 }
 
@@ -406,8 +408,16 @@ int orc_train(const uint8_t* bins, const int32_t* n_bins, int64_t N, int32_t F, 
   uint32_t* cnt = (uint32_t*)malloc(sizeof(uint32_t) * (size_t)F * ORC_NBINS);
   double* G = (double*)malloc(sizeof(double) * (size_t)F * ORC_NBINS);
   double* H = (double*)malloc(sizeof(double) * (size_t)F * ORC_NBINS);
-  if (!g || !order || !scratch || !seg_start || !seg_count || !cnt || !G || !H) {
+  const int32_t max_level = (int32_t)(1u << D); /* nodes of the widest level */
+  int32_t* lvl_do = (int32_t*)malloc(sizeof(int32_t) * (size_t)max_level);
+  int32_t* lvl_keep = (int32_t*)malloc(sizeof(int32_t) * (size_t)max_level);
+  int32_t* lvl_f = (int32_t*)malloc(sizeof(int32_t) * (size_t)max_level);
+  int32_t* lvl_b = (int32_t*)malloc(sizeof(int32_t) * (size_t)max_level);
+  double* lvl_gain = (double*)malloc(sizeof(double) * (size_t)max_level);
+  if (!g || !order || !scratch || !seg_start || !seg_count || !cnt || !G || !H || !lvl_do || !lvl_keep || !lvl_f ||
+      !lvl_b || !lvl_gain) {
     free(g), free(order), free(scratch), free(seg_start), free(seg_count), free(cnt), free(G), free(H);
+    free(lvl_do), free(lvl_keep), free(lvl_f), free(lvl_b), free(lvl_gain);
     return ORC_ENOMEM;
   }
 
@@ -429,7 +439,11 @@ int orc_train(const uint8_t* bins, const int32_t* n_bins, int64_t N, int32_t F, 
     seg_start[0] = 0;
     seg_count[0] = N;
     int32_t level_begin = 0, level_end = 1;
-    for (int32_t d = 0; d <= D; ++d) {
+    int32_t leaves_done = 0; /* nodes of earlier levels that stayed leaves */
+    int32_t last = D;        /* the level whose nodes are leaves without a search */
+    for (int32_t d = 0; d <= last; ++d) {
+      const int32_t nl = level_end - level_begin;
+      /* phase 1: every node of the level searches its best split */
       for (int32_t v = level_begin; v < level_end; ++v) {
         const int64_t* rows = order + seg_start[v];
         const int64_t n = seg_count[v];
@@ -457,7 +471,8 @@ int orc_train(const uint8_t* bins, const int32_t* n_bins, int64_t N, int32_t F, 
           ti[v].best_gain = -INFINITY;
           ti[v].second_gain = -INFINITY;
         }
-        if (d == D) continue; /* depth limit: leaf without search */
+        lvl_do[v - level_begin] = 0;
+        if (d == last) continue; /* depth limit (or budget): leaf without search */
 
         node_histogram(bins, N, F, g, rows, n, cnt, G, H, p->n_threads);
         orc_split sp;
@@ -474,35 +489,66 @@ int orc_train(const uint8_t* bins, const int32_t* n_bins, int64_t N, int32_t F, 
             ti[v].near_bin[k] = sp.near_bin[k];
           }
         }
-        if (tg) {
+        if (tg && do_split && tg[2 * v] >= 0 && (tg[2 * v] != f || tg[2 * v + 1] != b)) {
           int32_t gf = tg[2 * v], gb = tg[2 * v + 1];
-          int differs = do_split ? (gf != f || gb != b) : (gf != -1);
-          if (differs) {
-            int near = 0;
-            if (do_split && gf >= 0) {
-              int lim = sp.n_near < ORC_NEAR_MAX ? sp.n_near : ORC_NEAR_MAX;
-              for (int k = 0; k < lim; ++k)
-                if (sp.near_feature[k] == gf && sp.near_bin[k] == gb) near = 1;
+          int near = 0;
+          int lim = sp.n_near < ORC_NEAR_MAX ? sp.n_near : ORC_NEAR_MAX;
+          for (int k = 0; k < lim; ++k)
+            if (sp.near_feature[k] == gf && sp.near_bin[k] == gb) near = 1;
+          if (near) {
+            /* recompute the adopted candidate's gain from its own prefix sums */
+            const double* gg = G + (int64_t)gf * ORC_NBINS;
+            const double* hh = H + (int64_t)gf * ORC_NBINS;
+            double GL = 0.0, HL = 0.0;
+            for (int32_t q = 0; q <= gb; ++q) {
+              GL += gg[q];
+              HL += hh[q];
             }
-            if (near) {
-              /* recompute the adopted candidate's gain from its own prefix sums */
-              const double* gg = G + (int64_t)gf * ORC_NBINS;
-              const double* hh = H + (int64_t)gf * ORC_NBINS;
-              double GL = 0.0, HL = 0.0;
-              for (int32_t q = 0; q <= gb; ++q) {
-                GL += gg[q];
-                HL += hh[q];
-              }
-              f = gf;
-              b = gb;
-              gain = orc_gain(GL, HL, GP - GL, HP - HL, GP, HP, lambda, p->gamma);
-              if (ti) ti[v].adopted = 1;
-            } else if (ti) {
-              ti[v].guide_mismatch = 1;
-            }
+            f = gf;
+            b = gb;
+            gain = orc_gain(GL, HL, GP - GL, HP - HL, GP, HP, lambda, p->gamma);
+            if (ti) ti[v].adopted = 1;
+          } else if (ti) {
+            ti[v].guide_mismatch = 1;
           }
         }
-        if (!do_split) continue;
+        lvl_do[v - level_begin] = do_split;
+        lvl_f[v - level_begin] = f;
+        lvl_b[v - level_begin] = b;
+        lvl_gain[v - level_begin] = gain;
+      }
+      /* phase 2: leaf budget (NEXT-2, reading of the ExaBoost page's depth-capped final partial
+       * level).  If applying every split of this level would leave more than num_leaves leaves,
+       * keep the first K = num_leaves - (leaves so far + this level's nodes) candidates in the
+       * order (gain desc, node index asc), and make this the last level that splits. */
+      if (p->num_leaves > 0 && d < last) {
+        int32_t C = 0;
+        for (int32_t i = 0; i < nl; ++i) C += lvl_do[i];
+        const int32_t K = p->num_leaves - (leaves_done + nl);
+        if (C > K) {
+          for (int32_t i = 0; i < nl; ++i) {
+            if (!lvl_do[i]) continue;
+            int32_t rank = 0;
+            for (int32_t j = 0; j < nl; ++j)
+              if (lvl_do[j] && (lvl_gain[j] > lvl_gain[i] || (lvl_gain[j] == lvl_gain[i] && j < i))) ++rank;
+            lvl_keep[i] = rank < K;
+          }
+          for (int32_t i = 0; i < nl; ++i) lvl_do[i] = lvl_do[i] && lvl_keep[i];
+          last = d + 1;
+        }
+      }
+      /* phase 3: apply the splits in node order */
+      for (int32_t v = level_begin; v < level_end; ++v) {
+        const int32_t i = v - level_begin;
+        if (tg && d < D && ((tg[2 * v] >= 0) != (lvl_do[i] != 0)) && ti) ti[v].guide_mismatch = 1;
+        if (!lvl_do[i]) {
+          ++leaves_done;
+          continue;
+        }
+        const int32_t f = lvl_f[i], b = lvl_b[i];
+        const int64_t* rows = order + seg_start[v];
+        const int64_t n = seg_count[v];
+        orc_node* nd = &tn[v];
 
         /* stable partition of the node's rows: bin <= b left, others right */
         const uint8_t* col = bins + (int64_t)f * N;
@@ -510,7 +556,7 @@ int orc_train(const uint8_t* bins, const int32_t* n_bins, int64_t N, int32_t F, 
         int64_t w = 0;
         for (int64_t k = 0; k < n; ++k)
           if (col[rows[k]] <= b) dst[w++] = rows[k];
-        const int64_t nl = w;
+        const int64_t nlc = w;
         for (int64_t k = 0; k < n; ++k)
           if (!(col[rows[k]] <= b)) dst[w++] = rows[k];
         memcpy(order + seg_start[v], dst, sizeof(int64_t) * (size_t)n);
@@ -520,12 +566,12 @@ int orc_train(const uint8_t* bins, const int32_t* n_bins, int64_t N, int32_t F, 
         nd->threshold_bin = b;
         nd->left = L;
         nd->right = R;
-        nd->gain = gain;
+        nd->gain = lvl_gain[i];
         nd->is_leaf = 0;
         seg_start[L] = seg_start[v];
-        seg_count[L] = nl;
-        seg_start[R] = seg_start[v] + nl;
-        seg_count[R] = n - nl;
+        seg_count[L] = nlc;
+        seg_start[R] = seg_start[v] + nlc;
+        seg_count[R] = n - nlc;
       }
       level_begin = level_end;
       level_end = n_nodes;
@@ -545,6 +591,7 @@ int orc_train(const uint8_t* bins, const int32_t* n_bins, int64_t N, int32_t F, 
     }
   }
   free(g), free(order), free(scratch), free(seg_start), free(seg_count), free(cnt), free(G), free(H);
+  free(lvl_do), free(lvl_keep), free(lvl_f), free(lvl_b), free(lvl_gain);
   return ORC_OK;
 }
 

@@ -15,6 +15,7 @@ import oracle
 from tests import test_oracle_hand_trees as hand
 from tests import test_oracle_pins as pins
 from tests import test_oracle_predict as tp
+from tests import test_oracle_budget as tb
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
@@ -39,6 +40,9 @@ MUTATIONS = {
     "raw routing children swapped": ("v = x > thr ? tn[v].right : tn[v].left;", "v = x > thr ? tn[v].left : tn[v].right;"),
     "raw prediction without learning rate": ("const double step = lr * tn[v].leaf_value;\n      pred = pred + step;",
                                              "const double step = tn[v].leaf_value;\n      pred = pred + step;"),
+    "budget keeps the lowest gains": ("if (lvl_do[j] && (lvl_gain[j] > lvl_gain[i] || (lvl_gain[j] == lvl_gain[i] && j < i))) ++rank;",
+                                      "if (lvl_do[j] && (lvl_gain[j] < lvl_gain[i] || (lvl_gain[j] == lvl_gain[i] && j < i))) ++rank;"),
+    "budget one leaf too many": ("const int32_t K = p->num_leaves - (leaves_done + nl);", "const int32_t K = p->num_leaves + 1 - (leaves_done + nl);"),
     "feature index transposed": ("const uint8_t* col = bins + (int64_t)j * N;\n    uint32_t* c", "const uint8_t* col = bins + (int64_t)(F - 1 - j) * N;\n    uint32_t* c"),
 }
 
@@ -53,6 +57,8 @@ PINS = [
     ("quantize balanced", lambda o: pins.test_quantize_all_distinct_balanced(o, 1000, 32)),
     ("invariants", lambda o: pins.test_training_invariants(o, "tiny", None, 3)),
     ("predict hand", lambda o: tp.test_hand_model(o)),
+    ("budget truncation", lambda o: [tb.test_budget_tree_is_the_truncated_level_wise_tree("mid", 4000, 5, 12, o=o),
+                                     tb.test_budget_tree_is_the_truncated_level_wise_tree("covtype", 6000, 6, 40, o=o)]),
     ("predict = training",
      lambda o: tp.test_prediction_of_training_rows_equals_training_predictions("tiny", 3, 2, o=o)),
 ]
