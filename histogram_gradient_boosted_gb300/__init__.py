@@ -49,7 +49,7 @@ class GbdtError(RuntimeError):
 class Params(ctypes.Structure):
     _fields_ = [("n_trees", ctypes.c_int32), ("max_depth", ctypes.c_int32), ("learning_rate", ctypes.c_double),
                 ("reg_lambda", ctypes.c_double), ("gamma", ctypes.c_double), ("min_samples_leaf", ctypes.c_int32),
-                ("min_child_weight", ctypes.c_double)]
+                ("min_child_weight", ctypes.c_double), ("num_leaves", ctypes.c_int32), ("reserved", ctypes.c_int32)]
 
 
 class Diagnostics(ctypes.Structure):
@@ -164,9 +164,9 @@ def padded_ld(n: int) -> int:
 
 
 def make_params(n_trees=1, max_depth=6, learning_rate=0.1, reg_lambda=1.0, gamma=0.0, min_samples_leaf=1,
-                min_child_weight=0.0, **_ignored) -> Params:
+                min_child_weight=0.0, num_leaves=0, **_ignored) -> Params:
     return Params(int(n_trees), int(max_depth), float(learning_rate), float(reg_lambda), float(gamma),
-                  int(min_samples_leaf), float(min_child_weight))
+                  int(min_samples_leaf), float(min_child_weight), int(num_leaves), 0)
 
 
 def version() -> str:

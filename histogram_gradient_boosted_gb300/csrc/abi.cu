@@ -60,6 +60,10 @@ int validate_params(const gbdt_params* p) {
     set_error("parameters: need n_trees >= 0 and 0 <= max_depth <= %d", GBDT_MAX_DEPTH);
     return GBDT_ERR_INVALID_ARG;
   }
+  if (p->num_leaves < 0 || p->num_leaves == 1) {
+    set_error("parameters: num_leaves must be 0 (no budget) or at least 2");
+    return GBDT_ERR_INVALID_ARG;
+  }
   return GBDT_OK;
 }
 

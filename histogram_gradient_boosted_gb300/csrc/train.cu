@@ -36,11 +36,15 @@ struct LevelStats {
 
 std::atomic<int32_t> g_fail_after_levels{-1};
 
-__global__ void reset_root_kernel(gbdt_level* level, uint8_t* build_flag, gbdt_segment* seg, int64_t N) {
+// budget[0]: leaves of the tree's earlier levels; budget[1]: 1 once the leaf budget has bound.
+__global__ void reset_root_kernel(gbdt_level* level, uint8_t* build_flag, gbdt_segment* seg, int64_t N,
+                                  int32_t* budget) {
   level->node_begin = 0;
   level->n_slots = 1;
   build_flag[0] = 1;
   seg[0] = gbdt_segment{0, N};
+  budget[0] = 0;
+  budget[1] = 0;
 }
 
 __global__ void iota_kernel(uint32_t* __restrict__ v, int64_t N) {
@@ -72,8 +76,12 @@ __global__ void __launch_bounds__(1024)
                        int32_t* __restrict__ n_nodes_out, gbdt_level* __restrict__ next_level,
                        SlotTotals* __restrict__ next_totals, gbdt_segment* __restrict__ next_seg,
                        int32_t* __restrict__ pair_parent, uint8_t* __restrict__ next_build, Route* __restrict__ route,
-                       LevelStats* __restrict__ stats, int32_t* __restrict__ err) {
+                       LevelStats* __restrict__ stats, int32_t num_leaves, int32_t* __restrict__ budget,
+                       int32_t* __restrict__ err) {
   __shared__ int s_a[1024];
+  __shared__ double s_gain[kMaxSlots];                  // leaf budget: the level's candidate gains
+  __shared__ uint32_t s_cand[kMaxSlots / 32], s_keep[kMaxSlots / 32];
+  __shared__ int s_ncand, s_bind;
   __shared__ int s_pre;
   __shared__ unsigned long long s_act, s_built_rows, s_split_rows, s_scan_rows;
   __shared__ int s_built;
@@ -91,6 +99,42 @@ __global__ void __launch_bounds__(1024)
   }
   const int next_begin = node_begin + n_slots;
   const int S = *fixed_exp;
+  // After the leaf budget has bound, the level below it is the last: every node is a leaf.
+  const bool stopped = budget[1] != 0;
+  const bool leaf_level = d >= D || stopped;
+  // Leaf budget: if every candidate of the level splitting would leave more than num_leaves leaves,
+  // only the first K = num_leaves - (leaves so far + the level's nodes) in (gain desc, slot asc)
+  // split (a total order: the slot is unique), and the budget has bound.
+  if (threadIdx.x == 0) {
+    s_ncand = 0;
+    s_bind = 0;
+  }
+  for (int w = threadIdx.x; w < kMaxSlots / 32; w += blockDim.x) s_cand[w] = s_keep[w] = 0;
+  __syncthreads();
+  if (num_leaves > 0 && !leaf_level) {
+    for (int s = threadIdx.x; s < n_slots; s += blockDim.x) {
+      if (splits[s].feature >= 0) {
+        s_gain[s] = splits[s].gain;
+        atomicOr(&s_cand[s >> 5], 1u << (s & 31));
+        atomicAdd(&s_ncand, 1);
+      }
+    }
+    __syncthreads();
+    const int K = num_leaves - (budget[0] + n_slots);
+    if (s_ncand > K) {
+      for (int s = threadIdx.x; s < n_slots; s += blockDim.x) {
+        if (!(s_cand[s >> 5] >> (s & 31) & 1u)) continue;
+        const double gs = s_gain[s];
+        int rank = 0;
+        for (int o = 0; o < n_slots; ++o)
+          if ((s_cand[o >> 5] >> (o & 31) & 1u) && (s_gain[o] > gs || (s_gain[o] == gs && o < s))) ++rank;
+        if (rank < K) atomicOr(&s_keep[s >> 5], 1u << (s & 31));
+      }
+      if (threadIdx.x == 0) s_bind = 1;
+    }
+    __syncthreads();
+  }
+  const bool bind = s_bind != 0;
   for (int c0 = 0; c0 < n_slots; c0 += blockDim.x) {
     const int s = c0 + threadIdx.x;
     const bool in = s < n_slots;
@@ -100,7 +144,7 @@ __global__ void __launch_bounds__(1024)
     if (in) {
       if (d < D) {
         sp = splits[s];
-        is_split = sp.feature >= 0;
+        is_split = !stopped && sp.feature >= 0 && (!bind || (s_keep[s >> 5] >> (s & 31) & 1u));
         if (d > 0 && (sp.q_total != totals[s].q || sp.cnt_total != totals[s].cnt)) raise_error(err, kErrHistTotals);
         tot.q = sp.q_total;
         tot.cnt = sp.cnt_total;
@@ -166,6 +210,8 @@ __global__ void __launch_bounds__(1024)
     __syncthreads();
   }
   if (threadIdx.x == 0) {
+    budget[0] += n_slots - s_pre;  // this level's leaves
+    if (bind) budget[1] = 1;
     next_level->node_begin = next_begin;
     next_level->n_slots = 2 * s_pre;
     *n_nodes_out = next_begin + 2 * s_pre;
@@ -204,6 +250,7 @@ struct TrainWs {
   int32_t* n_nodes;
   LevelStats* stats;
   unsigned long long* maxabs;
+  int32_t* budget;  // leaf budget state of the current tree
   int32_t* fixed_exp;
   double* init;
   double* label_partials;
@@ -258,6 +305,7 @@ TrainWs carve_train(void* ws, size_t bytes, int64_t N, int32_t F, int64_t ldb, c
   w.n_nodes = c.take<int32_t>(T);
   w.stats = c.take<LevelStats>(static_cast<size_t>(T) * (D + 1));
   w.maxabs = c.take<unsigned long long>(1);
+  w.budget = c.take<int32_t>(2);
   w.fixed_exp = c.take<int32_t>(1);
   w.init = c.take<double>(1);
   w.label_partials = c.take<double>(kSumBlocks);
@@ -373,7 +421,7 @@ extern "C" int gbdt_train(const uint8_t* bins, int64_t ldb, const int32_t* n_bin
       launch_start_tree0(w.init, label, N, pred_out, w.g0, w.leaf, w.maxabs, s);
     }
     launch_fixed_exp(w.maxabs, N, w.fixed_exp, s);
-    reset_root_kernel<<<1, 1, 0, s>>>(w.level[0], w.build[0], w.seg[0], N);
+    reset_root_kernel<<<1, 1, 0, s>>>(w.level[0], w.build[0], w.seg[0], N, w.budget);
     count_launches();
     if (D == 0) {
       GBDT_CUDA(cudaMemsetAsync(w.totals[0], 0, sizeof(SlotTotals), s));
@@ -420,7 +468,8 @@ extern "C" int gbdt_train(const uint8_t* bins, int64_t ldb, const int32_t* n_bin
       apply_level_kernel<<<1, 1024, 0, s>>>(d, D, w.level[cur], max_slots, d < D ? w.splits : nullptr, w.totals[cur],
                                             w.build[cur], w.fixed_exp, p->reg_lambda, w.seg[cur], tree,
                                             w.n_nodes + t, w.level[nxt], w.totals[nxt], w.seg[nxt],
-                                            w.pair_parent[nxt], w.build[nxt], w.route[cur], st, w.err);
+                                            w.pair_parent[nxt], w.build[nxt], w.route[cur], st, p->num_leaves,
+                                            w.budget, w.err);
       count_launches();
       // rows: after an odd level they move into the next order (four grandchild runs per pair); at
       // even levels nothing moves and the rows of nodes that do not split record their leaf; at the

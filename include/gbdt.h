@@ -71,7 +71,13 @@ typedef struct gbdt_params {
   double gamma;             /* subtracted from every split gain */
   int32_t min_samples_leaf; /* rows each child must hold */
   double min_child_weight;  /* H each child must hold */
-} gbdt_params;
+  int32_t num_leaves;       /* leaf budget per tree, 0: none.  Levels split while all of their valid splits
+                               fit the budget; at the first level where they would not, the top
+                               K = num_leaves - (leaves so far + the level's nodes) candidates by (gain desc,
+                               node index asc) split and their children are leaves (the ExaBoost page's
+                               depth-capped final partial level).  1 is invalid. */
+  int32_t reserved;         /* 0 */
+} gbdt_params; /* 56 bytes */
 
 /* One tree node, "Module Design: Training Core" s.3 Tree Model: feature,
  * threshold bin, child indices, leaf value, gain and a leaf flag.  Trees are

@@ -71,7 +71,7 @@ def test_parameter_rules_on_host(lib):
 def test_struct_layouts_match_header():
     import histogram_gradient_boosted_gb300 as g
 
-    assert ctypes.sizeof(g.Params) == 48
+    assert ctypes.sizeof(g.Params) == 56
     assert g.NODE_DTYPE.itemsize == 40 and g.SPLIT_DTYPE.itemsize == 40
     assert g.LEVEL_DTYPE.itemsize == 8 and g.SEGMENT_DTYPE.itemsize == 16
     assert ctypes.sizeof(g.Diagnostics) == 72

@@ -125,3 +125,22 @@ def test_diagnostics_report_histogram_work():
     assert d["hist_ms"] > 0 and d["total_ms"] >= d["hist_ms"]
     assert d["hist_rows"] <= 3 * params["max_depth"] * 50_000 and d["hist_rows"] >= 3 * 50_000
     assert d["hist_bytes"] >= d["hist_rows"] * (28 + 10)
+
+
+@pytest.mark.parametrize("name,n,depth,budget,trees", [("covtype", 30_011, 10, 1023, 3), ("mid", 20_011, 6, 20, 3),
+                                                       ("tiny", 3_001, 4, 2, 2), ("large", 40_009, 8, 100, 2)])
+def test_leaf_budget_matches_oracle(name, n, depth, budget, trees):
+    """NEXT-2: levels split while all their valid splits fit num_leaves; the level where they would not
+    keeps its top candidates by (gain desc, node index asc) and is the last to split."""
+    bins, n_bins, yd, ob, on, y = _prepare(name, n)
+    params = dict(synth.CONFIGS[name], n_trees=trees, max_depth=depth, num_leaves=budget)
+    out = g.train(bins, n_bins, yd, **params)
+    for t in range(trees):
+        nd = out["nodes"][t][: out["nodes_per_tree"][t]]
+        assert 1 <= int(nd["is_leaf"].sum()) <= budget
+    compare_training(out, ob, on, y, params)
+
+
+def test_leaf_budget_of_one_is_rejected():
+    assert g.validate_params(num_leaves=1) == g.ERR_INVALID_ARG
+    assert g.validate_params(num_leaves=0) == g.OK and g.validate_params(num_leaves=2) == g.OK
