@@ -259,6 +259,8 @@ def microbench(g, torch, args, peak):
     split_out = torch.empty(n_nodes * g.SPLIT_DTYPE.itemsize, dtype=torch.uint8, device="cuda")
     stream = torch.cuda.current_stream()
     times = {"partition": [], "build": [], "subtract": [], "find": []}
+    rb_times = []
+    rb = None
     for it in range(args.warmup + args.steps):
         ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
         ev[0].record(stream)
@@ -273,21 +275,35 @@ def microbench(g, torch, args, peak):
                       min_samples_leaf=1, min_child_weight=0.0)
         ev[4].record(stream)
         torch.cuda.synchronize()
+        # the same build on the row-block layout the training levels use (converted once, untimed: the
+        # partition's output is the same every iteration)
+        if rb is None:
+            rb = g.to_row_blocks(cb, N)
+            torch.cuda.synchronize()
+        r0, r1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        r0.record(stream)
+        g.build_histograms_segmented(cb, N, cg, S, lvl, n_nodes, fd, P, cseg, hc, hq, ws=hws, row_blocks=rb)
+        r1.record(stream)
+        torch.cuda.synchronize()
         if it >= args.warmup:
             for k, name in enumerate(times):
                 times[name].append(ev[k].elapsed_time(ev[k + 1]))
+            rb_times.append(r0.elapsed_time(r1))
     ms = {k: statistics.mean(v) for k, v in times.items()}
+    rb_ms = statistics.mean(rb_times)
     n_small = int(np.minimum(counts[0::2], counts[1::2]).sum())
     build_bytes = n_small * (F + 4) + P * F * 256 * 12
     part_bytes = N * (2 * (F + 4 + 4) + 1)
     formula_bytes = N * (F + 4 + 1) + P * F * 256 * 12  # full-scan accounting: every active row read once
-    level_ms = sum(ms.values())
+    level_ms = ms["partition"] + rb_ms + ms["subtract"] + ms["find"]
     res = {"workload": f"one level: {N:,} rows x {F} pre-binned uint8 features (Zipf 1.1), {n_nodes} nodes "
                        f"(uniform), rows grouped by parent, fp32 g",
            "partition_ms": ms["partition"], "build_ms": ms["build"], "subtract_ms": ms["subtract"],
            "find_splits_ms": ms["find"], "level_ms": level_ms,
-           "build_algorithmic_bytes": build_bytes, "build_gbs": build_bytes / (ms["build"] * 1e-3) / 1e9,
-           "build_frac": build_bytes / (ms["build"] * 1e-3) / 1e9 / peak,
+           "build_algorithmic_bytes": build_bytes,
+           "build_gbs": build_bytes / (rb_ms * 1e-3) / 1e9, "build_frac": build_bytes / (rb_ms * 1e-3) / 1e9 / peak,
+           "build_layout": "row blocks (the layout the training levels read)", "build_row_blocks_ms": rb_ms,
+           "build_columns_ms": ms["build"], "build_columns_frac": build_bytes / (ms["build"] * 1e-3) / 1e9 / peak,
            "partition_gbs": part_bytes / (ms["partition"] * 1e-3) / 1e9,
            "partition_frac": part_bytes / (ms["partition"] * 1e-3) / 1e9 / peak,
            "level_effective_gbs": formula_bytes / (level_ms * 1e-3) / 1e9,

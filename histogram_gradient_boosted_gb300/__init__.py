@@ -26,6 +26,7 @@ __all__ = ["lib", "GbdtError", "Params", "NODE_DTYPE", "SPLIT_DTYPE", "LEVEL_DTY
 
 OK, ERR_INVALID_ARG, ERR_NONFINITE, ERR_WORKSPACE, ERR_CUDA, ERR_INTERNAL = 0, -1, -2, -3, -4, -5
 DTYPE_F32, DTYPE_F64 = 0, 1
+LAYOUT_COLUMNS, LAYOUT_ROW_BLOCKS = 0, 1
 MAX_BINS, MAX_DEPTH = 256, 12
 
 EXPORTED_SYMBOLS = [
@@ -36,7 +37,8 @@ EXPORTED_SYMBOLS = [
     "gbdt_partition_workspace_size", "gbdt_partition", "gbdt_update_predictions", "gbdt_train_workspace_size",
     "gbdt_train", "gbdt_debug_inject_failure", "gbdt_kernel_launch_count", "gbdt_partition_noalloc",
     "gbdt_histograms_segmented_workspace_size", "gbdt_build_histograms_segmented", "gbdt_partition_rows_workspace_size",
-    "gbdt_partition_rows", "gbdt_predict_workspace_size", "gbdt_predict",
+    "gbdt_partition_rows", "gbdt_predict_workspace_size", "gbdt_predict", "gbdt_row_block_pitch",
+    "gbdt_row_block_bytes", "gbdt_bins_to_row_blocks",
 ]
 
 
@@ -106,7 +108,11 @@ def lib():
         "gbdt_kernel_launch_count": ([], i64),
         "gbdt_partition_noalloc": ([P, i64, i64, i32, P, P, i32, P, P, P, P, P, P, P], i32),
         "gbdt_histograms_segmented_workspace_size": ([i32], sz),
-        "gbdt_build_histograms_segmented": ([P, i64, i64, i32, P, i32, P, P, i32, P, i32, P, P, P, P, P, sz, P], i32),
+        "gbdt_build_histograms_segmented": ([P, i64, i32, i64, i32, P, i32, P, P, i32, P, i32, P, P, P, P, P, sz, P],
+                                            i32),
+        "gbdt_row_block_pitch": ([i32], i64),
+        "gbdt_row_block_bytes": ([i64, i32], sz),
+        "gbdt_bins_to_row_blocks": ([P, i64, i64, i32, P, P], i32),
         "gbdt_partition_rows_workspace_size": ([i64, i32], sz),
         "gbdt_partition_rows": ([P, P, i64, i64, i32, P, P, i32, P, P, P, P, P, i32, P, P, P, P, P, sz, P], i32),
         "gbdt_predict_workspace_size": ([i32, i32], sz),
@@ -233,10 +239,23 @@ def build_histograms(bins, N, g, fixed_exp, node_of_row, level, max_slots, build
     return hist_cnt, hist_q
 
 
+def to_row_blocks(bins, N: int):
+    """Column-major bins (F, ldb) CUDA uint8 -> the row-block layout (a flat CUDA uint8 tensor) and its pitch."""
+    torch = _torch()
+    F, ldb = bins.shape
+    out = torch.empty(lib().gbdt_row_block_bytes(N, F) + 256, dtype=torch.uint8, device="cuda")
+    off = (-out.data_ptr()) % 256  # 256-byte aligned view
+    out = out[off: off + lib().gbdt_row_block_bytes(N, F)]
+    _check(lib().gbdt_bins_to_row_blocks(_ptr(bins), ldb, N, F, _ptr(out), _stream()))
+    return out, lib().gbdt_row_block_pitch(F)
+
+
 def build_histograms_segmented(bins, N, g, fixed_exp, level, max_slots, build_flag, max_build, segments,
-                               hist_cnt=None, hist_q=None, ws=None, filters=None):
+                               hist_cnt=None, hist_q=None, ws=None, filters=None, row_blocks=None):
     """Histograms of flagged slots whose rows are contiguous segments (SEGMENT_DTYPE bytes, device),
-    optionally narrowed per slot by FILTER_DTYPE records (device bytes)."""
+    optionally narrowed per slot by FILTER_DTYPE records (device bytes).  bins: column-major (F, ldb)
+    CUDA uint8; with row_blocks = (buffer, pitch) from to_row_blocks the kernel reads that layout instead
+    (bins then only gives F)."""
     torch = _torch()
     F, ldb = bins.shape
     if hist_cnt is None:
@@ -245,10 +264,12 @@ def build_histograms_segmented(bins, N, g, fixed_exp, level, max_slots, build_fl
     if ws is None:
         ws = _workspace(lib().gbdt_histograms_segmented_workspace_size(max_slots))
     dt = DTYPE_F32 if g.dtype == torch.float32 else DTYPE_F64
-    _check(lib().gbdt_build_histograms_segmented(_ptr(bins), ldb, N, F, _ptr(g), dt, _ptr(fixed_exp), _ptr(level),
-                                                 max_slots, _ptr(build_flag), max_build, _ptr(segments),
-                                                 _ptr(filters) if filters is not None else None, _ptr(hist_cnt),
-                                                 _ptr(hist_q), _ptr(ws), ws.numel(), _stream()))
+    src, ld, layout = (bins, ldb, LAYOUT_COLUMNS) if row_blocks is None else (row_blocks[0], row_blocks[1],
+                                                                              LAYOUT_ROW_BLOCKS)
+    _check(lib().gbdt_build_histograms_segmented(_ptr(src), ld, layout, N, F, _ptr(g), dt, _ptr(fixed_exp),
+                                                 _ptr(level), max_slots, _ptr(build_flag), max_build,
+                                                 _ptr(segments), _ptr(filters) if filters is not None else None,
+                                                 _ptr(hist_cnt), _ptr(hist_q), _ptr(ws), ws.numel(), _stream()))
     return hist_cnt, hist_q
 
 

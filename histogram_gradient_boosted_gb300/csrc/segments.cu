@@ -1393,8 +1393,27 @@ extern "C" size_t gbdt_histograms_segmented_workspace_size(int32_t max_slots) {
   return seg_hist_scratch_bytes(max_slots);
 }
 
-extern "C" int gbdt_build_histograms_segmented(const uint8_t* bins, int64_t ldb, int64_t N, int32_t F, const void* g,
-                                               int32_t g_dtype, const int32_t* fixed_exp, const gbdt_level* level,
+extern "C" int64_t gbdt_row_block_pitch(int32_t F) { return F >= 1 ? rb_pitch(F) : 0; }
+
+extern "C" size_t gbdt_row_block_bytes(int64_t N, int32_t F) {
+  return (N >= 1 && F >= 1) ? row_block_bytes(N, F) : 0;
+}
+
+extern "C" int gbdt_bins_to_row_blocks(const uint8_t* bins, int64_t ldb, int64_t N, int32_t F, uint8_t* out,
+                                       void* stream) {
+  clear_error();
+  GBDT_CHECK_ARG(bins && out, "gbdt_bins_to_row_blocks: null pointer");
+  GBDT_CHECK_ARG(N >= 1 && N < (int64_t(1) << 31) && F >= 1 && F <= 4096, "gbdt_bins_to_row_blocks: sizes out of range");
+  GBDT_CHECK_ARG(ldb >= N && ldb % 16 == 0 && aligned(bins, 16) && aligned(out, 32),
+                 "gbdt_bins_to_row_blocks: need ldb >= N, ldb %% 16 == 0, 16-byte aligned bins, 32-byte aligned out");
+  launch_cols_to_row_blocks(bins, ldb, N, F, out, static_cast<cudaStream_t>(stream));
+  GBDT_LAUNCH_CHECK();
+  return GBDT_OK;
+}
+
+extern "C" int gbdt_build_histograms_segmented(const uint8_t* bins, int64_t ldb, int32_t layout, int64_t N, int32_t F,
+                                               const void* g, int32_t g_dtype, const int32_t* fixed_exp,
+                                               const gbdt_level* level,
                                                int32_t max_slots, const uint8_t* build_flag, int32_t max_build,
                                                const gbdt_segment* segments, const gbdt_filter* filters,
                                                uint32_t* hist_cnt, int64_t* hist_q, void* ws, size_t ws_bytes,
@@ -1404,8 +1423,16 @@ extern "C" int gbdt_build_histograms_segmented(const uint8_t* bins, int64_t ldb,
                  "gbdt_build_histograms_segmented: null pointer");
   GBDT_CHECK_ARG(N >= 1 && N < (int64_t(1) << 31) && F >= 1 && F <= 4096,
                  "gbdt_build_histograms_segmented: sizes out of range");
-  GBDT_CHECK_ARG(ldb >= N && ldb % 16 == 0 && aligned(bins, 16) && aligned(g, 16),
-                 "gbdt_build_histograms_segmented: need ldb >= N, ldb %% 16 == 0, 16-byte aligned bins and g");
+  GBDT_CHECK_ARG(layout == GBDT_LAYOUT_COLUMNS || layout == GBDT_LAYOUT_ROW_BLOCKS,
+                 "gbdt_build_histograms_segmented: bad layout");
+  if (layout == GBDT_LAYOUT_COLUMNS) {
+    GBDT_CHECK_ARG(ldb >= N && ldb % 16 == 0 && aligned(bins, 16) && aligned(g, 16),
+                   "gbdt_build_histograms_segmented: need ldb >= N, ldb %% 16 == 0, 16-byte aligned bins and g");
+  } else {
+    GBDT_CHECK_ARG(ldb == rb_pitch(F) && aligned(bins, 32) && aligned(g, 16),
+                   "gbdt_build_histograms_segmented: row blocks need ldb = gbdt_row_block_pitch(F), 32-byte "
+                   "aligned bins, 16-byte aligned g");
+  }
   GBDT_CHECK_ARG(g_dtype == GBDT_DTYPE_F32 || g_dtype == GBDT_DTYPE_F64, "gbdt_build_histograms_segmented: bad dtype");
   GBDT_CHECK_ARG(max_slots >= 1 && max_slots <= kMaxSlots && max_build >= 1 && max_build <= max_slots,
                  "gbdt_build_histograms_segmented: slot bounds out of range");
@@ -1416,7 +1443,7 @@ extern "C" int gbdt_build_histograms_segmented(const uint8_t* bins, int64_t ldb,
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const SegHistPlan plan = plan_seg_histograms(N, F, max_slots, max_build);
   int rc = launch_seg_histograms(plan, bins, ldb, N, F, g, g_dtype, fixed_exp, level, max_slots, build_flag, segments,
-                                 filters, ws, hist_cnt, hist_q, s);
+                                 filters, ws, hist_cnt, hist_q, s, layout == GBDT_LAYOUT_ROW_BLOCKS);
   if (rc != GBDT_OK) return rc;
   GBDT_LAUNCH_CHECK();
   return GBDT_OK;

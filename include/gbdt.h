@@ -241,9 +241,26 @@ int gbdt_subtract_histograms(const uint32_t* prev_cnt, const int64_t* prev_q, co
  * 64 features of shared-memory histograms per CTA.  segments, filters
  * [max_slots] (device; filters may be NULL); other arguments and outputs as
  * gbdt_build_histograms.  Workspace: gbdt_histograms_segmented_workspace_size. */
+#define GBDT_LAYOUT_COLUMNS 0    /* bins [F][ldb]: feature j's row p at j * ldb + p */
+#define GBDT_LAYOUT_ROW_BLOCKS 1 /* feature j's row p at (p / 32) * pitch + 32 * j + p % 32 */
+
+/* The row-block layout of binned features (the layout gbdt_train keeps its
+ * per-level copies in; the pages have no counterpart): the 32 rows of a row
+ * block are contiguous per feature and the features of a row block are
+ * contiguous, so 32 lanes reading 32 rows of 32 consecutive features read one
+ * contiguous kilobyte.  pitch = 32 * (F rounded up to a multiple of 4) bytes
+ * per row block; a buffer holds ceil(N / 32) row blocks, 32-byte aligned.
+ * gbdt_bins_to_row_blocks converts column-major bins [F][ldb] (asynchronous);
+ * bytes of the last row block past N are copied as they are. */
+int64_t gbdt_row_block_pitch(int32_t F);
+size_t gbdt_row_block_bytes(int64_t N, int32_t F);
+int gbdt_bins_to_row_blocks(const uint8_t* bins, int64_t ldb, int64_t N, int32_t F, uint8_t* out, void* stream);
+
 size_t gbdt_histograms_segmented_workspace_size(int32_t max_slots);
-int gbdt_build_histograms_segmented(const uint8_t* bins, int64_t ldb, int64_t N, int32_t F, const void* g,
-                                    int32_t g_dtype, const int32_t* fixed_exp, const gbdt_level* level,
+/* layout: GBDT_LAYOUT_COLUMNS (ldb >= N, ldb % 16 == 0) or GBDT_LAYOUT_ROW_BLOCKS
+ * (ldb = gbdt_row_block_pitch(F), bins 32-byte aligned). */
+int gbdt_build_histograms_segmented(const uint8_t* bins, int64_t ldb, int32_t layout, int64_t N, int32_t F,
+                                    const void* g, int32_t g_dtype, const int32_t* fixed_exp, const gbdt_level* level,
                                     int32_t max_slots, const uint8_t* build_flag, int32_t max_build,
                                     const gbdt_segment* segments, const gbdt_filter* filters, uint32_t* hist_cnt,
                                     int64_t* hist_q, void* ws, size_t ws_bytes, void* stream);

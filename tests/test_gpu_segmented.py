@@ -27,10 +27,11 @@ def _segments(rng, N, n_slots, empty=()):
     return seg, slot
 
 
+@pytest.mark.parametrize("layout", ["columns", "row_blocks"])
 @pytest.mark.parametrize("N,F,n_slots,gdtype", [(200_003, 7, 5, np.float64), (150_001, 70, 9, np.float32),
                                                  (77_777, 130, 3, np.float64), (40_000, 3, 64, np.float64),
                                                  (5, 2, 4, np.float64)])
-def test_segmented_histograms_match_oracle(N, F, n_slots, gdtype):
+def test_segmented_histograms_match_oracle(N, F, n_slots, gdtype, layout):
     rng = np.random.default_rng(N + F)
     seg, slot = _segments(rng, N, n_slots, empty=(1,) if n_slots > 2 else ())
     bins = rng.integers(0, 256, (F, N)).astype(np.uint8)
@@ -46,8 +47,9 @@ def test_segmented_histograms_match_oracle(N, F, n_slots, gdtype):
     hc = torch.full((n_slots, F, 256), sentinel, dtype=torch.int32, device="cuda")
     hq = torch.full((n_slots, F, 256), sentinel, dtype=torch.int64, device="cuda")
     Bd, gd = dev_bins(bins), torch.from_numpy(gv).cuda()
+    rb = g.to_row_blocks(Bd, N) if layout == "row_blocks" else None
     g.build_histograms_segmented(Bd, N, gd, S, level(0, n_slots), n_slots, torch.from_numpy(flags).cuda(),
-                                 int(flags.sum()), dev_struct(seg, g.SEGMENT_DTYPE), hc, hq)
+                                 int(flags.sum()), dev_struct(seg, g.SEGMENT_DTYPE), hc, hq, row_blocks=rb)
     ref = oracle.histograms(bins, gv.astype(np.float64), slot.astype(np.int32), n_slots)
     # A/B against the node-id kernel on the same rows: bit-identical integers
     dc, dq = g.build_histograms(Bd, N, gd, S, u16(slot.astype(np.uint16)), level(0, n_slots), n_slots,
@@ -66,9 +68,10 @@ def test_segmented_histograms_match_oracle(N, F, n_slots, gdtype):
         assert torch.equal(hc[s], dc[s]) and torch.equal(hq[s], dq[s])
 
 
+@pytest.mark.parametrize("layout", ["columns", "row_blocks"])
 @pytest.mark.parametrize("N,F,n_slots,gdtype", [(180_001, 9, 6, np.float64), (120_003, 70, 4, np.float32),
                                                  (33, 3, 2, np.float64)])
-def test_filtered_histograms_match_oracle(N, F, n_slots, gdtype):
+def test_filtered_histograms_match_oracle(N, F, n_slots, gdtype, layout):
     """A slot whose rows still sit inside its parent's segment: the segment is the parent's and
     the filter keeps the rows on the slot's side of the parent's split."""
     rng = np.random.default_rng(3 * N + F)
@@ -93,9 +96,12 @@ def test_filtered_histograms_match_oracle(N, F, n_slots, gdtype):
     flags[n_slots - 1] = 1
     S = g.gradient_scale(torch.from_numpy(gv).cuda())
     s_exp = int(S.item())
-    hc, hq = g.build_histograms_segmented(dev_bins(bins), N, torch.from_numpy(gv).cuda(), S, level(0, n_slots),
+    Bd = dev_bins(bins)
+    rb = g.to_row_blocks(Bd, N) if layout == "row_blocks" else None
+    hc, hq = g.build_histograms_segmented(Bd, N, torch.from_numpy(gv).cuda(), S, level(0, n_slots),
                                           n_slots, torch.from_numpy(flags).cuda(), int(flags.sum()),
-                                          dev_struct(seg, g.SEGMENT_DTYPE), filters=dev_struct(filt, g.FILTER_DTYPE))
+                                          dev_struct(seg, g.SEGMENT_DTYPE), filters=dev_struct(filt, g.FILTER_DTYPE),
+                                          row_blocks=rb)
     hc_h, hq_h = hc.cpu().numpy().view(np.uint32), hq.cpu().numpy()
     for s in range(n_slots):
         if not flags[s]:
