@@ -34,7 +34,8 @@ class Params(ctypes.Structure):
     _fields_ = [("n_trees", ctypes.c_int32), ("max_depth", ctypes.c_int32),
                 ("learning_rate", ctypes.c_double), ("reg_lambda", ctypes.c_double),
                 ("gamma", ctypes.c_double), ("min_samples_leaf", ctypes.c_int32),
-                ("min_child_weight", ctypes.c_double), ("num_leaves", ctypes.c_int32), ("n_threads", ctypes.c_int32)]
+                ("min_child_weight", ctypes.c_double), ("num_leaves", ctypes.c_int32), ("objective", ctypes.c_int32),
+                ("n_threads", ctypes.c_int32)]
 
 
 class Split(ctypes.Structure):
@@ -85,6 +86,7 @@ def lib():
         L.orc_partition.argtypes = [P, i64, i32, P, P, P, P, P, P, P]
         L.orc_update_predictions.argtypes = [P, P, P, i64, dbl]
         L.orc_predict.argtypes = [P, i64, i32, P, i32, P, i32, i32, dbl, dbl, P]
+        L.orc_gradients_objective.argtypes = [P, P, i64, i32, P, P]
         L.orc_weight.argtypes = [dbl, dbl, dbl]
         L.orc_weight.restype = dbl
         L.orc_gain.argtypes = [dbl] * 8
@@ -110,9 +112,9 @@ class OracleError(RuntimeError):
 
 
 def make_params(n_trees=1, max_depth=3, learning_rate=0.1, reg_lambda=1.0, gamma=0.0, min_samples_leaf=1,
-                min_child_weight=0.0, num_leaves=0, n_threads=1, **_ignored) -> Params:
+                min_child_weight=0.0, num_leaves=0, objective=0, n_threads=1, **_ignored) -> Params:
     return Params(int(n_trees), int(max_depth), float(learning_rate), float(reg_lambda), float(gamma),
-                  int(min_samples_leaf), float(min_child_weight), int(num_leaves), int(n_threads))
+                  int(min_samples_leaf), float(min_child_weight), int(num_leaves), int(objective), int(n_threads))
 
 
 def weight(G: float, H: float, reg_lambda: float) -> float:
@@ -139,12 +141,13 @@ def quantize(X: np.ndarray, max_bins: int, n_threads: int = 1):
     return bins, edges, n_bins
 
 
-def gradients(pred: np.ndarray, label: np.ndarray):
+def gradients(pred: np.ndarray, label: np.ndarray, objective: int = 0):
     pred = np.ascontiguousarray(pred, dtype=np.float64)
     label = np.ascontiguousarray(label, dtype=np.float32)
     g = np.empty(pred.shape[0], dtype=np.float64)
     h = np.empty(pred.shape[0], dtype=np.float64)
-    _check(lib().orc_gradients(_p(pred), _p(label), pred.shape[0], _p(g), _p(h)), "gradients")
+    _check(lib().orc_gradients_objective(_p(pred), _p(label), pred.shape[0], int(objective), _p(g), _p(h)),
+           "gradients")
     return g, h
 
 

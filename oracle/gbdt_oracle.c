@@ -62,7 +62,8 @@ typedef struct {
   double gamma;
   int32_t min_samples_leaf;
   double min_child_weight;
-  int32_t num_leaves; /* leaf budget per tree; 0: none (NEXT-2, see orc_train) */
+  int32_t num_leaves; /* leaf budget per tree; 0: none (see orc_train) */
+  int32_t objective;  /* 0: squared error; 1: logistic (see orc_gradients_objective) */
   int32_t n_threads;  /* OpenMP threads over features; results do not depend on it */
 } orc_params;
 
@@ -125,6 +126,7 @@ int orc_validate_params(const orc_params* p) {
   if (p->min_samples_leaf < 1 || p->min_child_weight < 0.0 || p->reg_lambda < 0.0 || p->gamma < 0.0)
     return ORC_EINVAL;
   if (p->num_leaves < 0 || p->num_leaves == 1) return ORC_EINVAL;
+  if (p->objective != 0 && p->objective != 1) return ORC_EINVAL;
   return ORC_OK;
 }
 
@@ -211,6 +213,23 @@ int orc_gradients(const double* pred, const float* label, int64_t N, double* g, 
   return ORC_OK;
 }
 
+/* Gradients of the objective at the margins pred.  0, squared error ([MPS-TC]
+ * s.2): g = pred - label, h = 1.  1, logistic ("Gradient boosted trees
+ * (spec model)", binary cross-entropy with a sigmoid and its gradient
+ * sigmoid(pred) - target): p = 1 / (1 + exp(-pred)), g = p - label, and the
+ * second derivative of the loss in the margin, h = p (1 - p). */
+int orc_gradients_objective(const double* pred, const float* label, int64_t N, int32_t objective, double* g,
+                            double* h) {
+  if (objective == 0) return orc_gradients(pred, label, N, g, h);
+  if (objective != 1 || !pred || !label || !g || N < 0) return ORC_EINVAL;
+  for (int64_t i = 0; i < N; ++i) {
+    const double p = 1.0 / (1.0 + exp(-pred[i]));
+    g[i] = p - (double)label[i];
+    if (h) h[i] = p * (1.0 - p);
+  }
+  return ORC_OK;
+}
+
 /* ------------------------------------------------------------------------ */
 /* [MPS-TC] s.7: per-bin count/G/H in supplied row-index order, FP64.       */
 /* ------------------------------------------------------------------------ */
@@ -218,8 +237,8 @@ int orc_gradients(const double* pred, const float* label, int64_t N, double* g, 
  * Histogram of one node: rows[0..n) in the order given.  cnt/G/H are
  * [F][256]; A_out (optional) receives sum |g| over the node's rows.
  */
-static void node_histogram(const uint8_t* bins, int64_t N, int32_t F, const double* g, const int64_t* rows,
-                           int64_t n, uint32_t* cnt, double* G, double* H, int32_t n_threads) {
+static void node_histogram(const uint8_t* bins, int64_t N, int32_t F, const double* g, const double* h,
+                           const int64_t* rows, int64_t n, uint32_t* cnt, double* G, double* H, int32_t n_threads) {
   memset(cnt, 0, sizeof(uint32_t) * (size_t)F * ORC_NBINS);
   memset(G, 0, sizeof(double) * (size_t)F * ORC_NBINS);
   memset(H, 0, sizeof(double) * (size_t)F * ORC_NBINS);
@@ -237,7 +256,7 @@ static void node_histogram(const uint8_t* bins, int64_t N, int32_t F, const doub
       int b = col[r];
       c[b] += 1u;
       gg[b] += g[r];
-      hh[b] += 1.0;
+      hh[b] += h ? h[r] : 1.0;
     }
   }
 }
@@ -395,12 +414,17 @@ int orc_train(const uint8_t* bins, const int32_t* n_bins, int64_t N, int32_t F, 
     if (n_bins[j] < 1 || n_bins[j] > ORC_NBINS) return ORC_EINVAL;
   for (int64_t i = 0; i < N; ++i)
     if (!isfinite(label[i])) return ORC_ENONFINITE;
+  const int logistic = p->objective == 1;
+  if (logistic)
+    for (int64_t i = 0; i < N; ++i)
+      if (label[i] != 0.0f && label[i] != 1.0f) return ORC_EINVAL; /* binary labels */
 
   const int32_t D = p->max_depth;
   const int32_t max_nodes = (int32_t)((1u << (D + 1)) - 1u);
   const double lambda = p->reg_lambda;
 
   double* g = (double*)malloc(sizeof(double) * (size_t)N);
+  double* hv = logistic ? (double*)malloc(sizeof(double) * (size_t)N) : NULL;
   int64_t* order = (int64_t*)malloc(sizeof(int64_t) * (size_t)N); /* rows grouped by node */
   int64_t* scratch = (int64_t*)malloc(sizeof(int64_t) * (size_t)N);
   int64_t* seg_start = (int64_t*)malloc(sizeof(int64_t) * (size_t)max_nodes);
@@ -414,17 +438,19 @@ int orc_train(const uint8_t* bins, const int32_t* n_bins, int64_t N, int32_t F, 
   int32_t* lvl_f = (int32_t*)malloc(sizeof(int32_t) * (size_t)max_level);
   int32_t* lvl_b = (int32_t*)malloc(sizeof(int32_t) * (size_t)max_level);
   double* lvl_gain = (double*)malloc(sizeof(double) * (size_t)max_level);
-  if (!g || !order || !scratch || !seg_start || !seg_count || !cnt || !G || !H || !lvl_do || !lvl_keep || !lvl_f ||
-      !lvl_b || !lvl_gain) {
+  if (!g || (logistic && !hv) || !order || !scratch || !seg_start || !seg_count || !cnt || !G || !H || !lvl_do ||
+      !lvl_keep || !lvl_f || !lvl_b || !lvl_gain) {
+    free(hv);
     free(g), free(order), free(scratch), free(seg_start), free(seg_count), free(cnt), free(G), free(H);
     free(lvl_do), free(lvl_keep), free(lvl_f), free(lvl_b), free(lvl_gain);
     return ORC_ENOMEM;
   }
 
-  /* initial prediction: mean label, FP64 sum in row order */
+  /* initial prediction: mean label, FP64 sum in row order (squared error); margin 0, probability
+   * one half (logistic; a reading: the pages fix no initial value for it) */
   double sum = 0.0;
   for (int64_t i = 0; i < N; ++i) sum += (double)label[i];
-  const double init = sum / (double)N;
+  const double init = logistic ? 0.0 : sum / (double)N;
   *init_pred = init;
   for (int64_t i = 0; i < N; ++i) pred[i] = init;
 
@@ -432,7 +458,7 @@ int orc_train(const uint8_t* bins, const int32_t* n_bins, int64_t N, int32_t F, 
     orc_node* tn = nodes + (int64_t)t * max_nodes;
     orc_node_info* ti = info ? info + (int64_t)t * max_nodes : NULL;
     const int32_t* tg = guide ? guide + (int64_t)t * max_nodes * 2 : NULL;
-    orc_gradients(pred, label, N, g, NULL);
+    orc_gradients_objective(pred, label, N, p->objective, g, hv);
 
     for (int64_t i = 0; i < N; ++i) order[i] = i;
     int32_t n_nodes = 1;
@@ -450,7 +476,7 @@ int orc_train(const uint8_t* bins, const int32_t* n_bins, int64_t N, int32_t F, 
         double GP = 0.0, HP = 0.0, A = 0.0;
         for (int64_t k = 0; k < n; ++k) {
           GP += g[rows[k]];
-          HP += 1.0;
+          HP += hv ? hv[rows[k]] : 1.0;
           A += fabs(g[rows[k]]);
         }
         orc_node* nd = &tn[v];
@@ -474,7 +500,7 @@ int orc_train(const uint8_t* bins, const int32_t* n_bins, int64_t N, int32_t F, 
         lvl_do[v - level_begin] = 0;
         if (d == last) continue; /* depth limit (or budget): leaf without search */
 
-        node_histogram(bins, N, F, g, rows, n, cnt, G, H, p->n_threads);
+        node_histogram(bins, N, F, g, hv, rows, n, cnt, G, H, p->n_threads);
         orc_split sp;
         orc_best_split(cnt, G, H, F, n_bins, n, GP, HP, p, &sp);
         int do_split = sp.valid && sp.gain > 0.0;
@@ -517,7 +543,7 @@ int orc_train(const uint8_t* bins, const int32_t* n_bins, int64_t N, int32_t F, 
         lvl_b[v - level_begin] = b;
         lvl_gain[v - level_begin] = gain;
       }
-      /* phase 2: leaf budget (NEXT-2, reading of the ExaBoost page's depth-capped final partial
+      /* phase 2: leaf budget (a reading of the ExaBoost page's depth-capped final partial
        * level).  If applying every split of this level would leave more than num_leaves leaves,
        * keep the first K = num_leaves - (leaves so far + this level's nodes) candidates in the
        * order (gain desc, node index asc), and make this the last level that splits. */
@@ -592,6 +618,7 @@ int orc_train(const uint8_t* bins, const int32_t* n_bins, int64_t N, int32_t F, 
   }
   free(g), free(order), free(scratch), free(seg_start), free(seg_count), free(cnt), free(G), free(H);
   free(lvl_do), free(lvl_keep), free(lvl_f), free(lvl_b), free(lvl_gain);
+  free(hv);
   return ORC_OK;
 }
 

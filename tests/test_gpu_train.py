@@ -130,7 +130,7 @@ def test_diagnostics_report_histogram_work():
 @pytest.mark.parametrize("name,n,depth,budget,trees", [("covtype", 30_011, 10, 1023, 3), ("mid", 20_011, 6, 20, 3),
                                                        ("tiny", 3_001, 4, 2, 2), ("large", 40_009, 8, 100, 2)])
 def test_leaf_budget_matches_oracle(name, n, depth, budget, trees):
-    """NEXT-2: levels split while all their valid splits fit num_leaves; the level where they would not
+    """Leaf budget: levels split while all their valid splits fit num_leaves; the level where they would not
     keeps its top candidates by (gain desc, node index asc) and is the last to split."""
     bins, n_bins, yd, ob, on, y = _prepare(name, n)
     params = dict(synth.CONFIGS[name], n_trees=trees, max_depth=depth, num_leaves=budget)

@@ -1,4 +1,4 @@
-"""Pins of the oracle's leaf budget (NEXT-2, the ExaBoost page's "depth-capped
+"""Pins of the oracle's leaf budget (the ExaBoost page's "depth-capped
 final partial level"): levels split while every valid split fits the budget;
 at the first level where applying all of them would exceed num_leaves, only
 the top K = num_leaves - (leaves so far + the level's nodes) candidates by

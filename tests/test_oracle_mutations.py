@@ -16,6 +16,7 @@ from tests import test_oracle_hand_trees as hand
 from tests import test_oracle_pins as pins
 from tests import test_oracle_predict as tp
 from tests import test_oracle_budget as tb
+from tests import test_oracle_logistic as tl
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
@@ -34,7 +35,8 @@ MUTATIONS = {
                                "for (int32_t b = 0; b <= nb - 3; ++b) {\n      GL += gg[b];\n      HL += hh[b];\n      cL += c[b];\n      int64_t cR = n_P - cL;\n      double GR"),
     "prediction update sign": ("pred[rows[k]] = pred[rows[k]] + step;", "pred[rows[k]] = pred[rows[k]] - step;"),
     "quantile index off by one": ("int64_t pk = ((int64_t)k * N + B - 1) / B - 1;", "int64_t pk = ((int64_t)k * N + B - 1) / B;"),
-    "initial prediction": ("const double init = sum / (double)N;", "const double init = sum / (double)(N + 1);"),
+    "initial prediction": ("const double init = logistic ? 0.0 : sum / (double)N;",
+                           "const double init = logistic ? 0.0 : sum / (double)(N + 1);"),
     "gradient sign": ("g[i] = pred[i] - (double)label[i];", "g[i] = (double)label[i] - pred[i];"),
     "raw routing >= instead of >": ("v = x > thr ? tn[v].right : tn[v].left;", "v = x >= thr ? tn[v].right : tn[v].left;"),
     "raw routing children swapped": ("v = x > thr ? tn[v].right : tn[v].left;", "v = x > thr ? tn[v].left : tn[v].right;"),
@@ -43,6 +45,10 @@ MUTATIONS = {
     "budget keeps the lowest gains": ("if (lvl_do[j] && (lvl_gain[j] > lvl_gain[i] || (lvl_gain[j] == lvl_gain[i] && j < i))) ++rank;",
                                       "if (lvl_do[j] && (lvl_gain[j] < lvl_gain[i] || (lvl_gain[j] == lvl_gain[i] && j < i))) ++rank;"),
     "budget one leaf too many": ("const int32_t K = p->num_leaves - (leaves_done + nl);", "const int32_t K = p->num_leaves + 1 - (leaves_done + nl);"),
+    "sigmoid sign": ("const double p = 1.0 / (1.0 + exp(-pred[i]));", "const double p = 1.0 / (1.0 + exp(pred[i]));"),
+    "logistic hessian is p": ("if (h) h[i] = p * (1.0 - p);", "if (h) h[i] = p;"),
+    "histogram H ignores the hessian": ("hh[b] += h ? h[r] : 1.0;", "hh[b] += 1.0;"),
+    "node H ignores the hessian": ("HP += hv ? hv[rows[k]] : 1.0;", "HP += 1.0;"),
     "feature index transposed": ("const uint8_t* col = bins + (int64_t)j * N;\n    uint32_t* c", "const uint8_t* col = bins + (int64_t)(F - 1 - j) * N;\n    uint32_t* c"),
 }
 
@@ -59,6 +65,9 @@ PINS = [
     ("predict hand", lambda o: tp.test_hand_model(o)),
     ("budget truncation", lambda o: [tb.test_budget_tree_is_the_truncated_level_wise_tree("mid", 4000, 5, 12, o=o),
                                      tb.test_budget_tree_is_the_truncated_level_wise_tree("covtype", 6000, 6, 40, o=o)]),
+    ("logistic gradients", lambda o: tl.test_gradients_closed_form(o)),
+    ("logistic hand tree", lambda o: tl.test_hand_tree_depth_one(o)),
+    ("logistic second tree", lambda o: tl.test_second_tree_uses_new_margins(o)),
     ("predict = training",
      lambda o: tp.test_prediction_of_training_rows_equals_training_predictions("tiny", 3, 2, o=o)),
 ]
