@@ -79,7 +79,7 @@ def lib():
         i64, i32, dbl = ctypes.c_int64, ctypes.c_int32, ctypes.c_double
         L.orc_quantize.argtypes = [P, i64, i32, i32, i32, P, P, P]
         L.orc_gradients.argtypes = [P, P, i64, P, P]
-        L.orc_histograms.argtypes = [P, i64, i32, P, P, i32, P, P, P, P, P, P, P]
+        L.orc_histograms.argtypes = [P, i64, i32, P, P, P, i32, P, P, P, P, P, P, P]
         L.orc_best_split.argtypes = [P, P, P, i32, P, i64, dbl, dbl, ctypes.POINTER(Params),
                                      ctypes.POINTER(Split)]
         L.orc_train.argtypes = [P, P, i64, i32, P, ctypes.POINTER(Params), P, P, P, P, P, P, P]
@@ -151,17 +151,19 @@ def gradients(pred: np.ndarray, label: np.ndarray, objective: int = 0):
     return g, h
 
 
-def histograms(bins: np.ndarray, g: np.ndarray, slot_of_row: np.ndarray, n_slots: int):
-    """Row-order FP64 histograms of every slot.  Returns dict of arrays:
+def histograms(bins: np.ndarray, g: np.ndarray, slot_of_row: np.ndarray, n_slots: int, h: np.ndarray | None = None):
+    """Row-order FP64 histograms of every slot (h: per-row hessians, None for h = 1).  Returns dict of arrays:
     cnt (S,F,256) uint32, G/H (S,F,256) float64, n (S,) int64, Gt/Ht/At (S,) float64."""
     bins = np.ascontiguousarray(bins, dtype=np.uint8)
     F, N = bins.shape
     g = np.ascontiguousarray(g, dtype=np.float64)
+    h = None if h is None else np.ascontiguousarray(h, dtype=np.float64)
     slot = np.ascontiguousarray(slot_of_row, dtype=np.int32)
     out = dict(cnt=np.empty((n_slots, F, NBINS), np.uint32), G=np.empty((n_slots, F, NBINS), np.float64),
                H=np.empty((n_slots, F, NBINS), np.float64), n=np.empty(n_slots, np.int64),
                Gt=np.empty(n_slots, np.float64), Ht=np.empty(n_slots, np.float64), At=np.empty(n_slots, np.float64))
-    _check(lib().orc_histograms(_p(bins), N, F, _p(g), _p(slot), n_slots, _p(out["cnt"]), _p(out["G"]),
+    _check(lib().orc_histograms(_p(bins), N, F, _p(g), _p(h) if h is not None else None, _p(slot), n_slots,
+                                _p(out["cnt"]), _p(out["G"]),
                                 _p(out["H"]), _p(out["n"]), _p(out["Gt"]), _p(out["Ht"]), _p(out["At"])),
            "histograms")
     return out

@@ -266,11 +266,12 @@ static void node_histogram(const uint8_t* bins, int64_t N, int32_t F, const doub
  * [0, n_slots) selects the slot of row r (any other value: row inactive).
  * Rows are visited in ascending index order, which is the supplied order.
  * cnt/G/H are [n_slots][F][256]; n/Gt/Ht/At (optional) are per-slot row
- * counts and row-order sums of g, h and |g|.
+ * counts and row-order sums of g, h and |g|.  h: per-row hessians, or NULL
+ * for h = 1 (squared error).
  */
-int orc_histograms(const uint8_t* bins, int64_t N, int32_t F, const double* g, const int32_t* slot_of_row,
-                   int32_t n_slots, uint32_t* cnt, double* G, double* H, int64_t* n, double* Gt, double* Ht,
-                   double* At) {
+int orc_histograms(const uint8_t* bins, int64_t N, int32_t F, const double* g, const double* h,
+                   const int32_t* slot_of_row, int32_t n_slots, uint32_t* cnt, double* G, double* H, int64_t* n,
+                   double* Gt, double* Ht, double* At) {
   if (!bins || !g || !slot_of_row || !cnt || !G || !H || N < 0 || F < 1 || n_slots < 0) return ORC_EINVAL;
   const size_t per = (size_t)F * ORC_NBINS;
   memset(cnt, 0, sizeof(uint32_t) * per * (size_t)n_slots);
@@ -285,13 +286,14 @@ int orc_histograms(const uint8_t* bins, int64_t N, int32_t F, const double* g, c
     if (s < 0 || s >= n_slots) continue;
     if (n) n[s] += 1;
     if (Gt) Gt[s] += g[r];
-    if (Ht) Ht[s] += 1.0;
+    const double hr = h ? h[r] : 1.0;
+    if (Ht) Ht[s] += hr;
     if (At) At[s] += fabs(g[r]);
     for (int32_t j = 0; j < F; ++j) {
       size_t o = (size_t)s * per + (size_t)j * ORC_NBINS + bins[(int64_t)j * N + r];
       cnt[o] += 1u;
       G[o] += g[r];
-      H[o] += 1.0;
+      H[o] += hr;
     }
   }
   return ORC_OK;

@@ -68,3 +68,24 @@ def test_logistic_needs_binary_labels(o=oracle):
     with pytest.raises(o.OracleError):
         o.train(bins, n_bins, np.array([0, 0.5, 1, 1], np.float32), n_trees=1, max_depth=1, objective=1)
     assert o.validate_params(objective=2) != 0 and o.validate_params(objective=1) == 0
+
+
+def test_histograms_with_hessians_brute_force(o=oracle):
+    """H of a (slot, feature, bin) entry is the sum of h over its rows, visited one by one here."""
+    rng = np.random.default_rng(11)
+    F, N, n_slots = 3, 40, 3
+    bins = rng.integers(0, 5, size=(F, N)).astype(np.uint8)
+    g = rng.normal(size=N)
+    h = rng.uniform(0.0, 0.25, size=N)
+    slot = rng.integers(-1, n_slots, size=N).astype(np.int32)
+    out = o.histograms(bins, g, slot, n_slots, h=h)
+    for s in range(n_slots):
+        for j in range(F):
+            for b in range(5):
+                rows = [r for r in range(N) if slot[r] == s and bins[j, r] == b]
+                assert out["cnt"][s, j, b] == len(rows)
+                assert out["H"][s, j, b] == pytest.approx(sum(h[r] for r in rows), rel=1e-14, abs=1e-300)
+                assert out["G"][s, j, b] == pytest.approx(sum(g[r] for r in rows), rel=1e-14, abs=1e-15)
+        assert out["Ht"][s] == pytest.approx(sum(h[r] for r in range(N) if slot[r] == s), rel=1e-14)
+    unit = o.histograms(bins, g, slot, n_slots)
+    assert np.array_equal(unit["H"], unit["cnt"].astype(np.float64))

@@ -49,6 +49,7 @@ MUTATIONS = {
     "logistic hessian is p": ("if (h) h[i] = p * (1.0 - p);", "if (h) h[i] = p;"),
     "histogram H ignores the hessian": ("hh[b] += h ? h[r] : 1.0;", "hh[b] += 1.0;"),
     "node H ignores the hessian": ("HP += hv ? hv[rows[k]] : 1.0;", "HP += 1.0;"),
+    "level histograms ignore the hessian": ("      H[o] += hr;", "      H[o] += 1.0;"),
     "feature index transposed": ("const uint8_t* col = bins + (int64_t)j * N;\n    uint32_t* c", "const uint8_t* col = bins + (int64_t)(F - 1 - j) * N;\n    uint32_t* c"),
 }
 
@@ -68,6 +69,7 @@ PINS = [
     ("logistic gradients", lambda o: tl.test_gradients_closed_form(o)),
     ("logistic hand tree", lambda o: tl.test_hand_tree_depth_one(o)),
     ("logistic second tree", lambda o: tl.test_second_tree_uses_new_margins(o)),
+    ("logistic histograms", lambda o: tl.test_histograms_with_hessians_brute_force(o)),
     ("predict = training",
      lambda o: tp.test_prediction_of_training_rows_equals_training_predictions("tiny", 3, 2, o=o)),
 ]
