@@ -26,6 +26,7 @@ __all__ = ["lib", "GbdtError", "Params", "NODE_DTYPE", "SPLIT_DTYPE", "LEVEL_DTY
 
 OK, ERR_INVALID_ARG, ERR_NONFINITE, ERR_WORKSPACE, ERR_CUDA, ERR_INTERNAL = 0, -1, -2, -3, -4, -5
 DTYPE_F32, DTYPE_F64 = 0, 1
+OBJECTIVE_SQUARED_ERROR, OBJECTIVE_LOGISTIC = 0, 1
 LAYOUT_COLUMNS, LAYOUT_ROW_BLOCKS = 0, 1
 MAX_BINS, MAX_DEPTH = 256, 12
 
@@ -38,7 +39,8 @@ EXPORTED_SYMBOLS = [
     "gbdt_train", "gbdt_debug_inject_failure", "gbdt_kernel_launch_count", "gbdt_partition_noalloc",
     "gbdt_histograms_segmented_workspace_size", "gbdt_build_histograms_segmented", "gbdt_partition_rows_workspace_size",
     "gbdt_partition_rows", "gbdt_predict_workspace_size", "gbdt_predict", "gbdt_row_block_pitch",
-    "gbdt_row_block_bytes", "gbdt_bins_to_row_blocks",
+    "gbdt_row_block_bytes", "gbdt_bins_to_row_blocks", "gbdt_compute_gradients_objective",
+    "gbdt_subtract_histograms_h", "gbdt_build_histograms_segmented_h", "gbdt_find_splits_h",
 ]
 
 
@@ -51,7 +53,7 @@ class GbdtError(RuntimeError):
 class Params(ctypes.Structure):
     _fields_ = [("n_trees", ctypes.c_int32), ("max_depth", ctypes.c_int32), ("learning_rate", ctypes.c_double),
                 ("reg_lambda", ctypes.c_double), ("gamma", ctypes.c_double), ("min_samples_leaf", ctypes.c_int32),
-                ("min_child_weight", ctypes.c_double), ("num_leaves", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+                ("min_child_weight", ctypes.c_double), ("num_leaves", ctypes.c_int32), ("objective", ctypes.c_int32)]
 
 
 class Diagnostics(ctypes.Structure):
@@ -68,11 +70,12 @@ NODE_DTYPE = np.dtype([("feature", np.int32), ("threshold_bin", np.int32), ("lef
                        ("leaf_value", np.float64), ("gain", np.float64), ("is_leaf", np.uint8),
                        ("reserved", np.uint8, (7,))])
 SPLIT_DTYPE = np.dtype([("feature", np.int32), ("bin", np.int32), ("gain", np.float64), ("q_left", np.int64),
-                        ("q_total", np.int64), ("cnt_left", np.uint32), ("cnt_total", np.uint32)])
+                        ("q_total", np.int64), ("cnt_left", np.uint32), ("cnt_total", np.uint32),
+                        ("h_left", np.int64), ("h_total", np.int64)])
 LEVEL_DTYPE = np.dtype([("node_begin", np.int32), ("n_slots", np.int32)])
 SEGMENT_DTYPE = np.dtype([("start", np.int64), ("count", np.int64)])
 FILTER_DTYPE = np.dtype([("feature", np.int32), ("bin", np.int32), ("side", np.int32), ("reserved", np.int32)])
-assert NODE_DTYPE.itemsize == 40 and SPLIT_DTYPE.itemsize == 40
+assert NODE_DTYPE.itemsize == 40 and SPLIT_DTYPE.itemsize == 56
 
 _lib = None
 
@@ -93,12 +96,15 @@ def lib():
         "gbdt_quantize": ([P, i64, i64, i32, i32, P, i64, P, P, P, sz, P], i32),
         "gbdt_gradients_workspace_size": ([i64], sz),
         "gbdt_compute_gradients": ([P, P, i64, P, P, P, sz, P], i32),
+        "gbdt_compute_gradients_objective": ([P, P, i64, i32, P, P, P, sz, P], i32),
         "gbdt_gradient_scale": ([P, i32, i64, P, P, sz, P], i32),
         "gbdt_histograms_workspace_size": ([i64, i32, i32], sz),
         "gbdt_build_histograms": ([P, i64, i64, i32, P, i32, P, P, P, i32, P, i32, P, P, P, sz, P], i32),
         "gbdt_subtract_histograms": ([P, P, P, P, P, i32, i32, P, P, P], i32),
+        "gbdt_subtract_histograms_h": ([P, P, P, P, P, P, i32, i32, P, P, P, P], i32),
         "gbdt_find_splits_workspace_size": ([i32, i32], sz),
         "gbdt_find_splits": ([P, P, P, i32, P, P, i32, P, P, P, sz, P], i32),
+        "gbdt_find_splits_h": ([P, P, P, P, i32, P, P, i32, P, P, P, sz, P], i32),
         "gbdt_partition_workspace_size": ([i64, i32], sz),
         "gbdt_partition": ([P, i64, i64, i32, P, P, i32, P, P, P, P, P, P, P, sz, P], i32),
         "gbdt_update_predictions": ([P, P, P, i32, i64, dbl, P], i32),
@@ -110,6 +116,8 @@ def lib():
         "gbdt_histograms_segmented_workspace_size": ([i32], sz),
         "gbdt_build_histograms_segmented": ([P, i64, i32, i64, i32, P, i32, P, P, i32, P, i32, P, P, P, P, P, sz, P],
                                             i32),
+        "gbdt_build_histograms_segmented_h": ([P, i64, i32, i64, i32, P, i32, P, P, i32, P, i32, P, P, P, P, P, P, sz,
+                                               P], i32),
         "gbdt_row_block_pitch": ([i32], i64),
         "gbdt_row_block_bytes": ([i64, i32], sz),
         "gbdt_bins_to_row_blocks": ([P, i64, i64, i32, P, P], i32),
@@ -170,9 +178,9 @@ def padded_ld(n: int) -> int:
 
 
 def make_params(n_trees=1, max_depth=6, learning_rate=0.1, reg_lambda=1.0, gamma=0.0, min_samples_leaf=1,
-                min_child_weight=0.0, num_leaves=0, **_ignored) -> Params:
+                min_child_weight=0.0, num_leaves=0, objective=OBJECTIVE_SQUARED_ERROR, **_ignored) -> Params:
     return Params(int(n_trees), int(max_depth), float(learning_rate), float(reg_lambda), float(gamma),
-                  int(min_samples_leaf), float(min_child_weight), int(num_leaves), 0)
+                  int(min_samples_leaf), float(min_child_weight), int(num_leaves), int(objective))
 
 
 def version() -> str:
@@ -201,14 +209,19 @@ def quantize(X, max_bins: int, ldb: int | None = None):
     return bins, edges, n_bins
 
 
-def compute_gradients(pred, label):
+def compute_gradients(pred, label, objective=OBJECTIVE_SQUARED_ERROR):
+    """g (N,) f64 and the fixed-point exponents: S (1,) for squared error, (S, S_h) (2,) for logistic."""
     torch = _torch()
     N = pred.shape[0]
     g = torch.empty(N, dtype=torch.float64, device="cuda")
-    S = torch.empty(1, dtype=torch.int32, device="cuda")
+    S = torch.zeros(2 if objective == OBJECTIVE_LOGISTIC else 1, dtype=torch.int32, device="cuda")
     ws = _workspace(lib().gbdt_gradients_workspace_size(N))
-    _check(lib().gbdt_compute_gradients(_ptr(pred), _ptr(label), N, _ptr(g), _ptr(S), _ptr(ws), ws.numel(),
-                                        _stream()))
+    if objective == OBJECTIVE_SQUARED_ERROR:
+        _check(lib().gbdt_compute_gradients(_ptr(pred), _ptr(label), N, _ptr(g), _ptr(S), _ptr(ws), ws.numel(),
+                                            _stream()))
+    else:
+        _check(lib().gbdt_compute_gradients_objective(_ptr(pred), _ptr(label), N, int(objective), _ptr(g), _ptr(S),
+                                                      _ptr(ws), ws.numel(), _stream()))
     return g, S
 
 
@@ -251,25 +264,31 @@ def to_row_blocks(bins, N: int):
 
 
 def build_histograms_segmented(bins, N, g, fixed_exp, level, max_slots, build_flag, max_build, segments,
-                               hist_cnt=None, hist_q=None, ws=None, filters=None, row_blocks=None):
+                               hist_cnt=None, hist_q=None, ws=None, filters=None, row_blocks=None, hist_h=None,
+                               logistic=False):
     """Histograms of flagged slots whose rows are contiguous segments (SEGMENT_DTYPE bytes, device),
     optionally narrowed per slot by FILTER_DTYPE records (device bytes).  bins: column-major (F, ldb)
     CUDA uint8; with row_blocks = (buffer, pitch) from to_row_blocks the kernel reads that layout instead
-    (bins then only gives F)."""
+    (bins then only gives F).  logistic: also the H histograms of h = |g| (1 - |g|) with exponent
+    fixed_exp[1]; returns (hist_cnt, hist_q, hist_h) then, else (hist_cnt, hist_q)."""
     torch = _torch()
     F, ldb = bins.shape
     if hist_cnt is None:
         hist_cnt = torch.zeros((max_slots, F, 256), dtype=torch.int32, device="cuda")
         hist_q = torch.zeros((max_slots, F, 256), dtype=torch.int64, device="cuda")
+    if logistic and hist_h is None:
+        hist_h = torch.zeros((max_slots, F, 256), dtype=torch.int64, device="cuda")
     if ws is None:
         ws = _workspace(lib().gbdt_histograms_segmented_workspace_size(max_slots))
     dt = DTYPE_F32 if g.dtype == torch.float32 else DTYPE_F64
     src, ld, layout = (bins, ldb, LAYOUT_COLUMNS) if row_blocks is None else (row_blocks[0], row_blocks[1],
                                                                               LAYOUT_ROW_BLOCKS)
-    _check(lib().gbdt_build_histograms_segmented(_ptr(src), ld, layout, N, F, _ptr(g), dt, _ptr(fixed_exp),
-                                                 _ptr(level), max_slots, _ptr(build_flag), max_build,
-                                                 _ptr(segments), _ptr(filters) if filters is not None else None,
-                                                 _ptr(hist_cnt), _ptr(hist_q), _ptr(ws), ws.numel(), _stream()))
+    args = (_ptr(src), ld, layout, N, F, _ptr(g), dt, _ptr(fixed_exp), _ptr(level), max_slots, _ptr(build_flag),
+            max_build, _ptr(segments), _ptr(filters) if filters is not None else None, _ptr(hist_cnt), _ptr(hist_q))
+    if logistic:
+        _check(lib().gbdt_build_histograms_segmented_h(*args, _ptr(hist_h), _ptr(ws), ws.numel(), _stream()))
+        return hist_cnt, hist_q, hist_h
+    _check(lib().gbdt_build_histograms_segmented(*args, _ptr(ws), ws.numel(), _stream()))
     return hist_cnt, hist_q
 
 
@@ -293,22 +312,34 @@ def partition_rows(bins_in, N, g_in, orig_in, splits, level, max_slots, seg_in, 
     return bins_out, g_out, orig_out, seg_out, next_level
 
 
-def subtract_histograms(prev_cnt, prev_q, pair_parent, build_flag, level, max_slots, hist_cnt, hist_q):
+def subtract_histograms(prev_cnt, prev_q, pair_parent, build_flag, level, max_slots, hist_cnt, hist_q, prev_h=None,
+                        hist_h=None):
     F = hist_cnt.shape[1]
-    _check(lib().gbdt_subtract_histograms(_ptr(prev_cnt), _ptr(prev_q), _ptr(pair_parent), _ptr(build_flag),
-                                          _ptr(level), max_slots, F, _ptr(hist_cnt), _ptr(hist_q), _stream()))
-    return hist_cnt, hist_q
+    if prev_h is None and hist_h is None:
+        _check(lib().gbdt_subtract_histograms(_ptr(prev_cnt), _ptr(prev_q), _ptr(pair_parent), _ptr(build_flag),
+                                              _ptr(level), max_slots, F, _ptr(hist_cnt), _ptr(hist_q), _stream()))
+        return hist_cnt, hist_q
+    _check(lib().gbdt_subtract_histograms_h(_ptr(prev_cnt), _ptr(prev_q), _ptr(prev_h), _ptr(pair_parent),
+                                            _ptr(build_flag), _ptr(level), max_slots, F, _ptr(hist_cnt),
+                                            _ptr(hist_q), _ptr(hist_h), _stream()))
+    return hist_cnt, hist_q, hist_h
 
 
-def find_splits(hist_cnt, hist_q, fixed_exp, n_bins, level, max_slots, out=None, **params):
+def find_splits(hist_cnt, hist_q, fixed_exp, n_bins, level, max_slots, out=None, hist_h=None, **params):
+    """Best split per slot (SPLIT_DTYPE bytes, device); hist_h: H from that histogram (exponent fixed_exp[1])."""
     torch = _torch()
     F = hist_cnt.shape[1]
     p = make_params(**params)
     if out is None:
         out = torch.empty(max_slots * SPLIT_DTYPE.itemsize, dtype=torch.uint8, device="cuda")
     ws = _workspace(lib().gbdt_find_splits_workspace_size(F, max_slots))
-    _check(lib().gbdt_find_splits(_ptr(hist_cnt), _ptr(hist_q), _ptr(fixed_exp), F, _ptr(n_bins), _ptr(level),
-                                  max_slots, ctypes.byref(p), _ptr(out), _ptr(ws), ws.numel(), _stream()))
+    if hist_h is None:
+        _check(lib().gbdt_find_splits(_ptr(hist_cnt), _ptr(hist_q), _ptr(fixed_exp), F, _ptr(n_bins), _ptr(level),
+                                      max_slots, ctypes.byref(p), _ptr(out), _ptr(ws), ws.numel(), _stream()))
+    else:
+        _check(lib().gbdt_find_splits_h(_ptr(hist_cnt), _ptr(hist_q), _ptr(hist_h), _ptr(fixed_exp), F,
+                                        _ptr(n_bins), _ptr(level), max_slots, ctypes.byref(p), _ptr(out), _ptr(ws),
+                                        ws.numel(), _stream()))
     return out
 
 

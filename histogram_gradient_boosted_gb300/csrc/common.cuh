@@ -84,6 +84,18 @@ __host__ __device__ inline int fixed_exponent(double maxabs, int64_t N) {
 // round-half-even(g * 2^S) for the scale 2^S (an exact power of two).
 __device__ __forceinline__ int64_t to_fixed(double g, double scale) { return __double2ll_rn(g * scale); }
 
+// Hessian of the logistic loss from the row's gradient g = p - y (y is 0 or 1,
+// p = sigmoid(pred)): |g| is p when y = 0 and 1 - p when y = 1, so
+// p (1 - p) = |g| (1 - |g|).  For y = 0 this is the product p * (1 - p) itself;
+// for y = 1 it uses the rounded g.
+__device__ __forceinline__ double logistic_hess(double g) {
+  const double a = fabs(g);
+  return __dmul_rn(a, __dsub_rn(1.0, a));
+}
+
+// sigmoid(x) = 1 / (1 + exp(-x)) in FP64, each operation rounded once.
+__device__ __forceinline__ double sigmoid(double x) { return __ddiv_rn(1.0, __dadd_rn(1.0, exp(-x))); }
+
 // Convert a fixed-point sum back to a double: q * 2^-S.
 __host__ __device__ inline double from_fixed(int64_t q, int S) { return ldexp(static_cast<double>(q), -S); }
 

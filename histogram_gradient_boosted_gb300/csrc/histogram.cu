@@ -235,23 +235,26 @@ __global__ void __launch_bounds__(kHistThreads, 1)
 
 __global__ void hist_zero_kernel(const gbdt_level* __restrict__ level, int32_t max_slots,
                                  const uint8_t* __restrict__ build_flag, int32_t F, uint32_t* __restrict__ hist_cnt,
-                                 int64_t* __restrict__ hist_q) {
+                                 int64_t* __restrict__ hist_q, int64_t* __restrict__ hist_h) {
   const int n_slots = min(level->n_slots, max_slots);
   const int slot = blockIdx.y;
   if (slot >= n_slots || !build_flag[slot]) return;
   const int64_t per_slot = static_cast<int64_t>(F) * kBins;
   uint32_t* c = hist_cnt + slot * per_slot;
   int64_t* q = hist_q + slot * per_slot;
+  int64_t* h = hist_h ? hist_h + slot * per_slot : nullptr;
   for (int64_t e = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; e < per_slot; e += (int64_t)gridDim.x * blockDim.x) {
     c[e] = 0;
     q[e] = 0;
+    if (h) h[e] = 0;
   }
 }
 
 __global__ void hist_subtract_kernel(const uint32_t* __restrict__ prev_cnt, const int64_t* __restrict__ prev_q,
-                                     const int32_t* __restrict__ pair_parent, const uint8_t* __restrict__ build_flag,
-                                     const gbdt_level* __restrict__ level, int32_t max_slots, int32_t F,
-                                     uint32_t* __restrict__ hist_cnt, int64_t* __restrict__ hist_q,
+                                     const int64_t* __restrict__ prev_h, const int32_t* __restrict__ pair_parent,
+                                     const uint8_t* __restrict__ build_flag, const gbdt_level* __restrict__ level,
+                                     int32_t max_slots, int32_t F, uint32_t* __restrict__ hist_cnt,
+                                     int64_t* __restrict__ hist_q, int64_t* __restrict__ hist_h,
                                      int32_t* __restrict__ err) {
   const int n_slots = min(level->n_slots, max_slots);
   const int p = blockIdx.x;
@@ -268,6 +271,10 @@ __global__ void hist_subtract_kernel(const uint32_t* __restrict__ prev_cnt, cons
     hist_cnt[other * per_slot + e] = pc - bc;
     hist_q[other * per_slot + e] = static_cast<int64_t>(static_cast<uint64_t>(prev_q[parent * per_slot + e]) -
                                                         static_cast<uint64_t>(hist_q[built * per_slot + e]));
+    if (hist_h) {
+      hist_h[other * per_slot + e] = static_cast<int64_t>(static_cast<uint64_t>(prev_h[parent * per_slot + e]) -
+                                                          static_cast<uint64_t>(hist_h[built * per_slot + e]));
+    }
   }
   if (bad) raise_error(err, kErrHistTotals);
 }
@@ -306,10 +313,10 @@ HistPlan plan_histograms(int64_t N, int32_t F, int32_t max_slots, int32_t max_bu
 }
 
 void launch_hist_zero(const gbdt_level* level, int32_t max_slots, const uint8_t* build_flag, int32_t F,
-                      uint32_t* hist_cnt, int64_t* hist_q, cudaStream_t s) {
+                      uint32_t* hist_cnt, int64_t* hist_q, int64_t* hist_h, cudaStream_t s) {
   const int64_t per_slot = static_cast<int64_t>(F) * kBins;
   dim3 grid(static_cast<unsigned>((per_slot + 1023) / 1024), static_cast<unsigned>(max_slots));
-  hist_zero_kernel<<<grid, 256, 0, s>>>(level, max_slots, build_flag, F, hist_cnt, hist_q);
+  hist_zero_kernel<<<grid, 256, 0, s>>>(level, max_slots, build_flag, F, hist_cnt, hist_q, hist_h);
   count_launches();
 }
 
@@ -339,15 +346,16 @@ int launch_hist_build(const HistPlan& plan, const uint8_t* bins, int64_t ldb, in
   return GBDT_OK;
 }
 
-void launch_hist_subtract(const uint32_t* prev_cnt, const int64_t* prev_q, const int32_t* pair_parent,
-                          const uint8_t* build_flag, const gbdt_level* level, int32_t max_slots, int32_t F,
-                          uint32_t* hist_cnt, int64_t* hist_q, int32_t* err, cudaStream_t s) {
+void launch_hist_subtract(const uint32_t* prev_cnt, const int64_t* prev_q, const int64_t* prev_h,
+                          const int32_t* pair_parent, const uint8_t* build_flag, const gbdt_level* level,
+                          int32_t max_slots, int32_t F, uint32_t* hist_cnt, int64_t* hist_q, int64_t* hist_h,
+                          int32_t* err, cudaStream_t s) {
   const int pairs = max_slots / 2;
   if (pairs < 1) return;
   const int64_t per_slot = static_cast<int64_t>(F) * kBins;
   dim3 grid(static_cast<unsigned>(pairs), static_cast<unsigned>((per_slot + 1023) / 1024));
-  hist_subtract_kernel<<<grid, 256, 0, s>>>(prev_cnt, prev_q, pair_parent, build_flag, level, max_slots, F, hist_cnt,
-                                             hist_q, err);
+  hist_subtract_kernel<<<grid, 256, 0, s>>>(prev_cnt, prev_q, prev_h, pair_parent, build_flag, level, max_slots, F,
+                                             hist_cnt, hist_q, hist_h, err);
   count_launches();
 }
 
@@ -384,7 +392,7 @@ extern "C" int gbdt_build_histograms(const uint8_t* bins, int64_t ldb, int64_t N
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int32_t* err = static_cast<int32_t*>(ws);
   const HistPlan plan = plan_histograms(N, F, max_slots, max_build);
-  launch_hist_zero(level, max_slots, build_flag, F, hist_cnt, hist_q, s);
+  launch_hist_zero(level, max_slots, build_flag, F, hist_cnt, hist_q, nullptr, s);
   int rc = launch_hist_build(plan, bins, ldb, N, F, g, g_dtype, fixed_exp, node_of_row, level, max_slots,
                              build_flag, hist_cnt, hist_q, err, s);
   if (rc != GBDT_OK) return rc;
@@ -392,16 +400,26 @@ extern "C" int gbdt_build_histograms(const uint8_t* bins, int64_t ldb, int64_t N
   return GBDT_OK;
 }
 
-extern "C" int gbdt_subtract_histograms(const uint32_t* prev_cnt, const int64_t* prev_q, const int32_t* pair_parent,
-                                        const uint8_t* build_flag, const gbdt_level* level, int32_t max_slots,
-                                        int32_t F, uint32_t* hist_cnt, int64_t* hist_q, void* stream) {
+extern "C" int gbdt_subtract_histograms_h(const uint32_t* prev_cnt, const int64_t* prev_q, const int64_t* prev_h,
+                                          const int32_t* pair_parent, const uint8_t* build_flag,
+                                          const gbdt_level* level, int32_t max_slots, int32_t F, uint32_t* hist_cnt,
+                                          int64_t* hist_q, int64_t* hist_h, void* stream) {
   clear_error();
   GBDT_CHECK_ARG(prev_cnt && prev_q && pair_parent && build_flag && level && hist_cnt && hist_q,
                  "gbdt_subtract_histograms: null pointer");
+  GBDT_CHECK_ARG((prev_h == nullptr) == (hist_h == nullptr), "gbdt_subtract_histograms: prev_h and hist_h must both "
+                 "be given or both be NULL");
   GBDT_CHECK_ARG(max_slots >= 2 && max_slots <= kMaxSlots && F >= 1 && F <= 4096,
                  "gbdt_subtract_histograms: sizes out of range");
-  launch_hist_subtract(prev_cnt, prev_q, pair_parent, build_flag, level, max_slots, F, hist_cnt, hist_q, nullptr,
-                       static_cast<cudaStream_t>(stream));
+  launch_hist_subtract(prev_cnt, prev_q, prev_h, pair_parent, build_flag, level, max_slots, F, hist_cnt, hist_q,
+                       hist_h, nullptr, static_cast<cudaStream_t>(stream));
   GBDT_LAUNCH_CHECK();
   return GBDT_OK;
+}
+
+extern "C" int gbdt_subtract_histograms(const uint32_t* prev_cnt, const int64_t* prev_q, const int32_t* pair_parent,
+                                        const uint8_t* build_flag, const gbdt_level* level, int32_t max_slots,
+                                        int32_t F, uint32_t* hist_cnt, int64_t* hist_q, void* stream) {
+  return gbdt_subtract_histograms_h(prev_cnt, prev_q, nullptr, pair_parent, build_flag, level, max_slots, F, hist_cnt,
+                                    hist_q, nullptr, stream);
 }

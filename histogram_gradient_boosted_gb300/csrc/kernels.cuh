@@ -9,20 +9,24 @@ namespace gbdt {
 // Deterministic mean of labels: fixed grid, fixed reduction order.
 constexpr int kSumBlocks = 512;
 constexpr int kSumThreads = 256;
+// nonfinite: bit 1 for a NaN/Inf label; with binary, bit 2 for a label other than 0 or 1.
 void launch_label_sum(const float* label, int64_t N, double* partials /*[kSumBlocks]*/, int32_t* nonfinite,
-                      cudaStream_t s);
-void launch_label_mean(const double* partials, int64_t N, double* init /*device*/, cudaStream_t s);
-// pred = *init; g = pred - label; node = 0; maxabs = max |g| (maxabs must be reset to 0 first).
-void launch_start_tree0(const double* init, const float* label, int64_t N, double* pred, double* g, uint16_t* node,
-                        unsigned long long* maxabs, cudaStream_t s);
-// pred += lr * leaf_value(node); if next: g = pred - label, node = 0, maxabs = max|g|.
+                      bool binary, cudaStream_t s);
+// *init = mean(label), or 0 with zero (the logistic objective's initial margin).
+void launch_label_mean(const double* partials, int64_t N, double* init /*device*/, bool zero, cudaStream_t s);
+// pred = *init; g = gradient of the objective at pred; node = 0; maxabs[0] = max |g| and, for the
+// logistic objective, maxabs[1] = max h (maxabs must be reset to 0 first).
+void launch_start_tree0(const double* init, const float* label, int64_t N, int32_t objective, double* pred,
+                        double* g, uint16_t* node, unsigned long long* maxabs /*[2]*/, cudaStream_t s);
+// pred += lr * leaf_value(node); if next: g at the new pred, node = 0, maxabs as launch_start_tree0.
 void launch_finish_tree(const gbdt_node* tree_nodes, const int32_t* n_nodes, int32_t max_nodes, double lr,
-                        const float* label, int64_t N, double* pred, double* g, uint16_t* node,
+                        const float* label, int64_t N, int32_t objective, double* pred, double* g, uint16_t* node,
                         unsigned long long* maxabs, bool next, cudaStream_t s);
-void launch_gradients(const double* pred, const float* label, int64_t N, double* g, unsigned long long* maxabs,
-                      cudaStream_t s);
+void launch_gradients(const double* pred, const float* label, int64_t N, int32_t objective, double* g,
+                      unsigned long long* maxabs, cudaStream_t s);
 void launch_maxabs(const void* g, int32_t dtype, int64_t N, unsigned long long* maxabs, cudaStream_t s);
-void launch_fixed_exp(const unsigned long long* maxabs, int64_t N, int32_t* fixed_exp, cudaStream_t s);
+// fixed_exp[0] from maxabs[0]; with_h: fixed_exp[1] from maxabs[1].
+void launch_fixed_exp(const unsigned long long* maxabs, int64_t N, int32_t* fixed_exp, bool with_h, cudaStream_t s);
 
 // ---- histogram.cu ---------------------------------------------------------------------
 struct HistPlan {
@@ -34,22 +38,26 @@ struct HistPlan {
   int blocks() const { return n_sgroups * n_fgroups * n_chunks; }
 };
 HistPlan plan_histograms(int64_t N, int32_t F, int32_t max_slots, int32_t max_build);
-// Zeroes the flagged slots of hist_cnt/hist_q.
+// Zeroes the flagged slots of hist_cnt/hist_q (and hist_h when not null).
 void launch_hist_zero(const gbdt_level* level, int32_t max_slots, const uint8_t* build_flag, int32_t F,
-                      uint32_t* hist_cnt, int64_t* hist_q, cudaStream_t s);
+                      uint32_t* hist_cnt, int64_t* hist_q, int64_t* hist_h, cudaStream_t s);
 int launch_hist_build(const HistPlan& plan, const uint8_t* bins, int64_t ldb, int64_t N, int32_t F, const void* g,
                       int32_t g_dtype, const int32_t* fixed_exp, const uint16_t* node_of_row,
                       const gbdt_level* level, int32_t max_slots, const uint8_t* build_flag, uint32_t* hist_cnt,
                       int64_t* hist_q, int32_t* err, cudaStream_t s);
-void launch_hist_subtract(const uint32_t* prev_cnt, const int64_t* prev_q, const int32_t* pair_parent,
-                          const uint8_t* build_flag, const gbdt_level* level, int32_t max_slots, int32_t F,
-                          uint32_t* hist_cnt, int64_t* hist_q, int32_t* err, cudaStream_t s);
+// prev_h/hist_h: both null, or the H histograms subtracted likewise.
+void launch_hist_subtract(const uint32_t* prev_cnt, const int64_t* prev_q, const int64_t* prev_h,
+                          const int32_t* pair_parent, const uint8_t* build_flag, const gbdt_level* level,
+                          int32_t max_slots, int32_t F, uint32_t* hist_cnt, int64_t* hist_q, int64_t* hist_h,
+                          int32_t* err, cudaStream_t s);
 
 // ---- split.cu -------------------------------------------------------------------------
 size_t find_splits_scratch_bytes(int32_t F, int32_t max_slots);
-void launch_find_splits(const uint32_t* hist_cnt, const int64_t* hist_q, const int32_t* fixed_exp, int32_t F,
-                        const int32_t* n_bins, const gbdt_level* level, int32_t max_slots, const gbdt_params& p,
-                        gbdt_split* out, void* scratch, int32_t* err, cudaStream_t s);
+// hist_h: null (H = count) or the H histograms with exponent fixed_exp[1].
+void launch_find_splits(const uint32_t* hist_cnt, const int64_t* hist_q, const int64_t* hist_h,
+                        const int32_t* fixed_exp, int32_t F, const int32_t* n_bins, const gbdt_level* level,
+                        int32_t max_slots, const gbdt_params& p, gbdt_split* out, void* scratch, int32_t* err,
+                        cudaStream_t s);
 
 // ---- partition.cu ---------------------------------------------------------------------
 // Routing entry of a slot: split feature (-1: none), threshold bin, left child node id.
@@ -65,15 +73,17 @@ struct SegHistPlan {
   int n_fgroups, group_feats;
   int max_ctas;      // CTAs per feature group (one wave over the SMs)
   int64_t min_rows;  // fewest rows a CTA takes when the level is small
+  bool with_h;       // logistic: H histograms too (h = logistic_hess(g), exponent fixed_exp[1])
   size_t smem;
 };
-SegHistPlan plan_seg_histograms(int64_t N, int32_t F, int32_t max_slots, int32_t max_build);
+SegHistPlan plan_seg_histograms(int64_t N, int32_t F, int32_t max_slots, int32_t max_build, bool with_h = false);
 size_t seg_hist_scratch_bytes(int32_t max_slots);
 int launch_seg_histograms(const SegHistPlan& plan, const uint8_t* bins, int64_t ldb, int64_t N, int32_t F,
                           const void* g, int32_t g_dtype, const int32_t* fixed_exp, const gbdt_level* level,
                           int32_t max_slots, const uint8_t* build_flag, const gbdt_segment* seg,
                           const gbdt_filter* filters, void* scratch, uint32_t* hist_cnt, int64_t* hist_q,
-                          cudaStream_t s, bool row_blocks = false);  // row_blocks: ldb is the row-block pitch
+                          int64_t* hist_h, cudaStream_t s,
+                          bool row_blocks = false);  // row_blocks: ldb is the row-block pitch; hist_h: plan.with_h
 // Stable partition of the per-position data of every split slot (bins columns, g, original row
 // id) from *_in to *_out; slots without a split record leaf_of_row[orig] = their node id.
 size_t move_scratch_bytes(int64_t N, int32_t max_slots);

@@ -133,6 +133,14 @@ __device__ __forceinline__ void entry_hi(uint32_t addr, uint32_t ql, int32_t qh,
       : "memory");
 }
 
+// Low word of the H entry (logistic): add and return the old value, like entry_lo's G word.
+template <uint32_t kLo>
+__device__ __forceinline__ uint32_t atom_lo(uint32_t addr, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.shared.add.u32 %0, [%1+%3], %2;" : "=r"(old) : "r"(addr), "r"(v), "n"(kLo) : "memory");
+  return old;
+}
+
 // Byte k of w times 128 (the byte stride between bins) plus base.
 __device__ __forceinline__ uint32_t bin_addr(uint32_t w, int k, uint32_t base) {
   return base + (__byte_perm(w, 0u, 0x4440u | static_cast<uint32_t>(k)) << 7);
@@ -195,6 +203,43 @@ __device__ __forceinline__ void seg_rows_sparse(uint32_t base, const uint32_t (&
   }
 }
 
+// With H (logistic objective): one group half of up to 32 features, five words per entry (count,
+// G low and high, H low and high, one half size apart) and a staged record per row of (G low,
+// G high, H low, H high).  Full block: two rows at a time, their four returning atomics first.
+constexpr uint32_t kHLo = 3 * kHalfBytes, kHHi = 4 * kHalfBytes;
+
+__device__ __forceinline__ void seg_rows32_h(uint32_t base, const uint32_t (&w)[8], const uint4* s_q) {
+#pragma unroll
+  for (int i = 0; i < 32; i += 2) {
+    const uint4 q0 = s_q[i], q1 = s_q[i + 1];
+    const uint32_t a0 = bin_addr(w[i >> 2], i & 3, base), a1 = bin_addr(w[(i + 1) >> 2], (i + 1) & 3, base);
+    const uint32_t og0 = entry_lo<kHalfBytes>(a0, q0.x), oh0 = atom_lo<kHLo>(a0, q0.z);
+    const uint32_t og1 = entry_lo<kHalfBytes>(a1, q1.x), oh1 = atom_lo<kHLo>(a1, q1.z);
+    entry_hi<2 * kHalfBytes>(a0, q0.x, static_cast<int32_t>(q0.y), og0);
+    entry_hi<kHHi>(a0, q0.z, static_cast<int32_t>(q0.w), oh0);
+    entry_hi<2 * kHalfBytes>(a1, q1.x, static_cast<int32_t>(q1.y), og1);
+    entry_hi<kHHi>(a1, q1.z, static_cast<int32_t>(q1.w), oh1);
+  }
+}
+
+// Partial block with H: the valid rows only, as seg_rows_sparse.
+__device__ __forceinline__ void seg_rows_sparse_h(uint32_t base, const uint32_t (&w)[8], const uint4* s_q,
+                                                  uint32_t valid) {
+#pragma unroll
+  for (int wi = 0; wi < 8; ++wi) {
+    uint32_t m = (valid >> (4 * wi)) & 0xfu;  // warp-uniform
+    while (m != 0) {
+      const uint32_t k = __ffs(m) - 1;
+      m &= m - 1;
+      const uint4 q = s_q[4 * wi + k];
+      const uint32_t a = base + (__byte_perm(w[wi], 0u, 0x4440u | k) << 7);
+      const uint32_t og = entry_lo<kHalfBytes>(a, q.x), oh = atom_lo<kHLo>(a, q.z);
+      entry_hi<2 * kHalfBytes>(a, q.x, static_cast<int32_t>(q.y), og);
+      entry_hi<kHHi>(a, q.z, static_cast<int32_t>(q.w), oh);
+    }
+  }
+}
+
 // 32 bytes of a column (rows r0 .. r0 + 31 of one feature).  With kV8 the
 // column starts are 32-byte aligned and one 256-bit load reads them all.
 template <bool kV8>
@@ -216,11 +261,12 @@ __device__ __forceinline__ void load_rows32(const uint8_t* p, bool second, uint3
 // equals fside are added.
 // kRB: bins in the row-block layout (ldb is then the row-block pitch and col[h]
 // points at the feature's 32 bytes of row block 0).
-template <typename GT, int NH, bool kV8, bool kRB>
+// kH: also the logistic hessian h = |g| (1 - |g|) of each row, in fixed point with scale_h.
+template <typename GT, int NH, bool kV8, bool kRB, bool kH>
 __device__ __forceinline__ void seg_hist_rows(uint32_t base, const uint8_t* const (&col)[NH], const bool (&has)[NH],
-                                              int64_t ldb, const GT* __restrict__ g, double scale, int64_t p0,
-                                              int64_t p1, const uint8_t* __restrict__ fcol, int fbin, int fside,
-                                              uint4* s_q) {
+                                              int64_t ldb, const GT* __restrict__ g, double scale, double scale_h,
+                                              int64_t p0, int64_t p1, const uint8_t* __restrict__ fcol, int fbin,
+                                              int fside, uint4* s_q) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, n_warps = blockDim.x >> 5;
   // aligned 32-position blocks covering [p0, p1); positions outside are masked
   for (int64_t b = (p0 >> 5) + warp; (b << 5) < p1; b += n_warps) {
@@ -248,21 +294,35 @@ __device__ __forceinline__ void seg_hist_rows(uint32_t base, const uint8_t* cons
     if (valid == 0) continue;  // warp-uniform: no row of this block belongs to the slot
     const int64_t q = v ? to_fixed(gv, scale) : 0;
     __syncwarp();
-    reinterpret_cast<uint2*>(s_q)[lane] =
-        make_uint2(static_cast<uint32_t>(static_cast<uint64_t>(q)), static_cast<uint32_t>(q >> 32));
+    if constexpr (kH) {
+      const int64_t qh = v ? to_fixed(logistic_hess(gv), scale_h) : 0;
+      s_q[lane] = make_uint4(static_cast<uint32_t>(static_cast<uint64_t>(q)), static_cast<uint32_t>(q >> 32),
+                             static_cast<uint32_t>(static_cast<uint64_t>(qh)), static_cast<uint32_t>(qh >> 32));
+    } else {
+      reinterpret_cast<uint2*>(s_q)[lane] =
+          make_uint2(static_cast<uint32_t>(static_cast<uint64_t>(q)), static_cast<uint32_t>(q >> 32));
+    }
     __syncwarp();
-    if (valid == 0xffffffffu) seg_rows32<NH, true>(base, w, s_q, valid);
-    else seg_rows_sparse<NH>(base, w, s_q, valid);
+    if constexpr (kH) {
+      if (valid == 0xffffffffu) seg_rows32_h(base, w[0], s_q);
+      else seg_rows_sparse_h(base, w[0], s_q, valid);
+    } else {
+      if (valid == 0xffffffffu) seg_rows32<NH, true>(base, w, s_q, valid);
+      else seg_rows_sparse<NH>(base, w, s_q, valid);
+    }
   }
 }
 
 // Merge the CTA's shared histograms into slot's global histograms and leave
-// the shared ones zeroed for the next slot.
-template <int NH>
+// the shared ones zeroed for the next slot.  kH: the H words (s_hlo, s_hhi, the
+// two arrays after s_hi) go to hist_h.
+template <int NH, bool kH>
 __device__ __forceinline__ void seg_hist_flush(uint32_t* s_cnt, uint32_t* s_lo, int32_t* s_hi, int slot, int32_t F,
                                                int f_lo, int nf, uint32_t* __restrict__ hist_cnt,
-                                               int64_t* __restrict__ hist_q) {
+                                               int64_t* __restrict__ hist_q, int64_t* __restrict__ hist_h) {
   constexpr int entries = NH * kHalfWords;
+  uint32_t* s_hlo = reinterpret_cast<uint32_t*>(s_hi + entries);
+  int32_t* s_hhi = reinterpret_cast<int32_t*>(s_hlo + entries);
   for (int e = threadIdx.x; e < entries; e += blockDim.x) {
     const uint32_t cn = s_cnt[e];
     if (cn == 0) continue;
@@ -271,25 +331,33 @@ __device__ __forceinline__ void seg_hist_flush(uint32_t* s_cnt, uint32_t* s_lo, 
     s_cnt[e] = 0;
     s_lo[e] = 0;
     s_hi[e] = 0;
+    int64_t vh = 0;
+    if constexpr (kH) {
+      vh = static_cast<int64_t>(s_hhi[e]) * 4294967296ll + static_cast<int64_t>(s_hlo[e]);
+      s_hlo[e] = 0;
+      s_hhi[e] = 0;
+    }
     if (j >= nf) continue;  // unused entries of lanes without a feature
     const int bin = (e >> 5) & (kBins - 1);
     const int64_t o = (static_cast<int64_t>(slot) * F + f_lo + j) * kBins + bin;
     atomicAdd(hist_cnt + o, cn);
     atomicAdd(reinterpret_cast<unsigned long long*>(hist_q + o), static_cast<unsigned long long>(v));
+    if constexpr (kH) atomicAdd(reinterpret_cast<unsigned long long*>(hist_h + o), static_cast<unsigned long long>(vh));
   }
 }
 
 // One CTA per (share of the level's built rows, feature group): the built
 // slots' rows are concatenated in slot order and cut into equal shares, one
 // per CTA, so the level runs as one balanced wave.  A share that crosses
-// slot boundaries flushes its histograms at each crossing.
-template <typename GT, bool kV8, bool kRB>
+// slot boundaries flushes its histograms at each crossing.  kH (logistic):
+// also the H histograms, up to 32 features per CTA, fixed_exp[1] their exponent.
+template <typename GT, bool kV8, bool kRB, bool kH>
 __global__ void __launch_bounds__(kSegThreads, 1)
     seg_hist_kernel(const uint8_t* __restrict__ bins, int64_t ldb, int32_t F, const GT* __restrict__ g,
                     const int32_t* __restrict__ fixed_exp, const gbdt_segment* __restrict__ seg,
                     const gbdt_filter* __restrict__ filters, const int32_t* __restrict__ build_slot,
                     const int64_t* __restrict__ row_start, const SegWork* __restrict__ st, int32_t group_feats,
-                    uint32_t* __restrict__ hist_cnt, int64_t* __restrict__ hist_q) {
+                    uint32_t* __restrict__ hist_cnt, int64_t* __restrict__ hist_q, int64_t* __restrict__ hist_h) {
   extern __shared__ __align__(16) unsigned char smem[];
   const int ctas = st->ctas;
   if (static_cast<int>(blockIdx.x) >= ctas) return;
@@ -306,20 +374,20 @@ __global__ void __launch_bounds__(kSegThreads, 1)
     if (row_start[mid] <= lo) k = mid;
     else kh = mid - 1;
   }
-  const double scale = ldexp(1.0, *fixed_exp);
+  const double scale = ldexp(1.0, fixed_exp[0]);
+  const double scale_h = kH ? ldexp(1.0, fixed_exp[1]) : 0.0;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   auto run = [&](auto nh_tag) {
     constexpr int NH = decltype(nh_tag)::value;
     constexpr int entries = NH * kHalfWords;
+    constexpr int words = kH ? 5 : 3;  // shared words per entry
+    constexpr int stage = kH ? 32 : 16;  // uint4 of staged row records per warp
     uint32_t* s_cnt = reinterpret_cast<uint32_t*>(smem);
     uint32_t* s_lo = s_cnt + entries;
     int32_t* s_hi = reinterpret_cast<int32_t*>(s_lo + entries);
-    uint4* s_q = reinterpret_cast<uint4*>(s_hi + entries) + warp * 16;  // 32 rows x (low, high)
-    for (int e = threadIdx.x * 4; e < entries; e += blockDim.x * 4) {
+    uint4* s_q = reinterpret_cast<uint4*>(s_cnt + words * entries) + warp * stage;
+    for (int e = threadIdx.x * 4; e < words * entries; e += blockDim.x * 4)
       *reinterpret_cast<uint4*>(s_cnt + e) = make_uint4(0, 0, 0, 0);
-      *reinterpret_cast<uint4*>(s_lo + e) = make_uint4(0, 0, 0, 0);
-      *reinterpret_cast<uint4*>(s_hi + e) = make_uint4(0, 0, 0, 0);
-    }
     __syncthreads();
     const uint32_t base = smem_u32(s_cnt) + lane * 4;
     bool has[NH];
@@ -336,16 +404,20 @@ __global__ void __launch_bounds__(kSegThreads, 1)
       const gbdt_filter fl = filters ? filters[slot] : gbdt_filter{-1, 0, 0, 0};
       const uint8_t* fcol =
           fl.feature >= 0 ? bins + static_cast<int64_t>(fl.feature) * (kRB ? kRowBlock : ldb) : nullptr;
-      seg_hist_rows<GT, NH, kV8, kRB>(base, col, has, ldb, g, scale, p0, p0 + (r_end - r), fcol, fl.bin, fl.side,
-                                      s_q);
+      seg_hist_rows<GT, NH, kV8, kRB, kH>(base, col, has, ldb, g, scale, scale_h, p0, p0 + (r_end - r), fcol, fl.bin,
+                                          fl.side, s_q);
       __syncthreads();
-      seg_hist_flush<NH>(s_cnt, s_lo, s_hi, slot, F, f_lo, nf, hist_cnt, hist_q);
+      seg_hist_flush<NH, kH>(s_cnt, s_lo, s_hi, slot, F, f_lo, nf, hist_cnt, hist_q, hist_h);
       __syncthreads();
       r = r_end;
     }
   };
-  if (group_feats > 32) run(std::integral_constant<int, 2>{});
-  else run(std::integral_constant<int, 1>{});
+  if constexpr (kH) {
+    run(std::integral_constant<int, 1>{});
+  } else {
+    if (group_feats > 32) run(std::integral_constant<int, 2>{});
+    else run(std::integral_constant<int, 1>{});
+  }
 }
 
 // ---------------------------------------------------------------------------------------- partition
@@ -1160,15 +1232,18 @@ cudaError_t smem_attr(K kernel, size_t bytes) {
 }  // namespace
 
 // ---- plans and launchers ------------------------------------------------------------------------
-SegHistPlan plan_seg_histograms(int64_t N, int32_t F, int32_t max_slots, int32_t max_build) {
+SegHistPlan plan_seg_histograms(int64_t N, int32_t F, int32_t max_slots, int32_t max_build, bool with_h) {
   (void)N, (void)max_slots, (void)max_build;
   SegHistPlan p{};
-  p.n_fgroups = ceil_div(F, kSegMaxFeats);
+  const int max_feats = with_h ? 32 : kSegMaxFeats;  // five shared words per entry with H, three without
+  p.n_fgroups = ceil_div(F, max_feats);
   p.group_feats = ceil_div(F, p.n_fgroups);
   p.max_ctas = sm_count() / p.n_fgroups;  // one wave: a CTA per SM
   if (p.max_ctas < 1) p.max_ctas = 1;
   p.min_rows = 4096;
-  p.smem = static_cast<size_t>(ceil_div(p.group_feats, 32)) * kHalfWords * 12 + (kSegThreads / 32) * 256;
+  p.with_h = with_h;
+  const size_t words = with_h ? 5 : 3, stage = with_h ? 512 : 256;  // staged row records per warp
+  p.smem = static_cast<size_t>(ceil_div(p.group_feats, 32)) * kHalfWords * 4 * words + (kSegThreads / 32) * stage;
   return p;
 }
 
@@ -1181,13 +1256,13 @@ int launch_seg_histograms(const SegHistPlan& plan, const uint8_t* bins, int64_t 
                           const void* g, int32_t g_dtype, const int32_t* fixed_exp, const gbdt_level* level,
                           int32_t max_slots, const uint8_t* build_flag, const gbdt_segment* seg,
                           const gbdt_filter* filters, void* scratch, uint32_t* hist_cnt, int64_t* hist_q,
-                          cudaStream_t s, bool row_blocks) {
+                          int64_t* hist_h, cudaStream_t s, bool row_blocks) {
   (void)N;
   Carve c(scratch, seg_hist_scratch_bytes(max_slots));
   SegWork* st = c.take<SegWork>(1);
   int32_t* build_slot = c.take<int32_t>(max_slots + 1);
   int64_t* row_start = c.take<int64_t>(max_slots + 1);
-  launch_hist_zero(level, max_slots, build_flag, F, hist_cnt, hist_q, s);
+  launch_hist_zero(level, max_slots, build_flag, F, hist_cnt, hist_q, plan.with_h ? hist_h : nullptr, s);
   seg_work_setup_kernel<<<1, 1024, 0, s>>>(level, max_slots, build_flag, seg, plan.max_ctas, plan.min_rows,
                                            build_slot, row_start, st);
   count_launches();
@@ -1197,20 +1272,23 @@ int launch_seg_histograms(const SegHistPlan& plan, const uint8_t* bins, int64_t 
   auto launch = [&](auto kernel, const auto* gp) -> int {
     GBDT_CUDA(smem_attr(kernel, plan.smem));
     kernel<<<grid, kSegThreads, plan.smem, s>>>(bins, ldb, F, gp, fixed_exp, seg, filters, build_slot, row_start,
-                                                st, plan.group_feats, hist_cnt, hist_q);
+                                                st, plan.group_feats, hist_cnt, hist_q, hist_h);
     return GBDT_OK;
+  };
+  auto pick = [&](const auto* gp, auto h_tag) -> int {
+    using GT = std::remove_const_t<std::remove_pointer_t<decltype(gp)>>;
+    constexpr bool kH = decltype(h_tag)::value;
+    return row_blocks ? launch(seg_hist_kernel<GT, true, true, kH>, gp)
+           : v8       ? launch(seg_hist_kernel<GT, true, false, kH>, gp)
+                      : launch(seg_hist_kernel<GT, false, false, kH>, gp);
   };
   int rc;
   if (g_dtype == GBDT_DTYPE_F32) {
     const float* gp = static_cast<const float*>(g);
-    rc = row_blocks ? launch(seg_hist_kernel<float, true, true>, gp)
-         : v8       ? launch(seg_hist_kernel<float, true, false>, gp)
-                    : launch(seg_hist_kernel<float, false, false>, gp);
+    rc = plan.with_h ? pick(gp, std::true_type{}) : pick(gp, std::false_type{});
   } else {
     const double* gp = static_cast<const double*>(g);
-    rc = row_blocks ? launch(seg_hist_kernel<double, true, true>, gp)
-         : v8       ? launch(seg_hist_kernel<double, true, false>, gp)
-                    : launch(seg_hist_kernel<double, false, false>, gp);
+    rc = plan.with_h ? pick(gp, std::true_type{}) : pick(gp, std::false_type{});
   }
   if (rc != GBDT_OK) return rc;
   count_launches();
@@ -1411,42 +1489,62 @@ extern "C" int gbdt_bins_to_row_blocks(const uint8_t* bins, int64_t ldb, int64_t
   return GBDT_OK;
 }
 
-extern "C" int gbdt_build_histograms_segmented(const uint8_t* bins, int64_t ldb, int32_t layout, int64_t N, int32_t F,
-                                               const void* g, int32_t g_dtype, const int32_t* fixed_exp,
-                                               const gbdt_level* level,
-                                               int32_t max_slots, const uint8_t* build_flag, int32_t max_build,
-                                               const gbdt_segment* segments, const gbdt_filter* filters,
-                                               uint32_t* hist_cnt, int64_t* hist_q, void* ws, size_t ws_bytes,
-                                               void* stream) {
+namespace {
+int build_segmented(const char* fn, const uint8_t* bins, int64_t ldb, int32_t layout, int64_t N, int32_t F,
+                    const void* g, int32_t g_dtype, const int32_t* fixed_exp, const gbdt_level* level,
+                    int32_t max_slots, const uint8_t* build_flag, int32_t max_build, const gbdt_segment* segments,
+                    const gbdt_filter* filters, uint32_t* hist_cnt, int64_t* hist_q, int64_t* hist_h, bool with_h,
+                    void* ws, size_t ws_bytes, void* stream) {
   clear_error();
-  GBDT_CHECK_ARG(bins && g && fixed_exp && level && build_flag && segments && hist_cnt && hist_q,
-                 "gbdt_build_histograms_segmented: null pointer");
-  GBDT_CHECK_ARG(N >= 1 && N < (int64_t(1) << 31) && F >= 1 && F <= 4096,
-                 "gbdt_build_histograms_segmented: sizes out of range");
-  GBDT_CHECK_ARG(layout == GBDT_LAYOUT_COLUMNS || layout == GBDT_LAYOUT_ROW_BLOCKS,
-                 "gbdt_build_histograms_segmented: bad layout");
+  GBDT_CHECK_ARG(bins && g && fixed_exp && level && build_flag && segments && hist_cnt && hist_q && (hist_h || !with_h),
+                 "%s: null pointer", fn);
+  GBDT_CHECK_ARG(N >= 1 && N < (int64_t(1) << 31) && F >= 1 && F <= 4096, "%s: sizes out of range", fn);
+  GBDT_CHECK_ARG(layout == GBDT_LAYOUT_COLUMNS || layout == GBDT_LAYOUT_ROW_BLOCKS, "%s: bad layout", fn);
   if (layout == GBDT_LAYOUT_COLUMNS) {
     GBDT_CHECK_ARG(ldb >= N && ldb % 16 == 0 && aligned(bins, 16) && aligned(g, 16),
-                   "gbdt_build_histograms_segmented: need ldb >= N, ldb %% 16 == 0, 16-byte aligned bins and g");
+                   "%s: need ldb >= N, ldb %% 16 == 0, 16-byte aligned bins and g", fn);
   } else {
     GBDT_CHECK_ARG(ldb == rb_pitch(F) && aligned(bins, 32) && aligned(g, 16),
-                   "gbdt_build_histograms_segmented: row blocks need ldb = gbdt_row_block_pitch(F), 32-byte "
-                   "aligned bins, 16-byte aligned g");
+                   "%s: row blocks need ldb = gbdt_row_block_pitch(F), 32-byte aligned bins, 16-byte aligned g", fn);
   }
-  GBDT_CHECK_ARG(g_dtype == GBDT_DTYPE_F32 || g_dtype == GBDT_DTYPE_F64, "gbdt_build_histograms_segmented: bad dtype");
+  GBDT_CHECK_ARG(g_dtype == GBDT_DTYPE_F32 || g_dtype == GBDT_DTYPE_F64, "%s: bad dtype", fn);
   GBDT_CHECK_ARG(max_slots >= 1 && max_slots <= kMaxSlots && max_build >= 1 && max_build <= max_slots,
-                 "gbdt_build_histograms_segmented: slot bounds out of range");
+                 "%s: slot bounds out of range", fn);
   if (!ws || ws_bytes < seg_hist_scratch_bytes(max_slots) || !aligned(ws, kWsAlign)) {
-    set_error("gbdt_build_histograms_segmented: workspace needs %zu bytes", seg_hist_scratch_bytes(max_slots));
+    set_error("%s: workspace needs %zu bytes", fn, seg_hist_scratch_bytes(max_slots));
     return ws ? GBDT_ERR_WORKSPACE : GBDT_ERR_INVALID_ARG;
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const SegHistPlan plan = plan_seg_histograms(N, F, max_slots, max_build);
+  const SegHistPlan plan = plan_seg_histograms(N, F, max_slots, max_build, with_h);
   int rc = launch_seg_histograms(plan, bins, ldb, N, F, g, g_dtype, fixed_exp, level, max_slots, build_flag, segments,
-                                 filters, ws, hist_cnt, hist_q, s, layout == GBDT_LAYOUT_ROW_BLOCKS);
+                                 filters, ws, hist_cnt, hist_q, hist_h, s, layout == GBDT_LAYOUT_ROW_BLOCKS);
   if (rc != GBDT_OK) return rc;
   GBDT_LAUNCH_CHECK();
   return GBDT_OK;
+}
+}  // namespace
+
+extern "C" int gbdt_build_histograms_segmented(const uint8_t* bins, int64_t ldb, int32_t layout, int64_t N, int32_t F,
+                                               const void* g, int32_t g_dtype, const int32_t* fixed_exp,
+                                               const gbdt_level* level, int32_t max_slots, const uint8_t* build_flag,
+                                               int32_t max_build, const gbdt_segment* segments,
+                                               const gbdt_filter* filters, uint32_t* hist_cnt, int64_t* hist_q,
+                                               void* ws, size_t ws_bytes, void* stream) {
+  return build_segmented("gbdt_build_histograms_segmented", bins, ldb, layout, N, F, g, g_dtype, fixed_exp, level,
+                         max_slots, build_flag, max_build, segments, filters, hist_cnt, hist_q, nullptr, false, ws,
+                         ws_bytes, stream);
+}
+
+extern "C" int gbdt_build_histograms_segmented_h(const uint8_t* bins, int64_t ldb, int32_t layout, int64_t N,
+                                                 int32_t F, const void* g, int32_t g_dtype, const int32_t* fixed_exp,
+                                                 const gbdt_level* level, int32_t max_slots,
+                                                 const uint8_t* build_flag, int32_t max_build,
+                                                 const gbdt_segment* segments, const gbdt_filter* filters,
+                                                 uint32_t* hist_cnt, int64_t* hist_q, int64_t* hist_h, void* ws,
+                                                 size_t ws_bytes, void* stream) {
+  return build_segmented("gbdt_build_histograms_segmented_h", bins, ldb, layout, N, F, g, g_dtype, fixed_exp, level,
+                         max_slots, build_flag, max_build, segments, filters, hist_cnt, hist_q, hist_h, true, ws,
+                         ws_bytes, stream);
 }
 
 namespace {

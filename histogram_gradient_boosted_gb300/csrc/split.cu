@@ -12,6 +12,9 @@
 // contraction), reducing to the best candidate.  The
 // comparison (gain desc, feature asc, bin asc) is a total order on distinct
 // candidates, so the result does not depend on the reduction order.
+// With the logistic objective H comes from the H histograms (fixed point with
+// its own exponent) instead of the row counts; min_samples_leaf still applies
+// to the counts.
 #include "kernels.cuh"
 
 namespace gbdt {
@@ -27,6 +30,7 @@ struct Cand {
   int bin;
   uint32_t cnt_left;
   int64_t q_left;
+  int64_t qh_left;  // logistic: fixed-point H of the left side
 };
 
 // true if a is strictly preferred to b under the frozen rule
@@ -46,6 +50,7 @@ __device__ __forceinline__ Cand shfl_cand(const Cand& c, int src) {
   o.bin = __shfl_sync(0xffffffffu, c.bin, src);
   o.cnt_left = __shfl_sync(0xffffffffu, c.cnt_left, src);
   o.q_left = __shfl_sync(0xffffffffu, c.q_left, src);
+  o.qh_left = __shfl_sync(0xffffffffu, c.qh_left, src);
   return o;
 }
 
@@ -61,55 +66,80 @@ __device__ __forceinline__ double score(double G, double H, double lambda) {
   return __ddiv_rn(__dmul_rn(G, G), __dadd_rn(H, lambda));
 }
 
-// Node totals from feature 0 (every row has one bin per feature): warp-wide sums.
-__device__ __forceinline__ void node_totals(const uint32_t* __restrict__ cnt, const int64_t* __restrict__ q, int lane,
-                                            uint32_t* tc, long long* tq) {
-  const uint4* cp = reinterpret_cast<const uint4*>(cnt + lane * 8);
+__device__ __forceinline__ long long warp_sum8(const int64_t* __restrict__ q, int lane) {
   const longlong2* qp = reinterpret_cast<const longlong2*>(q + lane * 8);
-  uint4 c0 = cp[0], c1 = cp[1];
-  uint32_t c = c0.x + c0.y + c0.z + c0.w + c1.x + c1.y + c1.z + c1.w;
   long long s = 0;
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     longlong2 v = qp[i];
     s += v.x + v.y;
   }
-  for (int o = 16; o > 0; o >>= 1) {
-    c += __shfl_xor_sync(0xffffffffu, c, o);
-    s += __shfl_xor_sync(0xffffffffu, s, o);
-  }
-  *tc = c;
-  *tq = s;
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  return s;
 }
 
-// One warp per (slot, feature): best threshold of that feature.
+// Node totals from feature 0 (every row has one bin per feature): warp-wide sums.
+// h (may be null): the H histogram, summed into *th.
+__device__ __forceinline__ void node_totals(const uint32_t* __restrict__ cnt, const int64_t* __restrict__ q,
+                                            const int64_t* __restrict__ h, int lane, uint32_t* tc, long long* tq,
+                                            long long* th) {
+  const uint4* cp = reinterpret_cast<const uint4*>(cnt + lane * 8);
+  uint4 c0 = cp[0], c1 = cp[1];
+  uint32_t c = c0.x + c0.y + c0.z + c0.w + c1.x + c1.y + c1.z + c1.w;
+  for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+  *tc = c;
+  *tq = warp_sum8(q, lane);
+  *th = h ? warp_sum8(h, lane) : 0;
+}
+
+// Eight bins of one lane (bins 8 lane .. 8 lane + 7) as inclusive prefix sums
+// within the lane; returns the lane's exclusive offset over the warp and the
+// feature's total (lane 31's inclusive sum) through *total.
+template <typename T>
+__device__ __forceinline__ T lane_prefix8(T (&v)[8], int lane, T* total) {
+#pragma unroll
+  for (int i = 1; i < 8; ++i) v[i] += v[i - 1];
+  T x = v[7];
+  for (int o = 1; o < 32; o <<= 1) {
+    const T y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  *total = __shfl_sync(0xffffffffu, x, 31);
+  return x - v[7];
+}
+
+// One warp per (slot, feature): best threshold of that feature.  kH: H from
+// hist_h with exponent fixed_exp[1] (logistic), else H = the row count.
+template <bool kH>
 __global__ void __launch_bounds__(kSplitThreads)
     split_features_kernel(const uint32_t* __restrict__ hist_cnt, const int64_t* __restrict__ hist_q,
-                          const int32_t* __restrict__ fixed_exp, int32_t F, const int32_t* __restrict__ n_bins,
-                          const gbdt_level* __restrict__ level, int32_t max_slots, double lambda, double gamma,
-                          int32_t msl, double mcw, Cand* __restrict__ cand, int32_t* __restrict__ err) {
+                          const int64_t* __restrict__ hist_h, const int32_t* __restrict__ fixed_exp, int32_t F,
+                          const int32_t* __restrict__ n_bins, const gbdt_level* __restrict__ level, int32_t max_slots,
+                          double lambda, double gamma, int32_t msl, double mcw, Cand* __restrict__ cand,
+                          int32_t* __restrict__ err) {
   const int slot = blockIdx.x;
   const int n_slots = min(level->n_slots, max_slots);
   if (slot >= n_slots) return;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int f = blockIdx.y * kSplitWarps + warp;
-  const int S = *fixed_exp;
+  const int S = fixed_exp[0];
   const double inv = ldexp(1.0, -S);
+  const double inv_h = kH ? ldexp(1.0, -fixed_exp[1]) : 1.0;
   const int64_t base = static_cast<int64_t>(slot) * F * kBins;
   uint32_t tot_cnt;
-  long long tot_q;
-  node_totals(hist_cnt + base, hist_q + base, lane, &tot_cnt, &tot_q);
+  long long tot_q, tot_h;
+  node_totals(hist_cnt + base, hist_q + base, kH ? hist_h + base : nullptr, lane, &tot_cnt, &tot_q, &tot_h);
   if (f >= F) return;  // warp-uniform
   const double GP = static_cast<double>(tot_q) * inv;
-  const double HP = static_cast<double>(tot_cnt);
+  const double HP = kH ? static_cast<double>(tot_h) * inv_h : static_cast<double>(tot_cnt);
   const double sP = score(GP, HP, lambda);
 
   const int64_t off = base + static_cast<int64_t>(f) * kBins + lane * 8;
-  const uint4* cp = reinterpret_cast<const uint4*>(hist_cnt + off);
-  const longlong2* qp = reinterpret_cast<const longlong2*>(hist_q + off);
   uint32_t c[8];
-  long long q[8];
+  long long q[8], qh[8];
   {
+    const uint4* cp = reinterpret_cast<const uint4*>(hist_cnt + off);
+    const longlong2* qp = reinterpret_cast<const longlong2*>(hist_q + off);
     uint4 a = cp[0], b = cp[1];
     c[0] = a.x, c[1] = a.y, c[2] = a.z, c[3] = a.w, c[4] = b.x, c[5] = b.y, c[6] = b.z, c[7] = b.w;
 #pragma unroll
@@ -118,29 +148,23 @@ __global__ void __launch_bounds__(kSplitThreads)
       q[2 * i] = v.x;
       q[2 * i + 1] = v.y;
     }
-  }
+    if (kH) {
+      const longlong2* hp = reinterpret_cast<const longlong2*>(hist_h + off);
 #pragma unroll
-  for (int i = 1; i < 8; ++i) {
-    c[i] += c[i - 1];
-    q[i] += q[i - 1];
-  }
-  // exclusive warp scan of the lane totals
-  uint32_t ci = c[7];
-  long long qi = q[7];
-  for (int o = 1; o < 32; o <<= 1) {
-    uint32_t cv = __shfl_up_sync(0xffffffffu, ci, o);
-    long long qv = __shfl_up_sync(0xffffffffu, qi, o);
-    if (lane >= o) {
-      ci += cv;
-      qi += qv;
+      for (int i = 0; i < 4; ++i) {
+        longlong2 v = hp[i];
+        qh[2 * i] = v.x;
+        qh[2 * i + 1] = v.y;
+      }
     }
   }
-  const uint32_t ce = ci - c[7];
-  const long long qe = qi - q[7];
-  // the feature's total must equal the node total
-  const uint32_t fc = __shfl_sync(0xffffffffu, ci, 31);
-  const long long fq = __shfl_sync(0xffffffffu, qi, 31);
-  if (lane == 0 && (fc != tot_cnt || fq != tot_q)) raise_error(err, kErrHistTotals);
+  // prefix sums over the bins; the feature's totals must equal the node totals
+  uint32_t fc;
+  long long fq, fh = 0;
+  const uint32_t ce = lane_prefix8(c, lane, &fc);
+  const long long qe = lane_prefix8(q, lane, &fq);
+  const long long he = kH ? lane_prefix8(qh, lane, &fh) : 0;
+  if (lane == 0 && (fc != tot_cnt || fq != tot_q || (kH && fh != tot_h))) raise_error(err, kErrHistTotals);
 
   int nb = n_bins[f];
   nb = nb < 1 ? 1 : (nb > kBins ? kBins : nb);
@@ -153,7 +177,15 @@ __global__ void __launch_bounds__(kSplitThreads)
   // that could reach the FP64 maximum (ties included) has
   // x32 >= max x32 * (1 - 2^-16), and only those are evaluated in FP64.  The
   // chosen candidate is the one a full FP64 scan would choose.
+  // With H from the H histogram (kH) the screen uses the node-relative form
+  // (qL 2^-31)^2 / (qhL / qhP + lambda / HP), a positive multiple of the same
+  // x, whose terms stay in FP32's range however small H is (|qL| 2^-31 <= 2^31,
+  // qhL / qhP >= 2^-62); its conversions and one more division keep it within
+  // 20 * 2^-24 relative, far inside the margin.  (lambda / HP beyond FP32's
+  // range makes every term 0: every candidate is then kept.)
   const float lam = static_cast<float>(lambda);
+  const float hpf = kH ? abs_to_float(tot_h) : 1.0f;
+  const float lamn = kH ? static_cast<float>(lambda / HP) : 0.0f;
   float x32[8];
   uint32_t ok = 0;
   float xmax = -1.0f;
@@ -164,22 +196,33 @@ __global__ void __launch_bounds__(kSplitThreads)
     const int64_t qL = qe + q[i];
     const uint32_t cR = tot_cnt - cL;
     const int64_t qR = static_cast<int64_t>(static_cast<uint64_t>(tot_q) - static_cast<uint64_t>(qL));
-    const double HL = static_cast<double>(cL), HR = static_cast<double>(cR);
+    const int64_t qhL = kH ? he + qh[i] : 0;
+    const int64_t qhR = kH ? static_cast<int64_t>(static_cast<uint64_t>(tot_h) - static_cast<uint64_t>(qhL)) : 0;
+    const double HL = kH ? static_cast<double>(qhL) * inv_h : static_cast<double>(cL);
+    const double HR = kH ? static_cast<double>(qhR) * inv_h : static_cast<double>(cR);
     x32[i] = 0.0f;
     if (b > nb - 2) continue;
     if (!(static_cast<int64_t>(cL) >= msl && static_cast<int64_t>(cR) >= msl && HL >= mcw && HR >= mcw &&
           HL > 0.0 && HR > 0.0))
       continue;
-    const float gl = abs_to_float(qL), gr = abs_to_float(qR);
-    const float x = __fadd_rn(__fdividef(__fmul_rn(gl, gl), __fadd_rn(static_cast<float>(cL), lam)),
-                              __fdividef(__fmul_rn(gr, gr), __fadd_rn(static_cast<float>(cR), lam)));
+    float x;
+    if (kH) {
+      const float gl = abs_to_float(qL) * 0x1p-31f, gr = abs_to_float(qR) * 0x1p-31f;
+      const float hl = __fdividef(abs_to_float(qhL), hpf), hr = __fdividef(abs_to_float(qhR), hpf);
+      x = __fadd_rn(__fdividef(__fmul_rn(gl, gl), __fadd_rn(hl, lamn)),
+                    __fdividef(__fmul_rn(gr, gr), __fadd_rn(hr, lamn)));
+    } else {
+      const float gl = abs_to_float(qL), gr = abs_to_float(qR);
+      x = __fadd_rn(__fdividef(__fmul_rn(gl, gl), __fadd_rn(static_cast<float>(cL), lam)),
+                    __fdividef(__fmul_rn(gr, gr), __fadd_rn(static_cast<float>(cR), lam)));
+    }
     x32[i] = x;
     ok |= 1u << i;
     xmax = fmaxf(xmax, x);
   }
   for (int o = 16; o > 0; o >>= 1) xmax = fmaxf(xmax, __shfl_xor_sync(0xffffffffu, xmax, o));
   const float keep = xmax - xmax * 1.52587890625e-05f;  // xmax * (1 - 2^-16)
-  Cand lb{-INFINITY, -1, -1, 0, 0};
+  Cand lb{-INFINITY, -1, -1, 0, 0, 0};
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     if (!(ok >> i & 1u) || x32[i] < keep) continue;
@@ -188,12 +231,15 @@ __global__ void __launch_bounds__(kSplitThreads)
     const int64_t qL = qe + q[i];
     const uint32_t cR = tot_cnt - cL;
     const int64_t qR = static_cast<int64_t>(static_cast<uint64_t>(tot_q) - static_cast<uint64_t>(qL));
-    const double HL = static_cast<double>(cL), HR = static_cast<double>(cR);
+    const int64_t qhL = kH ? he + qh[i] : 0;
+    const int64_t qhR = kH ? static_cast<int64_t>(static_cast<uint64_t>(tot_h) - static_cast<uint64_t>(qhL)) : 0;
+    const double HL = kH ? static_cast<double>(qhL) * inv_h : static_cast<double>(cL);
+    const double HR = kH ? static_cast<double>(qhR) * inv_h : static_cast<double>(cR);
     const double GL = static_cast<double>(qL) * inv;
     const double GR = static_cast<double>(qR) * inv;
     const double sL = score(GL, HL, lambda), sR = score(GR, HR, lambda);
     const double gain = __dsub_rn(__dmul_rn(0.5, __dsub_rn(__dadd_rn(sL, sR), sP)), gamma);
-    if (lb.feature < 0 || gain > lb.gain) lb = Cand{gain, f, b, cL, qL};
+    if (lb.feature < 0 || gain > lb.gain) lb = Cand{gain, f, b, cL, qL, qhL};
   }
   for (int o = 16; o > 0; o >>= 1) {
     Cand other = shfl_cand(lb, lane ^ o);
@@ -204,17 +250,17 @@ __global__ void __launch_bounds__(kSplitThreads)
 
 // One CTA per slot: reduce the per-feature candidates under the frozen rule.
 __global__ void __launch_bounds__(kSplitThreads)
-    split_reduce_kernel(const uint32_t* __restrict__ hist_cnt, const int64_t* __restrict__ hist_q, int32_t F,
-                        const gbdt_level* __restrict__ level, int32_t max_slots, const Cand* __restrict__ cand,
-                        gbdt_split* __restrict__ out) {
+    split_reduce_kernel(const uint32_t* __restrict__ hist_cnt, const int64_t* __restrict__ hist_q,
+                        const int64_t* __restrict__ hist_h, int32_t F, const gbdt_level* __restrict__ level,
+                        int32_t max_slots, const Cand* __restrict__ cand, gbdt_split* __restrict__ out) {
   const int slot = blockIdx.x;
   const int n_slots = min(level->n_slots, max_slots);
   if (slot >= n_slots) return;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   __shared__ Cand s_best[kSplitWarps];
   __shared__ uint32_t s_tc;
-  __shared__ long long s_tq;
-  Cand best{-INFINITY, -1, -1, 0, 0};
+  __shared__ long long s_tq, s_th;
+  Cand best{-INFINITY, -1, -1, 0, 0, 0};
   for (int f = threadIdx.x; f < F; f += blockDim.x) {
     const Cand c = cand[static_cast<int64_t>(slot) * F + f];
     if (better(c, best)) best = c;
@@ -227,11 +273,12 @@ __global__ void __launch_bounds__(kSplitThreads)
   if (warp == 0) {
     const int64_t base = static_cast<int64_t>(slot) * F * kBins;
     uint32_t tc;
-    long long tq;
-    node_totals(hist_cnt + base, hist_q + base, lane, &tc, &tq);
+    long long tq, th;
+    node_totals(hist_cnt + base, hist_q + base, hist_h ? hist_h + base : nullptr, lane, &tc, &tq, &th);
     if (lane == 0) {
       s_tc = tc;
       s_tq = tq;
+      s_th = th;
     }
   }
   __syncthreads();
@@ -248,6 +295,8 @@ __global__ void __launch_bounds__(kSplitThreads)
     r.cnt_left = split ? b.cnt_left : 0;
     r.q_total = s_tq;
     r.cnt_total = s_tc;
+    r.h_left = split ? b.qh_left : 0;
+    r.h_total = s_th;
     out[slot] = r;
   }
 }
@@ -258,16 +307,23 @@ size_t find_splits_scratch_bytes(int32_t F, int32_t max_slots) {
   return sizeof(Cand) * static_cast<size_t>(F) * static_cast<size_t>(max_slots);
 }
 
-void launch_find_splits(const uint32_t* hist_cnt, const int64_t* hist_q, const int32_t* fixed_exp, int32_t F,
-                        const int32_t* n_bins, const gbdt_level* level, int32_t max_slots, const gbdt_params& p,
-                        gbdt_split* out, void* scratch, int32_t* err, cudaStream_t s) {
+void launch_find_splits(const uint32_t* hist_cnt, const int64_t* hist_q, const int64_t* hist_h,
+                        const int32_t* fixed_exp, int32_t F, const int32_t* n_bins, const gbdt_level* level,
+                        int32_t max_slots, const gbdt_params& p, gbdt_split* out, void* scratch, int32_t* err,
+                        cudaStream_t s) {
   Cand* cand = static_cast<Cand*>(scratch);
   dim3 grid(static_cast<unsigned>(max_slots), static_cast<unsigned>((F + kSplitWarps - 1) / kSplitWarps));
-  split_features_kernel<<<grid, kSplitThreads, 0, s>>>(hist_cnt, hist_q, fixed_exp, F, n_bins, level, max_slots,
-                                                        p.reg_lambda, p.gamma, p.min_samples_leaf,
-                                                        p.min_child_weight, cand, err);
+  if (hist_h) {
+    split_features_kernel<true><<<grid, kSplitThreads, 0, s>>>(hist_cnt, hist_q, hist_h, fixed_exp, F, n_bins, level,
+                                                               max_slots, p.reg_lambda, p.gamma, p.min_samples_leaf,
+                                                               p.min_child_weight, cand, err);
+  } else {
+    split_features_kernel<false><<<grid, kSplitThreads, 0, s>>>(hist_cnt, hist_q, nullptr, fixed_exp, F, n_bins,
+                                                                level, max_slots, p.reg_lambda, p.gamma,
+                                                                p.min_samples_leaf, p.min_child_weight, cand, err);
+  }
   count_launches();
-  split_reduce_kernel<<<max_slots, kSplitThreads, 0, s>>>(hist_cnt, hist_q, F, level, max_slots, cand, out);
+  split_reduce_kernel<<<max_slots, kSplitThreads, 0, s>>>(hist_cnt, hist_q, hist_h, F, level, max_slots, cand, out);
   count_launches();
 }
 
@@ -281,22 +337,31 @@ extern "C" size_t gbdt_find_splits_workspace_size(int32_t F, int32_t max_slots) 
   return find_splits_scratch_bytes(F, max_slots) + kWsAlign;
 }
 
-extern "C" int gbdt_find_splits(const uint32_t* hist_cnt, const int64_t* hist_q, const int32_t* fixed_exp, int32_t F,
-                                const int32_t* n_bins, const gbdt_level* level, int32_t max_slots,
-                                const gbdt_params* p, gbdt_split* out, void* ws, size_t ws_bytes, void* stream) {
+extern "C" int gbdt_find_splits_h(const uint32_t* hist_cnt, const int64_t* hist_q, const int64_t* hist_h,
+                                  const int32_t* fixed_exp, int32_t F, const int32_t* n_bins, const gbdt_level* level,
+                                  int32_t max_slots, const gbdt_params* p, gbdt_split* out, void* ws,
+                                  size_t ws_bytes, void* stream) {
   clear_error();
   GBDT_CHECK_ARG(hist_cnt && hist_q && fixed_exp && n_bins && level && p && out, "gbdt_find_splits: null pointer");
   GBDT_CHECK_ARG(F >= 1 && F <= 4096 && max_slots >= 1 && max_slots <= kMaxSlots,
                  "gbdt_find_splits: sizes out of range");
-  GBDT_CHECK_ARG(aligned(hist_cnt, 16) && aligned(hist_q, 16), "gbdt_find_splits: histograms must be 16-byte aligned");
+  GBDT_CHECK_ARG(aligned(hist_cnt, 16) && aligned(hist_q, 16) && aligned(hist_h, 16),
+                 "gbdt_find_splits: histograms must be 16-byte aligned");
   int rc = validate_params(p);
   if (rc != GBDT_OK) return rc;
   if (!ws || ws_bytes < gbdt_find_splits_workspace_size(F, max_slots) || !aligned(ws, kWsAlign)) {
     set_error("gbdt_find_splits: workspace needs %zu bytes", gbdt_find_splits_workspace_size(F, max_slots));
     return ws ? GBDT_ERR_WORKSPACE : GBDT_ERR_INVALID_ARG;
   }
-  launch_find_splits(hist_cnt, hist_q, fixed_exp, F, n_bins, level, max_slots, *p, out, ws, nullptr,
+  launch_find_splits(hist_cnt, hist_q, hist_h, fixed_exp, F, n_bins, level, max_slots, *p, out, ws, nullptr,
                      static_cast<cudaStream_t>(stream));
   GBDT_LAUNCH_CHECK();
   return GBDT_OK;
+}
+
+extern "C" int gbdt_find_splits(const uint32_t* hist_cnt, const int64_t* hist_q, const int32_t* fixed_exp, int32_t F,
+                                const int32_t* n_bins, const gbdt_level* level, int32_t max_slots,
+                                const gbdt_params* p, gbdt_split* out, void* ws, size_t ws_bytes, void* stream) {
+  return gbdt_find_splits_h(hist_cnt, hist_q, nullptr, fixed_exp, F, n_bins, level, max_slots, p, out, ws, ws_bytes,
+                            stream);
 }

@@ -21,6 +21,7 @@ namespace {
 
 struct SlotTotals {
   int64_t q;
+  int64_t qh;  // logistic: fixed-point H (exponent fixed_exp[1]); else 0
   uint32_t cnt;
   uint32_t pad;
 };
@@ -53,16 +54,25 @@ __global__ void iota_kernel(uint32_t* __restrict__ v, int64_t N) {
 }
 
 // Root totals when the root is also the last level (max_depth 0): count and
-// fixed-point sum of g over all rows; integer adds, so the order is irrelevant.
+// fixed-point sum of g (and, logistic, of h) over all rows; integer adds, so
+// the order is irrelevant.
 __global__ void root_totals_kernel(const double* __restrict__ g, int64_t N, const int32_t* __restrict__ fixed_exp,
-                                   SlotTotals* __restrict__ tot) {
-  const double scale = ldexp(1.0, *fixed_exp);
-  long long acc = 0;
-  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < N; i += (int64_t)gridDim.x * blockDim.x)
+                                   int logistic, SlotTotals* __restrict__ tot) {
+  const double scale = ldexp(1.0, fixed_exp[0]);
+  const double scale_h = logistic ? ldexp(1.0, fixed_exp[1]) : 0.0;
+  long long acc = 0, acc_h = 0;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < N; i += (int64_t)gridDim.x * blockDim.x) {
     acc += to_fixed(g[i], scale);
-  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (logistic) acc_h += to_fixed(logistic_hess(g[i]), scale_h);
+  }
+  for (int o = 16; o > 0; o >>= 1) {
+    acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    acc_h += __shfl_xor_sync(0xffffffffu, acc_h, o);
+  }
   if ((threadIdx.x & 31) == 0 && acc != 0)
     atomicAdd(reinterpret_cast<unsigned long long*>(&tot->q), static_cast<unsigned long long>(acc));
+  if ((threadIdx.x & 31) == 0 && acc_h != 0)
+    atomicAdd(reinterpret_cast<unsigned long long*>(&tot->qh), static_cast<unsigned long long>(acc_h));
   if (blockIdx.x == 0 && threadIdx.x == 0) tot->cnt = static_cast<uint32_t>(N);
 }
 
@@ -77,7 +87,7 @@ __global__ void __launch_bounds__(1024)
                        SlotTotals* __restrict__ next_totals, gbdt_segment* __restrict__ next_seg,
                        int32_t* __restrict__ pair_parent, uint8_t* __restrict__ next_build, Route* __restrict__ route,
                        LevelStats* __restrict__ stats, int32_t num_leaves, int32_t* __restrict__ budget,
-                       int32_t* __restrict__ err) {
+                       int logistic, int32_t* __restrict__ err) {
   __shared__ int s_a[1024];
   __shared__ double s_gain[kMaxSlots];                  // leaf budget: the level's candidate gains
   __shared__ uint32_t s_cand[kMaxSlots / 32], s_keep[kMaxSlots / 32];
@@ -98,7 +108,8 @@ __global__ void __launch_bounds__(1024)
     n_slots = max_slots;
   }
   const int next_begin = node_begin + n_slots;
-  const int S = *fixed_exp;
+  const int S = fixed_exp[0];
+  const int S_h = logistic ? fixed_exp[1] : 0;
   // After the leaf budget has bound, the level below it is the last: every node is a leaf.
   const bool stopped = budget[1] != 0;
   const bool leaf_level = d >= D || stopped;
@@ -145,8 +156,10 @@ __global__ void __launch_bounds__(1024)
       if (d < D) {
         sp = splits[s];
         is_split = !stopped && sp.feature >= 0 && (!bind || (s_keep[s >> 5] >> (s & 31) & 1u));
-        if (d > 0 && (sp.q_total != totals[s].q || sp.cnt_total != totals[s].cnt)) raise_error(err, kErrHistTotals);
+        if (d > 0 && (sp.q_total != totals[s].q || sp.cnt_total != totals[s].cnt || sp.h_total != totals[s].qh))
+          raise_error(err, kErrHistTotals);
         tot.q = sp.q_total;
+        tot.qh = sp.h_total;
         tot.cnt = sp.cnt_total;
       } else {
         tot = totals[s];
@@ -173,7 +186,7 @@ __global__ void __launch_bounds__(1024)
     if (in) {
       const int k = s_pre + s_a[threadIdx.x] - is_split;
       const double G = from_fixed(tot.q, S);
-      const double H = static_cast<double>(tot.cnt);
+      const double H = logistic ? from_fixed(tot.qh, S_h) : static_cast<double>(tot.cnt);
       gbdt_node nd;
       nd.leaf_value = __ddiv_rn(-G, __dadd_rn(H, lambda));
       nd.reserved[0] = nd.reserved[1] = nd.reserved[2] = nd.reserved[3] = 0;
@@ -187,9 +200,10 @@ __global__ void __launch_bounds__(1024)
         nd.gain = sp.gain;
         nd.is_leaf = 0;
         const uint32_t cl = sp.cnt_left, cr = sp.cnt_total - sp.cnt_left;
-        next_totals[2 * k] = SlotTotals{sp.q_left, cl, 0};
+        next_totals[2 * k] = SlotTotals{sp.q_left, sp.h_left, cl, 0};
         next_totals[2 * k + 1] = SlotTotals{
-            static_cast<int64_t>(static_cast<uint64_t>(sp.q_total) - static_cast<uint64_t>(sp.q_left)), cr, 0};
+            static_cast<int64_t>(static_cast<uint64_t>(sp.q_total) - static_cast<uint64_t>(sp.q_left)),
+            static_cast<int64_t>(static_cast<uint64_t>(sp.h_total) - static_cast<uint64_t>(sp.h_left)), cr, 0};
         next_seg[2 * k] = gbdt_segment{seg[s].start, static_cast<int64_t>(cl)};
         next_seg[2 * k + 1] = gbdt_segment{seg[s].start + cl, static_cast<int64_t>(cr)};
         pair_parent[k] = s;
@@ -239,6 +253,7 @@ struct TrainWs {
   void* move_scratch;
   uint32_t* hist_cnt[2];
   int64_t* hist_q[2];
+  int64_t* hist_h[2];  // logistic only (else null)
   gbdt_split* splits;
   void* split_scratch;
   SlotTotals* totals[2];
@@ -251,7 +266,7 @@ struct TrainWs {
   LevelStats* stats;
   unsigned long long* maxabs;
   int32_t* budget;  // leaf budget state of the current tree
-  int32_t* fixed_exp;
+  int32_t* fixed_exp;  // [2]: S of g, S_h of the logistic hessians
   double* init;
   double* label_partials;
   int32_t* err;
@@ -286,9 +301,11 @@ TrainWs carve_train(void* ws, size_t bytes, int64_t N, int32_t F, int64_t ldb, c
   w.filters = c.take<gbdt_filter>(level_slots);
   w.seg_scratch = c.take<unsigned char>(seg_hist_scratch_bytes(static_cast<int32_t>(hist_slots)));
   w.move_scratch = c.take<unsigned char>(move_scratch_bytes(N, level_slots));
+  const bool logistic = p.objective == GBDT_OBJECTIVE_LOGISTIC;
   for (int i = 0; i < 2; ++i) {
     w.hist_cnt[i] = c.take<uint32_t>(hist_entries);
     w.hist_q[i] = c.take<int64_t>(hist_entries);
+    w.hist_h[i] = logistic ? c.take<int64_t>(hist_entries) : nullptr;
   }
   w.splits = c.take<gbdt_split>(level_slots);
   w.split_scratch = c.take<unsigned char>(find_splits_scratch_bytes(F, static_cast<int32_t>(hist_slots)));
@@ -304,9 +321,9 @@ TrainWs carve_train(void* ws, size_t bytes, int64_t N, int32_t F, int64_t ldb, c
   w.trees = c.take<gbdt_node>(static_cast<size_t>(T) * max_nodes_of(D));
   w.n_nodes = c.take<int32_t>(T);
   w.stats = c.take<LevelStats>(static_cast<size_t>(T) * (D + 1));
-  w.maxabs = c.take<unsigned long long>(1);
+  w.maxabs = c.take<unsigned long long>(2);
   w.budget = c.take<int32_t>(2);
-  w.fixed_exp = c.take<int32_t>(1);
+  w.fixed_exp = c.take<int32_t>(2);
   w.init = c.take<double>(1);
   w.label_partials = c.take<double>(kSumBlocks);
   w.err = c.take<int32_t>(1);
@@ -372,21 +389,26 @@ extern "C" int gbdt_train(const uint8_t* bins, int64_t ldb, const int32_t* n_bin
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int D = p->max_depth, T = p->n_trees, M = max_nodes_of(D);
+  const bool logistic = p->objective == GBDT_OBJECTIVE_LOGISTIC;
 
   // ---- input checks (one synchronisation) ----
   std::vector<int32_t> hb(F);
   GBDT_CUDA(cudaMemcpyAsync(hb.data(), n_bins, sizeof(int32_t) * F, cudaMemcpyDeviceToHost, s));
   GBDT_CUDA(cudaMemsetAsync(w.err, 0, sizeof(int32_t), s));
   GBDT_CUDA(cudaMemsetAsync(w.nonfinite, 0, sizeof(int32_t), s));
-  launch_label_sum(label, N, w.label_partials, w.nonfinite, s);
+  launch_label_sum(label, N, w.label_partials, w.nonfinite, logistic, s);
   int32_t nonfinite = 0;
   GBDT_CUDA(cudaMemcpyAsync(&nonfinite, w.nonfinite, sizeof(int32_t), cudaMemcpyDeviceToHost, s));
   GBDT_CUDA(cudaStreamSynchronize(s));
   for (int j = 0; j < F; ++j)
     GBDT_CHECK_ARG(hb[j] >= 1 && hb[j] <= GBDT_MAX_BINS, "gbdt_train: n_bins[%d] = %d outside 1..256", j, hb[j]);
-  if (nonfinite) {
+  if (nonfinite & 1) {
     set_error("gbdt_train: labels contain NaN or Inf");
     return GBDT_ERR_NONFINITE;
+  }
+  if (nonfinite & 2) {
+    set_error("gbdt_train: the logistic objective needs labels 0 or 1");
+    return GBDT_ERR_INVALID_ARG;
   }
 
   EventPool& pool = event_pool();
@@ -397,7 +419,7 @@ extern "C" int gbdt_train(const uint8_t* bins, int64_t ldb, const int32_t* n_bin
   const int64_t launches0 = launch_count();
   if (timing) GBDT_CUDA(cudaEventRecord(pool.ev[0], s));
 
-  launch_label_mean(w.label_partials, N, w.init, s);
+  launch_label_mean(w.label_partials, N, w.init, logistic, s);
   iota_kernel<<<sm_count() * 4, 256, 0, s>>>(w.orig0, N);
   count_launches();
   // the training levels read the bins in the row-block layout; the pair moves read them through
@@ -417,15 +439,15 @@ extern "C" int gbdt_train(const uint8_t* bins, int64_t ldb, const int32_t* n_bin
   for (int t = 0; t < T; ++t) {
     gbdt_node* tree = w.trees + static_cast<size_t>(t) * M;
     if (t == 0) {
-      GBDT_CUDA(cudaMemsetAsync(w.maxabs, 0, sizeof(unsigned long long), s));
-      launch_start_tree0(w.init, label, N, pred_out, w.g0, w.leaf, w.maxabs, s);
+      GBDT_CUDA(cudaMemsetAsync(w.maxabs, 0, 2 * sizeof(unsigned long long), s));
+      launch_start_tree0(w.init, label, N, p->objective, pred_out, w.g0, w.leaf, w.maxabs, s);
     }
-    launch_fixed_exp(w.maxabs, N, w.fixed_exp, s);
+    launch_fixed_exp(w.maxabs, N, w.fixed_exp, logistic, s);
     reset_root_kernel<<<1, 1, 0, s>>>(w.level[0], w.build[0], w.seg[0], N, w.budget);
     count_launches();
     if (D == 0) {
       GBDT_CUDA(cudaMemsetAsync(w.totals[0], 0, sizeof(SlotTotals), s));
-      root_totals_kernel<<<sm_count() * 4, 256, 0, s>>>(w.g0, N, w.fixed_exp, w.totals[0]);
+      root_totals_kernel<<<sm_count() * 4, 256, 0, s>>>(w.g0, N, w.fixed_exp, logistic ? 1 : 0, w.totals[0]);
       count_launches();
     }
     for (int d = 0; d <= D; ++d) {
@@ -443,7 +465,7 @@ extern "C" int gbdt_train(const uint8_t* bins, int64_t ldb, const int32_t* n_bin
       const uint32_t* lo = ph < 0 ? w.orig0 : w.orig_xy[ph];
       if (d < D) {
         const int max_build = d == 0 ? 1 : max_slots / 2;
-        const SegHistPlan plan = plan_seg_histograms(N, F, max_slots, max_build);
+        const SegHistPlan plan = plan_seg_histograms(N, F, max_slots, max_build, logistic);
         if (timing) GBDT_CUDA(cudaEventRecord(ev_hist(t, d, 0), s));
         const gbdt_segment* hseg = w.seg[cur];
         const gbdt_filter* hfil = nullptr;
@@ -454,22 +476,22 @@ extern "C" int gbdt_train(const uint8_t* bins, int64_t ldb, const int32_t* n_bin
           hfil = w.filters;
         }
         rc = launch_seg_histograms(plan, lb, pitch, N, F, lg, GBDT_DTYPE_F64, w.fixed_exp, w.level[cur], max_slots,
-                                   w.build[cur], hseg, hfil, w.seg_scratch, w.hist_cnt[cur], w.hist_q[cur], s,
-                                   true);
+                                   w.build[cur], hseg, hfil, w.seg_scratch, w.hist_cnt[cur], w.hist_q[cur],
+                                   w.hist_h[cur], s, true);
         if (rc != GBDT_OK) return rc;
         if (timing) GBDT_CUDA(cudaEventRecord(ev_hist(t, d, 1), s));
         if (d > 0) {
-          launch_hist_subtract(w.hist_cnt[nxt], w.hist_q[nxt], w.pair_parent[cur], w.build[cur], w.level[cur],
-                               max_slots, F, w.hist_cnt[cur], w.hist_q[cur], w.err, s);
+          launch_hist_subtract(w.hist_cnt[nxt], w.hist_q[nxt], w.hist_h[nxt], w.pair_parent[cur], w.build[cur],
+                               w.level[cur], max_slots, F, w.hist_cnt[cur], w.hist_q[cur], w.hist_h[cur], w.err, s);
         }
-        launch_find_splits(w.hist_cnt[cur], w.hist_q[cur], w.fixed_exp, F, n_bins, w.level[cur], max_slots, *p,
-                           w.splits, w.split_scratch, w.err, s);
+        launch_find_splits(w.hist_cnt[cur], w.hist_q[cur], w.hist_h[cur], w.fixed_exp, F, n_bins, w.level[cur],
+                           max_slots, *p, w.splits, w.split_scratch, w.err, s);
       }
       apply_level_kernel<<<1, 1024, 0, s>>>(d, D, w.level[cur], max_slots, d < D ? w.splits : nullptr, w.totals[cur],
                                             w.build[cur], w.fixed_exp, p->reg_lambda, w.seg[cur], tree,
                                             w.n_nodes + t, w.level[nxt], w.totals[nxt], w.seg[nxt],
                                             w.pair_parent[nxt], w.build[nxt], w.route[cur], st, p->num_leaves,
-                                            w.budget, w.err);
+                                            w.budget, logistic ? 1 : 0, w.err);
       count_launches();
       // rows: after an odd level they move into the next order (four grandchild runs per pair); at
       // even levels nothing moves and the rows of nodes that do not split record their leaf; at the
@@ -502,15 +524,15 @@ extern "C" int gbdt_train(const uint8_t* bins, int64_t ldb, const int32_t* n_bin
       }
     }
     const bool next = t + 1 < T;
-    if (next) GBDT_CUDA(cudaMemsetAsync(w.maxabs, 0, sizeof(unsigned long long), s));
-    launch_finish_tree(tree, w.n_nodes + t, M, p->learning_rate, label, N, pred_out, w.g0, w.leaf, w.maxabs, next,
-                       s);
+    if (next) GBDT_CUDA(cudaMemsetAsync(w.maxabs, 0, 2 * sizeof(unsigned long long), s));
+    launch_finish_tree(tree, w.n_nodes + t, M, p->learning_rate, label, N, p->objective, pred_out, w.g0, w.leaf,
+                       w.maxabs, next, s);
     GBDT_LAUNCH_CHECK();
   }
   if (T == 0) {
     // no tree: predictions are the initial value
-    GBDT_CUDA(cudaMemsetAsync(w.maxabs, 0, sizeof(unsigned long long), s));
-    launch_start_tree0(w.init, label, N, pred_out, w.g0, w.leaf, w.maxabs, s);
+    GBDT_CUDA(cudaMemsetAsync(w.maxabs, 0, 2 * sizeof(unsigned long long), s));
+    launch_start_tree0(w.init, label, N, p->objective, pred_out, w.g0, w.leaf, w.maxabs, s);
   }
   if (timing) GBDT_CUDA(cudaEventRecord(pool.ev[1], s));
 
@@ -573,7 +595,7 @@ extern "C" int gbdt_train(const uint8_t* bins, int64_t ldb, const int32_t* n_bin
           dg.hist_launches += 1;
           dg.hist_rows += ls.n_built_rows;
           dg.hist_bytes += static_cast<double>(ls.n_scan_rows) * (row_bytes + (odd ? 1.0 : 0.0)) +
-                           static_cast<double>(ls.n_built) * F * kBins * 12.0;
+                           static_cast<double>(ls.n_built) * F * kBins * (logistic ? 20.0 : 12.0);
         }
         GBDT_CUDA(cudaEventElapsedTime(&ms, ev_hist(t, d, 2), ev_hist(t, d, 3)));
         dg.part_ms += ms;

@@ -2,7 +2,8 @@
  * gbdt.h -- C ABI of the GB300 (sm_103a) level-wise histogram GBDT library.
  *
  * The library trains gradient-boosted decision trees with the squared-error
- * objective, growing each tree level by level over uint8-binned features.
+ * objective (or, as an option, the logistic one), growing each tree level by
+ * level over uint8-binned features.
  * Its entry points follow the ComputeBackend contract of "Module Design:
  * Training Core" (MPSBoost spec), s.4 Backend Interface: the caller passes
  * plain views and preallocated outputs, the core decides when to call, the
@@ -29,12 +30,15 @@
  *   - Gradients are accumulated in histograms as exact 64-bit fixed point:
  *     q = round-half-even(g * 2^S) with one exponent S per call sequence
  *     (gbdt_gradient_scale), so histogram sums are independent of thread
- *     order and sibling subtraction is exact.  H is the row count (h = 1 for
- *     squared error), so no H array is stored.
+ *     order and sibling subtraction is exact.  For squared error H is the row
+ *     count (h = 1), so no H array is stored.  For the logistic objective H
+ *     has its own fixed-point histogram hist_h with a second exponent S_h
+ *     (fixed_exp then points at two int32: S, S_h).
  *
  * Histogram layout: hist_cnt[slot][feature][256] (uint32) and
  * hist_q[slot][feature][256] (int64, fixed point with exponent S); G of an
- * entry is hist_q * 2^-S.
+ * entry is hist_q * 2^-S; with the logistic objective also
+ * hist_h[slot][feature][256] (int64), H = hist_h * 2^-S_h.
  */
 #ifndef GBDT_H_
 #define GBDT_H_
@@ -59,6 +63,15 @@ extern "C" {
 #define GBDT_DTYPE_F32 0
 #define GBDT_DTYPE_F64 1
 
+/* Objectives.  Squared error ("Module Design: Training Core" s.2): g = pred -
+ * label, h = 1, initial prediction mean(label).  Logistic ("Gradient boosted
+ * trees (spec model)", binary cross-entropy of sigmoid(pred) against a 0/1
+ * target): g = sigmoid(pred) - label, h = p (1 - p) with p = sigmoid(pred),
+ * labels must be 0 or 1, initial prediction (margin) 0.  Predictions are
+ * margins for both. */
+#define GBDT_OBJECTIVE_SQUARED_ERROR 0
+#define GBDT_OBJECTIVE_LOGISTIC 1
+
 /* Training parameters; rules of "Module Design: Training Core" s.3:
  * min_samples_leaf >= 1, min_child_weight >= 0, reg_lambda >= 0, gamma >= 0,
  * every floating parameter finite; here also 0 <= max_depth <= GBDT_MAX_DEPTH
@@ -76,7 +89,7 @@ typedef struct gbdt_params {
                                K = num_leaves - (leaves so far + the level's nodes) candidates by (gain desc,
                                node index asc) split and their children are leaves (the ExaBoost page's
                                depth-capped final partial level).  1 is invalid. */
-  int32_t reserved;         /* 0 */
+  int32_t objective;        /* GBDT_OBJECTIVE_SQUARED_ERROR (0) or GBDT_OBJECTIVE_LOGISTIC (1) */
 } gbdt_params; /* 56 bytes */
 
 /* One tree node, "Module Design: Training Core" s.3 Tree Model: feature,
@@ -110,9 +123,11 @@ typedef struct gbdt_split {
   double gain;        /* gain of the chosen candidate */
   int64_t q_left;     /* fixed-point G of the left child */
   int64_t q_total;    /* fixed-point G of the node */
-  uint32_t cnt_left;  /* rows (= H) of the left child */
-  uint32_t cnt_total; /* rows (= H) of the node */
-} gbdt_split; /* 40 bytes */
+  uint32_t cnt_left;  /* rows (= H for squared error) of the left child */
+  uint32_t cnt_total; /* rows (= H for squared error) of the node */
+  int64_t h_left;     /* logistic: fixed-point H (exponent S_h) of the left child; else 0 */
+  int64_t h_total;    /* logistic: fixed-point H of the node; else 0 */
+} gbdt_split; /* 56 bytes */
 
 /* A contiguous run of the row-index array that holds one node's rows. */
 typedef struct gbdt_segment {
@@ -195,6 +210,17 @@ size_t gbdt_gradients_workspace_size(int64_t N);
 int gbdt_compute_gradients(const double* pred, const float* label, int64_t N, double* g, int32_t* fixed_exp,
                            void* ws, size_t ws_bytes, void* stream);
 
+/* gbdt_compute_gradients_objective: g of either objective (GBDT_OBJECTIVE_*).
+ * Squared error is gbdt_compute_gradients.  Logistic ("Gradient boosted trees
+ * (spec model)", BCE with a sigmoid): g_i = sigmoid(pred_i) - label_i, with
+ * sigmoid(x) = 1 / (1 + exp(-x)) in FP64; fixed_exp (device) receives two
+ * int32: S of the g and S_h of the hessians h_i = |g_i| (1 - |g_i|), which for
+ * a 0/1 label equal p (1 - p) (p = g for label 0, 1 + g for label 1), so h
+ * needs no array of its own.  Labels are not checked here (gbdt_train checks
+ * that they are 0 or 1).  Workspace: gbdt_gradients_workspace_size. */
+int gbdt_compute_gradients_objective(const double* pred, const float* label, int64_t N, int32_t objective,
+                                     double* g, int32_t* fixed_exp, void* ws, size_t ws_bytes, void* stream);
+
 /* gbdt_gradient_scale: exponent S for gradients g [N] (g_dtype F32 or F64):
  * S = 62 - ceil(log2 N) - E where max|g| < 2^E (S = 0 if all g are 0), so the
  * sum of |round(g*2^S)| over any set of rows is below 2^62. */
@@ -228,6 +254,12 @@ int gbdt_build_histograms(const uint8_t* bins, int64_t ldb, int64_t N, int32_t F
 int gbdt_subtract_histograms(const uint32_t* prev_cnt, const int64_t* prev_q, const int32_t* pair_parent,
                              const uint8_t* build_flag, const gbdt_level* level, int32_t max_slots, int32_t F,
                              uint32_t* hist_cnt, int64_t* hist_q, void* stream);
+/* The same with H histograms (logistic): prev_h and hist_h, both non-NULL,
+ * are subtracted like prev_q and hist_q. */
+int gbdt_subtract_histograms_h(const uint32_t* prev_cnt, const int64_t* prev_q, const int64_t* prev_h,
+                               const int32_t* pair_parent, const uint8_t* build_flag, const gbdt_level* level,
+                               int32_t max_slots, int32_t F, uint32_t* hist_cnt, int64_t* hist_q, int64_t* hist_h,
+                               void* stream);
 
 /* gbdt_build_histograms_segmented: the same per-bin count and fixed-point G
  * of every flagged slot of a level ("Module Design: Training Core" s.6 step 2,
@@ -264,6 +296,17 @@ int gbdt_build_histograms_segmented(const uint8_t* bins, int64_t ldb, int32_t la
                                     int32_t max_slots, const uint8_t* build_flag, int32_t max_build,
                                     const gbdt_segment* segments, const gbdt_filter* filters, uint32_t* hist_cnt,
                                     int64_t* hist_q, void* ws, size_t ws_bytes, void* stream);
+/* The same with the logistic objective's H histogram: hist_h [max_slots][F][256]
+ * (non-NULL) receives the fixed-point sums of h = |g| (1 - |g|) (the hessian
+ * of a row whose g is sigmoid(pred) - label, label 0 or 1, see
+ * gbdt_compute_gradients_objective) with exponent fixed_exp[1]; fixed_exp[0]
+ * is S of g.  Up to 32 features of shared-memory histograms per CTA. */
+int gbdt_build_histograms_segmented_h(const uint8_t* bins, int64_t ldb, int32_t layout, int64_t N, int32_t F,
+                                      const void* g, int32_t g_dtype, const int32_t* fixed_exp,
+                                      const gbdt_level* level, int32_t max_slots, const uint8_t* build_flag,
+                                      int32_t max_build, const gbdt_segment* segments, const gbdt_filter* filters,
+                                      uint32_t* hist_cnt, int64_t* hist_q, int64_t* hist_h, void* ws,
+                                      size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------
  * gbdt_find_splits: best split of every slot of a level, "Module Design:
@@ -283,6 +326,13 @@ size_t gbdt_find_splits_workspace_size(int32_t F, int32_t max_slots);
 int gbdt_find_splits(const uint32_t* hist_cnt, const int64_t* hist_q, const int32_t* fixed_exp, int32_t F,
                      const int32_t* n_bins, const gbdt_level* level, int32_t max_slots, const gbdt_params* p,
                      gbdt_split* out, void* ws, size_t ws_bytes, void* stream);
+/* The same with H from an H histogram (logistic): H = hist_h * 2^-fixed_exp[1]
+ * (hist_h non-NULL, 16-byte aligned).  min_samples_leaf applies to the row
+ * counts, min_child_weight and H > 0 to H; out[].h_left/h_total are filled. */
+int gbdt_find_splits_h(const uint32_t* hist_cnt, const int64_t* hist_q, const int64_t* hist_h,
+                       const int32_t* fixed_exp, int32_t F, const int32_t* n_bins, const gbdt_level* level,
+                       int32_t max_slots, const gbdt_params* p, gbdt_split* out, void* ws, size_t ws_bytes,
+                       void* stream);
 
 /* ---------------------------------------------------------------------------
  * gbdt_partition: "Module Design: Training Core" s.6 step 5.  The k-th slot
@@ -382,8 +432,9 @@ int gbdt_predict(const float* X, int64_t ldx, int64_t N, int32_t F, const float*
  * gbdt_train: whole training run ("Module Design: Training Core" s.6).
  *   bins [F][ldb] uint8, n_bins [F] int32 (1..256), label [N] fp32 (device)
  *   p: host pointer
- *   pred_out [N] fp64 (device): predictions after the last tree
- *   init_pred_out: host double, the initial prediction mean(label)
+ *   pred_out [N] fp64 (device): predictions (margins) after the last tree
+ *   init_pred_out: host double, the initial prediction: mean(label) for
+ *     squared error, 0 for the logistic objective
  *   nodes_out: HOST array [n_trees][2^(max_depth+1)-1] gbdt_node; tree t's
  *     nodes are nodes_out[t*(2^(max_depth+1)-1) + i], i < nodes_per_tree[t]
  *   nodes_per_tree: HOST [n_trees] int32
@@ -392,7 +443,8 @@ int gbdt_predict(const float* X, int64_t ldx, int64_t N, int32_t F, const float*
  * labels) and at the end.  On any error after parameter validation nodes_out
  * is left untouched and nodes_per_tree[*] = 0 (no partial model, s.5 State
  * Machine).
- * NaN/Inf labels: GBDT_ERR_NONFINITE.  1 <= N < 2^31, 1 <= F <= 4096.
+ * NaN/Inf labels: GBDT_ERR_NONFINITE; with the logistic objective a label
+ * other than 0 or 1: GBDT_ERR_INVALID_ARG.  1 <= N < 2^31, 1 <= F <= 4096.
  * ------------------------------------------------------------------------- */
 size_t gbdt_train_workspace_size(int64_t N, int32_t F, const gbdt_params* p);
 int gbdt_train(const uint8_t* bins, int64_t ldb, const int32_t* n_bins, int64_t N, int32_t F, const float* label,

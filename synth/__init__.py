@@ -23,6 +23,9 @@ stand in for their shapes):
 ``large``   10,000,000 x 100: 50 N(0,1), 30 LogNormal(0, 1.5), 20 integer
             columns with 2..16 distinct values; label = sum of 20 random full
             depth-3 step trees + N(0, 0.5).
+``make_binary(name)``: the same features with a 0/1 label, 1 where the
+            workload's label exceeds its median (input of the logistic
+            objective).
 ``micro``   one tree level: 50,000,000 x 64 pre-binned uint8 columns with
             P(b) ~ (b+1)^-1.1 on 0..255, 256 nodes (sibling pairs 2k, 2k+1),
             g ~ N(0,1) float32.
@@ -31,7 +34,7 @@ from __future__ import annotations
 
 import numpy as np
 
-__all__ = ["CONFIGS", "make", "make_tiny", "make_mid", "make_covtype", "make_large", "make_micro"]
+__all__ = ["CONFIGS", "make", "make_binary", "make_tiny", "make_mid", "make_covtype", "make_large", "make_micro"]
 
 # Training parameters of each workload.  Unspecified ones take the readings
 # recorded in the design notes: gamma 0, min_child_weight 0, lambda 1.
@@ -165,3 +168,9 @@ def make_micro(seed: int = 0, n: int | None = None, f: int | None = None, n_node
 
 def make(name: str, seed: int = 0, n: int | None = None):
     return {"tiny": make_tiny, "mid": make_mid, "covtype": make_covtype, "large": make_large}[name](seed, n)
+
+
+def make_binary(name: str, seed: int = 0, n: int | None = None):
+    """Features of workload ``name`` with a 0/1 float32 label: 1 where its label exceeds the median."""
+    X, y = make(name, seed, n)
+    return X, (y > np.median(y)).astype(np.float32)

@@ -6,6 +6,9 @@ Tolerances (also in the design notes):
     sum |g| over the entry's rows and the second term is the documented rounding
     bound of the library's fixed point (q = round(g * 2^S) per row);
   * leaf values: the node's G bound divided by (H + lambda);
+  * logistic objective: an H entry's |H_gpu - H_orc| <= 1e-9 * H + n * (2^-(S_h+1) + 2^-53),
+    the rounding bound of H's own fixed point plus the rounding of g = p - 1 from which the
+    library recovers h; a leaf value's bound is (G bound + |w| * H bound) / (H + lambda);
   * predictions: 1e-6 * max(|p_orc|, std(label)).
 """
 import math
@@ -61,6 +64,11 @@ def g_tolerance(A, n, S):
     return 1e-9 * np.asarray(A) + np.asarray(n, dtype=np.float64) * 2.0 ** (-(S + 1)) * (1 + 1e-12) + 1e-300
 
 
+def h_tolerance(H, n, S_h):
+    n = np.asarray(n, dtype=np.float64)
+    return 1e-9 * np.asarray(H) + n * (2.0 ** (-(S_h + 1)) + 2.0 ** -53) * (1 + 1e-12) + 1e-300
+
+
 def traverse(nodes, bins):
     v = np.zeros(bins.shape[1], np.int64)
     for _ in range(64):
@@ -84,6 +92,7 @@ def compare_training(gpu, bins, n_bins, y, params, report=None):
         guide[t, :n, 1] = gpu["nodes"][t][:n]["threshold_bin"]
     ref = oracle.train(bins, n_bins, y, guide=guide, **params)
     lam, lr = params["reg_lambda"], params["learning_rate"]
+    logistic = params.get("objective", 0) == 1
     assert gpu["init_pred"] == pytest.approx(ref["init_pred"], rel=1e-12)
     pred = np.full(bins.shape[1], ref["init_pred"])
     adopted = near = 0
@@ -104,9 +113,13 @@ def compare_training(gpu, bins, n_bins, y, params, report=None):
             assert np.array_equal(a[k].astype(np.int64), b[k].astype(np.int64)), f"tree {t}: {k} differs"
         adopted += int(info["adopted"].sum())
         near += int((info["n_near"] > 1).sum())
-        gt = pred - y.astype(np.float64)
+        gt, ht = oracle.gradients(pred, y, 1 if logistic else 0)
         S = fixed_exponent(float(np.abs(gt).max()), bins.shape[1])
         tol = g_tolerance(info["A"], info["n_rows"], S) / (info["H"] + lam)
+        if logistic:  # S_h one lower: the library's max h may sit an ulp across a power of two
+            th = h_tolerance(info["H"], info["n_rows"], fixed_exponent(float(ht.max()), bins.shape[1]) - 1)
+            tol = (g_tolerance(info["A"], info["n_rows"], S) + np.abs(b["leaf_value"]) * th) / np.maximum(
+                info["H"] + lam - th, 1e-300)
         err = np.abs(a["leaf_value"] - b["leaf_value"])
         assert np.all(err <= tol), f"tree {t}: leaf value off by {err.max()} (tol {tol[err.argmax()]})"
         internal = b["is_leaf"] == 0

@@ -62,17 +62,18 @@ def test_parameter_rules_on_host(lib):
     assert g.validate_params(n_trees=1, max_depth=3) == g.OK
     for bad in (dict(min_samples_leaf=0), dict(min_child_weight=-1.0), dict(reg_lambda=-0.1), dict(gamma=-1.0),
                 dict(learning_rate=float("nan")), dict(reg_lambda=float("inf")), dict(max_depth=13),
-                dict(n_trees=-1)):
+                dict(n_trees=-1), dict(objective=2), dict(objective=-1), dict(num_leaves=1)):
         assert g.validate_params(**bad) == g.ERR_INVALID_ARG, bad
-    assert b"min_samples_leaf" in lib.gbdt_last_error() or b"finite" in lib.gbdt_last_error() or \
-        b"max_depth" in lib.gbdt_last_error()
+        assert lib.gbdt_last_error() != b""
+    assert g.validate_params(objective=g.OBJECTIVE_LOGISTIC) == g.OK
 
 
 def test_struct_layouts_match_header():
     import histogram_gradient_boosted_gb300 as g
 
-    assert ctypes.sizeof(g.Params) == 56
-    assert g.NODE_DTYPE.itemsize == 40 and g.SPLIT_DTYPE.itemsize == 40
+    assert ctypes.sizeof(g.Params) == 56 and g.Params.objective.offset == 52
+    assert g.NODE_DTYPE.itemsize == 40 and g.SPLIT_DTYPE.itemsize == 56
+    assert g.SPLIT_DTYPE.fields["h_left"][1] == 40 and g.SPLIT_DTYPE.fields["h_total"][1] == 48
     assert g.LEVEL_DTYPE.itemsize == 8 and g.SEGMENT_DTYPE.itemsize == 16
     assert ctypes.sizeof(g.Diagnostics) == 72
 
@@ -83,4 +84,10 @@ def test_entry_points_reject_bad_arguments_before_any_launch(lib):
     assert lib.gbdt_train(None, 0, None, 0, 0, None, None, None, None, None, None, None, None, 0, None) == -1
     assert lib.gbdt_build_histograms(None, 0, 0, 0, None, 0, None, None, None, 0, None, 0, None, None, None, 0,
                                      None) == -1
+    assert b"null pointer" in lib.gbdt_last_error()
+    assert lib.gbdt_build_histograms_segmented_h(None, 0, 0, 0, 0, None, 0, None, None, 0, None, 0, None, None, None,
+                                                 None, None, None, 0, None) == -1
+    assert lib.gbdt_find_splits_h(None, None, None, None, 0, None, None, 0, None, None, None, 0, None) == -1
+    assert lib.gbdt_subtract_histograms_h(None, None, None, None, None, None, 0, 0, None, None, None, None) == -1
+    assert lib.gbdt_compute_gradients_objective(None, None, 0, 1, None, None, None, 0, None) == -1
     assert b"null pointer" in lib.gbdt_last_error()
