@@ -332,6 +332,51 @@ def microbench(g, torch, args, peak):
     return res
 
 
+def logistic_leg(g, torch, args, cfg, N, F, Xd, y, pred, peak, peak_kind, stream):
+    """The logistic objective on the same matrix (0/1 labels: above the median): whole training runs
+    timed with CUDA events, and the level histograms (count, G and H) against the HBM roofline."""
+    params = dict(cfg, objective=1)
+    T = params["n_trees"]
+    yb = torch.from_numpy(synth.binary_label(y)).cuda()
+    lws = g._workspace(g.train_workspace_size(N, F, **params))
+
+    def run(diag=False):
+        bins, _, n_bins = g.quantize(Xd, params["max_bins"])
+        return g.train(bins, n_bins, yb, diagnostics=diag, ws=lws, pred=pred, **params)
+
+    for _ in range(max(1, min(args.warmup, 2))):
+        run()
+    torch.cuda.synchronize()
+    steps = max(1, min(args.steps, 2))
+    diags = []
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        diags.append(run(diag=True)["diag"])
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    hist_ms = sum(d["hist_ms"] for d in diags)
+    hist_bytes = sum(d["hist_bytes"] for d in diags)
+    launches = sum(d["hist_launches"] for d in diags)
+    part_ms = sum(d["part_ms"] for d in diags)
+    part_bytes = sum(d["part_bytes"] for d in diags)
+    achieved = hist_bytes / (hist_ms * 1e-3) / 1e9
+    return {"metric": METRIC, "value": N * F * T / (ms * 1e-3), "unit": UNIT, "ms_per_step": ms, "steps": steps,
+            "objective": "logistic (binary cross-entropy of a sigmoid); labels 1 where the regression label "
+                         "exceeds its median",
+            "step": "gbdt_quantize + gbdt_train, same matrix and parameters as the main line",
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": None, "peak_kind": peak_kind,
+                         "kernel": "seg_hist_kernel with H (count, G and H per entry; 32 features per CTA)",
+                         "launches": launches, "avg_launch_ms": hist_ms / launches,
+                         "algorithmic_bytes_per_launch": hist_bytes / launches,
+                         "share_of_step": hist_ms / (ms * steps)},
+            "partition": {"achieved_gbs": part_bytes / (part_ms * 1e-3) / 1e9,
+                          "frac": part_bytes / (part_ms * 1e-3) / 1e9 / peak, "share_of_step": part_ms / (ms * steps)},
+            "trees_at_full_size": diags[-1]["trees_at_full_size"]}
+
+
 def run_ours(args, rank, local_rank, ws, dist):
     import torch
 
@@ -463,6 +508,9 @@ def run_ours(args, rank, local_rank, ws, dist):
                          "equals_training_predictions": bool(torch.equal(pout, model["pred"])),
                          "note": "gbdt_predict on the training rows, inputs resident; the call includes its node "
                                  "preparation pass and one stream synchronisation"}
+    del pout, pws
+    if not args.no_logistic:
+        line["logistic"] = logistic_leg(g, torch, args, cfg, N, F, Xd, y, pred, peak, peak_kind, stream)
     if rank == 0 and not args.no_micro:
         line["histogram_microbench"] = microbench(g, torch, args, peak)
     if rank == 0 and not args.no_cpu:
@@ -491,6 +539,7 @@ def main():
     ap.add_argument("--cpu-trees", type=int, default=2)
     ap.add_argument("--no-micro", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-logistic", action="store_true", help="skip the logistic-objective leg")
     ap.add_argument("--only-micro", action="store_true", help="run only the level microbench (profiling)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":

@@ -34,7 +34,7 @@ from __future__ import annotations
 
 import numpy as np
 
-__all__ = ["CONFIGS", "make", "make_binary", "make_tiny", "make_mid", "make_covtype", "make_large", "make_micro"]
+__all__ = ["CONFIGS", "make", "make_binary", "binary_label", "make_tiny", "make_mid", "make_covtype", "make_large", "make_micro"]
 
 # Training parameters of each workload.  Unspecified ones take the readings
 # recorded in the design notes: gamma 0, min_child_weight 0, lambda 1.
@@ -170,7 +170,12 @@ def make(name: str, seed: int = 0, n: int | None = None):
     return {"tiny": make_tiny, "mid": make_mid, "covtype": make_covtype, "large": make_large}[name](seed, n)
 
 
+def binary_label(y: np.ndarray) -> np.ndarray:
+    """0/1 float32 label: 1 where y exceeds its median."""
+    return (y > np.median(y)).astype(np.float32)
+
+
 def make_binary(name: str, seed: int = 0, n: int | None = None):
-    """Features of workload ``name`` with a 0/1 float32 label: 1 where its label exceeds the median."""
+    """Features of workload ``name`` with the 0/1 label of binary_label."""
     X, y = make(name, seed, n)
-    return X, (y > np.median(y)).astype(np.float32)
+    return X, binary_label(y)
