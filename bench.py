@@ -456,19 +456,24 @@ def run_ours(args, rank, local_rank, ws, dist):
     e2e_steps = max(1, min(args.steps, 2))
     _barrier(dist)
     torch.cuda.synchronize()
+    h2d_ms = 0.0
     t0 = time.perf_counter()
     for _ in range(e2e_steps):
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        c0.record(stream)
         Xd.copy_(Xp, non_blocking=True)
         yd.copy_(yp, non_blocking=True)
+        c1.record(stream)
         out = step()
         pred_h.copy_(out["pred"], non_blocking=True)
         torch.cuda.synchronize()
+        h2d_ms += c0.elapsed_time(c1)
     e2e_s = _max_over_ranks(time.perf_counter() - t0, dist)
     M = (1 << (cfg["max_depth"] + 1)) - 1
     h2d = Xp.numel() * 4 + yp.numel() * 4
     d2h = T * M * 40 + T * 4 + N * 8
     e2e = {"value": N * F * T * e2e_steps * ws / e2e_s, "unit": UNIT, "h2d_bytes_per_step": h2d,
-           "d2h_bytes_per_step": d2h, "ms_per_step": 1e3 * e2e_s / e2e_steps}
+           "d2h_bytes_per_step": d2h, "ms_per_step": 1e3 * e2e_s / e2e_steps, "h2d_ms_per_step": h2d_ms / e2e_steps}
 
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": ms_total / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,

@@ -27,6 +27,7 @@ __all__ = ["lib", "GbdtError", "Params", "NODE_DTYPE", "SPLIT_DTYPE", "LEVEL_DTY
 OK, ERR_INVALID_ARG, ERR_NONFINITE, ERR_WORKSPACE, ERR_CUDA, ERR_INTERNAL = 0, -1, -2, -3, -4, -5
 DTYPE_F32, DTYPE_F64 = 0, 1
 OBJECTIVE_SQUARED_ERROR, OBJECTIVE_LOGISTIC = 0, 1
+BIN_PACKING_4BIT, BIN_PACKING_OFF = 0, 1
 LAYOUT_COLUMNS, LAYOUT_ROW_BLOCKS = 0, 1
 MAX_BINS, MAX_DEPTH = 256, 12
 
@@ -40,7 +41,7 @@ EXPORTED_SYMBOLS = [
     "gbdt_histograms_segmented_workspace_size", "gbdt_build_histograms_segmented", "gbdt_partition_rows_workspace_size",
     "gbdt_partition_rows", "gbdt_predict_workspace_size", "gbdt_predict", "gbdt_row_block_pitch",
     "gbdt_row_block_bytes", "gbdt_bins_to_row_blocks", "gbdt_compute_gradients_objective",
-    "gbdt_subtract_histograms_h", "gbdt_build_histograms_segmented_h", "gbdt_find_splits_h",
+    "gbdt_subtract_histograms_h", "gbdt_build_histograms_segmented_h", "gbdt_find_splits_h", "gbdt_row_block_slots",
 ]
 
 
@@ -53,7 +54,8 @@ class GbdtError(RuntimeError):
 class Params(ctypes.Structure):
     _fields_ = [("n_trees", ctypes.c_int32), ("max_depth", ctypes.c_int32), ("learning_rate", ctypes.c_double),
                 ("reg_lambda", ctypes.c_double), ("gamma", ctypes.c_double), ("min_samples_leaf", ctypes.c_int32),
-                ("min_child_weight", ctypes.c_double), ("num_leaves", ctypes.c_int32), ("objective", ctypes.c_int32)]
+                ("min_child_weight", ctypes.c_double), ("num_leaves", ctypes.c_int32), ("objective", ctypes.c_int32),
+                ("bin_packing", ctypes.c_int32), ("reserved", ctypes.c_int32)]
 
 
 class Diagnostics(ctypes.Structure):
@@ -119,6 +121,7 @@ def lib():
         "gbdt_build_histograms_segmented_h": ([P, i64, i32, i64, i32, P, i32, P, P, i32, P, i32, P, P, P, P, P, P, sz,
                                                P], i32),
         "gbdt_row_block_pitch": ([i32], i64),
+        "gbdt_row_block_slots": ([P, i32, i32, P, P], i32),
         "gbdt_row_block_bytes": ([i64, i32], sz),
         "gbdt_bins_to_row_blocks": ([P, i64, i64, i32, P, P], i32),
         "gbdt_partition_rows_workspace_size": ([i64, i32], sz),
@@ -178,9 +181,10 @@ def padded_ld(n: int) -> int:
 
 
 def make_params(n_trees=1, max_depth=6, learning_rate=0.1, reg_lambda=1.0, gamma=0.0, min_samples_leaf=1,
-                min_child_weight=0.0, num_leaves=0, objective=OBJECTIVE_SQUARED_ERROR, **_ignored) -> Params:
+                min_child_weight=0.0, num_leaves=0, objective=OBJECTIVE_SQUARED_ERROR, bin_packing=BIN_PACKING_4BIT,
+                **_ignored) -> Params:
     return Params(int(n_trees), int(max_depth), float(learning_rate), float(reg_lambda), float(gamma),
-                  int(min_samples_leaf), float(min_child_weight), int(num_leaves), int(objective))
+                  int(min_samples_leaf), float(min_child_weight), int(num_leaves), int(objective), int(bin_packing), 0)
 
 
 def version() -> str:
@@ -250,6 +254,18 @@ def build_histograms(bins, N, g, fixed_exp, node_of_row, level, max_slots, build
                                        _ptr(level), max_slots, _ptr(build_flag), max_build, _ptr(hist_cnt),
                                        _ptr(hist_q), _ptr(ws), ws.numel(), _stream()))
     return hist_cnt, hist_q
+
+
+def row_block_slots(n_bins, packing=BIN_PACKING_4BIT):
+    """Host-side slot plan of gbdt_train's row-block copies: (loc (F,) uint32, src (S,) uint32)."""
+    nb = np.ascontiguousarray(n_bins, dtype=np.int32)
+    F = nb.shape[0]
+    loc = np.zeros(F, np.uint32)
+    src = np.zeros(F, np.uint32)
+    S = lib().gbdt_row_block_slots(nb.ctypes.data_as(ctypes.c_void_p), F, int(packing),
+                                   loc.ctypes.data_as(ctypes.c_void_p), src.ctypes.data_as(ctypes.c_void_p))
+    _check(0 if S > 0 else S)
+    return loc, src[:S]
 
 
 def to_row_blocks(bins, N: int):

@@ -64,6 +64,10 @@ int validate_params(const gbdt_params* p) {
     set_error("parameters: num_leaves must be 0 (no budget) or at least 2");
     return GBDT_ERR_INVALID_ARG;
   }
+  if (p->bin_packing != GBDT_BIN_PACKING_4BIT && p->bin_packing != GBDT_BIN_PACKING_OFF) {
+    set_error("parameters: bin_packing must be %d (4-bit) or %d (off)", GBDT_BIN_PACKING_4BIT, GBDT_BIN_PACKING_OFF);
+    return GBDT_ERR_INVALID_ARG;
+  }
   if (p->objective != GBDT_OBJECTIVE_SQUARED_ERROR && p->objective != GBDT_OBJECTIVE_LOGISTIC) {
     set_error("parameters: objective must be %d (squared error) or %d (logistic)", GBDT_OBJECTIVE_SQUARED_ERROR,
               GBDT_OBJECTIVE_LOGISTIC);

@@ -23,6 +23,7 @@ enum : int32_t {
   kErrPartitionCount = 4, // partition left count differs from the split record
   kErrLevelSize = 8,      // a level has more slots than the launch bound
   kErrWaitTimeout = 16,   // an asynchronous copy did not complete within its wait limit
+  kErrBinRange = 32,      // a caller's bin is not below its feature's n_bins
 };
 
 // ---- thread-local error message -------------------------------------------------
@@ -174,6 +175,21 @@ __host__ __device__ __forceinline__ int64_t rb_offset(int f, int64_t p, int64_t 
 }
 inline int64_t rb_pitch(int32_t F) { return static_cast<int64_t>(F) * kRowBlock; }
 inline int64_t rb_blocks(int64_t N) { return (N + kRowBlock - 1) / kRowBlock; }
+
+// 4-bit slots: in the training copies two features with at most 16 bins share one 32-byte slot
+// of a row block, the first of the pair in the low nibble of each byte, the second in the high
+// nibble ("two cells per byte"); every other feature has a slot of its own.  A feature's
+// locator says where its bins sit: loc = slot | nibble << 16, nibble 0 for a whole byte, 1 for
+// the low nibble, 2 for the high nibble.  The pitch is 32 bytes per slot.
+constexpr int kMaxPackedBins = 16;
+__host__ __device__ __forceinline__ uint32_t loc_slot(uint32_t loc) { return loc & 0xffffu; }
+__host__ __device__ __forceinline__ uint32_t loc_shift(uint32_t loc) { return (loc >> 16) == 2 ? 4u : 0u; }
+__host__ __device__ __forceinline__ uint32_t loc_mask(uint32_t loc) { return (loc >> 16) == 0 ? 0xffu : 0x0fu; }
+// Bin of position p of the feature at loc in a row-block buffer of the given pitch.
+__device__ __forceinline__ int rb_bin(const uint8_t* __restrict__ rb, uint32_t loc, int64_t p, int64_t pitch) {
+  const uint32_t b = rb[rb_offset(static_cast<int>(loc_slot(loc)), p, pitch)];
+  return static_cast<int>((b >> loc_shift(loc)) & loc_mask(loc));
+}
 
 inline int ceil_div(int64_t a, int64_t b) { return static_cast<int>((a + b - 1) / b); }
 

@@ -82,8 +82,10 @@ int launch_seg_histograms(const SegHistPlan& plan, const uint8_t* bins, int64_t 
                           const void* g, int32_t g_dtype, const int32_t* fixed_exp, const gbdt_level* level,
                           int32_t max_slots, const uint8_t* build_flag, const gbdt_segment* seg,
                           const gbdt_filter* filters, void* scratch, uint32_t* hist_cnt, int64_t* hist_q,
-                          int64_t* hist_h, cudaStream_t s,
-                          bool row_blocks = false);  // row_blocks: ldb is the row-block pitch; hist_h: plan.with_h
+                          int64_t* hist_h, cudaStream_t s, bool row_blocks = false,
+                          const uint32_t* floc = nullptr);  // row_blocks: ldb is the row-block pitch, floc the
+                                                            // feature locators (null: feature f in slot f);
+                                                            // hist_h: plan.with_h
 // Stable partition of the per-position data of every split slot (bins columns, g, original row
 // id) from *_in to *_out; slots without a split record leaf_of_row[orig] = their node id.
 size_t move_scratch_bytes(int64_t N, int32_t max_slots);
@@ -92,18 +94,26 @@ void launch_move_rows(const uint8_t* bins_in, uint8_t* bins_out, int64_t ldb, in
                       const uint8_t* go_right, const gbdt_level* level, int32_t max_slots, const gbdt_segment* seg,
                       const Route* route, const gbdt_split* splits, gbdt_segment* seg_out,
                       uint16_t* leaf_of_row, void* scratch, int32_t* err, cudaStream_t s);
-// ---- training-internal row-block layout (see rb_offset) ----
-// Bytes of a row-block copy of N rows x F features, and the conversion from the column layout.
-size_t row_block_bytes(int64_t N, int32_t F);
-void launch_cols_to_row_blocks(const uint8_t* cols, int64_t ldb, int64_t N, int32_t F, uint8_t* rb, cudaStream_t s);
-// The tensor map the pair move reads a row-block buffer through.
-int make_row_block_map(CUtensorMap* map, const uint8_t* rb, int64_t N, int32_t F);
+// ---- training-internal row-block layout (see rb_offset, and loc_slot for 4-bit slots) ----
+// Bytes of a row-block copy of N rows x S slots, and the conversion from the column layout:
+// slot_src (null: slot s holds feature s) from plan_row_block_slots; with n_bins every bin of the
+// N rows is checked against its feature's n_bins (kErrBinRange in err).
+size_t row_block_bytes(int64_t N, int32_t S);
+void launch_cols_to_row_blocks(const uint8_t* cols, int64_t ldb, int64_t N, int32_t S, const uint32_t* slot_src,
+                               const int32_t* n_bins, uint8_t* rb, int32_t* err, cudaStream_t s);
+// Host: the slots of a row-block copy.  With pack, features with n_bins <= 16 pair up in feature order
+// (the first of a pair in the low nibble, an unpaired one keeps a whole byte); every other feature has a
+// slot of its own.  Writes loc[F] (locators) and src[S] (per slot: first feature | second << 16, second
+// 0xffff for a whole-byte slot); returns S.
+int plan_row_block_slots(const int32_t* n_bins, int32_t F, bool pack, uint32_t* loc, uint32_t* src);
+// The tensor map the pair move reads a row-block buffer of S slots through.
+int make_row_block_map(CUtensorMap* map, const uint8_t* rb, int64_t N, int32_t S);
 // Record leaves without moving data: every row of the level (its child when its slot splits, its
 // own node when it does not), or with frozen_only only the rows of slots that do not split.  Needs
 // route from the level's splits; bins in the row-block layout; scratch is move_scratch_bytes.
-void launch_leaf_rows(const uint8_t* bins_rb, int64_t pitch, int64_t N, const uint32_t* orig_in,
-                      const gbdt_level* level, int32_t max_slots, const gbdt_segment* seg, const Route* route,
-                      bool frozen_only, uint16_t* leaf_of_row, void* scratch, cudaStream_t s);
+void launch_leaf_rows(const uint8_t* bins_rb, int64_t pitch, const uint32_t* floc, int64_t N,
+                      const uint32_t* orig_in, const gbdt_level* level, int32_t max_slots, const gbdt_segment* seg,
+                      const Route* route, bool frozen_only, uint16_t* leaf_of_row, void* scratch, cudaStream_t s);
 // Odd level: the scan range (the pair's rows) and filter (the parent's split, the slot's side) of
 // every slot, for the histogram of rows not yet partitioned.
 void launch_pair_scan_ranges(const gbdt_level* level, int32_t max_slots, const gbdt_segment* seg,
@@ -113,18 +123,18 @@ void launch_pair_scan_ranges(const gbdt_level* level, int32_t max_slots, const g
 // straight into the next level's order (four grandchild runs per pair); rows of children that do not
 // split record them as their leaf.  route_prev/pair_parent: the level above; seg_next: the next
 // level's segments.  Bins in the row-block layout, read through map_in (make_row_block_map of
-// bins_rb_in); g is fp64.  Scratch: move_scratch_bytes(N, max_slots).
+// bins_rb_in, S slots; floc the feature locators); g is fp64.  Scratch: move_scratch_bytes(N, max_slots).
 void launch_move_pairs(const CUtensorMap& map_in, const uint8_t* bins_rb_in, uint8_t* bins_rb_out, int64_t pitch,
-                       int64_t N, int32_t F, const double* g_in, double* g_out, const uint32_t* orig_in,
-                       uint32_t* orig_out, const gbdt_level* level, int32_t max_slots, const gbdt_segment* seg,
-                       const Route* route_cur, const Route* route_prev, const int32_t* pair_parent,
-                       const gbdt_segment* seg_next, uint16_t* leaf_of_row, void* scratch, int32_t* err,
-                       cudaStream_t s);
+                       const uint32_t* floc, int64_t N, int32_t S, const double* g_in, double* g_out,
+                       const uint32_t* orig_in, uint32_t* orig_out, const gbdt_level* level, int32_t max_slots,
+                       const gbdt_segment* seg, const Route* route_cur, const Route* route_prev,
+                       const int32_t* pair_parent, const gbdt_segment* seg_next, uint16_t* leaf_of_row, void* scratch,
+                       int32_t* err, cudaStream_t s);
 // Odd last split level: every row of every pair records its leaf; nothing moves.
-void launch_leaf_pairs(const uint8_t* bins_rb, int64_t pitch, int64_t N, const uint32_t* orig_in,
-                       const gbdt_level* level, int32_t max_slots, const gbdt_segment* seg, const Route* route_cur,
-                       const Route* route_prev, const int32_t* pair_parent, const gbdt_segment* seg_next,
-                       uint16_t* leaf_of_row, void* scratch, cudaStream_t s);
+void launch_leaf_pairs(const uint8_t* bins_rb, int64_t pitch, const uint32_t* floc, int64_t N,
+                       const uint32_t* orig_in, const gbdt_level* level, int32_t max_slots, const gbdt_segment* seg,
+                       const Route* route_cur, const Route* route_prev, const int32_t* pair_parent,
+                       const gbdt_segment* seg_next, uint16_t* leaf_of_row, void* scratch, cudaStream_t s);
 
 // node_of_row[r] = left_node + (bins[feature][r] > bin) for rows of slots with a split.
 void launch_route_rows(const uint8_t* bins, int64_t ldb, int64_t N, const Route* route, const gbdt_level* level,

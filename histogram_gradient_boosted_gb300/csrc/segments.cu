@@ -262,11 +262,14 @@ __device__ __forceinline__ void load_rows32(const uint8_t* p, bool second, uint3
 // kRB: bins in the row-block layout (ldb is then the row-block pitch and col[h]
 // points at the feature's 32 bytes of row block 0).
 // kH: also the logistic hessian h = |g| (1 - |g|) of each row, in fixed point with scale_h.
+// unpack: some lanes' features sit in 4-bit slots: their loaded words become (w >> sh) & mk (every
+// byte then holds the feature's bin); the filter byte likewise with fsh, fmk.
 template <typename GT, int NH, bool kV8, bool kRB, bool kH>
 __device__ __forceinline__ void seg_hist_rows(uint32_t base, const uint8_t* const (&col)[NH], const bool (&has)[NH],
                                               int64_t ldb, const GT* __restrict__ g, double scale, double scale_h,
                                               int64_t p0, int64_t p1, const uint8_t* __restrict__ fcol, int fbin,
-                                              int fside, uint4* s_q) {
+                                              int fside, uint4* s_q, bool unpack, const uint32_t (&sh)[NH],
+                                              const uint32_t (&mk)[NH], uint32_t fsh, uint32_t fmk) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, n_warps = blockDim.x >> 5;
   // aligned 32-position blocks covering [p0, p1); positions outside are masked
   for (int64_t b = (p0 >> 5) + warp; (b << 5) < p1; b += n_warps) {
@@ -277,7 +280,7 @@ __device__ __forceinline__ void seg_hist_rows(uint32_t base, const uint8_t* cons
     // all of the block's loads are issued before any of them is used: the filter byte, the gradient
     // and the bins (the bins of a block whose rows are all filtered out are loaded for nothing)
     const int64_t boff = kRB ? (r0 >> 5) * ldb : r0;  // the block's bytes of a feature, from col[h]
-    const int fb = (fcol && in) ? static_cast<int>(fcol[boff + lane]) : 0;
+    const int fb = (fcol && in) ? static_cast<int>((fcol[boff + lane] >> fsh) & fmk) : 0;
     const double gv = in ? static_cast<double>(g[pr]) : 0.0;
     uint32_t w[NH][8];
 #pragma unroll
@@ -292,6 +295,12 @@ __device__ __forceinline__ void seg_hist_rows(uint32_t base, const uint8_t* cons
     const bool v = in && (!fcol || (fb > fbin) == (fside != 0));
     const uint32_t valid = __ballot_sync(0xffffffffu, v);
     if (valid == 0) continue;  // warp-uniform: no row of this block belongs to the slot
+    if (unpack) {  // CTA-uniform
+#pragma unroll
+      for (int h = 0; h < NH; ++h)
+#pragma unroll
+        for (int k = 0; k < 8; ++k) w[h][k] = (w[h][k] >> sh[h]) & mk[h];
+    }
     const int64_t q = v ? to_fixed(gv, scale) : 0;
     __syncwarp();
     if constexpr (kH) {
@@ -357,7 +366,8 @@ __global__ void __launch_bounds__(kSegThreads, 1)
                     const int32_t* __restrict__ fixed_exp, const gbdt_segment* __restrict__ seg,
                     const gbdt_filter* __restrict__ filters, const int32_t* __restrict__ build_slot,
                     const int64_t* __restrict__ row_start, const SegWork* __restrict__ st, int32_t group_feats,
-                    uint32_t* __restrict__ hist_cnt, int64_t* __restrict__ hist_q, int64_t* __restrict__ hist_h) {
+                    uint32_t* __restrict__ hist_cnt, int64_t* __restrict__ hist_q, int64_t* __restrict__ hist_h,
+                    const uint32_t* __restrict__ floc) {
   extern __shared__ __align__(16) unsigned char smem[];
   const int ctas = st->ctas;
   if (static_cast<int>(blockIdx.x) >= ctas) return;
@@ -390,22 +400,30 @@ __global__ void __launch_bounds__(kSegThreads, 1)
       *reinterpret_cast<uint4*>(s_cnt + e) = make_uint4(0, 0, 0, 0);
     __syncthreads();
     const uint32_t base = smem_u32(s_cnt) + lane * 4;
+    // a lane's feature: its column, or with locators (4-bit slots, row blocks only) its slot and nibble
     bool has[NH];
     const uint8_t* col[NH];
+    uint32_t sh[NH], mk[NH];
+    const bool unpack = kRB && floc != nullptr;
 #pragma unroll
     for (int h = 0; h < NH; ++h) {
       has[h] = h * 32 + lane < nf;
-      col[h] = bins + static_cast<int64_t>(f_lo + (has[h] ? h * 32 + lane : 0)) * (kRB ? kRowBlock : ldb);
+      const int f = f_lo + (has[h] ? h * 32 + lane : 0);
+      const uint32_t loc = unpack ? floc[f] : static_cast<uint32_t>(f);
+      col[h] = bins + static_cast<int64_t>(loc_slot(loc)) * (kRB ? kRowBlock : ldb);
+      sh[h] = loc_shift(loc);
+      mk[h] = loc_mask(loc) * 0x01010101u;
     }
     for (int64_t r = lo; r < hi; ++k) {
       const int64_t r_end = min(hi, row_start[k + 1]);
       const int slot = build_slot[k];
       const int64_t p0 = seg[slot].start + (r - row_start[k]);
       const gbdt_filter fl = filters ? filters[slot] : gbdt_filter{-1, 0, 0, 0};
+      const uint32_t floc_f = fl.feature < 0 ? 0u : unpack ? floc[fl.feature] : static_cast<uint32_t>(fl.feature);
       const uint8_t* fcol =
-          fl.feature >= 0 ? bins + static_cast<int64_t>(fl.feature) * (kRB ? kRowBlock : ldb) : nullptr;
+          fl.feature >= 0 ? bins + static_cast<int64_t>(loc_slot(floc_f)) * (kRB ? kRowBlock : ldb) : nullptr;
       seg_hist_rows<GT, NH, kV8, kRB, kH>(base, col, has, ldb, g, scale, scale_h, p0, p0 + (r_end - r), fcol, fl.bin,
-                                          fl.side, s_q);
+                                          fl.side, s_q, unpack, sh, mk, loc_shift(floc_f), loc_mask(floc_f));
       __syncthreads();
       seg_hist_flush<NH, kH>(s_cnt, s_lo, s_hi, slot, F, f_lo, nf, hist_cnt, hist_q, hist_h);
       __syncthreads();
@@ -829,12 +847,13 @@ __global__ void __launch_bounds__(kMvThreads, 4)
 // records its leaf: the child its split sends it to, or the slot's own node
 // when the slot did not split.  With frozen_only, only the slots that did not
 // split record their rows (the others are handled at a later level).  Bins in
-// the row-block layout (pitch).
+// the row-block layout (pitch); floc: feature locators (null: feature f in slot f).
 __global__ void __launch_bounds__(kMvThreads)
-    mv_leaves_kernel(const uint8_t* __restrict__ bins_in, int64_t pitch, const uint32_t* __restrict__ orig_in,
-                     const gbdt_level* __restrict__ level, int32_t max_slots, const gbdt_segment* __restrict__ seg,
-                     const Route* __restrict__ route, const int32_t* __restrict__ tile_start,
-                     const MvState* __restrict__ st, bool frozen_only, uint16_t* __restrict__ leaf_of_row) {
+    mv_leaves_kernel(const uint8_t* __restrict__ bins_in, int64_t pitch, const uint32_t* __restrict__ floc,
+                     const uint32_t* __restrict__ orig_in, const gbdt_level* __restrict__ level, int32_t max_slots,
+                     const gbdt_segment* __restrict__ seg, const Route* __restrict__ route,
+                     const int32_t* __restrict__ tile_start, const MvState* __restrict__ st, bool frozen_only,
+                     uint16_t* __restrict__ leaf_of_row) {
   const int t = blockIdx.x;
   if (t >= st->total_tiles) return;
   const int n_slots = min(level->n_slots, max_slots);
@@ -848,13 +867,14 @@ __global__ void __launch_bounds__(kMvThreads)
     for (int i = threadIdx.x; i < n; i += blockDim.x) leaf_of_row[orig_in[p0 + i]] = node;
     return;
   }
+  const uint32_t loc = floc ? floc[rt.feature] : static_cast<uint32_t>(rt.feature);
   for (int i0 = threadIdx.x; i0 < n; i0 += 4 * blockDim.x) {  // four rows in flight per thread
     int d[4];
     uint32_t o[4];
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int i = i0 + u * blockDim.x;
-      d[u] = i < n ? bins_in[rb_offset(rt.feature, p0 + i, pitch)] : -1;
+      d[u] = i < n ? rb_bin(bins_in, loc, p0 + i, pitch) : -1;
       o[u] = i < n ? orig_in[p0 + i] : 0u;
     }
 #pragma unroll
@@ -863,23 +883,68 @@ __global__ void __launch_bounds__(kMvThreads)
   }
 }
 
-// Column layout [F][ldb] -> row-block layout: one thread per (feature, row block) piece of 32 bytes;
-// consecutive threads take consecutive row blocks of one feature, so the reads are coalesced and
+// Column layout [F][ldb] -> row-block layout: one thread per (slot, row block) piece of 32 bytes;
+// consecutive threads take consecutive row blocks of one slot, so the reads are coalesced and
 // every write is one whole 32-byte sector.  Bytes of the last block past N are copied as they are.
-__global__ void cols_to_row_blocks_kernel(const uint8_t* __restrict__ cols, int64_t ldb, int64_t n_blocks,
-                                          int32_t F, uint8_t* __restrict__ rb, int64_t pitch) {
-  const int64_t pieces = n_blocks * F;
+// src (null: slot s is feature s) gives each slot's features: first | second << 16, second 0xffff
+// for a whole-byte slot; a 4-bit slot's byte is first | second << 4 (both bins below 16).
+__device__ __forceinline__ void load_piece(const uint8_t* __restrict__ cols, int64_t ldb, int f, int64_t blk,
+                                           uint4& a, uint4& b) {
+  const uint8_t* p = cols + static_cast<int64_t>(f) * ldb + blk * kRowBlock;
+  a = *reinterpret_cast<const uint4*>(p);  // blk * 32 < N <= ldb, ldb % 16 == 0
+  b = blk * kRowBlock + 32 <= ldb ? *reinterpret_cast<const uint4*>(p + 16) : make_uint4(0, 0, 0, 0);
+}
+
+__device__ __forceinline__ uint4 nibbles(uint4 lo, uint4 hi) {
+  return make_uint4(lo.x | (hi.x << 4), lo.y | (hi.y << 4), lo.z | (hi.z << 4), lo.w | (hi.w << 4));
+}
+
+// Any byte of rows below `rows` (0..32) in the 32-byte piece (a, b) at or above nb (1..256)?
+__device__ __forceinline__ bool piece_out_of_range(uint4 a, uint4 b, int rows, int nb) {
+  if (nb >= 256) return false;
+  const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+  const uint32_t lim = static_cast<uint32_t>(nb) * 0x01010101u;
+  bool bad = false;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const int v = min(max(rows - 4 * k, 0), 4);  // valid bytes of word k
+    const uint32_t keep = v >= 4 ? 0xffffffffu : (1u << (8 * v)) - 1u;
+    bad |= (__vcmpgeu4(w[k], lim) & keep) != 0;
+  }
+  return bad;
+}
+
+// n_bins (may be null): every bin of rows below N is checked against its feature's n_bins;
+// a bin out of range raises kErrBinRange.
+__global__ void cols_to_row_blocks_kernel(const uint8_t* __restrict__ cols, int64_t ldb, int64_t N,
+                                          int64_t n_blocks, int32_t S, const uint32_t* __restrict__ src,
+                                          const int32_t* __restrict__ n_bins, uint8_t* __restrict__ rb,
+                                          int64_t pitch, int32_t* __restrict__ err) {
+  const int64_t pieces = n_blocks * S;
+  bool bad = false;
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < pieces;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int f = static_cast<int>(i / n_blocks);
-    const int64_t blk = i - static_cast<int64_t>(f) * n_blocks;
-    const uint8_t* src = cols + static_cast<int64_t>(f) * ldb + blk * kRowBlock;
-    const uint4 a = *reinterpret_cast<const uint4*>(src);  // blk * 32 < N <= ldb, ldb % 16 == 0
-    const uint4 b = blk * kRowBlock + 32 <= ldb ? *reinterpret_cast<const uint4*>(src + 16) : make_uint4(0, 0, 0, 0);
-    uint4* dst = reinterpret_cast<uint4*>(rb + blk * pitch + static_cast<int64_t>(f) * kRowBlock);
+    const int sl = static_cast<int>(i / n_blocks);
+    const int64_t blk = i - static_cast<int64_t>(sl) * n_blocks;
+    const int rows = static_cast<int>(min(static_cast<int64_t>(kRowBlock), N - blk * kRowBlock));
+    const uint32_t sv = src ? src[sl] : static_cast<uint32_t>(sl) | 0xffff0000u;
+    const int fa = static_cast<int>(sv & 0xffffu);
+    uint4 a, b;
+    load_piece(cols, ldb, fa, blk, a, b);
+    if (n_bins) bad |= piece_out_of_range(a, b, rows, n_bins[fa]);
+    if ((sv >> 16) != 0xffffu) {
+      const int fb = static_cast<int>(sv >> 16);
+      uint4 c, d;
+      load_piece(cols, ldb, fb, blk, c, d);
+      if (n_bins) bad |= piece_out_of_range(c, d, rows, n_bins[fb]);
+      a = nibbles(a, c);
+      b = nibbles(b, d);
+    }
+    uint4* dst = reinterpret_cast<uint4*>(rb + blk * pitch + static_cast<int64_t>(sl) * kRowBlock);
     dst[0] = a;
     dst[1] = b;
   }
+  if (bad) raise_error(err, kErrBinRange);
 }
 
 // ------------------------------------------------------------------------- two levels at once
@@ -893,8 +958,8 @@ struct PairRoute {
   int64_t start, count;  // the pair's rows (both children) in the current order
   int64_t dst[4];        // first position of each grandchild in the next order
   int64_t want[4];       // its row count from the split records; -1: its child does not split
-  int32_t f1, b1;        // the parent's split: which child a row belongs to
-  int32_t f2[2], b2[2];  // the children's splits; f2 < 0: the child is a leaf
+  int32_t f1, b1;        // the parent's split (f1: its feature's locator): which child a row belongs to
+  int32_t f2[2], b2[2];  // the children's splits (locators); f2 < 0: the child is a leaf
   int32_t node[2];       // the children's node ids
   int32_t left[2];       // node id of each child's left child
 };
@@ -914,8 +979,9 @@ struct RunPrefix {  // rows of each of the four runs before a tile
 __global__ void pair_routes_kernel(const gbdt_level* __restrict__ level, int32_t max_slots,
                                    const gbdt_segment* __restrict__ seg, const Route* __restrict__ route_cur,
                                    const Route* __restrict__ route_prev, const int32_t* __restrict__ pair_parent,
-                                   const gbdt_segment* __restrict__ seg_next, PairRoute* __restrict__ pairs,
-                                   int32_t* __restrict__ tile_start, PairState* __restrict__ st) {
+                                   const gbdt_segment* __restrict__ seg_next, const uint32_t* __restrict__ floc,
+                                   PairRoute* __restrict__ pairs, int32_t* __restrict__ tile_start,
+                                   PairState* __restrict__ st) {
   __shared__ int s_b[1024];
   __shared__ int s_pre;
   if (threadIdx.x == 0) s_pre = 0;
@@ -927,13 +993,14 @@ __global__ void pair_routes_kernel(const gbdt_level* __restrict__ level, int32_t
     if (k < n_pairs) {
       PairRoute pr;
       const Route up = route_prev[pair_parent[k]];
-      pr.f1 = up.feature, pr.b1 = up.bin;
+      pr.f1 = static_cast<int32_t>(floc ? floc[up.feature] : up.feature), pr.b1 = up.bin;
       pr.start = seg[2 * k].start;
       pr.count = seg[2 * k].count + seg[2 * k + 1].count;
       for (int c = 0; c < 2; ++c) {
         const Route rt = route_cur[2 * k + c];
         pr.node[c] = level->node_begin + 2 * k + c;
-        pr.f2[c] = rt.feature, pr.b2[c] = rt.bin, pr.left[c] = rt.left_node;
+        pr.f2[c] = rt.feature < 0 ? -1 : static_cast<int32_t>(floc ? floc[rt.feature] : rt.feature);
+        pr.b2[c] = rt.bin, pr.left[c] = rt.left_node;
         for (int j = 0; j < 2; ++j) {
           if (rt.feature >= 0) {
             const gbdt_segment g2 = seg_next[2 * rt.pad + j];
@@ -971,9 +1038,9 @@ __global__ void pair_routes_kernel(const gbdt_level* __restrict__ level, int32_t
 // are loaded together (independent loads), then the child's is selected.
 __device__ __forceinline__ int pair_run(const PairRoute& pr, const uint8_t* __restrict__ bins, int64_t pitch,
                                         int64_t p, int* child) {
-  const int d1 = bins[rb_offset(pr.f1, p, pitch)];
-  const int d20 = pr.f2[0] >= 0 ? bins[rb_offset(pr.f2[0], p, pitch)] : 0;
-  const int d21 = pr.f2[1] >= 0 ? bins[rb_offset(pr.f2[1], p, pitch)] : 0;
+  const int d1 = rb_bin(bins, static_cast<uint32_t>(pr.f1), p, pitch);
+  const int d20 = pr.f2[0] >= 0 ? rb_bin(bins, static_cast<uint32_t>(pr.f2[0]), p, pitch) : 0;
+  const int d21 = pr.f2[1] >= 0 ? rb_bin(bins, static_cast<uint32_t>(pr.f2[1]), p, pitch) : 0;
   const int c = d1 > pr.b1 ? 1 : 0;
   *child = c;
   const int f2 = c ? pr.f2[1] : pr.f2[0];
@@ -1256,7 +1323,7 @@ int launch_seg_histograms(const SegHistPlan& plan, const uint8_t* bins, int64_t 
                           const void* g, int32_t g_dtype, const int32_t* fixed_exp, const gbdt_level* level,
                           int32_t max_slots, const uint8_t* build_flag, const gbdt_segment* seg,
                           const gbdt_filter* filters, void* scratch, uint32_t* hist_cnt, int64_t* hist_q,
-                          int64_t* hist_h, cudaStream_t s, bool row_blocks) {
+                          int64_t* hist_h, cudaStream_t s, bool row_blocks, const uint32_t* floc) {
   (void)N;
   Carve c(scratch, seg_hist_scratch_bytes(max_slots));
   SegWork* st = c.take<SegWork>(1);
@@ -1272,7 +1339,8 @@ int launch_seg_histograms(const SegHistPlan& plan, const uint8_t* bins, int64_t 
   auto launch = [&](auto kernel, const auto* gp) -> int {
     GBDT_CUDA(smem_attr(kernel, plan.smem));
     kernel<<<grid, kSegThreads, plan.smem, s>>>(bins, ldb, F, gp, fixed_exp, seg, filters, build_slot, row_start,
-                                                st, plan.group_feats, hist_cnt, hist_q, hist_h);
+                                                st, plan.group_feats, hist_cnt, hist_q, hist_h,
+                                                row_blocks ? floc : nullptr);
     return GBDT_OK;
   };
   auto pick = [&](const auto* gp, auto h_tag) -> int {
@@ -1363,17 +1431,17 @@ void launch_move_rows(const uint8_t* bins_in, uint8_t* bins_out, int64_t ldb, in
   count_launches();
 }
 
-void launch_leaf_rows(const uint8_t* bins_rb, int64_t pitch, int64_t N, const uint32_t* orig_in,
-                      const gbdt_level* level, int32_t max_slots, const gbdt_segment* seg, const Route* route,
-                      bool frozen_only, uint16_t* leaf_of_row, void* scratch, cudaStream_t s) {
+void launch_leaf_rows(const uint8_t* bins_rb, int64_t pitch, const uint32_t* floc, int64_t N,
+                      const uint32_t* orig_in, const gbdt_level* level, int32_t max_slots, const gbdt_segment* seg,
+                      const Route* route, bool frozen_only, uint16_t* leaf_of_row, void* scratch, cudaStream_t s) {
   Carve c(scratch, two_way_scratch_bytes(N, max_slots));
   MvState* st = c.take<MvState>(1);
   int32_t* tile_start = c.take<int32_t>(max_slots + 1);
   const int max_tiles = ceil_div(N, kMvTile) + max_slots;
   mv_setup_kernel<<<1, 1024, 0, s>>>(level, max_slots, seg, tile_start, st);
   count_launches();
-  mv_leaves_kernel<<<max_tiles, kMvThreads, 0, s>>>(bins_rb, pitch, orig_in, level, max_slots, seg, route, tile_start,
-                                                    st, frozen_only, leaf_of_row);
+  mv_leaves_kernel<<<max_tiles, kMvThreads, 0, s>>>(bins_rb, pitch, floc, orig_in, level, max_slots, seg, route,
+                                                    tile_start, st, frozen_only, leaf_of_row);
   count_launches();
 }
 
@@ -1386,51 +1454,74 @@ void launch_pair_scan_ranges(const gbdt_level* level, int32_t max_slots, const g
 }
 
 void launch_move_pairs(const CUtensorMap& map_in, const uint8_t* bins_rb_in, uint8_t* bins_rb_out, int64_t pitch,
-                       int64_t N, int32_t F, const double* g_in, double* g_out, const uint32_t* orig_in,
-                       uint32_t* orig_out, const gbdt_level* level, int32_t max_slots, const gbdt_segment* seg,
-                       const Route* route_cur, const Route* route_prev, const int32_t* pair_parent,
-                       const gbdt_segment* seg_next, uint16_t* leaf_of_row, void* scratch, int32_t* err,
-                       cudaStream_t s) {
+                       const uint32_t* floc, int64_t N, int32_t S, const double* g_in, double* g_out,
+                       const uint32_t* orig_in, uint32_t* orig_out, const gbdt_level* level, int32_t max_slots,
+                       const gbdt_segment* seg, const Route* route_cur, const Route* route_prev,
+                       const int32_t* pair_parent, const gbdt_segment* seg_next, uint16_t* leaf_of_row, void* scratch,
+                       int32_t* err, cudaStream_t s) {
   const PairScratch p = carve_pairs(scratch, N, max_slots);
-  pair_routes_kernel<<<1, 1024, 0, s>>>(level, max_slots, seg, route_cur, route_prev, pair_parent, seg_next, p.pairs,
-                                        p.tile_start, p.st);
+  pair_routes_kernel<<<1, 1024, 0, s>>>(level, max_slots, seg, route_cur, route_prev, pair_parent, seg_next, floc,
+                                        p.pairs, p.tile_start, p.st);
   count_launches();
   pair_count_kernel<<<p.max_tiles, kMvThreads, 0, s>>>(bins_rb_in, pitch, p.pairs, p.tile_start, p.st, p.tile_cnt);
   count_launches();
   pair_scan_kernel<<<1, 1024, 0, s>>>(p.pairs, p.tile_start, p.st, p.tile_cnt, p.tile_excl, err);
   count_launches();
   pair_move_kernel<<<p.max_tiles, kMvThreads, 0, s>>>(
-      map_in, bins_rb_out, pitch, bins_rb_in, F, reinterpret_cast<const uint64_t*>(g_in),
+      map_in, bins_rb_out, pitch, bins_rb_in, S, reinterpret_cast<const uint64_t*>(g_in),
       reinterpret_cast<uint64_t*>(g_out), orig_in, orig_out, p.pairs, p.tile_start, p.st, p.tile_excl, leaf_of_row,
       err);
   count_launches();
 }
 
-void launch_leaf_pairs(const uint8_t* bins_rb, int64_t pitch, int64_t N, const uint32_t* orig_in,
-                       const gbdt_level* level, int32_t max_slots, const gbdt_segment* seg, const Route* route_cur,
-                       const Route* route_prev, const int32_t* pair_parent, const gbdt_segment* seg_next,
-                       uint16_t* leaf_of_row, void* scratch, cudaStream_t s) {
+void launch_leaf_pairs(const uint8_t* bins_rb, int64_t pitch, const uint32_t* floc, int64_t N,
+                       const uint32_t* orig_in, const gbdt_level* level, int32_t max_slots, const gbdt_segment* seg,
+                       const Route* route_cur, const Route* route_prev, const int32_t* pair_parent,
+                       const gbdt_segment* seg_next, uint16_t* leaf_of_row, void* scratch, cudaStream_t s) {
   const PairScratch p = carve_pairs(scratch, N, max_slots);
-  pair_routes_kernel<<<1, 1024, 0, s>>>(level, max_slots, seg, route_cur, route_prev, pair_parent, seg_next, p.pairs,
-                                        p.tile_start, p.st);
+  pair_routes_kernel<<<1, 1024, 0, s>>>(level, max_slots, seg, route_cur, route_prev, pair_parent, seg_next, floc,
+                                        p.pairs, p.tile_start, p.st);
   count_launches();
   pair_leaves_kernel<<<p.max_tiles, kMvThreads, 0, s>>>(bins_rb, pitch, orig_in, p.pairs, p.tile_start, p.st,
                                                         leaf_of_row);
   count_launches();
 }
 
-size_t row_block_bytes(int64_t N, int32_t F) { return static_cast<size_t>(rb_blocks(N)) * rb_pitch(F); }
+size_t row_block_bytes(int64_t N, int32_t S) { return static_cast<size_t>(rb_blocks(N)) * rb_pitch(S); }
 
-void launch_cols_to_row_blocks(const uint8_t* cols, int64_t ldb, int64_t N, int32_t F, uint8_t* rb, cudaStream_t s) {
-  const int64_t pieces = rb_blocks(N) * F;
+void launch_cols_to_row_blocks(const uint8_t* cols, int64_t ldb, int64_t N, int32_t S, const uint32_t* slot_src,
+                               const int32_t* n_bins, uint8_t* rb, int32_t* err, cudaStream_t s) {
+  const int64_t pieces = rb_blocks(N) * S;
   const int grid = static_cast<int>(std::min<int64_t>((pieces + 255) / 256, static_cast<int64_t>(sm_count()) * 16));
-  cols_to_row_blocks_kernel<<<grid, 256, 0, s>>>(cols, ldb, rb_blocks(N), F, rb, rb_pitch(F));
+  cols_to_row_blocks_kernel<<<grid, 256, 0, s>>>(cols, ldb, N, rb_blocks(N), S, slot_src, n_bins, rb, rb_pitch(S),
+                                                 err);
   count_launches();
 }
 
+int plan_row_block_slots(const int32_t* n_bins, int32_t F, bool pack, uint32_t* loc, uint32_t* src) {
+  int S = 0, open = -1;  // open: the slot whose low nibble holds an unpaired feature
+  for (int f = 0; f < F; ++f) {
+    if (pack && n_bins[f] <= kMaxPackedBins) {
+      if (open >= 0) {
+        loc[f] = static_cast<uint32_t>(open) | (2u << 16);
+        src[open] = (src[open] & 0xffffu) | (static_cast<uint32_t>(f) << 16);
+        open = -1;
+        continue;
+      }
+      open = S;
+      loc[f] = static_cast<uint32_t>(S) | (1u << 16);
+    } else {
+      loc[f] = static_cast<uint32_t>(S);
+    }
+    src[S++] = static_cast<uint32_t>(f) | 0xffff0000u;
+  }
+  if (open >= 0) loc[src[open] & 0xffffu] = static_cast<uint32_t>(open);  // unpaired: a whole byte
+  return S;
+}
+
 // The tensor map the pair move reads a row-block buffer through: a 3-D byte tensor (32 bytes of a
-// row block, F features, the row blocks) and a box of one feature over kMvBoxBlocks row blocks.
-int make_row_block_map(CUtensorMap* map, const uint8_t* rb, int64_t N, int32_t F) {
+// row block, S slots, the row blocks) and a box of one slot over kMvBoxBlocks row blocks.
+int make_row_block_map(CUtensorMap* map, const uint8_t* rb, int64_t N, int32_t S) {
   using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                    const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                    CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
@@ -1448,9 +1539,9 @@ int make_row_block_map(CUtensorMap* map, const uint8_t* rb, int64_t N, int32_t F
     set_error("tensor-map encoding is not available from the CUDA driver");
     return GBDT_ERR_CUDA;
   }
-  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kRowBlock), static_cast<cuuint64_t>(F),
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kRowBlock), static_cast<cuuint64_t>(S),
                               static_cast<cuuint64_t>(rb_blocks(N))};
-  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kRowBlock), static_cast<cuuint64_t>(rb_pitch(F))};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kRowBlock), static_cast<cuuint64_t>(rb_pitch(S))};
   const cuuint32_t box[3] = {static_cast<cuuint32_t>(kRowBlock), 1u, static_cast<cuuint32_t>(kMvBoxBlocks)};
   const cuuint32_t elem[3] = {1u, 1u, 1u};
   const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t*>(rb), dims, strides, box, elem,
@@ -1473,6 +1564,18 @@ extern "C" size_t gbdt_histograms_segmented_workspace_size(int32_t max_slots) {
 
 extern "C" int64_t gbdt_row_block_pitch(int32_t F) { return F >= 1 ? rb_pitch(F) : 0; }
 
+extern "C" int32_t gbdt_row_block_slots(const int32_t* n_bins, int32_t F, int32_t packing, uint32_t* loc,
+                                        uint32_t* src) {
+  clear_error();
+  GBDT_CHECK_ARG(n_bins && loc && src, "gbdt_row_block_slots: null pointer");
+  GBDT_CHECK_ARG(F >= 1 && F <= 4096, "gbdt_row_block_slots: F out of range");
+  GBDT_CHECK_ARG(packing == GBDT_BIN_PACKING_4BIT || packing == GBDT_BIN_PACKING_OFF,
+                 "gbdt_row_block_slots: bad packing mode");
+  for (int f = 0; f < F; ++f)
+    GBDT_CHECK_ARG(n_bins[f] >= 1 && n_bins[f] <= GBDT_MAX_BINS, "gbdt_row_block_slots: n_bins[%d] out of range", f);
+  return plan_row_block_slots(n_bins, F, packing == GBDT_BIN_PACKING_4BIT, loc, src);
+}
+
 extern "C" size_t gbdt_row_block_bytes(int64_t N, int32_t F) {
   return (N >= 1 && F >= 1) ? row_block_bytes(N, F) : 0;
 }
@@ -1484,7 +1587,7 @@ extern "C" int gbdt_bins_to_row_blocks(const uint8_t* bins, int64_t ldb, int64_t
   GBDT_CHECK_ARG(N >= 1 && N < (int64_t(1) << 31) && F >= 1 && F <= 4096, "gbdt_bins_to_row_blocks: sizes out of range");
   GBDT_CHECK_ARG(ldb >= N && ldb % 16 == 0 && aligned(bins, 16) && aligned(out, 32),
                  "gbdt_bins_to_row_blocks: need ldb >= N, ldb %% 16 == 0, 16-byte aligned bins, 32-byte aligned out");
-  launch_cols_to_row_blocks(bins, ldb, N, F, out, static_cast<cudaStream_t>(stream));
+  launch_cols_to_row_blocks(bins, ldb, N, F, nullptr, nullptr, out, nullptr, static_cast<cudaStream_t>(stream));
   GBDT_LAUNCH_CHECK();
   return GBDT_OK;
 }

@@ -243,6 +243,8 @@ struct TrainWs {
   uint32_t* orig0;    // identity: original row id of level-0 positions
   uint16_t* leaf;     // leaf of each original row in the current tree
   uint8_t* bins_rb0;    // the caller's bins in the row-block layout (levels 0 and 1)
+  uint32_t* floc;       // [F] where each feature's bins sit in the row-block copies (slot, nibble)
+  uint32_t* slot_src;   // [F] the features of each slot
   uint8_t* bins_xy[2];  // row-block copies in later orders (alternating)
   double* g_xy[2];
   uint32_t* orig_xy[2];
@@ -288,6 +290,8 @@ TrainWs carve_train(void* ws, size_t bytes, int64_t N, int32_t F, int64_t ldb, c
   w.g0 = c.take<double>(n16);
   w.orig0 = c.take<uint32_t>(n16);
   w.leaf = c.take<uint16_t>(n16);
+  w.floc = c.take<uint32_t>(F);
+  w.slot_src = c.take<uint32_t>(F);
   if (D >= 1) {
     w.bins_rb0 = c.take<uint8_t>(row_block_bytes(N, F));
     for (int i = 0; i < 2; ++i) {
@@ -422,15 +426,21 @@ extern "C" int gbdt_train(const uint8_t* bins, int64_t ldb, const int32_t* n_bin
   launch_label_mean(w.label_partials, N, w.init, logistic, s);
   iota_kernel<<<sm_count() * 4, 256, 0, s>>>(w.orig0, N);
   count_launches();
-  // the training levels read the bins in the row-block layout; the pair moves read them through
-  // tensor maps (one per buffer: the converted input and the two alternating orders)
-  const int64_t pitch = rb_pitch(F);
+  // the training levels read the bins in the row-block layout, features with at most 16 bins two per
+  // byte (4-bit slots); the pair moves read them through tensor maps (one per buffer: the converted
+  // input and the two alternating orders)
+  std::vector<uint32_t> h_loc(F), h_src(F);
+  const int S = plan_row_block_slots(hb.data(), F, p->bin_packing == GBDT_BIN_PACKING_4BIT, h_loc.data(),
+                                     h_src.data());
+  const int64_t pitch = rb_pitch(S);
   CUtensorMap maps[3];
   if (D >= 1) {
-    launch_cols_to_row_blocks(bins, ldb, N, F, w.bins_rb0, s);
+    GBDT_CUDA(cudaMemcpyAsync(w.floc, h_loc.data(), sizeof(uint32_t) * F, cudaMemcpyHostToDevice, s));
+    GBDT_CUDA(cudaMemcpyAsync(w.slot_src, h_src.data(), sizeof(uint32_t) * S, cudaMemcpyHostToDevice, s));
+    launch_cols_to_row_blocks(bins, ldb, N, S, w.slot_src, n_bins, w.bins_rb0, w.err, s);
     const uint8_t* bufs[3] = {w.bins_rb0, w.bins_xy[0], w.bins_xy[1]};
     for (int i = 0; i < 3; ++i) {
-      rc = make_row_block_map(&maps[i], bufs[i], N, F);
+      rc = make_row_block_map(&maps[i], bufs[i], N, S);
       if (rc != GBDT_OK) return rc;
     }
   }
@@ -477,7 +487,7 @@ extern "C" int gbdt_train(const uint8_t* bins, int64_t ldb, const int32_t* n_bin
         }
         rc = launch_seg_histograms(plan, lb, pitch, N, F, lg, GBDT_DTYPE_F64, w.fixed_exp, w.level[cur], max_slots,
                                    w.build[cur], hseg, hfil, w.seg_scratch, w.hist_cnt[cur], w.hist_q[cur],
-                                   w.hist_h[cur], s, true);
+                                   w.hist_h[cur], s, true, w.floc);
         if (rc != GBDT_OK) return rc;
         if (timing) GBDT_CUDA(cudaEventRecord(ev_hist(t, d, 1), s));
         if (d > 0) {
@@ -500,18 +510,19 @@ extern "C" int gbdt_train(const uint8_t* bins, int64_t ldb, const int32_t* n_bin
       if (d < D && d + 1 < D) {
         if (odd) {
           const int out = ((d + 1) >> 1) - 1 & 1;
-          launch_move_pairs(maps[ph + 1], lb, w.bins_xy[out], pitch, N, F, lg, w.g_xy[out], lo, w.orig_xy[out],
+          launch_move_pairs(maps[ph + 1], lb, w.bins_xy[out], pitch, w.floc, N, S, lg, w.g_xy[out], lo,
+                            w.orig_xy[out],
                             w.level[cur], max_slots, w.seg[cur], w.route[cur], w.route[nxt], w.pair_parent[cur],
                             w.seg[nxt], w.leaf, w.move_scratch, w.err, s);
         } else {
-          launch_leaf_rows(lb, pitch, N, lo, w.level[cur], max_slots, w.seg[cur], w.route[cur], true, w.leaf,
+          launch_leaf_rows(lb, pitch, w.floc, N, lo, w.level[cur], max_slots, w.seg[cur], w.route[cur], true, w.leaf,
                            w.move_scratch, s);
         }
       } else if (d + 1 == D && odd) {
-        launch_leaf_pairs(lb, pitch, N, lo, w.level[cur], max_slots, w.seg[cur], w.route[cur], w.route[nxt],
+        launch_leaf_pairs(lb, pitch, w.floc, N, lo, w.level[cur], max_slots, w.seg[cur], w.route[cur], w.route[nxt],
                           w.pair_parent[cur], w.seg[nxt], w.leaf, w.move_scratch, s);
       } else if (d + 1 == D || D == 0) {
-        launch_leaf_rows(lb, pitch, N, lo, w.level[cur], max_slots, w.seg[cur], w.route[cur], false, w.leaf,
+        launch_leaf_rows(lb, pitch, w.floc, N, lo, w.level[cur], max_slots, w.seg[cur], w.route[cur], false, w.leaf,
                          w.move_scratch, s);
       }
       if (timing) GBDT_CUDA(cudaEventRecord(ev_hist(t, d, 3), s));
@@ -550,6 +561,10 @@ extern "C" int gbdt_train(const uint8_t* bins, int64_t ldb, const int32_t* n_bin
   GBDT_CUDA(cudaMemcpyAsync(&h_err, w.err, sizeof(int32_t), cudaMemcpyDeviceToHost, s));
   GBDT_CUDA(cudaMemcpyAsync(&h_init, w.init, sizeof(double), cudaMemcpyDeviceToHost, s));
   GBDT_CUDA(cudaStreamSynchronize(s));
+  if (h_err & kErrBinRange) {
+    set_error("gbdt_train: a bin is not below its feature's n_bins");
+    return GBDT_ERR_INVALID_ARG;
+  }
   if (h_err != 0) {
     set_error("gbdt_train: device consistency check failed (error bits 0x%x)", h_err);
     return GBDT_ERR_INTERNAL;
@@ -583,8 +598,8 @@ extern "C" int gbdt_train(const uint8_t* bins, int64_t ldb, const int32_t* n_bin
     float ms = 0.f;
     GBDT_CUDA(cudaEventElapsedTime(&ms, pool.ev[0], pool.ev[1]));
     dg.total_ms = ms;
-    const double row_bytes = static_cast<double>(F) + 8.0;       // a scanned row: bins + fp64 g
-    const double move_bytes = 2.0 * (F + 8.0 + 4.0);             // a moved row: read + write every column
+    const double row_bytes = static_cast<double>(S) + 8.0;       // a scanned row: bins (slots) + fp64 g
+    const double move_bytes = 2.0 * (S + 8.0 + 4.0);             // a moved row: read + write every slot
     for (int t = 0; t < T; ++t) {
       for (int d = 0; d <= D; ++d) {
         const LevelStats& ls = h_stats[static_cast<size_t>(t) * (D + 1) + d];

@@ -90,7 +90,15 @@ typedef struct gbdt_params {
                                node index asc) split and their children are leaves (the ExaBoost page's
                                depth-capped final partial level).  1 is invalid. */
   int32_t objective;        /* GBDT_OBJECTIVE_SQUARED_ERROR (0) or GBDT_OBJECTIVE_LOGISTIC (1) */
-} gbdt_params; /* 56 bytes */
+  int32_t bin_packing;      /* GBDT_BIN_PACKING_4BIT (0): in gbdt_train's internal copies of the bins,
+                               features with n_bins <= 16 are stored two per byte (4 bits each, the
+                               ExaBoost page's packed bins); GBDT_BIN_PACKING_OFF (1): one byte each.
+                               Results are identical either way. */
+  int32_t reserved;         /* 0 */
+} gbdt_params; /* 64 bytes */
+
+#define GBDT_BIN_PACKING_4BIT 0
+#define GBDT_BIN_PACKING_OFF 1
 
 /* One tree node, "Module Design: Training Core" s.3 Tree Model: feature,
  * threshold bin, child indices, leaf value, gain and a leaf flag.  Trees are
@@ -285,6 +293,18 @@ int gbdt_subtract_histograms_h(const uint32_t* prev_cnt, const int64_t* prev_q, 
  * gbdt_bins_to_row_blocks converts column-major bins [F][ldb] (asynchronous);
  * bytes of the last row block past N are copied as they are. */
 int64_t gbdt_row_block_pitch(int32_t F);
+
+/* gbdt_row_block_slots (HOST only, no GPU): the slots of gbdt_train's internal
+ * row-block copies for features with n_bins [F] (host) and a GBDT_BIN_PACKING_*
+ * mode.  With GBDT_BIN_PACKING_4BIT, features with n_bins <= 16 pair up in
+ * feature order in one 32-byte slot, the first of a pair in the low nibble of
+ * each byte and the second in the high nibble (a last unpaired one keeps a whole
+ * byte); every other feature has a slot of its own, slots numbered in the order
+ * of their first feature.  loc [F] (host) receives slot | nibble << 16 (nibble
+ * 0: whole byte, 1: low, 2: high); src [F] (host) receives, for each slot s <
+ * the returned count, first feature | second feature << 16 (0xffff: none).
+ * Returns the slot count (pitch = 32 x slots), or GBDT_ERR_INVALID_ARG. */
+int32_t gbdt_row_block_slots(const int32_t* n_bins, int32_t F, int32_t packing, uint32_t* loc, uint32_t* src);
 size_t gbdt_row_block_bytes(int64_t N, int32_t F);
 int gbdt_bins_to_row_blocks(const uint8_t* bins, int64_t ldb, int64_t N, int32_t F, uint8_t* out, void* stream);
 
@@ -430,7 +450,8 @@ int gbdt_predict(const float* X, int64_t ldx, int64_t N, int32_t F, const float*
 
 /* ---------------------------------------------------------------------------
  * gbdt_train: whole training run ("Module Design: Training Core" s.6).
- *   bins [F][ldb] uint8, n_bins [F] int32 (1..256), label [N] fp32 (device)
+ *   bins [F][ldb] uint8, n_bins [F] int32 (1..256), label [N] fp32 (device);
+ *     every bin of feature j must be below n_bins[j] (checked: GBDT_ERR_INVALID_ARG)
  *   p: host pointer
  *   pred_out [N] fp64 (device): predictions (margins) after the last tree
  *   init_pred_out: host double, the initial prediction: mean(label) for

@@ -62,7 +62,8 @@ def test_parameter_rules_on_host(lib):
     assert g.validate_params(n_trees=1, max_depth=3) == g.OK
     for bad in (dict(min_samples_leaf=0), dict(min_child_weight=-1.0), dict(reg_lambda=-0.1), dict(gamma=-1.0),
                 dict(learning_rate=float("nan")), dict(reg_lambda=float("inf")), dict(max_depth=13),
-                dict(n_trees=-1), dict(objective=2), dict(objective=-1), dict(num_leaves=1)):
+                dict(n_trees=-1), dict(objective=2), dict(objective=-1), dict(num_leaves=1),
+                dict(bin_packing=2)):
         assert g.validate_params(**bad) == g.ERR_INVALID_ARG, bad
         assert lib.gbdt_last_error() != b""
     assert g.validate_params(objective=g.OBJECTIVE_LOGISTIC) == g.OK
@@ -71,7 +72,7 @@ def test_parameter_rules_on_host(lib):
 def test_struct_layouts_match_header():
     import histogram_gradient_boosted_gb300 as g
 
-    assert ctypes.sizeof(g.Params) == 56 and g.Params.objective.offset == 52
+    assert ctypes.sizeof(g.Params) == 64 and g.Params.objective.offset == 52 and g.Params.bin_packing.offset == 56
     assert g.NODE_DTYPE.itemsize == 40 and g.SPLIT_DTYPE.itemsize == 56
     assert g.SPLIT_DTYPE.fields["h_left"][1] == 40 and g.SPLIT_DTYPE.fields["h_total"][1] == 48
     assert g.LEVEL_DTYPE.itemsize == 8 and g.SEGMENT_DTYPE.itemsize == 16
@@ -91,3 +92,34 @@ def test_entry_points_reject_bad_arguments_before_any_launch(lib):
     assert lib.gbdt_subtract_histograms_h(None, None, None, None, None, None, 0, 0, None, None, None, None) == -1
     assert lib.gbdt_compute_gradients_objective(None, None, 0, 1, None, None, None, 0, None) == -1
     assert b"null pointer" in lib.gbdt_last_error()
+
+
+def test_row_block_slot_plan_on_host(lib):
+    """4-bit slots: features with <= 16 bins pair up in feature order (low nibble first), an unpaired
+    one keeps a whole byte, the rest have slots of their own, numbered by their first feature."""
+    import numpy as np
+
+    import histogram_gradient_boosted_gb300 as g
+
+    nb = [256, 16, 3, 17, 2, 255, 16, 2, 9]
+    loc, src = g.row_block_slots(nb)
+    slot, nib = loc & 0xFFFF, loc >> 16
+    # slots: 0 <- f0; 1 <- f1 (low) + f2 (high); 2 <- f3; 3 <- f4 (low) + f6 (high); 4 <- f5;
+    #        5 <- f7 (low) + f8 (high)
+    assert list(slot) == [0, 1, 1, 2, 3, 4, 3, 5, 5] and list(nib) == [0, 1, 2, 0, 1, 0, 2, 1, 2]
+    assert list(src & 0xFFFF) == [0, 1, 3, 4, 5, 7] and list(src >> 16) == [0xFFFF, 2, 0xFFFF, 6, 0xFFFF, 8]
+    loc, src = g.row_block_slots([2, 2, 2])  # an odd count: the last one keeps a whole byte
+    assert list(loc & 0xFFFF) == [0, 0, 1] and list(loc >> 16) == [1, 2, 0] and len(src) == 2
+    loc, src = g.row_block_slots(nb, packing=g.BIN_PACKING_OFF)
+    assert list(loc) == list(range(len(nb))) and list(src) == [f | 0xFFFF0000 for f in range(len(nb))]
+    # every feature is stored exactly once
+    rng = np.random.default_rng(0)
+    for _ in range(20):
+        nb = rng.choice([2, 5, 16, 17, 200, 256], size=rng.integers(1, 300))
+        loc, src = g.row_block_slots(nb)
+        seen = sorted([int(s & 0xFFFF) for s in src] + [int(s >> 16) for s in src if s >> 16 != 0xFFFF])
+        assert seen == list(range(len(nb)))
+        assert all((l >> 16) == 0 or nb[i] <= 16 for i, l in enumerate(loc))
+        assert len(src) == len(nb) - sum(1 for s in src if s >> 16 != 0xFFFF)
+    with pytest.raises(g.GbdtError):
+        g.row_block_slots([0, 3])

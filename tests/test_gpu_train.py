@@ -144,3 +144,50 @@ def test_leaf_budget_matches_oracle(name, n, depth, budget, trees):
 def test_leaf_budget_of_one_is_rejected():
     assert g.validate_params(num_leaves=1) == g.ERR_INVALID_ARG
     assert g.validate_params(num_leaves=0) == g.OK and g.validate_params(num_leaves=2) == g.OK
+
+
+def _mixed_cardinality(n, seed=5):
+    """Columns with 2..17 distinct values in an irregular order among continuous ones."""
+    rng = np.random.default_rng(seed)
+    ks = [2, 3, 300, 16, 17, 5, 2, 256, 9, 16, 4, 1000, 2, 7, 15, 3, 2, 40, 11]
+    X = np.empty((len(ks), n), np.float32)
+    for j, k in enumerate(ks):
+        X[j] = rng.integers(0, k, n) if k <= 300 else rng.standard_normal(n)
+    y = (X[0] * 2 - X[3] * 0.3 + np.sin(X[11]) + 0.5 * (X[9] > 7) + rng.normal(0, 0.3, n)).astype(np.float32)
+    return X, y
+
+
+@pytest.mark.parametrize("case", ["covtype", "large", "mixed", "mixed_logistic"])
+def test_4bit_slots_give_identical_training(case):
+    """Features with <= 16 bins stored two per byte in the training copies: the same model, bit for
+    bit, as one byte per feature, with fewer bytes read; and the oracle's model."""
+    if case in ("covtype", "large"):
+        bins, n_bins, yd, ob, on, y = _prepare(case, 30_011)
+        params = dict(synth.CONFIGS[case], n_trees=3)
+    else:
+        X, y = _mixed_cardinality(25_013)
+        if case == "mixed_logistic":
+            y = synth.binary_label(y)
+        bins, _, n_bins = g.quantize(torch.from_numpy(X).cuda(), 255)
+        ob, _, on = oracle.quantize(X, 255)
+        yd = torch.from_numpy(y).cuda()
+        params = dict(n_trees=4, max_depth=7, learning_rate=0.2, reg_lambda=1.0, gamma=0.0, min_samples_leaf=3,
+                      min_child_weight=0.0, objective=1 if case == "mixed_logistic" else 0)
+    assert int((n_bins <= 16).sum()) >= 2
+    a = g.train(bins, n_bins, yd, diagnostics=True, bin_packing=g.BIN_PACKING_4BIT, **params)
+    b = g.train(bins, n_bins, yd, diagnostics=True, bin_packing=g.BIN_PACKING_OFF, **params)
+    assert a["nodes"].tobytes() == b["nodes"].tobytes()
+    assert torch.equal(a["pred"], b["pred"])
+    assert a["diag"]["hist_bytes"] < b["diag"]["hist_bytes"] and a["diag"]["part_bytes"] < b["diag"]["part_bytes"]
+    compare_training(a, ob, on, y, params)
+
+
+def test_bins_beyond_n_bins_are_rejected():
+    bins, n_bins, yd, *_ = _prepare("large", 5_003)
+    nb = n_bins.cpu().numpy()
+    for f in (int(np.argmax(nb <= 16)), 0):  # a 4-bit feature and a whole-byte one
+        bad = n_bins.clone()
+        bad[f] -= 1
+        with pytest.raises(g.GbdtError) as e:
+            g.train(bins, bad, yd, **dict(synth.CONFIGS["large"], n_trees=1, max_depth=3))
+        assert e.value.code == g.ERR_INVALID_ARG and "n_bins" in str(e.value)
