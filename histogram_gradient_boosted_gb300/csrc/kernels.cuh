@@ -72,7 +72,7 @@ struct Route {
 struct SegHistPlan {
   int n_fgroups, group_feats;
   int max_ctas;      // CTAs per feature group (one wave over the SMs)
-  int64_t min_rows;  // fewest rows a CTA takes when the level is small
+  int64_t min_rows;  // least work (rows + a fixed cost per slot) a CTA takes when the level is small
   bool with_h;       // logistic: H histograms too (h = logistic_hess(g), exponent fixed_exp[1])
   size_t smem;
 };

@@ -31,15 +31,22 @@ namespace {
 constexpr int kSegThreads = 1024;
 constexpr int kSegMaxFeats = 64;  // features per CTA (64 x 256 x 12 B = 192 KB of shared memory)
 
+// The work of a level is cut by cost: every built slot costs its rows plus kSlotCost, the
+// fixed work of taking up a slot (the dependent loads of its first rows, two barriers and the
+// flush of the CTA's shared histograms, about what 128 rows of updates take).  Cutting by rows
+// alone put a run of many tiny slots (deep levels) on one CTA, which then took them one by one.
+constexpr int64_t kSlotCost = 128;
+
 struct SegWork {
   int64_t total_rows;  // rows over all built slots
+  int64_t total_cost;  // total_rows + kSlotCost x n_built
   int32_t n_built;     // built slots
-  int32_t ctas;        // CTAs per feature group that have rows
+  int32_t ctas;        // CTAs per feature group that have work
 };
 
 // One CTA: compact list of built slots, the prefix of their row counts, and
-// how many CTAs per feature group share the rows (at most max_ctas, and no
-// fewer than min_rows rows each).
+// how many CTAs per feature group share the work (at most max_ctas, and no
+// less than min_rows of cost each).
 __global__ void seg_work_setup_kernel(const gbdt_level* __restrict__ level, int32_t max_slots,
                                       const uint8_t* __restrict__ build_flag, const gbdt_segment* __restrict__ seg,
                                       int32_t max_ctas, int64_t min_rows, int32_t* __restrict__ build_slot,
@@ -81,9 +88,11 @@ __global__ void seg_work_setup_kernel(const gbdt_level* __restrict__ level, int3
   }
   if (threadIdx.x == 0) {
     row_start[s_pre_slots] = s_pre_rows;
+    const long long cost = s_pre_rows + kSlotCost * s_pre_slots;
     st->total_rows = s_pre_rows;
+    st->total_cost = cost;
     st->n_built = s_pre_slots;
-    const long long by_size = (s_pre_rows + min_rows - 1) / min_rows;
+    const long long by_size = (cost + min_rows - 1) / min_rows;
     st->ctas = static_cast<int32_t>(by_size < max_ctas ? by_size : max_ctas);
   }
 }
@@ -374,14 +383,16 @@ __global__ void __launch_bounds__(kSegThreads, 1)
   const int f_lo = blockIdx.y * group_feats;
   const int nf = min(group_feats, F - f_lo);
   if (nf <= 0) return;
-  const int64_t total = st->total_rows;
-  const int64_t lo = total * blockIdx.x / ctas, hi = total * (blockIdx.x + 1) / ctas;
-  if (lo >= hi) return;
+  // this CTA's share [xlo, xhi) of the cost line: built slot j covers [row_start[j] + kSlotCost * j,
+  // row_start[j + 1] + kSlotCost * (j + 1)), its rows first, its fixed cost after them
+  const int64_t total = st->total_cost;
+  const int64_t xlo = total * blockIdx.x / ctas, xhi = total * (blockIdx.x + 1) / ctas;
+  if (xlo >= xhi) return;
   const int n_built = st->n_built;
-  int k = 0, kh = n_built - 1;  // last built slot whose first row <= lo
+  int k = 0, kh = n_built - 1;  // last built slot whose cost range starts at or before xlo
   while (k < kh) {
     const int mid = (k + kh + 1) >> 1;
-    if (row_start[mid] <= lo) k = mid;
+    if (row_start[mid] + kSlotCost * mid <= xlo) k = mid;
     else kh = mid - 1;
   }
   const double scale = ldexp(1.0, fixed_exp[0]);
@@ -414,10 +425,14 @@ __global__ void __launch_bounds__(kSegThreads, 1)
       sh[h] = loc_shift(loc);
       mk[h] = loc_mask(loc) * 0x01010101u;
     }
-    for (int64_t r = lo; r < hi; ++k) {
-      const int64_t r_end = min(hi, row_start[k + 1]);
+    for (; k < n_built && row_start[k] + kSlotCost * k < xhi; ++k) {
+      // the share's rows of slot k: offsets [o0, o1) of its rows
+      const int64_t c0 = row_start[k] + kSlotCost * k, n_k = row_start[k + 1] - row_start[k];
+      const int64_t o0 = min(max(xlo - c0, int64_t(0)), n_k), o1 = min(xhi - c0, n_k);
+      if (o0 >= o1) continue;  // CTA-uniform: only the slot's fixed cost falls in this share
       const int slot = build_slot[k];
-      const int64_t p0 = seg[slot].start + (r - row_start[k]);
+      const int64_t p0 = seg[slot].start + o0;
+      const int64_t r = 0, r_end = o1 - o0;
       const gbdt_filter fl = filters ? filters[slot] : gbdt_filter{-1, 0, 0, 0};
       const uint32_t floc_f = fl.feature < 0 ? 0u : unpack ? floc[fl.feature] : static_cast<uint32_t>(fl.feature);
       const uint8_t* fcol =
@@ -427,7 +442,6 @@ __global__ void __launch_bounds__(kSegThreads, 1)
       __syncthreads();
       seg_hist_flush<NH, kH>(s_cnt, s_lo, s_hi, slot, F, f_lo, nf, hist_cnt, hist_q, hist_h);
       __syncthreads();
-      r = r_end;
     }
   };
   if constexpr (kH) {
@@ -1307,7 +1321,7 @@ SegHistPlan plan_seg_histograms(int64_t N, int32_t F, int32_t max_slots, int32_t
   p.group_feats = ceil_div(F, p.n_fgroups);
   p.max_ctas = sm_count() / p.n_fgroups;  // one wave: a CTA per SM
   if (p.max_ctas < 1) p.max_ctas = 1;
-  p.min_rows = 4096;
+  p.min_rows = 1024;  // least cost (rows + kSlotCost per slot) per CTA
   p.with_h = with_h;
   const size_t words = with_h ? 5 : 3, stage = with_h ? 512 : 256;  // staged row records per warp
   p.smem = static_cast<size_t>(ceil_div(p.group_feats, 32)) * kHalfWords * 4 * words + (kSegThreads / 32) * stage;

@@ -5,16 +5,21 @@
 // ties to the smaller feature then the smaller bin, invalid candidates never
 // compared, split only on gain > 0, bin <= threshold goes left.
 //
-// One CTA per slot, one warp per feature at a time.  A lane holds 8
-// consecutive bins; the warp forms prefix sums of (count, fixed-point G) with
-// shuffles, screens every threshold in FP32 with a proven error margin, and
-// evaluates the survivors in FP64 with explicitly rounded operations (no
-// contraction), reducing to the best candidate.  The
-// comparison (gain desc, feature asc, bin asc) is a total order on distinct
-// candidates, so the result does not depend on the reduction order.
-// With the logistic objective H comes from the H histograms (fixed point with
-// its own exponent) instead of the row counts; min_samples_leaf still applies
-// to the counts.
+// Two phases.  Screen: one warp per (slot, feature); a lane holds 8
+// consecutive bins, the warp forms prefix sums of (count, fixed-point G) with
+// shuffles and screens every threshold in FP32 with a proven error margin,
+// keeping the few that could reach the feature's maximum.  Select: one CTA per
+// slot applies the same margin across all of the slot's features and
+// evaluates only the survivors in FP64 with explicitly rounded operations (no
+// contraction), reducing under the frozen rule.  FP64 is scarce on this GPU,
+// so a node evaluates one or two thresholds in FP64 instead of one per
+// feature.  The comparison (gain desc, feature asc, bin asc) is a total order
+// on distinct candidates, so the result does not depend on the reduction
+// order.  With the logistic objective H comes from the H histograms (fixed
+// point with its own exponent) instead of the row counts; min_samples_leaf
+// still applies to the counts.
+#include <cmath>
+
 #include "kernels.cuh"
 
 namespace gbdt {
@@ -95,6 +100,44 @@ __device__ __forceinline__ void node_totals(const uint32_t* __restrict__ cnt, co
 // Eight bins of one lane (bins 8 lane .. 8 lane + 7) as inclusive prefix sums
 // within the lane; returns the lane's exclusive offset over the warp and the
 // feature's total (lane 31's inclusive sum) through *total.
+// A threshold that survived its feature's FP32 screen.
+constexpr int kSurv = 4;  // survivors kept per (slot, feature)
+struct Surv {
+  float x;            // its FP32 screening value; -1: empty entry
+  int32_t bin;
+  uint32_t cnt_left;
+  int32_t exact;      // 1: gain holds its FP64 gain (its feature had more than kSurv survivors)
+  int64_t q_left;
+  int64_t qh_left;
+  double gain;
+};
+
+// score of the node: G^2 / (H + lambda) from its fixed-point totals (H = count unless kH).
+template <bool kH>
+__device__ __forceinline__ double node_score(int64_t tot_q, uint32_t tot_cnt, int64_t tot_h, double inv,
+                                             double inv_h, double lambda) {
+  const double GP = static_cast<double>(tot_q) * inv;
+  const double HP = kH ? static_cast<double>(tot_h) * inv_h : static_cast<double>(tot_cnt);
+  return score(GP, HP, lambda);
+}
+
+// FP64 gain of the threshold whose left side holds (qL, cL, qhL) of the node totals, each
+// operation rounded once: 0.5 * ((s_L + s_R) - s_P) - gamma.
+template <bool kH>
+__device__ __forceinline__ double exact_gain(int64_t qL, uint32_t cL, int64_t qhL, int64_t tot_q, uint32_t tot_cnt,
+                                             int64_t tot_h, double inv, double inv_h, double sP, double lambda,
+                                             double gamma) {
+  const uint32_t cR = tot_cnt - cL;
+  const int64_t qR = static_cast<int64_t>(static_cast<uint64_t>(tot_q) - static_cast<uint64_t>(qL));
+  const int64_t qhR = static_cast<int64_t>(static_cast<uint64_t>(tot_h) - static_cast<uint64_t>(qhL));
+  const double HL = kH ? static_cast<double>(qhL) * inv_h : static_cast<double>(cL);
+  const double HR = kH ? static_cast<double>(qhR) * inv_h : static_cast<double>(cR);
+  const double GL = static_cast<double>(qL) * inv;
+  const double GR = static_cast<double>(qR) * inv;
+  const double sL = score(GL, HL, lambda), sR = score(GR, HR, lambda);
+  return __dsub_rn(__dmul_rn(0.5, __dsub_rn(__dadd_rn(sL, sR), sP)), gamma);
+}
+
 template <typename T>
 __device__ __forceinline__ T lane_prefix8(T (&v)[8], int lane, T* total) {
 #pragma unroll
@@ -108,31 +151,28 @@ __device__ __forceinline__ T lane_prefix8(T (&v)[8], int lane, T* total) {
   return x - v[7];
 }
 
-// One warp per (slot, feature): best threshold of that feature.  kH: H from
-// hist_h with exponent fixed_exp[1] (logistic), else H = the row count.
+// Screen: one warp per (slot, feature).  Writes the feature's survivors of the
+// FP32 screen to surv[slot][feature][0 .. kSurv): in bin order, or, when more
+// than kSurv survive (long runs of empty bins can tie), the best of them
+// evaluated in FP64 as one exact entry.  kH: H from hist_h with exponent
+// fixed_exp[1] (logistic), else H = the row count.
 template <bool kH>
 __global__ void __launch_bounds__(kSplitThreads)
     split_features_kernel(const uint32_t* __restrict__ hist_cnt, const int64_t* __restrict__ hist_q,
                           const int64_t* __restrict__ hist_h, const int32_t* __restrict__ fixed_exp, int32_t F,
                           const int32_t* __restrict__ n_bins, const gbdt_level* __restrict__ level, int32_t max_slots,
-                          double lambda, double gamma, int32_t msl, double mcw, Cand* __restrict__ cand,
-                          int32_t* __restrict__ err) {
+                          double lambda, double gamma, int32_t msl, double mcw, int64_t mcw_ceil,
+                          Surv* __restrict__ surv, int32_t* __restrict__ err) {
   const int slot = blockIdx.x;
   const int n_slots = min(level->n_slots, max_slots);
   if (slot >= n_slots) return;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int f = blockIdx.y * kSplitWarps + warp;
-  const int S = fixed_exp[0];
-  const double inv = ldexp(1.0, -S);
-  const double inv_h = kH ? ldexp(1.0, -fixed_exp[1]) : 1.0;
   const int64_t base = static_cast<int64_t>(slot) * F * kBins;
   uint32_t tot_cnt;
   long long tot_q, tot_h;
   node_totals(hist_cnt + base, hist_q + base, kH ? hist_h + base : nullptr, lane, &tot_cnt, &tot_q, &tot_h);
   if (f >= F) return;  // warp-uniform
-  const double GP = static_cast<double>(tot_q) * inv;
-  const double HP = kH ? static_cast<double>(tot_h) * inv_h : static_cast<double>(tot_cnt);
-  const double sP = score(GP, HP, lambda);
 
   const int64_t off = base + static_cast<int64_t>(f) * kBins + lane * 8;
   uint32_t c[8];
@@ -183,9 +223,17 @@ __global__ void __launch_bounds__(kSplitThreads)
   // qhL / qhP >= 2^-62); its conversions and one more division keep it within
   // 20 * 2^-24 relative, far inside the margin.  (lambda / HP beyond FP32's
   // range makes every term 0: every candidate is then kept.)
+  // an integer count c satisfies c >= msl, c >= mcw and c > 0 iff c >= cnt_min; a fixed-point H
+  // qh * 2^-S_h satisfies H >= mcw and H > 0 iff qh >= qh_min (mcw * 2^S_h is exact in FP64)
+  const int64_t cnt_min = max(max(static_cast<int64_t>(msl), int64_t(1)), mcw_ceil);
+  int64_t qh_min = 1;
+  if (kH) {
+    const double m = ceil(ldexp(mcw, fixed_exp[1]));
+    qh_min = m >= 9.2e18 ? INT64_MAX : max(int64_t(1), static_cast<int64_t>(m));
+  }
   const float lam = static_cast<float>(lambda);
   const float hpf = kH ? abs_to_float(tot_h) : 1.0f;
-  const float lamn = kH ? static_cast<float>(lambda / HP) : 0.0f;
+  const float lamn = kH ? static_cast<float>(lambda / (static_cast<double>(tot_h) * ldexp(1.0, -fixed_exp[1]))) : 0.0f;
   float x32[8];
   uint32_t ok = 0;
   float xmax = -1.0f;
@@ -198,12 +246,12 @@ __global__ void __launch_bounds__(kSplitThreads)
     const int64_t qR = static_cast<int64_t>(static_cast<uint64_t>(tot_q) - static_cast<uint64_t>(qL));
     const int64_t qhL = kH ? he + qh[i] : 0;
     const int64_t qhR = kH ? static_cast<int64_t>(static_cast<uint64_t>(tot_h) - static_cast<uint64_t>(qhL)) : 0;
-    const double HL = kH ? static_cast<double>(qhL) * inv_h : static_cast<double>(cL);
-    const double HR = kH ? static_cast<double>(qhR) * inv_h : static_cast<double>(cR);
     x32[i] = 0.0f;
     if (b > nb - 2) continue;
-    if (!(static_cast<int64_t>(cL) >= msl && static_cast<int64_t>(cR) >= msl && HL >= mcw && HR >= mcw &&
-          HL > 0.0 && HR > 0.0))
+    // validity in integers (the FP64 pipe is scarce): H = count, so count >= msl, H >= mcw and H > 0
+    // are count >= cnt_min; with H from its histogram, H >= mcw and H > 0 are qh >= qh_min
+    if (kH ? !(static_cast<int64_t>(cL) >= msl && static_cast<int64_t>(cR) >= msl && qhL >= qh_min && qhR >= qh_min)
+           : !(static_cast<int64_t>(cL) >= cnt_min && static_cast<int64_t>(cR) >= cnt_min))
       continue;
     float x;
     if (kH) {
@@ -222,65 +270,112 @@ __global__ void __launch_bounds__(kSplitThreads)
   }
   for (int o = 16; o > 0; o >>= 1) xmax = fmaxf(xmax, __shfl_xor_sync(0xffffffffu, xmax, o));
   const float keep = xmax - xmax * 1.52587890625e-05f;  // xmax * (1 - 2^-16)
+  uint32_t sv = 0;  // this lane's survivors
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    if ((ok >> i & 1u) && x32[i] >= keep) sv |= 1u << i;
+  const int mine = __popc(sv);
+  int before = mine;  // inclusive prefix over lanes (lanes hold consecutive bins)
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, before, o);
+    if (lane >= o) before += v;
+  }
+  const int total = __shfl_sync(0xffffffffu, before, 31);
+  before -= mine;
+  Surv* out = surv + (static_cast<int64_t>(slot) * F + f) * kSurv;
+  if (total <= kSurv) {
+    int k = before;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      if (!(sv >> i & 1u)) continue;
+      const uint32_t cL = ce + c[i];
+      out[k++] = Surv{x32[i], lane * 8 + i, cL, 0, qe + q[i], kH ? he + qh[i] : 0, 0.0};
+    }
+    if (lane >= total && lane < kSurv) out[lane] = Surv{-1.0f, -1, 0, 0, 0, 0, 0.0};
+    return;
+  }
+  // more survivors than entries: evaluate them all in FP64 here and keep the best
+  const double inv = ldexp(1.0, -fixed_exp[0]), inv_h = kH ? ldexp(1.0, -fixed_exp[1]) : 1.0;
+  const double sP = node_score<kH>(tot_q, tot_cnt, tot_h, inv, inv_h, lambda);
   Cand lb{-INFINITY, -1, -1, 0, 0, 0};
+  float lx = -1.0f;
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    if (!(ok >> i & 1u) || x32[i] < keep) continue;
-    const int b = lane * 8 + i;
+    if (!(sv >> i & 1u)) continue;
     const uint32_t cL = ce + c[i];
-    const int64_t qL = qe + q[i];
-    const uint32_t cR = tot_cnt - cL;
-    const int64_t qR = static_cast<int64_t>(static_cast<uint64_t>(tot_q) - static_cast<uint64_t>(qL));
-    const int64_t qhL = kH ? he + qh[i] : 0;
-    const int64_t qhR = kH ? static_cast<int64_t>(static_cast<uint64_t>(tot_h) - static_cast<uint64_t>(qhL)) : 0;
-    const double HL = kH ? static_cast<double>(qhL) * inv_h : static_cast<double>(cL);
-    const double HR = kH ? static_cast<double>(qhR) * inv_h : static_cast<double>(cR);
-    const double GL = static_cast<double>(qL) * inv;
-    const double GR = static_cast<double>(qR) * inv;
-    const double sL = score(GL, HL, lambda), sR = score(GR, HR, lambda);
-    const double gain = __dsub_rn(__dmul_rn(0.5, __dsub_rn(__dadd_rn(sL, sR), sP)), gamma);
-    if (lb.feature < 0 || gain > lb.gain) lb = Cand{gain, f, b, cL, qL, qhL};
+    const int64_t qL = qe + q[i], qhL = kH ? he + qh[i] : 0;
+    const double gain = exact_gain<kH>(qL, cL, qhL, tot_q, tot_cnt, tot_h, inv, inv_h, sP, lambda, gamma);
+    if (lb.feature < 0 || gain > lb.gain) lb = Cand{gain, f, lane * 8 + i, cL, qL, qhL}, lx = x32[i];
   }
   for (int o = 16; o > 0; o >>= 1) {
-    Cand other = shfl_cand(lb, lane ^ o);
-    if (better(other, lb)) lb = other;
+    const Cand other = shfl_cand(lb, lane ^ o);
+    const float ox = __shfl_xor_sync(0xffffffffu, lx, o);
+    if (better(other, lb)) lb = other, lx = ox;
   }
-  if (lane == 0) cand[static_cast<int64_t>(slot) * F + f] = lb;
+  if (lane == 0) out[0] = Surv{lx, lb.bin, lb.cnt_left, 1, lb.q_left, lb.qh_left, lb.gain};
+  if (lane >= 1 && lane < kSurv) out[lane] = Surv{-1.0f, -1, 0, 0, 0, 0, 0.0};
 }
 
-// One CTA per slot: reduce the per-feature candidates under the frozen rule.
+// Select: one CTA per slot.  The FP32 margin holds across the slot's features (x is the same
+// monotone proxy of the gain everywhere in a node), so only survivors within it of the largest
+// screening value of the slot are evaluated in FP64 (exact entries carry their gain), then reduced
+// under the frozen rule.
+template <bool kH>
 __global__ void __launch_bounds__(kSplitThreads)
     split_reduce_kernel(const uint32_t* __restrict__ hist_cnt, const int64_t* __restrict__ hist_q,
-                        const int64_t* __restrict__ hist_h, int32_t F, const gbdt_level* __restrict__ level,
-                        int32_t max_slots, const Cand* __restrict__ cand, gbdt_split* __restrict__ out) {
+                        const int64_t* __restrict__ hist_h, const int32_t* __restrict__ fixed_exp, int32_t F,
+                        const gbdt_level* __restrict__ level, int32_t max_slots, double lambda, double gamma,
+                        const Surv* __restrict__ surv, gbdt_split* __restrict__ out) {
   const int slot = blockIdx.x;
   const int n_slots = min(level->n_slots, max_slots);
   if (slot >= n_slots) return;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   __shared__ Cand s_best[kSplitWarps];
+  __shared__ float s_x[kSplitWarps];
   __shared__ uint32_t s_tc;
   __shared__ long long s_tq, s_th;
-  Cand best{-INFINITY, -1, -1, 0, 0, 0};
-  for (int f = threadIdx.x; f < F; f += blockDim.x) {
-    const Cand c = cand[static_cast<int64_t>(slot) * F + f];
-    if (better(c, best)) best = c;
-  }
-  for (int o = 16; o > 0; o >>= 1) {
-    Cand other = shfl_cand(best, lane ^ o);
-    if (better(other, best)) best = other;
-  }
-  if (lane == 0) s_best[warp] = best;
+  const Surv* sv = surv + static_cast<int64_t>(slot) * F * kSurv;
+  const int n = F * kSurv;
+  float xmax = -1.0f;
+  for (int e = threadIdx.x; e < n; e += blockDim.x) xmax = fmaxf(xmax, sv[e].x);
+  for (int o = 16; o > 0; o >>= 1) xmax = fmaxf(xmax, __shfl_xor_sync(0xffffffffu, xmax, o));
+  if (lane == 0) s_x[warp] = xmax;
   if (warp == 0) {
     const int64_t base = static_cast<int64_t>(slot) * F * kBins;
     uint32_t tc;
     long long tq, th;
-    node_totals(hist_cnt + base, hist_q + base, hist_h ? hist_h + base : nullptr, lane, &tc, &tq, &th);
+    node_totals(hist_cnt + base, hist_q + base, kH ? hist_h + base : nullptr, lane, &tc, &tq, &th);
     if (lane == 0) {
       s_tc = tc;
       s_tq = tq;
       s_th = th;
     }
   }
+  __syncthreads();
+  for (int w = 0; w < kSplitWarps; ++w) xmax = fmaxf(xmax, s_x[w]);
+  const float keep = xmax - xmax * 1.52587890625e-05f;  // xmax * (1 - 2^-16)
+  const uint32_t tot_cnt = s_tc;
+  const int64_t tot_q = s_tq, tot_h = s_th;
+  const double inv = ldexp(1.0, -fixed_exp[0]), inv_h = kH ? ldexp(1.0, -fixed_exp[1]) : 1.0;
+  double sP = 0.0;
+  bool have_sP = false;
+  Cand best{-INFINITY, -1, -1, 0, 0, 0};
+  for (int e = threadIdx.x; e < n; e += blockDim.x) {
+    const Surv c = sv[e];
+    if (c.bin < 0 || c.x < keep) continue;
+    double gain = c.gain;
+    if (!c.exact) {
+      if (!have_sP) sP = node_score<kH>(tot_q, tot_cnt, tot_h, inv, inv_h, lambda), have_sP = true;
+      gain = exact_gain<kH>(c.q_left, c.cnt_left, c.qh_left, tot_q, tot_cnt, tot_h, inv, inv_h, sP, lambda, gamma);
+    }
+    const Cand cd{gain, e / kSurv, c.bin, c.cnt_left, c.q_left, c.qh_left};
+    if (better(cd, best)) best = cd;
+  }
+  for (int o = 16; o > 0; o >>= 1) {
+    Cand other = shfl_cand(best, lane ^ o);
+    if (better(other, best)) best = other;
+  }
+  if (lane == 0) s_best[warp] = best;
   __syncthreads();
   if (threadIdx.x == 0) {
     Cand b = s_best[0];
@@ -304,26 +399,35 @@ __global__ void __launch_bounds__(kSplitThreads)
 }  // namespace
 
 size_t find_splits_scratch_bytes(int32_t F, int32_t max_slots) {
-  return sizeof(Cand) * static_cast<size_t>(F) * static_cast<size_t>(max_slots);
+  return sizeof(Surv) * kSurv * static_cast<size_t>(F) * static_cast<size_t>(max_slots);
 }
 
 void launch_find_splits(const uint32_t* hist_cnt, const int64_t* hist_q, const int64_t* hist_h,
                         const int32_t* fixed_exp, int32_t F, const int32_t* n_bins, const gbdt_level* level,
                         int32_t max_slots, const gbdt_params& p, gbdt_split* out, void* scratch, int32_t* err,
                         cudaStream_t s) {
-  Cand* cand = static_cast<Cand*>(scratch);
+  Surv* surv = static_cast<Surv*>(scratch);
   dim3 grid(static_cast<unsigned>(max_slots), static_cast<unsigned>((F + kSplitWarps - 1) / kSplitWarps));
+  // ceil(min_child_weight) for the count test (counts are below 2^32)
+  const double cm = std::ceil(p.min_child_weight);
+  const int64_t mcw_ceil = cm > 8.0e9 ? int64_t(8000000000) : static_cast<int64_t>(cm);
   if (hist_h) {
     split_features_kernel<true><<<grid, kSplitThreads, 0, s>>>(hist_cnt, hist_q, hist_h, fixed_exp, F, n_bins, level,
                                                                max_slots, p.reg_lambda, p.gamma, p.min_samples_leaf,
-                                                               p.min_child_weight, cand, err);
+                                                               p.min_child_weight, mcw_ceil, surv, err);
   } else {
     split_features_kernel<false><<<grid, kSplitThreads, 0, s>>>(hist_cnt, hist_q, nullptr, fixed_exp, F, n_bins,
                                                                 level, max_slots, p.reg_lambda, p.gamma,
-                                                                p.min_samples_leaf, p.min_child_weight, cand, err);
+                                                                p.min_samples_leaf, p.min_child_weight, mcw_ceil,
+                                                                surv, err);
   }
   count_launches();
-  split_reduce_kernel<<<max_slots, kSplitThreads, 0, s>>>(hist_cnt, hist_q, hist_h, F, level, max_slots, cand, out);
+  if (hist_h)
+    split_reduce_kernel<true><<<max_slots, kSplitThreads, 0, s>>>(hist_cnt, hist_q, hist_h, fixed_exp, F, level,
+                                                                  max_slots, p.reg_lambda, p.gamma, surv, out);
+  else
+    split_reduce_kernel<false><<<max_slots, kSplitThreads, 0, s>>>(hist_cnt, hist_q, nullptr, fixed_exp, F, level,
+                                                                   max_slots, p.reg_lambda, p.gamma, surv, out);
   count_launches();
 }
 
