@@ -586,7 +586,7 @@ def main():
     ap.add_argument("--trees", type=int, default=None, help="override the workload's tree count (profiling runs)")
     ap.add_argument("--micro-rows", type=int, default=synth.CONFIGS["micro"]["n"])
     ap.add_argument("--cpu-rows", type=int, default=1_000_000)
-    ap.add_argument("--cpu-trees", type=int, default=2)
+    ap.add_argument("--cpu-trees", type=int, default=32, help="trees of the oracle sample (about 10 s on 16 cores)")
     ap.add_argument("--no-micro", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-logistic", action="store_true", help="skip the logistic-objective leg")
