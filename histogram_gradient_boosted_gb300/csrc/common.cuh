@@ -100,6 +100,37 @@ __device__ __forceinline__ double sigmoid(double x) { return __ddiv_rn(1.0, __da
 // Convert a fixed-point sum back to a double: q * 2^-S.
 __host__ __device__ inline double from_fixed(int64_t q, int S) { return ldexp(static_cast<double>(q), -S); }
 
+// Exclusive scan of v over the block (blockDim.x a multiple of 32, at most 1024): warp scans by
+// shuffles, one warp scans the warp totals.  *total = the block's sum.  s_warp: 33 shared
+// elements.  Every thread of the block must call it (it holds three barriers).
+template <typename T>
+__device__ __forceinline__ T block_scan_excl(T v, T* s_warp, T* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  T incl = v;
+  for (int o = 1; o < 32; o <<= 1) {
+    const T t = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += t;
+  }
+  if (lane == 31) s_warp[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const int nw = blockDim.x >> 5;
+    const T w = lane < nw ? s_warp[lane] : T(0);
+    T wi = w;
+    for (int o = 1; o < 32; o <<= 1) {
+      const T t = __shfl_up_sync(0xffffffffu, wi, o);
+      if (lane >= o) wi += t;
+    }
+    if (lane < nw) s_warp[lane] = wi - w;
+    if (lane == 31) s_warp[32] = wi;
+  }
+  __syncthreads();
+  const T r = s_warp[warp] + incl - v;
+  *total = s_warp[32];
+  __syncthreads();
+  return r;
+}
+
 __device__ __forceinline__ void raise_error(int32_t* flag, int32_t bits) {
   if (flag) atomicOr(flag, bits);
 }

@@ -53,6 +53,9 @@ void launch_hist_subtract(const uint32_t* prev_cnt, const int64_t* prev_q, const
 
 // ---- split.cu -------------------------------------------------------------------------
 size_t find_splits_scratch_bytes(int32_t F, int32_t max_slots);
+// The per-slot counters inside that scratch: zero them before the first launch_find_splits on it
+// (every launch leaves them zero again).
+int32_t* split_counters(void* scratch, int32_t F, int32_t max_slots);
 // hist_h: null (H = count) or the H histograms with exponent fixed_exp[1].
 void launch_find_splits(const uint32_t* hist_cnt, const int64_t* hist_q, const int64_t* hist_h,
                         const int32_t* fixed_exp, int32_t F, const int32_t* n_bins, const gbdt_level* level,

@@ -52,39 +52,26 @@ __global__ void seg_work_setup_kernel(const gbdt_level* __restrict__ level, int3
                                       int32_t max_ctas, int64_t min_rows, int32_t* __restrict__ build_slot,
                                       int64_t* __restrict__ row_start /*[max_slots+1]*/, SegWork* __restrict__ st) {
   // (a slot's rows are its segment's positions, narrowed by its filter inside the histogram kernel)
-  __shared__ int s_a[1024];
-  __shared__ long long s_b[1024];
-  __shared__ int s_pre_slots;
-  __shared__ long long s_pre_rows;
-  if (threadIdx.x == 0) s_pre_slots = 0, s_pre_rows = 0;
-  __syncthreads();
+  __shared__ int s_wa[33];
+  __shared__ long long s_wb[33];
+  int s_pre_slots = 0;        // block-uniform running totals
+  long long s_pre_rows = 0;
   const int n_slots = min(level->n_slots, max_slots);
   for (int c0 = 0; c0 < n_slots; c0 += blockDim.x) {
     const int s = c0 + threadIdx.x;
     const bool in = s < n_slots && build_flag[s] && seg[s].count > 0;
     const long long rows = in ? seg[s].count : 0;
-    s_a[threadIdx.x] = in ? 1 : 0;
-    s_b[threadIdx.x] = rows;
-    __syncthreads();
-    for (int o = 1; o < blockDim.x; o <<= 1) {
-      const int a = threadIdx.x >= o ? s_a[threadIdx.x - o] : 0;
-      const long long b = threadIdx.x >= o ? s_b[threadIdx.x - o] : 0;
-      __syncthreads();
-      s_a[threadIdx.x] += a;
-      s_b[threadIdx.x] += b;
-      __syncthreads();
-    }
+    int n_in;
+    long long n_rows;
+    const int ea = block_scan_excl(in ? 1 : 0, s_wa, &n_in);
+    const long long eb = block_scan_excl(rows, s_wb, &n_rows);
     if (in) {
-      const int k = s_pre_slots + s_a[threadIdx.x] - 1;
+      const int k = s_pre_slots + ea;
       build_slot[k] = s;
-      row_start[k] = s_pre_rows + s_b[threadIdx.x] - rows;
+      row_start[k] = s_pre_rows + eb;
     }
-    __syncthreads();
-    if (threadIdx.x == blockDim.x - 1) {
-      s_pre_slots += s_a[threadIdx.x];
-      s_pre_rows += s_b[threadIdx.x];
-    }
-    __syncthreads();
+    s_pre_slots += n_in;
+    s_pre_rows += n_rows;
   }
   if (threadIdx.x == 0) {
     row_start[s_pre_slots] = s_pre_rows;
@@ -466,26 +453,16 @@ struct MvState {
 __global__ void mv_setup_kernel(const gbdt_level* __restrict__ level, int32_t max_slots,
                                 const gbdt_segment* __restrict__ seg, int32_t* __restrict__ tile_start,
                                 MvState* __restrict__ st) {
-  __shared__ int s_b[1024];
-  __shared__ int s_pre;
-  if (threadIdx.x == 0) s_pre = 0;
-  __syncthreads();
+  __shared__ int s_w[33];
+  int s_pre = 0;  // block-uniform running total
   const int n_slots = min(level->n_slots, max_slots);
   for (int c0 = 0; c0 < n_slots; c0 += blockDim.x) {
     const int s = c0 + threadIdx.x;
     const int tiles = s < n_slots ? static_cast<int>((seg[s].count + kMvTile - 1) / kMvTile) : 0;
-    s_b[threadIdx.x] = tiles;
-    __syncthreads();
-    for (int o = 1; o < blockDim.x; o <<= 1) {
-      const int b = threadIdx.x >= o ? s_b[threadIdx.x - o] : 0;
-      __syncthreads();
-      s_b[threadIdx.x] += b;
-      __syncthreads();
-    }
-    if (s < n_slots) tile_start[s] = s_pre + s_b[threadIdx.x] - tiles;
-    __syncthreads();
-    if (threadIdx.x == blockDim.x - 1) s_pre += s_b[threadIdx.x];
-    __syncthreads();
+    int n;
+    const int e = block_scan_excl(tiles, s_w, &n);
+    if (s < n_slots) tile_start[s] = s_pre + e;
+    s_pre += n;
   }
   if (threadIdx.x == 0) {
     tile_start[n_slots] = s_pre;
@@ -503,32 +480,6 @@ __device__ __forceinline__ int slot_of_tile(const int32_t* __restrict__ tile_sta
   return lo;
 }
 
-__device__ __forceinline__ int block_scan_excl(int v, int* s_warp, int* total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int incl = v;
-  for (int o = 1; o < 32; o <<= 1) {
-    const int t = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += t;
-  }
-  if (lane == 31) s_warp[warp] = incl;
-  __syncthreads();
-  if (warp == 0) {
-    const int nw = blockDim.x >> 5;
-    const int w = lane < nw ? s_warp[lane] : 0;
-    int wi = w;
-    for (int o = 1; o < 32; o <<= 1) {
-      const int t = __shfl_up_sync(0xffffffffu, wi, o);
-      if (lane >= o) wi += t;
-    }
-    if (lane < nw) s_warp[lane] = wi - w;
-    if (lane == 31) s_warp[32] = wi;
-  }
-  __syncthreads();
-  const int r = s_warp[warp] + incl - v;
-  *total = s_warp[32];
-  __syncthreads();
-  return r;
-}
 
 // Decision of position p of a split slot: 1 = goes right.
 __device__ __forceinline__ int goes_right(const uint8_t* __restrict__ col, int bin, const uint8_t* __restrict__ go_right,
@@ -996,10 +947,8 @@ __global__ void pair_routes_kernel(const gbdt_level* __restrict__ level, int32_t
                                    const gbdt_segment* __restrict__ seg_next, const uint32_t* __restrict__ floc,
                                    PairRoute* __restrict__ pairs, int32_t* __restrict__ tile_start,
                                    PairState* __restrict__ st) {
-  __shared__ int s_b[1024];
-  __shared__ int s_pre;
-  if (threadIdx.x == 0) s_pre = 0;
-  __syncthreads();
+  __shared__ int s_w[33];
+  int s_pre = 0;  // block-uniform running total
   const int n_pairs = min(level->n_slots, max_slots) / 2;
   for (int c0 = 0; c0 < n_pairs; c0 += blockDim.x) {
     const int k = c0 + threadIdx.x;
@@ -1027,18 +976,10 @@ __global__ void pair_routes_kernel(const gbdt_level* __restrict__ level, int32_t
       pairs[k] = pr;
       tiles = static_cast<int>((pr.count + kMvTile - 1) / kMvTile);
     }
-    s_b[threadIdx.x] = tiles;
-    __syncthreads();
-    for (int o = 1; o < blockDim.x; o <<= 1) {
-      const int b = threadIdx.x >= o ? s_b[threadIdx.x - o] : 0;
-      __syncthreads();
-      s_b[threadIdx.x] += b;
-      __syncthreads();
-    }
-    if (k < n_pairs) tile_start[k] = s_pre + s_b[threadIdx.x] - tiles;
-    __syncthreads();
-    if (threadIdx.x == blockDim.x - 1) s_pre += s_b[threadIdx.x];
-    __syncthreads();
+    int n;
+    const int e = block_scan_excl(tiles, s_w, &n);
+    if (k < n_pairs) tile_start[k] = s_pre + e;
+    s_pre += n;
   }
   if (threadIdx.x == 0) {
     tile_start[n_pairs] = s_pre;

@@ -113,6 +113,18 @@ struct Surv {
 };
 
 // score of the node: G^2 / (H + lambda) from its fixed-point totals (H = count unless kH).
+static_assert(sizeof(Surv) == 40, "Surv is five 8-byte words");
+// A survivor written by another CTA of the same launch, read through L2.
+__device__ __forceinline__ Surv load_surv(const Surv* p) {
+  const long long* w = reinterpret_cast<const long long*>(p);
+  long long v[5];
+#pragma unroll
+  for (int i = 0; i < 5; ++i) v[i] = __ldcg(w + i);
+  Surv s;
+  memcpy(&s, v, sizeof(s));
+  return s;
+}
+
 template <bool kH>
 __device__ __forceinline__ double node_score(int64_t tot_q, uint32_t tot_cnt, int64_t tot_h, double inv,
                                              double inv_h, double lambda) {
@@ -151,29 +163,19 @@ __device__ __forceinline__ T lane_prefix8(T (&v)[8], int lane, T* total) {
   return x - v[7];
 }
 
-// Screen: one warp per (slot, feature).  Writes the feature's survivors of the
-// FP32 screen to surv[slot][feature][0 .. kSurv): in bin order, or, when more
-// than kSurv survive (long runs of empty bins can tie), the best of them
-// evaluated in FP64 as one exact entry.  kH: H from hist_h with exponent
-// fixed_exp[1] (logistic), else H = the row count.
+// Screen of feature f of a slot (one warp).  Writes the feature's survivors of
+// the FP32 screen to surv[slot][f][0 .. kSurv): in bin order, or, when more than
+// kSurv survive (long runs of empty bins can tie), the best of them evaluated in
+// FP64 as one exact entry.  kH: H from hist_h with exponent fixed_exp[1]
+// (logistic), else H = the row count.  tot_*: the node totals.
 template <bool kH>
-__global__ void __launch_bounds__(kSplitThreads)
-    split_features_kernel(const uint32_t* __restrict__ hist_cnt, const int64_t* __restrict__ hist_q,
-                          const int64_t* __restrict__ hist_h, const int32_t* __restrict__ fixed_exp, int32_t F,
-                          const int32_t* __restrict__ n_bins, const gbdt_level* __restrict__ level, int32_t max_slots,
-                          double lambda, double gamma, int32_t msl, double mcw, int64_t mcw_ceil,
-                          Surv* __restrict__ surv, int32_t* __restrict__ err) {
-  const int slot = blockIdx.x;
-  const int n_slots = min(level->n_slots, max_slots);
-  if (slot >= n_slots) return;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int f = blockIdx.y * kSplitWarps + warp;
+__device__ __forceinline__ void screen_feature(const uint32_t* __restrict__ hist_cnt, const int64_t* __restrict__ hist_q,
+                                               const int64_t* __restrict__ hist_h, const int32_t* __restrict__ fixed_exp,
+                                               int32_t F, const int32_t* __restrict__ n_bins, int slot, int f, int lane,
+                                               uint32_t tot_cnt, long long tot_q, long long tot_h, double lambda,
+                                               double gamma, int32_t msl, double mcw, int64_t mcw_ceil,
+                                               Surv* __restrict__ surv, int32_t* __restrict__ err) {
   const int64_t base = static_cast<int64_t>(slot) * F * kBins;
-  uint32_t tot_cnt;
-  long long tot_q, tot_h;
-  node_totals(hist_cnt + base, hist_q + base, kH ? hist_h + base : nullptr, lane, &tot_cnt, &tot_q, &tot_h);
-  if (f >= F) return;  // warp-uniform
-
   const int64_t off = base + static_cast<int64_t>(f) * kBins + lane * 8;
   uint32_t c[8];
   long long q[8], qh[8];
@@ -316,52 +318,35 @@ __global__ void __launch_bounds__(kSplitThreads)
   if (lane >= 1 && lane < kSurv) out[lane] = Surv{-1.0f, -1, 0, 0, 0, 0, 0.0};
 }
 
-// Select: one CTA per slot.  The FP32 margin holds across the slot's features (x is the same
-// monotone proxy of the gain everywhere in a node), so only survivors within it of the largest
-// screening value of the slot are evaluated in FP64 (exact entries carry their gain), then reduced
-// under the frozen rule.
+// Select for one slot (the whole 64-thread CTA).  The FP32 margin holds across the slot's features
+// (x is the same monotone proxy of the gain everywhere in a node), so only survivors within it of
+// the largest screening value of the slot are evaluated in FP64 (exact entries carry their gain),
+// then reduced under the frozen rule.  The survivors were written by other CTAs: they are read
+// through L2 (ld.global.cg).
 template <bool kH>
-__global__ void __launch_bounds__(kSplitThreads)
-    split_reduce_kernel(const uint32_t* __restrict__ hist_cnt, const int64_t* __restrict__ hist_q,
-                        const int64_t* __restrict__ hist_h, const int32_t* __restrict__ fixed_exp, int32_t F,
-                        const gbdt_level* __restrict__ level, int32_t max_slots, double lambda, double gamma,
-                        const Surv* __restrict__ surv, gbdt_split* __restrict__ out) {
-  const int slot = blockIdx.x;
-  const int n_slots = min(level->n_slots, max_slots);
-  if (slot >= n_slots) return;
+__device__ __forceinline__ void select_slot(const uint32_t* __restrict__ hist_cnt, const int64_t* __restrict__ hist_q,
+                                            const int64_t* __restrict__ hist_h, const int32_t* __restrict__ fixed_exp,
+                                            int32_t F, int slot, uint32_t tot_cnt, long long tot_q, long long tot_h,
+                                            double lambda, double gamma, const Surv* __restrict__ surv,
+                                            gbdt_split* __restrict__ out) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   __shared__ Cand s_best[kSplitWarps];
   __shared__ float s_x[kSplitWarps];
-  __shared__ uint32_t s_tc;
-  __shared__ long long s_tq, s_th;
   const Surv* sv = surv + static_cast<int64_t>(slot) * F * kSurv;
   const int n = F * kSurv;
   float xmax = -1.0f;
-  for (int e = threadIdx.x; e < n; e += blockDim.x) xmax = fmaxf(xmax, sv[e].x);
+  for (int e = threadIdx.x; e < n; e += blockDim.x) xmax = fmaxf(xmax, __ldcg(&sv[e].x));
   for (int o = 16; o > 0; o >>= 1) xmax = fmaxf(xmax, __shfl_xor_sync(0xffffffffu, xmax, o));
   if (lane == 0) s_x[warp] = xmax;
-  if (warp == 0) {
-    const int64_t base = static_cast<int64_t>(slot) * F * kBins;
-    uint32_t tc;
-    long long tq, th;
-    node_totals(hist_cnt + base, hist_q + base, kH ? hist_h + base : nullptr, lane, &tc, &tq, &th);
-    if (lane == 0) {
-      s_tc = tc;
-      s_tq = tq;
-      s_th = th;
-    }
-  }
   __syncthreads();
   for (int w = 0; w < kSplitWarps; ++w) xmax = fmaxf(xmax, s_x[w]);
   const float keep = xmax - xmax * 1.52587890625e-05f;  // xmax * (1 - 2^-16)
-  const uint32_t tot_cnt = s_tc;
-  const int64_t tot_q = s_tq, tot_h = s_th;
   const double inv = ldexp(1.0, -fixed_exp[0]), inv_h = kH ? ldexp(1.0, -fixed_exp[1]) : 1.0;
   double sP = 0.0;
   bool have_sP = false;
   Cand best{-INFINITY, -1, -1, 0, 0, 0};
   for (int e = threadIdx.x; e < n; e += blockDim.x) {
-    const Surv c = sv[e];
+    const Surv c = load_surv(sv + e);
     if (c.bin < 0 || c.x < keep) continue;
     double gain = c.gain;
     if (!c.exact) {
@@ -388,46 +373,80 @@ __global__ void __launch_bounds__(kSplitThreads)
     r.gain = split ? b.gain : 0.0;
     r.q_left = split ? b.q_left : 0;
     r.cnt_left = split ? b.cnt_left : 0;
-    r.q_total = s_tq;
-    r.cnt_total = s_tc;
+    r.q_total = tot_q;
+    r.cnt_total = tot_cnt;
     r.h_left = split ? b.qh_left : 0;
-    r.h_total = s_th;
+    r.h_total = kH ? tot_h : 0;
     out[slot] = r;
   }
 }
 
+// One CTA of two warps per (slot, pair of features): each warp screens one feature; the CTA that
+// finishes a slot last (a per-slot counter, which that CTA resets to 0 for the next launch)
+// selects the slot's split.  No CTA waits for another.
+template <bool kH>
+__global__ void __launch_bounds__(kSplitThreads)
+    split_kernel(const uint32_t* __restrict__ hist_cnt, const int64_t* __restrict__ hist_q,
+                 const int64_t* __restrict__ hist_h, const int32_t* __restrict__ fixed_exp, int32_t F,
+                 const int32_t* __restrict__ n_bins, const gbdt_level* __restrict__ level, int32_t max_slots,
+                 double lambda, double gamma, int32_t msl, double mcw, int64_t mcw_ceil, Surv* __restrict__ surv,
+                 int32_t* __restrict__ slot_done, gbdt_split* __restrict__ out, int32_t* __restrict__ err) {
+  const int slot = blockIdx.x;
+  const int n_slots = min(level->n_slots, max_slots);
+  if (slot >= n_slots) return;  // every CTA of this slot
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int f = blockIdx.y * kSplitWarps + warp;
+  const int64_t base = static_cast<int64_t>(slot) * F * kBins;
+  uint32_t tot_cnt;
+  long long tot_q, tot_h;
+  node_totals(hist_cnt + base, hist_q + base, kH ? hist_h + base : nullptr, lane, &tot_cnt, &tot_q, &tot_h);
+  if (f < F)
+    screen_feature<kH>(hist_cnt, hist_q, hist_h, fixed_exp, F, n_bins, slot, f, lane, tot_cnt, tot_q, tot_h, lambda,
+                       gamma, msl, mcw, mcw_ceil, surv, err);
+  __shared__ int s_last;
+  __threadfence();  // this CTA's survivors are visible device-wide before it is counted
+  __syncthreads();
+  if (threadIdx.x == 0) s_last = atomicAdd(&slot_done[slot], 1) == static_cast<int>(gridDim.y) - 1;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  select_slot<kH>(hist_cnt, hist_q, hist_h, fixed_exp, F, slot, tot_cnt, tot_q, tot_h, lambda, gamma, surv, out);
+  if (threadIdx.x == 0) slot_done[slot] = 0;
+}
+
 }  // namespace
 
+// Scratch: the per-slot counters (kMaxSlots of them, at a fixed place so that every level's launch
+// finds them zero), then the survivors [max_slots][F][kSurv].
+constexpr size_t kCounterBytes = sizeof(int32_t) * kMaxSlots;
+
 size_t find_splits_scratch_bytes(int32_t F, int32_t max_slots) {
-  return sizeof(Surv) * kSurv * static_cast<size_t>(F) * static_cast<size_t>(max_slots);
+  return kCounterBytes + sizeof(Surv) * kSurv * static_cast<size_t>(F) * static_cast<size_t>(max_slots);
+}
+
+int32_t* split_counters(void* scratch, int32_t F, int32_t max_slots) {
+  (void)F, (void)max_slots;
+  return static_cast<int32_t*>(scratch);
 }
 
 void launch_find_splits(const uint32_t* hist_cnt, const int64_t* hist_q, const int64_t* hist_h,
                         const int32_t* fixed_exp, int32_t F, const int32_t* n_bins, const gbdt_level* level,
                         int32_t max_slots, const gbdt_params& p, gbdt_split* out, void* scratch, int32_t* err,
                         cudaStream_t s) {
-  Surv* surv = static_cast<Surv*>(scratch);
+  int32_t* done = split_counters(scratch, F, max_slots);
+  Surv* surv = reinterpret_cast<Surv*>(static_cast<char*>(scratch) + kCounterBytes);
   dim3 grid(static_cast<unsigned>(max_slots), static_cast<unsigned>((F + kSplitWarps - 1) / kSplitWarps));
   // ceil(min_child_weight) for the count test (counts are below 2^32)
   const double cm = std::ceil(p.min_child_weight);
   const int64_t mcw_ceil = cm > 8.0e9 ? int64_t(8000000000) : static_cast<int64_t>(cm);
-  if (hist_h) {
-    split_features_kernel<true><<<grid, kSplitThreads, 0, s>>>(hist_cnt, hist_q, hist_h, fixed_exp, F, n_bins, level,
-                                                               max_slots, p.reg_lambda, p.gamma, p.min_samples_leaf,
-                                                               p.min_child_weight, mcw_ceil, surv, err);
-  } else {
-    split_features_kernel<false><<<grid, kSplitThreads, 0, s>>>(hist_cnt, hist_q, nullptr, fixed_exp, F, n_bins,
-                                                                level, max_slots, p.reg_lambda, p.gamma,
-                                                                p.min_samples_leaf, p.min_child_weight, mcw_ceil,
-                                                                surv, err);
-  }
-  count_launches();
   if (hist_h)
-    split_reduce_kernel<true><<<max_slots, kSplitThreads, 0, s>>>(hist_cnt, hist_q, hist_h, fixed_exp, F, level,
-                                                                  max_slots, p.reg_lambda, p.gamma, surv, out);
+    split_kernel<true><<<grid, kSplitThreads, 0, s>>>(hist_cnt, hist_q, hist_h, fixed_exp, F, n_bins, level,
+                                                      max_slots, p.reg_lambda, p.gamma, p.min_samples_leaf,
+                                                      p.min_child_weight, mcw_ceil, surv, done, out, err);
   else
-    split_reduce_kernel<false><<<max_slots, kSplitThreads, 0, s>>>(hist_cnt, hist_q, nullptr, fixed_exp, F, level,
-                                                                   max_slots, p.reg_lambda, p.gamma, surv, out);
+    split_kernel<false><<<grid, kSplitThreads, 0, s>>>(hist_cnt, hist_q, nullptr, fixed_exp, F, n_bins, level,
+                                                       max_slots, p.reg_lambda, p.gamma, p.min_samples_leaf,
+                                                       p.min_child_weight, mcw_ceil, surv, done, out, err);
   count_launches();
 }
 
@@ -457,8 +476,9 @@ extern "C" int gbdt_find_splits_h(const uint32_t* hist_cnt, const int64_t* hist_
     set_error("gbdt_find_splits: workspace needs %zu bytes", gbdt_find_splits_workspace_size(F, max_slots));
     return ws ? GBDT_ERR_WORKSPACE : GBDT_ERR_INVALID_ARG;
   }
-  launch_find_splits(hist_cnt, hist_q, hist_h, fixed_exp, F, n_bins, level, max_slots, *p, out, ws, nullptr,
-                     static_cast<cudaStream_t>(stream));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  GBDT_CUDA(cudaMemsetAsync(split_counters(ws, F, max_slots), 0, sizeof(int32_t) * max_slots, s));
+  launch_find_splits(hist_cnt, hist_q, hist_h, fixed_exp, F, n_bins, level, max_slots, *p, out, ws, nullptr, s);
   GBDT_LAUNCH_CHECK();
   return GBDT_OK;
 }

@@ -88,15 +88,14 @@ __global__ void __launch_bounds__(1024)
                        int32_t* __restrict__ pair_parent, uint8_t* __restrict__ next_build, Route* __restrict__ route,
                        LevelStats* __restrict__ stats, int32_t num_leaves, int32_t* __restrict__ budget,
                        int logistic, int32_t* __restrict__ err) {
-  __shared__ int s_a[1024];
+  __shared__ int s_w[33];
   __shared__ double s_gain[kMaxSlots];                  // leaf budget: the level's candidate gains
   __shared__ uint32_t s_cand[kMaxSlots / 32], s_keep[kMaxSlots / 32];
   __shared__ int s_ncand, s_bind;
-  __shared__ int s_pre;
   __shared__ unsigned long long s_act, s_built_rows, s_split_rows, s_scan_rows;
   __shared__ int s_built;
+  int s_pre = 0;  // block-uniform: splitting slots before the current chunk
   if (threadIdx.x == 0) {
-    s_pre = 0;
     s_act = s_built_rows = s_split_rows = s_scan_rows = 0;
     s_built = 0;
   }
@@ -175,16 +174,10 @@ __global__ void __launch_bounds__(1024)
       if (is_split) atomicAdd(&s_split_rows, static_cast<unsigned long long>(tot.cnt));
       if (seg[s].count != static_cast<int64_t>(tot.cnt)) raise_error(err, kErrHistTotals);
     }
-    s_a[threadIdx.x] = is_split;
-    __syncthreads();
-    for (int o = 1; o < blockDim.x; o <<= 1) {
-      const int v = threadIdx.x >= o ? s_a[threadIdx.x - o] : 0;
-      __syncthreads();
-      s_a[threadIdx.x] += v;
-      __syncthreads();
-    }
+    int n_split;
+    const int e_split = block_scan_excl(is_split, s_w, &n_split);
     if (in) {
-      const int k = s_pre + s_a[threadIdx.x] - is_split;
+      const int k = s_pre + e_split;
       const double G = from_fixed(tot.q, S);
       const double H = logistic ? from_fixed(tot.qh, S_h) : static_cast<double>(tot.cnt);
       gbdt_node nd;
@@ -219,10 +212,9 @@ __global__ void __launch_bounds__(1024)
       tree[node_begin + s] = nd;
       route[s] = rt;
     }
-    __syncthreads();
-    if (threadIdx.x == blockDim.x - 1) s_pre += s_a[threadIdx.x];
-    __syncthreads();
+    s_pre += n_split;
   }
+  __syncthreads();  // the shared statistics are complete
   if (threadIdx.x == 0) {
     budget[0] += n_slots - s_pre;  // this level's leaves
     if (bind) budget[1] = 1;
@@ -400,6 +392,7 @@ extern "C" int gbdt_train(const uint8_t* bins, int64_t ldb, const int32_t* n_bin
   GBDT_CUDA(cudaMemcpyAsync(hb.data(), n_bins, sizeof(int32_t) * F, cudaMemcpyDeviceToHost, s));
   GBDT_CUDA(cudaMemsetAsync(w.err, 0, sizeof(int32_t), s));
   GBDT_CUDA(cudaMemsetAsync(w.nonfinite, 0, sizeof(int32_t), s));
+  GBDT_CUDA(cudaMemsetAsync(split_counters(w.split_scratch, F, 1), 0, sizeof(int32_t) * kMaxSlots, s));
   launch_label_sum(label, N, w.label_partials, w.nonfinite, logistic, s);
   int32_t nonfinite = 0;
   GBDT_CUDA(cudaMemcpyAsync(&nonfinite, w.nonfinite, sizeof(int32_t), cudaMemcpyDeviceToHost, s));
