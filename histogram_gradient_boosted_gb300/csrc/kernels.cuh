@@ -73,22 +73,27 @@ struct Route {
 // ---- segments.cu ----------------------------------------------------------------------
 // Histograms of the flagged slots of a level whose rows are contiguous segments.
 struct SegHistPlan {
-  int n_fgroups, group_feats;
-  int max_ctas;      // CTAs per feature group (one wave over the SMs)
+  int n_cols;        // columns the lanes read: slots of the row blocks (features in the column layout)
+  int n_fgroups, group_feats;  // groups of columns (full groups of group_feats and the remainder)
+  int total_weight;  // sum over groups of (32-lane halves + 1)
+  int sm_budget;     // CTAs of one wave, shared by the groups in proportion to their weights
+  int max_ctas;      // CTAs of a full group
   int64_t min_rows;  // least work (rows + a fixed cost per slot) a CTA takes when the level is small
   bool with_h;       // logistic: H histograms too (h = logistic_hess(g), exponent fixed_exp[1])
   size_t smem;
 };
-SegHistPlan plan_seg_histograms(int64_t N, int32_t F, int32_t max_slots, int32_t max_build, bool with_h = false);
+// S: the columns the lanes read (slots of the row blocks; F in the column layout).
+SegHistPlan plan_seg_histograms(int64_t N, int32_t S, int32_t max_slots, int32_t max_build, bool with_h = false);
 size_t seg_hist_scratch_bytes(int32_t max_slots);
 int launch_seg_histograms(const SegHistPlan& plan, const uint8_t* bins, int64_t ldb, int64_t N, int32_t F,
                           const void* g, int32_t g_dtype, const int32_t* fixed_exp, const gbdt_level* level,
                           int32_t max_slots, const uint8_t* build_flag, const gbdt_segment* seg,
                           const gbdt_filter* filters, void* scratch, uint32_t* hist_cnt, int64_t* hist_q,
-                          int64_t* hist_h, cudaStream_t s, bool row_blocks = false,
-                          const uint32_t* floc = nullptr);  // row_blocks: ldb is the row-block pitch, floc the
-                                                            // feature locators (null: feature f in slot f);
-                                                            // hist_h: plan.with_h
+                          int64_t* hist_h, cudaStream_t s, bool row_blocks = false, const uint32_t* floc = nullptr,
+                          const uint32_t* slot_src = nullptr);
+// row_blocks: ldb is the row-block pitch, floc the feature locators and slot_src each slot's features
+// (plan_row_block_slots; null: slot s holds feature s); a lane accumulates its slot's byte, the joint
+// code of a 4-bit slot, and the flush splits it into the two features' bins.  hist_h: plan.with_h.
 // Stable partition of the per-position data of every split slot (bins columns, g, original row
 // id) from *_in to *_out; slots without a split record leaf_of_row[orig] = their node id.
 size_t move_scratch_bytes(int64_t N, int32_t max_slots);

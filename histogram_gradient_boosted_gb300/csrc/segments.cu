@@ -258,14 +258,14 @@ __device__ __forceinline__ void load_rows32(const uint8_t* p, bool second, uint3
 // kRB: bins in the row-block layout (ldb is then the row-block pitch and col[h]
 // points at the feature's 32 bytes of row block 0).
 // kH: also the logistic hessian h = |g| (1 - |g|) of each row, in fixed point with scale_h.
-// unpack: some lanes' features sit in 4-bit slots: their loaded words become (w >> sh) & mk (every
-// byte then holds the feature's bin); the filter byte likewise with fsh, fmk.
+// A lane's byte is its slot's code: a feature's bin, or for a 4-bit slot the joint code of its two
+// features (first | second << 4), whose histogram the flush splits into the two.  The filter's
+// feature may sit in a 4-bit slot: its decision is (byte >> fsh) & fmk.
 template <typename GT, int NH, bool kV8, bool kRB, bool kH>
 __device__ __forceinline__ void seg_hist_rows(uint32_t base, const uint8_t* const (&col)[NH], const bool (&has)[NH],
                                               int64_t ldb, const GT* __restrict__ g, double scale, double scale_h,
                                               int64_t p0, int64_t p1, const uint8_t* __restrict__ fcol, int fbin,
-                                              int fside, uint4* s_q, bool unpack, const uint32_t (&sh)[NH],
-                                              const uint32_t (&mk)[NH], uint32_t fsh, uint32_t fmk) {
+                                              int fside, uint4* s_q, uint32_t fsh, uint32_t fmk) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, n_warps = blockDim.x >> 5;
   // aligned 32-position blocks covering [p0, p1); positions outside are masked
   for (int64_t b = (p0 >> 5) + warp; (b << 5) < p1; b += n_warps) {
@@ -291,12 +291,6 @@ __device__ __forceinline__ void seg_hist_rows(uint32_t base, const uint8_t* cons
     const bool v = in && (!fcol || (fb > fbin) == (fside != 0));
     const uint32_t valid = __ballot_sync(0xffffffffu, v);
     if (valid == 0) continue;  // warp-uniform: no row of this block belongs to the slot
-    if (unpack) {  // CTA-uniform
-#pragma unroll
-      for (int h = 0; h < NH; ++h)
-#pragma unroll
-        for (int k = 0; k < 8; ++k) w[h][k] = (w[h][k] >> sh[h]) & mk[h];
-    }
     const int64_t q = v ? to_fixed(gv, scale) : 0;
     __syncwarp();
     if constexpr (kH) {
@@ -320,18 +314,39 @@ __device__ __forceinline__ void seg_hist_rows(uint32_t base, const uint8_t* cons
 
 // Merge the CTA's shared histograms into slot's global histograms and leave
 // the shared ones zeroed for the next slot.  kH: the H words (s_hlo, s_hhi, the
-// two arrays after s_hi) go to hist_h.
+// two arrays after s_hi) go to hist_h.  Lane j of the group holds column s_lo + j
+// of the bins (a slot): src (the slot's features: first | second << 16, second
+// 0xffff for a whole-byte slot; null: slot s is feature s) sends a 4-bit slot's
+// joint entry to both features' bins.
+__device__ __forceinline__ void flush_add(uint32_t* __restrict__ hist_cnt, int64_t* __restrict__ hist_q,
+                                          int64_t* __restrict__ hist_h, int64_t o, uint32_t cn, int64_t v,
+                                          int64_t vh) {
+  atomicAdd(hist_cnt + o, cn);
+  atomicAdd(reinterpret_cast<unsigned long long*>(hist_q + o), static_cast<unsigned long long>(v));
+  if (hist_h) atomicAdd(reinterpret_cast<unsigned long long*>(hist_h + o), static_cast<unsigned long long>(vh));
+}
+
 template <int NH, bool kH>
 __device__ __forceinline__ void seg_hist_flush(uint32_t* s_cnt, uint32_t* s_lo, int32_t* s_hi, int slot, int32_t F,
-                                               int f_lo, int nf, uint32_t* __restrict__ hist_cnt,
-                                               int64_t* __restrict__ hist_q, int64_t* __restrict__ hist_h) {
+                                               int c_lo, int ns, const uint32_t* __restrict__ src,
+                                               uint32_t* __restrict__ hist_cnt, int64_t* __restrict__ hist_q,
+                                               int64_t* __restrict__ hist_h) {
   constexpr int entries = NH * kHalfWords;
   uint32_t* s_hlo = reinterpret_cast<uint32_t*>(s_hi + entries);
   int32_t* s_hhi = reinterpret_cast<int32_t*>(s_hlo + entries);
+  // a thread's entries all sit in one lane (blockDim.x is a multiple of 32): its slot per half
+  uint32_t sv[NH];
+#pragma unroll
+  for (int h = 0; h < NH; ++h) {
+    const int j = (h << 5) + (threadIdx.x & 31);
+    const int col = c_lo + (j < ns ? j : 0);
+    sv[h] = src ? src[col] : (static_cast<uint32_t>(col) | 0xffff0000u);
+  }
   for (int e = threadIdx.x; e < entries; e += blockDim.x) {
     const uint32_t cn = s_cnt[e];
     if (cn == 0) continue;
-    const int j = ((e / kHalfWords) << 5) + (e & 31);  // feature within the group
+    const int hh = e / kHalfWords;
+    const int j = (hh << 5) + (e & 31);  // column within the group
     const int64_t v = static_cast<int64_t>(s_hi[e]) * 4294967296ll + static_cast<int64_t>(s_lo[e]);
     s_cnt[e] = 0;
     s_lo[e] = 0;
@@ -342,12 +357,20 @@ __device__ __forceinline__ void seg_hist_flush(uint32_t* s_cnt, uint32_t* s_lo, 
       s_hlo[e] = 0;
       s_hhi[e] = 0;
     }
-    if (j >= nf) continue;  // unused entries of lanes without a feature
-    const int bin = (e >> 5) & (kBins - 1);
-    const int64_t o = (static_cast<int64_t>(slot) * F + f_lo + j) * kBins + bin;
-    atomicAdd(hist_cnt + o, cn);
-    atomicAdd(reinterpret_cast<unsigned long long*>(hist_q + o), static_cast<unsigned long long>(v));
-    if constexpr (kH) atomicAdd(reinterpret_cast<unsigned long long*>(hist_h + o), static_cast<unsigned long long>(vh));
+    if (j >= ns) continue;  // unused entries of lanes without a column
+    const int code = (e >> 5) & (kBins - 1);
+    uint32_t svh = sv[0];
+#pragma unroll
+    for (int h = 1; h < NH; ++h)
+      if (hh == h) svh = sv[h];
+    const int64_t fa = static_cast<int64_t>(svh & 0xffffu), fb = static_cast<int64_t>(svh >> 16);
+    const int64_t row = static_cast<int64_t>(slot) * F;
+    if (fb == 0xffff) {
+      flush_add(hist_cnt, hist_q, kH ? hist_h : nullptr, (row + fa) * kBins + code, cn, v, vh);
+    } else {  // a 4-bit slot: the joint entry adds to each feature's own bin
+      flush_add(hist_cnt, hist_q, kH ? hist_h : nullptr, (row + fa) * kBins + (code & 15), cn, v, vh);
+      flush_add(hist_cnt, hist_q, kH ? hist_h : nullptr, (row + fb) * kBins + (code >> 4), cn, v, vh);
+    }
   }
 }
 
@@ -358,18 +381,24 @@ __device__ __forceinline__ void seg_hist_flush(uint32_t* s_cnt, uint32_t* s_lo, 
 // also the H histograms, up to 32 features per CTA, fixed_exp[1] their exponent.
 template <typename GT, bool kV8, bool kRB, bool kH>
 __global__ void __launch_bounds__(kSegThreads, 1)
-    seg_hist_kernel(const uint8_t* __restrict__ bins, int64_t ldb, int32_t F, const GT* __restrict__ g,
+    seg_hist_kernel(const uint8_t* __restrict__ bins, int64_t ldb, int32_t F, int32_t S, const GT* __restrict__ g,
                     const int32_t* __restrict__ fixed_exp, const gbdt_segment* __restrict__ seg,
                     const gbdt_filter* __restrict__ filters, const int32_t* __restrict__ build_slot,
-                    const int64_t* __restrict__ row_start, const SegWork* __restrict__ st, int32_t group_feats,
-                    uint32_t* __restrict__ hist_cnt, int64_t* __restrict__ hist_q, int64_t* __restrict__ hist_h,
-                    const uint32_t* __restrict__ floc) {
+                    const int64_t* __restrict__ row_start, const SegWork* __restrict__ st, int32_t group_cols,
+                    int32_t sm_budget, int32_t total_weight, uint32_t* __restrict__ hist_cnt,
+                    int64_t* __restrict__ hist_q, int64_t* __restrict__ hist_h, const uint32_t* __restrict__ floc,
+                    const uint32_t* __restrict__ slot_src) {
   extern __shared__ __align__(16) unsigned char smem[];
-  const int ctas = st->ctas;
+  // this CTA's group: columns (slots) [c_lo, c_lo + ns) of the bins.  A CTA's time per row is about
+  // one half's atomics for each of its halves plus as much again for the row itself (its gradient,
+  // staging, ballots), so groups get CTAs in proportion to halves + 1
+  const int c_lo = blockIdx.y * group_cols;
+  const int ns = min(group_cols, S - c_lo);
+  if (ns <= 0) return;
+  const int weight = ((ns + 31) >> 5) + 1;
+  const int cap = max(1, static_cast<int>(static_cast<int64_t>(sm_budget) * weight / total_weight));
+  const int ctas = min(st->ctas, cap);
   if (static_cast<int>(blockIdx.x) >= ctas) return;
-  const int f_lo = blockIdx.y * group_feats;
-  const int nf = min(group_feats, F - f_lo);
-  if (nf <= 0) return;
   // this CTA's share [xlo, xhi) of the cost line: built slot j covers [row_start[j] + kSlotCost * j,
   // row_start[j + 1] + kSlotCost * (j + 1)), its rows first, its fixed cost after them
   const int64_t total = st->total_cost;
@@ -398,19 +427,16 @@ __global__ void __launch_bounds__(kSegThreads, 1)
       *reinterpret_cast<uint4*>(s_cnt + e) = make_uint4(0, 0, 0, 0);
     __syncthreads();
     const uint32_t base = smem_u32(s_cnt) + lane * 4;
-    // a lane's feature: its column, or with locators (4-bit slots, row blocks only) its slot and nibble
+    // a lane's column: a slot of the row blocks (one feature, or two in 4 bits each), or in the
+    // column layout a feature
     bool has[NH];
     const uint8_t* col[NH];
-    uint32_t sh[NH], mk[NH];
     const bool unpack = kRB && floc != nullptr;
 #pragma unroll
     for (int h = 0; h < NH; ++h) {
-      has[h] = h * 32 + lane < nf;
-      const int f = f_lo + (has[h] ? h * 32 + lane : 0);
-      const uint32_t loc = unpack ? floc[f] : static_cast<uint32_t>(f);
-      col[h] = bins + static_cast<int64_t>(loc_slot(loc)) * (kRB ? kRowBlock : ldb);
-      sh[h] = loc_shift(loc);
-      mk[h] = loc_mask(loc) * 0x01010101u;
+      has[h] = h * 32 + lane < ns;
+      const int c = c_lo + (has[h] ? h * 32 + lane : 0);
+      col[h] = bins + static_cast<int64_t>(c) * (kRB ? kRowBlock : ldb);
     }
     for (; k < n_built && row_start[k] + kSlotCost * k < xhi; ++k) {
       // the share's rows of slot k: offsets [o0, o1) of its rows
@@ -425,16 +451,17 @@ __global__ void __launch_bounds__(kSegThreads, 1)
       const uint8_t* fcol =
           fl.feature >= 0 ? bins + static_cast<int64_t>(loc_slot(floc_f)) * (kRB ? kRowBlock : ldb) : nullptr;
       seg_hist_rows<GT, NH, kV8, kRB, kH>(base, col, has, ldb, g, scale, scale_h, p0, p0 + (r_end - r), fcol, fl.bin,
-                                          fl.side, s_q, unpack, sh, mk, loc_shift(floc_f), loc_mask(floc_f));
+                                          fl.side, s_q, loc_shift(floc_f), loc_mask(floc_f));
       __syncthreads();
-      seg_hist_flush<NH, kH>(s_cnt, s_lo, s_hi, slot, F, f_lo, nf, hist_cnt, hist_q, hist_h);
+      seg_hist_flush<NH, kH>(s_cnt, s_lo, s_hi, slot, F, c_lo, ns, kRB ? slot_src : nullptr, hist_cnt, hist_q,
+                             hist_h);
       __syncthreads();
     }
   };
   if constexpr (kH) {
     run(std::integral_constant<int, 1>{});
   } else {
-    if (group_feats > 32) run(std::integral_constant<int, 2>{});
+    if (ns > 32) run(std::integral_constant<int, 2>{});
     else run(std::integral_constant<int, 1>{});
   }
 }
@@ -1254,14 +1281,21 @@ cudaError_t smem_attr(K kernel, size_t bytes) {
 }  // namespace
 
 // ---- plans and launchers ------------------------------------------------------------------------
-SegHistPlan plan_seg_histograms(int64_t N, int32_t F, int32_t max_slots, int32_t max_build, bool with_h) {
+SegHistPlan plan_seg_histograms(int64_t N, int32_t S, int32_t max_slots, int32_t max_build, bool with_h) {
   (void)N, (void)max_slots, (void)max_build;
   SegHistPlan p{};
   const int max_feats = with_h ? 32 : kSegMaxFeats;  // five shared words per entry with H, three without
-  p.n_fgroups = ceil_div(F, max_feats);
-  p.group_feats = ceil_div(F, p.n_fgroups);
-  p.max_ctas = sm_count() / p.n_fgroups;  // one wave: a CTA per SM
-  if (p.max_ctas < 1) p.max_ctas = 1;
+  // groups of whole 32-lane halves (an atomic instruction costs the same with idle lanes): full
+  // groups of max_feats columns and the remainder
+  p.n_cols = S;
+  p.n_fgroups = ceil_div(S, max_feats);
+  p.group_feats = p.n_fgroups == 1 ? S : max_feats;
+  const int rem = S - (p.n_fgroups - 1) * p.group_feats;
+  // a group's weight: its halves + 1 (see seg_hist_kernel)
+  p.total_weight = (p.n_fgroups - 1) * (ceil_div(p.group_feats, 32) + 1) + ceil_div(rem, 32) + 1;
+  p.sm_budget = sm_count();  // one wave: a CTA per SM, shared by the groups in proportion to their weights
+  p.max_ctas = std::max(1, static_cast<int>(static_cast<int64_t>(p.sm_budget) * (ceil_div(p.group_feats, 32) + 1) /
+                                            p.total_weight));
   p.min_rows = 1024;  // least cost (rows + kSlotCost per slot) per CTA
   p.with_h = with_h;
   const size_t words = with_h ? 5 : 3, stage = with_h ? 512 : 256;  // staged row records per warp
@@ -1278,7 +1312,8 @@ int launch_seg_histograms(const SegHistPlan& plan, const uint8_t* bins, int64_t 
                           const void* g, int32_t g_dtype, const int32_t* fixed_exp, const gbdt_level* level,
                           int32_t max_slots, const uint8_t* build_flag, const gbdt_segment* seg,
                           const gbdt_filter* filters, void* scratch, uint32_t* hist_cnt, int64_t* hist_q,
-                          int64_t* hist_h, cudaStream_t s, bool row_blocks, const uint32_t* floc) {
+                          int64_t* hist_h, cudaStream_t s, bool row_blocks, const uint32_t* floc,
+                          const uint32_t* slot_src) {
   (void)N;
   Carve c(scratch, seg_hist_scratch_bytes(max_slots));
   SegWork* st = c.take<SegWork>(1);
@@ -1293,9 +1328,10 @@ int launch_seg_histograms(const SegHistPlan& plan, const uint8_t* bins, int64_t 
   const bool v8 = aligned(bins, 32) && ldb % 32 == 0;
   auto launch = [&](auto kernel, const auto* gp) -> int {
     GBDT_CUDA(smem_attr(kernel, plan.smem));
-    kernel<<<grid, kSegThreads, plan.smem, s>>>(bins, ldb, F, gp, fixed_exp, seg, filters, build_slot, row_start,
-                                                st, plan.group_feats, hist_cnt, hist_q, hist_h,
-                                                row_blocks ? floc : nullptr);
+    kernel<<<grid, kSegThreads, plan.smem, s>>>(bins, ldb, F, plan.n_cols, gp, fixed_exp, seg, filters, build_slot,
+                                                row_start, st, plan.group_feats, plan.sm_budget, plan.total_weight,
+                                                hist_cnt, hist_q, hist_h, row_blocks ? floc : nullptr,
+                                                row_blocks ? slot_src : nullptr);
     return GBDT_OK;
   };
   auto pick = [&](const auto* gp, auto h_tag) -> int {

@@ -468,7 +468,7 @@ extern "C" int gbdt_train(const uint8_t* bins, int64_t ldb, const int32_t* n_bin
       const uint32_t* lo = ph < 0 ? w.orig0 : w.orig_xy[ph];
       if (d < D) {
         const int max_build = d == 0 ? 1 : max_slots / 2;
-        const SegHistPlan plan = plan_seg_histograms(N, F, max_slots, max_build, logistic);
+        const SegHistPlan plan = plan_seg_histograms(N, S, max_slots, max_build, logistic);
         if (timing) GBDT_CUDA(cudaEventRecord(ev_hist(t, d, 0), s));
         const gbdt_segment* hseg = w.seg[cur];
         const gbdt_filter* hfil = nullptr;
@@ -480,7 +480,7 @@ extern "C" int gbdt_train(const uint8_t* bins, int64_t ldb, const int32_t* n_bin
         }
         rc = launch_seg_histograms(plan, lb, pitch, N, F, lg, GBDT_DTYPE_F64, w.fixed_exp, w.level[cur], max_slots,
                                    w.build[cur], hseg, hfil, w.seg_scratch, w.hist_cnt[cur], w.hist_q[cur],
-                                   w.hist_h[cur], s, true, w.floc);
+                                   w.hist_h[cur], s, true, w.floc, w.slot_src);
         if (rc != GBDT_OK) return rc;
         if (timing) GBDT_CUDA(cudaEventRecord(ev_hist(t, d, 1), s));
         if (d > 0) {
