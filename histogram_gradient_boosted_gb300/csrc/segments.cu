@@ -28,7 +28,7 @@ namespace gbdt {
 namespace {
 
 // ---------------------------------------------------------------------------------------- histograms
-constexpr int kSegThreads = 1024;
+constexpr int kSegThreads = 768;  // 24 warps: registers for two blocks' loads per warp
 constexpr int kSegMaxFeats = 64;  // features per CTA (64 x 256 x 12 B = 192 KB of shared memory)
 
 // The work of a level is cut by cost: every built slot costs its rows plus kSlotCost, the
@@ -252,15 +252,49 @@ __device__ __forceinline__ void load_rows32(const uint8_t* p, bool second, uint3
   w[4] = x1.x, w[5] = x1.y, w[6] = x1.z, w[7] = x1.w;
 }
 
+// The loads of one 32-position block: the lane's bytes of every half, its row's gradient and, with a
+// filter, its row's decision byte.
+template <int NH>
+struct SegBlock {
+  uint32_t w[NH][8];
+  double gv;
+  int fb;
+};
+
+// Issue the loads of block b (positions outside [p0, p1) read nothing).  kRB: bins in the row-block
+// layout (ldb is then the row-block pitch and col[h] points at the column's 32 bytes of row block 0).
+template <typename GT, int NH, bool kV8, bool kRB>
+__device__ __forceinline__ void seg_load_block(SegBlock<NH>& x, int64_t b, const uint8_t* const (&col)[NH],
+                                               const bool (&has)[NH], int64_t ldb, const GT* __restrict__ g,
+                                               int64_t p0, int64_t p1, const uint8_t* __restrict__ fcol, uint32_t fsh,
+                                               uint32_t fmk) {
+  const int lane = threadIdx.x & 31;
+  const int64_t r0 = b << 5, pr = r0 + lane;
+  const bool in = pr >= p0 && pr < p1;
+  const bool second = r0 + 16 < p1;  // any row of the block's upper half is in range
+  const int64_t boff = kRB ? b * ldb : r0;  // the block's bytes of a column, from col[h]
+  x.fb = (fcol && in) ? static_cast<int>((fcol[boff + lane] >> fsh) & fmk) : 0;
+  x.gv = in ? static_cast<double>(g[pr]) : 0.0;
+#pragma unroll
+  for (int h = 0; h < NH; ++h) {
+    if (has[h]) {
+      load_rows32<kV8>(col[h] + boff, second, x.w[h]);
+    } else {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) x.w[h][k] = 0;
+    }
+  }
+}
+
 // Add the rows at positions [p0, p1) of one slot to the CTA's shared histograms.
 // With a filter (fcol != nullptr) only the rows whose decision fcol[p] > fbin
 // equals fside are added.
-// kRB: bins in the row-block layout (ldb is then the row-block pitch and col[h]
-// points at the feature's 32 bytes of row block 0).
 // kH: also the logistic hessian h = |g| (1 - |g|) of each row, in fixed point with scale_h.
 // A lane's byte is its slot's code: a feature's bin, or for a 4-bit slot the joint code of its two
 // features (first | second << 4), whose histogram the flush splits into the two.  The filter's
 // feature may sit in a 4-bit slot: its decision is (byte >> fsh) & fmk.
+// A warp takes every n_warps-th block and loads its next block before it counts the current one,
+// so the loads' latency is spent on the current block's atomics.
 template <typename GT, int NH, bool kV8, bool kRB, bool kH>
 __device__ __forceinline__ void seg_hist_rows(uint32_t base, const uint8_t* const (&col)[NH], const bool (&has)[NH],
                                               int64_t ldb, const GT* __restrict__ g, double scale, double scale_h,
@@ -268,47 +302,41 @@ __device__ __forceinline__ void seg_hist_rows(uint32_t base, const uint8_t* cons
                                               int fside, uint4* s_q, uint32_t fsh, uint32_t fmk) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, n_warps = blockDim.x >> 5;
   // aligned 32-position blocks covering [p0, p1); positions outside are masked
-  for (int64_t b = (p0 >> 5) + warp; (b << 5) < p1; b += n_warps) {
-    const int64_t r0 = b << 5;
-    const int64_t pr = r0 + lane;
+  int64_t b = (p0 >> 5) + warp;
+  if ((b << 5) >= p1) return;  // warp-uniform
+  SegBlock<NH> cur, nxt;
+  seg_load_block<GT, NH, kV8, kRB>(cur, b, col, has, ldb, g, p0, p1, fcol, fsh, fmk);
+  while (true) {
+    const int64_t bn = b + n_warps;
+    const bool more = (bn << 5) < p1;  // warp-uniform
+    if (more) seg_load_block<GT, NH, kV8, kRB>(nxt, bn, col, has, ldb, g, p0, p1, fcol, fsh, fmk);
+    const int64_t pr = (b << 5) + lane;
     const bool in = pr >= p0 && pr < p1;
-    const bool second = r0 + 16 < p1;  // any row of the block's upper half is in range
-    // all of the block's loads are issued before any of them is used: the filter byte, the gradient
-    // and the bins (the bins of a block whose rows are all filtered out are loaded for nothing)
-    const int64_t boff = kRB ? (r0 >> 5) * ldb : r0;  // the block's bytes of a feature, from col[h]
-    const int fb = (fcol && in) ? static_cast<int>((fcol[boff + lane] >> fsh) & fmk) : 0;
-    const double gv = in ? static_cast<double>(g[pr]) : 0.0;
-    uint32_t w[NH][8];
-#pragma unroll
-    for (int h = 0; h < NH; ++h) {
-      if (has[h]) {
-        load_rows32<kV8>(col[h] + boff, second, w[h]);
+    const bool v = in && (!fcol || (cur.fb > fbin) == (fside != 0));
+    const uint32_t valid = __ballot_sync(0xffffffffu, v);
+    if (valid != 0) {  // warp-uniform: some row of this block belongs to the slot
+      const int64_t q = v ? to_fixed(cur.gv, scale) : 0;
+      __syncwarp();
+      if constexpr (kH) {
+        const int64_t qh = v ? to_fixed(logistic_hess(cur.gv), scale_h) : 0;
+        s_q[lane] = make_uint4(static_cast<uint32_t>(static_cast<uint64_t>(q)), static_cast<uint32_t>(q >> 32),
+                               static_cast<uint32_t>(static_cast<uint64_t>(qh)), static_cast<uint32_t>(qh >> 32));
       } else {
-#pragma unroll
-        for (int k = 0; k < 8; ++k) w[h][k] = 0;
+        reinterpret_cast<uint2*>(s_q)[lane] =
+            make_uint2(static_cast<uint32_t>(static_cast<uint64_t>(q)), static_cast<uint32_t>(q >> 32));
+      }
+      __syncwarp();
+      if constexpr (kH) {
+        if (valid == 0xffffffffu) seg_rows32_h(base, cur.w[0], s_q);
+        else seg_rows_sparse_h(base, cur.w[0], s_q, valid);
+      } else {
+        if (valid == 0xffffffffu) seg_rows32<NH, true>(base, cur.w, s_q, valid);
+        else seg_rows_sparse<NH>(base, cur.w, s_q, valid);
       }
     }
-    const bool v = in && (!fcol || (fb > fbin) == (fside != 0));
-    const uint32_t valid = __ballot_sync(0xffffffffu, v);
-    if (valid == 0) continue;  // warp-uniform: no row of this block belongs to the slot
-    const int64_t q = v ? to_fixed(gv, scale) : 0;
-    __syncwarp();
-    if constexpr (kH) {
-      const int64_t qh = v ? to_fixed(logistic_hess(gv), scale_h) : 0;
-      s_q[lane] = make_uint4(static_cast<uint32_t>(static_cast<uint64_t>(q)), static_cast<uint32_t>(q >> 32),
-                             static_cast<uint32_t>(static_cast<uint64_t>(qh)), static_cast<uint32_t>(qh >> 32));
-    } else {
-      reinterpret_cast<uint2*>(s_q)[lane] =
-          make_uint2(static_cast<uint32_t>(static_cast<uint64_t>(q)), static_cast<uint32_t>(q >> 32));
-    }
-    __syncwarp();
-    if constexpr (kH) {
-      if (valid == 0xffffffffu) seg_rows32_h(base, w[0], s_q);
-      else seg_rows_sparse_h(base, w[0], s_q, valid);
-    } else {
-      if (valid == 0xffffffffu) seg_rows32<NH, true>(base, w, s_q, valid);
-      else seg_rows_sparse<NH>(base, w, s_q, valid);
-    }
+    if (!more) break;
+    b = bn;
+    cur = nxt;
   }
 }
 
