@@ -173,9 +173,11 @@ __device__ __forceinline__ void seg_rows32(uint32_t base, const uint32_t (&w)[NH
 }
 
 // Partial block (some rows outside the slot or filtered out): only the valid
-// rows are visited, word by word of the loaded bytes, so a row that does not
-// belong to the slot costs nothing.  The byte of row 4 * wi + k is selected
-// with a register selector.
+// rows are visited, a loaded word (four rows) at a time, so a row that does
+// not belong to the slot costs a uniform branch.  The low-word atomics of the
+// valid rows of each pair of a word's rows are issued before the first carry is
+// needed (pairs: a batch of four rows spills registers and runs slower).
+constexpr int kSparseBatch = 2;
 template <int NH>
 __device__ __forceinline__ void seg_rows_sparse(uint32_t base, const uint32_t (&w)[NH][8], const uint4* s_q,
                                                 uint32_t valid) {
@@ -183,18 +185,28 @@ __device__ __forceinline__ void seg_rows_sparse(uint32_t base, const uint32_t (&
   const uint2* s_q2 = reinterpret_cast<const uint2*>(s_q);
 #pragma unroll
   for (int wi = 0; wi < 8; ++wi) {
-    uint32_t m = (valid >> (4 * wi)) & 0xfu;  // warp-uniform
-    while (m != 0) {
-      const uint32_t k = __ffs(m) - 1;
-      m &= m - 1;
-      const uint2 q = s_q2[4 * wi + k];
-      uint32_t a[NH], old[NH];
+    const uint32_t m = (valid >> (4 * wi)) & 0xfu;  // warp-uniform
+    if (m == 0) continue;
 #pragma unroll
-      for (int h = 0; h < NH; ++h) a[h] = base + h * kHalfBytes + (__byte_perm(w[h][wi], 0u, 0x4440u | k) << 7);
+    for (int k0 = 0; k0 < 4; k0 += kSparseBatch) {
+      uint2 q[kSparseBatch];
+      uint32_t a[kSparseBatch][NH], old[kSparseBatch][NH];
 #pragma unroll
-      for (int h = 0; h < NH; ++h) old[h] = entry_lo<kLo>(a[h], q.x);
+      for (int j = 0; j < kSparseBatch; ++j) {
+        const int k = k0 + j;
+        if (!(m >> k & 1u)) continue;
+        q[j] = s_q2[4 * wi + k];
 #pragma unroll
-      for (int h = 0; h < NH; ++h) entry_hi<kHi>(a[h], q.x, static_cast<int32_t>(q.y), old[h]);
+        for (int h = 0; h < NH; ++h) a[j][h] = bin_addr(w[h][wi], k, base + h * kHalfBytes);
+#pragma unroll
+        for (int h = 0; h < NH; ++h) old[j][h] = entry_lo<kLo>(a[j][h], q[j].x);
+      }
+#pragma unroll
+      for (int j = 0; j < kSparseBatch; ++j) {
+        if (!(m >> (k0 + j) & 1u)) continue;
+#pragma unroll
+        for (int h = 0; h < NH; ++h) entry_hi<kHi>(a[j][h], q[j].x, static_cast<int32_t>(q[j].y), old[j][h]);
+      }
     }
   }
 }
