@@ -62,7 +62,8 @@ class Diagnostics(ctypes.Structure):
     _fields_ = [("hist_launches", ctypes.c_int64), ("hist_ms", ctypes.c_double), ("hist_bytes", ctypes.c_double),
                 ("hist_rows", ctypes.c_int64), ("part_ms", ctypes.c_double), ("part_bytes", ctypes.c_double),
                 ("total_ms", ctypes.c_double), ("kernel_launches", ctypes.c_int64),
-                ("trees_at_full_size", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+                ("trees_at_full_size", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("hist_level_bytes", ctypes.c_double)]
 
     def as_dict(self):
         return {k: getattr(self, k) for k, _ in self._fields_ if k != "reserved"}

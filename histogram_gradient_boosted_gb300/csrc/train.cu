@@ -602,8 +602,9 @@ extern "C" int gbdt_train(const uint8_t* bins, int64_t ldb, const int32_t* n_bin
           dg.hist_ms += ms;
           dg.hist_launches += 1;
           dg.hist_rows += ls.n_built_rows;
-          dg.hist_bytes += static_cast<double>(ls.n_scan_rows) * (row_bytes + (odd ? 1.0 : 0.0)) +
-                           static_cast<double>(ls.n_built) * F * kBins * (logistic ? 20.0 : 12.0);
+          const double out_bytes = static_cast<double>(ls.n_built) * F * kBins * (logistic ? 20.0 : 12.0);
+          dg.hist_bytes += static_cast<double>(ls.n_scan_rows) * (row_bytes + (odd ? 1.0 : 0.0)) + out_bytes;
+          dg.hist_level_bytes += static_cast<double>(ls.n_act) * (F + 8.0 + 2.0) + out_bytes;
         }
         GBDT_CUDA(cudaEventElapsedTime(&ms, ev_hist(t, d, 2), ev_hist(t, d, 3)));
         dg.part_ms += ms;

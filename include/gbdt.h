@@ -169,6 +169,11 @@ typedef struct gbdt_diagnostics {
   int64_t kernel_launches;   /* kernels launched by the call */
   int32_t trees_at_full_size; /* trees that reached 2^max_depth leaves */
   int32_t reserved;
+  double hist_level_bytes;   /* the same launches' bytes by the level formula, as if every row of
+                                the level's nodes were read once: rows x (F + 8 B gradient + 2 B
+                                node id) + built histograms x F x 256 x 12 B (20 B with H); the
+                                histogram reads fewer (hist_bytes: the smaller children's rows at a
+                                level after a move, both children's rows at the others) */
 } gbdt_diagnostics;
 
 /* Message of the last error on the calling thread ("" if none). */

@@ -76,7 +76,7 @@ def test_struct_layouts_match_header():
     assert g.NODE_DTYPE.itemsize == 40 and g.SPLIT_DTYPE.itemsize == 56
     assert g.SPLIT_DTYPE.fields["h_left"][1] == 40 and g.SPLIT_DTYPE.fields["h_total"][1] == 48
     assert g.LEVEL_DTYPE.itemsize == 8 and g.SEGMENT_DTYPE.itemsize == 16
-    assert ctypes.sizeof(g.Diagnostics) == 72
+    assert ctypes.sizeof(g.Diagnostics) == 80
 
 
 def test_entry_points_reject_bad_arguments_before_any_launch(lib):

@@ -125,6 +125,8 @@ def test_diagnostics_report_histogram_work():
     assert d["hist_ms"] > 0 and d["total_ms"] >= d["hist_ms"]
     assert d["hist_rows"] <= 3 * params["max_depth"] * 50_000 and d["hist_rows"] >= 3 * 50_000
     assert d["hist_bytes"] >= d["hist_rows"] * (28 + 10)
+    # the level formula counts every row of a level's nodes (every row at the root) once per level
+    assert d["hist_level_bytes"] >= 3 * 50_000 * (28 + 10) and d["hist_level_bytes"] >= d["hist_bytes"]
 
 
 @pytest.mark.parametrize("name,n,depth,budget,trees", [("covtype", 30_011, 10, 1023, 3), ("mid", 20_011, 6, 20, 3),
