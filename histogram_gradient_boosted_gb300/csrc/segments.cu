@@ -1142,7 +1142,7 @@ __global__ void __launch_bounds__(1024)
   }
 }
 
-__global__ void __launch_bounds__(kMvThreads, 4)
+__global__ void __launch_bounds__(kMvThreads, 5)
     pair_move_kernel(const __grid_constant__ CUtensorMap map_in, uint8_t* __restrict__ bins_out, int64_t pitch,
                      const uint8_t* __restrict__ bins_in, int32_t F,
                      const uint64_t* __restrict__ g_in, uint64_t* __restrict__ g_out,
