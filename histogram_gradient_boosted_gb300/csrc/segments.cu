@@ -382,7 +382,13 @@ __device__ __forceinline__ void seg_hist_flush(uint32_t* s_cnt, uint32_t* s_lo, 
     const int col = c_lo + (j < ns ? j : 0);
     sv[h] = src ? src[col] : (static_cast<uint32_t>(col) | 0xffff0000u);
   }
-  for (int e = threadIdx.x; e < entries; e += blockDim.x) {
+  // CTAs that flush the same slot at about the same time (every CTA at the root) start at different
+  // entries, so that their global atomics do not queue on the same addresses; the rotation is a
+  // multiple of 32, which keeps each entry in its lane
+  static_assert((entries & (entries - 1)) == 0, "entries is a power of two");
+  const int rot = (static_cast<int>(blockIdx.x) * 32 * 37) & (entries - 1);
+  for (int i = threadIdx.x; i < entries; i += blockDim.x) {
+    const int e = (i + rot) & (entries - 1);
     const uint32_t cn = s_cnt[e];
     if (cn == 0) continue;
     const int hh = e / kHalfWords;
