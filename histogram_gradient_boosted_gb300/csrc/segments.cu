@@ -1080,33 +1080,47 @@ __global__ void __launch_bounds__(kMvThreads)
     pair_count_kernel(const uint8_t* __restrict__ bins, int64_t pitch, const PairRoute* __restrict__ pairs,
                       const int32_t* __restrict__ tile_start, const PairState* __restrict__ st,
                       int4* __restrict__ tile_cnt) {
+  constexpr int U = 8;  // rows in flight per thread
   const int t = blockIdx.x;
   if (t >= st->total_tiles) return;
-  __shared__ int s_warp[33];
+  __shared__ int4 s_warp[kMvThreads / 32];
   const int k = slot_of_tile(tile_start, st->n_pairs, t);
   const PairRoute& pr = pairs[k];
   const int64_t p0 = pr.start + static_cast<int64_t>(t - tile_start[k]) * kMvTile;
   const int n = static_cast<int>(min(pr.start + pr.count - p0, static_cast<int64_t>(kMvTile)));
   int c[4] = {0, 0, 0, 0};
-  for (int j0 = threadIdx.x; j0 < n; j0 += 4 * blockDim.x) {  // four rows in flight per thread
-    int r[4];
+  for (int j0 = threadIdx.x; j0 < n; j0 += U * blockDim.x) {
+    int r[U];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
+    for (int u = 0; u < U; ++u) {
       const int j = j0 + u * blockDim.x;
       int child;
       r[u] = j < n ? pair_run(pr, bins, pitch, p0 + j, &child) : -1;
     }
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
+    for (int u = 0; u < U; ++u) {
       c[0] += r[u] == 0;
       c[1] += r[u] == 1;
       c[2] += r[u] == 2;
       c[3] += r[u] == 3;
     }
   }
-  int tot[4];
-  for (int r = 0; r < 4; ++r) block_scan_excl(c[r], s_warp, &tot[r]);
-  if (threadIdx.x == 0) tile_cnt[t] = make_int4(tot[0], tot[1], tot[2], tot[3]);
+  // the tile's four totals: warp sums by shuffles, then one warp adds the warps' sums
+  for (int o = 16; o > 0; o >>= 1) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) c[q] += __shfl_xor_sync(0xffffffffu, c[q], o);
+  }
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (lane == 0) s_warp[warp] = make_int4(c[0], c[1], c[2], c[3]);
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int4 tot = make_int4(0, 0, 0, 0);
+    for (int w = 0; w < kMvThreads / 32; ++w) {
+      const int4 v = s_warp[w];
+      tot.x += v.x, tot.y += v.y, tot.z += v.z, tot.w += v.w;
+    }
+    tile_cnt[t] = tot;
+  }
 }
 
 // One CTA: exclusive scan of each run's tile counts over all tiles; checks each
