@@ -1232,20 +1232,42 @@ __global__ void __launch_bounds__(kMvThreads, 5)
     ru.base[q] = acc;
     acc += len[q];
   }
+  // ---- the inverse permutation; the gradient and the row id of every moved row go straight to its
+  // output position (read in the tile's order, one coalesced load per chunk, written to at most four
+  // runs), four chunks' loads in flight, while the first column copies are in flight
   const uint32_t lt = (1u << lane) - 1u;
 #pragma unroll 1
-  for (int kk = 0; kk < kMvChunksPerWarp; ++kk) {
-    const int ch = warp * kMvChunksPerWarp + kk;
+  for (int k0 = 0; k0 < kMvChunksPerWarp; k0 += 4) {
+    uint64_t gv[4];
+    uint32_t ov[4];
+    int64_t dst[4];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const uint32_t m = s_mask[q][ch];
-      if (m >> lane & 1u) s_inv[ru.base[q] + s_cbase[q][ch] + __popc(m & lt)] = static_cast<uint16_t>(ch * 32 + lane);
+    for (int u = 0; u < 4; ++u) {
+      const int ch = warp * kMvChunksPerWarp + k0 + u;
+      dst[u] = -1;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint32_t m = s_mask[q][ch];
+        if (m >> lane & 1u) {
+          const int o = s_cbase[q][ch] + __popc(m & lt);  // the row's rank in its run
+          s_inv[ru.base[q] + o] = static_cast<uint16_t>(ch * 32 + lane);
+          dst[u] = ru.dst[q] + o;
+        }
+      }
+      if (dst[u] >= 0) {
+        gv[u] = g_in[p0 + ch * 32 + lane];
+        ov[u] = orig_in[p0 + ch * 32 + lane];
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      if (dst[u] >= 0) {
+        g_out[dst[u]] = gv[u];
+        orig_out[dst[u]] = ov[u];
+      }
     }
   }
   __syncthreads();
-  // ---- gradient and row id, while the first column copies are in flight
-  move_positions(g_in, g_out, p0, ru, s_inv);
-  move_positions(orig_in, orig_out, p0, ru, s_inv);
   int64_t wa[kMvWordsPerThread];
   uint32_t srcl[kMvWordsPerThread], srch[kMvWordsPerThread];
   mv_own_words<4, true>(ru, s_inv, a_off, pitch, wa, srcl, srch);
