@@ -1175,7 +1175,7 @@ __global__ void __launch_bounds__(kMvThreads, 5)
   __shared__ uint16_t s_inv[kMvTile];
   __shared__ __align__(128) uint8_t s_stage[kMvStages][kMvStageBytes];
   __shared__ __align__(8) uint64_t s_full[kMvStages];
-  __shared__ int s_warp[33];
+  __shared__ int s_wtot[kMvThreads / 32][4];
   const int t = blockIdx.x;
   if (t >= st->total_tiles) return;
   // the destinations come from the split records: if any run disagreed with its record (raised by
@@ -1214,12 +1214,36 @@ __global__ void __launch_bounds__(kMvThreads, 5)
     }
   }
   __syncthreads();
+  // each run's rows before each chunk: the four exclusive scans over the chunks in one pass (a warp
+  // per 32 chunks: shuffles; then the warps' totals)
   int len[4];
+  {
+    int c[4], e[4];
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const int c = threadIdx.x < kMvChunks ? __popc(s_mask[q][threadIdx.x]) : 0;
-    const int e = block_scan_excl(c, s_warp, &len[q]);
-    if (threadIdx.x < kMvChunks) s_cbase[q][threadIdx.x] = e;
+    for (int q = 0; q < 4; ++q) {
+      c[q] = threadIdx.x < kMvChunks ? __popc(s_mask[q][threadIdx.x]) : 0;
+      e[q] = c[q];
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, e[q], o);
+        if (lane >= o) e[q] += v;
+      }
+    }
+    if (lane == 31) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) s_wtot[warp][q] = e[q];
+    }
+    __syncthreads();
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      int before = 0, all = 0;
+      for (int w = 0; w < kMvThreads / 32; ++w) {
+        const int v = s_wtot[w][q];
+        before += w < warp ? v : 0;
+        all += v;
+      }
+      len[q] = all;
+      if (threadIdx.x < kMvChunks) s_cbase[q][threadIdx.x] = before + e[q] - c[q];
+    }
   }
   __syncthreads();
   MvRuns<4> ru;
