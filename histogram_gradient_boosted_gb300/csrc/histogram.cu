@@ -235,7 +235,8 @@ __global__ void __launch_bounds__(kHistThreads, 1)
 
 __global__ void hist_zero_kernel(const gbdt_level* __restrict__ level, int32_t max_slots,
                                  const uint8_t* __restrict__ build_flag, int32_t F, uint32_t* __restrict__ hist_cnt,
-                                 int64_t* __restrict__ hist_q, int64_t* __restrict__ hist_h) {
+                                 int64_t* __restrict__ hist_q, int64_t* __restrict__ hist_h,
+                                 const uint32_t* __restrict__ cnt0) {
   const int n_slots = min(level->n_slots, max_slots);
   const int slot = blockIdx.y;
   if (slot >= n_slots || !build_flag[slot]) return;
@@ -244,7 +245,7 @@ __global__ void hist_zero_kernel(const gbdt_level* __restrict__ level, int32_t m
   int64_t* q = hist_q + slot * per_slot;
   int64_t* h = hist_h ? hist_h + slot * per_slot : nullptr;
   for (int64_t e = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; e < per_slot; e += (int64_t)gridDim.x * blockDim.x) {
-    c[e] = 0;
+    c[e] = (cnt0 && slot == 0) ? cnt0[e] : 0u;
     q[e] = 0;
     if (h) h[e] = 0;
   }
@@ -313,10 +314,10 @@ HistPlan plan_histograms(int64_t N, int32_t F, int32_t max_slots, int32_t max_bu
 }
 
 void launch_hist_zero(const gbdt_level* level, int32_t max_slots, const uint8_t* build_flag, int32_t F,
-                      uint32_t* hist_cnt, int64_t* hist_q, int64_t* hist_h, cudaStream_t s) {
+                      uint32_t* hist_cnt, int64_t* hist_q, int64_t* hist_h, cudaStream_t s, const uint32_t* cnt0) {
   const int64_t per_slot = static_cast<int64_t>(F) * kBins;
   dim3 grid(static_cast<unsigned>((per_slot + 1023) / 1024), static_cast<unsigned>(max_slots));
-  hist_zero_kernel<<<grid, 256, 0, s>>>(level, max_slots, build_flag, F, hist_cnt, hist_q, hist_h);
+  hist_zero_kernel<<<grid, 256, 0, s>>>(level, max_slots, build_flag, F, hist_cnt, hist_q, hist_h, cnt0);
   count_launches();
 }
 

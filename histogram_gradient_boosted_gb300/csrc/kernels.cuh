@@ -38,9 +38,11 @@ struct HistPlan {
   int blocks() const { return n_sgroups * n_fgroups * n_chunks; }
 };
 HistPlan plan_histograms(int64_t N, int32_t F, int32_t max_slots, int32_t max_build);
-// Zeroes the flagged slots of hist_cnt/hist_q (and hist_h when not null).
+// Zeroes the flagged slots of hist_cnt/hist_q (and hist_h when not null); cnt0 (not null): slot 0's
+// counts are copied from cnt0 ([F][256]) instead.
 void launch_hist_zero(const gbdt_level* level, int32_t max_slots, const uint8_t* build_flag, int32_t F,
-                      uint32_t* hist_cnt, int64_t* hist_q, int64_t* hist_h, cudaStream_t s);
+                      uint32_t* hist_cnt, int64_t* hist_q, int64_t* hist_h, cudaStream_t s,
+                      const uint32_t* cnt0 = nullptr);
 int launch_hist_build(const HistPlan& plan, const uint8_t* bins, int64_t ldb, int64_t N, int32_t F, const void* g,
                       int32_t g_dtype, const int32_t* fixed_exp, const uint16_t* node_of_row,
                       const gbdt_level* level, int32_t max_slots, const uint8_t* build_flag, uint32_t* hist_cnt,
@@ -90,10 +92,13 @@ int launch_seg_histograms(const SegHistPlan& plan, const uint8_t* bins, int64_t 
                           int32_t max_slots, const uint8_t* build_flag, const gbdt_segment* seg,
                           const gbdt_filter* filters, void* scratch, uint32_t* hist_cnt, int64_t* hist_q,
                           int64_t* hist_h, cudaStream_t s, bool row_blocks = false, const uint32_t* floc = nullptr,
-                          const uint32_t* slot_src = nullptr);
+                          const uint32_t* slot_src = nullptr, const uint32_t* root_cnt = nullptr);
 // row_blocks: ldb is the row-block pitch, floc the feature locators and slot_src each slot's features
 // (plan_row_block_slots; null: slot s holds feature s); a lane accumulates its slot's byte, the joint
 // code of a 4-bit slot, and the flush splits it into the two features' bins.  hist_h: plan.with_h.
+// root_cnt (row blocks, fp64 g, a one-slot level only): the slot's count histogram [F][256], known
+// beforehand (the root's counts depend on the bins alone); it is copied in and the kernel adds only
+// G (and H), one shared atomic fewer per row and slot.
 // Stable partition of the per-position data of every split slot (bins columns, g, original row
 // id) from *_in to *_out; slots without a split record leaf_of_row[orig] = their node id.
 size_t move_scratch_bytes(int64_t N, int32_t max_slots);

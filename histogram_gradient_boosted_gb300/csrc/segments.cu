@@ -106,15 +106,21 @@ constexpr uint32_t kHalfBytes = kHalfWords * 4;
 // and a skipped add would cost a branch, not a wavefront.  addr is the
 // shared-memory byte address of the entry's count word; the low and high
 // words sit kLo and kHi bytes above it.
-template <uint32_t kLo>
+// kCnt false: the counts are known (the root level after the first tree: a row set's counts do not
+// depend on the gradients), only the low word is added.
+template <uint32_t kLo, bool kCnt = true>
 __device__ __forceinline__ uint32_t entry_lo(uint32_t addr, uint32_t ql) {
   uint32_t old;
-  asm volatile(
-      "red.shared.add.u32 [%1], 1;\n\t"
-      "atom.shared.add.u32 %0, [%1+%3], %2;"
-      : "=r"(old)
-      : "r"(addr), "r"(ql), "n"(kLo)
-      : "memory");
+  if constexpr (kCnt) {
+    asm volatile(
+        "red.shared.add.u32 [%1], 1;\n\t"
+        "atom.shared.add.u32 %0, [%1+%3], %2;"
+        : "=r"(old)
+        : "r"(addr), "r"(ql), "n"(kLo)
+        : "memory");
+  } else {
+    asm volatile("atom.shared.add.u32 %0, [%1+%2], %3;" : "=r"(old) : "r"(addr), "n"(kLo), "r"(ql) : "memory");
+  }
   return old;
 }
 
@@ -144,7 +150,7 @@ __device__ __forceinline__ uint32_t bin_addr(uint32_t w, int k, uint32_t base) {
 
 // Rows i and i + 1 of the block, every half: the low-word atomics of all of
 // them are issued before the first carry is needed.
-template <int NH, bool kFull>
+template <int NH, bool kFull, bool kCnt>
 __device__ __forceinline__ void seg_rows32(uint32_t base, const uint32_t (&w)[NH][8], const uint4* s_q,
                                            uint32_t valid) {
   constexpr uint32_t kLo = NH * kHalfBytes, kHi = 2 * NH * kHalfBytes;
@@ -161,8 +167,8 @@ __device__ __forceinline__ void seg_rows32(uint32_t base, const uint32_t (&w)[NH
       for (int h = 0; h < NH; ++h) a[r][h] = bin_addr(w[h][(i + r) >> 2], (i + r) & 3, base + h * kHalfBytes);
 #pragma unroll
     for (int h = 0; h < NH; ++h) {
-      if (use0) old[0][h] = entry_lo<kLo>(a[0][h], qq.x);
-      if (use1) old[1][h] = entry_lo<kLo>(a[1][h], qq.z);
+      if (use0) old[0][h] = entry_lo<kLo, kCnt>(a[0][h], qq.x);
+      if (use1) old[1][h] = entry_lo<kLo, kCnt>(a[1][h], qq.z);
     }
 #pragma unroll
     for (int h = 0; h < NH; ++h) {
@@ -178,7 +184,7 @@ __device__ __forceinline__ void seg_rows32(uint32_t base, const uint32_t (&w)[NH
 // valid rows of each pair of a word's rows are issued before the first carry is
 // needed (pairs: a batch of four rows spills registers and runs slower).
 constexpr int kSparseBatch = 2;
-template <int NH>
+template <int NH, bool kCnt>
 __device__ __forceinline__ void seg_rows_sparse(uint32_t base, const uint32_t (&w)[NH][8], const uint4* s_q,
                                                 uint32_t valid) {
   constexpr uint32_t kLo = NH * kHalfBytes, kHi = 2 * NH * kHalfBytes;
@@ -199,7 +205,7 @@ __device__ __forceinline__ void seg_rows_sparse(uint32_t base, const uint32_t (&
 #pragma unroll
         for (int h = 0; h < NH; ++h) a[j][h] = bin_addr(w[h][wi], k, base + h * kHalfBytes);
 #pragma unroll
-        for (int h = 0; h < NH; ++h) old[j][h] = entry_lo<kLo>(a[j][h], q[j].x);
+        for (int h = 0; h < NH; ++h) old[j][h] = entry_lo<kLo, kCnt>(a[j][h], q[j].x);
       }
 #pragma unroll
       for (int j = 0; j < kSparseBatch; ++j) {
@@ -216,13 +222,14 @@ __device__ __forceinline__ void seg_rows_sparse(uint32_t base, const uint32_t (&
 // G high, H low, H high).  Full block: two rows at a time, their four returning atomics first.
 constexpr uint32_t kHLo = 3 * kHalfBytes, kHHi = 4 * kHalfBytes;
 
+template <bool kCnt>
 __device__ __forceinline__ void seg_rows32_h(uint32_t base, const uint32_t (&w)[8], const uint4* s_q) {
 #pragma unroll
   for (int i = 0; i < 32; i += 2) {
     const uint4 q0 = s_q[i], q1 = s_q[i + 1];
     const uint32_t a0 = bin_addr(w[i >> 2], i & 3, base), a1 = bin_addr(w[(i + 1) >> 2], (i + 1) & 3, base);
-    const uint32_t og0 = entry_lo<kHalfBytes>(a0, q0.x), oh0 = atom_lo<kHLo>(a0, q0.z);
-    const uint32_t og1 = entry_lo<kHalfBytes>(a1, q1.x), oh1 = atom_lo<kHLo>(a1, q1.z);
+    const uint32_t og0 = entry_lo<kHalfBytes, kCnt>(a0, q0.x), oh0 = atom_lo<kHLo>(a0, q0.z);
+    const uint32_t og1 = entry_lo<kHalfBytes, kCnt>(a1, q1.x), oh1 = atom_lo<kHLo>(a1, q1.z);
     entry_hi<2 * kHalfBytes>(a0, q0.x, static_cast<int32_t>(q0.y), og0);
     entry_hi<kHHi>(a0, q0.z, static_cast<int32_t>(q0.w), oh0);
     entry_hi<2 * kHalfBytes>(a1, q1.x, static_cast<int32_t>(q1.y), og1);
@@ -231,6 +238,7 @@ __device__ __forceinline__ void seg_rows32_h(uint32_t base, const uint32_t (&w)[
 }
 
 // Partial block with H: the valid rows only, as seg_rows_sparse.
+template <bool kCnt>
 __device__ __forceinline__ void seg_rows_sparse_h(uint32_t base, const uint32_t (&w)[8], const uint4* s_q,
                                                   uint32_t valid) {
 #pragma unroll
@@ -241,7 +249,7 @@ __device__ __forceinline__ void seg_rows_sparse_h(uint32_t base, const uint32_t 
       m &= m - 1;
       const uint4 q = s_q[4 * wi + k];
       const uint32_t a = base + (__byte_perm(w[wi], 0u, 0x4440u | k) << 7);
-      const uint32_t og = entry_lo<kHalfBytes>(a, q.x), oh = atom_lo<kHLo>(a, q.z);
+      const uint32_t og = entry_lo<kHalfBytes, kCnt>(a, q.x), oh = atom_lo<kHLo>(a, q.z);
       entry_hi<2 * kHalfBytes>(a, q.x, static_cast<int32_t>(q.y), og);
       entry_hi<kHHi>(a, q.z, static_cast<int32_t>(q.w), oh);
     }
@@ -307,7 +315,7 @@ __device__ __forceinline__ void seg_load_block(SegBlock<NH>& x, int64_t b, const
 // feature may sit in a 4-bit slot: its decision is (byte >> fsh) & fmk.
 // A warp takes every n_warps-th block and loads its next block before it counts the current one,
 // so the loads' latency is spent on the current block's atomics.
-template <typename GT, int NH, bool kV8, bool kRB, bool kH>
+template <typename GT, int NH, bool kV8, bool kRB, bool kH, bool kCnt>
 __device__ __forceinline__ void seg_hist_rows(uint32_t base, const uint8_t* const (&col)[NH], const bool (&has)[NH],
                                               int64_t ldb, const GT* __restrict__ g, double scale, double scale_h,
                                               int64_t p0, int64_t p1, const uint8_t* __restrict__ fcol, int fbin,
@@ -339,11 +347,11 @@ __device__ __forceinline__ void seg_hist_rows(uint32_t base, const uint8_t* cons
       }
       __syncwarp();
       if constexpr (kH) {
-        if (valid == 0xffffffffu) seg_rows32_h(base, cur.w[0], s_q);
-        else seg_rows_sparse_h(base, cur.w[0], s_q, valid);
+        if (valid == 0xffffffffu) seg_rows32_h<kCnt>(base, cur.w[0], s_q);
+        else seg_rows_sparse_h<kCnt>(base, cur.w[0], s_q, valid);
       } else {
-        if (valid == 0xffffffffu) seg_rows32<NH, true>(base, cur.w, s_q, valid);
-        else seg_rows_sparse<NH>(base, cur.w, s_q, valid);
+        if (valid == 0xffffffffu) seg_rows32<NH, true, kCnt>(base, cur.w, s_q, valid);
+        else seg_rows_sparse<NH, kCnt>(base, cur.w, s_q, valid);
       }
     }
     if (!more) break;
@@ -358,15 +366,16 @@ __device__ __forceinline__ void seg_hist_rows(uint32_t base, const uint8_t* cons
 // of the bins (a slot): src (the slot's features: first | second << 16, second
 // 0xffff for a whole-byte slot; null: slot s is feature s) sends a 4-bit slot's
 // joint entry to both features' bins.
+template <bool kCnt>
 __device__ __forceinline__ void flush_add(uint32_t* __restrict__ hist_cnt, int64_t* __restrict__ hist_q,
                                           int64_t* __restrict__ hist_h, int64_t o, uint32_t cn, int64_t v,
                                           int64_t vh) {
-  atomicAdd(hist_cnt + o, cn);
+  if (kCnt) atomicAdd(hist_cnt + o, cn);
   atomicAdd(reinterpret_cast<unsigned long long*>(hist_q + o), static_cast<unsigned long long>(v));
   if (hist_h) atomicAdd(reinterpret_cast<unsigned long long*>(hist_h + o), static_cast<unsigned long long>(vh));
 }
 
-template <int NH, bool kH>
+template <int NH, bool kH, bool kCnt>
 __device__ __forceinline__ void seg_hist_flush(uint32_t* s_cnt, uint32_t* s_lo, int32_t* s_hi, int slot, int32_t F,
                                                int c_lo, int ns, const uint32_t* __restrict__ src,
                                                uint32_t* __restrict__ hist_cnt, int64_t* __restrict__ hist_q,
@@ -390,7 +399,9 @@ __device__ __forceinline__ void seg_hist_flush(uint32_t* s_cnt, uint32_t* s_lo, 
   for (int i = threadIdx.x; i < entries; i += blockDim.x) {
     const int e = (i + rot) & (entries - 1);
     const uint32_t cn = s_cnt[e];
-    if (cn == 0) continue;
+    if (kCnt ? cn == 0 : (s_lo[e] | static_cast<uint32_t>(s_hi[e]) |
+                          (kH ? s_hlo[e] | static_cast<uint32_t>(s_hhi[e]) : 0u)) == 0u)
+      continue;  // nothing to add (without counts: every word of the entry is zero)
     const int hh = e / kHalfWords;
     const int j = (hh << 5) + (e & 31);  // column within the group
     const int64_t v = static_cast<int64_t>(s_hi[e]) * 4294967296ll + static_cast<int64_t>(s_lo[e]);
@@ -412,10 +423,10 @@ __device__ __forceinline__ void seg_hist_flush(uint32_t* s_cnt, uint32_t* s_lo, 
     const int64_t fa = static_cast<int64_t>(svh & 0xffffu), fb = static_cast<int64_t>(svh >> 16);
     const int64_t row = static_cast<int64_t>(slot) * F;
     if (fb == 0xffff) {
-      flush_add(hist_cnt, hist_q, kH ? hist_h : nullptr, (row + fa) * kBins + code, cn, v, vh);
+      flush_add<kCnt>(hist_cnt, hist_q, kH ? hist_h : nullptr, (row + fa) * kBins + code, cn, v, vh);
     } else {  // a 4-bit slot: the joint entry adds to each feature's own bin
-      flush_add(hist_cnt, hist_q, kH ? hist_h : nullptr, (row + fa) * kBins + (code & 15), cn, v, vh);
-      flush_add(hist_cnt, hist_q, kH ? hist_h : nullptr, (row + fb) * kBins + (code >> 4), cn, v, vh);
+      flush_add<kCnt>(hist_cnt, hist_q, kH ? hist_h : nullptr, (row + fa) * kBins + (code & 15), cn, v, vh);
+      flush_add<kCnt>(hist_cnt, hist_q, kH ? hist_h : nullptr, (row + fb) * kBins + (code >> 4), cn, v, vh);
     }
   }
 }
@@ -425,7 +436,8 @@ __device__ __forceinline__ void seg_hist_flush(uint32_t* s_cnt, uint32_t* s_lo, 
 // per CTA, so the level runs as one balanced wave.  A share that crosses
 // slot boundaries flushes its histograms at each crossing.  kH (logistic):
 // also the H histograms, up to 32 features per CTA, fixed_exp[1] their exponent.
-template <typename GT, bool kV8, bool kRB, bool kH>
+// kCnt false: the counts are already in place (copied by the zeroing launch), only G (and H) add.
+template <typename GT, bool kV8, bool kRB, bool kH, bool kCnt = true>
 __global__ void __launch_bounds__(kSegThreads, 1)
     seg_hist_kernel(const uint8_t* __restrict__ bins, int64_t ldb, int32_t F, int32_t S, const GT* __restrict__ g,
                     const int32_t* __restrict__ fixed_exp, const gbdt_segment* __restrict__ seg,
@@ -496,10 +508,10 @@ __global__ void __launch_bounds__(kSegThreads, 1)
       const uint32_t floc_f = fl.feature < 0 ? 0u : unpack ? floc[fl.feature] : static_cast<uint32_t>(fl.feature);
       const uint8_t* fcol =
           fl.feature >= 0 ? bins + static_cast<int64_t>(loc_slot(floc_f)) * (kRB ? kRowBlock : ldb) : nullptr;
-      seg_hist_rows<GT, NH, kV8, kRB, kH>(base, col, has, ldb, g, scale, scale_h, p0, p0 + (r_end - r), fcol, fl.bin,
+      seg_hist_rows<GT, NH, kV8, kRB, kH, kCnt>(base, col, has, ldb, g, scale, scale_h, p0, p0 + (r_end - r), fcol, fl.bin,
                                           fl.side, s_q, loc_shift(floc_f), loc_mask(floc_f));
       __syncthreads();
-      seg_hist_flush<NH, kH>(s_cnt, s_lo, s_hi, slot, F, c_lo, ns, kRB ? slot_src : nullptr, hist_cnt, hist_q,
+      seg_hist_flush<NH, kH, kCnt>(s_cnt, s_lo, s_hi, slot, F, c_lo, ns, kRB ? slot_src : nullptr, hist_cnt, hist_q,
                              hist_h);
       __syncthreads();
     }
@@ -1419,13 +1431,17 @@ int launch_seg_histograms(const SegHistPlan& plan, const uint8_t* bins, int64_t 
                           int32_t max_slots, const uint8_t* build_flag, const gbdt_segment* seg,
                           const gbdt_filter* filters, void* scratch, uint32_t* hist_cnt, int64_t* hist_q,
                           int64_t* hist_h, cudaStream_t s, bool row_blocks, const uint32_t* floc,
-                          const uint32_t* slot_src) {
+                          const uint32_t* slot_src, const uint32_t* root_cnt) {
   (void)N;
+  if (root_cnt && !(row_blocks && g_dtype == GBDT_DTYPE_F64 && max_slots == 1)) {
+    set_error("known root counts need the row-block layout, fp64 gradients and a one-slot level");
+    return GBDT_ERR_INTERNAL;
+  }
   Carve c(scratch, seg_hist_scratch_bytes(max_slots));
   SegWork* st = c.take<SegWork>(1);
   int32_t* build_slot = c.take<int32_t>(max_slots + 1);
   int64_t* row_start = c.take<int64_t>(max_slots + 1);
-  launch_hist_zero(level, max_slots, build_flag, F, hist_cnt, hist_q, plan.with_h ? hist_h : nullptr, s);
+  launch_hist_zero(level, max_slots, build_flag, F, hist_cnt, hist_q, plan.with_h ? hist_h : nullptr, s, root_cnt);
   seg_work_setup_kernel<<<1, 1024, 0, s>>>(level, max_slots, build_flag, seg, plan.max_ctas, plan.min_rows,
                                            build_slot, row_start, st);
   count_launches();
@@ -1448,7 +1464,11 @@ int launch_seg_histograms(const SegHistPlan& plan, const uint8_t* bins, int64_t 
                       : launch(seg_hist_kernel<GT, false, false, kH>, gp);
   };
   int rc;
-  if (g_dtype == GBDT_DTYPE_F32) {
+  if (root_cnt) {  // the root's counts are known: G (and H) only
+    const double* gp = static_cast<const double*>(g);
+    rc = plan.with_h ? launch(seg_hist_kernel<double, true, true, true, false>, gp)
+                     : launch(seg_hist_kernel<double, true, true, false, false>, gp);
+  } else if (g_dtype == GBDT_DTYPE_F32) {
     const float* gp = static_cast<const float*>(g);
     rc = plan.with_h ? pick(gp, std::true_type{}) : pick(gp, std::false_type{});
   } else {

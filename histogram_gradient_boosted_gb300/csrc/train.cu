@@ -248,6 +248,7 @@ struct TrainWs {
   uint32_t* hist_cnt[2];
   int64_t* hist_q[2];
   int64_t* hist_h[2];  // logistic only (else null)
+  uint32_t* root_cnt;  // the root's count histogram [F][256] (the same for every tree of a call)
   gbdt_split* splits;
   void* split_scratch;
   SlotTotals* totals[2];
@@ -303,6 +304,7 @@ TrainWs carve_train(void* ws, size_t bytes, int64_t N, int32_t F, int64_t ldb, c
     w.hist_q[i] = c.take<int64_t>(hist_entries);
     w.hist_h[i] = logistic ? c.take<int64_t>(hist_entries) : nullptr;
   }
+  w.root_cnt = c.take<uint32_t>(static_cast<size_t>(F) * kBins);
   w.splits = c.take<gbdt_split>(level_slots);
   w.split_scratch = c.take<unsigned char>(find_splits_scratch_bytes(F, static_cast<int32_t>(hist_slots)));
   for (int i = 0; i < 2; ++i) {
@@ -478,11 +480,17 @@ extern "C" int gbdt_train(const uint8_t* bins, int64_t ldb, const int32_t* n_bin
           hseg = w.scan;
           hfil = w.filters;
         }
+        // the root's counts depend on the bins alone: the first tree counts them, the others copy them
+        // and add only G (and H)
         rc = launch_seg_histograms(plan, lb, pitch, N, F, lg, GBDT_DTYPE_F64, w.fixed_exp, w.level[cur], max_slots,
                                    w.build[cur], hseg, hfil, w.seg_scratch, w.hist_cnt[cur], w.hist_q[cur],
-                                   w.hist_h[cur], s, true, w.floc, w.slot_src);
+                                   w.hist_h[cur], s, true, w.floc, w.slot_src,
+                                   d == 0 && t > 0 ? w.root_cnt : nullptr);
         if (rc != GBDT_OK) return rc;
         if (timing) GBDT_CUDA(cudaEventRecord(ev_hist(t, d, 1), s));
+        if (d == 0 && t == 0)
+          GBDT_CUDA(cudaMemcpyAsync(w.root_cnt, w.hist_cnt[cur], sizeof(uint32_t) * F * kBins,
+                                    cudaMemcpyDeviceToDevice, s));
         if (d > 0) {
           launch_hist_subtract(w.hist_cnt[nxt], w.hist_q[nxt], w.hist_h[nxt], w.pair_parent[cur], w.build[cur],
                                w.level[cur], max_slots, F, w.hist_cnt[cur], w.hist_q[cur], w.hist_h[cur], w.err, s);
