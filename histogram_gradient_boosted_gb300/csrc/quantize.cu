@@ -120,29 +120,64 @@ __global__ void __launch_bounds__(256) radix_digit_scan_kernel(uint32_t* __restr
   t[threadIdx.x] = s[threadIdx.x] - v;
 }
 
-// Stable scatter: keys of a tile, taken in order 256 at a time; equal digits
-// inside a warp are ranked with ballots, across warps and rounds with counters.
+// Stable scatter of one tile (kQTile keys): the keys are ranked into shared memory in (digit,
+// original order) - taken 256 at a time, equal digits inside a warp ranked with ballots, across warps
+// and rounds with counters - and each digit's run of the tile is then written out with consecutive
+// addresses (a warp's stores cover one or two runs instead of up to 32).
 __global__ void __launch_bounds__(kQThreads)
     radix_scatter_kernel(const uint32_t* __restrict__ in, uint32_t* __restrict__ out, int64_t N, int tiles, int shift,
                          const uint32_t* __restrict__ offsets, const uint32_t* __restrict__ dbase) {
   constexpr int kWarps = kQThreads / 32;
-  __shared__ uint32_t s_base[256];       // running position of each digit in this tile
+  static_assert(kQThreads == 256, "one thread per digit");
+  __shared__ uint32_t s_keys[kQTile];     // the tile's keys, ranked
+  __shared__ uint32_t s_start[256];       // each digit's first position in s_keys
+  __shared__ uint32_t s_run[256];         // each digit's next position in s_keys
+  __shared__ uint32_t s_gbase[256];       // the global position of the tile's first key of each digit
   __shared__ uint32_t s_wc[kWarps][256];  // per-warp count, then per-warp start, of each digit
+  __shared__ uint32_t s_warp[kWarps];
   const int j = blockIdx.y, t = blockIdx.x;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  s_base[threadIdx.x] =
-      dbase[j * 256 + threadIdx.x] + offsets[(static_cast<int64_t>(j) * 256 + threadIdx.x) * tiles + t];
   const uint32_t* k = in + j * N;
   uint32_t* o = out + j * N;
   const int64_t b0 = static_cast<int64_t>(t) * kQTile;
+  const int n = static_cast<int>(min(static_cast<int64_t>(kQTile), N - b0));
+  uint32_t key[kQRounds];
+#pragma unroll
+  for (int r = 0; r < kQRounds; ++r) {
+    const int li = r * kQThreads + static_cast<int>(threadIdx.x);
+    key[r] = li < n ? k[b0 + li] : 0u;
+  }
+  // the tile's count of each digit, then its exclusive scan over the digits (thread d: digit d)
+  s_run[threadIdx.x] = 0;
+  __syncthreads();
+#pragma unroll
+  for (int r = 0; r < kQRounds; ++r)
+    if (r * kQThreads + static_cast<int>(threadIdx.x) < n) atomicAdd(&s_run[(key[r] >> shift) & 0xff], 1u);
+  __syncthreads();
+  {
+    const uint32_t c = s_run[threadIdx.x];
+    uint32_t incl = c;
+    for (int d = 1; d < 32; d <<= 1) {
+      const uint32_t v = __shfl_up_sync(0xffffffffu, incl, d);
+      if (lane >= d) incl += v;
+    }
+    if (lane == 31) s_warp[warp] = incl;
+    __syncthreads();
+    uint32_t before = 0;
+    for (int w = 0; w < warp; ++w) before += s_warp[w];
+    const uint32_t excl = before + incl - c;
+    s_start[threadIdx.x] = excl;
+    s_run[threadIdx.x] = excl;
+    s_gbase[threadIdx.x] =
+        dbase[j * 256 + threadIdx.x] + offsets[(static_cast<int64_t>(j) * 256 + threadIdx.x) * tiles + t];
+  }
   const uint32_t lt = (1u << lane) - 1u;
+#pragma unroll
   for (int r = 0; r < kQRounds; ++r) {
     for (int w = 0; w < kWarps; ++w) s_wc[w][threadIdx.x] = 0;
     __syncthreads();
-    const int64_t i = b0 + r * kQThreads + threadIdx.x;
-    const bool valid = i < N;
-    const uint32_t key = valid ? k[i] : 0u;
-    const uint32_t dg = (key >> shift) & 0xff;
+    const bool valid = r * kQThreads + static_cast<int>(threadIdx.x) < n;
+    const uint32_t dg = (key[r] >> shift) & 0xff;
     uint32_t peers = __ballot_sync(0xffffffffu, valid);
 #pragma unroll
     for (int b = 0; b < 8; ++b) {
@@ -152,19 +187,25 @@ __global__ void __launch_bounds__(kQThreads)
     const uint32_t rank = __popc(peers & lt);
     if (valid && rank == 0) s_wc[warp][dg] = __popc(peers);
     __syncthreads();
-    {  // thread d: exclusive prefix over warps of digit d, advance the running base
+    {  // thread d: exclusive prefix over warps of digit d, advance the running position
       const int d = threadIdx.x;
-      uint32_t run = s_base[d];
+      uint32_t run = s_run[d];
       for (int w = 0; w < kWarps; ++w) {
         const uint32_t c = s_wc[w][d];
         s_wc[w][d] = run;
         run += c;
       }
-      s_base[d] = run;
+      s_run[d] = run;
     }
     __syncthreads();
-    if (valid) o[s_wc[warp][dg] + rank] = key;
-    __syncthreads();
+    if (valid) s_keys[s_wc[warp][dg] + rank] = key[r];
+    __syncthreads();  // every thread has read its start before the next round clears them
+  }
+  for (int i = threadIdx.x; i < n; i += kQThreads) {
+    const uint32_t x = s_keys[i];
+    const uint32_t dg = (x >> shift) & 0xff;
+    const int64_t p = static_cast<int64_t>(s_gbase[dg]) + (i - static_cast<int64_t>(s_start[dg]));
+    if (p >= 0 && p < N) o[p] = x;  // always: the tile's counts and the scans agree
   }
 }
 
