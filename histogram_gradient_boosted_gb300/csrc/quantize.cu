@@ -300,6 +300,21 @@ __global__ void __launch_bounds__(256)
   if (threadIdx.x == 0) n_bins[j0 + j] = ne + 1;
 }
 
+// Number of the column's edges strictly below x (binary search over the ne edges in shared memory).
+__device__ __forceinline__ uint32_t bin_of(const float* s_e, int ne, float x) {
+  int lo = 0, hi = ne;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (s_e[mid] < x) lo = mid + 1;
+    else hi = mid;
+  }
+  return static_cast<uint32_t>(lo);
+}
+
+// kVec: X's columns 16-byte aligned (X aligned, ldx % 4 == 0): four values per thread per step (one
+// 16-byte load, four independent searches, one 4-byte store; bins' columns are 16-byte aligned),
+// the last N % 4 values of a column by the first CTA of its row.
+template <bool kVec>
 __global__ void bin_kernel(const float* __restrict__ X, int64_t ldx, int64_t N, int j0, int B,
                            const float* __restrict__ edges, const int32_t* __restrict__ n_bins,
                            uint8_t* __restrict__ bins, int64_t ldb) {
@@ -308,16 +323,24 @@ __global__ void bin_kernel(const float* __restrict__ X, int64_t ldx, int64_t N, 
   const int ne = n_bins[j] - 1;
   for (int k = threadIdx.x; k < ne; k += blockDim.x) s_e[k] = edges[static_cast<int64_t>(j) * (B - 1) + k];
   __syncthreads();
-  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < N; i += (int64_t)gridDim.x * blockDim.x) {
-    const float x = X[j * ldx + i];
-    int lo = 0, hi = ne;  // number of edges strictly below x
-    while (lo < hi) {
-      const int mid = (lo + hi) >> 1;
-      if (s_e[mid] < x) lo = mid + 1;
-      else hi = mid;
+  const float* xc = X + j * ldx;
+  uint8_t* bc = bins + j * ldb;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  int64_t i0 = 0;
+  if (kVec) {
+    const int64_t n4 = N / 4;
+    for (int64_t q = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; q < n4; q += stride) {
+      const float4 x = *reinterpret_cast<const float4*>(xc + 4 * q);
+      const uint32_t b = bin_of(s_e, ne, x.x) | bin_of(s_e, ne, x.y) << 8 | bin_of(s_e, ne, x.z) << 16 |
+                         bin_of(s_e, ne, x.w) << 24;
+      *reinterpret_cast<uint32_t*>(bc + 4 * q) = b;
     }
-    bins[j * ldb + i] = static_cast<uint8_t>(lo);
+    if (blockIdx.x != 0) return;
+    i0 = 4 * n4;
   }
+  for (int64_t i = i0 + (kVec ? 0 : blockIdx.x * static_cast<int64_t>(blockDim.x)) + threadIdx.x; i < N;
+       i += kVec ? blockDim.x : stride)
+    bc[i] = static_cast<uint8_t>(bin_of(s_e, ne, xc[i]));
 }
 
 int batch_columns(int64_t N, int32_t F) {
@@ -412,7 +435,10 @@ extern "C" int gbdt_quantize(const float* X, int64_t ldx, int64_t N, int32_t F, 
     count_launches();
     edges_kernel<<<nb, 256, 0, s>>>(src, N, j0, max_bins, w.chunk_cnt, w.chunk_vals, edges, n_bins);
     count_launches();
-    bin_kernel<<<dim3(gx, nb), 256, 0, s>>>(X, ldx, N, j0, max_bins, edges, n_bins, bins, ldb);
+    if (aligned(X, 16) && ldx % 4 == 0)
+      bin_kernel<true><<<dim3(gx, nb), 256, 0, s>>>(X, ldx, N, j0, max_bins, edges, n_bins, bins, ldb);
+    else
+      bin_kernel<false><<<dim3(gx, nb), 256, 0, s>>>(X, ldx, N, j0, max_bins, edges, n_bins, bins, ldb);
     count_launches();
     GBDT_LAUNCH_CHECK();
   }
