@@ -77,7 +77,8 @@ struct Route {
 struct SegHistPlan {
   int n_cols;        // columns the lanes read: slots of the row blocks (features in the column layout)
   int n_fgroups, group_feats;  // groups of columns (full groups of group_feats and the remainder)
-  int total_weight;  // sum over groups of (32-lane halves + 1)
+  int row_weight;    // a group's weight is its 32-lane halves + row_weight (see seg_hist_kernel)
+  int total_weight;  // sum over groups of (32-lane halves + row_weight)
   int sm_budget;     // CTAs of one wave, shared by the groups in proportion to their weights
   int max_ctas;      // CTAs of a full group
   int64_t min_rows;  // least work (rows + a fixed cost per slot) a CTA takes when the level is small
@@ -85,7 +86,9 @@ struct SegHistPlan {
   size_t smem;
 };
 // S: the columns the lanes read (slots of the row blocks; F in the column layout).
-SegHistPlan plan_seg_histograms(int64_t N, int32_t S, int32_t max_slots, int32_t max_build, bool with_h = false);
+// filtered: the level's slots are counted through filters (a node's rows inside its pair's segment).
+SegHistPlan plan_seg_histograms(int64_t N, int32_t S, int32_t max_slots, int32_t max_build, bool with_h = false,
+                                bool filtered = false);
 size_t seg_hist_scratch_bytes(int32_t max_slots);
 int launch_seg_histograms(const SegHistPlan& plan, const uint8_t* bins, int64_t ldb, int64_t N, int32_t F,
                           const void* g, int32_t g_dtype, const int32_t* fixed_exp, const gbdt_level* level,

@@ -443,17 +443,18 @@ __global__ void __launch_bounds__(kSegThreads, 1)
                     const int32_t* __restrict__ fixed_exp, const gbdt_segment* __restrict__ seg,
                     const gbdt_filter* __restrict__ filters, const int32_t* __restrict__ build_slot,
                     const int64_t* __restrict__ row_start, const SegWork* __restrict__ st, int32_t group_cols,
-                    int32_t sm_budget, int32_t total_weight, uint32_t* __restrict__ hist_cnt,
+                    int32_t sm_budget, int32_t total_weight, int32_t row_weight, uint32_t* __restrict__ hist_cnt,
                     int64_t* __restrict__ hist_q, int64_t* __restrict__ hist_h, const uint32_t* __restrict__ floc,
                     const uint32_t* __restrict__ slot_src) {
   extern __shared__ __align__(16) unsigned char smem[];
-  // this CTA's group: columns (slots) [c_lo, c_lo + ns) of the bins.  A CTA's time per row is about
-  // one half's atomics for each of its halves plus as much again for the row itself (its gradient,
-  // staging, ballots), so groups get CTAs in proportion to halves + 1
+  // this CTA's group: columns (slots) [c_lo, c_lo + ns) of the bins.  Groups get CTAs in proportion
+  // to their 32-lane halves + row_weight: where every scanned row is counted a CTA's time per row is
+  // about its halves' atomics (row_weight 0); where a filter skips about half of the scanned rows
+  // the row's own work (loads, ballots, the returned values' latency) adds about one half (1)
   const int c_lo = blockIdx.y * group_cols;
   const int ns = min(group_cols, S - c_lo);
   if (ns <= 0) return;
-  const int weight = ((ns + 31) >> 5) + 1;
+  const int weight = ((ns + 31) >> 5) + row_weight;
   const int cap = max(1, static_cast<int>(static_cast<int64_t>(sm_budget) * weight / total_weight));
   const int ctas = min(st->ctas, cap);
   if (static_cast<int>(blockIdx.x) >= ctas) return;
@@ -1399,7 +1400,8 @@ cudaError_t smem_attr(K kernel, size_t bytes) {
 }  // namespace
 
 // ---- plans and launchers ------------------------------------------------------------------------
-SegHistPlan plan_seg_histograms(int64_t N, int32_t S, int32_t max_slots, int32_t max_build, bool with_h) {
+SegHistPlan plan_seg_histograms(int64_t N, int32_t S, int32_t max_slots, int32_t max_build, bool with_h,
+                                bool filtered) {
   (void)N, (void)max_slots, (void)max_build;
   SegHistPlan p{};
   const int max_feats = with_h ? 32 : kSegMaxFeats;  // five shared words per entry with H, three without
@@ -1409,11 +1411,13 @@ SegHistPlan plan_seg_histograms(int64_t N, int32_t S, int32_t max_slots, int32_t
   p.n_fgroups = ceil_div(S, max_feats);
   p.group_feats = p.n_fgroups == 1 ? S : max_feats;
   const int rem = S - (p.n_fgroups - 1) * p.group_feats;
-  // a group's weight: its halves + 1 (see seg_hist_kernel)
-  p.total_weight = (p.n_fgroups - 1) * (ceil_div(p.group_feats, 32) + 1) + ceil_div(rem, 32) + 1;
+  // a group's weight: its halves + row_weight (see seg_hist_kernel; measured on the 10M x 100 levels,
+  // 64 + 26 slots: 2 : 1 fastest where every scanned row counts, 3 : 2 at the filtered levels)
+  p.row_weight = filtered ? 1 : 0;
+  p.total_weight = (p.n_fgroups - 1) * (ceil_div(p.group_feats, 32) + p.row_weight) + ceil_div(rem, 32) + p.row_weight;
   p.sm_budget = sm_count();  // one wave: a CTA per SM, shared by the groups in proportion to their weights
-  p.max_ctas = std::max(1, static_cast<int>(static_cast<int64_t>(p.sm_budget) * (ceil_div(p.group_feats, 32) + 1) /
-                                            p.total_weight));
+  p.max_ctas = std::max(1, static_cast<int>(static_cast<int64_t>(p.sm_budget) *
+                                            (ceil_div(p.group_feats, 32) + p.row_weight) / p.total_weight));
   p.min_rows = 1024;  // least cost (rows + kSlotCost per slot) per CTA
   p.with_h = with_h;
   const size_t words = with_h ? 5 : 3, stage = with_h ? 512 : 256;  // staged row records per warp
@@ -1452,6 +1456,7 @@ int launch_seg_histograms(const SegHistPlan& plan, const uint8_t* bins, int64_t 
     GBDT_CUDA(smem_attr(kernel, plan.smem));
     kernel<<<grid, kSegThreads, plan.smem, s>>>(bins, ldb, F, plan.n_cols, gp, fixed_exp, seg, filters, build_slot,
                                                 row_start, st, plan.group_feats, plan.sm_budget, plan.total_weight,
+                                                plan.row_weight,
                                                 hist_cnt, hist_q, hist_h, row_blocks ? floc : nullptr,
                                                 row_blocks ? slot_src : nullptr);
     return GBDT_OK;
@@ -1735,7 +1740,7 @@ int build_segmented(const char* fn, const uint8_t* bins, int64_t ldb, int32_t la
     return ws ? GBDT_ERR_WORKSPACE : GBDT_ERR_INVALID_ARG;
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const SegHistPlan plan = plan_seg_histograms(N, F, max_slots, max_build, with_h);
+  const SegHistPlan plan = plan_seg_histograms(N, F, max_slots, max_build, with_h, filters != nullptr);
   int rc = launch_seg_histograms(plan, bins, ldb, N, F, g, g_dtype, fixed_exp, level, max_slots, build_flag, segments,
                                  filters, ws, hist_cnt, hist_q, hist_h, s, layout == GBDT_LAYOUT_ROW_BLOCKS);
   if (rc != GBDT_OK) return rc;

@@ -470,7 +470,7 @@ extern "C" int gbdt_train(const uint8_t* bins, int64_t ldb, const int32_t* n_bin
       const uint32_t* lo = ph < 0 ? w.orig0 : w.orig_xy[ph];
       if (d < D) {
         const int max_build = d == 0 ? 1 : max_slots / 2;
-        const SegHistPlan plan = plan_seg_histograms(N, S, max_slots, max_build, logistic);
+        const SegHistPlan plan = plan_seg_histograms(N, S, max_slots, max_build, logistic, odd);
         if (timing) GBDT_CUDA(cudaEventRecord(ev_hist(t, d, 0), s));
         const gbdt_segment* hseg = w.seg[cur];
         const gbdt_filter* hfil = nullptr;
