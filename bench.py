@@ -31,6 +31,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -147,12 +148,20 @@ class ClockSampler:
 HIST_SOURCES = [os.path.join("histogram_gradient_boosted_gb300", "csrc", f) for f in ("segments.cu", "train.cu")]
 
 
+def _code_only(text: str) -> str:
+    """C++/CUDA source without its comments and blank lines (string literals here hold no comment
+    markers), so that a comment edit does not count as a change of the kernel."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    lines = (re.sub(r"//.*$", "", ln).rstrip() for ln in text.splitlines())
+    return "\n".join(ln for ln in lines if ln.strip())
+
+
 def hist_source_sha256() -> str:
-    """Hash of the sources that define the level-histogram launches (the kernel and the level loop)."""
+    """Hash of the code that defines the level-histogram launches (the kernel and the level loop)."""
     h = hashlib.sha256()
     for rel in HIST_SOURCES:
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()
 
 

@@ -1118,7 +1118,7 @@ __global__ void __launch_bounds__(kMvThreads)
       c[3] += r[u] == 3;
     }
   }
-  // the tile's four totals: warp sums by shuffles, then one warp adds the warps' sums
+  // the tile's four totals: warp sums by shuffles, then thread 0 adds the warps' sums
   for (int o = 16; o > 0; o >>= 1) {
 #pragma unroll
     for (int q = 0; q < 4; ++q) c[q] += __shfl_xor_sync(0xffffffffu, c[q], o);
