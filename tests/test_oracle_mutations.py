@@ -17,6 +17,7 @@ from tests import test_oracle_pins as pins
 from tests import test_oracle_predict as tp
 from tests import test_oracle_budget as tb
 from tests import test_oracle_logistic as tl
+from tests import test_oracle_update as tu
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
@@ -50,6 +51,13 @@ MUTATIONS = {
     "histogram H ignores the hessian": ("hh[b] += h ? h[r] : 1.0;", "hh[b] += 1.0;"),
     "node H ignores the hessian": ("HP += hv ? hv[rows[k]] : 1.0;", "HP += 1.0;"),
     "level histograms ignore the hessian": ("      H[o] += hr;", "      H[o] += 1.0;"),
+    "update step subtracted": ("    pred[i] = pred[i] + step;", "    pred[i] = pred[i] - step;"),
+    "update without learning rate": ("const double step = lr * leaf_value[node_of_row[i]];",
+                                     "const double step = leaf_value[node_of_row[i]];"),
+    "update reads the leaf of the row index": ("const double step = lr * leaf_value[node_of_row[i]];",
+                                               "const double step = lr * leaf_value[i];"),
+    "update fused multiply-add": ("const double step = lr * leaf_value[node_of_row[i]];\n    pred[i] = pred[i] + step;",
+                                  "pred[i] = fma(lr, leaf_value[node_of_row[i]], pred[i]);"),
     "feature index transposed": ("const uint8_t* col = bins + (int64_t)j * N;\n    uint32_t* c", "const uint8_t* col = bins + (int64_t)(F - 1 - j) * N;\n    uint32_t* c"),
 }
 
@@ -70,6 +78,8 @@ PINS = [
     ("logistic hand tree", lambda o: tl.test_hand_tree_depth_one(o)),
     ("logistic second tree", lambda o: tl.test_second_tree_uses_new_margins(o)),
     ("logistic histograms", lambda o: tl.test_histograms_with_hessians_brute_force(o)),
+    ("update hand values", lambda o: tu.test_hand_values_exact_fractions(o)),
+    ("update rounding order", lambda o: tu.test_product_rounded_before_the_sum(o)),
     ("predict = training",
      lambda o: tp.test_prediction_of_training_rows_equals_training_predictions("tiny", 3, 2, o=o)),
 ]
