@@ -42,6 +42,7 @@ EXPORTED_SYMBOLS = [
     "gbdt_partition_rows", "gbdt_predict_workspace_size", "gbdt_predict", "gbdt_row_block_pitch",
     "gbdt_row_block_bytes", "gbdt_bins_to_row_blocks", "gbdt_compute_gradients_objective",
     "gbdt_subtract_histograms_h", "gbdt_build_histograms_segmented_h", "gbdt_find_splits_h", "gbdt_row_block_slots",
+    "gbdt_workspace_status", "gbdt_partition_noalloc_status", "gbdt_subtract_histograms_workspace_size",
 ]
 
 
@@ -103,8 +104,11 @@ def lib():
         "gbdt_gradient_scale": ([P, i32, i64, P, P, sz, P], i32),
         "gbdt_histograms_workspace_size": ([i64, i32, i32], sz),
         "gbdt_build_histograms": ([P, i64, i64, i32, P, i32, P, P, P, i32, P, i32, P, P, P, sz, P], i32),
-        "gbdt_subtract_histograms": ([P, P, P, P, P, i32, i32, P, P, P], i32),
-        "gbdt_subtract_histograms_h": ([P, P, P, P, P, P, i32, i32, P, P, P, P], i32),
+        "gbdt_subtract_histograms_workspace_size": ([], sz),
+        "gbdt_subtract_histograms": ([P, P, P, P, P, i32, i32, P, P, P, sz, P], i32),
+        "gbdt_subtract_histograms_h": ([P, P, P, P, P, P, i32, i32, P, P, P, P, sz, P], i32),
+        "gbdt_workspace_status": ([P, P, P], i32),
+        "gbdt_partition_noalloc_status": ([P, P], i32),
         "gbdt_find_splits_workspace_size": ([i32, i32], sz),
         "gbdt_find_splits": ([P, P, P, i32, P, P, i32, P, P, P, sz, P], i32),
         "gbdt_find_splits_h": ([P, P, P, P, i32, P, P, i32, P, P, P, sz, P], i32),
@@ -330,26 +334,45 @@ def partition_rows(bins_in, N, g_in, orig_in, splits, level, max_slots, seg_in, 
 
 
 def subtract_histograms(prev_cnt, prev_q, pair_parent, build_flag, level, max_slots, hist_cnt, hist_q, prev_h=None,
-                        hist_h=None):
+                        hist_h=None, ws=None):
+    """Sibling subtraction; ws (optional, a workspace of gbdt_subtract_histograms_workspace_size bytes) receives
+    the call's error word (see workspace_status)."""
     F = hist_cnt.shape[1]
+    wp, wn = (_ptr(ws), ws.numel()) if ws is not None else (None, 0)
     if prev_h is None and hist_h is None:
         _check(lib().gbdt_subtract_histograms(_ptr(prev_cnt), _ptr(prev_q), _ptr(pair_parent), _ptr(build_flag),
-                                              _ptr(level), max_slots, F, _ptr(hist_cnt), _ptr(hist_q), _stream()))
+                                              _ptr(level), max_slots, F, _ptr(hist_cnt), _ptr(hist_q), wp, wn,
+                                              _stream()))
         return hist_cnt, hist_q
     _check(lib().gbdt_subtract_histograms_h(_ptr(prev_cnt), _ptr(prev_q), _ptr(prev_h), _ptr(pair_parent),
                                             _ptr(build_flag), _ptr(level), max_slots, F, _ptr(hist_cnt),
-                                            _ptr(hist_q), _ptr(hist_h), _stream()))
+                                            _ptr(hist_q), _ptr(hist_h), wp, wn, _stream()))
     return hist_cnt, hist_q, hist_h
 
 
-def find_splits(hist_cnt, hist_q, fixed_exp, n_bins, level, max_slots, out=None, hist_h=None, **params):
+def workspace_status(ws) -> int:
+    """Error word of the last call queued with workspace ws (synchronises the stream): 0, else GbdtError."""
+    bits = ctypes.c_int32(0)
+    _check(lib().gbdt_workspace_status(_ptr(ws), ctypes.byref(bits), _stream()))
+    return bits.value
+
+
+def partition_noalloc_status() -> int:
+    """Error word of the last gbdt_partition_noalloc call on this device: 0, else GbdtError."""
+    bits = ctypes.c_int32(0)
+    _check(lib().gbdt_partition_noalloc_status(ctypes.byref(bits), _stream()))
+    return bits.value
+
+
+def find_splits(hist_cnt, hist_q, fixed_exp, n_bins, level, max_slots, out=None, hist_h=None, ws=None, **params):
     """Best split per slot (SPLIT_DTYPE bytes, device); hist_h: H from that histogram (exponent fixed_exp[1])."""
     torch = _torch()
     F = hist_cnt.shape[1]
     p = make_params(**params)
     if out is None:
         out = torch.empty(max_slots * SPLIT_DTYPE.itemsize, dtype=torch.uint8, device="cuda")
-    ws = _workspace(lib().gbdt_find_splits_workspace_size(F, max_slots))
+    if ws is None:
+        ws = _workspace(lib().gbdt_find_splits_workspace_size(F, max_slots))
     if hist_h is None:
         _check(lib().gbdt_find_splits(_ptr(hist_cnt), _ptr(hist_q), _ptr(fixed_exp), F, _ptr(n_bins), _ptr(level),
                                       max_slots, ctypes.byref(p), _ptr(out), _ptr(ws), ws.numel(), _stream()))
@@ -360,14 +383,15 @@ def find_splits(hist_cnt, hist_q, fixed_exp, n_bins, level, max_slots, out=None,
     return out
 
 
-def partition(bins, N, splits, level, max_slots, seg_in, idx_in, node_of_row, idx_out=None):
+def partition(bins, N, splits, level, max_slots, seg_in, idx_in, node_of_row, idx_out=None, ws=None):
     torch = _torch()
     F, ldb = bins.shape
     if idx_out is None:
         idx_out = torch.zeros_like(idx_in)
     seg_out = torch.zeros(2 * max_slots * SEGMENT_DTYPE.itemsize, dtype=torch.uint8, device="cuda")
     next_level = torch.zeros(LEVEL_DTYPE.itemsize, dtype=torch.uint8, device="cuda")
-    ws = _workspace(lib().gbdt_partition_workspace_size(N, max_slots))
+    if ws is None:
+        ws = _workspace(lib().gbdt_partition_workspace_size(N, max_slots))
     _check(lib().gbdt_partition(_ptr(bins), ldb, N, F, _ptr(splits), _ptr(level), max_slots, _ptr(seg_in),
                                 _ptr(idx_in), _ptr(node_of_row), _ptr(idx_out), _ptr(seg_out), _ptr(next_level),
                                 _ptr(ws), ws.numel(), _stream()))

@@ -20,6 +20,27 @@ void set_error(const char* fmt, ...) {
 
 void clear_error() { t_msg[0] = '\0'; }
 
+int report_error_bits(const char* what, int32_t bits) {
+  if (bits == 0) return GBDT_OK;
+  char names[256] = "";
+  const struct {
+    int32_t bit;
+    const char* name;
+  } known[] = {{kErrHistTotals, "histogram totals"},
+               {kErrSlotRange, "node id outside the level"},
+               {kErrPartitionCount, "partition count differs from the split record"},
+               {kErrLevelSize, "level larger than max_slots"},
+               {kErrWaitTimeout, "asynchronous copy wait limit"},
+               {kErrBinRange, "bin not below n_bins"}};
+  for (const auto& k : known) {
+    if (!(bits & k.bit)) continue;
+    const size_t used = strlen(names);
+    snprintf(names + used, sizeof(names) - used, "%s%s", used ? "; " : "", k.name);
+  }
+  set_error("%s: device consistency check failed (error bits 0x%x: %s)", what, bits, names);
+  return (bits & ~kErrBinRange) ? GBDT_ERR_INTERNAL : GBDT_ERR_INVALID_ARG;
+}
+
 namespace {
 std::atomic<int64_t> g_launches{0};
 }
@@ -86,3 +107,18 @@ extern "C" int gbdt_validate_params(const gbdt_params* p) {
 }
 
 extern "C" int64_t gbdt_kernel_launch_count(void) { return gbdt::launch_count(); }
+
+extern "C" int gbdt_workspace_status(const void* ws, int32_t* bits, void* stream) {
+  gbdt::clear_error();
+  if (bits) *bits = 0;
+  if (!ws || !gbdt::aligned(ws, gbdt::kWsAlign)) {
+    gbdt::set_error("gbdt_workspace_status: ws must be a 256-byte aligned workspace");
+    return GBDT_ERR_INVALID_ARG;
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int32_t h = 0;
+  GBDT_CUDA(cudaMemcpyAsync(&h, ws, sizeof(int32_t), cudaMemcpyDeviceToHost, s));
+  GBDT_CUDA(cudaStreamSynchronize(s));
+  if (bits) *bits = h;
+  return gbdt::report_error_bits("gbdt_workspace_status", h);
+}

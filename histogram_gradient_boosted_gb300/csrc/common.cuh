@@ -29,6 +29,9 @@ enum : int32_t {
 // ---- thread-local error message -------------------------------------------------
 void set_error(const char* fmt, ...);
 void clear_error();
+// GBDT_OK for bits == 0; otherwise sets the message (naming each bit) and returns GBDT_ERR_INTERNAL,
+// or GBDT_ERR_INVALID_ARG when the only bit is kErrBinRange (a caller's input out of range).
+int report_error_bits(const char* what, int32_t bits);
 
 #define GBDT_CHECK_ARG(cond, ...)         \
   do {                                    \

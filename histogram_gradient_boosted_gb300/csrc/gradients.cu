@@ -241,7 +241,7 @@ using namespace gbdt;
 
 extern "C" size_t gbdt_gradients_workspace_size(int64_t N) {
   (void)N;
-  return kWsAlign;  // two 8-byte max accumulators
+  return 2 * kWsAlign;  // the error word (no check here: it stays 0), then two 8-byte max accumulators
 }
 
 extern "C" int gbdt_compute_gradients_objective(const double* pred, const float* label, int64_t N,
@@ -257,7 +257,8 @@ extern "C" int gbdt_compute_gradients_objective(const double* pred, const float*
     return ws ? GBDT_ERR_WORKSPACE : GBDT_ERR_INVALID_ARG;
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  auto* maxabs = static_cast<unsigned long long*>(ws);
+  GBDT_CUDA(cudaMemsetAsync(ws, 0, sizeof(int32_t), s));
+  auto* maxabs = reinterpret_cast<unsigned long long*>(static_cast<char*>(ws) + kWsAlign);
   GBDT_CUDA(cudaMemsetAsync(maxabs, 0, 2 * sizeof(*maxabs), s));
   launch_gradients(pred, label, N, objective, g, maxabs, s);
   launch_fixed_exp(maxabs, N, fixed_exp, objective == GBDT_OBJECTIVE_LOGISTIC, s);
@@ -283,7 +284,8 @@ extern "C" int gbdt_gradient_scale(const void* g, int32_t g_dtype, int64_t N, in
     return ws ? GBDT_ERR_WORKSPACE : GBDT_ERR_INVALID_ARG;
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  auto* maxabs = static_cast<unsigned long long*>(ws);
+  GBDT_CUDA(cudaMemsetAsync(ws, 0, sizeof(int32_t), s));
+  auto* maxabs = reinterpret_cast<unsigned long long*>(static_cast<char*>(ws) + kWsAlign);
   GBDT_CUDA(cudaMemsetAsync(maxabs, 0, sizeof(*maxabs), s));
   launch_maxabs(g, g_dtype, N, maxabs, s);
   launch_fixed_exp(maxabs, N, fixed_exp, false, s);

@@ -391,7 +391,8 @@ extern "C" int gbdt_build_histograms(const uint8_t* bins, int64_t ldb, int64_t N
     return ws ? GBDT_ERR_WORKSPACE : GBDT_ERR_INVALID_ARG;
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  int32_t* err = static_cast<int32_t*>(ws);
+  int32_t* err = static_cast<int32_t*>(ws);  // the call's error word (gbdt_workspace_status)
+  GBDT_CUDA(cudaMemsetAsync(err, 0, sizeof(int32_t), s));
   const HistPlan plan = plan_histograms(N, F, max_slots, max_build);
   launch_hist_zero(level, max_slots, build_flag, F, hist_cnt, hist_q, nullptr, s);
   int rc = launch_hist_build(plan, bins, ldb, N, F, g, g_dtype, fixed_exp, node_of_row, level, max_slots,
@@ -401,10 +402,13 @@ extern "C" int gbdt_build_histograms(const uint8_t* bins, int64_t ldb, int64_t N
   return GBDT_OK;
 }
 
+extern "C" size_t gbdt_subtract_histograms_workspace_size(void) { return kWsAlign; }
+
 extern "C" int gbdt_subtract_histograms_h(const uint32_t* prev_cnt, const int64_t* prev_q, const int64_t* prev_h,
                                           const int32_t* pair_parent, const uint8_t* build_flag,
                                           const gbdt_level* level, int32_t max_slots, int32_t F, uint32_t* hist_cnt,
-                                          int64_t* hist_q, int64_t* hist_h, void* stream) {
+                                          int64_t* hist_q, int64_t* hist_h, void* ws, size_t ws_bytes,
+                                          void* stream) {
   clear_error();
   GBDT_CHECK_ARG(prev_cnt && prev_q && pair_parent && build_flag && level && hist_cnt && hist_q,
                  "gbdt_subtract_histograms: null pointer");
@@ -412,15 +416,23 @@ extern "C" int gbdt_subtract_histograms_h(const uint32_t* prev_cnt, const int64_
                  "be given or both be NULL");
   GBDT_CHECK_ARG(max_slots >= 2 && max_slots <= kMaxSlots && F >= 1 && F <= 4096,
                  "gbdt_subtract_histograms: sizes out of range");
+  if (ws && (ws_bytes < gbdt_subtract_histograms_workspace_size() || !aligned(ws, kWsAlign))) {
+    set_error("gbdt_subtract_histograms: workspace too small or misaligned");
+    return GBDT_ERR_WORKSPACE;
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int32_t* err = static_cast<int32_t*>(ws);  // optional: the call's error word (gbdt_workspace_status)
+  if (err) GBDT_CUDA(cudaMemsetAsync(err, 0, sizeof(int32_t), s));
   launch_hist_subtract(prev_cnt, prev_q, prev_h, pair_parent, build_flag, level, max_slots, F, hist_cnt, hist_q,
-                       hist_h, nullptr, static_cast<cudaStream_t>(stream));
+                       hist_h, err, s);
   GBDT_LAUNCH_CHECK();
   return GBDT_OK;
 }
 
 extern "C" int gbdt_subtract_histograms(const uint32_t* prev_cnt, const int64_t* prev_q, const int32_t* pair_parent,
                                         const uint8_t* build_flag, const gbdt_level* level, int32_t max_slots,
-                                        int32_t F, uint32_t* hist_cnt, int64_t* hist_q, void* stream) {
+                                        int32_t F, uint32_t* hist_cnt, int64_t* hist_q, void* ws, size_t ws_bytes,
+                                        void* stream) {
   return gbdt_subtract_histograms_h(prev_cnt, prev_q, nullptr, pair_parent, build_flag, level, max_slots, F, hist_cnt,
-                                    hist_q, nullptr, stream);
+                                    hist_q, nullptr, ws, ws_bytes, stream);
 }

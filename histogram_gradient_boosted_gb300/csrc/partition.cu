@@ -397,10 +397,44 @@ constexpr int kNoAllocMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_partition_scratch[kNoAllocScratchBytes];
 
-std::mutex g_noalloc_mu;
-void* g_noalloc_ptr[kNoAllocMaxDevices] = {};
+// The array's device address is looked up once per device and context: a cached address is reused
+// only while the context it was taken in is the current one (a device reset, or a primary context
+// released and created again, gives a new context and a new lookup).  Contexts are told apart by
+// the driver's context id, which is never reused within a process.
+using CtxGetCurrent = CUresult (*)(CUcontext*);
+using CtxGetId = CUresult (*)(CUcontext, unsigned long long*);
 
-// Device address of the scratch array on the current device, looked up once per device.
+struct NoAllocEntry {
+  unsigned long long ctx_id;
+  void* ptr;
+};
+std::mutex g_noalloc_mu;
+NoAllocEntry g_noalloc[kNoAllocMaxDevices] = {};
+
+// Id of the current context (0 when there is none yet or the driver entry points are unavailable:
+// then the address is looked up, which also creates the device's primary context).
+unsigned long long current_context_id() {
+  static CtxGetCurrent get_ctx = nullptr;
+  static CtxGetId get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_ctx = reinterpret_cast<CtxGetCurrent>(fn);
+    fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<CtxGetId>(fn);
+  });
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (!get_ctx || !get_id || get_ctx(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
+// Device address of the scratch array in the current device's context.
 int noalloc_scratch(void** out) {
   int dev = -1;
   GBDT_CUDA(cudaGetDevice(&dev));
@@ -408,13 +442,16 @@ int noalloc_scratch(void** out) {
     set_error("gbdt_partition_noalloc: device %d outside the supported range", dev);
     return GBDT_ERR_INVALID_ARG;
   }
+  const unsigned long long id = current_context_id();
   std::lock_guard<std::mutex> lock(g_noalloc_mu);
-  if (!g_noalloc_ptr[dev]) {
+  NoAllocEntry& e = g_noalloc[dev];
+  if (!e.ptr || id == 0 || e.ctx_id != id) {
     void* p = nullptr;
     GBDT_CUDA(cudaGetSymbolAddress(&p, g_partition_scratch));
-    g_noalloc_ptr[dev] = p;
+    e.ptr = p;
+    e.ctx_id = id;
   }
-  *out = g_noalloc_ptr[dev];
+  *out = e.ptr;
   return GBDT_OK;
 }
 
@@ -462,4 +499,20 @@ extern "C" int gbdt_partition_noalloc(const uint8_t* bins, int64_t ldb, int64_t 
   count_launches();
   GBDT_LAUNCH_CHECK();
   return GBDT_OK;
+}
+
+extern "C" int gbdt_partition_noalloc_status(int32_t* bits, void* stream) {
+  clear_error();
+  if (bits) *bits = 0;
+  void* scratch = nullptr;
+  int rc = noalloc_scratch(&scratch);
+  if (rc != GBDT_OK) return rc;
+  size_t need = 0;
+  const PartWs w = carve_partition(scratch, kNoAllocScratchBytes, 1, 1, &need);  // the error word leads the carve
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int32_t h = 0;
+  GBDT_CUDA(cudaMemcpyAsync(&h, w.err, sizeof(int32_t), cudaMemcpyDeviceToHost, s));
+  GBDT_CUDA(cudaStreamSynchronize(s));
+  if (bits) *bits = h;
+  return report_error_bits("gbdt_partition_noalloc_status", h);
 }

@@ -1681,7 +1681,7 @@ int make_row_block_map(CUtensorMap* map, const uint8_t* rb, int64_t N, int32_t S
 using namespace gbdt;
 
 extern "C" size_t gbdt_histograms_segmented_workspace_size(int32_t max_slots) {
-  return seg_hist_scratch_bytes(max_slots);
+  return kWsAlign + seg_hist_scratch_bytes(max_slots);  // the error word, then the level's work list
 }
 
 extern "C" int64_t gbdt_row_block_pitch(int32_t F) { return F >= 1 ? rb_pitch(F) : 0; }
@@ -1735,14 +1735,18 @@ int build_segmented(const char* fn, const uint8_t* bins, int64_t ldb, int32_t la
   GBDT_CHECK_ARG(g_dtype == GBDT_DTYPE_F32 || g_dtype == GBDT_DTYPE_F64, "%s: bad dtype", fn);
   GBDT_CHECK_ARG(max_slots >= 1 && max_slots <= kMaxSlots && max_build >= 1 && max_build <= max_slots,
                  "%s: slot bounds out of range", fn);
-  if (!ws || ws_bytes < seg_hist_scratch_bytes(max_slots) || !aligned(ws, kWsAlign)) {
-    set_error("%s: workspace needs %zu bytes", fn, seg_hist_scratch_bytes(max_slots));
+  const size_t need = gbdt_histograms_segmented_workspace_size(max_slots);
+  if (!ws || ws_bytes < need || !aligned(ws, kWsAlign)) {
+    set_error("%s: workspace needs %zu bytes", fn, need);
     return ws ? GBDT_ERR_WORKSPACE : GBDT_ERR_INVALID_ARG;
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // the error word (gbdt_workspace_status; these kernels raise nothing, so it stays 0) and the scratch
+  GBDT_CUDA(cudaMemsetAsync(ws, 0, sizeof(int32_t), s));
+  void* scratch = static_cast<char*>(ws) + kWsAlign;
   const SegHistPlan plan = plan_seg_histograms(N, F, max_slots, max_build, with_h, filters != nullptr);
   int rc = launch_seg_histograms(plan, bins, ldb, N, F, g, g_dtype, fixed_exp, level, max_slots, build_flag, segments,
-                                 filters, ws, hist_cnt, hist_q, hist_h, s, layout == GBDT_LAYOUT_ROW_BLOCKS);
+                                 filters, scratch, hist_cnt, hist_q, hist_h, s, layout == GBDT_LAYOUT_ROW_BLOCKS);
   if (rc != GBDT_OK) return rc;
   GBDT_LAUNCH_CHECK();
   return GBDT_OK;

@@ -477,8 +477,12 @@ extern "C" int gbdt_find_splits_h(const uint32_t* hist_cnt, const int64_t* hist_
     return ws ? GBDT_ERR_WORKSPACE : GBDT_ERR_INVALID_ARG;
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  GBDT_CUDA(cudaMemsetAsync(split_counters(ws, F, max_slots), 0, sizeof(int32_t) * max_slots, s));
-  launch_find_splits(hist_cnt, hist_q, hist_h, fixed_exp, F, n_bins, level, max_slots, *p, out, ws, nullptr, s);
+  // the workspace: the call's error word (gbdt_workspace_status), then the search's scratch
+  int32_t* err = static_cast<int32_t*>(ws);
+  void* scratch = static_cast<char*>(ws) + kWsAlign;
+  GBDT_CUDA(cudaMemsetAsync(err, 0, sizeof(int32_t), s));
+  GBDT_CUDA(cudaMemsetAsync(split_counters(scratch, F, max_slots), 0, sizeof(int32_t) * max_slots, s));
+  launch_find_splits(hist_cnt, hist_q, hist_h, fixed_exp, F, n_bins, level, max_slots, *p, out, scratch, err, s);
   GBDT_LAUNCH_CHECK();
   return GBDT_OK;
 }

@@ -23,6 +23,16 @@
  *     it synchronises.
  *   - Arguments are validated before any launch; an invalid argument returns
  *     GBDT_ERR_INVALID_ARG and queues nothing.
+ *   - Consistency checks that only the device can make (a histogram that does
+ *     not add up to its node's totals, a partition whose counts differ from
+ *     its split records, a level larger than its bound; "Module Design:
+ *     Training Core" s.5, the Failed state) are recorded in a device error
+ *     word.  Every asynchronous call that takes a workspace keeps that word in
+ *     the workspace's first 4 bytes: the call clears it when it is queued and
+ *     its kernels OR error bits into it, so after the call the word describes
+ *     that call.  gbdt_workspace_status reads it back; gbdt_train and
+ *     gbdt_quantize read their own and return the error themselves.  A caller
+ *     that never asks does not pay for the check (no synchronisation).
  *   - Binned features are column-major uint8: feature j occupies
  *     bins[j*ldb .. j*ldb + N); ldb >= N, ldb % 16 == 0 and the base pointer
  *     16-byte aligned, so every column is read with 16-byte vector loads.
@@ -186,6 +196,15 @@ const char* gbdt_version(void);
  * (monotonic; a caller takes differences around a region of interest). */
 int64_t gbdt_kernel_launch_count(void);
 
+/* gbdt_workspace_status: the device error word of the last call queued with
+ * workspace ws (see the conventions above).  Copies the word to the host on
+ * `stream` and synchronises the stream; *bits (host, may be NULL) receives it.
+ * Returns GBDT_OK when it is 0, else GBDT_ERR_INTERNAL with a message naming
+ * each check that failed (GBDT_ERR_INVALID_ARG when the only failure is a bin
+ * at or above its feature's n_bins).  ws: the 256-byte aligned device
+ * workspace that was passed to the call. */
+int gbdt_workspace_status(const void* ws, int32_t* bits, void* stream);
+
 /* Parameter rules of "Module Design: Training Core" s.3 (see gbdt_params);
  * GBDT_OK or GBDT_ERR_INVALID_ARG.  Host only, queues nothing. */
 int gbdt_validate_params(const gbdt_params* p);
@@ -251,7 +270,8 @@ int gbdt_gradient_scale(const void* g, int32_t g_dtype, int64_t N, int32_t* fixe
  *     of flagged slots
  *   hist_cnt/hist_q [max_slots][F][256]: the flagged slots are overwritten;
  *     other slots are not touched.
- * 1 <= max_slots <= 4096.
+ * 1 <= max_slots <= 4096.  Device check (error word, gbdt_workspace_status):
+ * level->n_slots > max_slots (the extra slots are ignored).
  * ------------------------------------------------------------------------- */
 size_t gbdt_histograms_workspace_size(int64_t N, int32_t F, int32_t max_slots);
 int gbdt_build_histograms(const uint8_t* bins, int64_t ldb, int64_t N, int32_t F, const void* g, int32_t g_dtype,
@@ -259,20 +279,26 @@ int gbdt_build_histograms(const uint8_t* bins, int64_t ldb, int64_t N, int32_t F
                           int32_t max_slots, const uint8_t* build_flag, int32_t max_build, uint32_t* hist_cnt,
                           int64_t* hist_q, void* ws, size_t ws_bytes, void* stream);
 
-/* gbdt_subtract_histograms: sibling subtraction.  Slots come in sibling pairs
- * (2p, 2p+1); for p < level->n_slots/2 the slot of the pair with
- * build_flag = 0 receives parent - built, where the parent is slot
- * pair_parent[p] of prev_cnt/prev_q (the previous level's histograms).  Exact
- * (integer).  pair_parent [max_slots/2] int32 (device). */
+/* gbdt_subtract_histograms: sibling subtraction ("Module Design: Training
+ * Core" s.6 step 2: the larger child's histogram is the parent's minus the
+ * smaller one's).  Slots come in sibling pairs (2p, 2p+1); for
+ * p < level->n_slots/2 the slot of the pair with build_flag = 0 receives
+ * parent - built, where the parent is slot pair_parent[p] of prev_cnt/prev_q
+ * (the previous level's histograms).  Exact (integer).  pair_parent
+ * [max_slots/2] int32 (device).  ws (optional, may be NULL): a workspace of
+ * gbdt_subtract_histograms_workspace_size() bytes whose error word records a
+ * built count above its parent's (gbdt_workspace_status); with NULL that
+ * check is not recorded. */
+size_t gbdt_subtract_histograms_workspace_size(void);
 int gbdt_subtract_histograms(const uint32_t* prev_cnt, const int64_t* prev_q, const int32_t* pair_parent,
                              const uint8_t* build_flag, const gbdt_level* level, int32_t max_slots, int32_t F,
-                             uint32_t* hist_cnt, int64_t* hist_q, void* stream);
+                             uint32_t* hist_cnt, int64_t* hist_q, void* ws, size_t ws_bytes, void* stream);
 /* The same with H histograms (logistic): prev_h and hist_h, both non-NULL,
  * are subtracted like prev_q and hist_q. */
 int gbdt_subtract_histograms_h(const uint32_t* prev_cnt, const int64_t* prev_q, const int64_t* prev_h,
                                const int32_t* pair_parent, const uint8_t* build_flag, const gbdt_level* level,
                                int32_t max_slots, int32_t F, uint32_t* hist_cnt, int64_t* hist_q, int64_t* hist_h,
-                               void* stream);
+                               void* ws, size_t ws_bytes, void* stream);
 
 /* gbdt_build_histograms_segmented: the same per-bin count and fixed-point G
  * of every flagged slot of a level ("Module Design: Training Core" s.6 step 2,
@@ -346,6 +372,8 @@ int gbdt_build_histograms_segmented_h(const uint8_t* bins, int64_t ldb, int32_t 
  *   out [max_slots] gbdt_split (device); p: host pointer.
  * Work is spread over (slot, feature) pairs, then reduced per slot; since the
  * comparison is a total order the result does not depend on that split.
+ * Device check (error word, gbdt_workspace_status): a feature whose
+ * histogram does not add up to the node totals of feature 0.
  * ------------------------------------------------------------------------- */
 size_t gbdt_find_splits_workspace_size(int32_t F, int32_t max_slots);
 int gbdt_find_splits(const uint32_t* hist_cnt, const int64_t* hist_q, const int32_t* fixed_exp, int32_t F,
@@ -371,7 +399,10 @@ int gbdt_find_splits_h(const uint32_t* hist_cnt, const int64_t* hist_q, const in
  *   - seg_out[2k], seg_out[2k+1] are the children's segments.
  * Segments of slots without a split are copied unchanged to idx_out.
  * next_level (device) receives {node_begin + n_slots, 2*splits}.  Positions
- * outside the level's segments are not written.
+ * outside the level's segments are not written.  Device check (error word,
+ * gbdt_workspace_status): a split slot whose rows going left differ from its
+ * record's cnt_left (the rows are still placed by the counts the kernels
+ * compute, so every write stays inside the slot's segment).
  * ------------------------------------------------------------------------- */
 size_t gbdt_partition_workspace_size(int64_t N, int32_t max_slots);
 int gbdt_partition(const uint8_t* bins, int64_t ldb, int64_t N, int32_t F, const gbdt_split* splits,
@@ -390,7 +421,7 @@ int gbdt_partition(const uint8_t* bins, int64_t ldb, int64_t N, int32_t F, const
  * next_level (optional) receives {node_begin + n_slots, 2*splits}.  Slots
  * without a split are not copied; if leaf_of_row [original rows] (uint16) is
  * given, leaf_of_row[orig_in[p]] = node_begin + s for their positions.
- * Inputs and outputs must not alias. */
+ * Inputs and outputs must not alias.  Device check as gbdt_partition. */
 size_t gbdt_partition_rows_workspace_size(int64_t N, int32_t max_slots);
 int gbdt_partition_rows(const uint8_t* bins_in, uint8_t* bins_out, int64_t ldb, int64_t N, int32_t F,
                         const void* g_in, void* g_out, int32_t g_dtype, const uint32_t* orig_in, uint32_t* orig_out,
@@ -408,16 +439,25 @@ int gbdt_partition_rows(const uint8_t* bins_in, uint8_t* bins_out, int64_t ldb, 
  * which every GPU that loads the library holds until the process exits.
  * Limits of that scratch: N <= 16,777,216 rows and max_slots <= 1024; larger
  * sizes return GBDT_ERR_INVALID_ARG with a message naming the limit.
- * The first call on each device looks the array's device address up (with
- * that device current); make that first call before any stream capture.
+ * The first call on each device (and again in a new context of that device,
+ * e.g. after cudaDeviceReset) looks the array's device address up, with that
+ * device current; make that first call before any stream capture.
  * All calls on a device share the one array, and it keeps the previous
- * call's contents: each call clears what must start at zero, but calls that
- * overlap on the GPU (different streams, or host threads) race on it and must
- * be serialised by the caller.  Arguments and results are as gbdt_partition. */
+ * call's contents: each call clears what must start at zero (its error
+ * word), but calls that overlap on the GPU (different streams, or host
+ * threads) race on it and must be serialised by the caller.  Arguments and
+ * results are as gbdt_partition. */
 int gbdt_partition_noalloc(const uint8_t* bins, int64_t ldb, int64_t N, int32_t F, const gbdt_split* splits,
                            const gbdt_level* level, int32_t max_slots, const gbdt_segment* seg_in,
                            const uint32_t* idx_in, uint16_t* node_of_row, uint32_t* idx_out,
                            gbdt_segment* seg_out, gbdt_level* next_level, void* stream);
+/* gbdt_partition_noalloc_status: the device error word of the last
+ * gbdt_partition_noalloc call on the current device (its checks are those of
+ * gbdt_partition), which lives in the built-in scratch array.  Copies it to
+ * the host on `stream` and synchronises the stream; *bits (host, may be NULL)
+ * receives it.  Returns GBDT_OK or GBDT_ERR_INTERNAL as gbdt_workspace_status.
+ * Allocates nothing. */
+int gbdt_partition_noalloc_status(int32_t* bits, void* stream);
 
 /* ---------------------------------------------------------------------------
  * gbdt_update_predictions: "Module Design: Training Core" s.6 step 7 and

@@ -11,7 +11,9 @@ Tolerances (also in the design notes):
     library recovers h; a leaf value's bound is (G bound + |w| * H bound) / (H + lambda);
   * predictions: 1e-6 * max(|p_orc|, std(label)).
 """
+import json
 import math
+import os
 
 import numpy as np
 import pytest
@@ -131,3 +133,14 @@ def compare_training(gpu, bins, n_bins, y, params, report=None):
     if report is not None:
         report.update(adopted=adopted, near_ties=near, trees=T)
     return ref
+
+
+def record_parity(config: str, **fields):
+    """Print a parity record (near-tie counts and the like) and, when GBDT_PARITY_RECORD names a file,
+    append it there as one JSON line."""
+    rec = dict(config=config, **fields)
+    print("parity record:", json.dumps(rec))
+    path = os.environ.get("GBDT_PARITY_RECORD")
+    if path:
+        with open(path, "a") as f:
+            f.write(json.dumps(rec) + "\n")

@@ -89,9 +89,28 @@ def test_entry_points_reject_bad_arguments_before_any_launch(lib):
     assert lib.gbdt_build_histograms_segmented_h(None, 0, 0, 0, 0, None, 0, None, None, 0, None, 0, None, None, None,
                                                  None, None, None, 0, None) == -1
     assert lib.gbdt_find_splits_h(None, None, None, None, 0, None, None, 0, None, None, None, 0, None) == -1
-    assert lib.gbdt_subtract_histograms_h(None, None, None, None, None, None, 0, 0, None, None, None, None) == -1
+    assert lib.gbdt_subtract_histograms_h(None, None, None, None, None, None, 0, 0, None, None, None, None, 0,
+                                          None) == -1
     assert lib.gbdt_compute_gradients_objective(None, None, 0, 1, None, None, None, 0, None) == -1
     assert b"null pointer" in lib.gbdt_last_error()
+    # the status query needs a workspace pointer (checked before any copy)
+    assert lib.gbdt_workspace_status(None, None, None) == -1
+    assert b"workspace" in lib.gbdt_last_error()
+
+
+def test_noalloc_scratch_covers_its_limits(lib):
+    """gbdt_partition_noalloc's built-in scratch (128 KiB) must hold the partition's carve at its documented
+    limits (16,777,216 rows, 1,024 slots); the carve is the workspace gbdt_partition asks for."""
+    need = lib.gbdt_partition_workspace_size(1 << 24, 1024)
+    assert 0 < need <= 128 * 1024, need
+
+
+def test_error_word_leads_every_asynchronous_workspace(lib):
+    """Each asynchronous call's workspace starts with its 4-byte error word: the sizes leave room for it."""
+    assert lib.gbdt_subtract_histograms_workspace_size() >= 4
+    assert lib.gbdt_gradients_workspace_size(10) >= 256 + 16
+    assert lib.gbdt_histograms_segmented_workspace_size(8) >= 256 + 8 * 12
+    assert lib.gbdt_find_splits_workspace_size(4, 8) >= 256
 
 
 def test_row_block_slot_plan_on_host(lib):
