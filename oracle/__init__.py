@@ -51,7 +51,8 @@ NODE_DTYPE = np.dtype([("feature", np.int32), ("threshold_bin", np.int32), ("lef
 INFO_DTYPE = np.dtype([("n_rows", np.int64), ("G", np.float64), ("H", np.float64), ("A", np.float64),
                        ("best_gain", np.float64), ("second_gain", np.float64), ("n_near", np.int32),
                        ("near_feature", np.int32, (NEAR_MAX,)), ("near_bin", np.int32, (NEAR_MAX,)),
-                       ("adopted", np.int32), ("guide_mismatch", np.int32)], align=True)
+                       ("adopted", np.int32), ("guide_mismatch", np.int32), ("guide_gap", np.float64),
+                       ("guide_bound", np.float64)], align=True)
 
 
 def build(force: bool = False) -> str:
@@ -82,7 +83,7 @@ def lib():
         L.orc_histograms.argtypes = [P, i64, i32, P, P, P, i32, P, P, P, P, P, P, P]
         L.orc_best_split.argtypes = [P, P, P, i32, P, i64, dbl, dbl, ctypes.POINTER(Params),
                                      ctypes.POINTER(Split)]
-        L.orc_train.argtypes = [P, P, i64, i32, P, ctypes.POINTER(Params), P, P, P, P, P, P, P]
+        L.orc_train.argtypes = [P, P, i64, i32, P, ctypes.POINTER(Params), P, P, P, P, P, P, P, P, P]
         L.orc_partition.argtypes = [P, i64, i32, P, P, P, P, P, P, P]
         L.orc_update_predictions.argtypes = [P, P, P, i64, dbl]
         L.orc_predict.argtypes = [P, i64, i32, P, i32, P, i32, i32, dbl, dbl, P]
@@ -186,8 +187,12 @@ def max_nodes(max_depth: int) -> int:
 
 
 def train(bins: np.ndarray, n_bins: np.ndarray, label: np.ndarray, guide: np.ndarray | None = None,
-          want_info: bool = True, want_leaf_of_row: bool = False, **params):
-    """Train; returns dict(pred, init_pred, nodes (T, M) NODE_DTYPE, nodes_per_tree, info, leaf_of_row)."""
+          want_info: bool = True, want_leaf_of_row: bool = False, tie_quanta: np.ndarray | None = None,
+          pred_in: np.ndarray | None = None, **params):
+    """Train; returns dict(pred, init_pred, nodes (T, M) NODE_DTYPE, nodes_per_tree, info, leaf_of_row).
+
+    Parity-harness options: guide (T, M, 2) the other program's (feature, bin) per node, tie_quanta (T, 2)
+    its per-row rounding bounds of g and h (see orc_train), pred_in (N,) predictions to start from."""
     bins = np.ascontiguousarray(bins, dtype=np.uint8)
     F, N = bins.shape
     n_bins = np.ascontiguousarray(n_bins, dtype=np.int32)
@@ -203,8 +208,14 @@ def train(bins: np.ndarray, n_bins: np.ndarray, label: np.ndarray, guide: np.nda
     if guide is not None:
         guide = np.ascontiguousarray(guide, dtype=np.int32)
         assert guide.shape == (T, M, 2)
-    _check(lib().orc_train(_p(bins), _p(n_bins), N, F, _p(label), ctypes.byref(p), _p(guide), _p(pred),
-                           _p(init), _p(nodes), _p(npt), _p(info), _p(lor)), "train")
+    if tie_quanta is not None:
+        tie_quanta = np.ascontiguousarray(tie_quanta, dtype=np.float64)
+        assert tie_quanta.shape == (T, 2)
+    if pred_in is not None:
+        pred_in = np.ascontiguousarray(pred_in, dtype=np.float64)
+        assert pred_in.shape == (N,)
+    _check(lib().orc_train(_p(bins), _p(n_bins), N, F, _p(label), ctypes.byref(p), _p(guide), _p(tie_quanta),
+                           _p(pred_in), _p(pred), _p(init), _p(nodes), _p(npt), _p(info), _p(lor)), "train")
     return dict(pred=pred, init_pred=float(init[0]), nodes=nodes, nodes_per_tree=npt, info=info,
                 leaf_of_row=lor)
 

@@ -84,8 +84,11 @@ typedef struct {
   int32_t n_near;                /* candidates within ORC_NEAR_REL of the best */
   int32_t near_feature[ORC_NEAR_MAX];
   int32_t near_bin[ORC_NEAR_MAX];
-  int32_t adopted;        /* 1: the guide's near-tied choice replaced ours */
-  int32_t guide_mismatch; /* 1: the guide disagreed outside the near-tie set */
+  int32_t adopted;        /* the guide's choice replaced ours: 1 within ORC_NEAR_REL, 2 within the
+                             rounding bound of the tie quanta only (see orc_train) */
+  int32_t guide_mismatch; /* 1: the guide disagreed outside both */
+  double guide_gap;       /* where the guide differed: our best gain minus the guide's candidate's */
+  double guide_bound;     /* the rounding bound that gap was held against (0 without tie quanta) */
 } orc_node_info;
 
 typedef struct {
@@ -114,6 +117,53 @@ double orc_gain(double GL, double HL, double GR, double HR, double GP, double HP
   double sR = orc_score(GR, HR, lambda);
   double sP = orc_score(GP, HP, lambda);
   return 0.5 * ((sL + sR) - sP) - gamma;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Parity harness: how far a candidate's gain can move when another program   */
+/* sums the same per-row g (and h) with a bounded rounding per row.  Not part  */
+/* of the method; orc_train's lockstep guide uses it to tell rounding ties     */
+/* from real disagreements.                                                    */
+/* ------------------------------------------------------------------------ */
+/* gamma_n = n u / (1 - n u), u = 2^-53: the classical bound on the error of a sum of n terms
+ * accumulated one by one in FP64, relative to the sum of their magnitudes. */
+static double sum_error_factor(int64_t n) {
+  const double nu = (double)n * 0x1p-53;
+  return nu < 0.5 ? nu / (1.0 - nu) : INFINITY;
+}
+
+/* Bound on |s(G', H') - s(G, H)| for s = G^2 / (H + lambda), |G' - G| <= dG, |H' - H| <= dH:
+ * |G'^2 - G^2| <= 2|G| dG + dG^2 over a denominator of at least H + lambda - dH, plus
+ * G^2 |1/(H' + lambda) - 1/(H + lambda)| <= G^2 dH / ((H + lambda)(H + lambda - dH)). */
+static double score_spread(double G, double H, double dG, double dH, double lambda) {
+  const double hl = H + lambda, lo = hl - dH;
+  if (!(lo > 0.0)) return INFINITY;
+  return (2.0 * fabs(G) * dG + dG * dG) / lo + G * G * dH / (hl * lo);
+}
+
+/* Bound on how far a candidate's gain, 0.5 ((s_L + s_R) - s_P) - gamma, computed by this oracle
+ * and by another program from the same rows can differ.  The other program's per-row rounding of g
+ * is at most qg (of h, qh; 0 when H is a count); this oracle's row-order sums of n terms are off by
+ * at most gamma_(n + bins) times the sum of magnitudes (A for G, H_P for h >= 0; a side's
+ * magnitudes are at most the node's); each side's conversions add one rounding of its sums, and the
+ * gain's own evaluation a few roundings of its scores on each program. */
+static double gain_spread(double GL, double HL, int64_t nL, double GP, double HP, int64_t nP, double A, double qg,
+                          double qh, int h_counts, double lambda) {
+  const double u = 0x1p-53;
+  const double GR = GP - GL, HR = HP - HL;
+  const double dGL = (double)nL * qg + sum_error_factor(nL + ORC_NBINS) * A + u * fabs(GL);
+  const double dGP = (double)nP * qg + sum_error_factor(nP) * A + u * fabs(GP);
+  const double dGR = dGP + dGL + u * fabs(GR);
+  double dHL = 0.0, dHP = 0.0, dHR = 0.0;
+  if (!h_counts) {
+    dHL = (double)nL * qh + sum_error_factor(nL + ORC_NBINS) * HP + u * HL;
+    dHP = (double)nP * qh + sum_error_factor(nP) * HP + u * HP;
+    dHR = dHP + dHL + u * fabs(HR);
+  }
+  const double sL = orc_score(GL, HL, lambda), sR = orc_score(GR, HR, lambda), sP = orc_score(GP, HP, lambda);
+  return 0.5 * (score_spread(GL, HL, dGL, dHL, lambda) + score_spread(GR, HR, dGR, dHR, lambda) +
+                score_spread(GP, HP, dGP, dHP, lambda)) +
+         8.0 * u * (fabs(sL) + fabs(sR) + fabs(sP));
 }
 
 /* [MPS-TC] s.3: parameter rules. */
@@ -400,14 +450,23 @@ int orc_best_split(const uint32_t* cnt, const double* G, const double* H, int32_
  *
  * guide (optional, [n_trees][max_nodes][2] = feature, bin; feature -1 = leaf)
  * is the lockstep rule of the parity harness: where this oracle's choice at
- * a node differs from the guide's and the guide's (feature, bin) is among the
- * candidates this oracle itself rates within ORC_NEAR_REL of its best gain,
- * the guide's candidate is taken (info.adopted = 1).  Any other disagreement
- * is recorded (info.guide_mismatch = 1) and this oracle keeps its own choice.
+ * a node differs from the guide's and the guide's (feature, bin) is a valid
+ * candidate whose gain this oracle rates within ORC_NEAR_REL of its best, the
+ * guide's candidate is taken (info.adopted = 1).  With tie_quanta
+ * ([n_trees][2]: the other program's per-row rounding bound of g and of h, h
+ * 0 when H is a row count) the guide's candidate is also taken when the gap
+ * is within gain_spread of both candidates, i.e. rounding of the same rows'
+ * sums could reorder them (info.adopted = 2); likewise a node whose best gain
+ * is within its spread of 0 may split or not as the guide says.  Any other
+ * disagreement is recorded (info.guide_mismatch = 1) and this oracle keeps
+ * its own choice.
+ * pred_in (optional, [N]): start from these predictions instead of the
+ * initial value (*init_pred still receives the initial value).
  */
 int orc_train(const uint8_t* bins, const int32_t* n_bins, int64_t N, int32_t F, const float* label,
-              const orc_params* p, const int32_t* guide, double* pred, double* init_pred, orc_node* nodes,
-              int32_t* nodes_per_tree, orc_node_info* info, int32_t* leaf_of_row) {
+              const orc_params* p, const int32_t* guide, const double* tie_quanta, const double* pred_in,
+              double* pred, double* init_pred, orc_node* nodes, int32_t* nodes_per_tree, orc_node_info* info,
+              int32_t* leaf_of_row) {
   if (!bins || !n_bins || !label || !pred || !init_pred || !nodes || !nodes_per_tree || N < 1 || F < 1)
     return ORC_EINVAL;
   int rc = orc_validate_params(p);
@@ -454,7 +513,7 @@ int orc_train(const uint8_t* bins, const int32_t* n_bins, int64_t N, int32_t F, 
   for (int64_t i = 0; i < N; ++i) sum += (double)label[i];
   const double init = logistic ? 0.0 : sum / (double)N;
   *init_pred = init;
-  for (int64_t i = 0; i < N; ++i) pred[i] = init;
+  for (int64_t i = 0; i < N; ++i) pred[i] = pred_in ? pred_in[i] : init;
 
   for (int32_t t = 0; t < p->n_trees; ++t) {
     orc_node* tn = nodes + (int64_t)t * max_nodes;
@@ -517,27 +576,71 @@ int orc_train(const uint8_t* bins, const int32_t* n_bins, int64_t N, int32_t F, 
             ti[v].near_bin[k] = sp.near_bin[k];
           }
         }
-        if (tg && do_split && tg[2 * v] >= 0 && (tg[2 * v] != f || tg[2 * v + 1] != b)) {
+        if (tg && (do_split || tg[2 * v] >= 0) && (!do_split || tg[2 * v] != f || tg[2 * v + 1] != b)) {
+          /* the guide differs from this oracle: rate its choice with this oracle's own sums.  Only two
+           * different split candidates are a mismatch here; a split where the guide has a leaf (or the
+           * reverse) is adopted when rounding allows it, else left to the check after the leaf budget */
+          const int own_split = do_split;
+          const double* tq = tie_quanta ? tie_quanta + 2 * (int64_t)t : NULL;
+          const int h_counts = !logistic;
+          const double spread_best =
+              sp.valid && tq ? gain_spread(sp.G_left, sp.H_left, sp.cnt_left, GP, HP, n, A, tq[0], tq[1], h_counts,
+                                           lambda)
+                             : 0.0;
           int32_t gf = tg[2 * v], gb = tg[2 * v + 1];
-          int near = 0;
-          int lim = sp.n_near < ORC_NEAR_MAX ? sp.n_near : ORC_NEAR_MAX;
-          for (int k = 0; k < lim; ++k)
-            if (sp.near_feature[k] == gf && sp.near_bin[k] == gb) near = 1;
-          if (near) {
-            /* recompute the adopted candidate's gain from its own prefix sums */
-            const double* gg = G + (int64_t)gf * ORC_NBINS;
-            const double* hh = H + (int64_t)gf * ORC_NBINS;
-            double GL = 0.0, HL = 0.0;
-            for (int32_t q = 0; q <= gb; ++q) {
-              GL += gg[q];
-              HL += hh[q];
+          int kind = 0;
+          double gap = 0.0, bound = 0.0, gain_g = 0.0;
+          if (gf >= 0) {
+            if (gf < F && gb >= 0 && gb <= n_bins[gf] - 2) {
+              const uint32_t* cc = cnt + (int64_t)gf * ORC_NBINS;
+              const double* gg = G + (int64_t)gf * ORC_NBINS;
+              const double* hh = H + (int64_t)gf * ORC_NBINS;
+              double GL = 0.0, HL = 0.0;
+              int64_t cL = 0;
+              for (int32_t q = 0; q <= gb; ++q) {
+                GL += gg[q];
+                HL += hh[q];
+                cL += cc[q];
+              }
+              const double GR = GP - GL, HR = HP - HL;
+              const int64_t cR = n - cL;
+              const int valid = cL >= p->min_samples_leaf && cR >= p->min_samples_leaf && HL >= p->min_child_weight &&
+                                HR >= p->min_child_weight && HL > 0.0 && HR > 0.0;
+              if (valid) {
+                gain_g = orc_gain(GL, HL, GR, HR, GP, HP, lambda, p->gamma);
+                const double spread_g = tq ? gain_spread(GL, HL, cL, GP, HP, n, A, tq[0], tq[1], h_counts, lambda)
+                                           : 0.0;
+                if (do_split) {  /* both split, on different candidates */
+                  gap = gain - gain_g;
+                  bound = spread_best + spread_g;
+                  if (gap <= ORC_NEAR_REL * fabs(gain)) kind = 1;
+                  else if (tq && gap <= bound) kind = 2;
+                } else {  /* the guide splits where this oracle's best gain is not above 0 */
+                  gap = -gain_g;
+                  bound = spread_g;
+                  if (tq && gain_g > -spread_g && (!sp.valid || sp.gain - gain_g <= spread_best + spread_g)) kind = 2;
+                }
+              }
             }
-            f = gf;
-            b = gb;
-            gain = orc_gain(GL, HL, GP - GL, HP - HL, GP, HP, lambda, p->gamma);
-            if (ti) ti[v].adopted = 1;
-          } else if (ti) {
-            ti[v].guide_mismatch = 1;
+            if (kind) {
+              f = gf;
+              b = gb;
+              gain = gain_g;
+              do_split = 1;
+            }
+          } else if (do_split) {  /* the guide makes a leaf where this oracle's best gain is above 0 */
+            gap = gain;
+            bound = spread_best;
+            if (tq && gain <= spread_best) {
+              kind = 2;
+              do_split = 0;
+            }
+          }
+          if (ti) {
+            ti[v].guide_gap = gap;
+            ti[v].guide_bound = bound;
+            if (kind) ti[v].adopted = kind;
+            else if (gf >= 0 && own_split) ti[v].guide_mismatch = 1;
           }
         }
         lvl_do[v - level_begin] = do_split;
