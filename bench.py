@@ -220,129 +220,101 @@ def run_reference(args, rank, ws, dist):
 
 # ------------------------------------------------------------------------------------ our arm
 def microbench(g, torch, args, peak):
-    """One tree level at 50M rows x 64 pre-binned features, 256 nodes (128 sibling pairs).
-
-    Rows are stored grouped by parent (the order the trainer holds them in after the previous
-    level's partition); each row's child is uniform.  Timed, each with CUDA events: the partition
-    of every parent's rows into its two children (all columns move), the segmented histograms of
-    the smaller children, sibling subtraction, and split search.  The node-id scan over rows in
-    random node order (the first design) is timed too, for comparison.
+    """One tree level at 50M rows x 64 pre-binned features, 256 nodes (128 sibling pairs), the stated input
+    and calls: each row's node is uniform over the 256 nodes and the rows are in no node order (they carry
+    node ids, as a per-level node-id pass leaves them).  Timed, each with CUDA events: gbdt_build_histograms
+    of the smaller child of every pair (the call groups those rows by node inside itself, then builds),
+    sibling subtraction, and split search.  The parents' histograms are built untimed by the same call.
+    Also timed: the same call with a workspace that only holds its error word (the node-id scan, which
+    reads every row once per group of nodes) for comparison.
     """
     cfg = synth.CONFIGS["micro"]
     N, F, n_nodes = args.micro_rows, cfg["f"], cfg["n_nodes"]
     P = n_nodes // 2
-    bins_h, node_h, g_h = synth.make_micro(n=N, f=F, n_nodes=n_nodes, grouped=True)
+    bins_h, node_h, g_h = synth.make_micro(n=N, f=F, n_nodes=n_nodes, grouped=False)
     ld = g.padded_ld(N)
     bins = torch.zeros((F, ld), dtype=torch.uint8, device="cuda")
     bins[:, :N] = torch.from_numpy(bins_h).cuda()
     del bins_h
     gd = torch.from_numpy(g_h).cuda()
-    orig = torch.arange(N, dtype=torch.int32, device="cuda")
-    go_right = torch.from_numpy((node_h & 1).astype(np.uint8)).cuda()
     counts = np.bincount(node_h, minlength=n_nodes).astype(np.int64)
-    pc = counts[0::2] + counts[1::2]
-    pstart = np.concatenate([[0], np.cumsum(pc)[:-1]])
-    pseg = np.zeros(P, g.SEGMENT_DTYPE)
-    pseg["start"], pseg["count"] = pstart, pc
-    sp = np.zeros(P, g.SPLIT_DTYPE)
-    sp["feature"], sp["bin"], sp["cnt_left"], sp["cnt_total"] = 0, 0, counts[0::2], pc
     left_small = counts[0::2] <= counts[1::2]
     flags = np.empty(n_nodes, np.uint8)
     flags[0::2], flags[1::2] = left_small, ~left_small
     fd = torch.from_numpy(flags).cuda()
+    # node ids: parents 0..P-1 (the level above), children P .. P + n_nodes - 1
+    child_id = torch.from_numpy((P + node_h.astype(np.int32)).astype(np.uint16).view(np.int16)).cuda()
+    parent_id = torch.from_numpy((node_h >> 1).astype(np.uint16).view(np.int16)).cuda()
     dev = g._dev
-    plvl, lvl = dev(np.array([(0, P)], g.LEVEL_DTYPE), g.LEVEL_DTYPE), dev(np.array([(P, n_nodes)], g.LEVEL_DTYPE),
-                                                                           g.LEVEL_DTYPE)
-    pseg_d, sp_d = dev(pseg, g.SEGMENT_DTYPE), dev(sp, g.SPLIT_DTYPE)
+    plvl = dev(np.array([(0, P)], g.LEVEL_DTYPE), g.LEVEL_DTYPE)
+    lvl = dev(np.array([(P, n_nodes)], g.LEVEL_DTYPE), g.LEVEL_DTYPE)
     S = g.gradient_scale(gd)
     n_bins = torch.full((F,), 256, dtype=torch.int32, device="cuda")
-    # parents' histograms, untimed, from the parent-grouped rows
-    ph_c, ph_q = g.build_histograms_segmented(bins, N, gd, S, plvl, P, torch.ones(P, dtype=torch.uint8,
-                                              device="cuda"), P, pseg_d)
-    out = (torch.empty_like(bins), torch.empty_like(gd), torch.empty_like(orig))
-    pws = g._workspace(g.lib().gbdt_partition_rows_workspace_size(N, P))
-    hws = g._workspace(g.lib().gbdt_histograms_segmented_workspace_size(n_nodes))
+    hws = g._workspace(g.lib().gbdt_histograms_workspace_size(N, F, n_nodes))
+    ph_c, ph_q = g.build_histograms(bins, N, gd, S, parent_id, plvl, P, torch.ones(P, dtype=torch.uint8,
+                                    device="cuda"), P, ws=hws)
     hc = torch.zeros((n_nodes, F, 256), dtype=torch.int32, device="cuda")
     hq = torch.zeros((n_nodes, F, 256), dtype=torch.int64, device="cuda")
     pair_parent = torch.arange(P, dtype=torch.int32, device="cuda")
     split_out = torch.empty(n_nodes * g.SPLIT_DTYPE.itemsize, dtype=torch.uint8, device="cuda")
+    sws = g._workspace(g.lib().gbdt_subtract_histograms_workspace_size())
     stream = torch.cuda.current_stream()
-    times = {"partition": [], "build": [], "subtract": [], "find": []}
-    rb_times = []
-    rb = None
+    times = {"build": [], "subtract": [], "find": []}
     for it in range(args.warmup + args.steps):
-        ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
         ev[0].record(stream)
-        cb, cg, co, cseg, _ = g.partition_rows(bins, N, gd, orig, sp_d, plvl, P, pseg_d, go_right=go_right, out=out,
-                                               ws=pws)
+        g.build_histograms(bins, N, gd, S, child_id, lvl, n_nodes, fd, P, hc, hq, ws=hws)
         ev[1].record(stream)
-        g.build_histograms_segmented(cb, N, cg, S, lvl, n_nodes, fd, P, cseg, hc, hq, ws=hws)
+        g.subtract_histograms(ph_c, ph_q, pair_parent, fd, lvl, n_nodes, hc, hq, ws=sws)
         ev[2].record(stream)
-        g.subtract_histograms(ph_c, ph_q, pair_parent, fd, lvl, n_nodes, hc, hq)
-        ev[3].record(stream)
         g.find_splits(hc, hq, S, n_bins, lvl, n_nodes, out=split_out, reg_lambda=1.0, gamma=0.0,
                       min_samples_leaf=1, min_child_weight=0.0)
-        ev[4].record(stream)
-        torch.cuda.synchronize()
-        # the same build on the row-block layout the training levels use (converted once, untimed: the
-        # partition's output is the same every iteration)
-        if rb is None:
-            rb = g.to_row_blocks(cb, N)
-            torch.cuda.synchronize()
-        r0, r1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        r0.record(stream)
-        g.build_histograms_segmented(cb, N, cg, S, lvl, n_nodes, fd, P, cseg, hc, hq, ws=hws, row_blocks=rb)
-        r1.record(stream)
+        ev[3].record(stream)
         torch.cuda.synchronize()
         if it >= args.warmup:
             for k, name in enumerate(times):
                 times[name].append(ev[k].elapsed_time(ev[k + 1]))
-            rb_times.append(r0.elapsed_time(r1))
+    statuses = {"build": g.workspace_status(hws), "subtract": g.workspace_status(sws)}
     ms = {k: statistics.mean(v) for k, v in times.items()}
-    rb_ms = statistics.mean(rb_times)
     n_small = int(np.minimum(counts[0::2], counts[1::2]).sum())
-    build_bytes = n_small * (F + 4) + P * F * 256 * 12
-    part_bytes = N * (2 * (F + 4 + 4) + 1)
-    formula_bytes = N * (F + 4 + 1) + P * F * 256 * 12  # full-scan accounting: every active row read once
-    level_ms = ms["partition"] + rb_ms + ms["subtract"] + ms["find"]
+    hist_out = P * F * 256 * 12
+    formula_bytes = N * (F + 4 + 1) + hist_out  # the level formula: every row of the level read once
+    # what the call moves: node ids twice (count, scatter), every row's bins and g once, the smaller children's
+    # rows written grouped and read back by the histogram kernel, the built histograms written
+    moved_bytes = N * (2 + 2 + F + 4) + 2 * n_small * (F + 4) + hist_out
+    level_ms = ms["build"] + ms["subtract"] + ms["find"]
     res = {"workload": f"one level: {N:,} rows x {F} pre-binned uint8 features (Zipf 1.1), {n_nodes} nodes "
-                       f"(uniform), rows grouped by parent, fp32 g",
-           "partition_ms": ms["partition"], "build_ms": ms["build"], "subtract_ms": ms["subtract"],
-           "find_splits_ms": ms["find"], "level_ms": level_ms,
+                       f"(each row's node uniform, rows in no node order), fp32 g",
+           "call": "gbdt_build_histograms (rows grouped by node inside the call, then the node-contiguous "
+                   "histogram kernel) on the smaller child of each of the 128 pairs",
+           "build_ms": ms["build"], "subtract_ms": ms["subtract"], "find_splits_ms": ms["find"],
+           "level_ms": level_ms,
            "build_algorithmic_bytes": formula_bytes,
-           "build_gbs": formula_bytes / (rb_ms * 1e-3) / 1e9,
-           "build_frac": formula_bytes / (rb_ms * 1e-3) / 1e9 / peak,
+           "build_gbs": formula_bytes / (ms["build"] * 1e-3) / 1e9,
+           "build_frac": formula_bytes / (ms["build"] * 1e-3) / 1e9 / peak,
            "build_accounting": "level formula: N x (F + 4 B g + 1 B node id) + 128 built histograms x F x 256 x 12 B",
-           "build_read_bytes": build_bytes, "build_read_gbs": build_bytes / (rb_ms * 1e-3) / 1e9,
-           "build_read_frac": build_bytes / (rb_ms * 1e-3) / 1e9 / peak,
-           "build_layout": "row blocks (the layout the training levels read)", "build_row_blocks_ms": rb_ms,
-           "build_columns_ms": ms["build"], "build_columns_frac": formula_bytes / (ms["build"] * 1e-3) / 1e9 / peak,
-           "partition_gbs": part_bytes / (ms["partition"] * 1e-3) / 1e9,
-           "partition_frac": part_bytes / (ms["partition"] * 1e-3) / 1e9 / peak,
+           "build_moved_bytes": moved_bytes,
+           "build_moved_gbs": moved_bytes / (ms["build"] * 1e-3) / 1e9,
+           "build_moved_frac": moved_bytes / (ms["build"] * 1e-3) / 1e9 / peak,
+           "build_moved_accounting": "every byte the call reads or writes: node ids (count and scatter passes), "
+                                     "all bins and g, the grouped copy of the smaller children written and read, "
+                                     "the histograms",
            "level_effective_gbs": formula_bytes / (level_ms * 1e-3) / 1e9,
            "level_effective_frac": formula_bytes / (level_ms * 1e-3) / 1e9 / peak,
-           "peak_gbs": peak, "target_frac": 0.5,
-           "note": "build_gbs/build_frac: the histogram launch on the level formula's bytes; build_read_*: on the "
-                   "bytes it reads (the smaller children's rows); level_effective_*: the level formula's bytes over "
-                   "partition + build + subtract + find"}
-    # the first design: node-id scan over rows in random node order
-    perm = torch.randperm(N, device="cuda", generator=torch.Generator(device="cuda").manual_seed(0))
-    rb = bins[:, :N][:, perm].contiguous()
-    rbins = torch.zeros_like(bins)
-    rbins[:, :N] = rb
-    del rb
-    rnode = torch.from_numpy(node_h.view(np.int16)).cuda()[perm].contiguous()
-    rg = gd[perm].contiguous()
+           "device_status": statuses, "peak_gbs": peak, "target_frac": 0.5,
+           "note": "build_ms, build_gbs, build_frac and build_moved_* all time the same call; level_effective_* "
+                   "divides the level formula's bytes by build + subtract + find"}
+    # the node-id scan: the same call with a workspace holding only its error word
+    small = g._workspace(256)
     rt = []
     for it in range(2):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        g.build_histograms(rbins, N, rg, S, rnode, dev(np.array([(0, n_nodes)], g.LEVEL_DTYPE), g.LEVEL_DTYPE),
-                           n_nodes, fd, P, hc, hq)
+        g.build_histograms(bins, N, gd, S, child_id, lvl, n_nodes, fd, P, hc, hq, ws=small)
         e1.record(stream)
         torch.cuda.synchronize()
         rt.append(e0.elapsed_time(e1))
-    res["node_id_scan_random_order_build_ms"] = rt[-1]
+    res["node_id_scan_build_ms"] = rt[-1]
     return res
 
 
@@ -399,6 +371,8 @@ def covtype_leg(g, torch, args, peak, peak_kind, stream):
     """The covtype-shaped workload in the pages' configuration (581,012 x 54, 255 bins, depth 10,
     1023 leaves, 100 trees): whole quantize + training runs timed with CUDA events."""
     cfg = dict(synth.CONFIGS["covtype"], num_leaves=1023)
+    if args.covtype_trees is not None:
+        cfg["n_trees"] = args.covtype_trees
     X, y = synth.make("covtype")
     F, N = X.shape
     T = cfg["n_trees"]
@@ -452,6 +426,11 @@ def run_ours(args, rank, local_rank, ws, dist):
     g.lib()
     if args.only_micro:
         print(json.dumps({"histogram_microbench": microbench(g, torch, args, _peaks()[0])}), flush=True)
+        return 0
+    if args.only_covtype:
+        peak, peak_kind = _peaks()
+        print(json.dumps({"covtype": covtype_leg(g, torch, args, peak, peak_kind, torch.cuda.current_stream())}),
+              flush=True)
         return 0
     name = args.config
     cfg = dict(synth.CONFIGS[name])
@@ -622,6 +601,8 @@ def main():
     ap.add_argument("--no-logistic", action="store_true", help="skip the logistic-objective leg")
     ap.add_argument("--no-covtype", action="store_true", help="skip the covtype-shaped leg")
     ap.add_argument("--only-micro", action="store_true", help="run only the level microbench (profiling)")
+    ap.add_argument("--only-covtype", action="store_true", help="run only the covtype-shaped leg (profiling)")
+    ap.add_argument("--covtype-trees", type=int, default=None, help="trees of the covtype-shaped leg (profiling)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         print("note: fewer than 3 warm-up steps", file=sys.stderr)

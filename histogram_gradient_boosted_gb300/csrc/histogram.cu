@@ -364,9 +364,40 @@ void launch_hist_subtract(const uint32_t* prev_cnt, const int64_t* prev_q, const
 
 using namespace gbdt;
 
+namespace {
+// Workspace of gbdt_build_histograms: the error word, then what the grouping path needs (per-slot
+// counts, cursors and segments, the grouped row-block and gradient buffers, the segmented
+// histograms' scratch).  A workspace with the error word alone selects the node-id scan.
+struct HistWs {
+  int32_t* err;
+  uint32_t* count;
+  uint32_t* cursor;
+  gbdt_segment* seg;
+  uint8_t* rb;
+  void* g;
+  void* seg_scratch;
+};
+HistWs carve_hist(void* ws, size_t bytes, int64_t N, int32_t F, int32_t max_slots, size_t* need) {
+  Carve c(ws, bytes);
+  HistWs w{};
+  w.err = c.take<int32_t>(1);
+  const size_t cap = group_rows_capacity(N, max_slots);
+  w.count = c.take<uint32_t>(max_slots);
+  w.cursor = c.take<uint32_t>(max_slots);
+  w.seg = c.take<gbdt_segment>(max_slots);
+  w.rb = c.take<uint8_t>(static_cast<size_t>(rb_blocks(static_cast<int64_t>(cap))) * rb_pitch(F));
+  w.g = c.take<double>(cap);
+  w.seg_scratch = c.take<unsigned char>(seg_hist_scratch_bytes(max_slots));
+  *need = c.used;
+  return w;
+}
+}  // namespace
+
 extern "C" size_t gbdt_histograms_workspace_size(int64_t N, int32_t F, int32_t max_slots) {
-  (void)N, (void)F, (void)max_slots;
-  return kWsAlign;  // the error word
+  if (N < 1 || F < 1 || max_slots < 1) return kWsAlign;
+  size_t need = 0;
+  carve_hist(nullptr, 0, N, F, max_slots, &need);
+  return need;
 }
 
 extern "C" int gbdt_build_histograms(const uint8_t* bins, int64_t ldb, int64_t N, int32_t F, const void* g,
@@ -386,13 +417,28 @@ extern "C" int gbdt_build_histograms(const uint8_t* bins, int64_t ldb, int64_t N
   GBDT_CHECK_ARG(g_dtype == GBDT_DTYPE_F32 || g_dtype == GBDT_DTYPE_F64, "gbdt_build_histograms: bad g dtype");
   GBDT_CHECK_ARG(max_slots >= 1 && max_slots <= kMaxSlots, "gbdt_build_histograms: max_slots out of range");
   GBDT_CHECK_ARG(max_build >= 1 && max_build <= max_slots, "gbdt_build_histograms: max_build out of range");
-  if (!ws || ws_bytes < gbdt_histograms_workspace_size(N, F, max_slots) || !aligned(ws, kWsAlign)) {
+  if (!ws || ws_bytes < kWsAlign || !aligned(ws, kWsAlign)) {
     set_error("gbdt_build_histograms: workspace too small or misaligned");
     return ws ? GBDT_ERR_WORKSPACE : GBDT_ERR_INVALID_ARG;
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  int32_t* err = static_cast<int32_t*>(ws);  // the call's error word (gbdt_workspace_status)
+  size_t need = 0;
+  const HistWs w = carve_hist(ws, ws_bytes, N, F, max_slots, &need);
+  int32_t* err = w.err;  // the call's error word (gbdt_workspace_status)
   GBDT_CUDA(cudaMemsetAsync(err, 0, sizeof(int32_t), s));
+  if (max_build >= 2 && ws_bytes >= need) {
+    // rows grouped by slot first, then the node-contiguous histogram kernel on the grouped copy
+    const int g_size = g_dtype == GBDT_DTYPE_F64 ? 8 : 4;
+    launch_group_rows(bins, ldb, N, F, g, g_size, node_of_row, level, max_slots, build_flag, w.count, w.cursor,
+                      w.seg, w.rb, w.g, err, s);
+    const int64_t cap = static_cast<int64_t>(group_rows_capacity(N, max_slots));
+    const SegHistPlan plan = plan_seg_histograms(cap, F, max_slots, max_build, false, false);
+    int rc = launch_seg_histograms(plan, w.rb, rb_pitch(F), cap, F, w.g, g_dtype, fixed_exp, level, max_slots,
+                                   build_flag, w.seg, nullptr, w.seg_scratch, hist_cnt, hist_q, nullptr, s, true);
+    if (rc != GBDT_OK) return rc;
+    GBDT_LAUNCH_CHECK();
+    return GBDT_OK;
+  }
   const HistPlan plan = plan_histograms(N, F, max_slots, max_build);
   launch_hist_zero(level, max_slots, build_flag, F, hist_cnt, hist_q, nullptr, s);
   int rc = launch_hist_build(plan, bins, ldb, N, F, g, g_dtype, fixed_exp, node_of_row, level, max_slots,

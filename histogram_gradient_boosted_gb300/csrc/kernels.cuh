@@ -53,6 +53,18 @@ void launch_hist_subtract(const uint32_t* prev_cnt, const int64_t* prev_q, const
                           int32_t max_slots, int32_t F, uint32_t* hist_cnt, int64_t* hist_q, int64_t* hist_h,
                           int32_t* err, cudaStream_t s);
 
+// ---- grouping.cu -----------------------------------------------------------------------
+// Rows of a level's built slots copied, grouped by slot, into a row-block buffer rb (pitch
+// rb_pitch(F)) and a gradient buffer g_out (g_size bytes per row): slot s's rows are positions
+// seg[s].start .. + seg[s].count (start a multiple of 32; unbuilt slots get count 0), in no set order.
+// count, cursor: [max_slots] scratch.  Buffers hold group_rows_capacity(N, max_slots) rows.
+size_t group_rows_capacity(int64_t N, int32_t max_slots);
+size_t group_rows_smem_bytes(int32_t max_slots);
+void launch_group_rows(const uint8_t* bins, int64_t ldb, int64_t N, int32_t F, const void* g, int g_size,
+                       const uint16_t* node, const gbdt_level* level, int32_t max_slots, const uint8_t* build_flag,
+                       uint32_t* count, uint32_t* cursor, gbdt_segment* seg, uint8_t* rb, void* g_out,
+                       int32_t* err, cudaStream_t s);
+
 // ---- split.cu -------------------------------------------------------------------------
 size_t find_splits_scratch_bytes(int32_t F, int32_t max_slots);
 // The per-slot counters inside that scratch: zero them before the first launch_find_splits on it

@@ -155,3 +155,37 @@ def test_micro_level_all_nodes_after_partition():
     assert np.all(err <= tol), f"G off by {err.max()} (tol {tol.flat[err.argmax()]})"
     record_parity("micro 50,000,000 x 64, 256 nodes (row-grouped level)", built_nodes=int(len(built)),
                   segments_checked=n_nodes, max_G_err_over_tol=float((err / tol).max()))
+
+
+def test_micro_level_node_id_call_all_built_nodes():
+    """The 50M-row level as stated: rows in no node order, each carrying its node id; gbdt_build_histograms
+    (which groups the built slots' rows inside the call) against the oracle on every built node."""
+    N, F, n_nodes = synth.CONFIGS["micro"]["n"], synth.CONFIGS["micro"]["f"], synth.CONFIGS["micro"]["n_nodes"]
+    bins, node, gv = synth.make_micro(n=N, grouped=False)
+    P = n_nodes // 2
+    counts = np.bincount(node, minlength=n_nodes)
+    flags = np.zeros(n_nodes, np.uint8)
+    left_small = counts[0::2] <= counts[1::2]
+    flags[0::2], flags[1::2] = left_small, ~left_small
+    Bd = torch.zeros((F, g.padded_ld(N)), dtype=torch.uint8, device="cuda")
+    Bd[:, :N] = torch.from_numpy(bins).cuda()
+    gd = torch.from_numpy(gv).cuda()
+    S = g.gradient_scale(gd)
+    ids = torch.from_numpy((P + node.astype(np.int32)).astype(np.uint16).view(np.int16)).cuda()
+    ws = g._workspace(g.lib().gbdt_histograms_workspace_size(N, F, n_nodes))
+    hc, hq = g.build_histograms(Bd, N, gd, S, ids, level(P, n_nodes), n_nodes, torch.from_numpy(flags).cuda(), P,
+                                ws=ws)
+    assert g.workspace_status(ws) == 0
+    built = np.nonzero(flags)[0]
+    rank = np.full(n_nodes, -1, np.int32)
+    rank[built] = np.arange(len(built))
+    cnt, G, A = _oracle_histograms_parallel(bins, gv.astype(np.float64), rank[node], len(built))
+    hc_h, hq_h = hc.cpu().numpy().view(np.uint32), hq.cpu().numpy()
+    s_exp = int(S.item())
+    assert np.array_equal(hc_h[built], cnt)
+    Gg = np.ldexp(hq_h[built].astype(np.float64), -s_exp)
+    err = np.abs(Gg - G)
+    tol = g_tolerance(A, cnt, s_exp)
+    assert np.all(err <= tol), f"G off by {err.max()} (tol {tol.flat[err.argmax()]})"
+    record_parity("micro 50,000,000 x 64, 256 nodes (rows in no node order, gbdt_build_histograms)",
+                  built_nodes=int(len(built)), max_G_err_over_tol=float((err / tol).max()))

@@ -105,11 +105,14 @@ def _hist_case(N, F, n_slots, node_begin, flags, gdtype, seed, n_bins_max=256):
     return bins, node, gv, slot
 
 
+@pytest.mark.parametrize("path", ["grouped", "scan"])
 @pytest.mark.parametrize("N,F,n_slots,nb,gdtype", [
     (1, 1, 1, 0, np.float64), (15, 3, 1, 0, np.float64), (17, 2, 2, 3, np.float32),
     (50_003, 7, 6, 5, np.float64), (50_003, 7, 6, 5, np.float32), (120_001, 3, 40, 31, np.float64),
     (200_009, 5, 256, 255, np.float32), (33_333, 70, 2, 1, np.float64), (70_001, 130, 4, 3, np.float64)])
-def test_build_histograms_matches_oracle(N, F, n_slots, nb, gdtype):
+def test_build_histograms_matches_oracle(N, F, n_slots, nb, gdtype, path):
+    """Both paths of gbdt_build_histograms: rows grouped by slot in the workspace first (the full workspace,
+    two or more built slots), and the node-id scan (a workspace holding only the error word)."""
     bins, node, gv, slot = _hist_case(N, F, n_slots, nb, None, gdtype, seed=N + F + n_slots)
     rng = np.random.default_rng(N)
     flags = (rng.random(n_slots) < 0.6).astype(np.uint8)
@@ -119,8 +122,9 @@ def test_build_histograms_matches_oracle(N, F, n_slots, nb, gdtype):
     sentinel = 12345
     hc = torch.full((max_slots, F, 256), sentinel, dtype=torch.int32, device="cuda")
     hq = torch.full((max_slots, F, 256), sentinel, dtype=torch.int64, device="cuda")
+    ws = g._workspace(256) if path == "scan" else None
     g.build_histograms(dev_bins(bins), N, torch.from_numpy(gv).cuda(), S, u16(node), level(nb, n_slots), max_slots,
-                       torch.from_numpy(flags).cuda(), int(flags.sum()), hc, hq)
+                       torch.from_numpy(flags).cuda(), int(flags.sum()), hc, hq, ws=ws)
     ref = oracle.histograms(bins, gv.astype(np.float64), slot, n_slots)
     s_exp = int(S.item())
     assert s_exp == fixed_exponent(float(np.abs(gv.astype(np.float64)).max()), N)
