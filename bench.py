@@ -194,6 +194,117 @@ def cpu_baseline_sample(X, y, cfg, n_rows, n_trees, threads, repeats=1):
     return units, times
 
 
+def parity_sample(g, torch, X, y, cfg, n_rows, n_trees):
+    """The CUDA path against the oracle on a sample of the benchmark's matrix: every tree node by node, grown
+    from the same predictions (tests/gpu_util.compare_training), near-ties counted as the tests count them."""
+    import oracle
+    from tests.gpu_util import compare_training
+
+    Xs = np.ascontiguousarray(X[:, :n_rows])
+    ys = np.ascontiguousarray(y[:n_rows])
+    params = dict(cfg, n_trees=n_trees, n_threads=os.cpu_count() or 1)
+    bins, _, n_bins = g.quantize(torch.from_numpy(Xs).cuda(), cfg["max_bins"])
+    out = g.train(bins, n_bins, torch.from_numpy(ys).cuda(), **params)
+    ob, _, on = oracle.quantize(Xs, cfg["max_bins"], n_threads=params["n_threads"])
+    same_bins = bool(np.array_equal(bins[:, :n_rows].cpu().numpy(), ob))
+    rep = {}
+    compare_training(out, ob, on, ys, params, rep)
+    rep.pop("trees", None)
+    return dict(rows=n_rows, features=int(X.shape[0]), trees=n_trees, bins_identical=same_bins,
+                trees_identical=True, **rep,
+                rule="structure identical node by node; near_ties: nodes whose top two oracle gains differ by less "
+                     "than 1e-12 relative; adopted_*: nodes where the GPU's equally good choice was taken (within "
+                     "1e-12, or within the proven bound of its fixed-point rounding)")
+
+
+def baseline_table(g, torch, args):
+    """The results table of every configuration: the CUDA path (quantize + train, CUDA events; for the 50M-row
+    level, build + subtract + find) and the oracle on the machine's host cores, one thread and all threads, on
+    bounded samples of the same workload (rows x features x trees per second; the level: rows x features per
+    second).  Parity is what tests/ checks; this table times."""
+    import oracle
+
+    threads = os.cpu_count() or 1
+    stream = torch.cuda.current_stream()
+    peak = _peaks()[0]
+    out = {"cores": threads, "peak_gbs": peak, "configs": {}}
+    # (name, extra params, oracle sample for all threads (rows, trees), for one thread (rows, trees))
+    plan = [("tiny", {}, (None, None), (None, None)), ("mid", {}, (None, None), (None, 20)),
+            ("covtype", {"num_leaves": 1023}, (None, 10), (None, 2)), ("large", {}, (1_000_000, 8), (1_000_000, 1))]
+    for name, extra, s_all, s_one in plan:
+        cfg = dict(synth.CONFIGS[name], **extra)
+        X, y = synth.make(name)
+        F, N = X.shape
+        T = cfg["n_trees"]
+        Xd, yd = torch.from_numpy(X).cuda(), torch.from_numpy(y).cuda()
+        wsp = g._workspace(g.train_workspace_size(N, F, **cfg))
+        pred = torch.empty(N, dtype=torch.float64, device="cuda")
+
+        def run(diag=False):
+            bins, _, n_bins = g.quantize(Xd, cfg["max_bins"])
+            return g.train(bins, n_bins, yd, diagnostics=diag, ws=wsp, pred=pred, **cfg)
+
+        run()
+        torch.cuda.synchronize()
+        steps = 3 if name != "large" else 1
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        diags = []
+        e0.record(stream)
+        for _ in range(steps):
+            diags.append(run(diag=True)["diag"])
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / steps
+        hist_ms = sum(d["hist_ms"] for d in diags)
+        frac = sum(d["hist_level_bytes"] for d in diags) / (hist_ms * 1e-3) / 1e9 / peak if hist_ms else None
+        frac_read = sum(d["hist_bytes"] for d in diags) / (hist_ms * 1e-3) / 1e9 / peak if hist_ms else None
+        row = {"rows": N, "features": F, "trees": T, "gpu_ms": ms, "gpu_value": N * F * T / (ms * 1e-3),
+               "hist_frac": frac, "hist_frac_read": frac_read}
+        for key, (rows_s, trees_s), th in (("oracle_all", s_all, threads), ("oracle_1", s_one, 1)):
+            n_s = min(N, rows_s or N)
+            t_s = trees_s or T
+            units, times = cpu_baseline_sample(X, y, cfg, n_s, t_s, th)
+            row[key] = {"value": units / times[0], "seconds": times[0], "rows": n_s, "trees": t_s, "threads": th}
+        out["configs"][name] = row
+        del Xd, yd, wsp, pred
+    # the 50M-row level: the CUDA path's build + subtract + find; the oracle's histograms of every node of the
+    # level (it builds each node directly) and the split search of each, on a row sample
+    mb = microbench(g, torch, args, peak)
+    cfgm = synth.CONFIGS["micro"]
+    N, F, n_nodes = args.micro_rows, cfgm["f"], cfgm["n_nodes"]
+    out["configs"]["micro"] = {"rows": N, "features": F, "gpu_ms": mb["level_ms"],
+                               "gpu_value": N * F / (mb["level_ms"] * 1e-3), "hist_frac": mb["build_frac"],
+                               "hist_frac_moved": mb["build_moved_frac"], "unit": "rows*features/s (one level)"}
+    n_s = min(N, 5_000_000)
+    bins, node, gv = synth.make_micro(n=n_s, grouped=False)
+    g64 = gv.astype(np.float64)
+    params = dict(reg_lambda=1.0, gamma=0.0, min_samples_leaf=1, min_child_weight=0.0)
+    for key, th in (("oracle_all", threads), ("oracle_1", 1)):
+        groups = th if th > 1 else 1
+        bounds = np.linspace(0, n_nodes, groups + 1).astype(int)
+        t0 = time.perf_counter()
+        if groups > 1:
+            from concurrent.futures import ThreadPoolExecutor
+
+            def one(k):
+                lo, hi = bounds[k], bounds[k + 1]
+                loc = np.where((node >= lo) & (node < hi), node.astype(np.int32) - lo, -1).astype(np.int32)
+                h = oracle.histograms(bins, g64, loc, hi - lo)
+                return [oracle.best_split(h["cnt"][i], h["G"][i], h["H"][i], np.full(F, 256, np.int32), int(h["n"][i]),
+                                          float(h["Gt"][i]), float(h["Ht"][i]), **params) for i in range(hi - lo)]
+
+            with ThreadPoolExecutor(max_workers=groups) as ex:
+                list(ex.map(one, range(groups)))
+        else:
+            h = oracle.histograms(bins, g64, node.astype(np.int32), n_nodes)
+            for i in range(n_nodes):
+                oracle.best_split(h["cnt"][i], h["G"][i], h["H"][i], np.full(F, 256, np.int32), int(h["n"][i]),
+                                  float(h["Gt"][i]), float(h["Ht"][i]), **params)
+        sec = time.perf_counter() - t0
+        out["configs"]["micro"][key] = {"value": n_s * F / sec, "seconds": sec, "rows": n_s, "threads": th}
+    return out
+
+
 def run_reference(args, rank, ws, dist):
     if rank != 0:
         return 0
@@ -427,6 +538,9 @@ def run_ours(args, rank, local_rank, ws, dist):
     if args.only_micro:
         print(json.dumps({"histogram_microbench": microbench(g, torch, args, _peaks()[0])}), flush=True)
         return 0
+    if args.baseline_table:
+        print(json.dumps({"baseline_table": baseline_table(g, torch, args)}), flush=True)
+        return 0
     if args.only_covtype:
         peak, peak_kind = _peaks()
         print(json.dumps({"covtype": covtype_leg(g, torch, args, peak, peak_kind, torch.cuda.current_stream())}),
@@ -579,6 +693,13 @@ def run_ours(args, rank, local_rank, ws, dist):
         line["cpu_baseline"] = {"value": units_c / times_c[0], "unit": UNIT, "cores": threads, "kind": "oracle",
                                 "sample": f"first {n_rows:,} rows x {F} features x {args.cpu_trees} trees of the "
                                           f"same matrix (oracle quantize untimed)", "seconds": times_c[0]}
+        n1 = min(N, args.cpu_rows_single)
+        units_1, times_1 = cpu_baseline_sample(X, y, cfg, n1, args.cpu_trees_single, 1)
+        line["cpu_baseline"]["single_thread"] = {
+            "value": units_1 / times_1[0], "unit": UNIT, "cores": 1, "seconds": times_1[0],
+            "sample": f"first {n1:,} rows x {F} features x {args.cpu_trees_single} trees of the same matrix"}
+        if not args.no_parity_sample:
+            line["parity_sample"] = parity_sample(g, torch, X, y, cfg, min(N, args.parity_rows), args.parity_trees)
     if rank == 0:
         print(json.dumps(line), flush=True)
     return 0
@@ -596,12 +717,19 @@ def main():
     ap.add_argument("--micro-rows", type=int, default=synth.CONFIGS["micro"]["n"])
     ap.add_argument("--cpu-rows", type=int, default=1_000_000)
     ap.add_argument("--cpu-trees", type=int, default=32, help="trees of the oracle sample (about 10 s on 16 cores)")
+    ap.add_argument("--cpu-rows-single", type=int, default=1_000_000)
+    ap.add_argument("--cpu-trees-single", type=int, default=2, help="trees of the single-thread oracle sample")
+    ap.add_argument("--parity-rows", type=int, default=1_000_000)
+    ap.add_argument("--parity-trees", type=int, default=8, help="trees of the node-by-node parity sample")
+    ap.add_argument("--no-parity-sample", action="store_true")
     ap.add_argument("--no-micro", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-logistic", action="store_true", help="skip the logistic-objective leg")
     ap.add_argument("--no-covtype", action="store_true", help="skip the covtype-shaped leg")
     ap.add_argument("--only-micro", action="store_true", help="run only the level microbench (profiling)")
     ap.add_argument("--only-covtype", action="store_true", help="run only the covtype-shaped leg (profiling)")
+    ap.add_argument("--baseline-table", action="store_true",
+                    help="time every configuration on the GPU and the oracle (one thread, all threads)")
     ap.add_argument("--covtype-trees", type=int, default=None, help="trees of the covtype-shaped leg (profiling)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":

@@ -28,7 +28,7 @@ constexpr int kGrpThreads = 256;
 constexpr int kGrpTile = 4096;                             // rows per tile (one CTA)
 constexpr int kGrpRowsPerThread = kGrpTile / kGrpThreads;  // 16
 constexpr int kGrpStages = 4;                              // column copies in flight
-constexpr int kGrpWordsPerThread = 4;                      // output words a thread owns on the word path
+constexpr int kGrpMinBlocks = 3;                           // resident CTAs per SM the registers are sized for
 constexpr uint32_t kGrpWaitPolls = 1u << 20;
 
 // (1) Rows of every built slot: shared counters per CTA, one global atomic per slot per CTA.
@@ -101,7 +101,7 @@ __global__ void __launch_bounds__(1024)
 // column by column from the staged copies, the bin byte of the row at o.  Consecutive output positions
 // of a run are consecutive bytes of a row block, so a warp's byte stores cover a few sectors.
 template <int GS>
-__global__ void __launch_bounds__(kGrpThreads, 2)
+__global__ void __launch_bounds__(kGrpThreads, kGrpMinBlocks)
     grp_scatter_kernel(const uint8_t* __restrict__ bins, int64_t ldb, int64_t N, int32_t F,
                        const void* __restrict__ g_in, void* __restrict__ g_out, const uint16_t* __restrict__ node,
                        const gbdt_level* __restrict__ level, int32_t max_slots, const uint8_t* __restrict__ build_flag,
@@ -114,8 +114,7 @@ __global__ void __launch_bounds__(kGrpThreads, 2)
   uint32_t* s_cnt = s_inv + kGrpTile;                                           // [max_slots]
   uint32_t* s_off = s_cnt + max_slots;                                          // [max_slots]
   uint32_t* s_base = s_off + max_slots;                                         // [max_slots]
-  uint32_t* s_wpre = s_base + max_slots;                                        // [max_slots]
-  uint8_t* s_flag = reinterpret_cast<uint8_t*>(s_wpre + max_slots);             // [max_slots]
+  uint8_t* s_flag = reinterpret_cast<uint8_t*>(s_base + max_slots);             // [max_slots]
   __shared__ __align__(8) uint64_t s_full[kGrpStages];
   __shared__ uint32_t s_w[33];
 
@@ -176,117 +175,42 @@ __global__ void __launch_bounds__(kGrpThreads, 2)
     const uint32_t slot = e >> 16;
     go[s_base[slot] + (o - s_off[slot])] = gi[e & 0xffffu];
   }
-  // ---- the runs' output words: a word is 4 consecutive positions of a column (one aligned 4-byte word of
-  // the row-block layout); a run of c rows at s_base covers the words s_base / 4 .. (s_base + c - 1) / 4
-  uint32_t myw = 0;
-  for (int s = s0; s < s1; ++s) {
-    const uint32_t c = s_cnt[s];
-    myw += c ? ((s_base[s] + c + 3) >> 2) - (s_base[s] >> 2) : 0;
+  // ---- columns through the stages: a thread owns output positions o = threadIdx.x + k * kGrpThreads and
+  // stores each one's byte (a warp's 32 consecutive positions cover one or two runs: a few sectors).  Storing
+  // whole aligned words instead (four gathered bytes each) was measured slower: a run holds about 16 rows
+  // when 128 nodes share a 4096-row tile, so a warp's words spread over many more sectors than its bytes.
+  uint32_t src[kGrpRowsPerThread], dst[kGrpRowsPerThread];
+  const int n_own = n_out > threadIdx.x ? static_cast<int>((n_out - 1 - threadIdx.x) / kGrpThreads) + 1 : 0;
+#pragma unroll
+  for (int k = 0; k < kGrpRowsPerThread; ++k) {
+    const uint32_t o = threadIdx.x + k * kGrpThreads;
+    src[k] = 0;
+    dst[k] = 0;
+    if (k < n_own) {
+      const uint32_t e = s_inv[o];
+      const uint32_t slot = e >> 16;
+      src[k] = e & 0xffffu;
+      dst[k] = s_base[slot] + (o - s_off[slot]);
+    }
   }
-  uint32_t n_words;
-  uint32_t woff = block_scan_excl(myw, s_w, &n_words);
-  for (int s = s0; s < s1; ++s) {
-    const uint32_t c = s_cnt[s];
-    s_wpre[s] = woff;
-    woff += c ? ((s_base[s] + c + 3) >> 2) - (s_base[s] >> 2) : 0;
-  }
-  __syncthreads();
   int c_fail = -1;
-  if (n_words <= static_cast<uint32_t>(kGrpWordsPerThread * kGrpThreads)) {
-    // word path: a thread owns words vw = threadIdx.x + k * kGrpThreads; each word's four source rows (16 bits
-    // each, 0xffff: the position is not in the run) and its word index
-    uint32_t wi[kGrpWordsPerThread], wsl[kGrpWordsPerThread], wsh[kGrpWordsPerThread];
-#pragma unroll
-    for (int k = 0; k < kGrpWordsPerThread; ++k) {
-      const uint32_t vw = threadIdx.x + k * kGrpThreads;
-      wi[k] = ~0u;
-      wsl[k] = wsh[k] = 0xffffffffu;
-      if (vw < n_words) {
-        int lo = 0, hi = n_slots - 1;  // the run holding word vw: the last slot whose first word is <= vw
-        while (lo < hi) {
-          const int mid = (lo + hi + 1) >> 1;
-          if (s_wpre[mid] <= vw) lo = mid;
-          else hi = mid - 1;
-        }
-        const uint32_t base = s_base[lo], c = s_cnt[lo], w = (base >> 2) + (vw - s_wpre[lo]);
-        uint32_t sp[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const uint32_t p = 4 * w + i;
-          sp[i] = (p >= base && p < base + c) ? (s_inv[s_off[lo] + (p - base)] & 0xffffu) : 0xffffu;
-        }
-        wi[k] = w;
-        wsl[k] = sp[0] | (sp[1] << 16);
-        wsh[k] = sp[2] | (sp[3] << 16);
-      }
-    }
 #pragma unroll 1
-    for (int c = 0; c < F; ++c) {
-      const int st = c % kGrpStages;
-      const bool ok = mbar_wait(&s_full[st], static_cast<uint32_t>((c / kGrpStages) & 1), kGrpWaitPolls);
-      if (ok) {
-        const uint8_t* stage = s_stage[st];
-        uint8_t* out = rb + static_cast<int64_t>(c) * kRowBlock;
+  for (int c = 0; c < F; ++c) {
+    const int st = c % kGrpStages;
+    const bool ok = mbar_wait(&s_full[st], static_cast<uint32_t>((c / kGrpStages) & 1), kGrpWaitPolls);
+    if (ok) {
+      const uint8_t* stage = s_stage[st];
+      uint8_t* out = rb + static_cast<int64_t>(c) * kRowBlock;
 #pragma unroll
-        for (int k = 0; k < kGrpWordsPerThread; ++k) {
-          if (wi[k] == ~0u) continue;
-          uint8_t* o = out + static_cast<int64_t>(wi[k] >> 3) * pitch + 4 * (wi[k] & 7);
-          const uint32_t a0 = wsl[k] & 0xffffu, a1 = wsl[k] >> 16, a2 = wsh[k] & 0xffffu, a3 = wsh[k] >> 16;
-          if (a0 != 0xffffu && a1 != 0xffffu && a2 != 0xffffu && a3 != 0xffffu) {
-            *reinterpret_cast<uint32_t*>(o) = static_cast<uint32_t>(stage[a0]) |
-                                             (static_cast<uint32_t>(stage[a1]) << 8) |
-                                             (static_cast<uint32_t>(stage[a2]) << 16) |
-                                             (static_cast<uint32_t>(stage[a3]) << 24);
-          } else {  // a run starts or ends inside this word: only its own bytes (a neighbour run owns the rest)
-            if (a0 != 0xffffu) o[0] = stage[a0];
-            if (a1 != 0xffffu) o[1] = stage[a1];
-            if (a2 != 0xffffu) o[2] = stage[a2];
-            if (a3 != 0xffffu) o[3] = stage[a3];
-          }
-        }
-      }
-      if (__syncthreads_or(!ok)) {  // every thread is done with this stage (or a copy timed out)
-        c_fail = c;
-        break;
-      }
-      if (threadIdx.x == 0 && c + kGrpStages < F)
-        bulk_load(s_stage[st], bins + static_cast<int64_t>(c + kGrpStages) * ldb + p0, span, &s_full[st]);
+      for (int k = 0; k < kGrpRowsPerThread; ++k)
+        if (k < n_own) out[static_cast<int64_t>(dst[k] >> 5) * pitch + (dst[k] & 31)] = stage[src[k]];
     }
-  } else {
-    // byte path (runs so short that their words outnumber what the word path holds): a thread owns output
-    // positions o = threadIdx.x + k * kGrpThreads and stores each one's byte
-    uint32_t src[kGrpRowsPerThread], dst[kGrpRowsPerThread];
-    const int n_own = n_out > threadIdx.x ? static_cast<int>((n_out - 1 - threadIdx.x) / kGrpThreads) + 1 : 0;
-#pragma unroll
-    for (int k = 0; k < kGrpRowsPerThread; ++k) {
-      const uint32_t o = threadIdx.x + k * kGrpThreads;
-      src[k] = 0;
-      dst[k] = 0;
-      if (k < n_own) {
-        const uint32_t e = s_inv[o];
-        const uint32_t slot = e >> 16;
-        src[k] = e & 0xffffu;
-        dst[k] = s_base[slot] + (o - s_off[slot]);
-      }
+    if (__syncthreads_or(!ok)) {  // every thread is done with this stage (or a copy timed out)
+      c_fail = c;
+      break;
     }
-#pragma unroll 1
-    for (int c = 0; c < F; ++c) {
-      const int st = c % kGrpStages;
-      const bool ok = mbar_wait(&s_full[st], static_cast<uint32_t>((c / kGrpStages) & 1), kGrpWaitPolls);
-      if (ok) {
-        const uint8_t* stage = s_stage[st];
-        uint8_t* out = rb + static_cast<int64_t>(c) * kRowBlock;
-#pragma unroll
-        for (int k = 0; k < kGrpRowsPerThread; ++k)
-          if (k < n_own) out[static_cast<int64_t>(dst[k] >> 5) * pitch + (dst[k] & 31)] = stage[src[k]];
-      }
-      if (__syncthreads_or(!ok)) {
-        c_fail = c;
-        break;
-      }
-      if (threadIdx.x == 0 && c + kGrpStages < F)
-        bulk_load(s_stage[st], bins + static_cast<int64_t>(c + kGrpStages) * ldb + p0, span, &s_full[st]);
-    }
+    if (threadIdx.x == 0 && c + kGrpStages < F)
+      bulk_load(s_stage[st], bins + static_cast<int64_t>(c + kGrpStages) * ldb + p0, span, &s_full[st]);
   }
   if (c_fail >= 0 && threadIdx.x == 0) {
     raise_error(err, kErrWaitTimeout);
@@ -339,7 +263,7 @@ void launch_group_rows(const uint8_t* bins, int64_t ldb, int64_t N, int32_t F, c
 
 size_t group_rows_smem_bytes(int32_t max_slots) {
   return static_cast<size_t>(kGrpStages) * kGrpTile + sizeof(uint32_t) * kGrpTile +
-         static_cast<size_t>(max_slots) * (4 * sizeof(uint32_t) + 1);
+         static_cast<size_t>(max_slots) * (3 * sizeof(uint32_t) + 1);
 }
 
 }  // namespace gbdt

@@ -233,49 +233,79 @@ __global__ void __launch_bounds__(kHistThreads, 1)
   }
 }
 
-__global__ void hist_zero_kernel(const gbdt_level* __restrict__ level, int32_t max_slots,
-                                 const uint8_t* __restrict__ build_flag, int32_t F, uint32_t* __restrict__ hist_cnt,
-                                 int64_t* __restrict__ hist_q, int64_t* __restrict__ hist_h,
-                                 const uint32_t* __restrict__ cnt0) {
+// Both passes below take four consecutive bins of one feature per thread (16-byte loads and stores; a
+// slot's F x 256 entries are a multiple of 4 and every slot starts 16-byte aligned).  n_bins (may be
+// null): only the bins below each feature's n_bins are touched (the training's histogram passes never
+// write the others and its split search never reads them); null: every bin.
+__device__ __forceinline__ bool quad_used(const int32_t* __restrict__ n_bins, int64_t e) {
+  return !n_bins || static_cast<int>(e & (kBins - 1)) < n_bins[e >> 8];
+}
+
+__global__ void __launch_bounds__(256)
+    hist_zero_kernel(const gbdt_level* __restrict__ level, int32_t max_slots, const uint8_t* __restrict__ build_flag,
+                     int32_t F, uint32_t* __restrict__ hist_cnt, int64_t* __restrict__ hist_q,
+                     int64_t* __restrict__ hist_h, const uint32_t* __restrict__ cnt0,
+                     const int32_t* __restrict__ n_bins) {
   const int n_slots = min(level->n_slots, max_slots);
   const int slot = blockIdx.y;
   if (slot >= n_slots || !build_flag[slot]) return;
   const int64_t per_slot = static_cast<int64_t>(F) * kBins;
-  uint32_t* c = hist_cnt + slot * per_slot;
-  int64_t* q = hist_q + slot * per_slot;
-  int64_t* h = hist_h ? hist_h + slot * per_slot : nullptr;
-  for (int64_t e = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; e < per_slot; e += (int64_t)gridDim.x * blockDim.x) {
-    c[e] = (cnt0 && slot == 0) ? cnt0[e] : 0u;
-    q[e] = 0;
-    if (h) h[e] = 0;
+  const int64_t e = 4 * (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x);
+  if (e >= per_slot || !quad_used(n_bins, e)) return;
+  const int64_t o = slot * per_slot + e;
+  *reinterpret_cast<uint4*>(hist_cnt + o) =
+      (cnt0 && slot == 0) ? *reinterpret_cast<const uint4*>(cnt0 + e) : make_uint4(0, 0, 0, 0);
+  const longlong2 z = make_longlong2(0, 0);
+  reinterpret_cast<longlong2*>(hist_q + o)[0] = z;
+  reinterpret_cast<longlong2*>(hist_q + o)[1] = z;
+  if (hist_h) {
+    reinterpret_cast<longlong2*>(hist_h + o)[0] = z;
+    reinterpret_cast<longlong2*>(hist_h + o)[1] = z;
   }
 }
 
-__global__ void hist_subtract_kernel(const uint32_t* __restrict__ prev_cnt, const int64_t* __restrict__ prev_q,
-                                     const int64_t* __restrict__ prev_h, const int32_t* __restrict__ pair_parent,
-                                     const uint8_t* __restrict__ build_flag, const gbdt_level* __restrict__ level,
-                                     int32_t max_slots, int32_t F, uint32_t* __restrict__ hist_cnt,
-                                     int64_t* __restrict__ hist_q, int64_t* __restrict__ hist_h,
-                                     int32_t* __restrict__ err) {
+__device__ __forceinline__ longlong2 sub2(longlong2 a, longlong2 b) {
+  return make_longlong2(static_cast<long long>(static_cast<unsigned long long>(a.x) - static_cast<unsigned long long>(b.x)),
+                        static_cast<long long>(static_cast<unsigned long long>(a.y) - static_cast<unsigned long long>(b.y)));
+}
+
+__global__ void __launch_bounds__(256)
+    hist_subtract_kernel(const uint32_t* __restrict__ prev_cnt, const int64_t* __restrict__ prev_q,
+                         const int64_t* __restrict__ prev_h, const int32_t* __restrict__ pair_parent,
+                         const uint8_t* __restrict__ build_flag, const gbdt_level* __restrict__ level,
+                         int32_t max_slots, int32_t F, uint32_t* __restrict__ hist_cnt, int64_t* __restrict__ hist_q,
+                         int64_t* __restrict__ hist_h, int32_t* __restrict__ err, const int32_t* __restrict__ n_bins) {
   const int n_slots = min(level->n_slots, max_slots);
   const int p = blockIdx.x;
   if (2 * p + 1 >= n_slots) return;
+  const int64_t per_slot = static_cast<int64_t>(F) * kBins;
+  const int64_t e = 4 * (static_cast<int64_t>(blockIdx.y) * blockDim.x + threadIdx.x);
+  if (e >= per_slot || !quad_used(n_bins, e)) return;
   const int built = build_flag[2 * p] ? 2 * p : 2 * p + 1;
   const int other = built ^ 1;
   const int parent = pair_parent[p];
-  const int64_t per_slot = static_cast<int64_t>(F) * kBins;
-  bool bad = false;
-  for (int64_t e = blockIdx.y * (int64_t)blockDim.x + threadIdx.x; e < per_slot; e += (int64_t)gridDim.y * blockDim.x) {
-    const uint32_t pc = prev_cnt[parent * per_slot + e];
-    const uint32_t bc = hist_cnt[built * per_slot + e];
-    bad |= bc > pc;
-    hist_cnt[other * per_slot + e] = pc - bc;
-    hist_q[other * per_slot + e] = static_cast<int64_t>(static_cast<uint64_t>(prev_q[parent * per_slot + e]) -
-                                                        static_cast<uint64_t>(hist_q[built * per_slot + e]));
-    if (hist_h) {
-      hist_h[other * per_slot + e] = static_cast<int64_t>(static_cast<uint64_t>(prev_h[parent * per_slot + e]) -
-                                                          static_cast<uint64_t>(hist_h[built * per_slot + e]));
-    }
+  const int64_t op = parent * per_slot + e, ob = built * per_slot + e, oo = other * per_slot + e;
+  const uint4 pc = *reinterpret_cast<const uint4*>(prev_cnt + op);
+  const uint4 bc = *reinterpret_cast<const uint4*>(hist_cnt + ob);
+  const longlong2 pq0 = reinterpret_cast<const longlong2*>(prev_q + op)[0];
+  const longlong2 pq1 = reinterpret_cast<const longlong2*>(prev_q + op)[1];
+  const longlong2 bq0 = reinterpret_cast<const longlong2*>(hist_q + ob)[0];
+  const longlong2 bq1 = reinterpret_cast<const longlong2*>(hist_q + ob)[1];
+  // bins of a quad at or above n_bins hold anything: only the used ones are checked
+  const int nb = n_bins ? n_bins[e >> 8] : kBins;
+  const int b0 = static_cast<int>(e & (kBins - 1));
+  const bool bad = (bc.x > pc.x && b0 < nb) || (bc.y > pc.y && b0 + 1 < nb) || (bc.z > pc.z && b0 + 2 < nb) ||
+                   (bc.w > pc.w && b0 + 3 < nb);
+  *reinterpret_cast<uint4*>(hist_cnt + oo) = make_uint4(pc.x - bc.x, pc.y - bc.y, pc.z - bc.z, pc.w - bc.w);
+  reinterpret_cast<longlong2*>(hist_q + oo)[0] = sub2(pq0, bq0);
+  reinterpret_cast<longlong2*>(hist_q + oo)[1] = sub2(pq1, bq1);
+  if (hist_h) {
+    const longlong2 ph0 = reinterpret_cast<const longlong2*>(prev_h + op)[0];
+    const longlong2 ph1 = reinterpret_cast<const longlong2*>(prev_h + op)[1];
+    const longlong2 bh0 = reinterpret_cast<const longlong2*>(hist_h + ob)[0];
+    const longlong2 bh1 = reinterpret_cast<const longlong2*>(hist_h + ob)[1];
+    reinterpret_cast<longlong2*>(hist_h + oo)[0] = sub2(ph0, bh0);
+    reinterpret_cast<longlong2*>(hist_h + oo)[1] = sub2(ph1, bh1);
   }
   if (bad) raise_error(err, kErrHistTotals);
 }
@@ -314,10 +344,11 @@ HistPlan plan_histograms(int64_t N, int32_t F, int32_t max_slots, int32_t max_bu
 }
 
 void launch_hist_zero(const gbdt_level* level, int32_t max_slots, const uint8_t* build_flag, int32_t F,
-                      uint32_t* hist_cnt, int64_t* hist_q, int64_t* hist_h, cudaStream_t s, const uint32_t* cnt0) {
-  const int64_t per_slot = static_cast<int64_t>(F) * kBins;
-  dim3 grid(static_cast<unsigned>((per_slot + 1023) / 1024), static_cast<unsigned>(max_slots));
-  hist_zero_kernel<<<grid, 256, 0, s>>>(level, max_slots, build_flag, F, hist_cnt, hist_q, hist_h, cnt0);
+                      uint32_t* hist_cnt, int64_t* hist_q, int64_t* hist_h, cudaStream_t s, const uint32_t* cnt0,
+                      const int32_t* n_bins) {
+  const int64_t per_slot = static_cast<int64_t>(F) * kBins;  // 4 bins per thread, 256 threads per CTA
+  dim3 grid(static_cast<unsigned>((per_slot / 4 + 255) / 256), static_cast<unsigned>(max_slots));
+  hist_zero_kernel<<<grid, 256, 0, s>>>(level, max_slots, build_flag, F, hist_cnt, hist_q, hist_h, cnt0, n_bins);
   count_launches();
 }
 
@@ -350,13 +381,13 @@ int launch_hist_build(const HistPlan& plan, const uint8_t* bins, int64_t ldb, in
 void launch_hist_subtract(const uint32_t* prev_cnt, const int64_t* prev_q, const int64_t* prev_h,
                           const int32_t* pair_parent, const uint8_t* build_flag, const gbdt_level* level,
                           int32_t max_slots, int32_t F, uint32_t* hist_cnt, int64_t* hist_q, int64_t* hist_h,
-                          int32_t* err, cudaStream_t s) {
+                          int32_t* err, cudaStream_t s, const int32_t* n_bins) {
   const int pairs = max_slots / 2;
   if (pairs < 1) return;
-  const int64_t per_slot = static_cast<int64_t>(F) * kBins;
-  dim3 grid(static_cast<unsigned>(pairs), static_cast<unsigned>((per_slot + 1023) / 1024));
+  const int64_t per_slot = static_cast<int64_t>(F) * kBins;  // 4 bins per thread, 256 threads per CTA
+  dim3 grid(static_cast<unsigned>(pairs), static_cast<unsigned>((per_slot / 4 + 255) / 256));
   hist_subtract_kernel<<<grid, 256, 0, s>>>(prev_cnt, prev_q, prev_h, pair_parent, build_flag, level, max_slots, F,
-                                             hist_cnt, hist_q, hist_h, err);
+                                             hist_cnt, hist_q, hist_h, err, n_bins);
   count_launches();
 }
 

@@ -39,19 +39,21 @@ struct HistPlan {
 };
 HistPlan plan_histograms(int64_t N, int32_t F, int32_t max_slots, int32_t max_build);
 // Zeroes the flagged slots of hist_cnt/hist_q (and hist_h when not null); cnt0 (not null): slot 0's
-// counts are copied from cnt0 ([F][256]) instead.
+// counts are copied from cnt0 ([F][256]) instead.  n_bins (not null): only each feature's bins below
+// its n_bins (the training's histograms, whose other bins no pass writes or reads).
 void launch_hist_zero(const gbdt_level* level, int32_t max_slots, const uint8_t* build_flag, int32_t F,
                       uint32_t* hist_cnt, int64_t* hist_q, int64_t* hist_h, cudaStream_t s,
-                      const uint32_t* cnt0 = nullptr);
+                      const uint32_t* cnt0 = nullptr, const int32_t* n_bins = nullptr);
 int launch_hist_build(const HistPlan& plan, const uint8_t* bins, int64_t ldb, int64_t N, int32_t F, const void* g,
                       int32_t g_dtype, const int32_t* fixed_exp, const uint16_t* node_of_row,
                       const gbdt_level* level, int32_t max_slots, const uint8_t* build_flag, uint32_t* hist_cnt,
                       int64_t* hist_q, int32_t* err, cudaStream_t s);
-// prev_h/hist_h: both null, or the H histograms subtracted likewise.
+// prev_h/hist_h: both null, or the H histograms subtracted likewise.  n_bins (not null): only each
+// feature's bins below its n_bins.
 void launch_hist_subtract(const uint32_t* prev_cnt, const int64_t* prev_q, const int64_t* prev_h,
                           const int32_t* pair_parent, const uint8_t* build_flag, const gbdt_level* level,
                           int32_t max_slots, int32_t F, uint32_t* hist_cnt, int64_t* hist_q, int64_t* hist_h,
-                          int32_t* err, cudaStream_t s);
+                          int32_t* err, cudaStream_t s, const int32_t* n_bins = nullptr);
 
 // ---- grouping.cu -----------------------------------------------------------------------
 // Rows of a level's built slots copied, grouped by slot, into a row-block buffer rb (pitch
@@ -107,7 +109,8 @@ int launch_seg_histograms(const SegHistPlan& plan, const uint8_t* bins, int64_t 
                           int32_t max_slots, const uint8_t* build_flag, const gbdt_segment* seg,
                           const gbdt_filter* filters, void* scratch, uint32_t* hist_cnt, int64_t* hist_q,
                           int64_t* hist_h, cudaStream_t s, bool row_blocks = false, const uint32_t* floc = nullptr,
-                          const uint32_t* slot_src = nullptr, const uint32_t* root_cnt = nullptr);
+                          const uint32_t* slot_src = nullptr, const uint32_t* root_cnt = nullptr,
+                          const int32_t* n_bins = nullptr);
 // row_blocks: ldb is the row-block pitch, floc the feature locators and slot_src each slot's features
 // (plan_row_block_slots; null: slot s holds feature s); a lane accumulates its slot's byte, the joint
 // code of a 4-bit slot, and the flush splits it into the two features' bins.  hist_h: plan.with_h.

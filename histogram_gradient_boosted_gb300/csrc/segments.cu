@@ -1089,14 +1089,19 @@ __device__ __forceinline__ int pair_run(const PairRoute& pr, const uint8_t* __re
   return 2 * c + ((c ? d21 > pr.b2[1] : d20 > pr.b2[0]) ? 1 : 0);
 }
 
-__global__ void __launch_bounds__(kMvThreads)
+// A tile's runs counted by kPairCountThreads threads, U rows in flight each: one pass over the tile, and
+// four times the threads of the move, so that a level of few tiles (a small matrix) still keeps enough
+// decision loads in flight.
+constexpr int kPairCountThreads = 1024;
+
+__global__ void __launch_bounds__(kPairCountThreads)
     pair_count_kernel(const uint8_t* __restrict__ bins, int64_t pitch, const PairRoute* __restrict__ pairs,
                       const int32_t* __restrict__ tile_start, const PairState* __restrict__ st,
                       int4* __restrict__ tile_cnt) {
-  constexpr int U = 8;  // rows in flight per thread
+  constexpr int U = kMvTile / kPairCountThreads;  // rows in flight per thread
   const int t = blockIdx.x;
   if (t >= st->total_tiles) return;
-  __shared__ int4 s_warp[kMvThreads / 32];
+  __shared__ int4 s_warp[kPairCountThreads / 32];
   const int k = slot_of_tile(tile_start, st->n_pairs, t);
   const PairRoute& pr = pairs[k];
   const int64_t p0 = pr.start + static_cast<int64_t>(t - tile_start[k]) * kMvTile;
@@ -1128,7 +1133,7 @@ __global__ void __launch_bounds__(kMvThreads)
   __syncthreads();
   if (threadIdx.x == 0) {
     int4 tot = make_int4(0, 0, 0, 0);
-    for (int w = 0; w < kMvThreads / 32; ++w) {
+    for (int w = 0; w < kPairCountThreads / 32; ++w) {
       const int4 v = s_warp[w];
       tot.x += v.x, tot.y += v.y, tot.z += v.z, tot.w += v.w;
     }
@@ -1313,7 +1318,7 @@ __global__ void __launch_bounds__(kMvThreads, 5)
 
 // Last split level when it is an odd level: every row of a pair records its
 // leaf (a grandchild when its child splits, else the child), nothing moves.
-__global__ void __launch_bounds__(kMvThreads)
+__global__ void __launch_bounds__(kPairCountThreads)
     pair_leaves_kernel(const uint8_t* __restrict__ bins_in, int64_t pitch, const uint32_t* __restrict__ orig_in,
                        const PairRoute* __restrict__ pairs, const int32_t* __restrict__ tile_start,
                        const PairState* __restrict__ st, uint16_t* __restrict__ leaf_of_row) {
@@ -1435,7 +1440,7 @@ int launch_seg_histograms(const SegHistPlan& plan, const uint8_t* bins, int64_t 
                           int32_t max_slots, const uint8_t* build_flag, const gbdt_segment* seg,
                           const gbdt_filter* filters, void* scratch, uint32_t* hist_cnt, int64_t* hist_q,
                           int64_t* hist_h, cudaStream_t s, bool row_blocks, const uint32_t* floc,
-                          const uint32_t* slot_src, const uint32_t* root_cnt) {
+                          const uint32_t* slot_src, const uint32_t* root_cnt, const int32_t* n_bins) {
   (void)N;
   if (root_cnt && !(row_blocks && g_dtype == GBDT_DTYPE_F64 && max_slots == 1)) {
     set_error("known root counts need the row-block layout, fp64 gradients and a one-slot level");
@@ -1445,7 +1450,8 @@ int launch_seg_histograms(const SegHistPlan& plan, const uint8_t* bins, int64_t 
   SegWork* st = c.take<SegWork>(1);
   int32_t* build_slot = c.take<int32_t>(max_slots + 1);
   int64_t* row_start = c.take<int64_t>(max_slots + 1);
-  launch_hist_zero(level, max_slots, build_flag, F, hist_cnt, hist_q, plan.with_h ? hist_h : nullptr, s, root_cnt);
+  launch_hist_zero(level, max_slots, build_flag, F, hist_cnt, hist_q, plan.with_h ? hist_h : nullptr, s, root_cnt,
+                   n_bins);
   seg_work_setup_kernel<<<1, 1024, 0, s>>>(level, max_slots, build_flag, seg, plan.max_ctas, plan.min_rows,
                                            build_slot, row_start, st);
   count_launches();
@@ -1585,7 +1591,8 @@ void launch_move_pairs(const CUtensorMap& map_in, const uint8_t* bins_rb_in, uin
   pair_routes_kernel<<<1, 1024, 0, s>>>(level, max_slots, seg, route_cur, route_prev, pair_parent, seg_next, floc,
                                         p.pairs, p.tile_start, p.st);
   count_launches();
-  pair_count_kernel<<<p.max_tiles, kMvThreads, 0, s>>>(bins_rb_in, pitch, p.pairs, p.tile_start, p.st, p.tile_cnt);
+  pair_count_kernel<<<p.max_tiles, kPairCountThreads, 0, s>>>(bins_rb_in, pitch, p.pairs, p.tile_start, p.st,
+                                                                p.tile_cnt);
   count_launches();
   pair_scan_kernel<<<1, 1024, 0, s>>>(p.pairs, p.tile_start, p.st, p.tile_cnt, p.tile_excl, err);
   count_launches();
@@ -1604,8 +1611,8 @@ void launch_leaf_pairs(const uint8_t* bins_rb, int64_t pitch, const uint32_t* fl
   pair_routes_kernel<<<1, 1024, 0, s>>>(level, max_slots, seg, route_cur, route_prev, pair_parent, seg_next, floc,
                                         p.pairs, p.tile_start, p.st);
   count_launches();
-  pair_leaves_kernel<<<p.max_tiles, kMvThreads, 0, s>>>(bins_rb, pitch, orig_in, p.pairs, p.tile_start, p.st,
-                                                        leaf_of_row);
+  pair_leaves_kernel<<<p.max_tiles, kPairCountThreads, 0, s>>>(bins_rb, pitch, orig_in, p.pairs, p.tile_start,
+                                                               p.st, leaf_of_row);
   count_launches();
 }
 

@@ -71,30 +71,40 @@ __device__ __forceinline__ double score(double G, double H, double lambda) {
   return __ddiv_rn(__dmul_rn(G, G), __dadd_rn(H, lambda));
 }
 
-__device__ __forceinline__ long long warp_sum8(const int64_t* __restrict__ q, int lane) {
-  const longlong2* qp = reinterpret_cast<const longlong2*>(q + lane * 8);
+// Sum over the warp of the bins below nb (a lane holds bins 8 lane .. 8 lane + 7; lanes wholly at or above
+// nb load nothing, the bins of a lane's last word at or above nb are masked out).
+__device__ __forceinline__ long long warp_sum8(const int64_t* __restrict__ q, int lane, int nb) {
   long long s = 0;
+  if (lane * 8 < nb) {
+    const longlong2* qp = reinterpret_cast<const longlong2*>(q + lane * 8);
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    longlong2 v = qp[i];
-    s += v.x + v.y;
+    for (int i = 0; i < 4; ++i) {
+      longlong2 v = qp[i];
+      s += (lane * 8 + 2 * i < nb ? v.x : 0) + (lane * 8 + 2 * i + 1 < nb ? v.y : 0);
+    }
   }
   for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
   return s;
 }
 
-// Node totals from feature 0 (every row has one bin per feature): warp-wide sums.
-// h (may be null): the H histogram, summed into *th.
+// Node totals from feature 0 (every row has one bin per feature, below that feature's n_bins): warp-wide
+// sums over its bins below nb0.  h (may be null): the H histogram, summed into *th.  Bins at or above a
+// feature's n_bins are never read (the histogram passes do not write them).
 __device__ __forceinline__ void node_totals(const uint32_t* __restrict__ cnt, const int64_t* __restrict__ q,
-                                            const int64_t* __restrict__ h, int lane, uint32_t* tc, long long* tq,
-                                            long long* th) {
-  const uint4* cp = reinterpret_cast<const uint4*>(cnt + lane * 8);
-  uint4 c0 = cp[0], c1 = cp[1];
-  uint32_t c = c0.x + c0.y + c0.z + c0.w + c1.x + c1.y + c1.z + c1.w;
+                                            const int64_t* __restrict__ h, int lane, int nb0, uint32_t* tc,
+                                            long long* tq, long long* th) {
+  uint32_t c = 0;
+  if (lane * 8 < nb0) {
+    const uint4* cp = reinterpret_cast<const uint4*>(cnt + lane * 8);
+    const uint4 c0 = cp[0], c1 = cp[1];
+    const uint32_t v[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) c += lane * 8 + i < nb0 ? v[i] : 0u;
+  }
   for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
   *tc = c;
-  *tq = warp_sum8(q, lane);
-  *th = h ? warp_sum8(h, lane) : 0;
+  *tq = warp_sum8(q, lane, nb0);
+  *th = h ? warp_sum8(h, lane, nb0) : 0;
 }
 
 // Eight bins of one lane (bins 8 lane .. 8 lane + 7) as inclusive prefix sums
@@ -177,9 +187,15 @@ __device__ __forceinline__ void screen_feature(const uint32_t* __restrict__ hist
                                                Surv* __restrict__ surv, int32_t* __restrict__ err) {
   const int64_t base = static_cast<int64_t>(slot) * F * kBins;
   const int64_t off = base + static_cast<int64_t>(f) * kBins + lane * 8;
+  int nb = n_bins[f];
+  nb = nb < 1 ? 1 : (nb > kBins ? kBins : nb);
+  // only the bins below nb are read (the histogram passes do not write the others): a lane wholly at or
+  // above nb loads nothing, the bins of a lane's word at or above nb read as 0
   uint32_t c[8];
   long long q[8], qh[8];
-  {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) c[i] = 0, q[i] = 0, qh[i] = 0;
+  if (lane * 8 < nb) {
     const uint4* cp = reinterpret_cast<const uint4*>(hist_cnt + off);
     const longlong2* qp = reinterpret_cast<const longlong2*>(hist_q + off);
     uint4 a = cp[0], b = cp[1];
@@ -199,6 +215,9 @@ __device__ __forceinline__ void screen_feature(const uint32_t* __restrict__ hist
         qh[2 * i + 1] = v.y;
       }
     }
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      if (lane * 8 + i >= nb) c[i] = 0, q[i] = 0, qh[i] = 0;
   }
   // prefix sums over the bins; the feature's totals must equal the node totals
   uint32_t fc;
@@ -208,8 +227,6 @@ __device__ __forceinline__ void screen_feature(const uint32_t* __restrict__ hist
   const long long he = kH ? lane_prefix8(qh, lane, &fh) : 0;
   if (lane == 0 && (fc != tot_cnt || fq != tot_q || (kH && fh != tot_h))) raise_error(err, kErrHistTotals);
 
-  int nb = n_bins[f];
-  nb = nb < 1 ? 1 : (nb > kBins ? kBins : nb);
   // Screening in FP32.  Within a node the gain is a non-decreasing function of
   // x = qL^2/(HL+lambda) + qR^2/(HR+lambda) (fixed-point units; score_P,
   // gamma and the scale are the node's constants).  x is a sum of two
@@ -399,7 +416,8 @@ __global__ void __launch_bounds__(kSplitThreads)
   const int64_t base = static_cast<int64_t>(slot) * F * kBins;
   uint32_t tot_cnt;
   long long tot_q, tot_h;
-  node_totals(hist_cnt + base, hist_q + base, kH ? hist_h + base : nullptr, lane, &tot_cnt, &tot_q, &tot_h);
+  const int nb0 = min(max(n_bins[0], 1), kBins);
+  node_totals(hist_cnt + base, hist_q + base, kH ? hist_h + base : nullptr, lane, nb0, &tot_cnt, &tot_q, &tot_h);
   if (f < F)
     screen_feature<kH>(hist_cnt, hist_q, hist_h, fixed_exp, F, n_bins, slot, f, lane, tot_cnt, tot_q, tot_h, lambda,
                        gamma, msl, mcw, mcw_ceil, surv, err);

@@ -485,7 +485,7 @@ extern "C" int gbdt_train(const uint8_t* bins, int64_t ldb, const int32_t* n_bin
         rc = launch_seg_histograms(plan, lb, pitch, N, F, lg, GBDT_DTYPE_F64, w.fixed_exp, w.level[cur], max_slots,
                                    w.build[cur], hseg, hfil, w.seg_scratch, w.hist_cnt[cur], w.hist_q[cur],
                                    w.hist_h[cur], s, true, w.floc, w.slot_src,
-                                   d == 0 && t > 0 ? w.root_cnt : nullptr);
+                                   d == 0 && t > 0 ? w.root_cnt : nullptr, n_bins);
         if (rc != GBDT_OK) return rc;
         if (timing) GBDT_CUDA(cudaEventRecord(ev_hist(t, d, 1), s));
         if (d == 0 && t == 0)
@@ -493,7 +493,8 @@ extern "C" int gbdt_train(const uint8_t* bins, int64_t ldb, const int32_t* n_bin
                                     cudaMemcpyDeviceToDevice, s));
         if (d > 0) {
           launch_hist_subtract(w.hist_cnt[nxt], w.hist_q[nxt], w.hist_h[nxt], w.pair_parent[cur], w.build[cur],
-                               w.level[cur], max_slots, F, w.hist_cnt[cur], w.hist_q[cur], w.hist_h[cur], w.err, s);
+                               w.level[cur], max_slots, F, w.hist_cnt[cur], w.hist_q[cur], w.hist_h[cur], w.err, s,
+                               n_bins);
         }
         launch_find_splits(w.hist_cnt[cur], w.hist_q[cur], w.hist_h[cur], w.fixed_exp, F, n_bins, w.level[cur],
                            max_slots, *p, w.splits, w.split_scratch, w.err, s);

@@ -368,7 +368,8 @@ int gbdt_build_histograms_segmented_h(const uint8_t* bins, int64_t ldb, int32_t 
  * with s = G*G/(H+lambda), FP64, no contraction.  Best = strictly larger
  * gain, then smaller feature, then smaller bin; a slot splits iff its best
  * valid gain is > 0 (else out[slot].feature = -1).  Node totals are the sums
- * over the bins of feature 0 (the same for every feature).
+ * over feature 0's bins below n_bins[0] (the same for every feature); bins at
+ * or above a feature's n_bins are never read (they may hold anything).
  *   out [max_slots] gbdt_split (device); p: host pointer.
  * Work is spread over (slot, feature) pairs, then reduced per slot; since the
  * comparison is a total order the result does not depend on that split.

@@ -241,3 +241,30 @@ def test_partition_matches_oracle():
     for s in range(n_slots):
         if feats[s] < 0:
             assert np.all(new_node[slot == s] == nb + s)
+
+
+def test_find_splits_ignores_bins_at_or_above_n_bins():
+    """The split search reads a feature's bins below its n_bins only (the training's histogram passes never
+    write the others): garbage there changes nothing, not even the node totals' consistency check."""
+    rng = np.random.default_rng(11)
+    N, F, n_slots = 40_009, 7, 6
+    n_bins = np.array([3, 256, 2, 17, 64, 2, 200], np.int32)
+    bins = np.stack([rng.integers(0, nb, N) for nb in n_bins]).astype(np.uint8)
+    node = rng.integers(0, n_slots, N).astype(np.uint16)
+    gv = rng.normal(size=N) + 0.5 * (bins[3] > 8) * (node % 2)
+    S = g.gradient_scale(torch.from_numpy(gv).cuda())
+    hc, hq = g.build_histograms(dev_bins(bins), N, torch.from_numpy(gv).cuda(), S, u16(node), level(0, n_slots),
+                                n_slots, torch.ones(n_slots, dtype=torch.uint8, device="cuda"), n_slots)
+    nbd = torch.from_numpy(n_bins).cuda()
+    params = dict(reg_lambda=1.0, gamma=0.0, min_samples_leaf=5, min_child_weight=0.0)
+    clean = host_struct(g.find_splits(hc, hq, S, nbd, level(0, n_slots), n_slots, **params), g.SPLIT_DTYPE, n_slots)
+    unused = (torch.arange(256, device="cuda")[None, None, :] >= nbd[None, :, None]).expand(n_slots, F, 256)
+    hc2, hq2 = hc.clone(), hq.clone()
+    hc2[unused] = torch.randint(0, 1 << 30, (int(unused.sum()),), dtype=torch.int32, device="cuda")
+    hq2[unused] = torch.randint(-(1 << 60), 1 << 60, (int(unused.sum()),), dtype=torch.int64, device="cuda")
+    ws = g._workspace(g.lib().gbdt_find_splits_workspace_size(F, n_slots))
+    dirty = host_struct(g.find_splits(hc2, hq2, S, nbd, level(0, n_slots), n_slots, ws=ws, **params), g.SPLIT_DTYPE,
+                        n_slots)
+    assert g.workspace_status(ws) == 0
+    assert clean.tobytes() == dirty.tobytes()
+    assert (clean["feature"] >= 0).any()
