@@ -481,7 +481,7 @@ def logistic_leg(g, torch, args, cfg, N, F, Xd, y, pred, peak, peak_kind, stream
 def covtype_leg(g, torch, args, peak, peak_kind, stream):
     """The covtype-shaped workload in the pages' configuration (581,012 x 54, 255 bins, depth 10,
     1023 leaves, 100 trees): whole quantize + training runs timed with CUDA events."""
-    cfg = dict(synth.CONFIGS["covtype"], num_leaves=1023)
+    cfg = dict(synth.CONFIGS["covtype"], num_leaves=1023, hist_registers=args.hist_registers)
     if args.covtype_trees is not None:
         cfg["n_trees"] = args.covtype_trees
     X, y = synth.make("covtype")
@@ -547,7 +547,7 @@ def run_ours(args, rank, local_rank, ws, dist):
               flush=True)
         return 0
     name = args.config
-    cfg = dict(synth.CONFIGS[name])
+    cfg = dict(synth.CONFIGS[name], hist_registers=args.hist_registers)
     if args.trees is not None:
         cfg["n_trees"] = args.trees
     X, y = synth.make(name, n=args.rows)
@@ -728,6 +728,8 @@ def main():
     ap.add_argument("--no-covtype", action="store_true", help="skip the covtype-shaped leg")
     ap.add_argument("--only-micro", action="store_true", help="run only the level microbench (profiling)")
     ap.add_argument("--only-covtype", action="store_true", help="run only the covtype-shaped leg (profiling)")
+    ap.add_argument("--hist-registers", type=int, default=0, choices=[0, 1],
+                    help="accumulate features of at most 8 bins in registers (gbdt_params.hist_registers)")
     ap.add_argument("--baseline-table", action="store_true",
                     help="time every configuration on the GPU and the oracle (one thread, all threads)")
     ap.add_argument("--covtype-trees", type=int, default=None, help="trees of the covtype-shaped leg (profiling)")

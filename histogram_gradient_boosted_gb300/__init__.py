@@ -28,6 +28,7 @@ OK, ERR_INVALID_ARG, ERR_NONFINITE, ERR_WORKSPACE, ERR_CUDA, ERR_INTERNAL = 0, -
 DTYPE_F32, DTYPE_F64 = 0, 1
 OBJECTIVE_SQUARED_ERROR, OBJECTIVE_LOGISTIC = 0, 1
 BIN_PACKING_4BIT, BIN_PACKING_OFF = 0, 1
+HIST_REGISTERS_OFF, HIST_REGISTERS_ON = 0, 1
 LAYOUT_COLUMNS, LAYOUT_ROW_BLOCKS = 0, 1
 MAX_BINS, MAX_DEPTH = 256, 12
 
@@ -56,7 +57,7 @@ class Params(ctypes.Structure):
     _fields_ = [("n_trees", ctypes.c_int32), ("max_depth", ctypes.c_int32), ("learning_rate", ctypes.c_double),
                 ("reg_lambda", ctypes.c_double), ("gamma", ctypes.c_double), ("min_samples_leaf", ctypes.c_int32),
                 ("min_child_weight", ctypes.c_double), ("num_leaves", ctypes.c_int32), ("objective", ctypes.c_int32),
-                ("bin_packing", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+                ("bin_packing", ctypes.c_int32), ("hist_registers", ctypes.c_int32)]
 
 
 class Diagnostics(ctypes.Structure):
@@ -187,9 +188,10 @@ def padded_ld(n: int) -> int:
 
 def make_params(n_trees=1, max_depth=6, learning_rate=0.1, reg_lambda=1.0, gamma=0.0, min_samples_leaf=1,
                 min_child_weight=0.0, num_leaves=0, objective=OBJECTIVE_SQUARED_ERROR, bin_packing=BIN_PACKING_4BIT,
-                **_ignored) -> Params:
+                hist_registers=HIST_REGISTERS_OFF, **_ignored) -> Params:
     return Params(int(n_trees), int(max_depth), float(learning_rate), float(reg_lambda), float(gamma),
-                  int(min_samples_leaf), float(min_child_weight), int(num_leaves), int(objective), int(bin_packing), 0)
+                  int(min_samples_leaf), float(min_child_weight), int(num_leaves), int(objective), int(bin_packing),
+                  int(hist_registers))
 
 
 def version() -> str:

@@ -89,6 +89,11 @@ int validate_params(const gbdt_params* p) {
     set_error("parameters: bin_packing must be %d (4-bit) or %d (off)", GBDT_BIN_PACKING_4BIT, GBDT_BIN_PACKING_OFF);
     return GBDT_ERR_INVALID_ARG;
   }
+  if (p->hist_registers != GBDT_HIST_REGISTERS_OFF && p->hist_registers != GBDT_HIST_REGISTERS_ON) {
+    set_error("parameters: hist_registers must be %d (off) or %d (on)", GBDT_HIST_REGISTERS_OFF,
+              GBDT_HIST_REGISTERS_ON);
+    return GBDT_ERR_INVALID_ARG;
+  }
   if (p->objective != GBDT_OBJECTIVE_SQUARED_ERROR && p->objective != GBDT_OBJECTIVE_LOGISTIC) {
     set_error("parameters: objective must be %d (squared error) or %d (logistic)", GBDT_OBJECTIVE_SQUARED_ERROR,
               GBDT_OBJECTIVE_LOGISTIC);

@@ -72,11 +72,14 @@ size_t find_splits_scratch_bytes(int32_t F, int32_t max_slots);
 // The per-slot counters inside that scratch: zero them before the first launch_find_splits on it
 // (every launch leaves them zero again).
 int32_t* split_counters(void* scratch, int32_t F, int32_t max_slots);
-// hist_h: null (H = count) or the H histograms with exponent fixed_exp[1].
+// hist_h: null (H = count) or the H histograms with exponent fixed_exp[1].  fsched (device, may be null):
+// the features whose n_bins is above kSplitNarrowBins first, then the n_narrow others, each of which one
+// thread searches alone; null: a warp per feature, in order.
+constexpr int kSplitNarrowBins = 8;
 void launch_find_splits(const uint32_t* hist_cnt, const int64_t* hist_q, const int64_t* hist_h,
                         const int32_t* fixed_exp, int32_t F, const int32_t* n_bins, const gbdt_level* level,
                         int32_t max_slots, const gbdt_params& p, gbdt_split* out, void* scratch, int32_t* err,
-                        cudaStream_t s);
+                        cudaStream_t s, const int32_t* fsched = nullptr, int32_t n_narrow = 0);
 
 // ---- partition.cu ---------------------------------------------------------------------
 // Routing entry of a slot: split feature (-1: none), threshold bin, left child node id.
@@ -87,6 +90,17 @@ struct Route {
   int32_t pad;
 };
 // ---- segments.cu ----------------------------------------------------------------------
+// Register groups of a histogram launch: the slots from reg_begin on hold features of at most
+// kRegMaxCodes codes (one with at most 8 bins, or a 4-bit pair whose bin counts multiply to at most 8);
+// they form groups of 32 after the n_norm_groups ordinary ones, and accumulate in registers.
+constexpr int kRegMaxCodes = 8;
+struct RegGroups {
+  int32_t reg_begin;      // S when there are none
+  int32_t n_norm_groups;  // ordinary groups (they come first in grid.y)
+  int32_t weight;         // a register group's share weight
+  int32_t codes;          // codes a register lane keeps: 4 or 8
+  const int32_t* n_bins;  // device [F]
+};
 // Histograms of the flagged slots of a level whose rows are contiguous segments.
 struct SegHistPlan {
   int n_cols;        // columns the lanes read: slots of the row blocks (features in the column layout)
@@ -98,11 +112,35 @@ struct SegHistPlan {
   int64_t min_rows;  // least work (rows + a fixed cost per slot) a CTA takes when the level is small
   bool with_h;       // logistic: H histograms too (h = logistic_hess(g), exponent fixed_exp[1])
   size_t smem;
+  int reg_begin;     // first register slot (S: none)
+  int n_norm_groups; // ordinary groups
+  int reg_weight;    // share weight of a register group
+  int reg_codes;     // codes per register lane (4 or 8)
 };
+// The histogram work of a level is cut by cost: every built slot costs its rows plus kSlotCost, the
+// fixed work of taking up a slot (the dependent loads of its first rows, two barriers and the flush of
+// the CTA's shared histograms, about what 128 rows of updates take).  Cutting by rows alone put a run
+// of many tiny slots (deep levels) on one CTA, which then took them one by one.
+constexpr int64_t kSlotCost = 128;
+// The work list a level's histogram launch reads: the built slots with their rows in slot order.
+struct SegWork {
+  int64_t total_rows;  // rows over all built slots
+  int64_t total_cost;  // total_rows + kSlotCost x n_built
+  int32_t n_built;     // built slots
+  int32_t ctas;        // CTAs per feature group that have work (at most max_ctas, at least min_rows of cost each)
+};
+struct SegWorkView {
+  SegWork* st;
+  int32_t* build_slot;  // [max_slots + 1]: the k-th built slot
+  int64_t* row_start;   // [max_slots + 1]: rows of the built slots before the k-th (the total at n_built)
+};
+// Where the work list of a level of max_slots slots sits in seg_hist_scratch_bytes(max_slots) of scratch.
+SegWorkView seg_work_view(void* scratch, int32_t max_slots);
 // S: the columns the lanes read (slots of the row blocks; F in the column layout).
 // filtered: the level's slots are counted through filters (a node's rows inside its pair's segment).
+// reg_begin >= 0: slots from reg_begin on are register slots of at most reg_codes codes (squared error only).
 SegHistPlan plan_seg_histograms(int64_t N, int32_t S, int32_t max_slots, int32_t max_build, bool with_h = false,
-                                bool filtered = false);
+                                bool filtered = false, int32_t reg_begin = -1, int32_t reg_codes = 0);
 size_t seg_hist_scratch_bytes(int32_t max_slots);
 int launch_seg_histograms(const SegHistPlan& plan, const uint8_t* bins, int64_t ldb, int64_t N, int32_t F,
                           const void* g, int32_t g_dtype, const int32_t* fixed_exp, const gbdt_level* level,
@@ -110,7 +148,8 @@ int launch_seg_histograms(const SegHistPlan& plan, const uint8_t* bins, int64_t 
                           const gbdt_filter* filters, void* scratch, uint32_t* hist_cnt, int64_t* hist_q,
                           int64_t* hist_h, cudaStream_t s, bool row_blocks = false, const uint32_t* floc = nullptr,
                           const uint32_t* slot_src = nullptr, const uint32_t* root_cnt = nullptr,
-                          const int32_t* n_bins = nullptr);
+                          const int32_t* n_bins = nullptr, bool work_ready = false);
+// With register groups in the plan, n_bins (device) must be given.
 // row_blocks: ldb is the row-block pitch, floc the feature locators and slot_src each slot's features
 // (plan_row_block_slots; null: slot s holds feature s); a lane accumulates its slot's byte, the joint
 // code of a 4-bit slot, and the flush splits it into the two features' bins.  hist_h: plan.with_h.
@@ -137,6 +176,12 @@ void launch_cols_to_row_blocks(const uint8_t* cols, int64_t ldb, int64_t N, int3
 // slot of its own.  Writes loc[F] (locators) and src[S] (per slot: first feature | second << 16, second
 // 0xffff for a whole-byte slot); returns S.
 int plan_row_block_slots(const int32_t* n_bins, int32_t F, bool pack, uint32_t* loc, uint32_t* src);
+// The same with register slots (regs): features with at most kRegMaxCodes bins are taken out of the
+// ordinary plan and placed after it, paired in feature order when pack is on and the two bin counts
+// multiply to at most kRegMaxCodes; *reg_begin receives the first register slot (S: none) and *reg_codes
+// the most codes of a register slot.
+int plan_row_block_slots_ex(const int32_t* n_bins, int32_t F, bool pack, bool regs, uint32_t* loc, uint32_t* src,
+                            int* reg_begin, int* reg_codes);
 // The tensor map the pair move reads a row-block buffer of S slots through.
 int make_row_block_map(CUtensorMap* map, const uint8_t* rb, int64_t N, int32_t S);
 // Record leaves without moving data: every row of the level (its child when its slot splits, its
@@ -145,11 +190,6 @@ int make_row_block_map(CUtensorMap* map, const uint8_t* rb, int64_t N, int32_t S
 void launch_leaf_rows(const uint8_t* bins_rb, int64_t pitch, const uint32_t* floc, int64_t N,
                       const uint32_t* orig_in, const gbdt_level* level, int32_t max_slots, const gbdt_segment* seg,
                       const Route* route, bool frozen_only, uint16_t* leaf_of_row, void* scratch, cudaStream_t s);
-// Odd level: the scan range (the pair's rows) and filter (the parent's split, the slot's side) of
-// every slot, for the histogram of rows not yet partitioned.
-void launch_pair_scan_ranges(const gbdt_level* level, int32_t max_slots, const gbdt_segment* seg,
-                             const Route* route_prev, const int32_t* pair_parent, gbdt_segment* scan,
-                             gbdt_filter* filters, cudaStream_t s);
 // Odd level, after its splits: move the rows of every sibling pair (still in their parent's order)
 // straight into the next level's order (four grandchild runs per pair); rows of children that do not
 // split record them as their leaf.  route_prev/pair_parent: the level above; seg_next: the next

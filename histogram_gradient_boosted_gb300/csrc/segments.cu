@@ -31,18 +31,7 @@ namespace {
 constexpr int kSegThreads = 768;  // 24 warps: registers for two blocks' loads per warp
 constexpr int kSegMaxFeats = 64;  // features per CTA (64 x 256 x 12 B = 192 KB of shared memory)
 
-// The work of a level is cut by cost: every built slot costs its rows plus kSlotCost, the
-// fixed work of taking up a slot (the dependent loads of its first rows, two barriers and the
-// flush of the CTA's shared histograms, about what 128 rows of updates take).  Cutting by rows
-// alone put a run of many tiny slots (deep levels) on one CTA, which then took them one by one.
-constexpr int64_t kSlotCost = 128;
-
-struct SegWork {
-  int64_t total_rows;  // rows over all built slots
-  int64_t total_cost;  // total_rows + kSlotCost x n_built
-  int32_t n_built;     // built slots
-  int32_t ctas;        // CTAs per feature group that have work
-};
+// The work of a level is cut by cost (kSlotCost, SegWork: kernels.cuh).
 
 // One CTA: compact list of built slots, the prefix of their row counts, and
 // how many CTAs per feature group share the work (at most max_ctas, and no
@@ -360,6 +349,66 @@ __device__ __forceinline__ void seg_hist_rows(uint32_t base, const uint8_t* cons
   }
 }
 
+// ---- register histograms (slots of at most kRegMaxCodes codes: a feature with at most 8 bins, or two whose
+// bin counts multiply to at most 8, in one 4-bit slot).  A lane's code of a row is (byte & 15) + na *
+// (byte >> 4) (na: the first feature's bins; a single feature's byte is below 8, so its code is the byte),
+// and the lane keeps each code's count and fixed-point G in registers: no shared atomics, and a flush of
+// kCodes entries per lane instead of 256.
+template <int kCodes, bool kFull, bool kCnt>
+__device__ __forceinline__ void reg_rows32(const uint32_t (&w)[8], const uint2* s_q2, uint32_t valid, int na,
+                                           uint32_t (&rc)[kCodes], long long (&rq)[kCodes]) {
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    if (!kFull && !(valid >> i & 1u)) continue;  // warp-uniform
+    const uint2 qq = s_q2[i];
+    const long long q = static_cast<long long>((static_cast<unsigned long long>(qq.y) << 32) | qq.x);
+    const uint32_t byte = __byte_perm(w[i >> 2], 0u, 0x4440u | static_cast<uint32_t>(i & 3));
+    const int code = static_cast<int>(byte & 15u) + na * static_cast<int>(byte >> 4);
+#pragma unroll
+    for (int c = 0; c < kCodes; ++c) {
+      const bool m = code == c;
+      if (kCnt) rc[c] += m ? 1u : 0u;
+      rq[c] += m ? q : 0ll;
+    }
+  }
+}
+
+// The rows at positions [p0, p1) of one slot added to this lane's registers (a warp takes every n_warps-th
+// row block, loading the next before counting the current, as seg_hist_rows); fp64 g, row-block layout.
+template <int kCodes, bool kCnt>
+__device__ __forceinline__ void seg_reg_rows(const uint8_t* col, bool has, int64_t pitch, const double* __restrict__ g,
+                                             double scale, int64_t p0, int64_t p1, const uint8_t* __restrict__ fcol,
+                                             int fbin, int fside, uint2* s_q2, uint32_t fsh, uint32_t fmk, int na,
+                                             uint32_t (&rc)[kCodes], long long (&rq)[kCodes]) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, n_warps = blockDim.x >> 5;
+  int64_t b = (p0 >> 5) + warp;
+  if ((b << 5) >= p1) return;  // warp-uniform
+  const uint8_t* const cols[1] = {col};
+  const bool hs[1] = {has};
+  SegBlock<1> cur, nxt;
+  seg_load_block<double, 1, true, true>(cur, b, cols, hs, pitch, g, p0, p1, fcol, fsh, fmk);
+  while (true) {
+    const int64_t bn = b + n_warps;
+    const bool more = (bn << 5) < p1;  // warp-uniform
+    if (more) seg_load_block<double, 1, true, true>(nxt, bn, cols, hs, pitch, g, p0, p1, fcol, fsh, fmk);
+    const int64_t pr = (b << 5) + lane;
+    const bool in = pr >= p0 && pr < p1;
+    const bool v = in && (!fcol || (cur.fb > fbin) == (fside != 0));
+    const uint32_t valid = __ballot_sync(0xffffffffu, v);
+    if (valid != 0) {
+      const int64_t q = v ? to_fixed(cur.gv, scale) : 0;
+      __syncwarp();
+      s_q2[lane] = make_uint2(static_cast<uint32_t>(static_cast<uint64_t>(q)), static_cast<uint32_t>(q >> 32));
+      __syncwarp();
+      if (valid == 0xffffffffu) reg_rows32<kCodes, true, kCnt>(cur.w[0], s_q2, valid, na, rc, rq);
+      else reg_rows32<kCodes, false, kCnt>(cur.w[0], s_q2, valid, na, rc, rq);
+    }
+    if (!more) break;
+    b = bn;
+    cur = nxt;
+  }
+}
+
 // Merge the CTA's shared histograms into slot's global histograms and leave
 // the shared ones zeroed for the next slot.  kH: the H words (s_hlo, s_hhi, the
 // two arrays after s_hi) go to hist_h.  Lane j of the group holds column s_lo + j
@@ -437,7 +486,7 @@ __device__ __forceinline__ void seg_hist_flush(uint32_t* s_cnt, uint32_t* s_lo, 
 // slot boundaries flushes its histograms at each crossing.  kH (logistic):
 // also the H histograms, up to 32 features per CTA, fixed_exp[1] their exponent.
 // kCnt false: the counts are already in place (copied by the zeroing launch), only G (and H) add.
-template <typename GT, bool kV8, bool kRB, bool kH, bool kCnt = true>
+template <typename GT, bool kV8, bool kRB, bool kH, bool kCnt = true, bool kReg = false>
 __global__ void __launch_bounds__(kSegThreads, 1)
     seg_hist_kernel(const uint8_t* __restrict__ bins, int64_t ldb, int32_t F, int32_t S, const GT* __restrict__ g,
                     const int32_t* __restrict__ fixed_exp, const gbdt_segment* __restrict__ seg,
@@ -445,16 +494,19 @@ __global__ void __launch_bounds__(kSegThreads, 1)
                     const int64_t* __restrict__ row_start, const SegWork* __restrict__ st, int32_t group_cols,
                     int32_t sm_budget, int32_t total_weight, int32_t row_weight, uint32_t* __restrict__ hist_cnt,
                     int64_t* __restrict__ hist_q, int64_t* __restrict__ hist_h, const uint32_t* __restrict__ floc,
-                    const uint32_t* __restrict__ slot_src) {
+                    const uint32_t* __restrict__ slot_src, RegGroups rg) {
   extern __shared__ __align__(16) unsigned char smem[];
   // this CTA's group: columns (slots) [c_lo, c_lo + ns) of the bins.  Groups get CTAs in proportion
   // to their 32-lane halves + row_weight: where every scanned row is counted a CTA's time per row is
   // about its halves' atomics (row_weight 0); where a filter skips about half of the scanned rows
-  // the row's own work (loads, ballots, the returned values' latency) adds about one half (1)
-  const int c_lo = blockIdx.y * group_cols;
-  const int ns = min(group_cols, S - c_lo);
+  // the row's own work (loads, ballots, the returned values' latency) adds about one half (1).
+  // Register groups (rg: slots from rg.reg_begin on, 32 per group) weigh rg.weight.
+  const bool reg = static_cast<int>(blockIdx.y) >= rg.n_norm_groups;
+  const int c_lo = reg ? rg.reg_begin + (static_cast<int>(blockIdx.y) - rg.n_norm_groups) * 32
+                       : static_cast<int>(blockIdx.y) * group_cols;
+  const int ns = reg ? min(32, S - c_lo) : min(group_cols, rg.reg_begin - c_lo);
   if (ns <= 0) return;
-  const int weight = ((ns + 31) >> 5) + row_weight;
+  const int weight = reg ? rg.weight : ((ns + 31) >> 5) + row_weight;
   const int cap = max(1, static_cast<int>(static_cast<int64_t>(sm_budget) * weight / total_weight));
   const int ctas = min(st->ctas, cap);
   if (static_cast<int>(blockIdx.x) >= ctas) return;
@@ -517,6 +569,69 @@ __global__ void __launch_bounds__(kSegThreads, 1)
       __syncthreads();
     }
   };
+  if constexpr (kReg && kRB && !kH && std::is_same<GT, double>::value) {  // only launches with register groups
+    if (reg) {
+      // register groups: per lane kCodes counts and fixed-point sums; per slot a reduction over the warps in
+      // shared memory and one global add per (lane, code)
+      auto run_reg = [&](auto codes_tag) {
+        constexpr int kCodes = decltype(codes_tag)::value;
+        constexpr int kW = kSegThreads / 32;
+        uint32_t* s_rc = reinterpret_cast<uint32_t*>(smem);                              // [kW][32][kCodes]
+        long long* s_rq = reinterpret_cast<long long*>(smem + kW * 32 * kCodes * 4);    // [kW][32][kCodes]
+        uint2* s_q2 = reinterpret_cast<uint2*>(smem + kW * 32 * kCodes * 12) + warp * 32;
+        const bool has = lane < ns;
+        const int c = c_lo + (has ? lane : 0);
+        const uint8_t* col = bins + static_cast<int64_t>(c) * kRowBlock;
+        const uint32_t sv = slot_src[c];
+        const int fa = static_cast<int>(sv & 0xffffu), fb = static_cast<int>(sv >> 16);
+        const int na = rg.n_bins[fa];
+        for (; k < n_built && row_start[k] + kSlotCost * k < xhi; ++k) {
+          const int64_t c0 = row_start[k] + kSlotCost * k, n_k = row_start[k + 1] - row_start[k];
+          const int64_t o0 = min(max(xlo - c0, int64_t(0)), n_k), o1 = min(xhi - c0, n_k);
+          if (o0 >= o1) continue;  // CTA-uniform
+          const int slot = build_slot[k];
+          const int64_t p0 = seg[slot].start + o0;
+          const gbdt_filter fl = filters ? filters[slot] : gbdt_filter{-1, 0, 0, 0};
+          const uint32_t floc_f = fl.feature < 0 ? 0u : floc[fl.feature];
+          const uint8_t* fcol = fl.feature >= 0 ? bins + static_cast<int64_t>(loc_slot(floc_f)) * kRowBlock : nullptr;
+          uint32_t rc[kCodes];
+          long long rq[kCodes];
+#pragma unroll
+          for (int i = 0; i < kCodes; ++i) rc[i] = 0, rq[i] = 0;
+          seg_reg_rows<kCodes, kCnt>(col, has, ldb, reinterpret_cast<const double*>(g), scale, p0, p0 + (o1 - o0),
+                                     fcol, fl.bin, fl.side, s_q2, loc_shift(floc_f), loc_mask(floc_f), na, rc, rq);
+#pragma unroll
+          for (int i = 0; i < kCodes; ++i) {
+            s_rc[(warp * 32 + lane) * kCodes + i] = rc[i];
+            s_rq[(warp * 32 + lane) * kCodes + i] = rq[i];
+          }
+          __syncthreads();
+          for (int e = threadIdx.x; e < 32 * kCodes; e += blockDim.x) {
+            const int l = e / kCodes, code = e % kCodes;
+            if (l >= ns) continue;
+            uint32_t cn = 0;
+            long long v = 0;
+            for (int ww = 0; ww < kW; ++ww) {
+              cn += s_rc[(ww * 32 + l) * kCodes + code];
+              v += s_rq[(ww * 32 + l) * kCodes + code];
+            }
+            if (kCnt ? cn == 0 : v == 0) continue;
+            const uint32_t svl = slot_src[c_lo + l];
+            const int la = static_cast<int>(svl & 0xffffu), lb = static_cast<int>(svl >> 16);
+            const int nal = rg.n_bins[la];
+            const int64_t row = static_cast<int64_t>(slot) * F;
+            flush_add<kCnt>(hist_cnt, hist_q, nullptr, (row + la) * kBins + code % nal, cn, v, 0);
+            if (lb != 0xffff) flush_add<kCnt>(hist_cnt, hist_q, nullptr, (row + lb) * kBins + code / nal, cn, v, 0);
+          }
+          __syncthreads();
+        }
+        (void)fb;
+      };
+      if (rg.codes <= 4) run_reg(std::integral_constant<int, 4>{});
+      else run_reg(std::integral_constant<int, 8>{});
+      return;
+    }
+  }
   if constexpr (kH) {
     run(std::integral_constant<int, 1>{});
   } else {
@@ -1346,21 +1461,6 @@ __global__ void __launch_bounds__(kPairCountThreads)
   }
 }
 
-// Odd level: each slot's histogram scans its pair's rows (its parent's
-// segment) with the parent's split as the filter.
-__global__ void pair_scan_ranges_kernel(const gbdt_level* __restrict__ level, int32_t max_slots,
-                                        const gbdt_segment* __restrict__ seg, const Route* __restrict__ route_prev,
-                                        const int32_t* __restrict__ pair_parent, gbdt_segment* __restrict__ scan,
-                                        gbdt_filter* __restrict__ filters) {
-  const int n_slots = min(level->n_slots, max_slots);
-  for (int s = blockIdx.x * blockDim.x + threadIdx.x; s < n_slots; s += gridDim.x * blockDim.x) {
-    const int k = s >> 1;
-    const Route up = route_prev[pair_parent[k]];
-    scan[s] = gbdt_segment{seg[2 * k].start, seg[2 * k].count + seg[2 * k + 1].count};
-    filters[s] = gbdt_filter{up.feature, up.bin, s & 1, 0};
-  }
-}
-
 // One CTA: routing of every slot from its split record; the k-th splitting slot
 // (in slot order) gets child slots 2k, 2k+1 of the next level.
 __global__ void routes_from_splits_kernel(const gbdt_split* __restrict__ splits, const gbdt_level* __restrict__ level,
@@ -1406,27 +1506,41 @@ cudaError_t smem_attr(K kernel, size_t bytes) {
 
 // ---- plans and launchers ------------------------------------------------------------------------
 SegHistPlan plan_seg_histograms(int64_t N, int32_t S, int32_t max_slots, int32_t max_build, bool with_h,
-                                bool filtered) {
+                                bool filtered, int32_t reg_begin, int32_t reg_codes) {
   (void)N, (void)max_slots, (void)max_build;
   SegHistPlan p{};
   const int max_feats = with_h ? 32 : kSegMaxFeats;  // five shared words per entry with H, three without
+  const int Sn = (reg_begin >= 0 && !with_h) ? reg_begin : S;  // ordinary slots
   // groups of whole 32-lane halves (an atomic instruction costs the same with idle lanes): full
-  // groups of max_feats columns and the remainder
+  // groups of max_feats columns and the remainder; then register groups of 32 slots
   p.n_cols = S;
-  p.n_fgroups = ceil_div(S, max_feats);
-  p.group_feats = p.n_fgroups == 1 ? S : max_feats;
-  const int rem = S - (p.n_fgroups - 1) * p.group_feats;
+  p.n_norm_groups = Sn > 0 ? ceil_div(Sn, max_feats) : 0;
+  p.group_feats = p.n_norm_groups == 1 ? Sn : max_feats;
+  const int rem = Sn - (p.n_norm_groups - 1) * p.group_feats;
+  const int n_reg = Sn < S ? ceil_div(S - Sn, 32) : 0;
+  p.reg_begin = Sn;
+  p.reg_codes = reg_codes <= 4 ? 4 : kRegMaxCodes;
+  p.n_fgroups = p.n_norm_groups + n_reg;
   // a group's weight: its halves + row_weight (see seg_hist_kernel; measured on the 10M x 100 levels,
-  // 64 + 26 slots: 2 : 1 fastest where every scanned row counts, 3 : 2 at the filtered levels)
+  // 64 + 26 slots: 2 : 1 fastest where every scanned row counts, 3 : 2 at the filtered levels); a register
+  // group weighs as much as one half
   p.row_weight = filtered ? 1 : 0;
-  p.total_weight = (p.n_fgroups - 1) * (ceil_div(p.group_feats, 32) + p.row_weight) + ceil_div(rem, 32) + p.row_weight;
+  p.reg_weight = 1 + p.row_weight;
+  p.total_weight = n_reg * p.reg_weight;
+  if (p.n_norm_groups > 0)
+    p.total_weight += (p.n_norm_groups - 1) * (ceil_div(p.group_feats, 32) + p.row_weight) + ceil_div(rem, 32) +
+                      p.row_weight;
   p.sm_budget = sm_count();  // one wave: a CTA per SM, shared by the groups in proportion to their weights
-  p.max_ctas = std::max(1, static_cast<int>(static_cast<int64_t>(p.sm_budget) *
-                                            (ceil_div(p.group_feats, 32) + p.row_weight) / p.total_weight));
+  const int full_weight = p.n_norm_groups > 0 ? ceil_div(p.group_feats, 32) + p.row_weight : p.reg_weight;
+  p.max_ctas = std::max(1, static_cast<int>(static_cast<int64_t>(p.sm_budget) * full_weight / p.total_weight));
   p.min_rows = 1024;  // least cost (rows + kSlotCost per slot) per CTA
   p.with_h = with_h;
   const size_t words = with_h ? 5 : 3, stage = with_h ? 512 : 256;  // staged row records per warp
-  p.smem = static_cast<size_t>(ceil_div(p.group_feats, 32)) * kHalfWords * 4 * words + (kSegThreads / 32) * stage;
+  p.smem = p.n_norm_groups > 0
+               ? static_cast<size_t>(ceil_div(p.group_feats, 32)) * kHalfWords * 4 * words + (kSegThreads / 32) * stage
+               : 0;
+  if (n_reg > 0)  // per warp and lane each code's count and sum, then the staged row records
+    p.smem = std::max(p.smem, static_cast<size_t>(kSegThreads / 32) * 32 * p.reg_codes * 12 + (kSegThreads / 32) * 256);
   return p;
 }
 
@@ -1435,36 +1549,53 @@ size_t seg_hist_scratch_bytes(int32_t max_slots) {
          sizeof(int64_t) * (static_cast<size_t>(max_slots) + 1) + 3 * kWsAlign;
 }
 
+SegWorkView seg_work_view(void* scratch, int32_t max_slots) {
+  Carve c(scratch, seg_hist_scratch_bytes(max_slots));
+  SegWorkView v;
+  v.st = c.take<SegWork>(1);
+  v.build_slot = c.take<int32_t>(max_slots + 1);
+  v.row_start = c.take<int64_t>(max_slots + 1);
+  return v;
+}
+
 int launch_seg_histograms(const SegHistPlan& plan, const uint8_t* bins, int64_t ldb, int64_t N, int32_t F,
                           const void* g, int32_t g_dtype, const int32_t* fixed_exp, const gbdt_level* level,
                           int32_t max_slots, const uint8_t* build_flag, const gbdt_segment* seg,
                           const gbdt_filter* filters, void* scratch, uint32_t* hist_cnt, int64_t* hist_q,
                           int64_t* hist_h, cudaStream_t s, bool row_blocks, const uint32_t* floc,
-                          const uint32_t* slot_src, const uint32_t* root_cnt, const int32_t* n_bins) {
+                          const uint32_t* slot_src, const uint32_t* root_cnt, const int32_t* n_bins,
+                          bool work_ready) {
   (void)N;
   if (root_cnt && !(row_blocks && g_dtype == GBDT_DTYPE_F64 && max_slots == 1)) {
     set_error("known root counts need the row-block layout, fp64 gradients and a one-slot level");
     return GBDT_ERR_INTERNAL;
   }
-  Carve c(scratch, seg_hist_scratch_bytes(max_slots));
-  SegWork* st = c.take<SegWork>(1);
-  int32_t* build_slot = c.take<int32_t>(max_slots + 1);
-  int64_t* row_start = c.take<int64_t>(max_slots + 1);
+  if (plan.reg_begin < plan.n_cols && !(row_blocks && g_dtype == GBDT_DTYPE_F64 && !plan.with_h && n_bins && slot_src)) {
+    set_error("register histograms need the row-block layout, fp64 gradients, squared error, n_bins and slot sources");
+    return GBDT_ERR_INTERNAL;
+  }
+  const SegWorkView wv = seg_work_view(scratch, max_slots);
+  SegWork* st = wv.st;
+  int32_t* build_slot = wv.build_slot;
+  int64_t* row_start = wv.row_start;
   launch_hist_zero(level, max_slots, build_flag, F, hist_cnt, hist_q, plan.with_h ? hist_h : nullptr, s, root_cnt,
                    n_bins);
-  seg_work_setup_kernel<<<1, 1024, 0, s>>>(level, max_slots, build_flag, seg, plan.max_ctas, plan.min_rows,
-                                           build_slot, row_start, st);
-  count_launches();
+  if (!work_ready) {  // else the work list is already in the scratch (written by the level above)
+    seg_work_setup_kernel<<<1, 1024, 0, s>>>(level, max_slots, build_flag, seg, plan.max_ctas, plan.min_rows,
+                                             build_slot, row_start, st);
+    count_launches();
+  }
   dim3 grid(static_cast<unsigned>(plan.max_ctas), static_cast<unsigned>(plan.n_fgroups));
   // 256-bit column loads need every column start 32-byte aligned
   const bool v8 = aligned(bins, 32) && ldb % 32 == 0;
   auto launch = [&](auto kernel, const auto* gp) -> int {
     GBDT_CUDA(smem_attr(kernel, plan.smem));
+    const RegGroups rg{plan.reg_begin, plan.n_norm_groups, plan.reg_weight, plan.reg_codes, n_bins};
     kernel<<<grid, kSegThreads, plan.smem, s>>>(bins, ldb, F, plan.n_cols, gp, fixed_exp, seg, filters, build_slot,
                                                 row_start, st, plan.group_feats, plan.sm_budget, plan.total_weight,
                                                 plan.row_weight,
                                                 hist_cnt, hist_q, hist_h, row_blocks ? floc : nullptr,
-                                                row_blocks ? slot_src : nullptr);
+                                                row_blocks ? slot_src : nullptr, rg);
     return GBDT_OK;
   };
   auto pick = [&](const auto* gp, auto h_tag) -> int {
@@ -1475,7 +1606,11 @@ int launch_seg_histograms(const SegHistPlan& plan, const uint8_t* bins, int64_t 
                       : launch(seg_hist_kernel<GT, false, false, kH>, gp);
   };
   int rc;
-  if (root_cnt) {  // the root's counts are known: G (and H) only
+  if (plan.reg_begin < plan.n_cols) {  // register groups (row blocks, fp64 g, squared error: checked above)
+    const double* gp = static_cast<const double*>(g);
+    rc = root_cnt ? launch(seg_hist_kernel<double, true, true, false, false, true>, gp)
+                  : launch(seg_hist_kernel<double, true, true, false, true, true>, gp);
+  } else if (root_cnt) {  // the root's counts are known: G (and H) only
     const double* gp = static_cast<const double*>(g);
     rc = plan.with_h ? launch(seg_hist_kernel<double, true, true, true, false>, gp)
                      : launch(seg_hist_kernel<double, true, true, false, false>, gp);
@@ -1573,14 +1708,6 @@ void launch_leaf_rows(const uint8_t* bins_rb, int64_t pitch, const uint32_t* flo
   count_launches();
 }
 
-void launch_pair_scan_ranges(const gbdt_level* level, int32_t max_slots, const gbdt_segment* seg,
-                             const Route* route_prev, const int32_t* pair_parent, gbdt_segment* scan,
-                             gbdt_filter* filters, cudaStream_t s) {
-  pair_scan_ranges_kernel<<<ceil_div(max_slots, 256), 256, 0, s>>>(level, max_slots, seg, route_prev, pair_parent,
-                                                                    scan, filters);
-  count_launches();
-}
-
 void launch_move_pairs(const CUtensorMap& map_in, const uint8_t* bins_rb_in, uint8_t* bins_rb_out, int64_t pitch,
                        const uint32_t* floc, int64_t N, int32_t S, const double* g_in, double* g_out,
                        const uint32_t* orig_in, uint32_t* orig_out, const gbdt_level* level, int32_t max_slots,
@@ -1645,6 +1772,64 @@ int plan_row_block_slots(const int32_t* n_bins, int32_t F, bool pack, uint32_t* 
     src[S++] = static_cast<uint32_t>(f) | 0xffff0000u;
   }
   if (open >= 0) loc[src[open] & 0xffffu] = static_cast<uint32_t>(open);  // unpaired: a whole byte
+  return S;
+}
+
+int plan_row_block_slots_ex(const int32_t* n_bins, int32_t F, bool pack, bool regs, uint32_t* loc, uint32_t* src,
+                            int* reg_begin, int* reg_codes) {
+  *reg_codes = 0;
+  if (!regs) {
+    const int S = plan_row_block_slots(n_bins, F, pack, loc, src);
+    *reg_begin = S;
+    return S;
+  }
+  // ordinary slots: the features with more than kRegMaxCodes bins, as plan_row_block_slots pairs them
+  int S = 0, open = -1;
+  for (int f = 0; f < F; ++f) {
+    if (n_bins[f] <= kRegMaxCodes) continue;
+    if (pack && n_bins[f] <= kMaxPackedBins) {
+      if (open >= 0) {
+        loc[f] = static_cast<uint32_t>(open) | (2u << 16);
+        src[open] = (src[open] & 0xffffu) | (static_cast<uint32_t>(f) << 16);
+        open = -1;
+        continue;
+      }
+      open = S;
+      loc[f] = static_cast<uint32_t>(S) | (1u << 16);
+    } else {
+      loc[f] = static_cast<uint32_t>(S);
+    }
+    src[S++] = static_cast<uint32_t>(f) | 0xffff0000u;
+  }
+  if (open >= 0) loc[src[open] & 0xffffu] = static_cast<uint32_t>(open);
+  *reg_begin = S;
+  // register slots: the others in feature order, a pair when the two bin counts multiply to at most
+  // kRegMaxCodes (the first in the low nibble), else one feature in a whole byte
+  open = -1;
+  auto close_open = [&]() {
+    if (open < 0) return;
+    const int fa = static_cast<int>(src[open] & 0xffffu);
+    loc[fa] = static_cast<uint32_t>(open);
+    *reg_codes = std::max(*reg_codes, static_cast<int>(n_bins[fa]));
+    open = -1;
+  };
+  for (int f = 0; f < F; ++f) {
+    if (n_bins[f] > kRegMaxCodes) continue;
+    if (pack && open >= 0 && n_bins[src[open] & 0xffffu] * n_bins[f] <= kRegMaxCodes) {
+      const int fa = static_cast<int>(src[open] & 0xffffu);
+      loc[fa] = static_cast<uint32_t>(open) | (1u << 16);
+      loc[f] = static_cast<uint32_t>(open) | (2u << 16);
+      src[open] = (src[open] & 0xffffu) | (static_cast<uint32_t>(f) << 16);
+      *reg_codes = std::max(*reg_codes, static_cast<int>(n_bins[fa] * n_bins[f]));
+      open = -1;
+      continue;
+    }
+    close_open();
+    open = S;
+    loc[f] = static_cast<uint32_t>(S);
+    src[S++] = static_cast<uint32_t>(f) | 0xffff0000u;
+  }
+  close_open();
   return S;
 }
 

@@ -178,15 +178,18 @@ __device__ __forceinline__ T lane_prefix8(T (&v)[8], int lane, T* total) {
 // kSurv survive (long runs of empty bins can tie), the best of them evaluated in
 // FP64 as one exact entry.  kH: H from hist_h with exponent fixed_exp[1]
 // (logistic), else H = the row count.  tot_*: the node totals.
-template <bool kH>
+template <bool kH, bool kNarrow>
 __device__ __forceinline__ void screen_feature(const uint32_t* __restrict__ hist_cnt, const int64_t* __restrict__ hist_q,
                                                const int64_t* __restrict__ hist_h, const int32_t* __restrict__ fixed_exp,
                                                int32_t F, const int32_t* __restrict__ n_bins, int slot, int f, int lane,
                                                uint32_t tot_cnt, long long tot_q, long long tot_h, double lambda,
                                                double gamma, int32_t msl, double mcw, int64_t mcw_ceil,
                                                Surv* __restrict__ surv, int32_t* __restrict__ err) {
+  // kNarrow: this thread alone holds the whole feature (at most 8 bins: its bins 0..7), so every sum,
+  // maximum and survivor count below is the thread's own; otherwise the warp holds it, 8 bins per lane
+  const int sub = kNarrow ? 0 : lane;  // this thread's bins: 8 sub .. 8 sub + 7
   const int64_t base = static_cast<int64_t>(slot) * F * kBins;
-  const int64_t off = base + static_cast<int64_t>(f) * kBins + lane * 8;
+  const int64_t off = base + static_cast<int64_t>(f) * kBins + sub * 8;
   int nb = n_bins[f];
   nb = nb < 1 ? 1 : (nb > kBins ? kBins : nb);
   // only the bins below nb are read (the histogram passes do not write the others): a lane wholly at or
@@ -195,7 +198,7 @@ __device__ __forceinline__ void screen_feature(const uint32_t* __restrict__ hist
   long long q[8], qh[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) c[i] = 0, q[i] = 0, qh[i] = 0;
-  if (lane * 8 < nb) {
+  if (sub * 8 < nb) {
     const uint4* cp = reinterpret_cast<const uint4*>(hist_cnt + off);
     const longlong2* qp = reinterpret_cast<const longlong2*>(hist_q + off);
     uint4 a = cp[0], b = cp[1];
@@ -217,15 +220,22 @@ __device__ __forceinline__ void screen_feature(const uint32_t* __restrict__ hist
     }
 #pragma unroll
     for (int i = 0; i < 8; ++i)
-      if (lane * 8 + i >= nb) c[i] = 0, q[i] = 0, qh[i] = 0;
+      if (sub * 8 + i >= nb) c[i] = 0, q[i] = 0, qh[i] = 0;
   }
   // prefix sums over the bins; the feature's totals must equal the node totals
-  uint32_t fc;
-  long long fq, fh = 0;
-  const uint32_t ce = lane_prefix8(c, lane, &fc);
-  const long long qe = lane_prefix8(q, lane, &fq);
-  const long long he = kH ? lane_prefix8(qh, lane, &fh) : 0;
-  if (lane == 0 && (fc != tot_cnt || fq != tot_q || (kH && fh != tot_h))) raise_error(err, kErrHistTotals);
+  uint32_t fc, ce;
+  long long fq, fh = 0, qe, he;
+  if constexpr (kNarrow) {
+#pragma unroll
+    for (int i = 1; i < 8; ++i) c[i] += c[i - 1], q[i] += q[i - 1], qh[i] += qh[i - 1];
+    ce = 0, qe = 0, he = 0;
+    fc = c[7], fq = q[7], fh = kH ? qh[7] : 0;
+  } else {
+    ce = lane_prefix8(c, lane, &fc);
+    qe = lane_prefix8(q, lane, &fq);
+    he = kH ? lane_prefix8(qh, lane, &fh) : 0;
+  }
+  if ((kNarrow || lane == 0) && (fc != tot_cnt || fq != tot_q || (kH && fh != tot_h))) raise_error(err, kErrHistTotals);
 
   // Screening in FP32.  Within a node the gain is a non-decreasing function of
   // x = qL^2/(HL+lambda) + qR^2/(HR+lambda) (fixed-point units; score_P,
@@ -258,7 +268,7 @@ __device__ __forceinline__ void screen_feature(const uint32_t* __restrict__ hist
   float xmax = -1.0f;
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    const int b = lane * 8 + i;
+    const int b = sub * 8 + i;
     const uint32_t cL = ce + c[i];
     const int64_t qL = qe + q[i];
     const uint32_t cR = tot_cnt - cL;
@@ -287,19 +297,22 @@ __device__ __forceinline__ void screen_feature(const uint32_t* __restrict__ hist
     ok |= 1u << i;
     xmax = fmaxf(xmax, x);
   }
-  for (int o = 16; o > 0; o >>= 1) xmax = fmaxf(xmax, __shfl_xor_sync(0xffffffffu, xmax, o));
+  if constexpr (!kNarrow)
+    for (int o = 16; o > 0; o >>= 1) xmax = fmaxf(xmax, __shfl_xor_sync(0xffffffffu, xmax, o));
   const float keep = xmax - xmax * 1.52587890625e-05f;  // xmax * (1 - 2^-16)
   uint32_t sv = 0;  // this lane's survivors
 #pragma unroll
   for (int i = 0; i < 8; ++i)
     if ((ok >> i & 1u) && x32[i] >= keep) sv |= 1u << i;
   const int mine = __popc(sv);
-  int before = mine;  // inclusive prefix over lanes (lanes hold consecutive bins)
-  for (int o = 1; o < 32; o <<= 1) {
-    const int v = __shfl_up_sync(0xffffffffu, before, o);
-    if (lane >= o) before += v;
+  int before = mine, total = mine;  // inclusive prefix over lanes (lanes hold consecutive bins)
+  if constexpr (!kNarrow) {
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, before, o);
+      if (lane >= o) before += v;
+    }
+    total = __shfl_sync(0xffffffffu, before, 31);
   }
-  const int total = __shfl_sync(0xffffffffu, before, 31);
   before -= mine;
   Surv* out = surv + (static_cast<int64_t>(slot) * F + f) * kSurv;
   if (total <= kSurv) {
@@ -308,9 +321,13 @@ __device__ __forceinline__ void screen_feature(const uint32_t* __restrict__ hist
     for (int i = 0; i < 8; ++i) {
       if (!(sv >> i & 1u)) continue;
       const uint32_t cL = ce + c[i];
-      out[k++] = Surv{x32[i], lane * 8 + i, cL, 0, qe + q[i], kH ? he + qh[i] : 0, 0.0};
+      out[k++] = Surv{x32[i], sub * 8 + i, cL, 0, qe + q[i], kH ? he + qh[i] : 0, 0.0};
     }
-    if (lane >= total && lane < kSurv) out[lane] = Surv{-1.0f, -1, 0, 0, 0, 0, 0.0};
+    if constexpr (kNarrow) {
+      for (int e = total; e < kSurv; ++e) out[e] = Surv{-1.0f, -1, 0, 0, 0, 0, 0.0};
+    } else {
+      if (lane >= total && lane < kSurv) out[lane] = Surv{-1.0f, -1, 0, 0, 0, 0, 0.0};
+    }
     return;
   }
   // more survivors than entries: evaluate them all in FP64 here and keep the best
@@ -324,15 +341,20 @@ __device__ __forceinline__ void screen_feature(const uint32_t* __restrict__ hist
     const uint32_t cL = ce + c[i];
     const int64_t qL = qe + q[i], qhL = kH ? he + qh[i] : 0;
     const double gain = exact_gain<kH>(qL, cL, qhL, tot_q, tot_cnt, tot_h, inv, inv_h, sP, lambda, gamma);
-    if (lb.feature < 0 || gain > lb.gain) lb = Cand{gain, f, lane * 8 + i, cL, qL, qhL}, lx = x32[i];
+    if (lb.feature < 0 || gain > lb.gain) lb = Cand{gain, f, sub * 8 + i, cL, qL, qhL}, lx = x32[i];
   }
-  for (int o = 16; o > 0; o >>= 1) {
-    const Cand other = shfl_cand(lb, lane ^ o);
-    const float ox = __shfl_xor_sync(0xffffffffu, lx, o);
-    if (better(other, lb)) lb = other, lx = ox;
+  if constexpr (kNarrow) {
+    out[0] = Surv{lx, lb.bin, lb.cnt_left, 1, lb.q_left, lb.qh_left, lb.gain};
+    for (int e = 1; e < kSurv; ++e) out[e] = Surv{-1.0f, -1, 0, 0, 0, 0, 0.0};
+  } else {
+    for (int o = 16; o > 0; o >>= 1) {
+      const Cand other = shfl_cand(lb, lane ^ o);
+      const float ox = __shfl_xor_sync(0xffffffffu, lx, o);
+      if (better(other, lb)) lb = other, lx = ox;
+    }
+    if (lane == 0) out[0] = Surv{lx, lb.bin, lb.cnt_left, 1, lb.q_left, lb.qh_left, lb.gain};
+    if (lane >= 1 && lane < kSurv) out[lane] = Surv{-1.0f, -1, 0, 0, 0, 0, 0.0};
   }
-  if (lane == 0) out[0] = Surv{lx, lb.bin, lb.cnt_left, 1, lb.q_left, lb.qh_left, lb.gain};
-  if (lane >= 1 && lane < kSurv) out[lane] = Surv{-1.0f, -1, 0, 0, 0, 0, 0.0};
 }
 
 // Select for one slot (the whole 64-thread CTA).  The FP32 margin holds across the slot's features
@@ -407,20 +429,36 @@ __global__ void __launch_bounds__(kSplitThreads)
                  const int64_t* __restrict__ hist_h, const int32_t* __restrict__ fixed_exp, int32_t F,
                  const int32_t* __restrict__ n_bins, const gbdt_level* __restrict__ level, int32_t max_slots,
                  double lambda, double gamma, int32_t msl, double mcw, int64_t mcw_ceil, Surv* __restrict__ surv,
-                 int32_t* __restrict__ slot_done, gbdt_split* __restrict__ out, int32_t* __restrict__ err) {
+                 int32_t* __restrict__ slot_done, gbdt_split* __restrict__ out, int32_t* __restrict__ err,
+                 const int32_t* __restrict__ fsched, int32_t n_wide, int32_t n_narrow) {
   const int slot = blockIdx.x;
   const int n_slots = min(level->n_slots, max_slots);
   if (slot >= n_slots) return;  // every CTA of this slot
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int f = blockIdx.y * kSplitWarps + warp;
+  // the features of this CTA: the first ceil(n_wide / 2) CTAs of a slot take two wide features (a warp
+  // each), the others kSplitThreads narrow ones (a thread each); fsched (null: every feature wide, in
+  // order) lists the wide features, then the narrow ones
+  const int wide_ctas = (n_wide + kSplitWarps - 1) / kSplitWarps;
+  const bool narrow = static_cast<int>(blockIdx.y) >= wide_ctas;
+  int f = -1;
+  if (!narrow) {
+    const int j = blockIdx.y * kSplitWarps + warp;
+    if (j < n_wide) f = fsched ? fsched[j] : j;
+  } else {
+    const int j = (blockIdx.y - wide_ctas) * kSplitThreads + threadIdx.x;
+    if (j < n_narrow) f = fsched[n_wide + j];
+  }
   const int64_t base = static_cast<int64_t>(slot) * F * kBins;
   uint32_t tot_cnt;
   long long tot_q, tot_h;
   const int nb0 = min(max(n_bins[0], 1), kBins);
   node_totals(hist_cnt + base, hist_q + base, kH ? hist_h + base : nullptr, lane, nb0, &tot_cnt, &tot_q, &tot_h);
-  if (f < F)
-    screen_feature<kH>(hist_cnt, hist_q, hist_h, fixed_exp, F, n_bins, slot, f, lane, tot_cnt, tot_q, tot_h, lambda,
-                       gamma, msl, mcw, mcw_ceil, surv, err);
+  if (f >= 0 && narrow)
+    screen_feature<kH, true>(hist_cnt, hist_q, hist_h, fixed_exp, F, n_bins, slot, f, lane, tot_cnt, tot_q, tot_h,
+                             lambda, gamma, msl, mcw, mcw_ceil, surv, err);
+  else if (f >= 0)  // warp-uniform
+    screen_feature<kH, false>(hist_cnt, hist_q, hist_h, fixed_exp, F, n_bins, slot, f, lane, tot_cnt, tot_q, tot_h,
+                              lambda, gamma, msl, mcw, mcw_ceil, surv, err);
   __shared__ int s_last;
   __threadfence();  // this CTA's survivors are visible device-wide before it is counted
   __syncthreads();
@@ -450,21 +488,26 @@ int32_t* split_counters(void* scratch, int32_t F, int32_t max_slots) {
 void launch_find_splits(const uint32_t* hist_cnt, const int64_t* hist_q, const int64_t* hist_h,
                         const int32_t* fixed_exp, int32_t F, const int32_t* n_bins, const gbdt_level* level,
                         int32_t max_slots, const gbdt_params& p, gbdt_split* out, void* scratch, int32_t* err,
-                        cudaStream_t s) {
+                        cudaStream_t s, const int32_t* fsched, int32_t n_narrow) {
   int32_t* done = split_counters(scratch, F, max_slots);
   Surv* surv = reinterpret_cast<Surv*>(static_cast<char*>(scratch) + kCounterBytes);
-  dim3 grid(static_cast<unsigned>(max_slots), static_cast<unsigned>((F + kSplitWarps - 1) / kSplitWarps));
+  if (!fsched) n_narrow = 0;
+  const int n_wide = F - n_narrow;
+  const int ctas = (n_wide + kSplitWarps - 1) / kSplitWarps + (n_narrow + kSplitThreads - 1) / kSplitThreads;
+  dim3 grid(static_cast<unsigned>(max_slots), static_cast<unsigned>(ctas));
   // ceil(min_child_weight) for the count test (counts are below 2^32)
   const double cm = std::ceil(p.min_child_weight);
   const int64_t mcw_ceil = cm > 8.0e9 ? int64_t(8000000000) : static_cast<int64_t>(cm);
   if (hist_h)
     split_kernel<true><<<grid, kSplitThreads, 0, s>>>(hist_cnt, hist_q, hist_h, fixed_exp, F, n_bins, level,
                                                       max_slots, p.reg_lambda, p.gamma, p.min_samples_leaf,
-                                                      p.min_child_weight, mcw_ceil, surv, done, out, err);
+                                                      p.min_child_weight, mcw_ceil, surv, done, out, err, fsched,
+                                                      n_wide, n_narrow);
   else
     split_kernel<false><<<grid, kSplitThreads, 0, s>>>(hist_cnt, hist_q, nullptr, fixed_exp, F, n_bins, level,
                                                        max_slots, p.reg_lambda, p.gamma, p.min_samples_leaf,
-                                                       p.min_child_weight, mcw_ceil, surv, done, out, err);
+                                                       p.min_child_weight, mcw_ceil, surv, done, out, err, fsched,
+                                                      n_wide, n_narrow);
   count_launches();
 }
 

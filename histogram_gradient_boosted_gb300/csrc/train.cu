@@ -37,15 +37,39 @@ struct LevelStats {
 
 std::atomic<int32_t> g_fail_after_levels{-1};
 
+// The next level's histogram work (written by the level above, so that the histogram launch needs no
+// setup launch of its own): the work list in that level's scratch view, the plan's CTA bound and least
+// cost per CTA, and at a filtered (odd) level each slot's scan range and filter.  st null: no next
+// histogram level.
+struct NextWork {
+  SegWorkView wv;
+  int32_t max_ctas;
+  int64_t min_rows;
+  gbdt_segment* scan;    // non-null when the next level is filtered
+  gbdt_filter* filters;
+};
+
+__device__ __forceinline__ int32_t work_ctas(long long cost, const NextWork& nw) {
+  const long long by_size = (cost + nw.min_rows - 1) / nw.min_rows;
+  return static_cast<int32_t>(by_size < nw.max_ctas ? by_size : nw.max_ctas);
+}
+
 // budget[0]: leaves of the tree's earlier levels; budget[1]: 1 once the leaf budget has bound.
 __global__ void reset_root_kernel(gbdt_level* level, uint8_t* build_flag, gbdt_segment* seg, int64_t N,
-                                  int32_t* budget) {
+                                  int32_t* budget, NextWork nw) {
   level->node_begin = 0;
   level->n_slots = 1;
   build_flag[0] = 1;
   seg[0] = gbdt_segment{0, N};
   budget[0] = 0;
   budget[1] = 0;
+  if (nw.wv.st) {  // the root's work list: one slot of N rows
+    nw.wv.build_slot[0] = 0;
+    nw.wv.row_start[0] = 0;
+    nw.wv.row_start[1] = N;
+    const long long cost = N + kSlotCost;
+    *nw.wv.st = SegWork{N, cost, 1, work_ctas(cost, nw)};
+  }
 }
 
 __global__ void iota_kernel(uint32_t* __restrict__ v, int64_t N) {
@@ -87,8 +111,10 @@ __global__ void __launch_bounds__(1024)
                        SlotTotals* __restrict__ next_totals, gbdt_segment* __restrict__ next_seg,
                        int32_t* __restrict__ pair_parent, uint8_t* __restrict__ next_build, Route* __restrict__ route,
                        LevelStats* __restrict__ stats, int32_t num_leaves, int32_t* __restrict__ budget,
-                       int logistic, int32_t* __restrict__ err) {
+                       int logistic, int32_t* __restrict__ err, NextWork nw) {
   __shared__ int s_w[33];
+  __shared__ long long s_wl[33];
+  long long s_rows_pre = 0;  // block-uniform: rows of the next level's work list before the current chunk
   __shared__ double s_gain[kMaxSlots];                  // leaf budget: the level's candidate gains
   __shared__ uint32_t s_cand[kMaxSlots / 32], s_keep[kMaxSlots / 32];
   __shared__ int s_ncand, s_bind;
@@ -176,6 +202,14 @@ __global__ void __launch_bounds__(1024)
     }
     int n_split;
     const int e_split = block_scan_excl(is_split, s_w, &n_split);
+    // the next level's work list: the built child of the k-th split (its rows; at a filtered level the scan
+    // covers the whole pair, the parent's rows)
+    long long wrows = 0;
+    if (is_split) wrows = nw.scan ? static_cast<long long>(tot.cnt)
+                                  : static_cast<long long>(sp.cnt_left <= tot.cnt - sp.cnt_left ? sp.cnt_left
+                                                                                                 : tot.cnt - sp.cnt_left);
+    long long n_wrows;
+    const long long e_rows = block_scan_excl(wrows, s_wl, &n_wrows);
     if (in) {
       const int k = s_pre + e_split;
       const double G = from_fixed(tot.q, S);
@@ -204,6 +238,15 @@ __global__ void __launch_bounds__(1024)
         next_build[2 * k] = left_small;
         next_build[2 * k + 1] = 1 - left_small;
         rt = Route{sp.feature, sp.bin, next_begin + 2 * k, k};
+        if (nw.wv.st) {
+          nw.wv.build_slot[k] = left_small ? 2 * k : 2 * k + 1;
+          nw.wv.row_start[k] = s_rows_pre + e_rows;
+        }
+        if (nw.scan) {  // both children scan the pair's rows (the parent's segment), each keeps its side
+          nw.scan[2 * k] = nw.scan[2 * k + 1] = gbdt_segment{seg[s].start, static_cast<int64_t>(tot.cnt)};
+          nw.filters[2 * k] = gbdt_filter{sp.feature, sp.bin, 0, 0};
+          nw.filters[2 * k + 1] = gbdt_filter{sp.feature, sp.bin, 1, 0};
+        }
       } else {
         nd.feature = nd.threshold_bin = nd.left = nd.right = -1;
         nd.gain = 0.0;
@@ -213,6 +256,7 @@ __global__ void __launch_bounds__(1024)
       route[s] = rt;
     }
     s_pre += n_split;
+    s_rows_pre += n_wrows;
   }
   __syncthreads();  // the shared statistics are complete
   if (threadIdx.x == 0) {
@@ -227,6 +271,11 @@ __global__ void __launch_bounds__(1024)
     stats->n_scan_rows = static_cast<int64_t>(s_scan_rows);
     stats->n_slots = n_slots;
     stats->n_built = s_built;
+    if (nw.wv.st) {
+      nw.wv.row_start[s_pre] = s_rows_pre;
+      const long long cost = s_rows_pre + kSlotCost * s_pre;
+      *nw.wv.st = SegWork{s_rows_pre, cost, s_pre, work_ctas(cost, nw)};
+    }
   }
 }
 
@@ -237,6 +286,7 @@ struct TrainWs {
   uint8_t* bins_rb0;    // the caller's bins in the row-block layout (levels 0 and 1)
   uint32_t* floc;       // [F] where each feature's bins sit in the row-block copies (slot, nibble)
   uint32_t* slot_src;   // [F] the features of each slot
+  int32_t* fsched;      // [F] the split search's features: those with more than kSplitNarrowBins bins, then the rest
   uint8_t* bins_xy[2];  // row-block copies in later orders (alternating)
   double* g_xy[2];
   uint32_t* orig_xy[2];
@@ -285,6 +335,7 @@ TrainWs carve_train(void* ws, size_t bytes, int64_t N, int32_t F, int64_t ldb, c
   w.leaf = c.take<uint16_t>(n16);
   w.floc = c.take<uint32_t>(F);
   w.slot_src = c.take<uint32_t>(F);
+  w.fsched = c.take<int32_t>(F);
   if (D >= 1) {
     w.bins_rb0 = c.take<uint8_t>(row_block_bytes(N, F));
     for (int i = 0; i < 2; ++i) {
@@ -425,9 +476,22 @@ extern "C" int gbdt_train(const uint8_t* bins, int64_t ldb, const int32_t* n_bin
   // byte (4-bit slots); the pair moves read them through tensor maps (one per buffer: the converted
   // input and the two alternating orders)
   std::vector<uint32_t> h_loc(F), h_src(F);
-  const int S = plan_row_block_slots(hb.data(), F, p->bin_packing == GBDT_BIN_PACKING_4BIT, h_loc.data(),
-                                     h_src.data());
+  // register slots (features of at most kRegMaxCodes codes accumulated in registers), squared error only
+  int reg_begin = 0, reg_codes = 0;
+  const bool regs = p->hist_registers == GBDT_HIST_REGISTERS_ON && !logistic;
+  const int S = plan_row_block_slots_ex(hb.data(), F, p->bin_packing == GBDT_BIN_PACKING_4BIT, regs, h_loc.data(),
+                                        h_src.data(), &reg_begin, &reg_codes);
+  const int reg_arg = reg_begin < S ? reg_begin : -1;
   const int64_t pitch = rb_pitch(S);
+  // the split search's feature schedule: a warp for each wide feature, a thread for each narrow one
+  std::vector<int32_t> h_sched;
+  h_sched.reserve(F);
+  for (int j = 0; j < F; ++j)
+    if (hb[j] > kSplitNarrowBins) h_sched.push_back(j);
+  const int n_narrow = F - static_cast<int>(h_sched.size());
+  for (int j = 0; j < F; ++j)
+    if (hb[j] <= kSplitNarrowBins) h_sched.push_back(j);
+  GBDT_CUDA(cudaMemcpyAsync(w.fsched, h_sched.data(), sizeof(int32_t) * F, cudaMemcpyHostToDevice, s));
   CUtensorMap maps[3];
   if (D >= 1) {
     GBDT_CUDA(cudaMemcpyAsync(w.floc, h_loc.data(), sizeof(uint32_t) * F, cudaMemcpyHostToDevice, s));
@@ -439,6 +503,23 @@ extern "C" int gbdt_train(const uint8_t* bins, int64_t ldb, const int32_t* n_bin
       if (rc != GBDT_OK) return rc;
     }
   }
+  // the work the histogram launch of level dn reads, prepared by the level above it (none past the last
+  // histogram level)
+  auto next_work = [&](int dn) {
+    NextWork nw{};
+    if (dn >= D) return nw;
+    const int ms = 1 << dn;
+    const SegHistPlan pl = plan_seg_histograms(N, S, ms, dn == 0 ? 1 : ms / 2, logistic, (dn & 1) != 0, reg_arg,
+                                               reg_codes);
+    nw.wv = seg_work_view(w.seg_scratch, ms);
+    nw.max_ctas = pl.max_ctas;
+    nw.min_rows = pl.min_rows;
+    if (dn & 1) {
+      nw.scan = w.scan;
+      nw.filters = w.filters;
+    }
+    return nw;
+  };
   const int fail_after = g_fail_after_levels.load();
   int levels_done = 0;
   for (int t = 0; t < T; ++t) {
@@ -448,7 +529,7 @@ extern "C" int gbdt_train(const uint8_t* bins, int64_t ldb, const int32_t* n_bin
       launch_start_tree0(w.init, label, N, p->objective, pred_out, w.g0, w.leaf, w.maxabs, s);
     }
     launch_fixed_exp(w.maxabs, N, w.fixed_exp, logistic, s);
-    reset_root_kernel<<<1, 1, 0, s>>>(w.level[0], w.build[0], w.seg[0], N, w.budget);
+    reset_root_kernel<<<1, 1, 0, s>>>(w.level[0], w.build[0], w.seg[0], N, w.budget, next_work(0));
     count_launches();
     if (D == 0) {
       GBDT_CUDA(cudaMemsetAsync(w.totals[0], 0, sizeof(SlotTotals), s));
@@ -470,13 +551,11 @@ extern "C" int gbdt_train(const uint8_t* bins, int64_t ldb, const int32_t* n_bin
       const uint32_t* lo = ph < 0 ? w.orig0 : w.orig_xy[ph];
       if (d < D) {
         const int max_build = d == 0 ? 1 : max_slots / 2;
-        const SegHistPlan plan = plan_seg_histograms(N, S, max_slots, max_build, logistic, odd);
+        const SegHistPlan plan = plan_seg_histograms(N, S, max_slots, max_build, logistic, odd, reg_arg, reg_codes);
         if (timing) GBDT_CUDA(cudaEventRecord(ev_hist(t, d, 0), s));
         const gbdt_segment* hseg = w.seg[cur];
         const gbdt_filter* hfil = nullptr;
-        if (odd) {
-          launch_pair_scan_ranges(w.level[cur], max_slots, w.seg[cur], w.route[nxt], w.pair_parent[cur], w.scan,
-                                  w.filters, s);
+        if (odd) {  // scan ranges and filters written by the level above (apply_level_kernel)
           hseg = w.scan;
           hfil = w.filters;
         }
@@ -485,7 +564,7 @@ extern "C" int gbdt_train(const uint8_t* bins, int64_t ldb, const int32_t* n_bin
         rc = launch_seg_histograms(plan, lb, pitch, N, F, lg, GBDT_DTYPE_F64, w.fixed_exp, w.level[cur], max_slots,
                                    w.build[cur], hseg, hfil, w.seg_scratch, w.hist_cnt[cur], w.hist_q[cur],
                                    w.hist_h[cur], s, true, w.floc, w.slot_src,
-                                   d == 0 && t > 0 ? w.root_cnt : nullptr, n_bins);
+                                   d == 0 && t > 0 ? w.root_cnt : nullptr, n_bins, /*work_ready=*/true);
         if (rc != GBDT_OK) return rc;
         if (timing) GBDT_CUDA(cudaEventRecord(ev_hist(t, d, 1), s));
         if (d == 0 && t == 0)
@@ -497,13 +576,13 @@ extern "C" int gbdt_train(const uint8_t* bins, int64_t ldb, const int32_t* n_bin
                                n_bins);
         }
         launch_find_splits(w.hist_cnt[cur], w.hist_q[cur], w.hist_h[cur], w.fixed_exp, F, n_bins, w.level[cur],
-                           max_slots, *p, w.splits, w.split_scratch, w.err, s);
+                           max_slots, *p, w.splits, w.split_scratch, w.err, s, w.fsched, n_narrow);
       }
       apply_level_kernel<<<1, 1024, 0, s>>>(d, D, w.level[cur], max_slots, d < D ? w.splits : nullptr, w.totals[cur],
                                             w.build[cur], w.fixed_exp, p->reg_lambda, w.seg[cur], tree,
                                             w.n_nodes + t, w.level[nxt], w.totals[nxt], w.seg[nxt],
                                             w.pair_parent[nxt], w.build[nxt], w.route[cur], st, p->num_leaves,
-                                            w.budget, logistic ? 1 : 0, w.err);
+                                            w.budget, logistic ? 1 : 0, w.err, next_work(d + 1));
       count_launches();
       // rows: after an odd level they move into the next order (four grandchild runs per pair); at
       // even levels nothing moves and the rows of nodes that do not split record their leaf; at the

@@ -104,11 +104,17 @@ typedef struct gbdt_params {
                                features with n_bins <= 16 are stored two per byte (4 bits each, the
                                ExaBoost page's packed bins); GBDT_BIN_PACKING_OFF (1): one byte each.
                                Results are identical either way. */
-  int32_t reserved;         /* 0 */
+  int32_t hist_registers;   /* GBDT_HIST_REGISTERS_OFF (0): every level histogram is accumulated with shared-memory
+                               atomics; GBDT_HIST_REGISTERS_ON (1), squared error only: features with at most 8
+                               bins (two of them in one slot when their bin counts multiply to at most 8) are
+                               accumulated per code in registers instead (the ExaBoost page's register-
+                               accumulation construct body).  Results are identical either way. */
 } gbdt_params; /* 64 bytes */
 
 #define GBDT_BIN_PACKING_4BIT 0
 #define GBDT_BIN_PACKING_OFF 1
+#define GBDT_HIST_REGISTERS_OFF 0
+#define GBDT_HIST_REGISTERS_ON 1
 
 /* One tree node, "Module Design: Training Core" s.3 Tree Model: feature,
  * threshold bin, child indices, leaf value, gain and a leaf flag.  Trees are

@@ -193,3 +193,33 @@ def test_bins_beyond_n_bins_are_rejected():
         with pytest.raises(g.GbdtError) as e:
             g.train(bins, bad, yd, **dict(synth.CONFIGS["large"], n_trees=1, max_depth=3))
         assert e.value.code == g.ERR_INVALID_ARG and "n_bins" in str(e.value)
+
+
+@pytest.mark.parametrize("case,packing,budget", [("covtype", 0, 0), ("covtype", 0, 1023), ("large", 0, 0),
+                                                 ("mixed", 0, 0), ("mixed", 1, 0), ("mixed_logistic", 0, 0)])
+def test_register_histograms_give_identical_training(case, packing, budget):
+    """Features with at most 8 bins (two per slot when their bin counts multiply to at most 8) accumulated
+    per code in registers: the same model, bit for bit, as with shared-memory atomics, across filtered
+    levels, the root's reused counts (second and later trees), 4- and 8-code slots and the leaf budget;
+    with the logistic objective the option changes nothing."""
+    if case in ("covtype", "large"):
+        bins, n_bins, yd, ob, on, y = _prepare(case, 30_011)
+        params = dict(synth.CONFIGS[case], n_trees=3)
+        if budget:
+            params.update(num_leaves=budget)
+    else:
+        X, y = _mixed_cardinality(25_013)
+        if case == "mixed_logistic":
+            y = synth.binary_label(y)
+        bins, _, n_bins = g.quantize(torch.from_numpy(X).cuda(), 255)
+        ob, _, on = oracle.quantize(X, 255)
+        yd = torch.from_numpy(y).cuda()
+        params = dict(n_trees=4, max_depth=7, learning_rate=0.2, reg_lambda=1.0, gamma=0.0, min_samples_leaf=3,
+                      min_child_weight=0.0, objective=1 if case == "mixed_logistic" else 0)
+    assert int((n_bins <= 8).sum()) >= 2
+    a = g.train(bins, n_bins, yd, hist_registers=g.HIST_REGISTERS_ON, bin_packing=packing, **params)
+    b = g.train(bins, n_bins, yd, hist_registers=g.HIST_REGISTERS_OFF, bin_packing=packing, **params)
+    assert a["nodes"].tobytes() == b["nodes"].tobytes()
+    assert torch.equal(a["pred"], b["pred"])
+    if case != "mixed_logistic":
+        compare_training(a, ob, on, y, params)
