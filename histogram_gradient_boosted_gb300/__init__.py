@@ -44,6 +44,7 @@ EXPORTED_SYMBOLS = [
     "gbdt_row_block_bytes", "gbdt_bins_to_row_blocks", "gbdt_compute_gradients_objective",
     "gbdt_subtract_histograms_h", "gbdt_build_histograms_segmented_h", "gbdt_find_splits_h", "gbdt_row_block_slots",
     "gbdt_workspace_status", "gbdt_partition_noalloc_status", "gbdt_subtract_histograms_workspace_size",
+    "gbdt_row_block_slots_ex",
 ]
 
 
@@ -128,6 +129,7 @@ def lib():
                                                P], i32),
         "gbdt_row_block_pitch": ([i32], i64),
         "gbdt_row_block_slots": ([P, i32, i32, P, P], i32),
+        "gbdt_row_block_slots_ex": ([P, i32, i32, i32, P, P, P], i32),
         "gbdt_row_block_bytes": ([i64, i32], sz),
         "gbdt_bins_to_row_blocks": ([P, i64, i64, i32, P, P], i32),
         "gbdt_partition_rows_workspace_size": ([i64, i32], sz),
@@ -273,6 +275,20 @@ def row_block_slots(n_bins, packing=BIN_PACKING_4BIT):
                                    loc.ctypes.data_as(ctypes.c_void_p), src.ctypes.data_as(ctypes.c_void_p))
     _check(0 if S > 0 else S)
     return loc, src[:S]
+
+
+def row_block_slots_ex(n_bins, packing=BIN_PACKING_4BIT, hist_registers=HIST_REGISTERS_ON):
+    """Host-side slot plan with register slots: (loc (F,) uint32, src (S,) uint32, reg_begin)."""
+    nb = np.ascontiguousarray(n_bins, dtype=np.int32)
+    F = nb.shape[0]
+    loc = np.zeros(F, np.uint32)
+    src = np.zeros(F, np.uint32)
+    rb = ctypes.c_int32(0)
+    S = lib().gbdt_row_block_slots_ex(nb.ctypes.data_as(ctypes.c_void_p), F, int(packing), int(hist_registers),
+                                      loc.ctypes.data_as(ctypes.c_void_p), src.ctypes.data_as(ctypes.c_void_p),
+                                      ctypes.byref(rb))
+    _check(0 if S > 0 else S)
+    return loc, src[:S], rb.value
 
 
 def to_row_blocks(bins, N: int):

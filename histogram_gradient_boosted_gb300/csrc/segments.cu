@@ -1890,6 +1890,25 @@ extern "C" int32_t gbdt_row_block_slots(const int32_t* n_bins, int32_t F, int32_
   return plan_row_block_slots(n_bins, F, packing == GBDT_BIN_PACKING_4BIT, loc, src);
 }
 
+extern "C" int32_t gbdt_row_block_slots_ex(const int32_t* n_bins, int32_t F, int32_t packing, int32_t hist_registers,
+                                           uint32_t* loc, uint32_t* src, int32_t* reg_begin) {
+  clear_error();
+  GBDT_CHECK_ARG(n_bins && loc && src && reg_begin, "gbdt_row_block_slots_ex: null pointer");
+  GBDT_CHECK_ARG(F >= 1 && F <= 4096, "gbdt_row_block_slots_ex: F out of range");
+  GBDT_CHECK_ARG(packing == GBDT_BIN_PACKING_4BIT || packing == GBDT_BIN_PACKING_OFF,
+                 "gbdt_row_block_slots_ex: bad packing mode");
+  GBDT_CHECK_ARG(hist_registers == GBDT_HIST_REGISTERS_OFF || hist_registers == GBDT_HIST_REGISTERS_ON,
+                 "gbdt_row_block_slots_ex: bad hist_registers mode");
+  for (int f = 0; f < F; ++f)
+    GBDT_CHECK_ARG(n_bins[f] >= 1 && n_bins[f] <= GBDT_MAX_BINS, "gbdt_row_block_slots_ex: n_bins[%d] out of range",
+                   f);
+  int rb = 0, codes = 0;
+  const int S = plan_row_block_slots_ex(n_bins, F, packing == GBDT_BIN_PACKING_4BIT,
+                                        hist_registers == GBDT_HIST_REGISTERS_ON, loc, src, &rb, &codes);
+  *reg_begin = rb;
+  return S;
+}
+
 extern "C" size_t gbdt_row_block_bytes(int64_t N, int32_t F) {
   return (N >= 1 && F >= 1) ? row_block_bytes(N, F) : 0;
 }

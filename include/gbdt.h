@@ -342,6 +342,14 @@ int64_t gbdt_row_block_pitch(int32_t F);
  * the returned count, first feature | second feature << 16 (0xffff: none).
  * Returns the slot count (pitch = 32 x slots), or GBDT_ERR_INVALID_ARG. */
 int32_t gbdt_row_block_slots(const int32_t* n_bins, int32_t F, int32_t packing, uint32_t* loc, uint32_t* src);
+/* gbdt_row_block_slots_ex (HOST only, no GPU): the same plan with a GBDT_HIST_REGISTERS_* mode, the one
+ * gbdt_train uses (squared error).  With GBDT_HIST_REGISTERS_ON the features with at most 8 bins leave the
+ * ordinary plan and get register slots after it, in feature order: two share a slot (the first in the
+ * low nibble) when the packing mode is 4-bit and their bin counts multiply to at most 8, else one takes
+ * a whole byte.  *reg_begin (host) receives the first register slot (the returned count when there are
+ * none).  Returns the slot count, or GBDT_ERR_INVALID_ARG. */
+int32_t gbdt_row_block_slots_ex(const int32_t* n_bins, int32_t F, int32_t packing, int32_t hist_registers,
+                                uint32_t* loc, uint32_t* src, int32_t* reg_begin);
 size_t gbdt_row_block_bytes(int64_t N, int32_t F);
 int gbdt_bins_to_row_blocks(const uint8_t* bins, int64_t ldb, int64_t N, int32_t F, uint8_t* out, void* stream);
 

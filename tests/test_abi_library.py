@@ -142,3 +142,32 @@ def test_row_block_slot_plan_on_host(lib):
         assert len(src) == len(nb) - sum(1 for s in src if s >> 16 != 0xFFFF)
     with pytest.raises(g.GbdtError):
         g.row_block_slots([0, 3])
+
+
+def test_register_slot_plan_on_host(lib):
+    """With register slots the features of at most 8 bins follow the ordinary plan, in feature order, two to a
+    slot (low nibble first) when their bin counts multiply to at most 8, else one to a whole byte."""
+    import numpy as np
+
+    import histogram_gradient_boosted_gb300 as g
+
+    nb = [2, 3, 200, 16, 17, 5, 2, 256, 9, 16, 4, 7, 3, 2]
+    loc, src, rb = g.row_block_slots_ex(nb)
+    slot, nib = loc & 0xFFFF, loc >> 16
+    # ordinary: f2 (whole), f3 + f8 (4-bit pair: 16 and 9 bins), f4, f7, f9 (16 bins, unpaired: whole byte)
+    assert rb == 5 and list(src[:rb] & 0xFFFF) == [2, 3, 4, 7, 9]
+    assert list(src[1:2] >> 16) == [8] and slot[8] == 1 and nib[8] == 2 and nib[3] == 1
+    # register: (f0, f1) 2 x 3 = 6; f5 alone (5 x 2 > 8); (f6, f10) 2 x 4 = 8; f11 alone (7 x 3); (f12, f13) 3 x 2
+    reg = [(int(s & 0xFFFF), int(s >> 16)) for s in src[rb:]]
+    assert reg == [(0, 1), (5, 0xFFFF), (6, 10), (11, 0xFFFF), (12, 13)]
+    for a, b in reg:
+        assert (b == 0xFFFF and nb[a] <= 8) or nb[a] * nb[b] <= 8
+    # every feature exactly once; without registers the plan is gbdt_row_block_slots'
+    seen = sorted([int(s & 0xFFFF) for s in src] + [int(s >> 16) for s in src if s >> 16 != 0xFFFF])
+    assert seen == list(range(len(nb)))
+    l0, s0, rb0 = g.row_block_slots_ex(nb, hist_registers=g.HIST_REGISTERS_OFF)
+    l1, s1 = g.row_block_slots(nb)
+    assert rb0 == len(s0) and np.array_equal(l0, l1) and np.array_equal(s0, s1)
+    # packing off: register features keep whole bytes
+    _, s2, rb2 = g.row_block_slots_ex(nb, packing=g.BIN_PACKING_OFF)
+    assert all(s >> 16 == 0xFFFF for s in s2) and len(s2) == len(nb) and rb2 == 6
