@@ -175,6 +175,16 @@ def _traffic_record():
     return rec if rec.get("kernel_source_sha256") == hist_source_sha256() else None
 
 
+def _scaled_traffic(rec, read_bytes_per_launch):
+    """DRAM bytes per launch of this workload from a smaller capture: the captured bytes scaled by this
+    run's read bytes over the captured run's (rows scanned and built histograms both counted)."""
+    if not rec:
+        return None
+    if "read_bytes_per_launch_captured" not in rec:
+        return rec.get("dram_bytes_per_launch")
+    return rec["dram_bytes_per_launch_captured"] * read_bytes_per_launch / rec["read_bytes_per_launch_captured"]
+
+
 # ------------------------------------------------------------------------------------ reference arm
 def cpu_baseline_sample(X, y, cfg, n_rows, n_trees, threads, repeats=1):
     """The oracle as it stands on the first n_rows rows: quantize (untimed), train (timed)."""
@@ -447,11 +457,13 @@ def logistic_leg(g, torch, args, cfg, N, F, Xd, y, pred, peak, peak_kind, stream
     steps = max(1, min(args.steps, 2))
     diags = []
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    l0 = g.kernel_launch_count()
     e0.record(stream)
     for _ in range(steps):
         diags.append(run(diag=True)["diag"])
     e1.record(stream)
     torch.cuda.synchronize()
+    n_launch = g.kernel_launch_count() - l0
     ms = e0.elapsed_time(e1) / steps
     hist_ms = sum(d["hist_ms"] for d in diags)
     hist_bytes = sum(d["hist_bytes"] for d in diags)
@@ -501,11 +513,13 @@ def covtype_leg(g, torch, args, peak, peak_kind, stream):
     steps = 3
     diags = []
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    l0 = g.kernel_launch_count()
     e0.record(stream)
     for _ in range(steps):
         diags.append(run(diag=True)["diag"])
     e1.record(stream)
     torch.cuda.synchronize()
+    n_launch = g.kernel_launch_count() - l0
     ms = e0.elapsed_time(e1) / steps
     hist_ms = sum(d["hist_ms"] for d in diags)
     hist_bytes = sum(d["hist_bytes"] for d in diags)
@@ -517,6 +531,8 @@ def covtype_leg(g, torch, args, peak, peak_kind, stream):
             "workload": f"covtype-shaped: {N:,} rows x {F} features (10 integer, 44 one-hot binary), 255 bins, "
                         f"depth 10, 1023 leaves, {T} trees",
             "step": "gbdt_quantize + gbdt_train",
+            "launches_per_step": n_launch / steps,
+            "launches_per_tree": n_launch / (steps * T),
             "hist": {"achieved_gbs": achieved, "frac": achieved / peak, "accounting": "level formula",
                      "achieved_read_gbs": achieved_read, "frac_read": achieved_read / peak, "peak_kind": peak_kind,
                      "avg_launch_ms": hist_ms / launches, "share_of_step": hist_ms / (ms * steps)},
@@ -600,7 +616,10 @@ def run_ours(args, rank, local_rank, ws, dist):
     part_ms = sum(d["part_ms"] for d in diags)
     part_bytes = sum(d["part_bytes"] for d in diags)
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                "traffic": (trec["dram_bytes_per_launch"] if trec else None),
+                "traffic": _scaled_traffic(trec, hist_bytes / hist_launches),
+                "traffic_source": (f"ncu DRAM bytes of one tree's level histograms at {trec.get('captured_rows', N):,} "
+                                   "rows, scaled to this workload's launches by the bytes they read "
+                                   "(profiles/histogram_traffic.json)" if trec else "not recorded for this kernel"),
                 "kernel": "seg_hist_kernel (level histograms inside gbdt_train; smaller children, node-contiguous)",
                 "launches": hist_launches, "avg_launch_ms": hist_ms / hist_launches,
                 "algorithmic_bytes_per_launch": level_bytes / hist_launches,
