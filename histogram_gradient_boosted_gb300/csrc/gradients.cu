@@ -114,12 +114,15 @@ __global__ void start_tree0_kernel(const double* __restrict__ init, const float*
   block_max_to(m, mh, maxabs, logistic);
 }
 
-__global__ void finish_tree_kernel(const gbdt_node* __restrict__ tree, const int32_t* __restrict__ n_nodes,
-                                   int32_t max_nodes, double lr, const float* __restrict__ label, int64_t N,
-                                   int objective, double* __restrict__ pred, double* __restrict__ g,
-                                   uint16_t* __restrict__ node, unsigned long long* maxabs, int next) {
+__global__ void finish_tree_kernel(const gbdt_node* __restrict__ trees, const int32_t* __restrict__ n_nodes,
+                                   const int32_t* __restrict__ tree_index, int32_t max_nodes, double lr,
+                                   const float* __restrict__ label, int64_t N, int objective,
+                                   double* __restrict__ pred, double* __restrict__ g, uint16_t* __restrict__ node,
+                                   unsigned long long* maxabs, int next) {
   extern __shared__ double s_step[];  // lr * leaf_value per node of the tree
-  const int nn = min(*n_nodes, max_nodes);
+  const int t = *tree_index;
+  const gbdt_node* __restrict__ tree = trees + static_cast<int64_t>(t) * max_nodes;
+  const int nn = min(n_nodes[t], max_nodes);
   const bool logistic = objective == GBDT_OBJECTIVE_LOGISTIC;
   for (int i = threadIdx.x; i < nn; i += blockDim.x) s_step[i] = __dmul_rn(lr, tree[i].leaf_value);
   __syncthreads();
@@ -207,15 +210,15 @@ void launch_start_tree0(const double* init, const float* label, int64_t N, int32
   start_tree0_kernel<<<elementwise_grid(N), 256, 0, s>>>(init, label, N, objective, pred, g, node, maxabs);
   count_launches();
 }
-void launch_finish_tree(const gbdt_node* tree_nodes, const int32_t* n_nodes, int32_t max_nodes, double lr,
-                        const float* label, int64_t N, int32_t objective, double* pred, double* g, uint16_t* node,
-                        unsigned long long* maxabs, bool next, cudaStream_t s) {
+void launch_finish_tree(const gbdt_node* trees, const int32_t* n_nodes, const int32_t* tree_index,
+                        int32_t max_nodes, double lr, const float* label, int64_t N, int32_t objective, double* pred,
+                        double* g, uint16_t* node, unsigned long long* maxabs, bool next, cudaStream_t s) {
   static bool once = (cudaFuncSetAttribute(finish_tree_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(sizeof(double) * ((1 << (GBDT_MAX_DEPTH + 1)) - 1))),
                       true);
   (void)once;
   finish_tree_kernel<<<elementwise_grid(N), 256, sizeof(double) * max_nodes, s>>>(
-      tree_nodes, n_nodes, max_nodes, lr, label, N, objective, pred, g, node, maxabs, next ? 1 : 0);
+      trees, n_nodes, tree_index, max_nodes, lr, label, N, objective, pred, g, node, maxabs, next ? 1 : 0);
   count_launches();
 }
 void launch_gradients(const double* pred, const float* label, int64_t N, int32_t objective, double* g,

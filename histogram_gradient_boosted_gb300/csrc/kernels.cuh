@@ -19,9 +19,11 @@ void launch_label_mean(const double* partials, int64_t N, double* init /*device*
 void launch_start_tree0(const double* init, const float* label, int64_t N, int32_t objective, double* pred,
                         double* g, uint16_t* node, unsigned long long* maxabs /*[2]*/, cudaStream_t s);
 // pred += lr * leaf_value(node); if next: g at the new pred, node = 0, maxabs as launch_start_tree0.
-void launch_finish_tree(const gbdt_node* tree_nodes, const int32_t* n_nodes, int32_t max_nodes, double lr,
-                        const float* label, int64_t N, int32_t objective, double* pred, double* g, uint16_t* node,
-                        unsigned long long* maxabs, bool next, cudaStream_t s);
+// trees / n_nodes: per-tree arrays (max_nodes nodes per tree); the tree is the one *tree_index names
+// (device memory), so the launch is the same for every tree.
+void launch_finish_tree(const gbdt_node* trees, const int32_t* n_nodes, const int32_t* tree_index,
+                        int32_t max_nodes, double lr, const float* label, int64_t N, int32_t objective, double* pred,
+                        double* g, uint16_t* node, unsigned long long* maxabs, bool next, cudaStream_t s);
 void launch_gradients(const double* pred, const float* label, int64_t N, int32_t objective, double* g,
                       unsigned long long* maxabs, cudaStream_t s);
 void launch_maxabs(const void* g, int32_t dtype, int64_t N, unsigned long long* maxabs, cudaStream_t s);

@@ -54,7 +54,9 @@ __device__ __forceinline__ int32_t work_ctas(long long cost, const NextWork& nw)
   return static_cast<int32_t>(by_size < nw.max_ctas ? by_size : nw.max_ctas);
 }
 
-// budget[0]: leaves of the tree's earlier levels; budget[1]: 1 once the leaf budget has bound.
+// budget[0]: leaves of the tree's earlier levels; budget[1]: 1 once the leaf budget has bound;
+// budget[2]: index of the tree being grown (-1 before the first), advanced here at each tree's start so
+// that the per-tree launch sequence is the same for every tree (it can be replayed as one graph).
 __global__ void reset_root_kernel(gbdt_level* level, uint8_t* build_flag, gbdt_segment* seg, int64_t N,
                                   int32_t* budget, NextWork nw) {
   level->node_begin = 0;
@@ -63,6 +65,7 @@ __global__ void reset_root_kernel(gbdt_level* level, uint8_t* build_flag, gbdt_s
   seg[0] = gbdt_segment{0, N};
   budget[0] = 0;
   budget[1] = 0;
+  budget[2] += 1;
   if (nw.wv.st) {  // the root's work list: one slot of N rows
     nw.wv.build_slot[0] = 0;
     nw.wv.row_start[0] = 0;
@@ -106,12 +109,18 @@ __global__ void __launch_bounds__(1024)
     apply_level_kernel(int d, int D, const gbdt_level* __restrict__ level, int32_t max_slots,
                        const gbdt_split* __restrict__ splits, const SlotTotals* __restrict__ totals,
                        const uint8_t* __restrict__ build_flag, const int32_t* __restrict__ fixed_exp, double lambda,
-                       const gbdt_segment* __restrict__ seg, gbdt_node* __restrict__ tree,
-                       int32_t* __restrict__ n_nodes_out, gbdt_level* __restrict__ next_level,
+                       const gbdt_segment* __restrict__ seg, gbdt_node* __restrict__ trees,
+                       int32_t* __restrict__ n_nodes, gbdt_level* __restrict__ next_level,
                        SlotTotals* __restrict__ next_totals, gbdt_segment* __restrict__ next_seg,
                        int32_t* __restrict__ pair_parent, uint8_t* __restrict__ next_build, Route* __restrict__ route,
-                       LevelStats* __restrict__ stats, int32_t num_leaves, int32_t* __restrict__ budget,
+                       LevelStats* __restrict__ level_stats, int32_t num_leaves, int32_t* __restrict__ budget,
                        int logistic, int32_t* __restrict__ err, NextWork nw) {
+  // this tree's node array, node count and level statistics (trees, n_nodes: per tree; level_stats:
+  // level d of tree 0, D + 1 records per tree)
+  const int t = budget[2];
+  gbdt_node* __restrict__ tree = trees + static_cast<int64_t>(t) * ((2 << D) - 1);
+  int32_t* __restrict__ n_nodes_out = n_nodes + t;
+  LevelStats* __restrict__ stats = level_stats + static_cast<int64_t>(t) * (D + 1);
   __shared__ int s_w[33];
   __shared__ long long s_wl[33];
   long long s_rows_pre = 0;  // block-uniform: rows of the next level's work list before the current chunk
@@ -310,7 +319,7 @@ struct TrainWs {
   int32_t* n_nodes;
   LevelStats* stats;
   unsigned long long* maxabs;
-  int32_t* budget;  // leaf budget state of the current tree
+  int32_t* budget;  // leaf budget state of the current tree; [2]: the tree's index
   int32_t* fixed_exp;  // [2]: S of g, S_h of the logistic hessians
   double* init;
   double* label_partials;
@@ -319,6 +328,49 @@ struct TrainWs {
 };
 
 int32_t max_nodes_of(int D) { return (1 << (D + 1)) - 1; }
+
+// A captured sequence of launches (one tree) replayed with cudaGraphLaunch.  The capture runs on a
+// stream of its own (the caller's stream may be the legacy default stream, which cannot capture);
+// capturing only records the launches, and the launch counter is corrected for them.
+struct TreeGraph {
+  cudaStream_t cs = nullptr;
+  cudaGraphExec_t exec = nullptr;
+  int64_t launches = 0;  // kernels in the graph
+  TreeGraph() = default;
+  TreeGraph(const TreeGraph&) = delete;
+  TreeGraph& operator=(const TreeGraph&) = delete;
+  ~TreeGraph() {  // an executable graph still in flight is released when it completes
+    if (exec) cudaGraphExecDestroy(exec);
+    if (cs) cudaStreamDestroy(cs);
+  }
+  template <typename F>
+  int capture(F&& record) {
+    GBDT_CUDA(cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking));
+    GBDT_CUDA(cudaStreamBeginCapture(cs, cudaStreamCaptureModeRelaxed));
+    const int64_t l0 = launch_count();
+    const int rc = record(cs);
+    cudaGraph_t graph = nullptr;
+    const cudaError_t e = cudaStreamEndCapture(cs, &graph);
+    launches = launch_count() - l0;
+    count_launches(static_cast<int>(-launches));
+    if (rc != GBDT_OK) {
+      if (graph) cudaGraphDestroy(graph);
+      return rc;
+    }
+    if (e != cudaSuccess) {
+      set_error("gbdt_train: capturing a tree's launches failed: %s", cudaGetErrorString(e));
+      return GBDT_ERR_CUDA;
+    }
+    const cudaError_t ei = cudaGraphInstantiate(&exec, graph, 0);
+    cudaGraphDestroy(graph);
+    if (ei != cudaSuccess) {
+      exec = nullptr;
+      set_error("gbdt_train: instantiating a tree's graph failed: %s", cudaGetErrorString(ei));
+      return GBDT_ERR_CUDA;
+    }
+    return GBDT_OK;
+  }
+};
 
 TrainWs carve_train(void* ws, size_t bytes, int64_t N, int32_t F, int64_t ldb, const gbdt_params& p,
                     size_t* need) {
@@ -371,7 +423,7 @@ TrainWs carve_train(void* ws, size_t bytes, int64_t N, int32_t F, int64_t ldb, c
   w.n_nodes = c.take<int32_t>(T);
   w.stats = c.take<LevelStats>(static_cast<size_t>(T) * (D + 1));
   w.maxabs = c.take<unsigned long long>(2);
-  w.budget = c.take<int32_t>(2);
+  w.budget = c.take<int32_t>(4);
   w.fixed_exp = c.take<int32_t>(2);
   w.init = c.take<double>(1);
   w.label_partials = c.take<double>(kSumBlocks);
@@ -522,12 +574,11 @@ extern "C" int gbdt_train(const uint8_t* bins, int64_t ldb, const int32_t* n_bin
   };
   const int fail_after = g_fail_after_levels.load();
   int levels_done = 0;
-  for (int t = 0; t < T; ++t) {
-    gbdt_node* tree = w.trees + static_cast<size_t>(t) * M;
-    if (t == 0) {
-      GBDT_CUDA(cudaMemsetAsync(w.maxabs, 0, 2 * sizeof(unsigned long long), s));
-      launch_start_tree0(w.init, label, N, p->objective, pred_out, w.g0, w.leaf, w.maxabs, s);
-    }
+  // The launches of one tree on stream s.  Every kernel finds the tree it works on through the tree
+  // index in device memory (budget[2], advanced by reset_root_kernel), so the sequence is the same for
+  // every tree but the first (which counts the root's counts and keeps them) and the last (no next
+  // gradients), and the trees between them replay it as one captured graph.
+  auto grow_tree = [&](int t, cudaStream_t s) -> int {
     launch_fixed_exp(w.maxabs, N, w.fixed_exp, logistic, s);
     reset_root_kernel<<<1, 1, 0, s>>>(w.level[0], w.build[0], w.seg[0], N, w.budget, next_work(0));
     count_launches();
@@ -540,7 +591,7 @@ extern "C" int gbdt_train(const uint8_t* bins, int64_t ldb, const int32_t* n_bin
       const int cur = d & 1, nxt = cur ^ 1;
       const bool odd = (d & 1) != 0;
       const int max_slots = 1 << d;
-      LevelStats* st = w.stats + static_cast<size_t>(t) * (D + 1) + d;
+      LevelStats* st = w.stats + d;  // level d of tree 0: the kernel adds the tree's offset
       // Rows are partitioned every second level: levels 0 and 1 read the caller's order; after each
       // odd level the rows move straight into the order of the level below it.  At an odd level a
       // node's rows still sit in its pair's segment, and its histogram filters them by the parent's
@@ -579,8 +630,8 @@ extern "C" int gbdt_train(const uint8_t* bins, int64_t ldb, const int32_t* n_bin
                            max_slots, *p, w.splits, w.split_scratch, w.err, s, w.fsched, n_narrow);
       }
       apply_level_kernel<<<1, 1024, 0, s>>>(d, D, w.level[cur], max_slots, d < D ? w.splits : nullptr, w.totals[cur],
-                                            w.build[cur], w.fixed_exp, p->reg_lambda, w.seg[cur], tree,
-                                            w.n_nodes + t, w.level[nxt], w.totals[nxt], w.seg[nxt],
+                                            w.build[cur], w.fixed_exp, p->reg_lambda, w.seg[cur], w.trees,
+                                            w.n_nodes, w.level[nxt], w.totals[nxt], w.seg[nxt],
                                             w.pair_parent[nxt], w.build[nxt], w.route[cur], st, p->num_leaves,
                                             w.budget, logistic ? 1 : 0, w.err, next_work(d + 1));
       count_launches();
@@ -617,9 +668,34 @@ extern "C" int gbdt_train(const uint8_t* bins, int64_t ldb, const int32_t* n_bin
     }
     const bool next = t + 1 < T;
     if (next) GBDT_CUDA(cudaMemsetAsync(w.maxabs, 0, 2 * sizeof(unsigned long long), s));
-    launch_finish_tree(tree, w.n_nodes + t, M, p->learning_rate, label, N, p->objective, pred_out, w.g0, w.leaf,
-                       w.maxabs, next, s);
+    launch_finish_tree(w.trees, w.n_nodes, w.budget + 2, M, p->learning_rate, label, N, p->objective, pred_out,
+                       w.g0, w.leaf, w.maxabs, next, s);
     GBDT_LAUNCH_CHECK();
+    return GBDT_OK;
+  };
+
+  GBDT_CUDA(cudaMemsetAsync(w.budget + 2, 0xff, sizeof(int32_t), s));  // tree index -1
+  // Trees 1 .. T - 2 as one graph, captured once per call: a deep tree is a long chain of short
+  // launches, whose launch gaps a graph replay removes.  Timed (diagnostics) and failure-injection
+  // runs launch tree by tree.
+  const bool use_graph = !timing && fail_after < 0 && T >= 4;
+  TreeGraph tg;
+  for (int t = 0; t < T; ++t) {
+    if (t == 0) {
+      GBDT_CUDA(cudaMemsetAsync(w.maxabs, 0, 2 * sizeof(unsigned long long), s));
+      launch_start_tree0(w.init, label, N, p->objective, pred_out, w.g0, w.leaf, w.maxabs, s);
+    }
+    if (use_graph && t >= 1 && t + 1 < T) {
+      if (tg.exec == nullptr) {
+        rc = tg.capture([&](cudaStream_t cs) { return grow_tree(t, cs); });
+        if (rc != GBDT_OK) return rc;
+      }
+      GBDT_CUDA(cudaGraphLaunch(tg.exec, s));
+      count_launches(static_cast<int>(tg.launches));
+      continue;
+    }
+    rc = grow_tree(t, s);
+    if (rc != GBDT_OK) return rc;
   }
   if (T == 0) {
     // no tree: predictions are the initial value
