@@ -863,46 +863,50 @@ __device__ __forceinline__ void mv_own_words(const MvRuns<R>& ru, const uint16_t
   }
 }
 
-// The pair move's output words, owned by row-block units: a unit is one aligned 32-position row block
-// of one grandchild run's output (8 words; the first and last of a run may be partial), and the units
-// of the four runs are ordered by the tile position of their first row (an exact merge of four lists
-// that are each in that order already, the runs being stable).  A warp takes four consecutive units,
-// lane l word l & 7 of unit l >> 3, so that the rows a gather instruction reads lie close together in
-// the staged column (consecutive units of the merged order come from the same stretch of the tile)
-// and spread over more banks than 32 consecutive words of one run would; each store still writes whole
-// 32-byte row-block pieces.
-constexpr int kMvMaxUnits = 4 * kMvThreads / 32 * kMvWordsPerThread;  // 160 >= 4096 / 32 + 4 runs x 2
-
+// The pair move's output words, owned by units: a unit is kMvUnit aligned positions of one grandchild
+// run's output (a 32-position unit is one row block of a slot, 8 words; the first and last unit of a
+// run may be partial), and the units of the four runs are ordered by the tile position of their first
+// row (an exact merge of four lists that are each in that order already, the runs being stable).  A
+// warp takes 32 / (kMvUnit / 4) consecutive units, one word per lane, so that the rows a gather
+// instruction reads lie close together in the staged column (consecutive units of the merged order
+// come from the same stretch of the tile) and spread over more banks than 32 consecutive words of one
+// run would.
+constexpr int kMvUnit = 32;                        // positions per unit
+constexpr int kMvUnitWords = kMvUnit / 4;          // lanes per unit
+constexpr int kMvMaxUnits = 32 / kMvUnitWords * kMvThreads / 32 * kMvWordsPerThread;
+static_assert(kMvMaxUnits >= kMvTile / kMvUnit + 8, "every unit of a tile has an owner");
 
 // The four runs of a tile in shared memory (read by the unit functions with a run index).
 struct MvRunTable {
   long long dst[4];
-  int len[4], base[4], a[4], nu[4];  // a: dst & 31; nu: the run's units
+  int len[4], base[4], a[4], nu[4];  // a: dst % kMvUnit; nu: the run's units
 };
 
-// Merge position of every unit (one thread per unit): its rank in its own run plus, for each other
-// run, how many of that run's units start at an earlier tile position.  mask/cbase: per run and
-// 32-row chunk, the run's rows in the chunk and before it.
+// Merge position of every unit: its rank in its own run plus, for each other run, how many of that
+// run's units start at an earlier tile position.  mask/cbase: per run and 32-row chunk, the run's
+// rows in the chunk and before it.
 __device__ __forceinline__ void mv_order_units(const MvRunTable& rt, const uint16_t* s_inv,
                                                const uint32_t (*mask)[kMvChunks], const int (*cbase)[kMvChunks],
                                                uint16_t* s_unit) {
-  int i = threadIdx.x, q = 0;
-  while (q < 4 && i >= rt.nu[q]) i -= rt.nu[q++];  // unit i of the concatenated runs -> run q, unit i of q
-  if (q >= 4) return;
-  const int o_first = i == 0 ? 0 : 32 * i - rt.a[q];  // the unit's first offset in its run
-  const int src = s_inv[rt.base[q] + o_first];        // its tile position
-  int pos = i;
+  const int n_units = rt.nu[0] + rt.nu[1] + rt.nu[2] + rt.nu[3];
+  for (int k = threadIdx.x; k < n_units; k += blockDim.x) {
+    int i = k, q = 0;
+    while (i >= rt.nu[q]) i -= rt.nu[q++];                    // unit k of the concatenated runs -> run q, unit i
+    const int o_first = i == 0 ? 0 : kMvUnit * i - rt.a[q];  // the unit's first offset in its run
+    const int src = s_inv[rt.base[q] + o_first];             // its tile position
+    int pos = i;
 #pragma unroll
-  for (int r = 0; r < 4; ++r) {
-    if (r == q || rt.nu[r] == 0) continue;
-    const int c = src >> 5;
-    const int rows = cbase[r][c] + __popc(mask[r][c] & ((1u << (src & 31)) - 1u));  // run r rows before src
-    pos += rows == 0 ? 0 : min(rt.nu[r], (rows + rt.a[r] + 31) >> 5);
+    for (int r = 0; r < 4; ++r) {
+      if (r == q || rt.nu[r] == 0) continue;
+      const int c = src >> 5;
+      const int rows = cbase[r][c] + __popc(mask[r][c] & ((1u << (src & 31)) - 1u));  // run r rows before src
+      pos += rows == 0 ? 0 : min(rt.nu[r], (rows + rt.a[r] + kMvUnit - 1) / kMvUnit);
+    }
+    s_unit[pos] = static_cast<uint16_t>((q << 14) | i);
   }
-  s_unit[pos] = static_cast<uint16_t>((q << 8) | i);
 }
 
-// This thread's words in unit order (off, srcl, srch as mv_own_words).
+// This thread's words in unit order (off, srcl, srch as mv_own_words; row-block layout).
 __device__ __forceinline__ void mv_own_units(const MvRunTable& rt, const uint16_t* s_inv, const uint16_t* s_unit,
                                              int n_units, int a_off, int64_t pitch,
                                              int64_t (&off)[kMvWordsPerThread], uint32_t (&srcl)[kMvWordsPerThread],
@@ -910,21 +914,20 @@ __device__ __forceinline__ void mv_own_units(const MvRunTable& rt, const uint16_
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
   for (int m = 0; m < kMvWordsPerThread; ++m) {
-    const int k = 4 * (warp + (kMvThreads / 32) * m) + (lane >> 3);
+    const int k = 32 / kMvUnitWords * (warp + (kMvThreads / 32) * m) + lane / kMvUnitWords;
     uint32_t sp[4] = {0xffffu, 0xffffu, 0xffffu, 0xffffu};
     off[m] = -1;
     if (k < n_units) {
-      const int e = s_unit[k], q = e >> 8, u = e & 255;
+      const int e = s_unit[k], q = e >> 14, u = e & 0x3fff;
       const int64_t dst = rt.dst[q];
       const int len = rt.len[q], base = rt.base[q];
-      const int64_t blk = (dst >> 5) + u;            // the unit's row block in the output order
-      const int64_t p0 = blk * 32 + 4 * (lane & 7);  // the word's first output position
+      const int64_t p0 = (dst / kMvUnit + u) * kMvUnit + 4 * (lane % kMvUnitWords);  // the word's first position
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const int64_t o = p0 + j - dst;  // offset in the run
         if (o >= 0 && o < len) sp[j] = s_inv[base + o] + a_off;
       }
-      if ((sp[0] & sp[1] & sp[2] & sp[3]) != 0xffffu) off[m] = blk * pitch + 4 * (lane & 7);
+      if ((sp[0] & sp[1] & sp[2] & sp[3]) != 0xffffu) off[m] = (p0 >> 5) * pitch + (p0 & 31);
     }
     srcl[m] = sp[0] | (sp[1] << 16);
     srch[m] = sp[2] | (sp[3] << 16);
@@ -1465,8 +1468,8 @@ __global__ void __launch_bounds__(kMvThreads, 5)
       s_rt.dst[q] = ru.dst[q];
       s_rt.len[q] = ru.len[q];
       s_rt.base[q] = ru.base[q];
-      s_rt.a[q] = static_cast<int>(ru.dst[q] & 31);
-      s_rt.nu[q] = ru.len[q] > 0 ? (s_rt.a[q] + ru.len[q] + 31) >> 5 : 0;
+      s_rt.a[q] = static_cast<int>(ru.dst[q] % kMvUnit);
+      s_rt.nu[q] = ru.len[q] > 0 ? (s_rt.a[q] + ru.len[q] + kMvUnit - 1) / kMvUnit : 0;
     }
   }
   // ---- the inverse permutation; the gradient and the row id of every moved row go straight to its
