@@ -222,6 +222,12 @@ __device__ __forceinline__ void screen_feature(const uint32_t* __restrict__ hist
     for (int i = 0; i < 8; ++i)
       if (sub * 8 + i >= nb) c[i] = 0, q[i] = 0, qh[i] = 0;
   }
+  // A threshold whose own bin is empty has the same left side (count, G, H) as the threshold before
+  // it, hence the same gain, and loses the tie to that smaller bin: only thresholds at non-empty bins
+  // are candidates (runs of empty bins would otherwise all tie and survive the screen together).
+  uint32_t filled = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) filled |= (c[i] != 0 ? 1u : 0u) << i;
   // prefix sums over the bins; the feature's totals must equal the node totals
   uint32_t fc, ce;
   long long fq, fh = 0, qe, he;
@@ -276,7 +282,7 @@ __device__ __forceinline__ void screen_feature(const uint32_t* __restrict__ hist
     const int64_t qhL = kH ? he + qh[i] : 0;
     const int64_t qhR = kH ? static_cast<int64_t>(static_cast<uint64_t>(tot_h) - static_cast<uint64_t>(qhL)) : 0;
     x32[i] = 0.0f;
-    if (b > nb - 2) continue;
+    if (b > nb - 2 || !(filled >> i & 1u)) continue;
     // validity in integers (the FP64 pipe is scarce): H = count, so count >= msl, H >= mcw and H > 0
     // are count >= cnt_min; with H from its histogram, H >= mcw and H > 0 are qh >= qh_min
     if (kH ? !(static_cast<int64_t>(cL) >= msl && static_cast<int64_t>(cR) >= msl && qhL >= qh_min && qhR >= qh_min)
