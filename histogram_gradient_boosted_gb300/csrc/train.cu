@@ -157,11 +157,14 @@ __global__ void __launch_bounds__(1024)
   for (int w = threadIdx.x; w < kMaxSlots / 32; w += blockDim.x) s_cand[w] = s_keep[w] = 0;
   __syncthreads();
   if (num_leaves > 0 && !leaf_level) {
-    for (int s = threadIdx.x; s < n_slots; s += blockDim.x) {
-      if (splits[s].feature >= 0) {
-        s_gain[s] = splits[s].gain;
-        atomicOr(&s_cand[s >> 5], 1u << (s & 31));
-        atomicAdd(&s_ncand, 1);
+    for (int c0 = 0; c0 < n_slots; c0 += blockDim.x) {  // one ballot per warp of 32 slots
+      const int s = c0 + threadIdx.x;
+      const bool cand = s < n_slots && splits[s].feature >= 0;
+      if (cand) s_gain[s] = splits[s].gain;
+      const uint32_t m = __ballot_sync(0xffffffffu, cand);
+      if ((threadIdx.x & 31) == 0 && m) {
+        s_cand[s >> 5] = m;  // s is a multiple of 32 here (blockDim.x is)
+        atomicAdd(&s_ncand, __popc(m));
       }
     }
     __syncthreads();
@@ -198,16 +201,32 @@ __global__ void __launch_bounds__(1024)
       } else {
         tot = totals[s];
       }
-      atomicAdd(&s_act, static_cast<unsigned long long>(tot.cnt));
-      if (d < D && build_flag[s]) {
-        atomicAdd(&s_built, 1);
-        atomicAdd(&s_built_rows, static_cast<unsigned long long>(tot.cnt));
-        // at odd levels a node's rows still sit in its pair's (its parent's) segment
-        const int64_t scan = (d & 1) ? seg[s & ~1].count + seg[s | 1].count : seg[s].count;
-        atomicAdd(&s_scan_rows, static_cast<unsigned long long>(scan));
-      }
-      if (is_split) atomicAdd(&s_split_rows, static_cast<unsigned long long>(tot.cnt));
       if (seg[s].count != static_cast<int64_t>(tot.cnt)) raise_error(err, kErrHistTotals);
+    }
+    {  // the level's statistics: warp sums, one shared atomic per warp and counter
+      const bool built = in && d < D && build_flag[s];
+      // at odd levels a node's rows still sit in its pair's (its parent's) segment
+      const unsigned long long scan =
+          built ? static_cast<unsigned long long>((d & 1) ? seg[s & ~1].count + seg[s | 1].count : seg[s].count) : 0;
+      unsigned long long act = in ? tot.cnt : 0, brows = built ? tot.cnt : 0, srows = is_split ? tot.cnt : 0;
+      unsigned long long sc = scan;
+      int nb = built ? 1 : 0;
+      for (int o = 16; o > 0; o >>= 1) {
+        act += __shfl_xor_sync(0xffffffffu, act, o);
+        brows += __shfl_xor_sync(0xffffffffu, brows, o);
+        srows += __shfl_xor_sync(0xffffffffu, srows, o);
+        sc += __shfl_xor_sync(0xffffffffu, sc, o);
+        nb += __shfl_xor_sync(0xffffffffu, nb, o);
+      }
+      if ((threadIdx.x & 31) == 0) {
+        if (act) atomicAdd(&s_act, act);
+        if (nb) {
+          atomicAdd(&s_built, nb);
+          atomicAdd(&s_built_rows, brows);
+          atomicAdd(&s_scan_rows, sc);
+        }
+        if (srows) atomicAdd(&s_split_rows, srows);
+      }
     }
     int n_split;
     const int e_split = block_scan_excl(is_split, s_w, &n_split);
