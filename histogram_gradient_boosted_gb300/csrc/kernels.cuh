@@ -70,18 +70,28 @@ void launch_group_rows(const uint8_t* bins, int64_t ldb, int64_t N, int32_t F, c
                        int32_t* err, cudaStream_t s);
 
 // ---- split.cu -------------------------------------------------------------------------
+// A slot's totals: fixed-point G, fixed-point H (logistic; else 0) and the row count.
+struct SlotTotals {
+  int64_t q;
+  int64_t qh;  // logistic: fixed-point H (exponent fixed_exp[1]); else 0
+  uint32_t cnt;
+  uint32_t pad;
+};
 size_t find_splits_scratch_bytes(int32_t F, int32_t max_slots);
 // The per-slot counters inside that scratch: zero them before the first launch_find_splits on it
 // (every launch leaves them zero again).
 int32_t* split_counters(void* scratch, int32_t F, int32_t max_slots);
 // hist_h: null (H = count) or the H histograms with exponent fixed_exp[1].  fsched (device, may be null):
 // the features whose n_bins is above kSplitNarrowBins first, then the n_narrow others, each of which one
-// thread searches alone; null: a warp per feature, in order.
+// thread searches alone; null: a warp per feature, in order.  totals (device, may be null): each slot's
+// expected totals (the parent split's sides), which every feature's histogram must sum to; null: the
+// totals are summed from feature 0's histogram.
 constexpr int kSplitNarrowBins = 8;
 void launch_find_splits(const uint32_t* hist_cnt, const int64_t* hist_q, const int64_t* hist_h,
                         const int32_t* fixed_exp, int32_t F, const int32_t* n_bins, const gbdt_level* level,
                         int32_t max_slots, const gbdt_params& p, gbdt_split* out, void* scratch, int32_t* err,
-                        cudaStream_t s, const int32_t* fsched = nullptr, int32_t n_narrow = 0);
+                        cudaStream_t s, const int32_t* fsched = nullptr, int32_t n_narrow = 0,
+                        const SlotTotals* totals = nullptr);
 
 // ---- partition.cu ---------------------------------------------------------------------
 // Routing entry of a slot: split feature (-1: none), threshold bin, left child node id.

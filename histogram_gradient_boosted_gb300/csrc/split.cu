@@ -380,6 +380,7 @@ __device__ __forceinline__ void select_slot(const uint32_t* __restrict__ hist_cn
   const Surv* sv = surv + static_cast<int64_t>(slot) * F * kSurv;
   const int n = F * kSurv;
   float xmax = -1.0f;
+#pragma unroll 4
   for (int e = threadIdx.x; e < n; e += blockDim.x) xmax = fmaxf(xmax, __ldcg(&sv[e].x));
   for (int o = 16; o > 0; o >>= 1) xmax = fmaxf(xmax, __shfl_xor_sync(0xffffffffu, xmax, o));
   if (lane == 0) s_x[warp] = xmax;
@@ -436,7 +437,8 @@ __global__ void __launch_bounds__(kSplitThreads)
                  const int32_t* __restrict__ n_bins, const gbdt_level* __restrict__ level, int32_t max_slots,
                  double lambda, double gamma, int32_t msl, double mcw, int64_t mcw_ceil, Surv* __restrict__ surv,
                  int32_t* __restrict__ slot_done, gbdt_split* __restrict__ out, int32_t* __restrict__ err,
-                 const int32_t* __restrict__ fsched, int32_t n_wide, int32_t n_narrow) {
+                 const int32_t* __restrict__ fsched, int32_t n_wide, int32_t n_narrow,
+                 const SlotTotals* __restrict__ totals) {
   const int slot = blockIdx.x;
   const int n_slots = min(level->n_slots, max_slots);
   if (slot >= n_slots) return;  // every CTA of this slot
@@ -457,8 +459,15 @@ __global__ void __launch_bounds__(kSplitThreads)
   const int64_t base = static_cast<int64_t>(slot) * F * kBins;
   uint32_t tot_cnt;
   long long tot_q, tot_h;
-  const int nb0 = min(max(n_bins[0], 1), kBins);
-  node_totals(hist_cnt + base, hist_q + base, kH ? hist_h + base : nullptr, lane, nb0, &tot_cnt, &tot_q, &tot_h);
+  if (totals) {  // the expected totals: every feature's histogram is checked against them below
+    const SlotTotals t = totals[slot];
+    tot_cnt = t.cnt;
+    tot_q = t.q;
+    tot_h = kH ? t.qh : 0;
+  } else {
+    const int nb0 = min(max(n_bins[0], 1), kBins);
+    node_totals(hist_cnt + base, hist_q + base, kH ? hist_h + base : nullptr, lane, nb0, &tot_cnt, &tot_q, &tot_h);
+  }
   if (f >= 0 && narrow)
     screen_feature<kH, true>(hist_cnt, hist_q, hist_h, fixed_exp, F, n_bins, slot, f, lane, tot_cnt, tot_q, tot_h,
                              lambda, gamma, msl, mcw, mcw_ceil, surv, err);
@@ -494,7 +503,7 @@ int32_t* split_counters(void* scratch, int32_t F, int32_t max_slots) {
 void launch_find_splits(const uint32_t* hist_cnt, const int64_t* hist_q, const int64_t* hist_h,
                         const int32_t* fixed_exp, int32_t F, const int32_t* n_bins, const gbdt_level* level,
                         int32_t max_slots, const gbdt_params& p, gbdt_split* out, void* scratch, int32_t* err,
-                        cudaStream_t s, const int32_t* fsched, int32_t n_narrow) {
+                        cudaStream_t s, const int32_t* fsched, int32_t n_narrow, const SlotTotals* totals) {
   int32_t* done = split_counters(scratch, F, max_slots);
   Surv* surv = reinterpret_cast<Surv*>(static_cast<char*>(scratch) + kCounterBytes);
   if (!fsched) n_narrow = 0;
@@ -508,12 +517,12 @@ void launch_find_splits(const uint32_t* hist_cnt, const int64_t* hist_q, const i
     split_kernel<true><<<grid, kSplitThreads, 0, s>>>(hist_cnt, hist_q, hist_h, fixed_exp, F, n_bins, level,
                                                       max_slots, p.reg_lambda, p.gamma, p.min_samples_leaf,
                                                       p.min_child_weight, mcw_ceil, surv, done, out, err, fsched,
-                                                      n_wide, n_narrow);
+                                                      n_wide, n_narrow, totals);
   else
     split_kernel<false><<<grid, kSplitThreads, 0, s>>>(hist_cnt, hist_q, nullptr, fixed_exp, F, n_bins, level,
                                                        max_slots, p.reg_lambda, p.gamma, p.min_samples_leaf,
                                                        p.min_child_weight, mcw_ceil, surv, done, out, err, fsched,
-                                                      n_wide, n_narrow);
+                                                      n_wide, n_narrow, totals);
   count_launches();
 }
 

@@ -19,12 +19,6 @@ namespace gbdt {
 
 namespace {
 
-struct SlotTotals {
-  int64_t q;
-  int64_t qh;  // logistic: fixed-point H (exponent fixed_exp[1]); else 0
-  uint32_t cnt;
-  uint32_t pad;
-};
 
 struct LevelStats {
   int64_t n_act;         // rows in the level's nodes
@@ -646,7 +640,8 @@ extern "C" int gbdt_train(const uint8_t* bins, int64_t ldb, const int32_t* n_bin
                                n_bins);
         }
         launch_find_splits(w.hist_cnt[cur], w.hist_q[cur], w.hist_h[cur], w.fixed_exp, F, n_bins, w.level[cur],
-                           max_slots, *p, w.splits, w.split_scratch, w.err, s, w.fsched, n_narrow);
+                           max_slots, *p, w.splits, w.split_scratch, w.err, s, w.fsched, n_narrow,
+                           d > 0 ? w.totals[cur] : nullptr);
       }
       apply_level_kernel<<<1, 1024, 0, s>>>(d, D, w.level[cur], max_slots, d < D ? w.splits : nullptr, w.totals[cur],
                                             w.build[cur], w.fixed_exp, p->reg_lambda, w.seg[cur], w.trees,
