@@ -44,7 +44,7 @@ EXPORTED_SYMBOLS = [
     "gbdt_row_block_bytes", "gbdt_bins_to_row_blocks", "gbdt_compute_gradients_objective",
     "gbdt_subtract_histograms_h", "gbdt_build_histograms_segmented_h", "gbdt_find_splits_h", "gbdt_row_block_slots",
     "gbdt_workspace_status", "gbdt_partition_noalloc_status", "gbdt_subtract_histograms_workspace_size",
-    "gbdt_row_block_slots_ex",
+    "gbdt_row_block_slots_ex", "gbdt_quantize_host",
 ]
 
 
@@ -100,6 +100,7 @@ def lib():
         "gbdt_validate_params": ([P], i32),
         "gbdt_quantize_workspace_size": ([i64, i32], sz),
         "gbdt_quantize": ([P, i64, i64, i32, i32, P, i64, P, P, P, sz, P], i32),
+        "gbdt_quantize_host": ([P, i64, i64, i32, i32, P, P, i64, P, P, P, sz, P], i32),
         "gbdt_gradients_workspace_size": ([i64], sz),
         "gbdt_compute_gradients": ([P, P, i64, P, P, P, sz, P], i32),
         "gbdt_compute_gradients_objective": ([P, P, i64, i32, P, P, P, sz, P], i32),
@@ -206,10 +207,14 @@ def validate_params(**kw) -> int:
 
 
 # ---------------------------------------------------------------------------------------- entry points
-def quantize(X, max_bins: int, ldb: int | None = None):
-    """X: (F, N) float32 CUDA tensor -> bins (F, ldb) uint8, edges (F, max_bins-1) f32, n_bins (F,) i32."""
+def quantize(X, max_bins: int, ldb: int | None = None, x_device=None):
+    """X: (F, N) float32 tensor -> bins (F, ldb) uint8, edges (F, max_bins-1) f32, n_bins (F,) i32 (CUDA).
+
+    X on the GPU: gbdt_quantize.  X in host memory (pinned for overlap): gbdt_quantize_host, which copies X
+    into x_device (a (F, N) float32 CUDA tensor with X's strides; allocated if None) column batch by column
+    batch while the earlier batches are binned."""
     torch = _torch()
-    assert X.is_cuda and X.dtype == torch.float32 and X.dim() == 2 and X.stride(1) == 1
+    assert X.dtype == torch.float32 and X.dim() == 2 and X.stride(1) == 1
     F, N = X.shape
     ldb = padded_ld(N) if ldb is None else ldb
     bins = torch.empty((F, ldb), dtype=torch.uint8, device="cuda")
@@ -217,8 +222,16 @@ def quantize(X, max_bins: int, ldb: int | None = None):
     n_bins = torch.empty(F, dtype=torch.int32, device="cuda")
     ws = _workspace(lib().gbdt_quantize_workspace_size(N, F))
     ldx = X.stride(0) if F > 1 else N  # a size-1 leading dim may carry any stride
-    _check(lib().gbdt_quantize(_ptr(X), ldx, N, F, max_bins, _ptr(bins), ldb, _ptr(edges), _ptr(n_bins),
-                               _ptr(ws), ws.numel(), _stream()))
+    if X.is_cuda:
+        _check(lib().gbdt_quantize(_ptr(X), ldx, N, F, max_bins, _ptr(bins), ldb, _ptr(edges), _ptr(n_bins),
+                                   _ptr(ws), ws.numel(), _stream()))
+        return bins, edges, n_bins
+    if x_device is None:
+        x_device = torch.empty_strided((F, N), (ldx, 1), dtype=torch.float32, device="cuda")
+    assert x_device.is_cuda and x_device.dtype == torch.float32 and x_device.shape == X.shape
+    assert F == 1 or x_device.stride(0) == ldx, "x_device needs X's leading dimension"
+    _check(lib().gbdt_quantize_host(_ptr(X), ldx, N, F, max_bins, _ptr(x_device), _ptr(bins), ldb, _ptr(edges),
+                                    _ptr(n_bins), _ptr(ws), ws.numel(), _stream()))
     return bins, edges, n_bins
 
 

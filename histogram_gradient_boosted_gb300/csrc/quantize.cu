@@ -11,6 +11,7 @@
 // with 8 ballots), read the edges off the sorted keys (run starts counted in
 // chunks), then bin every value by binary search over its column's edges.
 #include <algorithm>
+#include <vector>
 
 #include "kernels.cuh"
 
@@ -373,6 +374,43 @@ QuantWs carve_quant(void* ws, size_t bytes, int64_t N, int32_t F, size_t* need) 
   return w;
 }
 
+// Sort, edges and bins of columns j0 .. j0 + nb - 1 (X on the device).
+int quantize_batch(const float* X, int64_t ldx, int64_t N, int j0, int nb, int max_bins, uint8_t* bins, int64_t ldb,
+                   float* edges, int32_t* n_bins, const QuantWs& w, cudaStream_t s) {
+  const int gx = std::min<int64_t>(ceil_div(N, 256), sm_count() * 4);
+  const int tiles = ceil_div(N, kQTile);
+  keys_kernel<<<dim3(gx, nb), 256, 0, s>>>(X, ldx, N, j0, w.a);
+  count_launches();
+  uint32_t* src = w.a;
+  uint32_t* dst = w.b;
+  for (int pass = 0; pass < 4; ++pass) {
+    radix_count_kernel<<<dim3(tiles, nb), kQThreads, 0, s>>>(src, N, tiles, 8 * pass, w.counts);
+    count_launches();
+    radix_tile_scan_kernel<<<dim3(256, nb), 256, 0, s>>>(w.counts, tiles, w.dtot);
+    count_launches();
+    radix_digit_scan_kernel<<<nb, 256, 0, s>>>(w.dtot);
+    count_launches();
+    radix_scatter_kernel<<<dim3(tiles, nb), kQThreads, 0, s>>>(src, dst, N, tiles, 8 * pass, w.counts, w.dtot);
+    count_launches();
+    std::swap(src, dst);
+  }
+  run_starts_kernel<<<dim3(kEdgeChunks, nb), 256, 0, s>>>(src, N, w.chunk_cnt, w.chunk_vals);
+  count_launches();
+  edges_kernel<<<nb, 256, 0, s>>>(src, N, j0, max_bins, w.chunk_cnt, w.chunk_vals, edges, n_bins);
+  count_launches();
+  if (aligned(X, 16) && ldx % 4 == 0)
+    bin_kernel<true><<<dim3(gx, nb), 256, 0, s>>>(X, ldx, N, j0, max_bins, edges, n_bins, bins, ldb);
+  else
+    bin_kernel<false><<<dim3(gx, nb), 256, 0, s>>>(X, ldx, N, j0, max_bins, edges, n_bins, bins, ldb);
+  count_launches();
+  GBDT_LAUNCH_CHECK();
+  return GBDT_OK;
+}
+
+// Columns per batch when the features arrive from the host: small batches, so that the first batch's
+// sort starts after a small part of the copy and every later copy runs under an earlier batch's sort.
+constexpr int kHostBatchColumns = 8;
+
 }  // namespace
 
 }  // namespace gbdt
@@ -413,34 +451,74 @@ extern "C" int gbdt_quantize(const float* X, int64_t ldx, int64_t N, int32_t F, 
     return GBDT_ERR_NONFINITE;
   }
   const int fb = batch_columns(N, F);
-  const int tiles = ceil_div(N, kQTile);
   for (int j0 = 0; j0 < F; j0 += fb) {
-    const int nb = std::min(fb, F - j0);
-    keys_kernel<<<dim3(gx, nb), 256, 0, s>>>(X, ldx, N, j0, w.a);
-    count_launches();
-    uint32_t* src = w.a;
-    uint32_t* dst = w.b;
-    for (int pass = 0; pass < 4; ++pass) {
-      radix_count_kernel<<<dim3(tiles, nb), kQThreads, 0, s>>>(src, N, tiles, 8 * pass, w.counts);
-      count_launches();
-      radix_tile_scan_kernel<<<dim3(256, nb), 256, 0, s>>>(w.counts, tiles, w.dtot);
-      count_launches();
-      radix_digit_scan_kernel<<<nb, 256, 0, s>>>(w.dtot);
-      count_launches();
-      radix_scatter_kernel<<<dim3(tiles, nb), kQThreads, 0, s>>>(src, dst, N, tiles, 8 * pass, w.counts, w.dtot);
-      count_launches();
-      std::swap(src, dst);
+    const int rc = quantize_batch(X, ldx, N, j0, std::min(fb, F - j0), max_bins, bins, ldb, edges, n_bins, w, s);
+    if (rc != GBDT_OK) return rc;
+  }
+  return GBDT_OK;
+}
+
+extern "C" int gbdt_quantize_host(const float* X_host, int64_t ldx, int64_t N, int32_t F, int32_t max_bins,
+                                  float* X_dev, uint8_t* bins, int64_t ldb, float* edges, int32_t* n_bins, void* ws,
+                                  size_t ws_bytes, void* stream) {
+  clear_error();
+  GBDT_CHECK_ARG(X_host && X_dev && bins && edges && n_bins, "gbdt_quantize_host: null pointer");
+  GBDT_CHECK_ARG(N >= 1 && N < (int64_t(1) << 31) && F >= 1 && F <= 65535, "gbdt_quantize_host: sizes out of range");
+  GBDT_CHECK_ARG(max_bins >= 2 && max_bins <= GBDT_MAX_BINS, "gbdt_quantize_host: max_bins must be in 2..256");
+  GBDT_CHECK_ARG(ldx >= N && ldb >= N && ldb % 16 == 0 && aligned(bins, 16),
+                 "gbdt_quantize_host: need ldx >= N, ldb >= N, ldb %% 16 == 0 and 16-byte aligned bins");
+  size_t need = 0;
+  QuantWs w = carve_quant(ws, ws_bytes, N, F, &need);
+  if (!ws || ws_bytes < need || !aligned(ws, kWsAlign)) {
+    set_error("gbdt_quantize_host: workspace needs %zu bytes", need);
+    return ws ? GBDT_ERR_WORKSPACE : GBDT_ERR_INVALID_ARG;
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int fb = std::min(batch_columns(N, F), kHostBatchColumns);
+  const int n_batches = ceil_div(F, fb);
+  // the copies run on a stream of their own, after the work already queued on `stream` (which may still
+  // read X_dev); each batch's sort waits for its own copy only
+  struct Res {
+    cudaStream_t cs = nullptr;
+    std::vector<cudaEvent_t> ev;
+    ~Res() {  // on an early return the copies from X_host still in flight finish first
+      if (cs) cudaStreamSynchronize(cs);
+      for (cudaEvent_t e : ev)
+        if (e) cudaEventDestroy(e);
+      if (cs) cudaStreamDestroy(cs);
     }
-    run_starts_kernel<<<dim3(kEdgeChunks, nb), 256, 0, s>>>(src, N, w.chunk_cnt, w.chunk_vals);
+  } r;
+  r.ev.assign(n_batches + 1, nullptr);
+  for (cudaEvent_t& e : r.ev) GBDT_CUDA(cudaEventCreateWithFlags(&e, cudaEventDisableTiming));
+  GBDT_CUDA(cudaStreamCreateWithFlags(&r.cs, cudaStreamNonBlocking));
+  GBDT_CUDA(cudaEventRecord(r.ev[n_batches], s));
+  GBDT_CUDA(cudaStreamWaitEvent(r.cs, r.ev[n_batches], 0));
+  for (int b = 0; b < n_batches; ++b) {
+    const int j0 = b * fb, nb = std::min(fb, F - j0);
+    const size_t count = static_cast<size_t>(nb - 1) * static_cast<size_t>(ldx) + static_cast<size_t>(N);
+    GBDT_CUDA(cudaMemcpyAsync(X_dev + static_cast<int64_t>(j0) * ldx, X_host + static_cast<int64_t>(j0) * ldx,
+                              count * sizeof(float), cudaMemcpyHostToDevice, r.cs));
+    GBDT_CUDA(cudaEventRecord(r.ev[b], r.cs));
+  }
+  GBDT_CUDA(cudaMemsetAsync(w.flag, 0, sizeof(int32_t), s));
+  const int gx = std::min<int64_t>(ceil_div(N, 256), sm_count() * 4);
+  for (int b = 0; b < n_batches; ++b) {
+    const int j0 = b * fb, nb = std::min(fb, F - j0);
+    GBDT_CUDA(cudaStreamWaitEvent(s, r.ev[b], 0));
+    // finiteness of the batch, read once more at the end: the outputs of a call that fails it are
+    // not to be used
+    finite_kernel<<<dim3(gx, std::min(nb, 64)), 256, 0, s>>>(X_dev + static_cast<int64_t>(j0) * ldx, ldx, N, nb,
+                                                             w.flag);
     count_launches();
-    edges_kernel<<<nb, 256, 0, s>>>(src, N, j0, max_bins, w.chunk_cnt, w.chunk_vals, edges, n_bins);
-    count_launches();
-    if (aligned(X, 16) && ldx % 4 == 0)
-      bin_kernel<true><<<dim3(gx, nb), 256, 0, s>>>(X, ldx, N, j0, max_bins, edges, n_bins, bins, ldb);
-    else
-      bin_kernel<false><<<dim3(gx, nb), 256, 0, s>>>(X, ldx, N, j0, max_bins, edges, n_bins, bins, ldb);
-    count_launches();
-    GBDT_LAUNCH_CHECK();
+    const int rc = quantize_batch(X_dev, ldx, N, j0, nb, max_bins, bins, ldb, edges, n_bins, w, s);
+    if (rc != GBDT_OK) return rc;
+  }
+  int32_t bad = 0;
+  GBDT_CUDA(cudaMemcpyAsync(&bad, w.flag, sizeof(int32_t), cudaMemcpyDeviceToHost, s));
+  GBDT_CUDA(cudaStreamSynchronize(s));
+  if (bad) {
+    set_error("gbdt_quantize_host: features contain NaN or Inf");
+    return GBDT_ERR_NONFINITE;
   }
   return GBDT_OK;
 }

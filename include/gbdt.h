@@ -237,6 +237,21 @@ size_t gbdt_quantize_workspace_size(int64_t N, int32_t F);
 int gbdt_quantize(const float* X, int64_t ldx, int64_t N, int32_t F, int32_t max_bins, uint8_t* bins,
                   int64_t ldb, float* edges, int32_t* n_bins, void* ws, size_t ws_bytes, void* stream);
 
+/* gbdt_quantize_host: gbdt_quantize of features that are in HOST memory.
+ *   X_host [F][ldx] fp32 (host; page-locked memory lets the copies overlap)
+ *   X_dev  [F][ldx] fp32 (device, caller-owned): receives the copy of X_host
+ * The same rule and outputs as gbdt_quantize (workspace: gbdt_quantize_workspace_size).
+ * The columns are copied in batches on a stream the call creates and
+ * destroys, each after the work already queued on `stream`; each batch is
+ * binned as soon as its copy has landed, so the copy of later columns runs
+ * under the sort of earlier ones.  NaN/Inf in X: GBDT_ERR_NONFINITE, found
+ * after the outputs were written (do not use them).  Synchronises the stream
+ * once, at the end; X_host may be released when the call returns.
+ * ------------------------------------------------------------------------- */
+int gbdt_quantize_host(const float* X_host, int64_t ldx, int64_t N, int32_t F, int32_t max_bins, float* X_dev,
+                       uint8_t* bins, int64_t ldb, float* edges, int32_t* n_bins, void* ws, size_t ws_bytes,
+                       void* stream);
+
 /* ---------------------------------------------------------------------------
  * gbdt_compute_gradients: squared error, "Module Design: Training Core" s.2:
  * g_i = pred_i - label_i (FP64), h_i = 1 (implicit).  Also computes the

@@ -64,6 +64,35 @@ def test_quantize_rejects_nonfinite():
     assert e.value.code == g.ERR_NONFINITE
 
 
+@pytest.mark.parametrize("pinned", [True, False])
+@pytest.mark.parametrize("name,n", [("large", 25_003), ("covtype", 30_007)])
+def test_quantize_from_host_equals_device_path(name, n, pinned):
+    """gbdt_quantize_host (column batches copied on a stream of their own while earlier batches are binned)
+    gives the oracle's bins, edges and n_bins, and leaves the device copy equal to the host features; also
+    with a leading dimension above N (the copy of the last column stops at N)."""
+    X, _ = synth.make(name, n=n)
+    B = synth.CONFIGS[name]["max_bins"]
+    ob, oe, on = oracle.quantize(X, B, n_threads=8)
+    F, N = X.shape
+    for ld in (N, N + 5):
+        Xh = torch.zeros((F, ld), dtype=torch.float32, pin_memory=pinned)[:, :N]
+        Xh.copy_(torch.from_numpy(X))
+        Xd = torch.full((F, ld), -1.0, dtype=torch.float32, device="cuda")[:, :N]
+        bins, edges, n_bins = g.quantize(Xh, B, x_device=Xd)
+        assert np.array_equal(n_bins.cpu().numpy(), on)
+        assert np.array_equal(edges.cpu().numpy(), oe)
+        assert np.array_equal(bins[:, :N].cpu().numpy(), ob)
+        assert torch.equal(Xd.cpu(), Xh)
+
+
+def test_quantize_from_host_rejects_nonfinite():
+    X = torch.zeros((20, 1000), dtype=torch.float32, pin_memory=True)
+    X[17, 999] = float("inf")  # in the last batch of columns
+    with pytest.raises(g.GbdtError) as e:
+        g.quantize(X, 32)
+    assert e.value.code == g.ERR_NONFINITE
+
+
 # ----------------------------------------------------------------------------- gradients
 def test_gradients_and_scale():
     rng = np.random.default_rng(1)

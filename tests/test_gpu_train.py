@@ -65,6 +65,30 @@ def test_repeated_training_is_bit_identical():
     assert torch.equal(a["pred"], b["pred"])
 
 
+@pytest.mark.parametrize("name,n,trees,extra", [("covtype", 20_000, 6, dict(num_leaves=200)),
+                                                ("large", 30_000, 5, {}), ("mid", 10_000, 4, dict(objective=1))])
+def test_graph_replay_equals_tree_by_tree(name, n, trees, extra):
+    """Without diagnostics trees 1 .. T-2 replay one captured graph; with diagnostics every tree is launched
+    on its own.  Both must give the same model and predictions bit for bit (and the graph path must count
+    the replayed kernels)."""
+    bins, n_bins, yd, *_ = _prepare(name, n)
+    y = yd
+    if extra.get("objective") == 1:
+        y = torch.from_numpy(synth.binary_label(yd.cpu().numpy())).cuda()
+    params = dict(synth.CONFIGS[name], n_trees=trees, **extra)
+    l0 = g.kernel_launch_count()
+    a = g.train(bins, n_bins, y, **params)
+    torch.cuda.synchronize()
+    l1 = g.kernel_launch_count()
+    b = g.train(bins, n_bins, y, diagnostics=True, **params)
+    torch.cuda.synchronize()
+    l2 = g.kernel_launch_count()
+    assert a["nodes"].tobytes() == b["nodes"].tobytes()
+    assert list(a["nodes_per_tree"]) == list(b["nodes_per_tree"])
+    assert torch.equal(a["pred"], b["pred"]) and a["init_pred"] == b["init_pred"]
+    assert l1 - l0 == l2 - l1  # the replayed graph's kernels are counted as launches
+
+
 def _raw_train(bins, n_bins, label, params, nodes, npt):
     L = g.lib()
     p = g.make_params(**params)
