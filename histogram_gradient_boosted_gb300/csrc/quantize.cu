@@ -4,12 +4,14 @@
 // without its rule; the rule used here is stated in gbdt.h.  It is made of
 // order statistics and comparisons only, so it is reproducible bit for bit.
 //
-// Per batch of columns: map each value to an order-preserving uint32 key
-// (-0.0 read as +0.0), sort every column with a stable 4-pass LSD radix sort
-// (8-bit digits; tile counts, a scan over tiles per (column, digit) and over
-// digits per column, and a stable scatter that ranks equal digits inside a warp
-// with 8 ballots), read the edges off the sorted keys (run starts counted in
-// chunks), then bin every value by binary search over its column's edges.
+// First one pass over every value: its finiteness and, per column, whether it has at most max_bins
+// distinct values (a hash set of the values in each CTA's shared memory, merged per column).  A column
+// with at most max_bins distinct values takes its edges from that set and is never sorted.  The other
+// columns, per batch: map each value to an order-preserving uint32 key (-0.0 read as +0.0), sort the
+// column with a stable 4-pass LSD radix sort (8-bit digits; tile counts, a scan over tiles per (column,
+// digit) and over digits per column, and a stable scatter that ranks equal digits inside a warp with 8
+// ballots), and read the order statistics off the sorted keys.  Then every value is binned by binary
+// search over its column's edges.
 #include <algorithm>
 #include <vector>
 
@@ -40,8 +42,170 @@ __global__ void finite_kernel(const float* __restrict__ X, int64_t ldx, int64_t 
   if (__syncthreads_or(bad) && threadIdx.x == 0) atomicOr(flag, 1);
 }
 
-__global__ void keys_kernel(const float* __restrict__ X, int64_t ldx, int64_t N, int j0, uint32_t* __restrict__ keys) {
+// ---- distinct values (at most B per column are tracked)
+constexpr int kSetSlots = 512;        // open-addressing slots of a CTA's set (> 2 * 256: probes stay short)
+constexpr int kDistinctCtas = 64;     // CTAs per column of the distinct pass
+constexpr int kListCap = kDistinctCtas * 256;  // per column: every CTA's set (each at most 256 values)
+constexpr uint32_t kEmptyKey = 0xffffffffu;     // no finite value maps to it
+
+__device__ __forceinline__ uint32_t set_hash(uint32_t k) { return (k * 2654435761u) >> (32 - 9); }
+
+// Grid (kDistinctCtas, columns of the batch).  Each CTA: its rows of column j = j0 + y, their finiteness
+// (flag), and the distinct keys among them while there are at most B; more than B in one CTA marks the
+// column for sorting (more[j] = 1).  Otherwise the CTA's keys are appended to the column's list
+// (list[y][0 .. cnt[j]): the batch's lists, kListCap entries each, room for every CTA's set).
+__device__ __forceinline__ bool nonfinite_bits(float v) {  // exponent all ones: Inf or NaN
+  return (__float_as_uint(v) & 0x7f800000u) == 0x7f800000u;
+}
+
+// Add key k to the CTA's set (open addressing over kSetSlots slots).  More than B keys, or no free slot
+// within kMaxProbes (a set of at most B <= 256 keys in 512 slots practically never needs that many),
+// set *over: the column is then sorted, which is always correct.
+constexpr int kMaxProbes = 32;
+__device__ __forceinline__ void set_insert(uint32_t* s_set, int* s_n, int* s_over, uint32_t k, int B) {
+  if (*reinterpret_cast<volatile int*>(s_over)) return;
+  uint32_t h = set_hash(k);
+  for (int probe = 0; probe < kMaxProbes; ++probe, h = (h + 1) & (kSetSlots - 1)) {
+    const uint32_t cur = s_set[h];
+    if (cur == k) return;
+    if (cur == kEmptyKey) {
+      const uint32_t old = atomicCAS(&s_set[h], kEmptyKey, k);
+      if (old == kEmptyKey) {
+        if (atomicAdd(s_n, 1) >= B) *s_over = 1;
+        return;
+      }
+      if (old == k) return;
+    }
+  }
+  *s_over = 1;
+}
+
+// kVec: X's columns 16-byte aligned (four values per load).
+template <bool kVec>
+__global__ void __launch_bounds__(256)
+    distinct_kernel(const float* __restrict__ X, int64_t ldx, int64_t N, int j0, int B, int32_t* flag,
+                    uint32_t* __restrict__ list, uint32_t* __restrict__ cnt, int32_t* __restrict__ more) {
+  __shared__ uint32_t s_set[kSetSlots];
+  __shared__ int s_n, s_over;
+  __shared__ uint32_t s_pos;
+  const int j = j0 + blockIdx.y;
+  for (int i = threadIdx.x; i < kSetSlots; i += blockDim.x) s_set[i] = kEmptyKey;
+  if (threadIdx.x == 0) s_n = 0, s_over = 0;
+  __syncthreads();
+  const float* x = X + static_cast<int64_t>(j) * ldx;
+  // this CTA's rows [r0, r1), a multiple of four of them per CTA
+  const int64_t per = (N + 4 * gridDim.x - 1) / (4 * gridDim.x) * 4;
+  const int64_t r0 = per * blockIdx.x, r1 = min(N, r0 + per);
+  volatile int* over = &s_over;
+  bool bad = false;
+  int64_t i = r0;
+  if (kVec) {
+    const int64_t n4 = r1 > r0 ? (r1 - r0) / 4 : 0;
+    const float4* x4 = reinterpret_cast<const float4*>(x + r0);
+    int64_t q = threadIdx.x;
+    for (; q < n4 && !*over; q += blockDim.x) {  // values still counted
+      const float4 v = x4[q];
+      bad |= nonfinite_bits(v.x) | nonfinite_bits(v.y) | nonfinite_bits(v.z) | nonfinite_bits(v.w);
+      set_insert(s_set, &s_n, &s_over, f2key(v.x), B);
+      set_insert(s_set, &s_n, &s_over, f2key(v.y), B);
+      set_insert(s_set, &s_n, &s_over, f2key(v.z), B);
+      set_insert(s_set, &s_n, &s_over, f2key(v.w), B);
+    }
+    for (; q < n4; q += blockDim.x) {  // more than B values: only the finiteness is left to check
+      const float4 v = x4[q];
+      bad |= nonfinite_bits(v.x) | nonfinite_bits(v.y) | nonfinite_bits(v.z) | nonfinite_bits(v.w);
+    }
+    i = r0 + 4 * n4;
+  }
+  for (i += threadIdx.x; i < r1; i += blockDim.x) {
+    const float v = x[i];
+    bad |= nonfinite_bits(v);
+    if (!*over) set_insert(s_set, &s_n, &s_over, f2key(v), B);
+  }
+  if (__syncthreads_or(bad) && threadIdx.x == 0) atomicOr(flag, 1);
+  if (s_over) {
+    if (threadIdx.x == 0) more[j] = 1;
+    return;
+  }
+  if (threadIdx.x == 0) {
+    const uint32_t pos = atomicAdd(&cnt[j], static_cast<uint32_t>(s_n));
+    s_pos = pos;
+    if (pos + s_n > static_cast<uint32_t>(kListCap)) more[j] = 1;
+    s_n = 0;  // reused as the write cursor
+  }
+  __syncthreads();
+  const uint32_t pos = s_pos;
+  uint32_t* out = list + static_cast<int64_t>(blockIdx.y) * kListCap;
+  for (int k = threadIdx.x; k < kSetSlots; k += blockDim.x) {
+    const uint32_t key = s_set[k];
+    if (key == kEmptyKey) continue;
+    const uint32_t at = pos + static_cast<uint32_t>(atomicAdd(&s_n, 1));
+    if (at < static_cast<uint32_t>(kListCap)) out[at] = key;
+  }
+}
+
+// One CTA per column j = j0 + x of the batch: a column not marked for sorting has its list's distinct keys
+// counted; U <= B of them: its edges are the U-1 smallest (the largest is no edge), n_bins = U;
+// more than B (the CTAs' sets together exceed B): marked for sorting.
+__global__ void __launch_bounds__(256)
+    distinct_edges_kernel(const uint32_t* __restrict__ list, const uint32_t* __restrict__ cnt, int32_t* __restrict__ more,
+                          int j0, int B, float* __restrict__ edges, int32_t* __restrict__ n_bins) {
+  __shared__ uint32_t s_set[kSetSlots];
+  __shared__ uint32_t s_vals[256];
+  __shared__ int s_n, s_over;
+  const int j = j0 + blockIdx.x;
+  if (more[j]) return;  // CTA-uniform
+  for (int i = threadIdx.x; i < kSetSlots; i += blockDim.x) s_set[i] = kEmptyKey;
+  if (threadIdx.x == 0) s_n = 0, s_over = 0;
+  __syncthreads();
+  const uint32_t n = min(cnt[j], static_cast<uint32_t>(kListCap));
+  const uint32_t* in = list + static_cast<int64_t>(blockIdx.x) * kListCap;
+  for (uint32_t i = threadIdx.x; i < n; i += blockDim.x) {
+    if (*reinterpret_cast<volatile int*>(&s_over)) break;
+    const uint32_t k = in[i];
+    uint32_t h = set_hash(k);
+    bool placed = false;  // found or inserted; a key that finds no slot within kMaxProbes sends the column to the sort
+    for (int probe = 0; probe < kMaxProbes && !placed; ++probe, h = (h + 1) & (kSetSlots - 1)) {
+      const uint32_t cur = s_set[h];
+      if (cur == k) {
+        placed = true;
+      } else if (cur == kEmptyKey) {
+        const uint32_t old = atomicCAS(&s_set[h], kEmptyKey, k);
+        if (old == kEmptyKey) {
+          const int at = atomicAdd(&s_n, 1);
+          if (at < B) s_vals[at] = k;
+          else s_over = 1;
+          placed = true;
+        } else if (old == k) {
+          placed = true;
+        }
+      }
+    }
+    if (!placed) s_over = 1;
+  }
+  __syncthreads();
+  if (s_over) {
+    if (threadIdx.x == 0) more[j] = 1;
+    return;
+  }
+  const int U = s_n;
+  float* e = edges + static_cast<int64_t>(j) * (B - 1);
+  for (int i = threadIdx.x; i < U; i += blockDim.x) {  // rank among the distinct values
+    const uint32_t x = s_vals[i];
+    int r = 0;
+    for (int m = 0; m < U; ++m) r += s_vals[m] < x ? 1 : 0;
+    if (r + 1 < U) e[r] = key2f(x);
+  }
+  for (int k = U - 1 + threadIdx.x; k < B - 1; k += blockDim.x) e[k] = INFINITY;
+  if (threadIdx.x == 0) n_bins[j] = U;
+}
+
+// The kernels of the sort take the columns j0 .. j0 + nb - 1 of a batch and skip those that more[]
+// (the batch's part: more[j] for column j0 + j) does not mark.
+__global__ void keys_kernel(const float* __restrict__ X, int64_t ldx, int64_t N, int j0, uint32_t* __restrict__ keys,
+                            const int32_t* __restrict__ more) {
   const int j = blockIdx.y;
+  if (!more[j]) return;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < N; i += (int64_t)gridDim.x * blockDim.x)
     keys[j * N + i] = f2key(X[(j0 + j) * ldx + i]);
 }
@@ -49,9 +213,10 @@ __global__ void keys_kernel(const float* __restrict__ X, int64_t ldx, int64_t N,
 // counts[j][digit][tile]
 __global__ void __launch_bounds__(kQThreads)
     radix_count_kernel(const uint32_t* __restrict__ keys, int64_t N, int tiles, int shift,
-                       uint32_t* __restrict__ counts) {
+                       uint32_t* __restrict__ counts, const int32_t* __restrict__ more) {
   __shared__ uint32_t h[256];
   const int j = blockIdx.y, t = blockIdx.x;
+  if (!more[j]) return;
   h[threadIdx.x] = 0;
   __syncthreads();
   const uint32_t* k = keys + j * N;
@@ -67,10 +232,12 @@ __global__ void __launch_bounds__(kQThreads)
 // In-place exclusive scan over the tiles of one (column, digit) row of the
 // counts; the row's total goes to dtot[j][digit].
 __global__ void __launch_bounds__(256)
-    radix_tile_scan_kernel(uint32_t* __restrict__ counts, int tiles, uint32_t* __restrict__ dtot) {
+    radix_tile_scan_kernel(uint32_t* __restrict__ counts, int tiles, uint32_t* __restrict__ dtot,
+                           const int32_t* __restrict__ more) {
   __shared__ uint32_t s_warp[33];
   __shared__ uint32_t s_carry;
   const int d = blockIdx.x, j = blockIdx.y;
+  if (!more[j]) return;
   uint32_t* c = counts + (static_cast<int64_t>(j) * 256 + d) * tiles;
   if (threadIdx.x == 0) s_carry = 0;
   __syncthreads();
@@ -106,8 +273,10 @@ __global__ void __launch_bounds__(256)
 }
 
 // Exclusive scan of one column's 256 digit totals (in place): the digit's first position.
-__global__ void __launch_bounds__(256) radix_digit_scan_kernel(uint32_t* __restrict__ dtot) {
+__global__ void __launch_bounds__(256) radix_digit_scan_kernel(uint32_t* __restrict__ dtot,
+                                                               const int32_t* __restrict__ more) {
   __shared__ uint32_t s[256];
+  if (!more[blockIdx.x]) return;
   uint32_t* t = dtot + blockIdx.x * 256;
   const uint32_t v = t[threadIdx.x];
   s[threadIdx.x] = v;
@@ -127,7 +296,8 @@ __global__ void __launch_bounds__(256) radix_digit_scan_kernel(uint32_t* __restr
 // addresses (a warp's stores cover one or two runs instead of up to 32).
 __global__ void __launch_bounds__(kQThreads)
     radix_scatter_kernel(const uint32_t* __restrict__ in, uint32_t* __restrict__ out, int64_t N, int tiles, int shift,
-                         const uint32_t* __restrict__ offsets, const uint32_t* __restrict__ dbase) {
+                         const uint32_t* __restrict__ offsets, const uint32_t* __restrict__ dbase,
+                         const int32_t* __restrict__ more) {
   constexpr int kWarps = kQThreads / 32;
   static_assert(kQThreads == 256, "one thread per digit");
   __shared__ uint32_t s_keys[kQTile];     // the tile's keys, ranked
@@ -137,6 +307,7 @@ __global__ void __launch_bounds__(kQThreads)
   __shared__ uint32_t s_wc[kWarps][256];  // per-warp count, then per-warp start, of each digit
   __shared__ uint32_t s_warp[kWarps];
   const int j = blockIdx.y, t = blockIdx.x;
+  if (!more[j]) return;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const uint32_t* k = in + j * N;
   uint32_t* o = out + j * N;
@@ -210,75 +381,17 @@ __global__ void __launch_bounds__(kQThreads)
   }
 }
 
-// Distinct values of a sorted column, in chunks: each CTA counts the run
-// starts of its chunk (position i starts a run if i == 0 or v[i] != v[i-1])
-// with coalesced reads, and keeps up to kRunKeep of their values (unordered).
-constexpr int kEdgeChunks = 64;
-constexpr int kRunKeep = 257;
-
+// One CTA per sorted column (more than B distinct values): the order statistics
+// v[ceil(kN/B) - 1], k = 1..B-1, strictly increasing, without one equal to the largest value.
 __global__ void __launch_bounds__(256)
-    run_starts_kernel(const uint32_t* __restrict__ sorted, int64_t N, uint32_t* __restrict__ chunk_cnt,
-                      uint32_t* __restrict__ chunk_vals /*[col][chunk][kRunKeep]*/) {
-  const int j = blockIdx.y, c = blockIdx.x;
-  const uint32_t* v = sorted + j * N;
-  const int64_t per = (N + kEdgeChunks - 1) / kEdgeChunks;
-  const int64_t a = c * per, bnd = min(N, a + per);
-  __shared__ uint32_t s_cnt;
-  if (threadIdx.x == 0) s_cnt = 0;
-  __syncthreads();
-  uint32_t* keep = chunk_vals + (static_cast<int64_t>(j) * kEdgeChunks + c) * kRunKeep;
-  for (int64_t i = a + threadIdx.x; i < bnd; i += blockDim.x) {
-    const uint32_t x = v[i];
-    if (i == 0 || x != v[i - 1]) {
-      const uint32_t slot = atomicAdd(&s_cnt, 1u);
-      if (slot < kRunKeep) keep[slot] = x;
-    }
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) chunk_cnt[j * kEdgeChunks + c] = s_cnt;
-}
-
-// One CTA per column: U = number of distinct values; U <= B: the U-1 smallest
-// distinct values (all of them were kept: every chunk has at most U run
-// starts); otherwise the order statistics v[ceil(kN/B) - 1], strictly
-// increasing, without one equal to the largest value.
-__global__ void __launch_bounds__(256)
-    edges_kernel(const uint32_t* __restrict__ sorted, int64_t N, int j0, int B, const uint32_t* __restrict__ chunk_cnt,
-                 const uint32_t* __restrict__ chunk_vals, float* __restrict__ edges, int32_t* __restrict__ n_bins) {
+    order_edges_kernel(const uint32_t* __restrict__ sorted, int64_t N, int j0, int B, const int32_t* __restrict__ more,
+                       float* __restrict__ edges, int32_t* __restrict__ n_bins) {
   const int j = blockIdx.x;
+  if (!more[j]) return;
   const uint32_t* v = sorted + j * N;
-  __shared__ uint32_t s_cnt[kEdgeChunks + 1];
-  __shared__ uint32_t s_vals[256];
   __shared__ float s_e[256];
   __shared__ int s_ne;
-  if (threadIdx.x == 0) {
-    uint32_t acc = 0;
-    for (int c = 0; c < kEdgeChunks; ++c) {
-      s_cnt[c] = acc;
-      acc += chunk_cnt[j * kEdgeChunks + c];
-    }
-    s_cnt[kEdgeChunks] = acc;
-  }
-  __syncthreads();
-  const uint32_t U = s_cnt[kEdgeChunks];
   float* e = edges + static_cast<int64_t>(j0 + j) * (B - 1);
-  if (U <= static_cast<uint32_t>(B)) {
-    for (int c = 0; c < kEdgeChunks; ++c) {  // gather the distinct values (at most B <= 256)
-      const uint32_t n = s_cnt[c + 1] - s_cnt[c];
-      for (uint32_t i = threadIdx.x; i < n; i += blockDim.x)
-        s_vals[s_cnt[c] + i] = chunk_vals[(static_cast<int64_t>(j) * kEdgeChunks + c) * kRunKeep + i];
-    }
-    __syncthreads();
-    for (uint32_t i = threadIdx.x; i < U; i += blockDim.x) {  // rank among distinct values
-      const uint32_t x = s_vals[i];
-      uint32_t r = 0;
-      for (uint32_t m = 0; m < U; ++m) r += s_vals[m] < x ? 1u : 0u;
-      if (r + 1 < U) e[r] = key2f(x);
-    }
-    for (int k = static_cast<int>(U) - 1 + threadIdx.x; k < B - 1; k += blockDim.x) e[k] = INFINITY;
-    if (threadIdx.x == 0) n_bins[j0 + j] = static_cast<int32_t>(U);
-    return;
-  }
   for (int k = 1 + threadIdx.x; k <= B - 1; k += blockDim.x) {
     const int64_t pk = (static_cast<int64_t>(k) * N + B - 1) / B - 1;
     s_e[k - 1] = key2f(v[pk]);
@@ -345,7 +458,8 @@ __global__ void bin_kernel(const float* __restrict__ X, int64_t ldx, int64_t N, 
 }
 
 int batch_columns(int64_t N, int32_t F) {
-  const size_t per_col = static_cast<size_t>(N) * 8 + static_cast<size_t>(256) * ceil_div(N, kQTile) * 4;
+  const size_t per_col = static_cast<size_t>(N) * 8 + static_cast<size_t>(256) * ceil_div(N, kQTile) * 4 +
+                         sizeof(uint32_t) * kListCap;
   int fb = static_cast<int>(kQBatchBudget / (per_col ? per_col : 1));
   return std::max(1, std::min<int>(fb, F));
 }
@@ -355,8 +469,9 @@ struct QuantWs {
   uint32_t* b;
   uint32_t* counts;
   uint32_t* dtot;
-  uint32_t* chunk_cnt;
-  uint32_t* chunk_vals;
+  uint32_t* list;   // [batch columns][kListCap] distinct keys per column of a batch
+  uint32_t* cnt;    // [F] entries of each list
+  int32_t* more;    // [F] 1: more than max_bins distinct values (the column is sorted)
   int32_t* flag;
 };
 QuantWs carve_quant(void* ws, size_t bytes, int64_t N, int32_t F, size_t* need) {
@@ -367,36 +482,49 @@ QuantWs carve_quant(void* ws, size_t bytes, int64_t N, int32_t F, size_t* need) 
   w.b = c.take<uint32_t>(static_cast<size_t>(fb) * N);
   w.counts = c.take<uint32_t>(static_cast<size_t>(fb) * 256 * ceil_div(N, kQTile));
   w.dtot = c.take<uint32_t>(static_cast<size_t>(fb) * 256);
-  w.chunk_cnt = c.take<uint32_t>(static_cast<size_t>(fb) * kEdgeChunks);
-  w.chunk_vals = c.take<uint32_t>(static_cast<size_t>(fb) * kEdgeChunks * kRunKeep);
+  w.list = c.take<uint32_t>(static_cast<size_t>(fb) * kListCap);
+  w.cnt = c.take<uint32_t>(F);
+  w.more = c.take<int32_t>(F);
   w.flag = c.take<int32_t>(1);
   *need = c.used;
   return w;
 }
 
-// Sort, edges and bins of columns j0 .. j0 + nb - 1 (X on the device).
+// Finiteness and distinct values of columns j0 .. j0 + nb - 1; the edges of those with at most B distinct
+// values (the others are marked in w.more for the sort).  w.cnt and w.more of the columns must be zero.
+void distinct_batch(const float* X, int64_t ldx, int64_t N, int j0, int nb, int B, float* edges, int32_t* n_bins,
+                    const QuantWs& w, cudaStream_t s) {
+  if (aligned(X, 16) && ldx % 4 == 0)
+    distinct_kernel<true><<<dim3(kDistinctCtas, nb), 256, 0, s>>>(X, ldx, N, j0, B, w.flag, w.list, w.cnt, w.more);
+  else
+    distinct_kernel<false><<<dim3(kDistinctCtas, nb), 256, 0, s>>>(X, ldx, N, j0, B, w.flag, w.list, w.cnt, w.more);
+  count_launches();
+  distinct_edges_kernel<<<nb, 256, 0, s>>>(w.list, w.cnt, w.more, j0, B, edges, n_bins);
+  count_launches();
+}
+
+// Sort and order statistics of the marked columns among j0 .. j0 + nb - 1, then the bins of all of them.
 int quantize_batch(const float* X, int64_t ldx, int64_t N, int j0, int nb, int max_bins, uint8_t* bins, int64_t ldb,
                    float* edges, int32_t* n_bins, const QuantWs& w, cudaStream_t s) {
   const int gx = std::min<int64_t>(ceil_div(N, 256), sm_count() * 4);
   const int tiles = ceil_div(N, kQTile);
-  keys_kernel<<<dim3(gx, nb), 256, 0, s>>>(X, ldx, N, j0, w.a);
+  const int32_t* more = w.more + j0;
+  keys_kernel<<<dim3(gx, nb), 256, 0, s>>>(X, ldx, N, j0, w.a, more);
   count_launches();
   uint32_t* src = w.a;
   uint32_t* dst = w.b;
   for (int pass = 0; pass < 4; ++pass) {
-    radix_count_kernel<<<dim3(tiles, nb), kQThreads, 0, s>>>(src, N, tiles, 8 * pass, w.counts);
+    radix_count_kernel<<<dim3(tiles, nb), kQThreads, 0, s>>>(src, N, tiles, 8 * pass, w.counts, more);
     count_launches();
-    radix_tile_scan_kernel<<<dim3(256, nb), 256, 0, s>>>(w.counts, tiles, w.dtot);
+    radix_tile_scan_kernel<<<dim3(256, nb), 256, 0, s>>>(w.counts, tiles, w.dtot, more);
     count_launches();
-    radix_digit_scan_kernel<<<nb, 256, 0, s>>>(w.dtot);
+    radix_digit_scan_kernel<<<nb, 256, 0, s>>>(w.dtot, more);
     count_launches();
-    radix_scatter_kernel<<<dim3(tiles, nb), kQThreads, 0, s>>>(src, dst, N, tiles, 8 * pass, w.counts, w.dtot);
+    radix_scatter_kernel<<<dim3(tiles, nb), kQThreads, 0, s>>>(src, dst, N, tiles, 8 * pass, w.counts, w.dtot, more);
     count_launches();
     std::swap(src, dst);
   }
-  run_starts_kernel<<<dim3(kEdgeChunks, nb), 256, 0, s>>>(src, N, w.chunk_cnt, w.chunk_vals);
-  count_launches();
-  edges_kernel<<<nb, 256, 0, s>>>(src, N, j0, max_bins, w.chunk_cnt, w.chunk_vals, edges, n_bins);
+  order_edges_kernel<<<nb, 256, 0, s>>>(src, N, j0, max_bins, more, edges, n_bins);
   count_launches();
   if (aligned(X, 16) && ldx % 4 == 0)
     bin_kernel<true><<<dim3(gx, nb), 256, 0, s>>>(X, ldx, N, j0, max_bins, edges, n_bins, bins, ldb);
@@ -440,6 +568,8 @@ extern "C" int gbdt_quantize(const float* X, int64_t ldx, int64_t N, int32_t F, 
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   GBDT_CUDA(cudaMemsetAsync(w.flag, 0, sizeof(int32_t), s));
+  GBDT_CUDA(cudaMemsetAsync(w.cnt, 0, sizeof(uint32_t) * F, s));
+  GBDT_CUDA(cudaMemsetAsync(w.more, 0, sizeof(int32_t) * F, s));
   const int gx = std::min<int64_t>(ceil_div(N, 256), sm_count() * 4);
   finite_kernel<<<dim3(gx, std::min(F, 64)), 256, 0, s>>>(X, ldx, N, F, w.flag);
   count_launches();
@@ -452,7 +582,9 @@ extern "C" int gbdt_quantize(const float* X, int64_t ldx, int64_t N, int32_t F, 
   }
   const int fb = batch_columns(N, F);
   for (int j0 = 0; j0 < F; j0 += fb) {
-    const int rc = quantize_batch(X, ldx, N, j0, std::min(fb, F - j0), max_bins, bins, ldb, edges, n_bins, w, s);
+    const int nb = std::min(fb, F - j0);
+    distinct_batch(X, ldx, N, j0, nb, max_bins, edges, n_bins, w, s);
+    const int rc = quantize_batch(X, ldx, N, j0, nb, max_bins, bins, ldb, edges, n_bins, w, s);
     if (rc != GBDT_OK) return rc;
   }
   return GBDT_OK;
@@ -501,15 +633,14 @@ extern "C" int gbdt_quantize_host(const float* X_host, int64_t ldx, int64_t N, i
     GBDT_CUDA(cudaEventRecord(r.ev[b], r.cs));
   }
   GBDT_CUDA(cudaMemsetAsync(w.flag, 0, sizeof(int32_t), s));
-  const int gx = std::min<int64_t>(ceil_div(N, 256), sm_count() * 4);
+  GBDT_CUDA(cudaMemsetAsync(w.cnt, 0, sizeof(uint32_t) * F, s));
+  GBDT_CUDA(cudaMemsetAsync(w.more, 0, sizeof(int32_t) * F, s));
   for (int b = 0; b < n_batches; ++b) {
     const int j0 = b * fb, nb = std::min(fb, F - j0);
     GBDT_CUDA(cudaStreamWaitEvent(s, r.ev[b], 0));
-    // finiteness of the batch, read once more at the end: the outputs of a call that fails it are
-    // not to be used
-    finite_kernel<<<dim3(gx, std::min(nb, 64)), 256, 0, s>>>(X_dev + static_cast<int64_t>(j0) * ldx, ldx, N, nb,
-                                                             w.flag);
-    count_launches();
+    // finiteness (read once at the end: the outputs of a call that fails it are not to be used) and
+    // distinct values of the batch, then its sort
+    distinct_batch(X_dev, ldx, N, j0, nb, max_bins, edges, n_bins, w, s);
     const int rc = quantize_batch(X_dev, ldx, N, j0, nb, max_bins, bins, ldb, edges, n_bins, w, s);
     if (rc != GBDT_OK) return rc;
   }

@@ -26,7 +26,7 @@ def test_quantize_matches_oracle(name, n):
 
 
 @pytest.mark.parametrize("case", ["constant", "two_values", "signed_zero", "n1", "n15", "n17", "all_distinct_256",
-                                  "ties_at_quantiles", "huge_range"])
+                                  "ties_at_quantiles", "huge_range", "sorted_blocks_300", "u256", "u257"])
 def test_quantize_edge_cases(case):
     rng = np.random.default_rng(hash(case) % 2**32)
     if case == "constant":
@@ -45,6 +45,11 @@ def test_quantize_edge_cases(case):
         X = rng.permutation(np.arange(70_000, dtype=np.float32))[None, :]
     elif case == "ties_at_quantiles":
         X = np.round(rng.exponential(3.0, (4, 40_000))).astype(np.float32)
+    elif case == "sorted_blocks_300":  # few distinct values per stretch of rows, 300 in the column
+        X = np.repeat(np.arange(300, dtype=np.float32), 200)[None, :] * 0.5 - 20.0
+    elif case in ("u256", "u257"):  # exactly max_bins distinct values, and one more, in random order
+        U = 256 if case == "u256" else 257
+        X = rng.permutation(np.tile(rng.normal(size=U).astype(np.float32), 90))[None, :]
     else:
         X = (rng.normal(size=(2, 9000)) * 10.0 ** rng.integers(-30, 30, (2, 9000))).astype(np.float32)
     for B in (2, 16, 255, 256):
