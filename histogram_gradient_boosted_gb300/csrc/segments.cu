@@ -1275,38 +1275,69 @@ __device__ __forceinline__ int pair_run(const PairRoute& pr, const uint8_t* __re
   return 2 * c + ((c ? d21 > pr.b2[1] : d20 > pr.b2[0]) ? 1 : 0);
 }
 
-// A tile's runs counted by kPairCountThreads threads, U rows in flight each: one pass over the tile, and
-// four times the threads of the move, so that a level of few tiles (a small matrix) still keeps enough
-// decision loads in flight.
+// Threads of the leaf pass (pair_leaves_kernel): four times the threads of the move, so that a level
+// of few tiles (a small matrix) still keeps enough decision loads in flight.
 constexpr int kPairCountThreads = 1024;
 
-__global__ void __launch_bounds__(kPairCountThreads)
+// A tile's runs counted from whole words: four consecutive positions of a slot are four consecutive
+// bytes of a row block, so one aligned 4-byte load brings a feature's decisions for four rows (three
+// loads per four rows: the parent's feature and both children's); a thread keeps kPairWordsInFlight
+// words of each in flight.
+constexpr int kPairWordThreads = 256;
+constexpr int kPairWordsInFlight = 4;
+
+__device__ __forceinline__ uint32_t rb_word(const uint8_t* __restrict__ rb, uint32_t loc, int64_t p4, int64_t pitch) {
+  return __ldg(reinterpret_cast<const uint32_t*>(rb + rb_offset(static_cast<int>(loc_slot(loc)), p4, pitch)));
+}
+
+__global__ void __launch_bounds__(kPairWordThreads)
     pair_count_kernel(const uint8_t* __restrict__ bins, int64_t pitch, const PairRoute* __restrict__ pairs,
                       const int32_t* __restrict__ tile_start, const PairState* __restrict__ st,
                       int4* __restrict__ tile_cnt) {
-  constexpr int U = kMvTile / kPairCountThreads;  // rows in flight per thread
+  constexpr int U = kPairWordsInFlight;
   const int t = blockIdx.x;
   if (t >= st->total_tiles) return;
-  __shared__ int4 s_warp[kPairCountThreads / 32];
+  __shared__ int4 s_warp[kPairWordThreads / 32];
   const int k = slot_of_tile(tile_start, st->n_pairs, t);
   const PairRoute& pr = pairs[k];
   const int64_t p0 = pr.start + static_cast<int64_t>(t - tile_start[k]) * kMvTile;
-  const int n = static_cast<int>(min(pr.start + pr.count - p0, static_cast<int64_t>(kMvTile)));
+  const int64_t p1 = p0 + min(pr.start + pr.count - p0, static_cast<int64_t>(kMvTile));
+  const int64_t w0 = p0 >> 2, w1 = (p1 + 3) >> 2;  // aligned words covering [p0, p1)
+  const uint32_t f1 = static_cast<uint32_t>(pr.f1);
+  const int b1 = pr.b1;
+  const bool s0 = pr.f2[0] >= 0, s1 = pr.f2[1] >= 0;  // the children that split
   int c[4] = {0, 0, 0, 0};
-  for (int j0 = threadIdx.x; j0 < n; j0 += U * blockDim.x) {
-    int r[U];
+  for (int64_t wb = w0 + threadIdx.x; wb < w1; wb += static_cast<int64_t>(U) * kPairWordThreads) {
+    uint32_t dp[U], da[U], db[U];
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int j = j0 + u * blockDim.x;
-      int child;
-      r[u] = j < n ? pair_run(pr, bins, pitch, p0 + j, &child) : -1;
+    for (int u = 0; u < U; ++u) {  // the words' loads first
+      const int64_t w = wb + static_cast<int64_t>(u) * kPairWordThreads;
+      dp[u] = da[u] = db[u] = 0;
+      if (w < w1) {
+        dp[u] = rb_word(bins, f1, 4 * w, pitch);
+        if (s0) da[u] = rb_word(bins, static_cast<uint32_t>(pr.f2[0]), 4 * w, pitch);
+        if (s1) db[u] = rb_word(bins, static_cast<uint32_t>(pr.f2[1]), 4 * w, pitch);
+      }
     }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      c[0] += r[u] == 0;
-      c[1] += r[u] == 1;
-      c[2] += r[u] == 2;
-      c[3] += r[u] == 3;
+      const int64_t w = wb + static_cast<int64_t>(u) * kPairWordThreads;
+      if (w >= w1) continue;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int64_t p = 4 * w + i;
+        if (p < p0 || p >= p1) continue;
+        const int d1 = static_cast<int>((dp[u] >> (8 * i + loc_shift(f1))) & loc_mask(f1));
+        const int ch = d1 > b1 ? 1 : 0;
+        if (!(ch ? s1 : s0)) continue;  // the child is a leaf: its rows are in no run
+        const uint32_t loc = static_cast<uint32_t>(ch ? pr.f2[1] : pr.f2[0]);
+        const int d2 = static_cast<int>(((ch ? db[u] : da[u]) >> (8 * i + loc_shift(loc))) & loc_mask(loc));
+        const int r = 2 * ch + (d2 > (ch ? pr.b2[1] : pr.b2[0]) ? 1 : 0);
+        c[0] += r == 0;
+        c[1] += r == 1;
+        c[2] += r == 2;
+        c[3] += r == 3;
+      }
     }
   }
   // the tile's four totals: warp sums by shuffles, then thread 0 adds the warps' sums
@@ -1319,7 +1350,7 @@ __global__ void __launch_bounds__(kPairCountThreads)
   __syncthreads();
   if (threadIdx.x == 0) {
     int4 tot = make_int4(0, 0, 0, 0);
-    for (int w = 0; w < kPairCountThreads / 32; ++w) {
+    for (int w = 0; w < kPairWordThreads / 32; ++w) {
       const int4 v = s_warp[w];
       tot.x += v.x, tot.y += v.y, tot.z += v.z, tot.w += v.w;
     }
@@ -1804,8 +1835,8 @@ void launch_move_pairs(const CUtensorMap& map_in, const uint8_t* bins_rb_in, uin
   pair_routes_kernel<<<1, 1024, 0, s>>>(level, max_slots, seg, route_cur, route_prev, pair_parent, seg_next, floc,
                                         p.pairs, p.tile_start, p.st);
   count_launches();
-  pair_count_kernel<<<p.max_tiles, kPairCountThreads, 0, s>>>(bins_rb_in, pitch, p.pairs, p.tile_start, p.st,
-                                                                p.tile_cnt);
+  pair_count_kernel<<<p.max_tiles, kPairWordThreads, 0, s>>>(bins_rb_in, pitch, p.pairs, p.tile_start, p.st,
+                                                               p.tile_cnt);
   count_launches();
   pair_scan_kernel<<<1, 1024, 0, s>>>(p.pairs, p.tile_start, p.st, p.tile_cnt, p.tile_excl, err);
   count_launches();
