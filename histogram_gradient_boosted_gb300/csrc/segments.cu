@@ -1275,8 +1275,10 @@ __device__ __forceinline__ int pair_run(const PairRoute& pr, const uint8_t* __re
   return 2 * c + ((c ? d21 > pr.b2[1] : d20 > pr.b2[0]) ? 1 : 0);
 }
 
-// Threads of the leaf pass (pair_leaves_kernel): four times the threads of the move, so that a level
-// of few tiles (a small matrix) still keeps enough decision loads in flight.
+// Threads of the leaf pass (pair_leaves_kernel): a thread per row of a tile and four rows in flight;
+// consecutive lanes take consecutive rows, whose row ids (stable moves from the identity) are close
+// together, so the leaf writes of a warp fall on few sectors.  (Whole-word decision loads, as in
+// pair_count_kernel, spread a warp's writes over more sectors and were slower.)
 constexpr int kPairCountThreads = 1024;
 
 // A tile's runs counted from whole words: four consecutive positions of a slot are four consecutive
@@ -1369,16 +1371,28 @@ __global__ void __launch_bounds__(1024)
   const int total = st->total_tiles;
   if (threadIdx.x < 4) s_carry[threadIdx.x] = 0;
   __syncthreads();
-  for (int c0 = 0; c0 < total; c0 += blockDim.x) {
-    const int t = c0 + threadIdx.x;
-    const int4 v = t < total ? tile_cnt[t] : make_int4(0, 0, 0, 0);
-    const int vv[4] = {v.x, v.y, v.z, v.w};
+  constexpr int kPer = 4;  // consecutive tiles per thread: one pass of four block scans covers 4096 tiles
+  for (int c0 = 0; c0 < total; c0 += kPer * static_cast<int>(blockDim.x)) {
+    const int t0 = c0 + kPer * static_cast<int>(threadIdx.x);
+    int4 v[kPer];
+    int sum[4] = {0, 0, 0, 0};
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      v[i] = t0 + i < total ? tile_cnt[t0 + i] : make_int4(0, 0, 0, 0);
+      sum[0] += v[i].x, sum[1] += v[i].y, sum[2] += v[i].z, sum[3] += v[i].w;
+    }
     int ct[4], e[4];
-    for (int r = 0; r < 4; ++r) e[r] = block_scan_excl(vv[r], s_warp, &ct[r]);
-    if (t < total) {
-      RunPrefix x;
-      for (int r = 0; r < 4; ++r) x.r[r] = s_carry[r] + e[r];
-      tile_excl[t] = x;
+    for (int r = 0; r < 4; ++r) e[r] = block_scan_excl(sum[r], s_warp, &ct[r]);
+    long long run[4];
+    for (int r = 0; r < 4; ++r) run[r] = s_carry[r] + e[r];
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      if (t0 + i < total) {
+        RunPrefix x;
+        for (int r = 0; r < 4; ++r) x.r[r] = run[r];
+        tile_excl[t0 + i] = x;
+      }
+      run[0] += v[i].x, run[1] += v[i].y, run[2] += v[i].z, run[3] += v[i].w;
     }
     __syncthreads();
     if (threadIdx.x < 4) s_carry[threadIdx.x] += ct[threadIdx.x];
