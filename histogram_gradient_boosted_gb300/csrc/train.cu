@@ -344,16 +344,22 @@ int32_t max_nodes_of(int D) { return (1 << (D + 1)) - 1; }
 
 // A captured sequence of launches (one tree) replayed with cudaGraphLaunch.  The capture runs on a
 // stream of its own (the caller's stream may be the legacy default stream, which cannot capture);
-// capturing only records the launches, and the launch counter is corrected for them.
+// capturing only records the launches, and the launch counter is corrected for them.  Timing events
+// recorded during the capture become event-record nodes; before each replay they are pointed at that
+// tree's events (the graph is kept for their node handles).
 struct TreeGraph {
   cudaStream_t cs = nullptr;
+  cudaGraph_t graph = nullptr;
   cudaGraphExec_t exec = nullptr;
-  int64_t launches = 0;  // kernels in the graph
+  int64_t launches = 0;                  // kernels in the graph
+  std::vector<cudaGraphNode_t> marks;    // event-record nodes
+  std::vector<cudaEvent_t> mark_events;  // the event each one recorded in the capture
   TreeGraph() = default;
   TreeGraph(const TreeGraph&) = delete;
   TreeGraph& operator=(const TreeGraph&) = delete;
   ~TreeGraph() {  // an executable graph still in flight is released when it completes
     if (exec) cudaGraphExecDestroy(exec);
+    if (graph) cudaGraphDestroy(graph);
     if (cs) cudaStreamDestroy(cs);
   }
   template <typename F>
@@ -362,20 +368,28 @@ struct TreeGraph {
     GBDT_CUDA(cudaStreamBeginCapture(cs, cudaStreamCaptureModeRelaxed));
     const int64_t l0 = launch_count();
     const int rc = record(cs);
-    cudaGraph_t graph = nullptr;
     const cudaError_t e = cudaStreamEndCapture(cs, &graph);
     launches = launch_count() - l0;
     count_launches(static_cast<int>(-launches));
-    if (rc != GBDT_OK) {
-      if (graph) cudaGraphDestroy(graph);
-      return rc;
-    }
+    if (rc != GBDT_OK) return rc;
     if (e != cudaSuccess) {
       set_error("gbdt_train: capturing a tree's launches failed: %s", cudaGetErrorString(e));
       return GBDT_ERR_CUDA;
     }
+    size_t n = 0;
+    GBDT_CUDA(cudaGraphGetNodes(graph, nullptr, &n));
+    std::vector<cudaGraphNode_t> nodes(n);
+    GBDT_CUDA(cudaGraphGetNodes(graph, nodes.data(), &n));
+    for (cudaGraphNode_t node : nodes) {
+      cudaGraphNodeType type;
+      GBDT_CUDA(cudaGraphNodeGetType(node, &type));
+      if (type != cudaGraphNodeTypeEventRecord) continue;
+      cudaEvent_t ev = nullptr;
+      GBDT_CUDA(cudaGraphEventRecordNodeGetEvent(node, &ev));
+      marks.push_back(node);
+      mark_events.push_back(ev);
+    }
     const cudaError_t ei = cudaGraphInstantiate(&exec, graph, 0);
-    cudaGraphDestroy(graph);
     if (ei != cudaSuccess) {
       exec = nullptr;
       set_error("gbdt_train: instantiating a tree's graph failed: %s", cudaGetErrorString(ei));
@@ -384,7 +398,6 @@ struct TreeGraph {
     return GBDT_OK;
   }
 };
-
 TrainWs carve_train(void* ws, size_t bytes, int64_t N, int32_t F, int64_t ldb, const gbdt_params& p,
                     size_t* need) {
   Carve c(ws, bytes);
@@ -591,6 +604,8 @@ extern "C" int gbdt_train(const uint8_t* bins, int64_t ldb, const int32_t* n_bin
   // index in device memory (budget[2], advanced by reset_root_kernel), so the sequence is the same for
   // every tree but the first (which counts the root's counts and keeps them) and the last (no next
   // gradients), and the trees between them replay it as one captured graph.
+  // timing events recorded while a tree is captured become event-record nodes of its graph
+  unsigned rec_flags = cudaEventRecordDefault;
   auto grow_tree = [&](int t, cudaStream_t s) -> int {
     launch_fixed_exp(w.maxabs, N, w.fixed_exp, logistic, s);
     reset_root_kernel<<<1, 1, 0, s>>>(w.level[0], w.build[0], w.seg[0], N, w.budget, next_work(0));
@@ -616,7 +631,7 @@ extern "C" int gbdt_train(const uint8_t* bins, int64_t ldb, const int32_t* n_bin
       if (d < D) {
         const int max_build = d == 0 ? 1 : max_slots / 2;
         const SegHistPlan plan = plan_seg_histograms(N, S, max_slots, max_build, logistic, odd, reg_arg, reg_codes);
-        if (timing) GBDT_CUDA(cudaEventRecord(ev_hist(t, d, 0), s));
+        if (timing) GBDT_CUDA(cudaEventRecordWithFlags(ev_hist(t, d, 0), s, rec_flags));
         const gbdt_segment* hseg = w.seg[cur];
         const gbdt_filter* hfil = nullptr;
         if (odd) {  // scan ranges and filters written by the level above (apply_level_kernel)
@@ -630,7 +645,7 @@ extern "C" int gbdt_train(const uint8_t* bins, int64_t ldb, const int32_t* n_bin
                                    w.hist_h[cur], s, true, w.floc, w.slot_src,
                                    d == 0 && t > 0 ? w.root_cnt : nullptr, n_bins, /*work_ready=*/true);
         if (rc != GBDT_OK) return rc;
-        if (timing) GBDT_CUDA(cudaEventRecord(ev_hist(t, d, 1), s));
+        if (timing) GBDT_CUDA(cudaEventRecordWithFlags(ev_hist(t, d, 1), s, rec_flags));
         if (d == 0 && t == 0)
           GBDT_CUDA(cudaMemcpyAsync(w.root_cnt, w.hist_cnt[cur], sizeof(uint32_t) * F * kBins,
                                     cudaMemcpyDeviceToDevice, s));
@@ -652,7 +667,7 @@ extern "C" int gbdt_train(const uint8_t* bins, int64_t ldb, const int32_t* n_bin
       // rows: after an odd level they move into the next order (four grandchild runs per pair); at
       // even levels nothing moves and the rows of nodes that do not split record their leaf; at the
       // last split level every row records its leaf.
-      if (timing) GBDT_CUDA(cudaEventRecord(ev_hist(t, d, 2), s));
+      if (timing) GBDT_CUDA(cudaEventRecordWithFlags(ev_hist(t, d, 2), s, rec_flags));
       if (d < D && d + 1 < D) {
         if (odd) {
           const int out = ((d + 1) >> 1) - 1 & 1;
@@ -671,7 +686,7 @@ extern "C" int gbdt_train(const uint8_t* bins, int64_t ldb, const int32_t* n_bin
         launch_leaf_rows(lb, pitch, w.floc, N, lo, w.level[cur], max_slots, w.seg[cur], w.route[cur], false, w.leaf,
                          w.move_scratch, s);
       }
-      if (timing) GBDT_CUDA(cudaEventRecord(ev_hist(t, d, 3), s));
+      if (timing) GBDT_CUDA(cudaEventRecordWithFlags(ev_hist(t, d, 3), s, rec_flags));
       GBDT_LAUNCH_CHECK();
       ++levels_done;
       if (fail_after >= 0 && levels_done >= fail_after) {
@@ -689,10 +704,11 @@ extern "C" int gbdt_train(const uint8_t* bins, int64_t ldb, const int32_t* n_bin
   };
 
   GBDT_CUDA(cudaMemsetAsync(w.budget + 2, 0xff, sizeof(int32_t), s));  // tree index -1
-  // Trees 1 .. T - 2 as one graph, captured once per call: a deep tree is a long chain of short
-  // launches, whose launch gaps a graph replay removes.  Timed (diagnostics) and failure-injection
-  // runs launch tree by tree.
-  const bool use_graph = !timing && fail_after < 0 && T >= 4;
+  // Trees 1 .. T - 2 as one graph, captured once per call: a tree is a chain of dependent launches,
+  // and a graph replay shortens the gap between each and the next.  With diagnostics the per-level
+  // timing events are nodes of the graph, pointed at each tree's events before its replay.
+  // Failure-injection runs launch tree by tree.
+  const bool use_graph = fail_after < 0 && T >= 4;
   TreeGraph tg;
   for (int t = 0; t < T; ++t) {
     if (t == 0) {
@@ -701,8 +717,22 @@ extern "C" int gbdt_train(const uint8_t* bins, int64_t ldb, const int32_t* n_bin
     }
     if (use_graph && t >= 1 && t + 1 < T) {
       if (tg.exec == nullptr) {
+        rec_flags = cudaEventRecordExternal;
         rc = tg.capture([&](cudaStream_t cs) { return grow_tree(t, cs); });
+        rec_flags = cudaEventRecordDefault;
         if (rc != GBDT_OK) return rc;
+      }
+      for (size_t i = 0; i < tg.marks.size(); ++i) {  // this tree's timing events (captured as tree t0's)
+        const int t0 = 1;
+        int slot = -1;
+        for (int d = 0; d <= D && slot < 0; ++d)
+          for (int k = 0; k < 4; ++k)
+            if (tg.mark_events[i] == ev_hist(t0, d, k)) slot = 4 * d + k;
+        if (slot < 0) {
+          set_error("gbdt_train: an event of the tree graph is not a timing event");
+          return GBDT_ERR_INTERNAL;
+        }
+        GBDT_CUDA(cudaGraphExecEventRecordNodeSetEvent(tg.exec, tg.marks[i], ev_hist(t, slot / 4, slot % 4)));
       }
       GBDT_CUDA(cudaGraphLaunch(tg.exec, s));
       count_launches(static_cast<int>(tg.launches));

@@ -68,9 +68,10 @@ def test_repeated_training_is_bit_identical():
 @pytest.mark.parametrize("name,n,trees,extra", [("covtype", 20_000, 6, dict(num_leaves=200)),
                                                 ("large", 30_000, 5, {}), ("mid", 10_000, 4, dict(objective=1))])
 def test_graph_replay_equals_tree_by_tree(name, n, trees, extra):
-    """Without diagnostics trees 1 .. T-2 replay one captured graph; with diagnostics every tree is launched
-    on its own.  Both must give the same model and predictions bit for bit (and the graph path must count
-    the replayed kernels)."""
+    """Trees 1 .. T-2 replay one captured graph (T >= 4), with or without diagnostics (whose timing events
+    are nodes of the graph); a run of 3 trees launches every tree on its own.  The first trees of both
+    must be the same, the runs with and without diagnostics identical (model, predictions, launch counts),
+    and the graph trees' histogram timings present."""
     bins, n_bins, yd, *_ = _prepare(name, n)
     y = yd
     if extra.get("objective") == 1:
@@ -87,6 +88,11 @@ def test_graph_replay_equals_tree_by_tree(name, n, trees, extra):
     assert list(a["nodes_per_tree"]) == list(b["nodes_per_tree"])
     assert torch.equal(a["pred"], b["pred"]) and a["init_pred"] == b["init_pred"]
     assert l1 - l0 == l2 - l1  # the replayed graph's kernels are counted as launches
+    D = params["max_depth"]
+    assert b["diag"]["hist_launches"] == trees * D and b["diag"]["hist_ms"] > 0
+    c = g.train(bins, n_bins, y, **dict(params, n_trees=3))  # tree by tree
+    assert a["nodes"][:3].tobytes() == c["nodes"].tobytes()
+    assert list(a["nodes_per_tree"][:3]) == list(c["nodes_per_tree"])
 
 
 def _raw_train(bins, n_bins, label, params, nodes, npt):
