@@ -536,11 +536,12 @@ int gbdt_predict(const float* X, int64_t ldx, int64_t N, int32_t F, const float*
  *   nodes_per_tree: HOST [n_trees] int32
  *   diag: optional HOST diagnostics (NULL to skip the timing events)
  * Synchronises the stream twice: after the input checks (n_bins range, finite
- * labels) and at the end.  With diag NULL and n_trees >= 4 the launches of
- * one tree are captured once per call into a CUDA graph (on a stream the call
- * creates and destroys) and trees 1 .. n_trees-2 replay it on `stream`; the
- * results are the same as launching tree by tree (which diag != NULL and the
- * failure-injection hook use).  On any error after parameter validation nodes_out
+ * labels) and at the end.  With n_trees >= 4 the launches of one tree are
+ * captured once per call into a CUDA graph (on a stream the call creates and
+ * destroys) and trees 1 .. n_trees-2 replay it on `stream` (with diag, its
+ * timing events are nodes of that graph, pointed at each tree's events); the
+ * results are the same as launching tree by tree (which the failure-injection
+ * hook uses).  On any error after parameter validation nodes_out
  * is left untouched and nodes_per_tree[*] = 0 (no partial model, s.5 State
  * Machine).
  * NaN/Inf labels: GBDT_ERR_NONFINITE; with the logistic objective a label
