@@ -1206,10 +1206,6 @@ struct PairState {
   int32_t total_tiles;
 };
 
-struct RunPrefix {  // rows of each of the four runs before a tile
-  long long r[4];
-};
-
 // One CTA: the pair records of a level and the tiles per pair.  level, seg and
 // route_cur describe the level (slots in sibling pairs); route_prev and
 // pair_parent the level above; seg_next the next level.
@@ -1277,138 +1273,87 @@ __device__ __forceinline__ int pair_run(const PairRoute& pr, const uint8_t* __re
 
 // Threads of the leaf pass (pair_leaves_kernel): a thread per row of a tile and four rows in flight;
 // consecutive lanes take consecutive rows, whose row ids (stable moves from the identity) are close
-// together, so the leaf writes of a warp fall on few sectors.  (Whole-word decision loads, as in
-// pair_count_kernel, spread a warp's writes over more sectors and were slower.)
-constexpr int kPairCountThreads = 1024;
+// together, so the leaf writes of a warp fall on few sectors.  (Whole-word decision loads, four rows
+// per thread, spread a warp's writes over more sectors and were slower.)
+constexpr int kPairLeafThreads = 1024;
 
-// A tile's runs counted from whole words: four consecutive positions of a slot are four consecutive
-// bytes of a row block, so one aligned 4-byte load brings a feature's decisions for four rows (three
-// loads per four rows: the parent's feature and both children's); a thread keeps kPairWordsInFlight
-// words of each in flight.
-constexpr int kPairWordThreads = 256;
-constexpr int kPairWordsInFlight = 4;
+// Decoupled look-back over the tiles of one pair (tiles first .. t-1, consecutive CTAs of this launch;
+// each waits only for earlier ones).  Warp 0 of tile t: publishes its run counts (status[t] = AGG |
+// counts, 13 bits each), sums the counts of the tiles before it - from the nearest tile that has
+// published its inclusive prefix (incl[], status PREFIX) or from the pair's first tile - into
+// s_pref, then publishes its own inclusive prefix.  status[] is zeroed before the launch.  Every wait
+// is bounded: a tile that gives up raises kErrWaitTimeout (its prefix is then incomplete; the writes
+// stay clamped to the runs' records).  The pair's last tile checks the four totals against the split
+// records (kErrPartitionCount).
+constexpr unsigned long long kTileAgg = 1ull << 62, kTilePrefix = 2ull << 62;
 
-__device__ __forceinline__ uint32_t rb_word(const uint8_t* __restrict__ rb, uint32_t loc, int64_t p4, int64_t pitch) {
-  return __ldg(reinterpret_cast<const uint32_t*>(rb + rb_offset(static_cast<int>(loc_slot(loc)), p4, pitch)));
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_u64(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 
-__global__ void __launch_bounds__(kPairWordThreads)
-    pair_count_kernel(const uint8_t* __restrict__ bins, int64_t pitch, const PairRoute* __restrict__ pairs,
-                      const int32_t* __restrict__ tile_start, const PairState* __restrict__ st,
-                      int4* __restrict__ tile_cnt) {
-  constexpr int U = kPairWordsInFlight;
-  const int t = blockIdx.x;
-  if (t >= st->total_tiles) return;
-  __shared__ int4 s_warp[kPairWordThreads / 32];
-  const int k = slot_of_tile(tile_start, st->n_pairs, t);
-  const PairRoute& pr = pairs[k];
-  const int64_t p0 = pr.start + static_cast<int64_t>(t - tile_start[k]) * kMvTile;
-  const int64_t p1 = p0 + min(pr.start + pr.count - p0, static_cast<int64_t>(kMvTile));
-  const int64_t w0 = p0 >> 2, w1 = (p1 + 3) >> 2;  // aligned words covering [p0, p1)
-  const uint32_t f1 = static_cast<uint32_t>(pr.f1);
-  const int b1 = pr.b1;
-  const bool s0 = pr.f2[0] >= 0, s1 = pr.f2[1] >= 0;  // the children that split
-  int c[4] = {0, 0, 0, 0};
-  for (int64_t wb = w0 + threadIdx.x; wb < w1; wb += static_cast<int64_t>(U) * kPairWordThreads) {
-    uint32_t dp[U], da[U], db[U];
-#pragma unroll
-    for (int u = 0; u < U; ++u) {  // the words' loads first
-      const int64_t w = wb + static_cast<int64_t>(u) * kPairWordThreads;
-      dp[u] = da[u] = db[u] = 0;
-      if (w < w1) {
-        dp[u] = rb_word(bins, f1, 4 * w, pitch);
-        if (s0) da[u] = rb_word(bins, static_cast<uint32_t>(pr.f2[0]), 4 * w, pitch);
-        if (s1) db[u] = rb_word(bins, static_cast<uint32_t>(pr.f2[1]), 4 * w, pitch);
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int64_t w = wb + static_cast<int64_t>(u) * kPairWordThreads;
-      if (w >= w1) continue;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int64_t p = 4 * w + i;
-        if (p < p0 || p >= p1) continue;
-        const int d1 = static_cast<int>((dp[u] >> (8 * i + loc_shift(f1))) & loc_mask(f1));
-        const int ch = d1 > b1 ? 1 : 0;
-        if (!(ch ? s1 : s0)) continue;  // the child is a leaf: its rows are in no run
-        const uint32_t loc = static_cast<uint32_t>(ch ? pr.f2[1] : pr.f2[0]);
-        const int d2 = static_cast<int>(((ch ? db[u] : da[u]) >> (8 * i + loc_shift(loc))) & loc_mask(loc));
-        const int r = 2 * ch + (d2 > (ch ? pr.b2[1] : pr.b2[0]) ? 1 : 0);
-        c[0] += r == 0;
-        c[1] += r == 1;
-        c[2] += r == 2;
-        c[3] += r == 3;
-      }
-    }
-  }
-  // the tile's four totals: warp sums by shuffles, then thread 0 adds the warps' sums
-  for (int o = 16; o > 0; o >>= 1) {
-#pragma unroll
-    for (int q = 0; q < 4; ++q) c[q] += __shfl_xor_sync(0xffffffffu, c[q], o);
-  }
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  if (lane == 0) s_warp[warp] = make_int4(c[0], c[1], c[2], c[3]);
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    int4 tot = make_int4(0, 0, 0, 0);
-    for (int w = 0; w < kPairWordThreads / 32; ++w) {
-      const int4 v = s_warp[w];
-      tot.x += v.x, tot.y += v.y, tot.z += v.z, tot.w += v.w;
-    }
-    tile_cnt[t] = tot;
-  }
-}
+struct Want4 {
+  long long v[4];  // each grandchild's rows from the split records (-1: its child does not split)
+};
 
-// One CTA: exclusive scan of each run's tile counts over all tiles; checks each
-// grandchild's total against its split record.
-__global__ void __launch_bounds__(1024)
-    pair_scan_kernel(const PairRoute* __restrict__ pairs, const int32_t* __restrict__ tile_start,
-                     const PairState* __restrict__ st, const int4* __restrict__ tile_cnt,
-                     RunPrefix* __restrict__ tile_excl, int32_t* __restrict__ err) {
-  __shared__ int s_warp[33];
-  __shared__ long long s_carry[4];
-  const int total = st->total_tiles;
-  if (threadIdx.x < 4) s_carry[threadIdx.x] = 0;
-  __syncthreads();
-  constexpr int kPer = 4;  // consecutive tiles per thread: one pass of four block scans covers 4096 tiles
-  for (int c0 = 0; c0 < total; c0 += kPer * static_cast<int>(blockDim.x)) {
-    const int t0 = c0 + kPer * static_cast<int>(threadIdx.x);
-    int4 v[kPer];
-    int sum[4] = {0, 0, 0, 0};
-#pragma unroll
-    for (int i = 0; i < kPer; ++i) {
-      v[i] = t0 + i < total ? tile_cnt[t0 + i] : make_int4(0, 0, 0, 0);
-      sum[0] += v[i].x, sum[1] += v[i].y, sum[2] += v[i].z, sum[3] += v[i].w;
-    }
-    int ct[4], e[4];
-    for (int r = 0; r < 4; ++r) e[r] = block_scan_excl(sum[r], s_warp, &ct[r]);
-    long long run[4];
-    for (int r = 0; r < 4; ++r) run[r] = s_carry[r] + e[r];
-#pragma unroll
-    for (int i = 0; i < kPer; ++i) {
-      if (t0 + i < total) {
-        RunPrefix x;
-        for (int r = 0; r < 4; ++r) x.r[r] = run[r];
-        tile_excl[t0 + i] = x;
+__device__ __forceinline__ void mv_tile_prefix(int t, int first, int end, int4 len4, Want4 want,
+                                               unsigned long long* __restrict__ status, int4* __restrict__ incl,
+                                               long long* s_pref, int32_t* __restrict__ err) {
+  const int lane = threadIdx.x & 31;
+  const int len[4] = {len4.x, len4.y, len4.z, len4.w};
+  const unsigned long long agg = static_cast<unsigned long long>(len[0]) |
+                                 static_cast<unsigned long long>(len[1]) << 13 |
+                                 static_cast<unsigned long long>(len[2]) << 26 |
+                                 static_cast<unsigned long long>(len[3]) << 39;
+  if (lane == 0) st_release_u64(&status[t], kTileAgg | agg);
+  long long pref[4] = {0, 0, 0, 0};
+  bool gave_up = false;
+  for (int top = t - 1; top >= first; top -= 32) {  // window of predecessors top, top - 1, ...
+    const int p = top - lane;
+    unsigned long long v = 0;
+    if (p >= first) {
+      for (uint32_t i = 0; i < kMvWaitPolls; ++i) {
+        v = ld_acquire_u64(&status[p]);
+        if (v >> 62) break;
       }
-      run[0] += v[i].x, run[1] += v[i].y, run[2] += v[i].z, run[3] += v[i].w;
+      if (!(v >> 62)) gave_up = true;
     }
-    __syncthreads();
-    if (threadIdx.x < 4) s_carry[threadIdx.x] += ct[threadIdx.x];
-    __syncthreads();
+    const uint32_t has_prefix = __ballot_sync(0xffffffffu, p >= first && (v >> 62) == 2);
+    const int stop = has_prefix ? __ffs(has_prefix) - 1 : 32;  // the nearest predecessor with a prefix
+    long long c[4] = {0, 0, 0, 0};
+    if (p >= first && lane < stop) {
+      c[0] = v & 0x1fff, c[1] = (v >> 13) & 0x1fff, c[2] = (v >> 26) & 0x1fff, c[3] = (v >> 39) & 0x1fff;
+    } else if (lane == stop) {
+      const int4 x = incl[p];  // written before its PREFIX status (acquired above)
+      c[0] = x.x, c[1] = x.y, c[2] = x.z, c[3] = x.w;
+    }
+    for (int o = 16; o > 0; o >>= 1) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) c[q] += __shfl_xor_sync(0xffffffffu, c[q], o);
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) pref[q] += c[q];
+    if (stop < 32) break;
   }
-  if (threadIdx.x == 0) {
-    RunPrefix x;
-    for (int r = 0; r < 4; ++r) x.r[r] = s_carry[r];
-    tile_excl[total] = x;
+  if (__any_sync(0xffffffffu, gave_up) && lane == 0) raise_error(err, kErrWaitTimeout);
+  if (lane == 0) {
+    incl[t] = make_int4(static_cast<int>(pref[0] + len[0]), static_cast<int>(pref[1] + len[1]),
+                        static_cast<int>(pref[2] + len[2]), static_cast<int>(pref[3] + len[3]));
+    __threadfence();
+    st_release_u64(&status[t], kTilePrefix | agg);
+    bool bad = false;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const long long tot = pref[q] + len[q];
+      if (want.v[q] < 0 ? len[q] != 0 : (tot > want.v[q] || (t == end - 1 && tot != want.v[q]))) bad = true;
+    }
+    if (bad) raise_error(err, kErrPartitionCount);
   }
-  __syncthreads();
-  for (int k = threadIdx.x; k < st->n_pairs; k += blockDim.x) {
-    const RunPrefix a = tile_excl[tile_start[k]], b = tile_excl[tile_start[k + 1]];
-    for (int r = 0; r < 4; ++r)
-      if (pairs[k].want[r] >= 0 && b.r[r] - a.r[r] != pairs[k].want[r]) raise_error(err, kErrPartitionCount);
-  }
+  if (lane < 4) s_pref[lane] = pref[lane];
 }
 
 __global__ void __launch_bounds__(kMvThreads, 5)
@@ -1417,8 +1362,8 @@ __global__ void __launch_bounds__(kMvThreads, 5)
                      const uint64_t* __restrict__ g_in, uint64_t* __restrict__ g_out,
                      const uint32_t* __restrict__ orig_in, uint32_t* __restrict__ orig_out,
                      const PairRoute* __restrict__ pairs, const int32_t* __restrict__ tile_start,
-                     const PairState* __restrict__ st, const RunPrefix* __restrict__ tile_excl,
-                     uint16_t* __restrict__ leaf_of_row, int32_t* __restrict__ err) {
+                     const PairState* __restrict__ st, unsigned long long* __restrict__ status,
+                     int4* __restrict__ incl, uint16_t* __restrict__ leaf_of_row, int32_t* __restrict__ err) {
   __shared__ uint32_t s_mask[4][kMvChunks];  // per run, per 32-row chunk: rows of the run
   __shared__ int s_cbase[4][kMvChunks];      // per run, per chunk: the run's rows before the chunk
   __shared__ uint16_t s_inv[kMvTile];
@@ -1427,11 +1372,12 @@ __global__ void __launch_bounds__(kMvThreads, 5)
   __shared__ int s_wtot[kMvThreads / 32][4];
   __shared__ uint16_t s_unit[kMvMaxUnits];
   __shared__ MvRunTable s_rt;
+  __shared__ long long s_pref[4];
   const int t = blockIdx.x;
   if (t >= st->total_tiles) return;
-  // the destinations come from the split records: if any run disagreed with its record (raised by
-  // the scan before this launch), nothing moves and the caller sees the error
-  if (*reinterpret_cast<volatile int32_t*>(err) & kErrPartitionCount) return;
+  // Every tile of the launch publishes its run counts (see mv_tile_prefix), so none returns early; a
+  // run whose rows disagree with its split record is clamped to the record's range and the error
+  // raised, so no write leaves the grandchild's range.
   const int k = slot_of_tile(tile_start, st->n_pairs, t);
   const PairRoute pr = pairs[k];
   const int64_t tile_off = static_cast<int64_t>(t - tile_start[k]) * kMvTile;
@@ -1497,24 +1443,32 @@ __global__ void __launch_bounds__(kMvThreads, 5)
     }
   }
   __syncthreads();
+  if (warp == 0)
+    mv_tile_prefix(t, tile_start[k], tile_start[k + 1], make_int4(len[0], len[1], len[2], len[3]),
+                   Want4{{pr.want[0], pr.want[1], pr.want[2], pr.want[3]}},
+                   status, incl, s_pref, err);
+  __syncthreads();
   MvRuns<4> ru;
-  const RunPrefix ex = tile_excl[t], ex0 = tile_excl[tile_start[k]];
+  int lim[4];  // rows of each run this tile may write: clamped to the run's record
   int acc = 0;
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
-    ru.dst[q] = pr.dst[q] + (ex.r[q] - ex0.r[q]);
+    const long long pref = s_pref[q];
+    ru.dst[q] = pr.dst[q] + pref;
     ru.len[q] = len[q];
     ru.base[q] = acc;
     acc += len[q];
+    const long long room = pr.want[q] < 0 ? 0 : pr.want[q] - pref;
+    lim[q] = static_cast<int>(room < 0 ? 0 : (room < len[q] ? room : len[q]));
   }
   if (threadIdx.x == 0) {
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       s_rt.dst[q] = ru.dst[q];
-      s_rt.len[q] = ru.len[q];
+      s_rt.len[q] = lim[q];
       s_rt.base[q] = ru.base[q];
       s_rt.a[q] = static_cast<int>(ru.dst[q] % kMvUnit);
-      s_rt.nu[q] = ru.len[q] > 0 ? (s_rt.a[q] + ru.len[q] + kMvUnit - 1) / kMvUnit : 0;
+      s_rt.nu[q] = lim[q] > 0 ? (s_rt.a[q] + lim[q] + kMvUnit - 1) / kMvUnit : 0;
     }
   }
   // ---- the inverse permutation; the gradient and the row id of every moved row go straight to its
@@ -1536,7 +1490,7 @@ __global__ void __launch_bounds__(kMvThreads, 5)
         if (m >> lane & 1u) {
           const int o = s_cbase[q][ch] + __popc(m & lt);  // the row's rank in its run
           s_inv[ru.base[q] + o] = static_cast<uint16_t>(ch * 32 + lane);
-          dst[u] = ru.dst[q] + o;
+          if (o < lim[q]) dst[u] = ru.dst[q] + o;
         }
       }
       if (dst[u] >= 0) {
@@ -1564,7 +1518,7 @@ __global__ void __launch_bounds__(kMvThreads, 5)
 
 // Last split level when it is an odd level: every row of a pair records its
 // leaf (a grandchild when its child splits, else the child), nothing moves.
-__global__ void __launch_bounds__(kPairCountThreads)
+__global__ void __launch_bounds__(kPairLeafThreads)
     pair_leaves_kernel(const uint8_t* __restrict__ bins_in, int64_t pitch, const uint32_t* __restrict__ orig_in,
                        const PairRoute* __restrict__ pairs, const int32_t* __restrict__ tile_start,
                        const PairState* __restrict__ st, uint16_t* __restrict__ leaf_of_row) {
@@ -1768,15 +1722,15 @@ size_t pair_scratch_bytes(int64_t N, int32_t max_slots) {
   const size_t pairs = static_cast<size_t>(max_slots) / 2 + 1;
   const size_t tiles = static_cast<size_t>(ceil_div(N, kMvTile)) + pairs;
   return sizeof(PairState) + sizeof(PairRoute) * pairs + sizeof(int32_t) * (pairs + 1) + sizeof(int4) * tiles +
-         sizeof(RunPrefix) * (tiles + 1) + 6 * kWsAlign;
+         sizeof(unsigned long long) * tiles + 6 * kWsAlign;
 }
 
 struct PairScratch {
   PairState* st;
   PairRoute* pairs;
   int32_t* tile_start;
-  int4* tile_cnt;
-  RunPrefix* tile_excl;
+  int4* tile_cnt;  // per tile: its runs' inclusive prefix within its pair (the look-back)
+  unsigned long long* tile_status;
   int max_tiles;
 };
 
@@ -1789,7 +1743,7 @@ PairScratch carve_pairs(void* scratch, int64_t N, int32_t max_slots) {
   p.pairs = c.take<PairRoute>(pairs);
   p.tile_start = c.take<int32_t>(pairs + 1);
   p.tile_cnt = c.take<int4>(p.max_tiles);
-  p.tile_excl = c.take<RunPrefix>(p.max_tiles + 1);
+  p.tile_status = c.take<unsigned long long>(p.max_tiles);
   return p;
 }
 }  // namespace
@@ -1849,15 +1803,11 @@ void launch_move_pairs(const CUtensorMap& map_in, const uint8_t* bins_rb_in, uin
   pair_routes_kernel<<<1, 1024, 0, s>>>(level, max_slots, seg, route_cur, route_prev, pair_parent, seg_next, floc,
                                         p.pairs, p.tile_start, p.st);
   count_launches();
-  pair_count_kernel<<<p.max_tiles, kPairWordThreads, 0, s>>>(bins_rb_in, pitch, p.pairs, p.tile_start, p.st,
-                                                               p.tile_cnt);
-  count_launches();
-  pair_scan_kernel<<<1, 1024, 0, s>>>(p.pairs, p.tile_start, p.st, p.tile_cnt, p.tile_excl, err);
-  count_launches();
+  cudaMemsetAsync(p.tile_status, 0, sizeof(unsigned long long) * p.max_tiles, s);
   pair_move_kernel<<<p.max_tiles, kMvThreads, 0, s>>>(
       map_in, bins_rb_out, pitch, bins_rb_in, S, reinterpret_cast<const uint64_t*>(g_in),
-      reinterpret_cast<uint64_t*>(g_out), orig_in, orig_out, p.pairs, p.tile_start, p.st, p.tile_excl, leaf_of_row,
-      err);
+      reinterpret_cast<uint64_t*>(g_out), orig_in, orig_out, p.pairs, p.tile_start, p.st, p.tile_status, p.tile_cnt,
+      leaf_of_row, err);
   count_launches();
 }
 
@@ -1869,7 +1819,7 @@ void launch_leaf_pairs(const uint8_t* bins_rb, int64_t pitch, const uint32_t* fl
   pair_routes_kernel<<<1, 1024, 0, s>>>(level, max_slots, seg, route_cur, route_prev, pair_parent, seg_next, floc,
                                         p.pairs, p.tile_start, p.st);
   count_launches();
-  pair_leaves_kernel<<<p.max_tiles, kPairCountThreads, 0, s>>>(bins_rb, pitch, orig_in, p.pairs, p.tile_start,
+  pair_leaves_kernel<<<p.max_tiles, kPairLeafThreads, 0, s>>>(bins_rb, pitch, orig_in, p.pairs, p.tile_start,
                                                                p.st, leaf_of_row);
   count_launches();
 }
