@@ -264,6 +264,28 @@ __global__ void __launch_bounds__(256)
   }
 }
 
+// The same for the k-th slot of a level's work list (blockIdx.y = k < st->n_built).
+__global__ void __launch_bounds__(256)
+    hist_zero_built_kernel(const SegWork* __restrict__ st, const int32_t* __restrict__ build_slot, int32_t F,
+                           uint32_t* __restrict__ hist_cnt, int64_t* __restrict__ hist_q, int64_t* __restrict__ hist_h,
+                           const uint32_t* cnt0, const int32_t* __restrict__ n_bins) {
+  if (static_cast<int>(blockIdx.y) >= st->n_built) return;
+  const int slot = build_slot[blockIdx.y];
+  const int64_t per_slot = static_cast<int64_t>(F) * kBins;
+  const int64_t e = 4 * (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x);
+  if (e >= per_slot || !quad_used(n_bins, e)) return;
+  const int64_t o = slot * per_slot + e;
+  *reinterpret_cast<uint4*>(hist_cnt + o) =
+      (cnt0 && slot == 0) ? *reinterpret_cast<const uint4*>(cnt0 + e) : make_uint4(0, 0, 0, 0);
+  const longlong2 z = make_longlong2(0, 0);
+  reinterpret_cast<longlong2*>(hist_q + o)[0] = z;
+  reinterpret_cast<longlong2*>(hist_q + o)[1] = z;
+  if (hist_h) {
+    reinterpret_cast<longlong2*>(hist_h + o)[0] = z;
+    reinterpret_cast<longlong2*>(hist_h + o)[1] = z;
+  }
+}
+
 __device__ __forceinline__ longlong2 sub2(longlong2 a, longlong2 b) {
   return make_longlong2(static_cast<long long>(static_cast<unsigned long long>(a.x) - static_cast<unsigned long long>(b.x)),
                         static_cast<long long>(static_cast<unsigned long long>(a.y) - static_cast<unsigned long long>(b.y)));
@@ -349,6 +371,15 @@ void launch_hist_zero(const gbdt_level* level, int32_t max_slots, const uint8_t*
   const int64_t per_slot = static_cast<int64_t>(F) * kBins;  // 4 bins per thread, 256 threads per CTA
   dim3 grid(static_cast<unsigned>((per_slot / 4 + 255) / 256), static_cast<unsigned>(max_slots));
   hist_zero_kernel<<<grid, 256, 0, s>>>(level, max_slots, build_flag, F, hist_cnt, hist_q, hist_h, cnt0, n_bins);
+  count_launches();
+}
+
+void launch_hist_zero_built(const SegWork* st, const int32_t* build_slot, int32_t max_built, int32_t F,
+                            uint32_t* hist_cnt, int64_t* hist_q, int64_t* hist_h, cudaStream_t s,
+                            const uint32_t* cnt0, const int32_t* n_bins) {
+  const int64_t per_slot = static_cast<int64_t>(F) * kBins;  // 4 bins per thread, 256 threads per CTA
+  dim3 grid(static_cast<unsigned>((per_slot / 4 + 255) / 256), static_cast<unsigned>(max_built < 1 ? 1 : max_built));
+  hist_zero_built_kernel<<<grid, 256, 0, s>>>(st, build_slot, F, hist_cnt, hist_q, hist_h, cnt0, n_bins);
   count_launches();
 }
 

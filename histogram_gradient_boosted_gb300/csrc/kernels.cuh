@@ -148,6 +148,11 @@ struct SegWorkView {
 };
 // Where the work list of a level of max_slots slots sits in seg_hist_scratch_bytes(max_slots) of scratch.
 SegWorkView seg_work_view(void* scratch, int32_t max_slots);
+// launch_hist_zero for the slots of a level's work list (st->n_built of them, build_slot[k]), at most
+// max_built: a CTA row per built slot instead of per slot.
+void launch_hist_zero_built(const SegWork* st, const int32_t* build_slot, int32_t max_built, int32_t F,
+                            uint32_t* hist_cnt, int64_t* hist_q, int64_t* hist_h, cudaStream_t s,
+                            const uint32_t* cnt0, const int32_t* n_bins);
 // S: the columns the lanes read (slots of the row blocks; F in the column layout).
 // filtered: the level's slots are counted through filters (a node's rows inside its pair's segment).
 // reg_begin >= 0: slots from reg_begin on are register slots of at most reg_codes codes (squared error only).

@@ -1663,8 +1663,13 @@ int launch_seg_histograms(const SegHistPlan& plan, const uint8_t* bins, int64_t 
   SegWork* st = wv.st;
   int32_t* build_slot = wv.build_slot;
   int64_t* row_start = wv.row_start;
-  launch_hist_zero(level, max_slots, build_flag, F, hist_cnt, hist_q, plan.with_h ? hist_h : nullptr, s, root_cnt,
-                   n_bins);
+  if (work_ready)  // the work list (written by the level above) names the built slots: at most half the
+                   // slots past the root, one of each sibling pair
+    launch_hist_zero_built(st, build_slot, max_slots > 1 ? max_slots / 2 : 1, F, hist_cnt, hist_q,
+                           plan.with_h ? hist_h : nullptr, s, root_cnt, n_bins);
+  else
+    launch_hist_zero(level, max_slots, build_flag, F, hist_cnt, hist_q, plan.with_h ? hist_h : nullptr, s, root_cnt,
+                     n_bins);
   if (!work_ready) {  // else the work list is already in the scratch (written by the level above)
     seg_work_setup_kernel<<<1, 1024, 0, s>>>(level, max_slots, build_flag, seg, plan.max_ctas, plan.min_rows,
                                              build_slot, row_start, st);
