@@ -85,13 +85,18 @@ int32_t* split_counters(void* scratch, int32_t F, int32_t max_slots);
 // the features whose n_bins is above kSplitNarrowBins first, then the n_narrow others, each of which one
 // thread searches alone; null: a warp per feature, in order.  totals (device, may be null): each slot's
 // expected totals (the parent split's sides), which every feature's histogram must sum to; null: the
-// totals are summed from feature 0's histogram.
+// totals are summed from feature 0's histogram.  prev_cnt (device, may be null): the previous level's
+// histograms (prev_q, prev_h), pair_parent and build_flag of this level: each slot not built is formed
+// as its parent's histogram minus its built sibling's, searched and stored (the sibling subtraction
+// fused into the search); null: every slot's histogram is in place.
 constexpr int kSplitNarrowBins = 8;
 void launch_find_splits(const uint32_t* hist_cnt, const int64_t* hist_q, const int64_t* hist_h,
                         const int32_t* fixed_exp, int32_t F, const int32_t* n_bins, const gbdt_level* level,
                         int32_t max_slots, const gbdt_params& p, gbdt_split* out, void* scratch, int32_t* err,
                         cudaStream_t s, const int32_t* fsched = nullptr, int32_t n_narrow = 0,
-                        const SlotTotals* totals = nullptr);
+                        const SlotTotals* totals = nullptr, const uint32_t* prev_cnt = nullptr,
+                        const int64_t* prev_q = nullptr, const int64_t* prev_h = nullptr,
+                        const int32_t* pair_parent = nullptr, const uint8_t* build_flag = nullptr);
 
 // ---- partition.cu ---------------------------------------------------------------------
 // Routing entry of a slot: split feature (-1: none), threshold bin, left child node id.

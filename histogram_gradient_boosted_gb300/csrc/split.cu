@@ -173,18 +173,30 @@ __device__ __forceinline__ T lane_prefix8(T (&v)[8], int lane, T* total) {
   return x - v[7];
 }
 
+// Where a slot's histogram comes from in training: a slot that was not built (the larger child of its
+// pair) is its parent's histogram (the previous level's, pair_parent[slot / 2]) minus its built sibling's
+// (slot ^ 1); the screen forms it, bin by bin, and also stores it (the next level subtracts from it).
+// pc null: every slot's histogram is in place (the ABI call).
+struct SubSrc {
+  const uint32_t* pc;
+  const int64_t* pq;
+  const int64_t* ph;
+  const int32_t* pair_parent;
+  const uint8_t* build_flag;
+};
+
 // Screen of feature f of a slot (one warp).  Writes the feature's survivors of
 // the FP32 screen to surv[slot][f][0 .. kSurv): in bin order, or, when more than
 // kSurv survive (long runs of empty bins can tie), the best of them evaluated in
 // FP64 as one exact entry.  kH: H from hist_h with exponent fixed_exp[1]
 // (logistic), else H = the row count.  tot_*: the node totals.
 template <bool kH, bool kNarrow>
-__device__ __forceinline__ void screen_feature(const uint32_t* __restrict__ hist_cnt, const int64_t* __restrict__ hist_q,
-                                               const int64_t* __restrict__ hist_h, const int32_t* __restrict__ fixed_exp,
+__device__ __forceinline__ void screen_feature(const uint32_t* hist_cnt, const int64_t* hist_q,
+                                               const int64_t* hist_h, const int32_t* __restrict__ fixed_exp,
                                                int32_t F, const int32_t* __restrict__ n_bins, int slot, int f, int lane,
                                                uint32_t tot_cnt, long long tot_q, long long tot_h, double lambda,
                                                double gamma, int32_t msl, double mcw, int64_t mcw_ceil,
-                                               Surv* __restrict__ surv, int32_t* __restrict__ err) {
+                                               Surv* __restrict__ surv, int32_t* __restrict__ err, const SubSrc& src) {
   // kNarrow: this thread alone holds the whole feature (at most 8 bins: its bins 0..7), so every sum,
   // maximum and survivor count below is the thread's own; otherwise the warp holds it, 8 bins per lane
   const int sub = kNarrow ? 0 : lane;  // this thread's bins: 8 sub .. 8 sub + 7
@@ -198,25 +210,60 @@ __device__ __forceinline__ void screen_feature(const uint32_t* __restrict__ hist
   long long q[8], qh[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) c[i] = 0, q[i] = 0, qh[i] = 0;
-  if (sub * 8 < nb) {
-    const uint4* cp = reinterpret_cast<const uint4*>(hist_cnt + off);
-    const longlong2* qp = reinterpret_cast<const longlong2*>(hist_q + off);
-    uint4 a = cp[0], b = cp[1];
-    c[0] = a.x, c[1] = a.y, c[2] = a.z, c[3] = a.w, c[4] = b.x, c[5] = b.y, c[6] = b.z, c[7] = b.w;
+  auto load8 = [&](const uint32_t* hc, const int64_t* hq, const int64_t* hh, int64_t o, uint32_t (&cc)[8],
+                   long long (&qq)[8], long long (&hv)[8]) {
+    const uint4* cp = reinterpret_cast<const uint4*>(hc + o);
+    const longlong2* qp = reinterpret_cast<const longlong2*>(hq + o);
+    const uint4 a = cp[0], b = cp[1];
+    cc[0] = a.x, cc[1] = a.y, cc[2] = a.z, cc[3] = a.w, cc[4] = b.x, cc[5] = b.y, cc[6] = b.z, cc[7] = b.w;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      longlong2 v = qp[i];
-      q[2 * i] = v.x;
-      q[2 * i + 1] = v.y;
+      const longlong2 v = qp[i];
+      qq[2 * i] = v.x;
+      qq[2 * i + 1] = v.y;
     }
     if (kH) {
-      const longlong2* hp = reinterpret_cast<const longlong2*>(hist_h + off);
+      const longlong2* hp = reinterpret_cast<const longlong2*>(hh + o);
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        longlong2 v = hp[i];
-        qh[2 * i] = v.x;
-        qh[2 * i + 1] = v.y;
+        const longlong2 v = hp[i];
+        hv[2 * i] = v.x;
+        hv[2 * i + 1] = v.y;
       }
+    }
+  };
+  if (sub * 8 < nb) {
+    if (src.pc && !src.build_flag[slot]) {  // parent minus the built sibling, stored for the next level
+      const int64_t fo = static_cast<int64_t>(f) * kBins + sub * 8;
+      const int64_t op = static_cast<int64_t>(src.pair_parent[slot >> 1]) * F * kBins + fo;
+      const int64_t ob = static_cast<int64_t>(slot ^ 1) * F * kBins + fo;
+      uint32_t bc[8];
+      long long bq[8], bh[8];
+      load8(src.pc, src.pq, src.ph, op, c, q, qh);
+      load8(hist_cnt, hist_q, hist_h, ob, bc, bq, bh);
+      bool bad = false;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        bad |= bc[i] > c[i] && sub * 8 + i < nb;
+        c[i] -= bc[i];
+        q[i] = static_cast<long long>(static_cast<unsigned long long>(q[i]) - static_cast<unsigned long long>(bq[i]));
+        if (kH)
+          qh[i] = static_cast<long long>(static_cast<unsigned long long>(qh[i]) - static_cast<unsigned long long>(bh[i]));
+      }
+      if (bad) raise_error(err, kErrHistTotals);
+      uint4* cs = reinterpret_cast<uint4*>(const_cast<uint32_t*>(hist_cnt) + off);
+      longlong2* qs = reinterpret_cast<longlong2*>(const_cast<int64_t*>(hist_q) + off);
+      cs[0] = make_uint4(c[0], c[1], c[2], c[3]);
+      cs[1] = make_uint4(c[4], c[5], c[6], c[7]);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) qs[i] = make_longlong2(q[2 * i], q[2 * i + 1]);
+      if (kH) {
+        longlong2* hs = reinterpret_cast<longlong2*>(const_cast<int64_t*>(hist_h) + off);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) hs[i] = make_longlong2(qh[2 * i], qh[2 * i + 1]);
+      }
+    } else {
+      load8(hist_cnt, hist_q, hist_h, off, c, q, qh);
     }
 #pragma unroll
     for (int i = 0; i < 8; ++i)
@@ -432,13 +479,12 @@ __device__ __forceinline__ void select_slot(const uint32_t* __restrict__ hist_cn
 // selects the slot's split.  No CTA waits for another.
 template <bool kH>
 __global__ void __launch_bounds__(kSplitThreads)
-    split_kernel(const uint32_t* __restrict__ hist_cnt, const int64_t* __restrict__ hist_q,
-                 const int64_t* __restrict__ hist_h, const int32_t* __restrict__ fixed_exp, int32_t F,
-                 const int32_t* __restrict__ n_bins, const gbdt_level* __restrict__ level, int32_t max_slots,
-                 double lambda, double gamma, int32_t msl, double mcw, int64_t mcw_ceil, Surv* __restrict__ surv,
-                 int32_t* __restrict__ slot_done, gbdt_split* __restrict__ out, int32_t* __restrict__ err,
-                 const int32_t* __restrict__ fsched, int32_t n_wide, int32_t n_narrow,
-                 const SlotTotals* __restrict__ totals) {
+    split_kernel(const uint32_t* hist_cnt, const int64_t* hist_q, const int64_t* hist_h,
+                 const int32_t* __restrict__ fixed_exp, int32_t F, const int32_t* __restrict__ n_bins,
+                 const gbdt_level* __restrict__ level, int32_t max_slots, double lambda, double gamma, int32_t msl,
+                 double mcw, int64_t mcw_ceil, Surv* __restrict__ surv, int32_t* __restrict__ slot_done,
+                 gbdt_split* __restrict__ out, int32_t* __restrict__ err, const int32_t* __restrict__ fsched,
+                 int32_t n_wide, int32_t n_narrow, const SlotTotals* __restrict__ totals, SubSrc src) {
   const int slot = blockIdx.x;
   const int n_slots = min(level->n_slots, max_slots);
   if (slot >= n_slots) return;  // every CTA of this slot
@@ -470,10 +516,10 @@ __global__ void __launch_bounds__(kSplitThreads)
   }
   if (f >= 0 && narrow)
     screen_feature<kH, true>(hist_cnt, hist_q, hist_h, fixed_exp, F, n_bins, slot, f, lane, tot_cnt, tot_q, tot_h,
-                             lambda, gamma, msl, mcw, mcw_ceil, surv, err);
+                             lambda, gamma, msl, mcw, mcw_ceil, surv, err, src);
   else if (f >= 0)  // warp-uniform
     screen_feature<kH, false>(hist_cnt, hist_q, hist_h, fixed_exp, F, n_bins, slot, f, lane, tot_cnt, tot_q, tot_h,
-                              lambda, gamma, msl, mcw, mcw_ceil, surv, err);
+                              lambda, gamma, msl, mcw, mcw_ceil, surv, err, src);
   __shared__ int s_last;
   __threadfence();  // this CTA's survivors are visible device-wide before it is counted
   __syncthreads();
@@ -503,7 +549,10 @@ int32_t* split_counters(void* scratch, int32_t F, int32_t max_slots) {
 void launch_find_splits(const uint32_t* hist_cnt, const int64_t* hist_q, const int64_t* hist_h,
                         const int32_t* fixed_exp, int32_t F, const int32_t* n_bins, const gbdt_level* level,
                         int32_t max_slots, const gbdt_params& p, gbdt_split* out, void* scratch, int32_t* err,
-                        cudaStream_t s, const int32_t* fsched, int32_t n_narrow, const SlotTotals* totals) {
+                        cudaStream_t s, const int32_t* fsched, int32_t n_narrow, const SlotTotals* totals,
+                        const uint32_t* prev_cnt, const int64_t* prev_q, const int64_t* prev_h,
+                        const int32_t* pair_parent, const uint8_t* build_flag) {
+  const SubSrc src{prev_cnt, prev_q, prev_h, pair_parent, build_flag};
   int32_t* done = split_counters(scratch, F, max_slots);
   Surv* surv = reinterpret_cast<Surv*>(static_cast<char*>(scratch) + kCounterBytes);
   if (!fsched) n_narrow = 0;
@@ -517,12 +566,12 @@ void launch_find_splits(const uint32_t* hist_cnt, const int64_t* hist_q, const i
     split_kernel<true><<<grid, kSplitThreads, 0, s>>>(hist_cnt, hist_q, hist_h, fixed_exp, F, n_bins, level,
                                                       max_slots, p.reg_lambda, p.gamma, p.min_samples_leaf,
                                                       p.min_child_weight, mcw_ceil, surv, done, out, err, fsched,
-                                                      n_wide, n_narrow, totals);
+                                                      n_wide, n_narrow, totals, src);
   else
     split_kernel<false><<<grid, kSplitThreads, 0, s>>>(hist_cnt, hist_q, nullptr, fixed_exp, F, n_bins, level,
                                                        max_slots, p.reg_lambda, p.gamma, p.min_samples_leaf,
                                                        p.min_child_weight, mcw_ceil, surv, done, out, err, fsched,
-                                                      n_wide, n_narrow, totals);
+                                                      n_wide, n_narrow, totals, src);
   count_launches();
 }
 

@@ -649,14 +649,12 @@ extern "C" int gbdt_train(const uint8_t* bins, int64_t ldb, const int32_t* n_bin
         if (d == 0 && t == 0)
           GBDT_CUDA(cudaMemcpyAsync(w.root_cnt, w.hist_cnt[cur], sizeof(uint32_t) * F * kBins,
                                     cudaMemcpyDeviceToDevice, s));
-        if (d > 0) {
-          launch_hist_subtract(w.hist_cnt[nxt], w.hist_q[nxt], w.hist_h[nxt], w.pair_parent[cur], w.build[cur],
-                               w.level[cur], max_slots, F, w.hist_cnt[cur], w.hist_q[cur], w.hist_h[cur], w.err, s,
-                               n_bins);
-        }
+        // past the root the larger child of each pair is its parent minus its built sibling, formed and
+        // stored by the split search itself
         launch_find_splits(w.hist_cnt[cur], w.hist_q[cur], w.hist_h[cur], w.fixed_exp, F, n_bins, w.level[cur],
                            max_slots, *p, w.splits, w.split_scratch, w.err, s, w.fsched, n_narrow,
-                           d > 0 ? w.totals[cur] : nullptr);
+                           d > 0 ? w.totals[cur] : nullptr, d > 0 ? w.hist_cnt[nxt] : nullptr, w.hist_q[nxt],
+                           w.hist_h[nxt], w.pair_parent[cur], w.build[cur]);
       }
       apply_level_kernel<<<1, 1024, 0, s>>>(d, D, w.level[cur], max_slots, d < D ? w.splits : nullptr, w.totals[cur],
                                             w.build[cur], w.fixed_exp, p->reg_lambda, w.seg[cur], w.trees,
