@@ -266,7 +266,7 @@ def baseline_table(g, torch, args):
         e1.record(stream)
         torch.cuda.synchronize()
         ms = e0.elapsed_time(e1) / steps
-        diags = [run(diag=True)["diag"]]  # the histogram launches' event times (tree by tree)
+        diags = [run(diag=True)["diag"]]  # the histogram launches' event times (timing nodes in the tree graph)
         hist_ms = sum(d["hist_ms"] for d in diags)
         frac = sum(d["hist_level_bytes"] for d in diags) / (hist_ms * 1e-3) / 1e9 / peak if hist_ms else None
         frac_read = sum(d["hist_bytes"] for d in diags) / (hist_ms * 1e-3) / 1e9 / peak if hist_ms else None
@@ -522,8 +522,9 @@ def covtype_leg(g, torch, args, peak, peak_kind, stream):
     torch.cuda.synchronize()
     n_launch = g.kernel_launch_count() - l0
     ms = e0.elapsed_time(e1) / steps
-    # the histogram launches' own times: the same runs with diagnostics (events around every level's
-    # launches, so these runs launch tree by tree instead of replaying the captured tree graph)
+    # the histogram launches' own times: the same runs with diagnostics (timing events around every
+    # level's launches, recorded as nodes of the replayed tree graph; they add gaps, so these runs are
+    # not the timed ones)
     diags = [run(diag=True)["diag"] for _ in range(2)]
     torch.cuda.synchronize()
     ms_diag = sum(d["total_ms"] for d in diags) / len(diags)
@@ -539,9 +540,10 @@ def covtype_leg(g, torch, args, peak, peak_kind, stream):
             "step": "gbdt_quantize + gbdt_train",
             "launches_per_step": n_launch / steps,
             "launches_per_tree": n_launch / (steps * T),
-            "train_ms_tree_by_tree": ms_diag,
+            "train_ms_with_diagnostics": ms_diag,
             "timing": "ms_per_step: runs without diagnostics (trees 1 .. T-2 replay one captured graph); hist: "
-                      "two more runs with diagnostics (tree by tree, events around each level's launches)",
+                      "two more runs with diagnostics (the same graph with timing events around each level's "
+                      "launches)",
             "hist": {"achieved_gbs": achieved, "frac": achieved / peak, "accounting": "level formula",
                      "achieved_read_gbs": achieved_read, "frac_read": achieved_read / peak, "peak_kind": peak_kind,
                      "avg_launch_ms": hist_ms / launches, "share_of_step": hist_ms / (ms * len(diags))},

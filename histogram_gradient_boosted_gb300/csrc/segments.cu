@@ -14,9 +14,12 @@
 // histogram.cu: 32-bit atomics only (count, low word with carry from the
 // returned value, high word when needed), merged into global memory once.
 //
-// The partition is a tile count, a scan over tiles, and a move in which each
-// CTA ranks its tile once and then streams several columns through shared
-// memory, writing the left and right runs with aligned 16-byte stores.
+// The one-level partition is a tile count, a scan over tiles, and a move in
+// which each CTA ranks its tile once and then streams several columns through
+// shared memory, writing the left and right runs with aligned 16-byte stores.
+// The training's pair move (two levels at once, four runs) needs no count or
+// scan launch: each tile finds its place by a look-back over its pair's
+// earlier tiles.
 #include <algorithm>
 #include <mutex>
 #include <type_traits>
