@@ -27,8 +27,9 @@ void launch_finish_tree(const gbdt_node* trees, const int32_t* n_nodes, const in
 void launch_gradients(const double* pred, const float* label, int64_t N, int32_t objective, double* g,
                       unsigned long long* maxabs, cudaStream_t s);
 void launch_maxabs(const void* g, int32_t dtype, int64_t N, unsigned long long* maxabs, cudaStream_t s);
-// fixed_exp[0] from maxabs[0]; with_h: fixed_exp[1] from maxabs[1].
-void launch_fixed_exp(const unsigned long long* maxabs, int64_t N, int32_t* fixed_exp, bool with_h, cudaStream_t s);
+// fixed_exp[0] from maxabs[0]; with_h: fixed_exp[1] from maxabs[1]; clear: maxabs reset to 0 after it is read.
+void launch_fixed_exp(unsigned long long* maxabs, int64_t N, int32_t* fixed_exp, bool with_h, cudaStream_t s,
+                      bool clear = false);
 
 // ---- histogram.cu ---------------------------------------------------------------------
 struct HistPlan {

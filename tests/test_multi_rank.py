@@ -52,12 +52,19 @@ def test_barrier_and_max_over_ranks(tmp_path):
 
 def test_reference_arm_prints_once_from_rank_zero():
     pytest.importorskip("torch")
-    port = _free_port()
-    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2", "--master-addr",
-           "127.0.0.1", "--master-port", str(port), os.path.join(ROOT, "bench.py"), "--impl", "reference", "--gpus",
-           "2", "--steps", "1", "--warmup", "0", "--config", "tiny", "--cpu-rows", "2000", "--cpu-trees", "1"]
     env = dict(os.environ, OMP_NUM_THREADS="1")
-    p = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=300, env=env)
+    for attempt in range(3):
+        # the port is free when chosen but is bound again only by the launcher: another process may take
+        # it in between, so a rendezvous that fails on its address is retried on a new port
+        port = _free_port()
+        cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2", "--master-addr",
+               "127.0.0.1", "--master-port", str(port), os.path.join(ROOT, "bench.py"), "--impl", "reference",
+               "--gpus", "2", "--steps", "1", "--warmup", "0", "--config", "tiny", "--cpu-rows", "2000",
+               "--cpu-trees", "1"]
+        p = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=300, env=env)
+        if p.returncode == 0 or not any(m in p.stderr for m in ("EADDRINUSE", "Address already in use",
+                                                                 "DistNetworkError")):
+            break
     assert p.returncode == 0, p.stderr[-2000:]
     lines = [json.loads(ln) for ln in p.stdout.splitlines() if ln.startswith("{")]
     assert len(lines) == 1, p.stdout
