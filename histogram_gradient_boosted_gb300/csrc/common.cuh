@@ -7,7 +7,6 @@
 
 #include <cstdarg>
 #include <cstdio>
-#include <utility>
 
 #include "gbdt.h"
 
@@ -235,37 +234,5 @@ int sm_count();
 // gbdt_kernel_launch_count so a caller can count launches in a timed region).
 void count_launches(int n = 1);
 int64_t launch_count();
-
-// ---- chained launches (programmatic dependent launch) ------------------------------------------
-// A tree is a chain of short dependent launches.  A kernel launched by launch_chained may have its
-// CTAs dispatched while the kernel before it on the stream is still running (once every CTA of that
-// kernel has passed chain_start); those CTAs wait in chain_start until that kernel has completed and
-// its writes are visible.  So every kernel launched this way calls chain_start first, before it
-// touches global memory and before any early return: a launch whose CTAs all returned without
-// waiting could complete before its predecessor, and the kernel after it would no longer wait for
-// that one.  For a kernel launched the ordinary way both instructions return at once.
-__device__ __forceinline__ void chain_start() {
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-
-// Launches kernel<<<grid, block, smem, s>>>(args...) with programmatic stream serialization (on the
-// legacy default stream, which synchronises with every other stream, an ordinary launch); a failed
-// launch is left in the runtime's last-error state, as with <<<>>>.
-template <typename... KArgs, typename... Args>
-inline void launch_chained(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
-                           Args&&... args) {
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cudaLaunchConfig_t cfg{};
-  cfg.gridDim = grid;
-  cfg.blockDim = block;
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = s;
-  cfg.attrs = attr;
-  cfg.numAttrs = (s == nullptr || s == cudaStreamLegacy) ? 0 : 1;
-  (void)cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
-}
 
 }  // namespace gbdt

@@ -120,7 +120,6 @@ __global__ void finish_tree_kernel(const gbdt_node* __restrict__ trees, const in
                                    double* __restrict__ pred, double* __restrict__ g, uint16_t* __restrict__ node,
                                    unsigned long long* maxabs, int next) {
   extern __shared__ double s_step[];  // lr * leaf_value per node of the tree
-  chain_start();
   const int t = *tree_index;
   const gbdt_node* __restrict__ tree = trees + static_cast<int64_t>(t) * max_nodes;
   const int nn = min(n_nodes[t], max_nodes);
@@ -177,7 +176,6 @@ __global__ void maxabs_kernel(const T* __restrict__ g, int64_t N, unsigned long 
 // fixed_exp[0] from maxabs[0]; with_h: fixed_exp[1] (S_h of the hessians) from maxabs[1].  clear: the
 // maxima are then reset to 0 for the next tree's gradients to raise (training reads them only here).
 __global__ void fixed_exp_kernel(unsigned long long* maxabs, int64_t N, int32_t* fixed_exp, int with_h, int clear) {
-  chain_start();
   const unsigned long long m = maxabs[0], mh = with_h ? maxabs[1] : 0ull;
   fixed_exp[0] = fixed_exponent(__longlong_as_double(static_cast<long long>(m)), N);
   if (with_h) fixed_exp[1] = fixed_exponent(__longlong_as_double(static_cast<long long>(mh)), N);
@@ -225,8 +223,8 @@ void launch_finish_tree(const gbdt_node* trees, const int32_t* n_nodes, const in
                                            static_cast<int>(sizeof(double) * ((1 << (GBDT_MAX_DEPTH + 1)) - 1))),
                       true);
   (void)once;
-  launch_chained(finish_tree_kernel, elementwise_grid(N), 256, sizeof(double) * max_nodes, s, trees, n_nodes,
-                 tree_index, max_nodes, lr, label, N, objective, pred, g, node, maxabs, next ? 1 : 0);
+  finish_tree_kernel<<<elementwise_grid(N), 256, sizeof(double) * max_nodes, s>>>(
+      trees, n_nodes, tree_index, max_nodes, lr, label, N, objective, pred, g, node, maxabs, next ? 1 : 0);
   count_launches();
 }
 void launch_gradients(const double* pred, const float* label, int64_t N, int32_t objective, double* g,
@@ -243,7 +241,7 @@ void launch_maxabs(const void* g, int32_t dtype, int64_t N, unsigned long long* 
 }
 void launch_fixed_exp(unsigned long long* maxabs, int64_t N, int32_t* fixed_exp, bool with_h, cudaStream_t s,
                       bool clear) {
-  launch_chained(fixed_exp_kernel, 1, 1, 0, s, maxabs, N, fixed_exp, with_h ? 1 : 0, clear ? 1 : 0);
+  fixed_exp_kernel<<<1, 1, 0, s>>>(maxabs, N, fixed_exp, with_h ? 1 : 0, clear ? 1 : 0);
   count_launches();
 }
 

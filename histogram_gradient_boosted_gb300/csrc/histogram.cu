@@ -269,7 +269,6 @@ __global__ void __launch_bounds__(256)
     hist_zero_built_kernel(const SegWork* __restrict__ st, const int32_t* __restrict__ build_slot, int32_t F,
                            uint32_t* __restrict__ hist_cnt, int64_t* __restrict__ hist_q, int64_t* __restrict__ hist_h,
                            const uint32_t* cnt0, const int32_t* __restrict__ n_bins) {
-  chain_start();
   if (static_cast<int>(blockIdx.y) >= st->n_built) return;
   const int slot = build_slot[blockIdx.y];
   const int64_t per_slot = static_cast<int64_t>(F) * kBins;
@@ -380,7 +379,7 @@ void launch_hist_zero_built(const SegWork* st, const int32_t* build_slot, int32_
                             const uint32_t* cnt0, const int32_t* n_bins) {
   const int64_t per_slot = static_cast<int64_t>(F) * kBins;  // 4 bins per thread, 256 threads per CTA
   dim3 grid(static_cast<unsigned>((per_slot / 4 + 255) / 256), static_cast<unsigned>(max_built < 1 ? 1 : max_built));
-  launch_chained(hist_zero_built_kernel, grid, 256, 0, s, st, build_slot, F, hist_cnt, hist_q, hist_h, cnt0, n_bins);
+  hist_zero_built_kernel<<<grid, 256, 0, s>>>(st, build_slot, F, hist_cnt, hist_q, hist_h, cnt0, n_bins);
   count_launches();
 }
 

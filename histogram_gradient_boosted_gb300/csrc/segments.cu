@@ -499,7 +499,6 @@ __global__ void __launch_bounds__(kSegThreads, 1)
                     int64_t* __restrict__ hist_q, int64_t* __restrict__ hist_h, const uint32_t* __restrict__ floc,
                     const uint32_t* __restrict__ slot_src, RegGroups rg) {
   extern __shared__ __align__(16) unsigned char smem[];
-  chain_start();
   // this CTA's group: columns (slots) [c_lo, c_lo + ns) of the bins.  Groups get CTAs in proportion
   // to their 32-lane halves + row_weight: where every scanned row is counted a CTA's time per row is
   // about its halves' atomics (row_weight 0); where a filter skips about half of the scanned rows
@@ -659,7 +658,6 @@ __global__ void mv_setup_kernel(const gbdt_level* __restrict__ level, int32_t ma
                                 const gbdt_segment* __restrict__ seg, int32_t* __restrict__ tile_start,
                                 MvState* __restrict__ st) {
   __shared__ int s_w[33];
-  chain_start();
   int s_pre = 0;  // block-uniform running total
   const int n_slots = min(level->n_slots, max_slots);
   for (int c0 = 0; c0 < n_slots; c0 += blockDim.x) {
@@ -1096,7 +1094,6 @@ __global__ void __launch_bounds__(kMvThreads)
                      const gbdt_segment* __restrict__ seg, const Route* __restrict__ route,
                      const int32_t* __restrict__ tile_start, const MvState* __restrict__ st, bool frozen_only,
                      uint16_t* __restrict__ leaf_of_row) {
-  chain_start();
   const int t = blockIdx.x;
   if (t >= st->total_tiles) return;
   const int n_slots = min(level->n_slots, max_slots);
@@ -1223,7 +1220,6 @@ __global__ void pair_routes_kernel(const gbdt_level* __restrict__ level, int32_t
                                    PairState* __restrict__ st, unsigned long long* __restrict__ tile_status,
                                    int32_t n_status) {
   __shared__ int s_w[33];
-  chain_start();
   // the look-back status words of the move that follows start at 0 (null: no move follows)
   for (int i = threadIdx.x; i < n_status; i += blockDim.x) tile_status[i] = 0;
   int s_pre = 0;  // block-uniform running total
@@ -1383,7 +1379,6 @@ __global__ void __launch_bounds__(kMvThreads, 5)
   __shared__ uint16_t s_unit[kMvMaxUnits];
   __shared__ MvRunTable s_rt;
   __shared__ long long s_pref[4];
-  chain_start();
   const int t = blockIdx.x;
   if (t >= st->total_tiles) return;
   // Every tile of the launch publishes its run counts (see mv_tile_prefix), so none returns early; a
@@ -1533,7 +1528,6 @@ __global__ void __launch_bounds__(kPairLeafThreads)
     pair_leaves_kernel(const uint8_t* __restrict__ bins_in, int64_t pitch, const uint32_t* __restrict__ orig_in,
                        const PairRoute* __restrict__ pairs, const int32_t* __restrict__ tile_start,
                        const PairState* __restrict__ st, uint16_t* __restrict__ leaf_of_row) {
-  chain_start();
   const int t = blockIdx.x;
   if (t >= st->total_tiles) return;
   const int k = slot_of_tile(tile_start, st->n_pairs, t);
@@ -1693,9 +1687,11 @@ int launch_seg_histograms(const SegHistPlan& plan, const uint8_t* bins, int64_t 
   auto launch = [&](auto kernel, const auto* gp) -> int {
     GBDT_CUDA(smem_attr(kernel, plan.smem));
     const RegGroups rg{plan.reg_begin, plan.n_norm_groups, plan.reg_weight, plan.reg_codes, n_bins};
-    launch_chained(kernel, grid, kSegThreads, plan.smem, s, bins, ldb, F, plan.n_cols, gp, fixed_exp, seg, filters,
-                   build_slot, row_start, st, plan.group_feats, plan.sm_budget, plan.total_weight, plan.row_weight,
-                   hist_cnt, hist_q, hist_h, row_blocks ? floc : nullptr, row_blocks ? slot_src : nullptr, rg);
+    kernel<<<grid, kSegThreads, plan.smem, s>>>(bins, ldb, F, plan.n_cols, gp, fixed_exp, seg, filters, build_slot,
+                                                row_start, st, plan.group_feats, plan.sm_budget, plan.total_weight,
+                                                plan.row_weight,
+                                                hist_cnt, hist_q, hist_h, row_blocks ? floc : nullptr,
+                                                row_blocks ? slot_src : nullptr, rg);
     return GBDT_OK;
   };
   auto pick = [&](const auto* gp, auto h_tag) -> int {
@@ -1780,7 +1776,7 @@ void launch_move_rows(const uint8_t* bins_in, uint8_t* bins_out, int64_t ldb, in
   int32_t* tile_left = c.take<int32_t>(max_tiles);
   int64_t* tile_excl = c.take<int64_t>(max_tiles + 1);
   int64_t* seg_left = c.take<int64_t>(max_slots);
-  launch_chained(mv_setup_kernel, 1, 1024, 0, s, level, max_slots, seg, tile_start, st);
+  mv_setup_kernel<<<1, 1024, 0, s>>>(level, max_slots, seg, tile_start, st);
   count_launches();
   mv_count_kernel<<<max_tiles, kMvThreads, 0, s>>>(bins_in, ldb, go_right, level, max_slots, seg, route, tile_start,
                                                    st, tile_left);
@@ -1801,10 +1797,10 @@ void launch_leaf_rows(const uint8_t* bins_rb, int64_t pitch, const uint32_t* flo
   MvState* st = c.take<MvState>(1);
   int32_t* tile_start = c.take<int32_t>(max_slots + 1);
   const int max_tiles = ceil_div(N, kMvTile) + max_slots;
-  launch_chained(mv_setup_kernel, 1, 1024, 0, s, level, max_slots, seg, tile_start, st);
+  mv_setup_kernel<<<1, 1024, 0, s>>>(level, max_slots, seg, tile_start, st);
   count_launches();
-  launch_chained(mv_leaves_kernel, max_tiles, kMvThreads, 0, s, bins_rb, pitch, floc, orig_in, level, max_slots, seg,
-                 route, tile_start, st, frozen_only, leaf_of_row);
+  mv_leaves_kernel<<<max_tiles, kMvThreads, 0, s>>>(bins_rb, pitch, floc, orig_in, level, max_slots, seg, route,
+                                                    tile_start, st, frozen_only, leaf_of_row);
   count_launches();
 }
 
@@ -1815,12 +1811,13 @@ void launch_move_pairs(const CUtensorMap& map_in, const uint8_t* bins_rb_in, uin
                        const int32_t* pair_parent, const gbdt_segment* seg_next, uint16_t* leaf_of_row, void* scratch,
                        int32_t* err, cudaStream_t s) {
   const PairScratch p = carve_pairs(scratch, N, max_slots);
-  launch_chained(pair_routes_kernel, 1, 1024, 0, s, level, max_slots, seg, route_cur, route_prev, pair_parent,
-                 seg_next, floc, p.pairs, p.tile_start, p.st, p.tile_status, p.max_tiles);
+  pair_routes_kernel<<<1, 1024, 0, s>>>(level, max_slots, seg, route_cur, route_prev, pair_parent, seg_next, floc,
+                                        p.pairs, p.tile_start, p.st, p.tile_status, p.max_tiles);
   count_launches();
-  launch_chained(pair_move_kernel, p.max_tiles, kMvThreads, 0, s, map_in, bins_rb_out, pitch, bins_rb_in, S,
-                 reinterpret_cast<const uint64_t*>(g_in), reinterpret_cast<uint64_t*>(g_out), orig_in, orig_out,
-                 p.pairs, p.tile_start, p.st, p.tile_status, p.tile_cnt, leaf_of_row, err);
+  pair_move_kernel<<<p.max_tiles, kMvThreads, 0, s>>>(
+      map_in, bins_rb_out, pitch, bins_rb_in, S, reinterpret_cast<const uint64_t*>(g_in),
+      reinterpret_cast<uint64_t*>(g_out), orig_in, orig_out, p.pairs, p.tile_start, p.st, p.tile_status, p.tile_cnt,
+      leaf_of_row, err);
   count_launches();
 }
 
@@ -1829,11 +1826,11 @@ void launch_leaf_pairs(const uint8_t* bins_rb, int64_t pitch, const uint32_t* fl
                        const Route* route_cur, const Route* route_prev, const int32_t* pair_parent,
                        const gbdt_segment* seg_next, uint16_t* leaf_of_row, void* scratch, cudaStream_t s) {
   const PairScratch p = carve_pairs(scratch, N, max_slots);
-  launch_chained(pair_routes_kernel, 1, 1024, 0, s, level, max_slots, seg, route_cur, route_prev, pair_parent,
-                 seg_next, floc, p.pairs, p.tile_start, p.st, nullptr, 0);
+  pair_routes_kernel<<<1, 1024, 0, s>>>(level, max_slots, seg, route_cur, route_prev, pair_parent, seg_next, floc,
+                                        p.pairs, p.tile_start, p.st, nullptr, 0);
   count_launches();
-  launch_chained(pair_leaves_kernel, p.max_tiles, kPairLeafThreads, 0, s, bins_rb, pitch, orig_in, p.pairs,
-                 p.tile_start, p.st, leaf_of_row);
+  pair_leaves_kernel<<<p.max_tiles, kPairLeafThreads, 0, s>>>(bins_rb, pitch, orig_in, p.pairs, p.tile_start,
+                                                               p.st, leaf_of_row);
   count_launches();
 }
 

@@ -485,7 +485,6 @@ __global__ void __launch_bounds__(kSplitThreads)
                  double mcw, int64_t mcw_ceil, Surv* __restrict__ surv, int32_t* __restrict__ slot_done,
                  gbdt_split* __restrict__ out, int32_t* __restrict__ err, const int32_t* __restrict__ fsched,
                  int32_t n_wide, int32_t n_narrow, const SlotTotals* __restrict__ totals, SubSrc src) {
-  chain_start();
   const int slot = blockIdx.x;
   const int n_slots = min(level->n_slots, max_slots);
   if (slot >= n_slots) return;  // every CTA of this slot
@@ -564,13 +563,15 @@ void launch_find_splits(const uint32_t* hist_cnt, const int64_t* hist_q, const i
   const double cm = std::ceil(p.min_child_weight);
   const int64_t mcw_ceil = cm > 8.0e9 ? int64_t(8000000000) : static_cast<int64_t>(cm);
   if (hist_h)
-    launch_chained(split_kernel<true>, grid, kSplitThreads, 0, s, hist_cnt, hist_q, hist_h, fixed_exp, F, n_bins,
-                   level, max_slots, p.reg_lambda, p.gamma, p.min_samples_leaf, p.min_child_weight, mcw_ceil, surv,
-                   done, out, err, fsched, n_wide, n_narrow, totals, src);
+    split_kernel<true><<<grid, kSplitThreads, 0, s>>>(hist_cnt, hist_q, hist_h, fixed_exp, F, n_bins, level,
+                                                      max_slots, p.reg_lambda, p.gamma, p.min_samples_leaf,
+                                                      p.min_child_weight, mcw_ceil, surv, done, out, err, fsched,
+                                                      n_wide, n_narrow, totals, src);
   else
-    launch_chained(split_kernel<false>, grid, kSplitThreads, 0, s, hist_cnt, hist_q, nullptr, fixed_exp, F, n_bins,
-                   level, max_slots, p.reg_lambda, p.gamma, p.min_samples_leaf, p.min_child_weight, mcw_ceil, surv,
-                   done, out, err, fsched, n_wide, n_narrow, totals, src);
+    split_kernel<false><<<grid, kSplitThreads, 0, s>>>(hist_cnt, hist_q, nullptr, fixed_exp, F, n_bins, level,
+                                                       max_slots, p.reg_lambda, p.gamma, p.min_samples_leaf,
+                                                       p.min_child_weight, mcw_ceil, surv, done, out, err, fsched,
+                                                      n_wide, n_narrow, totals, src);
   count_launches();
 }
 

@@ -53,7 +53,6 @@ __device__ __forceinline__ int32_t work_ctas(long long cost, const NextWork& nw)
 // that the per-tree launch sequence is the same for every tree (it can be replayed as one graph).
 __global__ void reset_root_kernel(gbdt_level* level, uint8_t* build_flag, gbdt_segment* seg, int64_t N,
                                   int32_t* budget, NextWork nw) {
-  chain_start();
   level->node_begin = 0;
   level->n_slots = 1;
   build_flag[0] = 1;
@@ -110,7 +109,6 @@ __global__ void __launch_bounds__(1024)
                        int32_t* __restrict__ pair_parent, uint8_t* __restrict__ next_build, Route* __restrict__ route,
                        LevelStats* __restrict__ level_stats, int32_t num_leaves, int32_t* __restrict__ budget,
                        int logistic, int32_t* __restrict__ err, NextWork nw) {
-  chain_start();
   // this tree's node array, node count and level statistics (trees, n_nodes: per tree; level_stats:
   // level d of tree 0, D + 1 records per tree)
   const int t = budget[2];
@@ -610,7 +608,7 @@ extern "C" int gbdt_train(const uint8_t* bins, int64_t ldb, const int32_t* n_bin
   unsigned rec_flags = cudaEventRecordDefault;
   auto grow_tree = [&](int t, cudaStream_t s) -> int {
     launch_fixed_exp(w.maxabs, N, w.fixed_exp, logistic, s, /*clear=*/true);  // finish_tree raises them again
-    launch_chained(reset_root_kernel, 1, 1, 0, s, w.level[0], w.build[0], w.seg[0], N, w.budget, next_work(0));
+    reset_root_kernel<<<1, 1, 0, s>>>(w.level[0], w.build[0], w.seg[0], N, w.budget, next_work(0));
     count_launches();
     if (D == 0) {
       GBDT_CUDA(cudaMemsetAsync(w.totals[0], 0, sizeof(SlotTotals), s));
@@ -658,10 +656,11 @@ extern "C" int gbdt_train(const uint8_t* bins, int64_t ldb, const int32_t* n_bin
                            d > 0 ? w.totals[cur] : nullptr, d > 0 ? w.hist_cnt[nxt] : nullptr, w.hist_q[nxt],
                            w.hist_h[nxt], w.pair_parent[cur], w.build[cur]);
       }
-      launch_chained(apply_level_kernel, 1, 1024, 0, s, d, D, w.level[cur], max_slots,
-                     d < D ? w.splits : nullptr, w.totals[cur], w.build[cur], w.fixed_exp, p->reg_lambda, w.seg[cur],
-                     w.trees, w.n_nodes, w.level[nxt], w.totals[nxt], w.seg[nxt], w.pair_parent[nxt], w.build[nxt],
-                     w.route[cur], st, p->num_leaves, w.budget, logistic ? 1 : 0, w.err, next_work(d + 1));
+      apply_level_kernel<<<1, 1024, 0, s>>>(d, D, w.level[cur], max_slots, d < D ? w.splits : nullptr, w.totals[cur],
+                                            w.build[cur], w.fixed_exp, p->reg_lambda, w.seg[cur], w.trees,
+                                            w.n_nodes, w.level[nxt], w.totals[nxt], w.seg[nxt],
+                                            w.pair_parent[nxt], w.build[nxt], w.route[cur], st, p->num_leaves,
+                                            w.budget, logistic ? 1 : 0, w.err, next_work(d + 1));
       count_launches();
       // rows: after an odd level they move into the next order (four grandchild runs per pair); at
       // even levels nothing moves and the rows of nodes that do not split record their leaf; at the
