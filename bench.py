@@ -667,6 +667,14 @@ def run_ours(args, rank, local_rank, ws, dist):
     # one untimed step first, as for the device-resident steps: the first host-input call allocates its
     # outputs and workspace (the caching allocator may have no block of that size yet)
     e2e_step()
+    # this machine's host link: one plain copy of the pinned features (boxes differ several-fold here)
+    torch.cuda.synchronize()
+    k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    k0.record(stream)
+    Xd.copy_(Xp, non_blocking=True)
+    k1.record(stream)
+    torch.cuda.synchronize()
+    host_copy_gbs = Xp.numel() * 4 / (k0.elapsed_time(k1) * 1e-3) / 1e9
     _barrier(dist)
     torch.cuda.synchronize()
     h2d_each = []
@@ -681,7 +689,7 @@ def run_ours(args, rank, local_rank, ws, dist):
     e2e = {"value": N * F * T * e2e_steps * ws / e2e_s, "unit": UNIT, "h2d_bytes_per_step": h2d,
            "d2h_bytes_per_step": d2h, "ms_per_step": 1e3 * e2e_s / e2e_steps,
            "h2d_and_quantize_ms_per_step": h2d_ms / e2e_steps, "h2d_and_quantize_ms_each": h2d_each,
-           "warmup": 1,
+           "warmup": 1, "host_copy_gbs": host_copy_gbs,
            "path": "gbdt_quantize_host (pinned host features, copies overlapped with binning) + gbdt_train; "
                    "labels copied before, predictions and model read back"}
 

@@ -631,7 +631,8 @@ extern "C" int gbdt_train(const uint8_t* bins, int64_t ldb, const int32_t* n_bin
       if (d < D) {
         const int max_build = d == 0 ? 1 : max_slots / 2;
         const SegHistPlan plan = plan_seg_histograms(N, S, max_slots, max_build, logistic, odd, reg_arg, reg_codes);
-        if (timing) GBDT_CUDA(cudaEventRecordWithFlags(ev_hist(t, d, 0), s, rec_flags));
+        // a level's histograms start where the level above ended its partition (that event serves both)
+        if (timing && d == 0) GBDT_CUDA(cudaEventRecordWithFlags(ev_hist(t, d, 0), s, rec_flags));
         const gbdt_segment* hseg = w.seg[cur];
         const gbdt_filter* hfil = nullptr;
         if (odd) {  // scan ranges and filters written by the level above (apply_level_kernel)
@@ -665,7 +666,9 @@ extern "C" int gbdt_train(const uint8_t* bins, int64_t ldb, const int32_t* n_bin
       // rows: after an odd level they move into the next order (four grandchild runs per pair); at
       // even levels nothing moves and the rows of nodes that do not split record their leaf; at the
       // last split level every row records its leaf.
-      if (timing) GBDT_CUDA(cudaEventRecordWithFlags(ev_hist(t, d, 2), s, rec_flags));
+      // the last level of a tree partitions nothing: no events around it
+      const bool part_events = timing && (d < D || D == 0);
+      if (part_events) GBDT_CUDA(cudaEventRecordWithFlags(ev_hist(t, d, 2), s, rec_flags));
       if (d < D && d + 1 < D) {
         if (odd) {
           const int out = ((d + 1) >> 1) - 1 & 1;
@@ -684,7 +687,7 @@ extern "C" int gbdt_train(const uint8_t* bins, int64_t ldb, const int32_t* n_bin
         launch_leaf_rows(lb, pitch, w.floc, N, lo, w.level[cur], max_slots, w.seg[cur], w.route[cur], false, w.leaf,
                          w.move_scratch, s);
       }
-      if (timing) GBDT_CUDA(cudaEventRecordWithFlags(ev_hist(t, d, 3), s, rec_flags));
+      if (part_events) GBDT_CUDA(cudaEventRecordWithFlags(ev_hist(t, d, 3), s, rec_flags));
       GBDT_LAUNCH_CHECK();
       ++levels_done;
       if (fail_after >= 0 && levels_done >= fail_after) {
@@ -803,7 +806,7 @@ extern "C" int gbdt_train(const uint8_t* bins, int64_t ldb, const int32_t* n_bin
         const LevelStats& ls = h_stats[static_cast<size_t>(t) * (D + 1) + d];
         const bool odd = (d & 1) != 0;
         if (d < D) {
-          GBDT_CUDA(cudaEventElapsedTime(&ms, ev_hist(t, d, 0), ev_hist(t, d, 1)));
+          GBDT_CUDA(cudaEventElapsedTime(&ms, d == 0 ? ev_hist(t, 0, 0) : ev_hist(t, d - 1, 3), ev_hist(t, d, 1)));
           dg.hist_ms += ms;
           dg.hist_launches += 1;
           dg.hist_rows += ls.n_built_rows;
@@ -811,6 +814,7 @@ extern "C" int gbdt_train(const uint8_t* bins, int64_t ldb, const int32_t* n_bin
           dg.hist_bytes += static_cast<double>(ls.n_scan_rows) * (row_bytes + (odd ? 1.0 : 0.0)) + out_bytes;
           dg.hist_level_bytes += static_cast<double>(ls.n_act) * (F + 8.0 + 2.0) + out_bytes;
         }
+        if (d == D && D > 0) continue;  // nothing partitioned (no events recorded)
         GBDT_CUDA(cudaEventElapsedTime(&ms, ev_hist(t, d, 2), ev_hist(t, d, 3)));
         dg.part_ms += ms;
         // a moved row reads and writes every column and its two decision bytes are read; a row that
