@@ -606,6 +606,32 @@ extern "C" int gbdt_train(const uint8_t* bins, int64_t ldb, const int32_t* n_bin
   // gradients), and the trees between them replay it as one captured graph.
   // timing events recorded while a tree is captured become event-record nodes of its graph
   unsigned rec_flags = cudaEventRecordDefault;
+  // The timing events hang off a stream of their own: at each mark it waits for the tree's stream and
+  // records the event there, so in a replayed tree the event nodes are branches of the graph that no
+  // kernel waits for; each tree ends by joining that stream back.
+  struct Marks {
+    cudaStream_t ts = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+    Marks() = default;
+    Marks(const Marks&) = delete;
+    Marks& operator=(const Marks&) = delete;
+    ~Marks() {
+      if (fork) cudaEventDestroy(fork);
+      if (join) cudaEventDestroy(join);
+      if (ts) cudaStreamDestroy(ts);
+    }
+  } mk;
+  if (timing) {
+    GBDT_CUDA(cudaStreamCreateWithFlags(&mk.ts, cudaStreamNonBlocking));
+    GBDT_CUDA(cudaEventCreateWithFlags(&mk.fork, cudaEventDisableTiming));
+    GBDT_CUDA(cudaEventCreateWithFlags(&mk.join, cudaEventDisableTiming));
+  }
+  auto mark = [&](cudaEvent_t ev, cudaStream_t s) -> int {
+    GBDT_CUDA(cudaEventRecord(mk.fork, s));
+    GBDT_CUDA(cudaStreamWaitEvent(mk.ts, mk.fork, 0));
+    GBDT_CUDA(cudaEventRecordWithFlags(ev, mk.ts, rec_flags));
+    return GBDT_OK;
+  };
   auto grow_tree = [&](int t, cudaStream_t s) -> int {
     launch_fixed_exp(w.maxabs, N, w.fixed_exp, logistic, s, /*clear=*/true);  // finish_tree raises them again
     reset_root_kernel<<<1, 1, 0, s>>>(w.level[0], w.build[0], w.seg[0], N, w.budget, next_work(0));
@@ -632,7 +658,7 @@ extern "C" int gbdt_train(const uint8_t* bins, int64_t ldb, const int32_t* n_bin
         const int max_build = d == 0 ? 1 : max_slots / 2;
         const SegHistPlan plan = plan_seg_histograms(N, S, max_slots, max_build, logistic, odd, reg_arg, reg_codes);
         // a level's histograms start where the level above ended its partition (that event serves both)
-        if (timing && d == 0) GBDT_CUDA(cudaEventRecordWithFlags(ev_hist(t, d, 0), s, rec_flags));
+        if (timing && d == 0 && (rc = mark(ev_hist(t, d, 0), s)) != GBDT_OK) return rc;
         const gbdt_segment* hseg = w.seg[cur];
         const gbdt_filter* hfil = nullptr;
         if (odd) {  // scan ranges and filters written by the level above (apply_level_kernel)
@@ -646,7 +672,7 @@ extern "C" int gbdt_train(const uint8_t* bins, int64_t ldb, const int32_t* n_bin
                                    w.hist_h[cur], s, true, w.floc, w.slot_src,
                                    d == 0 && t > 0 ? w.root_cnt : nullptr, n_bins, /*work_ready=*/true);
         if (rc != GBDT_OK) return rc;
-        if (timing) GBDT_CUDA(cudaEventRecordWithFlags(ev_hist(t, d, 1), s, rec_flags));
+        if (timing && (rc = mark(ev_hist(t, d, 1), s)) != GBDT_OK) return rc;
         if (d == 0 && t == 0)
           GBDT_CUDA(cudaMemcpyAsync(w.root_cnt, w.hist_cnt[cur], sizeof(uint32_t) * F * kBins,
                                     cudaMemcpyDeviceToDevice, s));
@@ -668,7 +694,7 @@ extern "C" int gbdt_train(const uint8_t* bins, int64_t ldb, const int32_t* n_bin
       // last split level every row records its leaf.
       // the last level of a tree partitions nothing: no events around it
       const bool part_events = timing && (d < D || D == 0);
-      if (part_events) GBDT_CUDA(cudaEventRecordWithFlags(ev_hist(t, d, 2), s, rec_flags));
+      if (part_events && (rc = mark(ev_hist(t, d, 2), s)) != GBDT_OK) return rc;
       if (d < D && d + 1 < D) {
         if (odd) {
           const int out = ((d + 1) >> 1) - 1 & 1;
@@ -687,7 +713,7 @@ extern "C" int gbdt_train(const uint8_t* bins, int64_t ldb, const int32_t* n_bin
         launch_leaf_rows(lb, pitch, w.floc, N, lo, w.level[cur], max_slots, w.seg[cur], w.route[cur], false, w.leaf,
                          w.move_scratch, s);
       }
-      if (part_events) GBDT_CUDA(cudaEventRecordWithFlags(ev_hist(t, d, 3), s, rec_flags));
+      if (part_events && (rc = mark(ev_hist(t, d, 3), s)) != GBDT_OK) return rc;
       GBDT_LAUNCH_CHECK();
       ++levels_done;
       if (fail_after >= 0 && levels_done >= fail_after) {
@@ -700,6 +726,10 @@ extern "C" int gbdt_train(const uint8_t* bins, int64_t ldb, const int32_t* n_bin
     launch_finish_tree(w.trees, w.n_nodes, w.budget + 2, M, p->learning_rate, label, N, p->objective, pred_out,
                        w.g0, w.leaf, w.maxabs, next, s);
     GBDT_LAUNCH_CHECK();
+    if (timing) {  // the timing stream joins the tree's stream (a captured tree must end joined)
+      GBDT_CUDA(cudaEventRecord(mk.join, mk.ts));
+      GBDT_CUDA(cudaStreamWaitEvent(s, mk.join, 0));
+    }
     return GBDT_OK;
   };
 

@@ -539,7 +539,8 @@ int gbdt_predict(const float* X, int64_t ldx, int64_t N, int32_t F, const float*
  * labels) and at the end.  With n_trees >= 4 the launches of one tree are
  * captured once per call into a CUDA graph (on a stream the call creates and
  * destroys) and trees 1 .. n_trees-2 replay it on `stream` (with diag, its
- * timing events are nodes of that graph, pointed at each tree's events); the
+ * timing events are nodes of that graph on a branch of their own, recorded on
+ * a second stream the call creates, pointed at each tree's events); the
  * results are the same as launching tree by tree (which the failure-injection
  * hook uses).  On any error after parameter validation nodes_out
  * is left untouched and nodes_per_tree[*] = 0 (no partial model, s.5 State
