@@ -210,9 +210,12 @@ int make_row_block_map(CUtensorMap* map, const uint8_t* rb, int64_t N, int32_t S
 // Record leaves without moving data: every row of the level (its child when its slot splits, its
 // own node when it does not), or with frozen_only only the rows of slots that do not split.  Needs
 // route from the level's splits; bins in the row-block layout; scratch is move_scratch_bytes.
+// setup_done: the kernel before has done rows_setup_slot_tiles' setup (rows.cuh) on this scratch; the
+// same holds for the two pair launchers below with rows_setup_pairs.
 void launch_leaf_rows(const uint8_t* bins_rb, int64_t pitch, const uint32_t* floc, int64_t N,
                       const uint32_t* orig_in, const gbdt_level* level, int32_t max_slots, const gbdt_segment* seg,
-                      const Route* route, bool frozen_only, uint16_t* leaf_of_row, void* scratch, cudaStream_t s);
+                      const Route* route, bool frozen_only, uint16_t* leaf_of_row, void* scratch, cudaStream_t s,
+                      bool setup_done = false);
 // Odd level, after its splits: move the rows of every sibling pair (still in their parent's order)
 // straight into the next level's order (four grandchild runs per pair); rows of children that do not
 // split record them as their leaf.  route_prev/pair_parent: the level above; seg_next: the next
@@ -223,12 +226,13 @@ void launch_move_pairs(const CUtensorMap& map_in, const uint8_t* bins_rb_in, uin
                        const uint32_t* orig_in, uint32_t* orig_out, const gbdt_level* level, int32_t max_slots,
                        const gbdt_segment* seg, const Route* route_cur, const Route* route_prev,
                        const int32_t* pair_parent, const gbdt_segment* seg_next, uint16_t* leaf_of_row, void* scratch,
-                       int32_t* err, cudaStream_t s);
+                       int32_t* err, cudaStream_t s, bool setup_done = false);
 // Odd last split level: every row of every pair records its leaf; nothing moves.
 void launch_leaf_pairs(const uint8_t* bins_rb, int64_t pitch, const uint32_t* floc, int64_t N,
                        const uint32_t* orig_in, const gbdt_level* level, int32_t max_slots, const gbdt_segment* seg,
                        const Route* route_cur, const Route* route_prev, const int32_t* pair_parent,
-                       const gbdt_segment* seg_next, uint16_t* leaf_of_row, void* scratch, cudaStream_t s);
+                       const gbdt_segment* seg_next, uint16_t* leaf_of_row, void* scratch, cudaStream_t s,
+                       bool setup_done = false);
 
 // node_of_row[r] = left_node + (bins[feature][r] > bin) for rows of slots with a split.
 void launch_route_rows(const uint8_t* bins, int64_t ldb, int64_t N, const Route* route, const gbdt_level* level,

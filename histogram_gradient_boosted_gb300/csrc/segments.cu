@@ -24,7 +24,7 @@
 #include <mutex>
 #include <type_traits>
 
-#include "kernels.cuh"
+#include "rows.cuh"
 
 namespace gbdt {
 
@@ -645,33 +645,12 @@ __global__ void __launch_bounds__(kSegThreads, 1)
 
 // ---------------------------------------------------------------------------------------- partition
 constexpr int kMvThreads = 256;
-constexpr int kMvTile = 4096;  // positions per tile
-
-struct MvState {
-  int32_t total_tiles;
-  int32_t pad;
-};
-
 // One CTA: tiles per slot (every slot of the level: split slots are moved,
 // the others have their rows recorded as leaves).
 __global__ void mv_setup_kernel(const gbdt_level* __restrict__ level, int32_t max_slots,
                                 const gbdt_segment* __restrict__ seg, int32_t* __restrict__ tile_start,
                                 MvState* __restrict__ st) {
-  __shared__ int s_w[33];
-  int s_pre = 0;  // block-uniform running total
-  const int n_slots = min(level->n_slots, max_slots);
-  for (int c0 = 0; c0 < n_slots; c0 += blockDim.x) {
-    const int s = c0 + threadIdx.x;
-    const int tiles = s < n_slots ? static_cast<int>((seg[s].count + kMvTile - 1) / kMvTile) : 0;
-    int n;
-    const int e = block_scan_excl(tiles, s_w, &n);
-    if (s < n_slots) tile_start[s] = s_pre + e;
-    s_pre += n;
-  }
-  if (threadIdx.x == 0) {
-    tile_start[n_slots] = s_pre;
-    st->total_tiles = s_pre;
-  }
+  rows_slot_tiles(level, max_slots, seg, tile_start, st);
 }
 
 __device__ __forceinline__ int slot_of_tile(const int32_t* __restrict__ tile_start, int n_slots, int t) {
@@ -1194,20 +1173,6 @@ __global__ void cols_to_row_blocks_kernel(const uint8_t* __restrict__ cols, int6
 // child 1 left, child 1 right); rows of a child that does not split record
 // that child as their leaf instead.  The grandchildren's segments are the
 // next level's (virtual) segments computed from the split records.
-struct PairRoute {
-  int64_t start, count;  // the pair's rows (both children) in the current order
-  int64_t dst[4];        // first position of each grandchild in the next order
-  int64_t want[4];       // its row count from the split records; -1: its child does not split
-  int32_t f1, b1;        // the parent's split (f1: its feature's locator): which child a row belongs to
-  int32_t f2[2], b2[2];  // the children's splits (locators); f2 < 0: the child is a leaf
-  int32_t node[2];       // the children's node ids
-  int32_t left[2];       // node id of each child's left child
-};
-
-struct PairState {
-  int32_t n_pairs;
-  int32_t total_tiles;
-};
 
 // One CTA: the pair records of a level and the tiles per pair.  level, seg and
 // route_cur describe the level (slots in sibling pairs); route_prev and
@@ -1219,47 +1184,8 @@ __global__ void pair_routes_kernel(const gbdt_level* __restrict__ level, int32_t
                                    PairRoute* __restrict__ pairs, int32_t* __restrict__ tile_start,
                                    PairState* __restrict__ st, unsigned long long* __restrict__ tile_status,
                                    int32_t n_status) {
-  __shared__ int s_w[33];
-  // the look-back status words of the move that follows start at 0 (null: no move follows)
-  for (int i = threadIdx.x; i < n_status; i += blockDim.x) tile_status[i] = 0;
-  int s_pre = 0;  // block-uniform running total
-  const int n_pairs = min(level->n_slots, max_slots) / 2;
-  for (int c0 = 0; c0 < n_pairs; c0 += blockDim.x) {
-    const int k = c0 + threadIdx.x;
-    int tiles = 0;
-    if (k < n_pairs) {
-      PairRoute pr;
-      const Route up = route_prev[pair_parent[k]];
-      pr.f1 = static_cast<int32_t>(floc ? floc[up.feature] : up.feature), pr.b1 = up.bin;
-      pr.start = seg[2 * k].start;
-      pr.count = seg[2 * k].count + seg[2 * k + 1].count;
-      for (int c = 0; c < 2; ++c) {
-        const Route rt = route_cur[2 * k + c];
-        pr.node[c] = level->node_begin + 2 * k + c;
-        pr.f2[c] = rt.feature < 0 ? -1 : static_cast<int32_t>(floc ? floc[rt.feature] : rt.feature);
-        pr.b2[c] = rt.bin, pr.left[c] = rt.left_node;
-        for (int j = 0; j < 2; ++j) {
-          if (rt.feature >= 0) {
-            const gbdt_segment g2 = seg_next[2 * rt.pad + j];
-            pr.dst[2 * c + j] = g2.start, pr.want[2 * c + j] = g2.count;
-          } else {
-            pr.dst[2 * c + j] = 0, pr.want[2 * c + j] = -1;
-          }
-        }
-      }
-      pairs[k] = pr;
-      tiles = static_cast<int>((pr.count + kMvTile - 1) / kMvTile);
-    }
-    int n;
-    const int e = block_scan_excl(tiles, s_w, &n);
-    if (k < n_pairs) tile_start[k] = s_pre + e;
-    s_pre += n;
-  }
-  if (threadIdx.x == 0) {
-    tile_start[n_pairs] = s_pre;
-    st->n_pairs = n_pairs;
-    st->total_tiles = s_pre;
-  }
+  rows_pair_routes(level, max_slots, seg, route_cur, route_prev, pair_parent, seg_next, floc, pairs, tile_start, st,
+                   tile_status, n_status);
 }
 
 // Run of position p of pair pr: 0..3, or -1 when its child is a leaf (*child is set either way).
@@ -1759,6 +1685,31 @@ PairScratch carve_pairs(void* scratch, int64_t N, int32_t max_slots) {
 }
 }  // namespace
 
+RowsSetup rows_setup_slot_tiles(void* scratch, int64_t N, int32_t max_slots) {
+  Carve c(scratch, two_way_scratch_bytes(N, max_slots));  // as launch_leaf_rows carves it
+  RowsSetup r{};
+  r.kind = kRowsSlotTiles;
+  r.mv_st = c.take<MvState>(1);
+  r.mv_tile_start = c.take<int32_t>(max_slots + 1);
+  return r;
+}
+
+RowsSetup rows_setup_pairs(void* scratch, int64_t N, int32_t max_slots, bool move, const Route* route_prev,
+                           const int32_t* pair_parent, const uint32_t* floc) {
+  const PairScratch p = carve_pairs(scratch, N, max_slots);  // as launch_move_pairs / launch_leaf_pairs carve it
+  RowsSetup r{};
+  r.kind = kRowsPairRoutes;
+  r.pairs = p.pairs;
+  r.pair_tile_start = p.tile_start;
+  r.pair_st = p.st;
+  r.tile_status = move ? p.tile_status : nullptr;
+  r.n_status = move ? p.max_tiles : 0;
+  r.route_prev = route_prev;
+  r.pair_parent = pair_parent;
+  r.floc = floc;
+  return r;
+}
+
 size_t move_scratch_bytes(int64_t N, int32_t max_slots) {
   const size_t a = two_way_scratch_bytes(N, max_slots), b = pair_scratch_bytes(N, max_slots);
   return a > b ? a : b;
@@ -1792,13 +1743,16 @@ void launch_move_rows(const uint8_t* bins_in, uint8_t* bins_out, int64_t ldb, in
 
 void launch_leaf_rows(const uint8_t* bins_rb, int64_t pitch, const uint32_t* floc, int64_t N,
                       const uint32_t* orig_in, const gbdt_level* level, int32_t max_slots, const gbdt_segment* seg,
-                      const Route* route, bool frozen_only, uint16_t* leaf_of_row, void* scratch, cudaStream_t s) {
+                      const Route* route, bool frozen_only, uint16_t* leaf_of_row, void* scratch, cudaStream_t s,
+                      bool setup_done) {
   Carve c(scratch, two_way_scratch_bytes(N, max_slots));
   MvState* st = c.take<MvState>(1);
   int32_t* tile_start = c.take<int32_t>(max_slots + 1);
   const int max_tiles = ceil_div(N, kMvTile) + max_slots;
-  mv_setup_kernel<<<1, 1024, 0, s>>>(level, max_slots, seg, tile_start, st);
-  count_launches();
+  if (!setup_done) {  // else rows_setup_slot_tiles' setup was done by the kernel before
+    mv_setup_kernel<<<1, 1024, 0, s>>>(level, max_slots, seg, tile_start, st);
+    count_launches();
+  }
   mv_leaves_kernel<<<max_tiles, kMvThreads, 0, s>>>(bins_rb, pitch, floc, orig_in, level, max_slots, seg, route,
                                                     tile_start, st, frozen_only, leaf_of_row);
   count_launches();
@@ -1809,11 +1763,13 @@ void launch_move_pairs(const CUtensorMap& map_in, const uint8_t* bins_rb_in, uin
                        const uint32_t* orig_in, uint32_t* orig_out, const gbdt_level* level, int32_t max_slots,
                        const gbdt_segment* seg, const Route* route_cur, const Route* route_prev,
                        const int32_t* pair_parent, const gbdt_segment* seg_next, uint16_t* leaf_of_row, void* scratch,
-                       int32_t* err, cudaStream_t s) {
+                       int32_t* err, cudaStream_t s, bool setup_done) {
   const PairScratch p = carve_pairs(scratch, N, max_slots);
-  pair_routes_kernel<<<1, 1024, 0, s>>>(level, max_slots, seg, route_cur, route_prev, pair_parent, seg_next, floc,
-                                        p.pairs, p.tile_start, p.st, p.tile_status, p.max_tiles);
-  count_launches();
+  if (!setup_done) {  // else rows_setup_pairs' setup (move true) was done by the kernel before
+    pair_routes_kernel<<<1, 1024, 0, s>>>(level, max_slots, seg, route_cur, route_prev, pair_parent, seg_next, floc,
+                                          p.pairs, p.tile_start, p.st, p.tile_status, p.max_tiles);
+    count_launches();
+  }
   pair_move_kernel<<<p.max_tiles, kMvThreads, 0, s>>>(
       map_in, bins_rb_out, pitch, bins_rb_in, S, reinterpret_cast<const uint64_t*>(g_in),
       reinterpret_cast<uint64_t*>(g_out), orig_in, orig_out, p.pairs, p.tile_start, p.st, p.tile_status, p.tile_cnt,
@@ -1824,11 +1780,14 @@ void launch_move_pairs(const CUtensorMap& map_in, const uint8_t* bins_rb_in, uin
 void launch_leaf_pairs(const uint8_t* bins_rb, int64_t pitch, const uint32_t* floc, int64_t N,
                        const uint32_t* orig_in, const gbdt_level* level, int32_t max_slots, const gbdt_segment* seg,
                        const Route* route_cur, const Route* route_prev, const int32_t* pair_parent,
-                       const gbdt_segment* seg_next, uint16_t* leaf_of_row, void* scratch, cudaStream_t s) {
+                       const gbdt_segment* seg_next, uint16_t* leaf_of_row, void* scratch, cudaStream_t s,
+                       bool setup_done) {
   const PairScratch p = carve_pairs(scratch, N, max_slots);
-  pair_routes_kernel<<<1, 1024, 0, s>>>(level, max_slots, seg, route_cur, route_prev, pair_parent, seg_next, floc,
-                                        p.pairs, p.tile_start, p.st, nullptr, 0);
-  count_launches();
+  if (!setup_done) {  // else rows_setup_pairs' setup (move false) was done by the kernel before
+    pair_routes_kernel<<<1, 1024, 0, s>>>(level, max_slots, seg, route_cur, route_prev, pair_parent, seg_next, floc,
+                                          p.pairs, p.tile_start, p.st, nullptr, 0);
+    count_launches();
+  }
   pair_leaves_kernel<<<p.max_tiles, kPairLeafThreads, 0, s>>>(bins_rb, pitch, orig_in, p.pairs, p.tile_start,
                                                                p.st, leaf_of_row);
   count_launches();

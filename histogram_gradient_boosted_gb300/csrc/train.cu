@@ -13,7 +13,7 @@
 #include <atomic>
 #include <vector>
 
-#include "kernels.cuh"
+#include "rows.cuh"
 
 namespace gbdt {
 
@@ -108,7 +108,7 @@ __global__ void __launch_bounds__(1024)
                        SlotTotals* __restrict__ next_totals, gbdt_segment* __restrict__ next_seg,
                        int32_t* __restrict__ pair_parent, uint8_t* __restrict__ next_build, Route* __restrict__ route,
                        LevelStats* __restrict__ level_stats, int32_t num_leaves, int32_t* __restrict__ budget,
-                       int logistic, int32_t* __restrict__ err, NextWork nw) {
+                       int logistic, int32_t* __restrict__ err, NextWork nw, RowsSetup rs) {
   // this tree's node array, node count and level statistics (trees, n_nodes: per tree; level_stats:
   // level d of tree 0, D + 1 records per tree)
   const int t = budget[2];
@@ -280,7 +280,7 @@ __global__ void __launch_bounds__(1024)
     s_pre += n_split;
     s_rows_pre += n_wrows;
   }
-  __syncthreads();  // the shared statistics are complete
+  __syncthreads();  // the shared statistics are complete, and this level's routes and next segments
   if (threadIdx.x == 0) {
     budget[0] += n_slots - s_pre;  // this level's leaves
     if (bind) budget[1] = 1;
@@ -298,6 +298,14 @@ __global__ void __launch_bounds__(1024)
       const long long cost = s_rows_pre + kSlotCost * s_pre;
       *nw.wv.st = SegWork{s_rows_pre, cost, s_pre, work_ctas(cost, nw)};
     }
+  }
+  // the setup of the row launches that follow (the pair routes read the routes and next segments this
+  // block wrote before the barrier above)
+  if (rs.kind == kRowsSlotTiles) {
+    rows_slot_tiles(level, max_slots, seg, rs.mv_tile_start, rs.mv_st);
+  } else if (rs.kind == kRowsPairRoutes) {
+    rows_pair_routes(level, max_slots, seg, route, rs.route_prev, rs.pair_parent, next_seg, rs.floc, rs.pairs,
+                     rs.pair_tile_start, rs.pair_st, rs.tile_status, rs.n_status);
   }
 }
 
@@ -683,11 +691,21 @@ extern "C" int gbdt_train(const uint8_t* bins, int64_t ldb, const int32_t* n_bin
                            d > 0 ? w.totals[cur] : nullptr, d > 0 ? w.hist_cnt[nxt] : nullptr, w.hist_q[nxt],
                            w.hist_h[nxt], w.pair_parent[cur], w.build[cur]);
       }
+      // the row launches after this level (below) find their tiles and pair records set up by the level
+      // kernel itself
+      RowsSetup rs{};
+      if (d < D && d + 1 < D)
+        rs = odd ? rows_setup_pairs(w.move_scratch, N, max_slots, true, w.route[nxt], w.pair_parent[cur], w.floc)
+                 : rows_setup_slot_tiles(w.move_scratch, N, max_slots);
+      else if (d + 1 == D && odd)
+        rs = rows_setup_pairs(w.move_scratch, N, max_slots, false, w.route[nxt], w.pair_parent[cur], w.floc);
+      else if (d + 1 == D || D == 0)
+        rs = rows_setup_slot_tiles(w.move_scratch, N, max_slots);
       apply_level_kernel<<<1, 1024, 0, s>>>(d, D, w.level[cur], max_slots, d < D ? w.splits : nullptr, w.totals[cur],
                                             w.build[cur], w.fixed_exp, p->reg_lambda, w.seg[cur], w.trees,
                                             w.n_nodes, w.level[nxt], w.totals[nxt], w.seg[nxt],
                                             w.pair_parent[nxt], w.build[nxt], w.route[cur], st, p->num_leaves,
-                                            w.budget, logistic ? 1 : 0, w.err, next_work(d + 1));
+                                            w.budget, logistic ? 1 : 0, w.err, next_work(d + 1), rs);
       count_launches();
       // rows: after an odd level they move into the next order (four grandchild runs per pair); at
       // even levels nothing moves and the rows of nodes that do not split record their leaf; at the
@@ -701,17 +719,17 @@ extern "C" int gbdt_train(const uint8_t* bins, int64_t ldb, const int32_t* n_bin
           launch_move_pairs(maps[ph + 1], lb, w.bins_xy[out], pitch, w.floc, N, S, lg, w.g_xy[out], lo,
                             w.orig_xy[out],
                             w.level[cur], max_slots, w.seg[cur], w.route[cur], w.route[nxt], w.pair_parent[cur],
-                            w.seg[nxt], w.leaf, w.move_scratch, w.err, s);
+                            w.seg[nxt], w.leaf, w.move_scratch, w.err, s, /*setup_done=*/true);
         } else {
           launch_leaf_rows(lb, pitch, w.floc, N, lo, w.level[cur], max_slots, w.seg[cur], w.route[cur], true, w.leaf,
-                           w.move_scratch, s);
+                           w.move_scratch, s, /*setup_done=*/true);
         }
       } else if (d + 1 == D && odd) {
         launch_leaf_pairs(lb, pitch, w.floc, N, lo, w.level[cur], max_slots, w.seg[cur], w.route[cur], w.route[nxt],
-                          w.pair_parent[cur], w.seg[nxt], w.leaf, w.move_scratch, s);
+                          w.pair_parent[cur], w.seg[nxt], w.leaf, w.move_scratch, s, /*setup_done=*/true);
       } else if (d + 1 == D || D == 0) {
         launch_leaf_rows(lb, pitch, w.floc, N, lo, w.level[cur], max_slots, w.seg[cur], w.route[cur], false, w.leaf,
-                         w.move_scratch, s);
+                         w.move_scratch, s, /*setup_done=*/true);
       }
       if (part_events && (rc = mark(ev_hist(t, d, 3), s)) != GBDT_OK) return rc;
       GBDT_LAUNCH_CHECK();
