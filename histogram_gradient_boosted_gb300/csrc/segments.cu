@@ -1213,7 +1213,7 @@ constexpr int kPairLeafThreads = 1024;
 // each waits only for earlier ones).  Warp 0 of tile t: publishes its run counts (status[t] = AGG |
 // counts, 13 bits each), sums the counts of the tiles before it - from the nearest tile that has
 // published its inclusive prefix (incl[], status PREFIX) or from the pair's first tile - into
-// s_pref, then publishes its own inclusive prefix.  status[] is zeroed by pair_routes_kernel.  Every wait
+// s_pref, then publishes its own inclusive prefix.  status[] is zeroed with the pair records (rows_pair_routes).  Every wait
 // is bounded: a tile that gives up raises kErrWaitTimeout (its prefix is then incomplete; the writes
 // stay clamped to the runs' records).  The pair's last tile checks the four totals against the split
 // records (kErrPartitionCount).
