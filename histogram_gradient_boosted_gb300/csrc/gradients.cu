@@ -127,19 +127,42 @@ __global__ void finish_tree_kernel(const gbdt_node* __restrict__ trees, const in
   for (int i = threadIdx.x; i < nn; i += blockDim.x) s_step[i] = __dmul_rn(lr, tree[i].leaf_value);
   __syncthreads();
   unsigned long long m = 0, mh = 0;
-  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < N; i += (int64_t)gridDim.x * blockDim.x) {
-    const int v = node[i];
-    const double p = (v < nn) ? __dadd_rn(pred[i], s_step[v]) : pred[i];
-    pred[i] = p;
+  // two rows per thread and step (stride apart), their loads issued before either is used, so that each
+  // SM has twice the bytes in flight of one row per step
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < N; i += 2 * stride) {
+    const int64_t j = i + stride;
+    const bool two = j < N;
+    const int v0 = node[i], v1 = two ? node[j] : 0;
+    const double q0 = pred[i], q1 = two ? pred[j] : 0.0;
+    float y0 = 0.f, y1 = 0.f;
     if (next) {
-      const double gi = gradient_of(p, label[i], objective);
-      g[i] = gi;
+      y0 = label[i];
+      y1 = two ? label[j] : 0.f;
+    }
+    const double p0 = (v0 < nn) ? __dadd_rn(q0, s_step[v0]) : q0;
+    const double p1 = (v1 < nn) ? __dadd_rn(q1, s_step[v1]) : q1;
+    pred[i] = p0;
+    if (two) pred[j] = p1;
+    if (next) {
+      const double g0 = gradient_of(p0, y0, objective), g1 = gradient_of(p1, y1, objective);
+      g[i] = g0;
       node[i] = 0;
-      const unsigned long long a = abs_bits(gi);
+      unsigned long long a = abs_bits(g0);
       m = a > m ? a : m;
       if (logistic) {
-        const unsigned long long b = abs_bits(logistic_hess(gi));
+        const unsigned long long b = abs_bits(logistic_hess(g0));
         mh = b > mh ? b : mh;
+      }
+      if (two) {
+        g[j] = g1;
+        node[j] = 0;
+        a = abs_bits(g1);
+        m = a > m ? a : m;
+        if (logistic) {
+          const unsigned long long b = abs_bits(logistic_hess(g1));
+          mh = b > mh ? b : mh;
+        }
       }
     }
   }
