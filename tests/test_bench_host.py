@@ -2,6 +2,7 @@
 ncu traffic still belongs to the histogram kernel, and the scaling of a smaller capture's traffic to the
 bench's own launches."""
 import hashlib
+import json
 import os
 import sys
 
@@ -41,8 +42,6 @@ def test_traffic_record_is_used_only_for_its_own_source(tmp_path, monkeypatch):
            "read_bytes_per_launch_captured": 1.0}
     prof = tmp_path / "profiles"
     prof.mkdir()
-    import json
-
     (prof / "histogram_traffic.json").write_text(json.dumps(rec))
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     monkeypatch.setattr(bench, "hist_source_sha256", lambda: rec["kernel_source_sha256"])
